@@ -1,0 +1,280 @@
+/*
+ * gdp_oracle.c -- float64 CPU oracle for the chunked, variable-length Gated
+ * DeltaProduct (GDP) prefill forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the
+ * CPU-baseline leg of bench.py may load this library.  It shares no code,
+ * header, table or helper with the CUDA library; it is written from the
+ * method's definition alone:
+ *
+ *   FlashInfer API page "flashinfer.gdp_prefill.chunk_gated_delta_product",
+ *   opening paragraph and its display equation: per real token t,
+ *       S *= alpha_t
+ *       for j = 0 .. n-1:  v_new = beta_{t,j} (v_{t,j} - S k_{t,j});  S += v_new (x) k_{t,j}
+ *       o_t = scale * S q_t
+ *   with the n sub-token rows of k / v / beta at t*n .. t*n+n-1 (parameters k, v, beta),
+ *   the state V-major [.., V, K] (parameter initial_state), packed THD input over
+ *   cu_seqlens (parameter cu_seqlens).
+ *
+ *   Megatron-Core API page "core.ssm.ops.gdp.chunk": g holds natural-log decays
+ *   (parameter g), so alpha_t = exp(g_t); chunk size 64 and the two chunkings
+ *   (stage list, last paragraph; parameter chunk_indices_dp); the chunk-state row
+ *   chunk_offsets[i] + c is the state ENTERING chunk c, i.e. after 64*c tokens
+ *   (parameter return_chunk_states); the state cache is written in place at
+ *   state_indices, -1 marking padding (parameters state, state_indices).
+ *
+ * Everything is computed in float64 from the exact values of the bf16 / fp32
+ * inputs (a bf16 bit pattern widened to float is exact).  The only liberty
+ * taken: the V rows of S are handed to different threads.  Each row of S
+ * evolves on its own (row v of v_new only reads row v of S), so every row
+ * sees exactly the arithmetic of the unsplit loop, in the same order.
+ *
+ * Readings where the pages are silent (the same list is kept in the design
+ * notes): q/k L2 normalisation is x / sqrt(sum x^2 + 1e-6), applied in float64
+ * and not rounded; a padding sequence (slot -1) starts from a zero state, its
+ * output is still produced, and nothing is written to the cache for it; an
+ * empty sequence copies its initial state through and owns no chunk rows.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_CHUNK 64
+#define ORACLE_L2_EPS 1e-6
+#define ORACLE_VROWS 16
+
+static double widen_bf16(uint16_t bits) {
+  uint32_t u = ((uint32_t)bits) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+static int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+/* Varlen descriptors (Megatron page, parameters chunk_indices, chunk_indices_dp,
+ * chunk_offsets; capture note in the closing paragraph).  Rows are
+ * (sequence, local chunk); rows past the real count are (-1, -1).
+ * Returns 0, or -1 if cu_seqlens is not non-decreasing from 0, or -2 if a
+ * padded bound is too small. */
+int gdp_oracle_descriptors(const int64_t *cu_seqlens, int64_t N, int M,
+                           int32_t *chunk_indices, int64_t nt_pad,
+                           int32_t *chunk_indices_dp, int64_t ntdp_pad,
+                           int32_t *chunk_offsets, int32_t *chunk_offsets_dp) {
+  int64_t nt = 0, ntdp = 0;
+  if (N > 0 && cu_seqlens[0] != 0) return -1;
+  for (int64_t i = 0; i < N; ++i) {
+    int64_t L = cu_seqlens[i + 1] - cu_seqlens[i];
+    if (L < 0) return -1;
+    if (chunk_offsets) chunk_offsets[i] = (int32_t)nt;
+    if (chunk_offsets_dp) chunk_offsets_dp[i] = (int32_t)ntdp;
+    nt += ceil_div64(L, ORACLE_CHUNK);
+    ntdp += ceil_div64(L * M, ORACLE_CHUNK);
+  }
+  if (chunk_offsets) chunk_offsets[N] = (int32_t)nt;
+  if (chunk_offsets_dp) chunk_offsets_dp[N] = (int32_t)ntdp;
+  if ((chunk_indices && nt > nt_pad) || (chunk_indices_dp && ntdp > ntdp_pad)) return -2;
+  if (chunk_indices) {
+    int64_t r = 0;
+    for (int64_t i = 0; i < N; ++i) {
+      int64_t n = ceil_div64(cu_seqlens[i + 1] - cu_seqlens[i], ORACLE_CHUNK);
+      for (int64_t c = 0; c < n; ++c, ++r) {
+        chunk_indices[2 * r] = (int32_t)i;
+        chunk_indices[2 * r + 1] = (int32_t)c;
+      }
+    }
+    for (; r < nt_pad; ++r) chunk_indices[2 * r] = chunk_indices[2 * r + 1] = -1;
+  }
+  if (chunk_indices_dp) {
+    int64_t r = 0;
+    for (int64_t i = 0; i < N; ++i) {
+      int64_t n = ceil_div64((cu_seqlens[i + 1] - cu_seqlens[i]) * M, ORACLE_CHUNK);
+      for (int64_t c = 0; c < n; ++c, ++r) {
+        chunk_indices_dp[2 * r] = (int32_t)i;
+        chunk_indices_dp[2 * r + 1] = (int32_t)c;
+      }
+    }
+    for (; r < ntdp_pad; ++r) chunk_indices_dp[2 * r] = chunk_indices_dp[2 * r + 1] = -1;
+  }
+  return 0;
+}
+
+/* Load a head-row of a bf16 [rows][H][D] tensor as float64, optionally
+ * L2-normalised (FlashInfer page, parameter use_qk_l2norm_in_kernel). */
+static void load_row(const uint16_t *base, int64_t row, int H, int h, int D,
+                     int normalise, double *out) {
+  const uint16_t *p = base + (row * H + h) * (int64_t)D;
+  double ss = 0.0;
+  for (int d = 0; d < D; ++d) {
+    out[d] = widen_bf16(p[d]);
+    ss += out[d] * out[d];
+  }
+  if (normalise) {
+    double inv = 1.0 / sqrt(ss + ORACLE_L2_EPS);
+    for (int d = 0; d < D; ++d) out[d] *= inv;
+  }
+}
+
+/*
+ * The forward pass, token by token.
+ *
+ *   q [T][H][K], k [T*M][H][K], v [T*M][H][V]: bf16 bit patterns.
+ *   g [T][H] natural-log decay (NULL: no decay); beta [T*M][H] (NULL: ones).
+ *   Incoming state: state-cache mode when state_in != NULL (slot = state_indices[i],
+ *   slot >= 0 reads state_in[slot], slot -1 starts from zero); otherwise
+ *   initial_state[i] when non-NULL; otherwise zero.  States are [..][H][V][K] fp32.
+ *   head_mask [H] (NULL: all heads) selects the heads computed; other heads'
+ *   outputs are left as they are.
+ * Outputs (float64, any may be NULL):
+ *   o [T][H][V]; final_state [N][H][V][K] (every sequence, padding included);
+ *   state_out [num_slots][H][V][K]: in cache mode, the final state of each
+ *   sequence with slot >= 0 is stored at its slot (the caller fills the rest);
+ *   chunk_states [NT][H][V][K] with NT = chunk_offsets[N]: row
+ *   chunk_offsets[i] + c holds the state entering token chunk c.
+ * Returns 0, or a negative code for an argument the definition cannot serve.
+ */
+int gdp_oracle_forward(int64_t T, int64_t N, int H, int K, int V, int M,
+                       const int64_t *cu_seqlens,
+                       const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                       const float *g, const float *beta, double scale,
+                       int use_qk_l2norm,
+                       const float *initial_state,
+                       const float *state_in, const int32_t *state_indices,
+                       int64_t num_slots,
+                       const int32_t *chunk_offsets,
+                       const uint8_t *head_mask,
+                       double *o, double *final_state, double *state_out,
+                       double *chunk_states, int num_threads) {
+  if (T < 0 || N < 0 || H <= 0 || K <= 0 || V <= 0 || M <= 0) return -1;
+  if (chunk_states && !chunk_offsets) return -2;
+  if (state_in && !state_indices) return -3;
+  if (N > 0 && (cu_seqlens[0] != 0 || cu_seqlens[N] != T)) return -4;
+  for (int64_t i = 0; i < N; ++i)
+    if (cu_seqlens[i + 1] < cu_seqlens[i]) return -4;
+  if (state_in)
+    for (int64_t i = 0; i < N; ++i)
+      if (state_indices[i] >= num_slots || state_indices[i] < -1) return -5;
+
+  const int vblocks = (V + ORACLE_VROWS - 1) / ORACLE_VROWS;
+  const int64_t ntasks = N * (int64_t)H * vblocks;
+  const int64_t KV = (int64_t)K * V;
+  int rc = 0;
+
+#ifdef _OPENMP
+  if (num_threads > 0) omp_set_num_threads(num_threads);
+#pragma omp parallel
+#endif
+  {
+    double *S = (double *)malloc(sizeof(double) * ORACLE_VROWS * K);
+    double *kr = (double *)malloc(sizeof(double) * K);
+    double *qt = (double *)malloc(sizeof(double) * K);
+    if (!S || !kr || !qt) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+      rc = -10;
+    } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+      for (int64_t task = 0; task < ntasks; ++task) {
+        const int64_t i = task / ((int64_t)H * vblocks);
+        const int h = (int)((task / vblocks) % H);
+        const int vb = (int)(task % vblocks);
+        if (head_mask && !head_mask[h]) continue;
+        const int v0 = vb * ORACLE_VROWS;
+        const int nv = (V - v0) < ORACLE_VROWS ? (V - v0) : ORACLE_VROWS;
+        const int64_t bos = cu_seqlens[i], eos = cu_seqlens[i + 1];
+
+        /* incoming state rows v0 .. v0+nv-1 */
+        const float *src = NULL;
+        if (state_in) {
+          int32_t slot = state_indices[i];
+          if (slot >= 0) src = state_in + ((int64_t)slot * H + h) * KV;
+        } else if (initial_state) {
+          src = initial_state + (i * H + h) * KV;
+        }
+        for (int r = 0; r < nv; ++r)
+          for (int d = 0; d < K; ++d)
+            S[r * K + d] = src ? (double)src[(int64_t)(v0 + r) * K + d] : 0.0;
+
+        for (int64_t t = bos; t < eos; ++t) {
+          const int64_t lt = t - bos;
+          if (chunk_states && lt % ORACLE_CHUNK == 0) {
+            double *dst = chunk_states +
+                          (((int64_t)chunk_offsets[i] + lt / ORACLE_CHUNK) * H + h) * KV;
+            for (int r = 0; r < nv; ++r)
+              for (int d = 0; d < K; ++d) dst[(int64_t)(v0 + r) * K + d] = S[r * K + d];
+          }
+          /* decay once per real token, before its updates */
+          const double alpha = g ? exp((double)g[t * H + h]) : 1.0;
+          for (int x = 0; x < nv * K; ++x) S[x] *= alpha;
+          /* n beta-gated Householder updates on the expanded rows t*M + j */
+          for (int j = 0; j < M; ++j) {
+            const int64_t row = t * M + j;
+            load_row(k, row, H, h, K, use_qk_l2norm, kr);
+            const double b = beta ? (double)beta[row * H + h] : 1.0;
+            for (int r = 0; r < nv; ++r) {
+              double *Sr = S + r * K;
+              double pred = 0.0;
+              for (int d = 0; d < K; ++d) pred += Sr[d] * kr[d];
+              const double vv = widen_bf16(v[(row * H + h) * (int64_t)V + v0 + r]);
+              const double vnew = b * (vv - pred);
+              for (int d = 0; d < K; ++d) Sr[d] += vnew * kr[d];
+            }
+          }
+          /* readout after the last update */
+          if (o) {
+            load_row(q, t, H, h, K, use_qk_l2norm, qt);
+            for (int r = 0; r < nv; ++r) {
+              const double *Sr = S + r * K;
+              double acc = 0.0;
+              for (int d = 0; d < K; ++d) acc += Sr[d] * qt[d];
+              o[(t * H + h) * (int64_t)V + v0 + r] = scale * acc;
+            }
+          }
+        }
+
+        if (final_state) {
+          double *dst = final_state + (i * H + h) * KV;
+          for (int r = 0; r < nv; ++r)
+            for (int d = 0; d < K; ++d) dst[(int64_t)(v0 + r) * K + d] = S[r * K + d];
+        }
+        if (state_in && state_out && state_indices[i] >= 0) {
+          double *dst = state_out + ((int64_t)state_indices[i] * H + h) * KV;
+          for (int r = 0; r < nv; ++r)
+            for (int d = 0; d < K; ++d) dst[(int64_t)(v0 + r) * K + d] = S[r * K + d];
+        }
+      }
+    }
+    free(S);
+    free(kr);
+    free(qt);
+  }
+  return rc;
+}
+
+/* Within-chunk cumulative decay of the expanded stream in base 2 (Megatron
+ * page, stage 1): row r = t*M + j carries g_t when j == 0 and 0 otherwise;
+ * the sum restarts at every 64-row chunk of the expanded sequence and is
+ * multiplied by log2(e).  Output G2 [T*M][H] (float64). */
+int gdp_oracle_decay_cumsum(int64_t T, int64_t N, int H, int M,
+                            const int64_t *cu_seqlens, const float *g, double *G2) {
+  const double log2e = 1.0 / log(2.0);
+  for (int64_t i = 0; i < N; ++i) {
+    const int64_t r0 = cu_seqlens[i] * M, r1 = cu_seqlens[i + 1] * M;
+    for (int h = 0; h < H; ++h) {
+      double acc = 0.0;
+      for (int64_t r = r0; r < r1; ++r) {
+        if ((r - r0) % ORACLE_CHUNK == 0) acc = 0.0;
+        if (g && r % M == 0) acc += (double)g[(r / M) * H + h];
+        G2[r * H + h] = acc * log2e;
+      }
+    }
+  }
+  return 0;
+}
