@@ -1,0 +1,253 @@
+"""Thin ctypes binding of ``libgdp_gb300.so`` (argument marshalling only).
+
+The names mirror the C ABI in ``include/gdp_prefill.h``: ``gdp_prefill_varlen``,
+``gdp_prefill_varlen_profiled``, ``gdp_prefill_workspace_bytes``,
+``gdp_build_descriptors``, ``gdp_last_error``, ``gdp_nt_pad``, ``gdp_ntdp_pad``.
+``chunk_gated_delta_product`` wraps them with the keyword signature of the
+pages (FlashInfer API page "flashinfer.gdp_prefill.chunk_gated_delta_product";
+Megatron-Core API page "core.ssm.ops.gdp.chunk", function
+chunk_gated_delta_product_varlen): torch supplies device memory and the
+current stream, every step of the computation runs in the library's CUDA
+kernels.  There is no fallback: if the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgdp_gb300.so")
+
+GDP_OK, GDP_ERR_INVALID_ARG, GDP_ERR_UNSUPPORTED, GDP_ERR_ALIAS, GDP_ERR_WORKSPACE, GDP_ERR_CUDA = range(6)
+GDP_DEV_ERR_CU_SEQLENS, GDP_DEV_ERR_SLOT, GDP_DEV_ERR_DESC = 0x1, 0x2, 0x4
+STATUS_NAMES = {0: "GDP_OK", 1: "GDP_ERR_INVALID_ARG", 2: "GDP_ERR_UNSUPPORTED", 3: "GDP_ERR_ALIAS",
+                4: "GDP_ERR_WORKSPACE", 5: "GDP_ERR_CUDA"}
+
+_vp, _i64, _int, _f32, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+
+
+class GdpPrefillArgs(ctypes.Structure):
+    """Mirror of ``gdp_prefill_args`` (field order and types of the header)."""
+    _fields_ = [
+        ("q", _vp), ("q_stride_t", _i64), ("q_stride_h", _i64),
+        ("k", _vp), ("k_stride_t", _i64), ("k_stride_h", _i64),
+        ("v", _vp), ("v_stride_t", _i64), ("v_stride_h", _i64),
+        ("g", _vp), ("beta", _vp),
+        ("cu_seqlens", _vp), ("cu_seqlens_int64", _int),
+        ("T", _i64), ("N", _i64),
+        ("H", _int), ("K", _int), ("V", _int), ("num_householder", _int),
+        ("scale", _f32), ("use_qk_l2norm", _int),
+        ("initial_state", _vp), ("state", _vp), ("state_indices", _vp), ("num_slots", _i64),
+        ("output", _vp), ("output_state", _vp), ("chunk_states", _vp),
+        ("chunk_indices", _vp), ("chunk_indices_dp", _vp), ("chunk_offsets", _vp),
+        ("nt_pad", _i64), ("ntdp_pad", _i64),
+        ("workspace", _vp), ("workspace_bytes", _sz),
+        ("device_status", _vp),
+    ]
+
+
+class GdpError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library(path: str | None = None):
+    """Load libgdp_gb300.so (built by ``__graft_entry__.build()``); raise if absent."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(p)
+    lib.gdp_prefill_varlen.restype = _int
+    lib.gdp_prefill_varlen.argtypes = [ctypes.POINTER(GdpPrefillArgs), _vp]
+    lib.gdp_prefill_varlen_profiled.restype = _int
+    lib.gdp_prefill_varlen_profiled.argtypes = [ctypes.POINTER(GdpPrefillArgs), _vp, ctypes.POINTER(_vp), _int]
+    lib.gdp_prefill_workspace_bytes.restype = _sz
+    lib.gdp_prefill_workspace_bytes.argtypes = [_i64, _i64, _int, _int, _int, _int]
+    lib.gdp_build_descriptors.restype = _int
+    lib.gdp_build_descriptors.argtypes = [_vp, _int, _i64, _i64, _int, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _vp]
+    lib.gdp_last_error.restype = ctypes.c_char_p
+    lib.gdp_last_error.argtypes = []
+    lib.gdp_abi_version.restype = _int
+    lib.gdp_nt_pad.restype = _i64
+    lib.gdp_nt_pad.argtypes = [_i64, _i64]
+    lib.gdp_ntdp_pad.restype = _i64
+    lib.gdp_ntdp_pad.argtypes = [_i64, _i64, _int]
+    lib.gdp_prefill_args_size.restype = _sz
+    if lib.gdp_prefill_args_size() != ctypes.sizeof(GdpPrefillArgs):
+        raise RuntimeError("gdp_prefill_args layout mismatch between the binding and the library")
+    if path is None:
+        _lib = lib
+    return lib
+
+
+# ---- the C entry points, same names ----------------------------------------------------------
+
+def gdp_last_error() -> str:
+    return load_library().gdp_last_error().decode()
+
+
+def gdp_nt_pad(T: int, N: int) -> int:
+    return int(load_library().gdp_nt_pad(T, N))
+
+
+def gdp_ntdp_pad(T: int, N: int, M: int) -> int:
+    return int(load_library().gdp_ntdp_pad(T, N, M))
+
+
+def gdp_prefill_workspace_bytes(T: int, N: int, H: int, K: int, V: int, M: int) -> int:
+    return int(load_library().gdp_prefill_workspace_bytes(T, N, H, K, V, M))
+
+
+def _stream(stream):
+    return torch.cuda.current_stream().cuda_stream if stream is None else stream
+
+
+def gdp_prefill_varlen(args: GdpPrefillArgs, stream: int | None = None) -> None:
+    """Enqueue one prefill on ``stream`` (default: torch's current stream)."""
+    lib = load_library()
+    st = lib.gdp_prefill_varlen(ctypes.byref(args), ctypes.c_void_p(_stream(stream)))
+    if st != GDP_OK:
+        raise GdpError(st, lib.gdp_last_error().decode())
+
+
+def gdp_prefill_varlen_profiled(args: GdpPrefillArgs, events, stream: int | None = None) -> None:
+    """As gdp_prefill_varlen, recording the 4 torch.cuda.Event objects around the stages."""
+    lib = load_library()
+    arr = (_vp * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    st = lib.gdp_prefill_varlen_profiled(ctypes.byref(args), ctypes.c_void_p(_stream(stream)), arr, len(events))
+    if st != GDP_OK:
+        raise GdpError(st, lib.gdp_last_error().decode())
+
+
+def gdp_build_descriptors(cu_seqlens: torch.Tensor, T: int, num_householder: int, nt_pad: int | None = None,
+                          ntdp_pad: int | None = None, device_status: torch.Tensor | None = None,
+                          stream: int | None = None):
+    """Device descriptors (chunk_indices [nt_pad,2], chunk_indices_dp [ntdp_pad,2], chunk_offsets [N+1])."""
+    lib = load_library()
+    N = cu_seqlens.numel() - 1
+    nt_pad = gdp_nt_pad(T, N) if nt_pad is None else nt_pad
+    ntdp_pad = gdp_ntdp_pad(T, N, num_householder) if ntdp_pad is None else ntdp_pad
+    dev = cu_seqlens.device
+    ci = torch.empty((nt_pad, 2), dtype=torch.int32, device=dev)
+    cid = torch.empty((ntdp_pad, 2), dtype=torch.int32, device=dev)
+    co = torch.empty(N + 1, dtype=torch.int32, device=dev)
+    cod = torch.empty(N + 1, dtype=torch.int32, device=dev)
+    st = lib.gdp_build_descriptors(
+        _ptr(cu_seqlens), int(cu_seqlens.dtype == torch.int64), T, N, num_householder, _ptr(ci), nt_pad, _ptr(cid),
+        ntdp_pad, _ptr(co), _ptr(cod), _ptr(device_status), ctypes.c_void_p(_stream(stream)))
+    if st != GDP_OK:
+        raise GdpError(st, lib.gdp_last_error().decode())
+    return ci, cid, co
+
+
+# ---- convenience wrapper ------------------------------------------------------------------------
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _addr(t):
+    return t.data_ptr() if t is not None else None
+
+
+def make_args(q, k, v, g, beta, cu_seqlens, num_householder, scale, initial_state, state, state_indices,
+              output, output_state, chunk_states, chunk_indices, chunk_indices_dp, chunk_offsets,
+              nt_pad, ntdp_pad, use_qk_l2norm, workspace, device_status) -> GdpPrefillArgs:
+    """Fill a GdpPrefillArgs from tensors (no copies; the library checks shapes and modes)."""
+    T, H, K = q.shape
+    V = v.shape[-1]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16:
+            raise GdpError(GDP_ERR_UNSUPPORTED, f"{name} must be bfloat16 (got {t.dtype})")
+        if t.stride(-1) != 1:
+            raise GdpError(GDP_ERR_INVALID_ARG, f"{name} must be contiguous in its last dimension")
+    for name, t in (("g", g), ("beta", beta), ("initial_state", initial_state), ("state", state)):
+        if t is not None and (t.dtype != torch.float32 or not t.is_contiguous()):
+            raise GdpError(GDP_ERR_UNSUPPORTED, f"{name} must be a contiguous float32 tensor")
+    a = GdpPrefillArgs()
+    a.q, a.q_stride_t, a.q_stride_h = q.data_ptr(), q.stride(0), q.stride(1)
+    a.k, a.k_stride_t, a.k_stride_h = k.data_ptr(), k.stride(0), k.stride(1)
+    a.v, a.v_stride_t, a.v_stride_h = v.data_ptr(), v.stride(0), v.stride(1)
+    a.g, a.beta = _addr(g), _addr(beta)
+    a.cu_seqlens = cu_seqlens.data_ptr()
+    a.cu_seqlens_int64 = int(cu_seqlens.dtype == torch.int64)
+    a.T, a.N = T, cu_seqlens.numel() - 1
+    a.H, a.K, a.V, a.num_householder = H, K, V, int(num_householder)
+    a.scale = 0.0 if scale is None else float(scale)
+    a.use_qk_l2norm = int(bool(use_qk_l2norm))
+    a.initial_state, a.state, a.state_indices = _addr(initial_state), _addr(state), _addr(state_indices)
+    a.num_slots = state.shape[0] if state is not None else 0
+    a.output, a.output_state, a.chunk_states = output.data_ptr(), _addr(output_state), _addr(chunk_states)
+    a.chunk_indices, a.chunk_indices_dp, a.chunk_offsets = _addr(chunk_indices), _addr(chunk_indices_dp), _addr(
+        chunk_offsets)
+    a.nt_pad = int(nt_pad or 0)
+    a.ntdp_pad = int(ntdp_pad or 0)
+    a.workspace = workspace.data_ptr()
+    a.workspace_bytes = workspace.numel() * workspace.element_size()
+    a.device_status = _addr(device_status)
+    return a
+
+
+def alloc_workspace(T, N, H, K, V, M, device) -> torch.Tensor:
+    nbytes = gdp_prefill_workspace_bytes(T, N, H, K, V, M)
+    if nbytes == 0:
+        raise GdpError(GDP_ERR_INVALID_ARG, "invalid shape for the workspace query")
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def chunk_gated_delta_product(q, k, v, g=None, beta=None, cu_seqlens=None, num_householder=1, scale=None,
+                              initial_state=None, output_final_state=False, use_qk_l2norm_in_kernel=False,
+                              chunk_indices=None, chunk_indices_dp=None, chunk_offsets=None, state=None,
+                              state_indices=None, return_chunk_states=False, output=None, output_state=None,
+                              workspace=None, device_status=None, nt_pad=None, ntdp_pad=None, stream=None):
+    """Chunked Gated DeltaProduct varlen prefill on the GPU.
+
+    q [T,H,K] (or [1,T,H,K]), k/v [T*M,H,K]/[T*M,H,V] bf16; g [T,H] natural-log
+    decays fp32; beta [T*M,H] fp32; cu_seqlens [N+1] int32/int64 (required).
+    Returns ``o`` [T,H,V] bf16, or ``(o, final_state)`` when output_final_state,
+    or ``(o, final_state, chunk_states)`` when return_chunk_states.  In state-cache
+    mode (``state``/``state_indices``) the final state is written into the cache
+    and ``final_state`` is None.
+    """
+    if cu_seqlens is None:
+        raise GdpError(GDP_ERR_INVALID_ARG, "cu_seqlens is required (packed THD input only)")
+    if q.dim() == 4 and q.shape[0] == 1:
+        q, k, v = q[0], k[0], v[0]
+    if g is not None and g.dim() == 3:
+        g = g[0]
+    if beta is not None and beta.dim() == 3:
+        beta = beta[0]
+    T, H, K = q.shape
+    V = v.shape[-1]
+    M = int(num_householder)
+    N = cu_seqlens.numel() - 1
+    dev = q.device
+    if output is None:
+        output = torch.empty((T, H, V), dtype=torch.bfloat16, device=dev)
+    if output_final_state and state is None and output_state is None:
+        output_state = torch.empty((N, H, V, K), dtype=torch.float32, device=dev)
+    cs = None
+    if return_chunk_states:
+        rows = nt_pad if nt_pad else gdp_nt_pad(T, N)
+        cs = torch.zeros((rows, H, V, K), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(T, N, H, K, V, M, dev)
+    a = make_args(q, k, v, g, beta, cu_seqlens, M, scale, initial_state, state, state_indices, output,
+                  output_state if state is None else None, cs, chunk_indices, chunk_indices_dp, chunk_offsets,
+                  nt_pad, ntdp_pad, use_qk_l2norm_in_kernel, workspace, device_status)
+    gdp_prefill_varlen(a, stream)
+    final = output_state if (output_final_state and state is None) else None
+    if return_chunk_states:
+        return output, final, cs
+    if output_final_state:
+        return output, final
+    return output

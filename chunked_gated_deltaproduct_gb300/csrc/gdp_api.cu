@@ -1,0 +1,248 @@
+// gdp_api.cu -- host side of the C ABI: argument checks, workspace carving,
+// kernel launches on the caller's stream.  Nothing here allocates, syncs or
+// reads device memory, so a call can be captured in a CUDA graph (Megatron-Core
+// API page "core.ssm.ops.gdp.chunk", closing paragraph).
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "gdp_internal.cuh"
+
+#define GDP_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+gdp_status fail(gdp_status st, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+int64_t nt_bound(int64_t T, int64_t N) { return (T + (int64_t)(gdp::kChunk - 1) * N) / gdp::kChunk; }
+int64_t ntdp_bound(int64_t T, int64_t N, int M) {
+  return ((int64_t)M * T + (int64_t)(gdp::kChunk - 1) * N) / gdp::kChunk;
+}
+
+// Workspace layout; identical for the size query and the carving.
+struct Layout {
+  size_t cod, ci, cid, co, W, U, P, meta, total;
+};
+
+Layout layout_for(int64_t T, int64_t N, int H, int K, int V, int M) {
+  Layout l{};
+  const int64_t ntp = nt_bound(T, N), ntdp = ntdp_bound(T, N, M);
+  const int qp = gdp::qpad_for(M);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = off;
+    off = align_up(off + bytes);
+    return at;
+  };
+  l.cod = take(sizeof(int32_t) * (size_t)(N + 1));
+  l.ci = take(sizeof(int32_t) * 2 * (size_t)ntp);
+  l.cid = take(sizeof(int32_t) * 2 * (size_t)ntdp);
+  l.co = take(sizeof(int32_t) * (size_t)(N + 1));
+  const size_t tiles = (size_t)ntdp * (size_t)H;
+  l.W = take(sizeof(float) * tiles * gdp::kChunk * (size_t)K);
+  l.U = take(sizeof(float) * tiles * gdp::kChunk * (size_t)V);
+  l.P = take(sizeof(float) * tiles * (size_t)qp * gdp::kChunk);
+  l.meta = take(sizeof(gdp::ChunkMeta) * tiles);
+  l.total = off;
+  return l;
+}
+
+bool shape_ok(int64_t T, int64_t N, int H, int K, int V, int M) {
+  return T >= 0 && N >= 0 && H >= 1 && K >= 1 && V >= 1 && M >= 1 && M <= 64 &&
+         T <= (int64_t)INT32_MAX / (M > 0 ? M : 1) && N < (int64_t)INT32_MAX;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+  return x < y + nb && y < x + na;
+}
+
+gdp_status record(cudaEvent_t ev, cudaStream_t stream) {
+  if (!ev) return GDP_OK;
+  cudaError_t e = cudaEventRecord(ev, stream);
+  return e == cudaSuccess ? GDP_OK : fail(GDP_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(e));
+}
+
+// Checks + launches shared by gdp_prefill_varlen and its profiled form.
+gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t const *ev) {
+  g_last_error[0] = 0;
+  if (!a) return fail(GDP_ERR_INVALID_ARG, "args is NULL");
+  const int64_t T = a->T, N = a->N;
+  const int H = a->H, K = a->K, V = a->V, M = a->num_householder;
+  if (!shape_ok(T, N, H, K, V, M))
+    return fail(GDP_ERR_INVALID_ARG, "bad shape T=%lld N=%lld H=%d K=%d V=%d M=%d", (long long)T, (long long)N, H, K,
+                V, M);
+  if (K != V || (K != 64 && K != 128))
+    return fail(GDP_ERR_UNSUPPORTED, "head sizes K=%d V=%d: this build serves K == V in {64, 128}", K, V);
+  if (!a->cu_seqlens && N > 0) return fail(GDP_ERR_INVALID_ARG, "cu_seqlens is NULL");
+  if (T > 0 && (!a->q || !a->k || !a->v || !a->output))
+    return fail(GDP_ERR_INVALID_ARG, "q, k, v and output are required");
+  const int64_t strides[6] = {a->q_stride_t, a->q_stride_h, a->k_stride_t, a->k_stride_h, a->v_stride_t, a->v_stride_h};
+  for (int i = 0; i < 6; ++i)
+    if (T > 0 && (strides[i] <= 0 || strides[i] % 8 != 0))
+      return fail(GDP_ERR_INVALID_ARG, "strides must be positive multiples of 8 elements (16 bytes)");
+  if (T > 0 && (a->q_stride_h < K || a->k_stride_h < K || a->v_stride_h < V || a->q_stride_t < (int64_t)H * K ||
+                a->k_stride_t < (int64_t)H * K || a->v_stride_t < (int64_t)H * V))
+    return fail(GDP_ERR_INVALID_ARG, "strides describe overlapping rows");
+  const uintptr_t align16 = ((uintptr_t)a->q | (uintptr_t)a->k | (uintptr_t)a->v | (uintptr_t)a->output) & 15u;
+  if (align16) return fail(GDP_ERR_INVALID_ARG, "q, k, v and output must be 16-byte aligned");
+  if (a->state && a->initial_state)
+    return fail(GDP_ERR_INVALID_ARG, "state (cache mode) and initial_state are mutually exclusive");
+  if (a->state && (!a->state_indices || a->num_slots < 1))
+    return fail(GDP_ERR_INVALID_ARG, "state cache needs state_indices and num_slots >= 1");
+  if (a->state && a->output_state)
+    return fail(GDP_ERR_INVALID_ARG, "in cache mode the final state is written to the cache; output_state must be NULL");
+  const size_t state_bytes = sizeof(float) * (size_t)N * H * (size_t)V * K;
+  if (overlaps(a->output_state, state_bytes, a->initial_state, state_bytes))
+    return fail(GDP_ERR_ALIAS, "output_state must not alias initial_state");
+  const int nprebuilt = (a->chunk_indices != nullptr) + (a->chunk_indices_dp != nullptr) + (a->chunk_offsets != nullptr);
+  if (nprebuilt != 0 && nprebuilt != 3)
+    return fail(GDP_ERR_INVALID_ARG, "pass all three prebuilt descriptors or none");
+  const int64_t ntb = nt_bound(T, N), ntdpb = ntdp_bound(T, N, M);
+  const int64_t nt_pad = a->nt_pad ? a->nt_pad : ntb, ntdp_pad = a->ntdp_pad ? a->ntdp_pad : ntdpb;
+  if (nt_pad < ntb || ntdp_pad < ntdpb)
+    return fail(GDP_ERR_INVALID_ARG, "nt_pad/ntdp_pad (%lld/%lld) below the shape bounds (%lld/%lld)",
+                (long long)nt_pad, (long long)ntdp_pad, (long long)ntb, (long long)ntdpb);
+  if (nprebuilt == 0 && (nt_pad != ntb || ntdp_pad != ntdpb))
+    return fail(GDP_ERR_INVALID_ARG, "nt_pad/ntdp_pad other than the bounds need prebuilt descriptors");
+  const Layout lay = layout_for(T, N, H, K, V, M);
+  if (!a->workspace || ((uintptr_t)a->workspace % kAlign) != 0)
+    return fail(GDP_ERR_WORKSPACE, "workspace must be non-NULL and %zu-byte aligned", kAlign);
+  if (a->workspace_bytes < lay.total)
+    return fail(GDP_ERR_WORKSPACE, "workspace of %zu bytes < required %zu", a->workspace_bytes, lay.total);
+
+  gdp_status st;
+  if (ev && (st = record(ev[0], stream)) != GDP_OK) return st;
+  if (N == 0) {
+    for (int i = 1; ev && i < 4; ++i)
+      if ((st = record(ev[i], stream)) != GDP_OK) return st;
+    return GDP_OK;
+  }
+
+  char *ws = (char *)a->workspace;
+  gdp::Problem p{};
+  p.q = (const __nv_bfloat16 *)a->q;
+  p.k = (const __nv_bfloat16 *)a->k;
+  p.v = (const __nv_bfloat16 *)a->v;
+  p.q_st = a->q_stride_t; p.q_sh = a->q_stride_h;
+  p.k_st = a->k_stride_t; p.k_sh = a->k_stride_h;
+  p.v_st = a->v_stride_t; p.v_sh = a->v_stride_h;
+  p.g = a->g;
+  p.beta = a->beta;
+  p.cu = a->cu_seqlens;
+  p.cu64 = a->cu_seqlens_int64 ? 1 : 0;
+  p.T = T; p.N = N; p.H = H; p.K = K; p.V = V; p.M = M;
+  p.scale = (a->scale > 0.f && !isnan(a->scale)) ? a->scale : 1.0f / sqrtf((float)K);
+  p.l2norm = a->use_qk_l2norm ? 1 : 0;
+  p.init = a->initial_state;
+  p.cache = a->state;
+  p.slots = a->state_indices;
+  p.num_slots = a->num_slots;
+  p.out = (__nv_bfloat16 *)a->output;
+  p.out_state = a->output_state;
+  p.chunk_states = a->chunk_states;
+  p.nt_pad = nt_pad;
+  p.ntdp_pad = ntdp_pad;
+  p.ws_rows = ntdpb;
+  p.cod = (int32_t *)(ws + lay.cod);
+  if (nprebuilt == 3) {
+    p.ci = a->chunk_indices;
+    p.cid = a->chunk_indices_dp;
+    p.co = a->chunk_offsets;
+  } else {
+    p.ci = (int32_t *)(ws + lay.ci);
+    p.cid = (int32_t *)(ws + lay.cid);
+    p.co = (int32_t *)(ws + lay.co);
+  }
+  p.W = (float *)(ws + lay.W);
+  p.U = (float *)(ws + lay.U);
+  p.P = (float *)(ws + lay.P);
+  p.meta = (gdp::ChunkMeta *)(ws + lay.meta);
+  p.status = a->device_status;
+  p.qpad = gdp::qpad_for(M);
+
+  cudaError_t e;
+  if (nprebuilt == 3)  // only the internal expanded-stream offsets
+    e = gdp::launch_descriptors(p.cu, p.cu64, T, N, M, nullptr, 0, nullptr, 0, nullptr, (int32_t *)p.cod, p.status,
+                                stream);
+  else
+    e = gdp::launch_descriptors(p.cu, p.cu64, T, N, M, (int32_t *)p.ci, nt_pad, (int32_t *)p.cid, ntdp_pad,
+                                (int32_t *)p.co, (int32_t *)p.cod, p.status, stream);
+  if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "descriptor kernel: %s", cudaGetErrorString(e));
+  if (ev && (st = record(ev[1], stream)) != GDP_OK) return st;
+  e = gdp::launch_wy(p, stream);
+  if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "WY kernel: %s", cudaGetErrorString(e));
+  if (ev && (st = record(ev[2], stream)) != GDP_OK) return st;
+  e = gdp::launch_scan(p, stream);
+  if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "scan kernel: %s", cudaGetErrorString(e));
+  if (ev && (st = record(ev[3], stream)) != GDP_OK) return st;
+  return GDP_OK;
+}
+
+}  // namespace
+
+GDP_EXPORT int64_t gdp_nt_pad(int64_t T, int64_t N) { return nt_bound(T, N); }
+
+GDP_EXPORT int64_t gdp_ntdp_pad(int64_t T, int64_t N, int M) { return ntdp_bound(T, N, M); }
+
+GDP_EXPORT size_t gdp_prefill_workspace_bytes(int64_t T, int64_t N, int H, int K, int V, int M) {
+  if (!shape_ok(T, N, H, K, V, M)) return 0;
+  return layout_for(T, N, H, K, V, M).total;
+}
+
+GDP_EXPORT const char *gdp_last_error(void) { return g_last_error; }
+
+GDP_EXPORT int gdp_abi_version(void) { return GDP_ABI_VERSION; }
+
+GDP_EXPORT size_t gdp_prefill_args_size(void) { return sizeof(gdp_prefill_args); }
+
+GDP_EXPORT gdp_status gdp_build_descriptors(const void *cu_seqlens, int cu_seqlens_int64, int64_t T, int64_t N,
+                                            int M, int32_t *chunk_indices, int64_t nt_pad,
+                                            int32_t *chunk_indices_dp, int64_t ntdp_pad, int32_t *chunk_offsets,
+                                            int32_t *chunk_offsets_dp, uint32_t *device_status, void *stream) {
+  g_last_error[0] = 0;
+  if (!cu_seqlens) return fail(GDP_ERR_INVALID_ARG, "cu_seqlens is NULL");
+  if (T < 0 || N < 0 || M < 1 || M > 64)
+    return fail(GDP_ERR_INVALID_ARG, "bad shape T=%lld N=%lld M=%d", (long long)T, (long long)N, M);
+  if (chunk_indices && !chunk_offsets) return fail(GDP_ERR_INVALID_ARG, "chunk_indices needs chunk_offsets");
+  if (chunk_indices_dp && !chunk_offsets_dp)
+    return fail(GDP_ERR_INVALID_ARG, "chunk_indices_dp needs chunk_offsets_dp");
+  if (chunk_indices && nt_pad < nt_bound(T, N))
+    return fail(GDP_ERR_INVALID_ARG, "nt_pad %lld < bound %lld", (long long)nt_pad, (long long)nt_bound(T, N));
+  if (chunk_indices_dp && ntdp_pad < ntdp_bound(T, N, M))
+    return fail(GDP_ERR_INVALID_ARG, "ntdp_pad %lld < bound %lld", (long long)ntdp_pad,
+                (long long)ntdp_bound(T, N, M));
+  cudaError_t e = gdp::launch_descriptors(cu_seqlens, cu_seqlens_int64, T, N, M, chunk_indices, nt_pad,
+                                          chunk_indices_dp, ntdp_pad, chunk_offsets, chunk_offsets_dp,
+                                          device_status, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "descriptor kernel: %s", cudaGetErrorString(e));
+  return GDP_OK;
+}
+
+GDP_EXPORT gdp_status gdp_prefill_varlen(const gdp_prefill_args *a, void *stream) {
+  return prefill(a, (cudaStream_t)stream, nullptr);
+}
+
+GDP_EXPORT gdp_status gdp_prefill_varlen_profiled(const gdp_prefill_args *a, void *stream, void *const *events,
+                                                  int num_events) {
+  if (!events || num_events != 4) {
+    g_last_error[0] = 0;
+    return fail(GDP_ERR_INVALID_ARG, "gdp_prefill_varlen_profiled needs exactly 4 events");
+  }
+  cudaEvent_t ev[4];
+  for (int i = 0; i < 4; ++i) ev[i] = (cudaEvent_t)events[i];
+  return prefill(a, (cudaStream_t)stream, ev);
+}

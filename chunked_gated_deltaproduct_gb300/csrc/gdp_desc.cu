@@ -1,0 +1,120 @@
+// gdp_desc.cu -- varlen descriptor builder (K1).
+//
+// Megatron-Core API page "core.ssm.ops.gdp.chunk": parameters chunk_indices,
+// chunk_indices_dp (the expanded stream, M times longer; not a rescaling of
+// chunk_indices since ceil(L*M/64) != M*ceil(L/64) in general), chunk_offsets
+// (prefix sum of the unexpanded chunk counts), and the closing paragraph
+// (descriptors padded to a fixed length keep the launch grids constant, which
+// makes the call capturable).
+//
+// One CTA: a block-wide exclusive scan over the sequences (tiles of 1024),
+// then every padded row finds its sequence by binary search over the offsets.
+// Grid and block sizes depend on nothing but the padded lengths.
+#include "gdp_internal.cuh"
+
+namespace gdp {
+namespace {
+
+constexpr int kDescThreads = 1024;
+
+__device__ __forceinline__ int block_exclusive_scan(int x, int *warp_sums, int *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = (lane < (int)(blockDim.x >> 5)) ? warp_sums[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    warp_sums[lane] = wi - w;
+    if (lane == 31) *total = wi;
+  }
+  __syncthreads();
+  int r = warp_sums[warp] + incl - x;
+  __syncthreads();
+  return r;
+}
+
+// Rows of one descriptor table: row r -> (sequence, local chunk), (-1,-1) past the end.
+__device__ void fill_rows(int32_t *rows, int64_t pad, const int32_t *offs, int64_t N) {
+  const int64_t total = offs[N];
+  for (int64_t r = threadIdx.x; r < pad; r += blockDim.x) {
+    int32_t seq = -1, c = -1;
+    if (r < total) {
+      int64_t lo = 0, hi = N - 1;  // last i with offs[i] <= r
+      while (lo < hi) {
+        int64_t mid = (lo + hi + 1) >> 1;
+        if (offs[mid] <= r) lo = mid; else hi = mid - 1;
+      }
+      seq = (int32_t)lo;
+      c = (int32_t)(r - offs[lo]);
+    }
+    rows[2 * r] = seq;
+    rows[2 * r + 1] = c;
+  }
+}
+
+__global__ void __launch_bounds__(kDescThreads) gdp_desc_kernel(const void *cu, int cu64, int64_t T, int64_t N,
+                                                                int M, int32_t *ci, int64_t nt_pad, int32_t *cid,
+                                                                int64_t ntdp_pad, int32_t *co, int32_t *cod,
+                                                                uint32_t *status) {
+  __shared__ int warp_sums[32];
+  __shared__ int tot_a, tot_b;
+  __shared__ int carry_a, carry_b;
+  if (threadIdx.x == 0) {
+    carry_a = carry_b = 0;
+    if (N > 0 && (load_cu(cu, cu64, 0) != 0 || load_cu(cu, cu64, N) != T)) set_status(status, GDP_DEV_ERR_CU_SEQLENS);
+  }
+  __syncthreads();
+  for (int64_t base = 0; base < N; base += blockDim.x) {
+    const int64_t i = base + threadIdx.x;
+    int a = 0, b = 0;
+    if (i < N) {
+      int64_t bos, L;
+      if (!seq_bounds(cu, cu64, T, i, &bos, &L)) set_status(status, GDP_DEV_ERR_CU_SEQLENS);  // owns no chunks
+      a = (int)((L + kChunk - 1) / kChunk);
+      b = (int)((L * M + kChunk - 1) / kChunk);
+    }
+    int ea = block_exclusive_scan(a, warp_sums, &tot_a);
+    int eb = block_exclusive_scan(b, warp_sums, &tot_b);
+    if (i < N) {
+      if (co) co[i] = carry_a + ea;
+      if (cod) cod[i] = carry_b + eb;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      carry_a += tot_a;
+      carry_b += tot_b;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    int a = carry_a, b = carry_b;
+    if ((ci && a > nt_pad) || (cid && b > ntdp_pad)) set_status(status, GDP_DEV_ERR_DESC);
+    if (co) co[N] = a;
+    if (cod) cod[N] = b;
+  }
+  __syncthreads();  // makes the offsets written above visible to the whole block
+  if (ci) fill_rows(ci, nt_pad, co, N);
+  if (cid) fill_rows(cid, ntdp_pad, cod, N);
+}
+
+}  // namespace
+
+cudaError_t launch_descriptors(const void *cu, int cu64, int64_t T, int64_t N, int M, int32_t *ci, int64_t nt_pad,
+                               int32_t *cid, int64_t ntdp_pad, int32_t *co, int32_t *cod, uint32_t *status,
+                               cudaStream_t stream) {
+  gdp_desc_kernel<<<1, kDescThreads, 0, stream>>>(cu, cu64, T, N, M, ci, nt_pad, cid, ntdp_pad, co, cod, status);
+  return cudaGetLastError();
+}
+
+}  // namespace gdp

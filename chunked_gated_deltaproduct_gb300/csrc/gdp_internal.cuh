@@ -1,0 +1,89 @@
+// gdp_internal.cuh -- shared definitions of the CUDA library (not part of the ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gdp_prefill.h"
+
+namespace gdp {
+
+constexpr int kChunk = GDP_CHUNK;       // rows per chunk on both streams
+constexpr float kL2Eps = 1e-6f;         // L2-norm epsilon: x / sqrt(sum x^2 + eps)
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Number of readout rows (rows t*M + M-1) a 64-row expanded chunk can hold,
+// rounded up to the MMA N granularity of 16.
+__host__ __device__ inline int qpad_for(int M) {
+  int q = (kChunk + M - 1) / M;
+  return (q + 15) / 16 * 16;
+}
+
+// Per-(expanded chunk, head) metadata written by the WY kernel.
+struct ChunkMeta {
+  float kscale[kChunk];  // 2^(G2_last - G2_s) * rk_s  (0 past the chunk end)
+  float qscale[kChunk];  // scale * 2^(G2_p) * rq_p for the q-th readout row p
+  float gamma_last;      // 2^(G2_last): decay of the whole chunk
+  int nq;                // readout rows in the chunk
+  int p0;                // local row of the first readout row
+  int len;               // rows in the chunk (<= 64)
+  int pad[4];
+};
+static_assert(sizeof(ChunkMeta) % 16 == 0, "ChunkMeta must stay 16-byte sized");
+
+// Everything a kernel needs about one call (passed by value).
+struct Problem {
+  const __nv_bfloat16 *q, *k, *v;
+  int64_t q_st, q_sh, k_st, k_sh, v_st, v_sh;
+  const float *g, *beta;
+  const void *cu;
+  int cu64;
+  int64_t T, N;
+  int H, K, V, M;
+  float scale;
+  int l2norm;
+  const float *init;
+  float *cache;
+  const int32_t *slots;
+  int64_t num_slots;
+  __nv_bfloat16 *out;
+  float *out_state;
+  float *chunk_states;
+  const int32_t *ci, *cid, *co, *cod;
+  int64_t nt_pad, ntdp_pad;
+  int64_t ws_rows;   // expanded-chunk rows the workspace tiles cover (shape bound)
+  // workspace tiles, indexed by (expanded chunk row r, head h): tile (r * H + h)
+  float *W;          // -W, [64][K] fp32 per tile
+  float *U;          // U, [64][V] fp32 per tile
+  float *P;          // masked decayed scores, [qpad][64] fp32 per tile
+  ChunkMeta *meta;   // one per tile
+  uint32_t *status;
+  int qpad;
+};
+
+__device__ __forceinline__ int64_t load_cu(const void *cu, int cu64, int64_t i) {
+  return cu64 ? reinterpret_cast<const int64_t *>(cu)[i] : (int64_t) reinterpret_cast<const int32_t *>(cu)[i];
+}
+
+// Bounds of sequence i; false (and L = 0) unless 0 <= cu[i] <= cu[i+1] <= T.
+__device__ __forceinline__ bool seq_bounds(const void *cu, int cu64, int64_t T, int64_t i, int64_t *bos, int64_t *L) {
+  const int64_t b = load_cu(cu, cu64, i), e = load_cu(cu, cu64, i + 1);
+  const bool ok = (b >= 0) && (b <= e) && (e <= T);
+  *bos = ok ? b : 0;
+  *L = ok ? e - b : 0;
+  return ok;
+}
+
+__device__ __forceinline__ void set_status(uint32_t *status, uint32_t bits) {
+  if (status) atomicOr(status, bits);
+}
+
+// Kernel launchers (defined in their .cu files).  Each returns a CUDA error.
+cudaError_t launch_descriptors(const void *cu, int cu64, int64_t T, int64_t N, int M, int32_t *ci, int64_t nt_pad,
+                               int32_t *cid, int64_t ntdp_pad, int32_t *co, int32_t *cod, uint32_t *status,
+                               cudaStream_t stream);
+cudaError_t launch_wy(const Problem &p, cudaStream_t stream);
+cudaError_t launch_scan(const Problem &p, cudaStream_t stream);
+
+}  // namespace gdp

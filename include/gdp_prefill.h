@@ -1,0 +1,198 @@
+/*
+ * gdp_prefill.h -- C ABI of the GB300 (sm_103a) chunked Gated DeltaProduct
+ * varlen prefill library (libgdp_gb300.so).
+ *
+ * What it computes (FlashInfer API page
+ * "flashinfer.gdp_prefill.chunk_gated_delta_product", opening paragraph and
+ * display equation): per real token t of each packed sequence,
+ *
+ *     S *= alpha_t                                   (alpha_t = exp(g_t))
+ *     for j = 0 .. n-1:  v_new = beta_{t,j} (v_{t,j} - S k_{t,j});  S += v_new (x) k_{t,j}
+ *     o_t = scale * S q_t
+ *
+ * with n = num_householder updates per token on the expanded sub-token stream
+ * (rows t*n .. t*n+n-1 of k, v, beta) and a V-major fp32 state S[v][k] per
+ * (sequence, head).  The work is chunked in 64-row chunks (Megatron-Core API
+ * page "core.ssm.ops.gdp.chunk", stage list): descriptors, within-chunk base-2
+ * decay cumsum (+ optional q/k L2 norm), WY factors, inter-chunk state scan,
+ * output combine and final-state scatter.
+ *
+ * Conventions for every entry point:
+ *   - Every pointer is a DEVICE pointer owned by the caller, except the
+ *     gdp_prefill_args struct itself (host memory, read during the call only).
+ *   - The library allocates nothing, never synchronises the device and never
+ *     reads device memory from the host, so a call can be captured in a CUDA
+ *     graph (Megatron page, closing paragraph: data-dependent descriptor
+ *     lengths on the host are what break capture; here they are built on the
+ *     device into buffers whose sizes depend on shapes only).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream); all work is
+ *     enqueued on it, in order.
+ *   - A host-side argument error returns a non-zero gdp_status before any
+ *     launch and leaves every buffer untouched; gdp_last_error() then returns
+ *     a one-line reason (per calling thread).  Data-dependent errors that
+ *     only the device can see (a bad cu_seqlens entry, an out-of-range slot)
+ *     are reported by OR-ing GDP_DEV_ERR_* bits into *device_status (when
+ *     given); the affected sequence is skipped, nothing traps.
+ *   - The caller serialises calls that share a workspace (same stream).
+ */
+#ifndef GDP_PREFILL_H
+#define GDP_PREFILL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDP_ABI_VERSION 1
+#define GDP_CHUNK 64 /* chunk size of both streams (Megatron page, stage list) */
+
+typedef enum gdp_status {
+  GDP_OK = 0,
+  GDP_ERR_INVALID_ARG = 1, /* NULL required pointer, bad shape, bad stride, bad mode mix */
+  GDP_ERR_UNSUPPORTED = 2, /* a shape/dtype this build does not serve (reason in gdp_last_error) */
+  GDP_ERR_ALIAS = 3,       /* output_state overlaps initial_state (FlashInfer page, output_state) */
+  GDP_ERR_WORKSPACE = 4,   /* workspace NULL, misaligned or smaller than gdp_prefill_workspace_bytes */
+  GDP_ERR_CUDA = 5         /* a CUDA launch/attribute call failed (reason in gdp_last_error) */
+} gdp_status;
+
+/* Bits OR-ed into *device_status by the kernels. */
+#define GDP_DEV_ERR_CU_SEQLENS 0x1u /* cu_seqlens not non-decreasing from 0 to T: bad sequences skipped */
+#define GDP_DEV_ERR_SLOT 0x2u       /* state_indices entry outside [-1, num_slots): treated as padding */
+#define GDP_DEV_ERR_DESC 0x4u       /* chunk counts exceed the padded descriptor lengths: tail skipped */
+
+/*
+ * Arguments of one prefill call.  Shapes use T real tokens, N sequences,
+ * H heads (q, k, v and the gates share one head count), K = V = head size,
+ * M = num_householder.  Element strides are in ELEMENTS; the innermost
+ * dimension is always contiguous (FlashInfer page, parameter q).
+ */
+typedef struct gdp_prefill_args {
+  /* q [T, H, K] bf16 at real-token rows (FlashInfer page, parameter q). */
+  const void *q;
+  int64_t q_stride_t, q_stride_h;
+  /* k [T*M, H, K] bf16 on the expanded stream: token t's M updates are rows
+     t*M .. t*M+M-1 (FlashInfer page, parameter k; Megatron page, parameter k). */
+  const void *k;
+  int64_t k_stride_t, k_stride_h;
+  /* v [T*M, H, V] bf16, same rows as k (FlashInfer page, parameter v). */
+  const void *v;
+  int64_t v_stride_t, v_stride_h;
+  /* g [T, H] fp32, contiguous: natural-log decay, alpha_t = exp(g_t)
+     (Megatron page, parameter g).  NULL = no decay. */
+  const float *g;
+  /* beta [T*M, H] fp32, contiguous, post-sigmoid (FlashInfer page, parameter
+     beta).  NULL = all ones. */
+  const float *beta;
+  /* cu_seqlens [N+1] over real tokens, int32 (cu_seqlens_int64 = 0) or int64
+     (FlashInfer page, parameter cu_seqlens). */
+  const void *cu_seqlens;
+  int cu_seqlens_int64;
+  int64_t T, N;
+  int H, K, V, num_householder;
+  /* Readout scale; <= 0 (or NaN) selects 1/sqrt(K) (FlashInfer page, scale:
+     None or 0.0; Megatron page, scale: K ** -0.5). */
+  float scale;
+  /* Non-zero: L2-normalise q and k rows in fp32 inside the kernels,
+     x / sqrt(sum x^2 + 1e-6) (FlashInfer page, use_qk_l2norm_in_kernel). */
+  int use_qk_l2norm;
+
+  /* Incoming state, one of two modes (or neither = zero state):
+     dense: initial_state [N, H, V, K] fp32 V-major (FlashInfer page,
+     initial_state); cache: state [num_slots, H, V, K] fp32 read and written IN
+     PLACE at slot state_indices[i] (int32 [N]); -1 marks a padding sequence,
+     which starts from zero, still produces output and writes no slot
+     (Megatron page, parameters state and state_indices).  In cache mode
+     output_state must be NULL: the final state goes to the cache only. */
+  const float *initial_state;
+  float *state;
+  const int32_t *state_indices;
+  int64_t num_slots;
+
+  /* o [T, H, V] bf16, contiguous, written (FlashInfer page, output). */
+  void *output;
+  /* Final state [N, H, V, K] fp32 or NULL.  Must not overlap initial_state:
+     several CTAs share one sequence, so a CTA writing the final state would
+     race one still reading the incoming state (FlashInfer page,
+     output_state). */
+  float *output_state;
+  /* Chunk states [nt_pad, H, V, K] fp32 or NULL (= return_chunk_states off).
+     Row chunk_offsets[i] + c holds sequence i's state ENTERING token chunk c,
+     i.e. after its first 64*c tokens (Megatron page, return_chunk_states).
+     Rows past the real count are not written. */
+  float *chunk_states;
+
+  /* Optional prebuilt descriptors from gdp_build_descriptors (all three or
+     none; Megatron page, parameters chunk_indices, chunk_indices_dp,
+     chunk_offsets): chunk_indices [nt_pad, 2], chunk_indices_dp [ntdp_pad, 2]
+     int32 rows (sequence, local chunk), (-1, -1) past the real count;
+     chunk_offsets [N+1] int32 exclusive prefix sum of ceil(L_i / 64).
+     They must come from the same cu_seqlens and M.  When NULL the call builds
+     them itself on the device.  nt_pad / ntdp_pad must be at least the
+     shape-only bounds gdp_nt_pad(T, N) / gdp_ntdp_pad(T, N, M) (0 = use those
+     bounds); chunk_states, when given, has nt_pad rows. */
+  const int32_t *chunk_indices;
+  const int32_t *chunk_indices_dp;
+  const int32_t *chunk_offsets;
+  int64_t nt_pad, ntdp_pad;
+
+  /* Scratch: at least gdp_prefill_workspace_bytes(...) bytes, 256-byte
+     aligned, owned by the caller, contents undefined on entry and exit. */
+  void *workspace;
+  size_t workspace_bytes;
+  /* Optional uint32 status word; GDP_DEV_ERR_* bits are OR-ed in. */
+  uint32_t *device_status;
+} gdp_prefill_args;
+
+/* Shape-only descriptor bounds: floor((T + 63 N) / 64) and floor((M T + 63 N) / 64). */
+int64_t gdp_nt_pad(int64_t T, int64_t N);
+int64_t gdp_ntdp_pad(int64_t T, int64_t N, int num_householder);
+
+/* Workspace bytes for a call of this shape (shape-only; the same value for
+   every cu_seqlens with the same T and N).  Returns 0 for an invalid shape. */
+size_t gdp_prefill_workspace_bytes(int64_t T, int64_t N, int H, int K, int V, int num_householder);
+
+/*
+ * The prefill forward pass: enqueue descriptors (unless prebuilt), the prep
+ * + WY kernel and the state-scan / output kernel on `stream`.
+ * Returns GDP_OK once enqueued.
+ */
+gdp_status gdp_prefill_varlen(const gdp_prefill_args *args, void *stream);
+
+/*
+ * Same as gdp_prefill_varlen, and records `events` (cudaEvent_t handles
+ * created by the caller with timing enabled) on `stream` around the stages:
+ * events[0] before the descriptor kernel, [1] after it, [2] after the WY
+ * kernel, [3] after the scan/output kernel.  num_events must be 4.  Used by
+ * the bench to time each kernel on its own stream; the results are identical
+ * to gdp_prefill_varlen.
+ */
+gdp_status gdp_prefill_varlen_profiled(const gdp_prefill_args *args, void *stream, void *const *events,
+                                       int num_events);
+
+/*
+ * Build the varlen descriptors on the device (Megatron page, parameters
+ * chunk_indices, chunk_indices_dp, chunk_offsets; capture note in the closing
+ * paragraph).  cu_seqlens [N+1] int32/int64 device; outputs as described in
+ * gdp_prefill_args; chunk_offsets_dp (optional, [N+1]) receives the prefix
+ * sum of ceil(L_i M / 64).  Grid sizes depend on N, nt_pad, ntdp_pad only.
+ */
+gdp_status gdp_build_descriptors(const void *cu_seqlens, int cu_seqlens_int64, int64_t T, int64_t N,
+                                 int num_householder, int32_t *chunk_indices, int64_t nt_pad,
+                                 int32_t *chunk_indices_dp, int64_t ntdp_pad, int32_t *chunk_offsets,
+                                 int32_t *chunk_offsets_dp, uint32_t *device_status, void *stream);
+
+/* One-line reason for the last non-OK status returned on this thread ("" if none). */
+const char *gdp_last_error(void);
+
+/* GDP_ABI_VERSION of the loaded library. */
+int gdp_abi_version(void);
+
+/* sizeof(gdp_prefill_args) as compiled into the library (lets a binding check its struct layout). */
+size_t gdp_prefill_args_size(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GDP_PREFILL_H */

@@ -1,0 +1,115 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every entry point the header declares, agrees with the binding on the argument
+struct, answers the shape-only queries, and rejects bad arguments before any
+launch with the documented status codes."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import chunked_gated_deltaproduct_gb300 as pkg
+from chunked_gated_deltaproduct_gb300 import build as libbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return pkg.load_library()
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(HEADER_DIR):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(HEADER_DIR, fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(gdp_[a-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert "gdp_prefill_varlen" in declared and "gdp_build_descriptors" in declared
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+    assert lib.gdp_abi_version() == 1
+
+
+def test_args_struct_layout(lib):
+    assert lib.gdp_prefill_args_size() == ctypes.sizeof(pkg.GdpPrefillArgs)
+
+
+def test_padding_bounds_and_workspace(lib):
+    assert pkg.gdp_nt_pad(1421, 4) == 26 and pkg.gdp_ntdp_pad(1421, 4, 2) == 48
+    assert pkg.gdp_ntdp_pad(257, 1, 3) == 13
+    a = pkg.gdp_prefill_workspace_bytes(65536, 1, 32, 128, 128, 2)
+    b = pkg.gdp_prefill_workspace_bytes(65536, 1, 32, 128, 128, 2)
+    assert a == b > 0 and a % 256 == 0
+    assert pkg.gdp_prefill_workspace_bytes(-1, 1, 1, 64, 64, 1) == 0
+    assert pkg.gdp_prefill_workspace_bytes(10, 1, 1, 64, 64, 0) == 0
+
+
+def _args(**over):
+    a = pkg.GdpPrefillArgs()
+    T, N, H, K = 8, 1, 1, 64
+    fake = 1 << 20  # a 16-byte aligned non-NULL address; never dereferenced on these paths
+    a.q = a.k = a.v = a.output = fake
+    a.q_stride_t, a.q_stride_h = H * K, K
+    a.k_stride_t, a.k_stride_h = H * K, K
+    a.v_stride_t, a.v_stride_h = H * K, K
+    a.cu_seqlens = fake
+    a.T, a.N, a.H, a.K, a.V, a.num_householder = T, N, H, K, K, 1
+    a.workspace = fake
+    a.workspace_bytes = pkg.gdp_prefill_workspace_bytes(T, N, H, K, K, 1)
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(K=96, V=96), pkg.GDP_ERR_UNSUPPORTED),
+    (dict(K=64, V=128), pkg.GDP_ERR_UNSUPPORTED),
+    (dict(num_householder=0), pkg.GDP_ERR_INVALID_ARG),
+    (dict(q=None), pkg.GDP_ERR_INVALID_ARG),
+    (dict(q_stride_h=60), pkg.GDP_ERR_INVALID_ARG),
+    (dict(q=(1 << 20) + 8), pkg.GDP_ERR_INVALID_ARG),
+    (dict(initial_state=1 << 21, state=1 << 22, state_indices=1 << 23, num_slots=4), pkg.GDP_ERR_INVALID_ARG),
+    (dict(state=1 << 22), pkg.GDP_ERR_INVALID_ARG),
+    (dict(state=1 << 22, state_indices=1 << 23, num_slots=4, output_state=1 << 24), pkg.GDP_ERR_INVALID_ARG),
+    (dict(initial_state=1 << 24, output_state=(1 << 24) + 4096), pkg.GDP_ERR_ALIAS),
+    (dict(chunk_indices=1 << 21), pkg.GDP_ERR_INVALID_ARG),
+    (dict(workspace=None), pkg.GDP_ERR_WORKSPACE),
+    (dict(workspace=(1 << 20) + 16), pkg.GDP_ERR_WORKSPACE),
+    (dict(workspace_bytes=64), pkg.GDP_ERR_WORKSPACE),
+    (dict(T=200, nt_pad=1, ntdp_pad=1, chunk_indices=1 << 21, chunk_indices_dp=1 << 21, chunk_offsets=1 << 21),
+     pkg.GDP_ERR_INVALID_ARG),
+])
+def test_host_validation(lib, over, status):
+    a = _args(**over)
+    st = lib.gdp_prefill_varlen(ctypes.byref(a), None)
+    assert st == status, (st, pkg.gdp_last_error())
+    assert pkg.gdp_last_error() != ""
+
+
+def test_profiled_needs_four_events(lib):
+    a = _args()
+    st = lib.gdp_prefill_varlen_profiled(ctypes.byref(a), None, None, 0)
+    assert st == pkg.GDP_ERR_INVALID_ARG
+
+
+def test_empty_batch_is_ok_without_launch(lib):
+    a = _args(T=0, N=0)
+    a.workspace_bytes = pkg.gdp_prefill_workspace_bytes(0, 0, 1, 64, 64, 1)
+    assert lib.gdp_prefill_varlen(ctypes.byref(a), None) == pkg.GDP_OK
+    assert pkg.gdp_last_error() == ""
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError):
+        pkg.load_library(str(tmp_path / "nope.so"))
