@@ -1,0 +1,383 @@
+"""Bench: real tokens/s of the GDP varlen prefill on one GB300 (device-timed),
+with the dominant kernel's roofline fraction, an end-to-end leg through host
+buffers, and the float64 CPU oracle as the reported CPU baseline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 2] [--impl gdp|reference]
+
+A step is one full gdp_prefill_varlen call (descriptor kernel, prep + WY
+kernel, scan/output kernel) over one batch of the synthetic workload, inputs
+resident in HBM.  Between timed steps a 256 MiB buffer is written to flush the
+129 MB L2.  Each stage is timed with CUDA events recorded by the library on
+the launching stream (gdp_prefill_varlen_profiled).  Under torchrun every rank
+runs its own independent batch of the same shape (weak scaling, no
+collective); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gdp_workloads import WORKLOADS, make_workload  # noqa: E402
+
+METRIC = "GDP prefill real tokens/s on 1 GB300 (device-timed) and % of roofline"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+# DRAM traffic of the dominant kernel per launch, from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the sha256 of the
+# kernel source it was taken on; reported as null once the source changes.
+NCU_TRAFFIC = {}
+
+
+def alg_bytes(w) -> int:
+    """Algorithmic bytes of one call: inputs read once, outputs written once
+    (q, o bf16; M x (k, v) bf16; g fp32; M x beta fp32 per token-head) plus the
+    fp32 states read and written and the requested chunk states."""
+    d, M, H = w.d, w.M, w.H
+    b_tok = 2 * d * (1 + 2 * M + 1) + 4 + 4 * M
+    total = b_tok * w.T * H
+    st = d * d * 4
+    if w.initial_state is not None:
+        total += w.N * H * st
+    if w.state is not None:
+        live = int((w.state_indices >= 0).sum())
+        total += 2 * live * H * st  # slot read + slot write
+    elif w.output_final_state:
+        total += w.N * H * st
+    if w.return_chunk_states:
+        total += w.NT * H * st
+    return int(total)
+
+
+def alg_flops(w) -> float:
+    """Dense-tile flops per expanded chunk (r rows, q = r/M readout rows)."""
+    d, M = w.d, w.M
+    f = 0.0
+    for L in w.lengths:
+        rows = L * M
+        for c in range(0, rows, 64):
+            r = min(64, rows - c)
+            q = r / M
+            f += 2 * r * r * d + r ** 3 / 3 + 4 * r * r * d + 4 * r * d * d + 2 * q * d * d + 4 * q * r * d
+    return f * w.H
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            j = json.load(fh)
+        return float(j.get("hbm_gbs", FALLBACK_HBM_GBS)), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc, self.path = index, None, None
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _kernel_sha(name: str) -> str:
+    p = os.path.join(ROOT, "chunked_gated_deltaproduct_gb300", "csrc", name)
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16] if os.path.exists(p) else ""
+
+
+def cpu_oracle_baseline(w, budget_s: float):
+    """The oracle as it stands on this host's cores, over a bounded sample:
+    whole-workload repetitions, or a subset of heads when one run is too long."""
+    import oracle
+
+    threads = oracle.oracle_threads()
+    heads = list(range(w.H))
+    t0 = time.perf_counter()
+    oracle.forward(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, w.M, w.scale, use_qk_l2norm=w.use_qk_l2norm,
+                   initial_state=w.initial_state, state=w.state, state_indices=w.state_indices,
+                   chunk_states=w.return_chunk_states, heads=[0], threads=threads)
+    per_head = time.perf_counter() - t0
+    nh = max(1, min(w.H, int(budget_s / max(per_head, 1e-6))))
+    heads = heads[:nh]
+    reps = max(1, int(budget_s / max(per_head * nh, 1e-6))) if nh == w.H else 1
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.forward(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, w.M, w.scale, use_qk_l2norm=w.use_qk_l2norm,
+                       initial_state=w.initial_state, state=w.state, state_indices=w.state_indices,
+                       chunk_states=w.return_chunk_states, heads=heads, threads=threads)
+    el = time.perf_counter() - t0
+    value = w.T * (nh / w.H) * reps / el
+    return {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{reps} run(s) of heads 0..{nh - 1} of {w.H} over all {w.T} tokens, {el:.1f} s"}
+
+
+def run_reference(args, w, rank):
+    """Reference arm: the float64 oracle on the host cores, a bounded sample per step."""
+    import oracle
+
+    if rank != 0:
+        return
+    threads = oracle.oracle_threads()
+    total_steps = args.steps + args.warmup
+    per_step_budget = max(0.02, min(5.0, 150.0 / max(total_steps, 1)))
+    t0 = time.perf_counter()
+    oracle.forward(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, w.M, w.scale, use_qk_l2norm=w.use_qk_l2norm,
+                   initial_state=w.initial_state, state=w.state, state_indices=w.state_indices,
+                   chunk_states=w.return_chunk_states, heads=[0], threads=threads)
+    per_head = time.perf_counter() - t0
+    frac = min(1.0, per_step_budget / max(per_head, 1e-9))
+    # sample: head h (rotating), every sequence truncated to its first `frac` share of tokens
+    lens = [max(1, int(math.ceil(L * frac))) if L else 0 for L in w.lengths]
+    cu = w.cu_seqlens.tolist()
+    tok = torch.cat([torch.arange(cu[i], cu[i] + lens[i]) for i in range(w.N)]) if w.T else torch.arange(0)
+    rows = (tok[:, None] * w.M + torch.arange(w.M)[None]).reshape(-1)
+    sub_cu = [0]
+    for L in lens:
+        sub_cu.append(sub_cu[-1] + L)
+    q, k, v = w.q[tok], w.k[rows], w.v[rows]
+    g = None if w.g is None else w.g[tok]
+    beta = None if w.beta is None else w.beta[rows]
+    Ts = len(tok)
+    times = []
+    for s in range(total_steps):
+        h = s % w.H
+        t0 = time.perf_counter()
+        oracle.forward(q, k, v, g, beta, sub_cu, w.M, w.scale, use_qk_l2norm=w.use_qk_l2norm,
+                       initial_state=w.initial_state, state=w.state, state_indices=w.state_indices,
+                       chunk_states=w.return_chunk_states, heads=[h], threads=threads)
+        if s >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    el = sum(times)
+    value = Ts * (1.0 / w.H) * len(times) / el if el > 0 else 0.0
+    sample = f"per step: 1 of {w.H} heads (rotating), first {frac:.3f} of each sequence ({Ts} of {w.T} tokens)"
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * el / max(len(times), 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {**w.describe(), "l2_flush": False}, "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=2, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="gdp", choices=["gdp", "reference"])
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+
+        dist = dist_mod
+        dist.init_process_group("nccl" if args.impl == "gdp" else "gloo")
+
+    seed = 1000 + args.workload + 7919 * rank if rank else None
+    w = make_workload(args.workload, seed=seed)
+
+    if args.impl == "reference":
+        run_reference(args, w, rank)
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    import chunked_gated_deltaproduct_gb300 as pkg
+
+    pkg.load_library()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(dev)
+    q, k, v = w.q.to(dev), w.k.to(dev), w.v.to(dev)
+    g = None if w.g is None else w.g.to(dev)
+    beta = None if w.beta is None else w.beta.to(dev)
+    cu = w.cu_seqlens.to(dev)
+    init = None if w.initial_state is None else w.initial_state.to(dev)
+    cache = None if w.state is None else w.state.to(dev)
+    sidx = None if w.state_indices is None else w.state_indices.to(dev)
+    out = torch.empty((w.T, w.H, w.d), dtype=torch.bfloat16, device=dev)
+    fin = torch.empty((w.N, w.H, w.d, w.d), dtype=torch.float32, device=dev) if (
+        w.output_final_state and cache is None) else None
+    cs = torch.zeros((pkg.gdp_nt_pad(w.T, w.N), w.H, w.d, w.d), dtype=torch.float32, device=dev) if (
+        w.return_chunk_states) else None
+    ci = cid = co = None
+    if w.prebuilt_descriptors:
+        ci, cid, co = pkg.gdp_build_descriptors(cu, w.T, w.M)
+    ws = pkg.alloc_workspace(w.T, w.N, w.H, w.d, w.d, w.M, dev)
+    a = pkg.make_args(q, k, v, g, beta, cu, w.M, w.scale, init, cache, sidx, out, fin, cs, ci, cid, co, None, None,
+                      w.use_qk_l2norm, ws, None)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    sid = stream.cuda_stream
+    torch.cuda.synchronize()
+
+    def new_events():
+        # torch creates the CUDA event lazily at its first record(); record once so the raw
+        # handle exists and torch accepts elapsed_time(); the library then re-records it.
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        for e in evs:
+            e.record(stream)
+        return evs
+
+    def step(evs):
+        with torch.cuda.stream(stream):
+            flush.zero_()
+        pkg.gdp_prefill_varlen_profiled(a, evs, sid)
+
+    for _ in range(args.warmup):
+        step(new_events())
+    torch.cuda.synchronize()
+
+    events = [new_events() for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for s in range(args.steps):
+            step(events[s])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    if dist:
+        dist.barrier()
+    stage = [[ev[i].elapsed_time(ev[i + 1]) for i in range(3)] for ev in events]
+    step_ms = [ev[0].elapsed_time(ev[3]) for ev in events]
+    total_s = sum(step_ms) / 1e3
+    if dist:
+        t = torch.tensor([total_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_s = float(t.item())
+    value = world * w.T * args.steps / total_s
+    kernel_names = ["gdp_desc_kernel", "gdp_wy_kernel", "gdp_scan_kernel"]
+    kernel_ms = [statistics.fmean(x[i] for x in stage) for i in range(3)]
+    dom = max(range(3), key=lambda i: kernel_ms[i])
+    peak, peak_src = measured_peaks()
+    ab = alg_bytes(w)
+    achieved = ab / (kernel_ms[dom] / 1e3) / 1e9
+    step_gbs = ab / (statistics.fmean(step_ms) / 1e3) / 1e9
+    src_file = {0: "gdp_desc.cu", 1: "gdp_wy.cu", 2: "gdp_scan.cu"}[dom]
+    tr = NCU_TRAFFIC.get(kernel_names[dom])
+    traffic = tr["bytes_per_launch"] if (tr and tr.get("sha") == _kernel_sha(src_file)) else None
+
+    # ---- end to end: pinned host inputs -> device -> call -> host outputs
+    host_in = [t.pin_memory() for t in (w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, w.initial_state, w.state,
+                                        w.state_indices) if t is not None]
+    dev_in = [t for t in (q, k, v, g, beta, cu, init, cache, sidx) if t is not None]
+    dev_out = [t for t in (out, fin, cs) if t is not None]
+    if cache is not None:
+        dev_out.append(cache)
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_out]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    e2e_ms = []
+    for s in range(args.e2e_steps + 2):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            e0.record(stream)
+            for hsrc, ddst in zip(host_in, dev_in):
+                ddst.copy_(hsrc, non_blocking=True)
+            pkg.gdp_prefill_varlen(a, sid)
+            for dsrc, hdst in zip(dev_out, host_out):
+                hdst.copy_(dsrc, non_blocking=True)
+            e1.record(stream)
+        e1.synchronize()
+        if s >= 2:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_value = world * w.T / (statistics.fmean(e2e_ms) / 1e3)
+
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            cpu = cpu_oracle_baseline(w, args.cpu_budget_s)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {**w.describe(), "l2_flush": True, "flush_bytes": flush.numel()},
+            "roofline": {"bound": "hbm", "kernel": kernel_names[dom], "achieved": achieved, "peak": peak,
+                         "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                         "alg_bytes_per_launch": ab, "kernel_ms": kernel_ms[dom],
+                         "step_achieved": step_gbs, "step_frac": step_gbs / peak,
+                         "alg_gflop_per_step": alg_flops(w) / 1e9},
+            "kernels_ms": dict(zip(kernel_names, kernel_ms)),
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": statistics.fmean(e2e_ms)},
+            "gpu_launches": 3 * args.steps,
+            "clocks": clk.summary(),
+            "wall_s_timed": wall,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

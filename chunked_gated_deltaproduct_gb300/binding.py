@@ -122,7 +122,10 @@ def gdp_prefill_varlen(args: GdpPrefillArgs, stream: int | None = None) -> None:
 def gdp_prefill_varlen_profiled(args: GdpPrefillArgs, events, stream: int | None = None) -> None:
     """As gdp_prefill_varlen, recording the 4 torch.cuda.Event objects around the stages."""
     lib = load_library()
-    arr = (_vp * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    handles = [e.cuda_event for e in events]
+    if len(handles) != 4 or not all(handles):
+        raise GdpError(GDP_ERR_INVALID_ARG, "need 4 created events (record each once before passing it)")
+    arr = (_vp * 4)(*[ctypes.c_void_p(h) for h in handles])
     st = lib.gdp_prefill_varlen_profiled(ctypes.byref(args), ctypes.c_void_p(_stream(stream)), arr, len(events))
     if st != GDP_OK:
         raise GdpError(st, lib.gdp_last_error().decode())
