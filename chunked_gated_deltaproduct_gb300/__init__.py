@@ -25,6 +25,8 @@ from .binding import (  # noqa: F401
     gdp_ntdp_pad,
     gdp_prefill_varlen,
     gdp_prefill_varlen_profiled,
+    gdp_prefill_varlen_static_scratch,
+    GDP_STATIC_SCRATCH_BYTES,
     gdp_prefill_workspace_bytes,
     load_library,
     make_args,

@@ -70,6 +70,8 @@ def load_library(path: str | None = None):
     lib.gdp_prefill_varlen.argtypes = [ctypes.POINTER(GdpPrefillArgs), _vp]
     lib.gdp_prefill_varlen_profiled.restype = _int
     lib.gdp_prefill_varlen_profiled.argtypes = [ctypes.POINTER(GdpPrefillArgs), _vp, ctypes.POINTER(_vp), _int]
+    lib.gdp_prefill_varlen_static_scratch.restype = _int
+    lib.gdp_prefill_varlen_static_scratch.argtypes = [ctypes.POINTER(GdpPrefillArgs), _vp]
     lib.gdp_prefill_workspace_bytes.restype = _sz
     lib.gdp_prefill_workspace_bytes.argtypes = [_i64, _i64, _int, _int, _int, _int]
     lib.gdp_build_descriptors.restype = _int
@@ -127,6 +129,19 @@ def gdp_prefill_varlen_profiled(args: GdpPrefillArgs, events, stream: int | None
         raise GdpError(GDP_ERR_INVALID_ARG, "need 4 created events (record each once before passing it)")
     arr = (_vp * 4)(*[ctypes.c_void_p(h) for h in handles])
     st = lib.gdp_prefill_varlen_profiled(ctypes.byref(args), ctypes.c_void_p(_stream(stream)), arr, len(events))
+    if st != GDP_OK:
+        raise GdpError(st, lib.gdp_last_error().decode())
+
+
+GDP_STATIC_SCRATCH_BYTES = 64 << 20
+
+
+def gdp_prefill_varlen_static_scratch(args: GdpPrefillArgs, stream: int | None = None) -> None:
+    """The prefill without a caller workspace: the library's own static scratch
+    (GDP_STATIC_SCRATCH_BYTES) is used instead, for callers that cannot allocate
+    device memory; args.workspace is ignored.  Calls that overlap on the GPU race."""
+    lib = load_library()
+    st = lib.gdp_prefill_varlen_static_scratch(ctypes.byref(args), ctypes.c_void_p(_stream(stream)))
     if st != GDP_OK:
         raise GdpError(st, lib.gdp_last_error().decode())
 

@@ -194,6 +194,13 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
 
 }  // namespace
 
+void gdp::set_last_error(const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+}
+
 GDP_EXPORT int64_t gdp_nt_pad(int64_t T, int64_t N) { return nt_bound(T, N); }
 
 GDP_EXPORT int64_t gdp_ntdp_pad(int64_t T, int64_t N, int M) { return ntdp_bound(T, N, M); }

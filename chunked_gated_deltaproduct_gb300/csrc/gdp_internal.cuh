@@ -86,4 +86,7 @@ cudaError_t launch_descriptors(const void *cu, int cu64, int64_t T, int64_t N, i
 cudaError_t launch_wy(const Problem &p, cudaStream_t stream);
 cudaError_t launch_scan(const Problem &p, cudaStream_t stream);
 
+// Sets the calling thread's gdp_last_error() text (defined in gdp_api.cu).
+void set_last_error(const char *fmt, ...);
+
 }  // namespace gdp

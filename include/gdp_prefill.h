@@ -172,6 +172,28 @@ gdp_status gdp_prefill_varlen_profiled(const gdp_prefill_args *args, void *strea
                                        int num_events);
 
 /*
+ * gdp_prefill_varlen_static_scratch: the same prefill for callers that cannot
+ * allocate device memory.  No counterpart on the pages: it exists because the
+ * main entry point needs a caller-owned workspace, and some callers cannot
+ * provide one -- a plugin inside another runtime that owns all device memory
+ * through its own pool, or a host program without a caching allocator that may
+ * not call cudaMalloc in its serving loop (cudaMalloc can synchronise the device).
+ *
+ * Arguments are those of gdp_prefill_varlen, except that args->workspace and
+ * args->workspace_bytes are ignored: the scratch is a GDP_STATIC_SCRATCH_BYTES
+ * (64 MiB) array inside the library, held by every GPU that loads the library
+ * until the process exits.  A shape whose gdp_prefill_workspace_bytes exceeds
+ * it is rejected with GDP_ERR_WORKSPACE before any launch.  Nothing is
+ * allocated.  The first call on each device looks the array's device address
+ * up (cudaGetSymbolAddress, that device current) and caches it; make that
+ * first call outside any stream capture.  All calls share the array, so calls
+ * whose kernels overlap on the GPU (other streams, other threads) race:
+ * serialise them.  Nothing in the array needs to start at zero.
+ */
+#define GDP_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
+gdp_status gdp_prefill_varlen_static_scratch(const gdp_prefill_args *args, void *stream);
+
+/*
  * Build the varlen descriptors on the device (Megatron page, parameters
  * chunk_indices, chunk_indices_dp, chunk_offsets; capture note in the closing
  * paragraph).  cu_seqlens [N+1] int32/int64 device; outputs as described in
