@@ -21,7 +21,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libgdp_gb300.so")
 
 GDP_OK, GDP_ERR_INVALID_ARG, GDP_ERR_UNSUPPORTED, GDP_ERR_ALIAS, GDP_ERR_WORKSPACE, GDP_ERR_CUDA = range(6)
-GDP_DEV_ERR_CU_SEQLENS, GDP_DEV_ERR_SLOT, GDP_DEV_ERR_DESC = 0x1, 0x2, 0x4
+GDP_DEV_ERR_CU_SEQLENS, GDP_DEV_ERR_SLOT, GDP_DEV_ERR_DESC, GDP_DEV_ERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 STATUS_NAMES = {0: "GDP_OK", 1: "GDP_ERR_INVALID_ARG", 2: "GDP_ERR_UNSUPPORTED", 3: "GDP_ERR_ALIAS",
                 4: "GDP_ERR_WORKSPACE", 5: "GDP_ERR_CUDA"}
 

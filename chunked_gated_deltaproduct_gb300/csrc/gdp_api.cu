@@ -33,7 +33,7 @@ int64_t ntdp_bound(int64_t T, int64_t N, int M) {
 
 // Workspace layout; identical for the size query and the carving.
 struct Layout {
-  size_t cod, ci, cid, co, W, U, P, meta, total;
+  size_t cod, ci, cid, co, img, img_stride, U, total;
 };
 
 Layout layout_for(int64_t T, int64_t N, int H, int K, int V, int M) {
@@ -51,10 +51,9 @@ Layout layout_for(int64_t T, int64_t N, int H, int K, int V, int M) {
   l.cid = take(sizeof(int32_t) * 2 * (size_t)ntdp);
   l.co = take(sizeof(int32_t) * (size_t)(N + 1));
   const size_t tiles = (size_t)ntdp * (size_t)H;
-  l.W = take(sizeof(float) * tiles * gdp::kChunk * (size_t)K);
+  l.img_stride = align_up(gdp::ImageLayout(K, qp).bytes);
+  l.img = take(l.img_stride * tiles);
   l.U = take(sizeof(float) * tiles * gdp::kChunk * (size_t)V);
-  l.P = take(sizeof(float) * tiles * (size_t)qp * gdp::kChunk);
-  l.meta = take(sizeof(gdp::ChunkMeta) * tiles);
   l.total = off;
   return l;
 }
@@ -167,10 +166,9 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
     p.cid = (int32_t *)(ws + lay.cid);
     p.co = (int32_t *)(ws + lay.co);
   }
-  p.W = (float *)(ws + lay.W);
+  p.img = (unsigned char *)(ws + lay.img);
+  p.img_stride = lay.img_stride;
   p.U = (float *)(ws + lay.U);
-  p.P = (float *)(ws + lay.P);
-  p.meta = (gdp::ChunkMeta *)(ws + lay.meta);
   p.status = a->device_status;
   p.qpad = gdp::qpad_for(M);
 

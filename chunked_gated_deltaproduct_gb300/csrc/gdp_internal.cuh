@@ -20,17 +20,31 @@ __host__ __device__ inline int qpad_for(int M) {
   return (q + 15) / 16 * 16;
 }
 
-// Per-(expanded chunk, head) metadata written by the WY kernel.
-struct ChunkMeta {
-  float kscale[kChunk];  // 2^(G2_last - G2_s) * rk_s  (0 past the chunk end)
-  float qscale[kChunk];  // scale * 2^(G2_p) * rq_p for the q-th readout row p
-  float gamma_last;      // 2^(G2_last): decay of the whole chunk
-  int nq;                // readout rows in the chunk
-  int p0;                // local row of the first readout row
-  int len;               // rows in the chunk (<= 64)
-  int pad[4];
+// Per-(expanded chunk, head) operand image written by the WY kernel and copied
+// as one block into shared memory by the scan kernel.  Every sub-tile is fp32,
+// K-major with the 128-byte swizzle (gdp_sm100.cuh), 1024-byte aligned:
+//   Wn  [64 rows s][d]   : -W                        (B of V_new  = U - W S^T)
+//   Kt  [d rows f][64 s] : 2^(G2_last-G2_s) khat_s^T (B of S     += V_new^T Ktil)
+//   Qh  [qpad rows][d]   : scale 2^(G2_p) qhat       (B of o      = S qhat...)
+//   Pm  [qpad rows][64 s]: masked decayed scores     (B of o     += P V_new)
+//   meta                 : gamma_last, nq, p0, len
+struct ImageLayout {
+  uint32_t wn, kt, qh, pm, meta, bytes;
+  __host__ __device__ ImageLayout(int d, int qpad) {
+    wn = 0;
+    kt = wn + 64u * d * 4u;
+    qh = kt + (uint32_t)d * 64u * 4u;
+    pm = qh + (uint32_t)qpad * d * 4u;
+    meta = pm + (uint32_t)qpad * 64u * 4u;
+    bytes = meta + 64u;
+  }
 };
-static_assert(sizeof(ChunkMeta) % 16 == 0, "ChunkMeta must stay 16-byte sized");
+struct ImageMeta {
+  float gamma_last;  // 2^(G2_last): decay of the whole chunk
+  int nq;            // readout rows in the chunk
+  int p0;            // local row of the first readout row
+  int len;           // rows in the chunk (<= 64)
+};
 
 // Everything a kernel needs about one call (passed by value).
 struct Problem {
@@ -54,10 +68,9 @@ struct Problem {
   int64_t nt_pad, ntdp_pad;
   int64_t ws_rows;   // expanded-chunk rows the workspace tiles cover (shape bound)
   // workspace tiles, indexed by (expanded chunk row r, head h): tile (r * H + h)
-  float *W;          // -W, [64][K] fp32 per tile
-  float *U;          // U, [64][V] fp32 per tile
-  float *P;          // masked decayed scores, [qpad][64] fp32 per tile
-  ChunkMeta *meta;   // one per tile
+  unsigned char *img;  // operand images, img_stride bytes per tile (ImageLayout)
+  size_t img_stride;
+  float *U;            // U = T diag(beta) V, [64][V] fp32 per tile, row-major
   uint32_t *status;
   int qpad;
 };

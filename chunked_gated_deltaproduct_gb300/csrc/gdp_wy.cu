@@ -1,49 +1,72 @@
-// gdp_wy.cu -- per-(expanded chunk, head) prep + WY kernel.
+// gdp_wy.cu -- per-(expanded chunk, head) prep + WY kernel on the tcgen05 tensor cores.
 //
 // Megatron-Core API page "core.ssm.ops.gdp.chunk", stages 1 and 2:
 //   stage 1: the log decay of token t is placed on its first expanded row
 //            t*M (interleave), the within-chunk cumulative sum is taken on the
-//            expanded stream and converted to base 2 (exp2 everywhere);
+//            expanded stream and converted to base 2 (exp2 everywhere); q and k
+//            are optionally L2-normalised (FlashInfer page,
+//            use_qk_l2norm_in_kernel) -- applied as per-row scale factors;
 //   stage 2: A = beta K K^T (strictly lower, decay-weighted), T = (I + A)^-1,
 //            then the w and u factors.
-// With gamma_r = 2^G2_r and khat = k / |k| (or k):
+// With gamma_r = 2^G2_r, khat = rk k (rk = 1 / |k| or 1):
 //   A[i][j] = beta_i 2^(G2_i - G2_j) (khat_i . khat_j)        (i > j)
 //   W = T diag(beta gamma) Khat,   U = T diag(beta) V
 // so that inside the chunk the new values are V_new = U - W S0^T for the
 // entering state S0 (derived from the recurrence on the FlashInfer page,
-// display equation).  The kernel also forms the masked, decay-weighted
-// intra-chunk scores of the readout rows used by the output stage:
-//   P[q][s] = scale 2^(G2_p - G2_s) (qhat_t . khat_s)   for s <= p,
-// where p = t*M + M - 1 is the readout row of token t.  Every exponent is of
-// a difference G2_i - G2_j with i >= j, so every factor is <= 1.
+// display equation).  The kernel also forms what the output stage needs:
+//   P[q][s] = scale 2^(G2_p - G2_s) (qhat_t . khat_s)   for s <= p  (p = t*M + M - 1)
+//   Qh[q]   = scale 2^(G2_p) qhat_t,    Kt[s] = 2^(G2_last - G2_s) khat_s.
+// Every exponent is of a difference G2_i - G2_j with i >= j (or of a partial
+// sum <= 0), so no factor exceeds 1.
+//
+// Tensor-core work (cta_group::1, fp32 accumulators in TMEM):
+//   [K; Q] K^T  : kind::f16, M = 128 (64 key rows + up to 64 query rows), N = 64, K = d
+//   W^T = K^T (T diag(beta gamma rk))^T, U^T = V^T (T diag(beta))^T : kind::f16,
+//                 M = d, N = 64, K = 64, with T split as hi + lo bf16 (two MMAs
+//                 each) so that T keeps ~16 significant bits.
+// The inverse of the unit lower-triangular I + A runs on the CUDA cores in
+// 16 x 16 blocks: the four diagonal blocks by forward substitution (one warp
+// each), then T_ij = -T_ii sum_k A_ik T_kj for the off-diagonal blocks.
 #include "gdp_internal.cuh"
+#include "gdp_sm100.cuh"
 
 namespace gdp {
 namespace {
 
-constexpr int kWyThreads = 256;
+using namespace sm100;
 
-struct WySmem {
-  float *ks, *vs, *qs, *A, *Tm;
-  float *G2, *bt, *rk, *rq, *wc, *uc;
-  __device__ WySmem(float *base, int K, int V, int QP) {
-    ks = base;
-    vs = ks + kChunk * (K + 1);
-    qs = vs + kChunk * (V + 1);
-    A = qs + QP * (K + 1);
-    Tm = A + kChunk * (kChunk + 1);
-    G2 = Tm + kChunk * (kChunk + 1);
-    bt = G2 + kChunk;
-    rk = bt + kChunk;
-    rq = rk + kChunk;
-    wc = rq + kChunk;
-    uc = wc + kChunk;
-  }
-  __host__ __device__ static size_t bytes(int K, int V, int QP) {
-    return sizeof(float) * ((size_t)kChunk * (K + 1) + (size_t)kChunk * (V + 1) + (size_t)QP * (K + 1) +
-                            2 * (size_t)kChunk * (kChunk + 1) + 6 * kChunk);
+constexpr int kWyThreads = 128;
+constexpr int kLd = kChunk + 1;  // padded row length of the fp32 A / T scratch
+
+struct WyLayout {
+  uint32_t kq, vt, twh, twl, tuh, tul, A, T, Y, scal, total;
+  __host__ __device__ WyLayout(int d) {
+    const uint32_t nb = (uint32_t)d / 64;  // 64-element (128-byte) K blocks of a bf16 row
+    kq = 0;                                // [nb][128 rows][128 B]: rows 0..63 k, 64..127 q
+    vt = kq + nb * 16384u;                 // [nb][64 rows][128 B]
+    if (d == 128) {                        // reuse the query half of kq once [K;Q]K^T is done
+      twh = kq + 8192u;
+      twl = kq + 16384u + 8192u;
+      tuh = vt + nb * 8192u;
+      tul = tuh + 8192u;
+    } else {
+      twh = vt + nb * 8192u;
+      twl = twh + 8192u;
+      tuh = twl + 8192u;
+      tul = tuh + 8192u;
+    }
+    A = tul + 8192u;                       // fp32 [64][65]
+    T = A + 4u * kChunk * kLd;             // fp32 [64][65]
+    Y = T + 4u * kChunk * kLd;             // fp32 [3][16][16] block products
+    scal = Y + 4u * 3 * 256;               // G2, beta, rk, rq, wc, uc  [6][64]
+    total = scal + 4u * 6 * kChunk;
   }
 };
+
+__device__ __forceinline__ float bf16_at(const unsigned char *tile, int rows_per_block, int r, int f) {
+  const uint32_t off = (uint32_t)(f >> 6) * rows_per_block * 128u + swz(r, (uint32_t)(f & 63) * 2u);
+  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + off));
+}
 
 __global__ void __launch_bounds__(kWyThreads) gdp_wy_kernel(Problem p) {
   const int row = blockIdx.x, h = blockIdx.y;
@@ -52,158 +75,285 @@ __global__ void __launch_bounds__(kWyThreads) gdp_wy_kernel(Problem p) {
   int64_t bos, L;
   if (!seq_bounds(p.cu, p.cu64, p.T, seq, &bos, &L)) return;
   if (c < 0 || L <= 0 || (int64_t)c * kChunk >= L * p.M) return;
-  const int M = p.M, K = p.K, V = p.V, QP = p.qpad;
+  const int M = p.M, d = p.K, QP = p.qpad;
   const int64_t R0 = bos * M + (int64_t)c * kChunk;  // first global expanded row
   const int len = (int)min((int64_t)kChunk, L * M - (int64_t)c * kChunk);
   const int p0 = (int)((M - 1 - (R0 % M)) % M);
   const int nq = (p0 < len) ? (len - 1 - p0) / M + 1 : 0;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  extern __shared__ float4 smem_f4[];
-  WySmem sm(reinterpret_cast<float *>(smem_f4), K, V, QP);
-  const int tid = threadIdx.x;
+  extern __shared__ __align__(1024) unsigned char wy_smem_raw[];
+  unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)wy_smem_raw + 1023) & ~(uintptr_t)1023);
+  const WyLayout lay(d);
+  unsigned char *kq = sm + lay.kq, *vt = sm + lay.vt;
+  float *A = reinterpret_cast<float *>(sm + lay.A);
+  float *Tm = reinterpret_cast<float *>(sm + lay.T);
+  float *Y = reinterpret_cast<float *>(sm + lay.Y);
+  float *G2 = reinterpret_cast<float *>(sm + lay.scal);
+  float *bt = G2 + kChunk, *rk = bt + kChunk, *rq = rk + kChunk, *wc = rq + kChunk, *uc = wc + kChunk;
+  __shared__ uint32_t tmem_slot;
+  __shared__ __align__(8) uint64_t mma_bar;
+  __shared__ float warp_tot;
+  __shared__ int abort_flag;
 
-  // ---- loads (zero past the chunk end) ----
-  for (int idx = tid; idx < kChunk * K; idx += blockDim.x) {
-    int r = idx / K, f = idx % K;
-    float x = 0.f;
-    if (r < len) x = __bfloat162float(p.k[(R0 + r) * p.k_st + (int64_t)h * p.k_sh + f]);
-    sm.ks[r * (K + 1) + f] = x;
+  if (warp == 0) tmem_alloc(&tmem_slot, 256);
+  if (tid == 0) {
+    mbar_init(&mma_bar, 1);
+    mbar_init_fence();
+    abort_flag = 0;
   }
-  for (int idx = tid; idx < kChunk * V; idx += blockDim.x) {
-    int r = idx / V, f = idx % V;
-    float x = 0.f;
-    if (r < len) x = __bfloat162float(p.v[(R0 + r) * p.v_st + (int64_t)h * p.v_sh + f]);
-    sm.vs[r * (V + 1) + f] = x;
-  }
-  for (int idx = tid; idx < QP * K; idx += blockDim.x) {
-    int qi = idx / K, f = idx % K;
-    float x = 0.f;
-    if (qi < nq) {
-      int64_t t = (R0 + p0 + (int64_t)qi * M) / M;
-      x = __bfloat162float(p.q[t * p.q_st + (int64_t)h * p.q_sh + f]);
+
+  // ---- loads: 16-byte chunks into the swizzled bf16 tiles (zero past the chunk end) ----
+  const int cpr = d / 8;  // 16-byte chunks per row
+  for (int idx = tid; idx < 128 * cpr; idx += kWyThreads) {
+    const int r = idx / cpr, ch = idx % cpr;
+    uint4 x = make_uint4(0, 0, 0, 0);
+    if (r < kChunk) {
+      if (r < len) x = *reinterpret_cast<const uint4 *>(p.k + (R0 + r) * p.k_st + (int64_t)h * p.k_sh + ch * 8);
+    } else {
+      const int qi = r - kChunk;
+      if (qi < nq) {
+        const int64_t t = (R0 + p0 + (int64_t)qi * M) / M;
+        x = *reinterpret_cast<const uint4 *>(p.q + t * p.q_st + (int64_t)h * p.q_sh + ch * 8);
+      }
     }
-    sm.qs[qi * (K + 1) + f] = x;
+    *reinterpret_cast<uint4 *>(kq + (ch >> 3) * 16384u + swz(r, (ch & 7) * 16u)) = x;
   }
+  for (int idx = tid; idx < kChunk * cpr; idx += kWyThreads) {
+    const int r = idx / cpr, ch = idx % cpr;
+    uint4 x = make_uint4(0, 0, 0, 0);
+    if (r < len) x = *reinterpret_cast<const uint4 *>(p.v + (R0 + r) * p.v_st + (int64_t)h * p.v_sh + ch * 8);
+    *reinterpret_cast<uint4 *>(vt + (ch >> 3) * 8192u + swz(r, (ch & 7) * 16u)) = x;
+  }
+  fence_async_smem();
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_slot;
+  const uint32_t tD1 = tbase, tW = tbase + 64, tU = tbase + 128;
 
-  // ---- per-row scalars: beta, decay gate, inverse norms ----
-  if (tid < kChunk) {
-    const int r = tid;
-    const int64_t gr = R0 + r;
-    float b = 0.f, gate = 0.f;
-    if (r < len) {
-      b = p.beta ? p.beta[gr * p.H + h] : 1.f;
-      if (p.g && gr % M == 0) gate = p.g[(gr / M) * p.H + h];
+  // ---- [K; Q] K^T on the tensor cores (issued first, overlaps the scalar prologue) ----
+  if (tid == 0) {
+    const uint32_t id = idesc(kFmtBF16, 0, 0, 64, 128);
+    for (int kk = 0; kk < d / 16; ++kk) {
+      const uint32_t a = smem_u32(kq) + (kk >> 2) * 16384u + (kk & 3) * 32u;
+      mma_bf16_ss(tD1, desc_sw128(a, 16, 1024), desc_sw128(a, 16, 1024), id, kk > 0);
     }
-    sm.bt[r] = b;
-    sm.G2[r] = gate;  // raw gate; the scan below turns it into the cumsum
+    mma_commit(&mma_bar);
+  }
+
+  // ---- per-row scalars: beta, decay gate, inverse norms; base-2 cumsum ----
+  {
+    const int r = tid;  // rows 0..63 keys, 64..127 query rows
     float ss = 0.f;
-    for (int f = 0; f < K; ++f) ss += sm.ks[r * (K + 1) + f] * sm.ks[r * (K + 1) + f];
-    sm.rk[r] = p.l2norm ? rsqrtf(ss + kL2Eps) : 1.f;
-    float sq = 0.f;
-    if (r < QP)
-      for (int f = 0; f < K; ++f) sq += sm.qs[r * (K + 1) + f] * sm.qs[r * (K + 1) + f];
-    sm.rq[r] = p.l2norm ? rsqrtf(sq + kL2Eps) : 1.f;
-  }
-  __syncthreads();
-  if (tid == 0) {  // within-chunk cumsum, base 2
-    float acc = 0.f;
-    for (int r = 0; r < kChunk; ++r) {
-      acc += sm.G2[r];
-      sm.G2[r] = acc * kLog2e;
-    }
-  }
-  __syncthreads();
-  if (tid < kChunk) {
-    const int j = tid;
-    sm.wc[j] = sm.bt[j] * exp2f(sm.G2[j]) * sm.rk[j];
-    sm.uc[j] = sm.bt[j];
-  }
-
-  // ---- A = beta K K^T, strictly lower, decay weighted ----
-  for (int idx = tid; idx < kChunk * kChunk; idx += blockDim.x) {
-    int i = idx / kChunk, j = idx % kChunk;
-    float a = 0.f;
-    if (j < i && i < len) {
-      float d = 0.f;
-      for (int f = 0; f < K; ++f) d += sm.ks[i * (K + 1) + f] * sm.ks[j * (K + 1) + f];
-      a = sm.bt[i] * exp2f(sm.G2[i] - sm.G2[j]) * sm.rk[i] * sm.rk[j] * d;
-    }
-    sm.A[i * (kChunk + 1) + j] = a;
-  }
-  __syncthreads();
-
-  // ---- T = (I + A)^-1, unit lower triangular; one column per thread ----
-  if (tid < kChunk) {
-    const int cc = tid;
-    for (int i = 0; i < kChunk; ++i) {
-      float t;
-      if (i < cc) t = 0.f;
-      else if (i == cc) t = 1.f;
-      else {
-        float acc = 0.f;
-        for (int j = cc; j < i; ++j) acc += sm.A[i * (kChunk + 1) + j] * sm.Tm[j * (kChunk + 1) + cc];
-        t = -acc;
+    if (p.l2norm)
+      for (int f = 0; f < d; ++f) {
+        const float x = bf16_at(kq, 128, r, f);
+        ss += x * x;
       }
-      sm.Tm[i * (kChunk + 1) + cc] = t;
+    if (r < kChunk) {
+      const int64_t gr = R0 + r;
+      float b = 0.f, gate = 0.f;
+      if (r < len) {
+        b = p.beta ? p.beta[gr * p.H + h] : 1.f;
+        if (p.g && gr % M == 0) gate = p.g[(gr / M) * p.H + h];
+      }
+      bt[r] = b;
+      rk[r] = p.l2norm ? rsqrtf(ss + kL2Eps) : 1.f;
+      // inclusive scan of the gates over the 64 rows (two warps)
+      float x = gate;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (r == 31) warp_tot = x;
+      G2[r] = x;
+    } else {
+      rq[r - kChunk] = p.l2norm ? rsqrtf(ss + kL2Eps) : 1.f;
+    }
+  }
+  __syncthreads();
+  if (tid < kChunk) {
+    const float x = (tid >= 32 ? G2[tid] + warp_tot : G2[tid]) * kLog2e;
+    G2[tid] = x;
+  }
+  __syncthreads();
+  if (tid < kChunk) {
+    wc[tid] = bt[tid] * exp2f(G2[tid]) * rk[tid];
+    uc[tid] = bt[tid];
+  }
+
+  // ---- epilogue of [K;Q]K^T: A rows (lanes 0..63), score rows and query images (lanes 64..127) ----
+  const bool ok1 = mbar_wait(&mma_bar, 0);
+  if (!ok1) abort_flag = 1;
+  tc_fence_after();
+  __syncthreads();
+  const ImageLayout il(d, QP);
+  unsigned char *img = p.img + (size_t)((int64_t)row * p.H + h) * p.img_stride;
+  const float G2last = G2[len - 1];
+  {
+    float dv[64];
+    const uint32_t taddr = tD1 + ((uint32_t)(warp * 32) << 16);
+#pragma unroll
+    for (int c0 = 0; c0 < 64; c0 += 16) tmem_ld16(taddr + c0, dv + c0);
+    const int r = tid;
+    if (r < kChunk) {
+      const int i = r;
+      for (int j = 0; j < kChunk; ++j)
+        A[i * kLd + j] = (j < i && i < len) ? bt[i] * exp2f(G2[i] - G2[j]) * rk[i] * rk[j] * dv[j] : 0.f;
+    } else {
+      const int qi = r - kChunk;
+      if (qi < QP) {
+        const int pr = p0 + qi * M;
+        const bool live = qi < nq;
+        const float qscale = live ? p.scale * exp2f(G2[pr]) * rq[qi] : 0.f;
+        const float sc = live ? p.scale * rq[qi] : 0.f;
+        for (int s0 = 0; s0 < kChunk; s0 += 4) {
+          float4 o4;
+          float *o = &o4.x;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int s = s0 + u;
+            o[u] = (live && s <= pr) ? sc * exp2f(G2[pr] - G2[s]) * rk[s] * dv[s] : 0.f;
+          }
+          *reinterpret_cast<float4 *>(img + il.pm + (s0 >> 5) * (QP * 128u) + swz(qi, (s0 & 31) * 4u)) = o4;
+        }
+        for (int f0 = 0; f0 < d; f0 += 4) {
+          float4 o4;
+          float *o = &o4.x;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) o[u] = qscale * bf16_at(kq, 128, r, f0 + u);
+          *reinterpret_cast<float4 *>(img + il.qh + (f0 >> 5) * (QP * 128u) + swz(qi, (f0 & 31) * 4u)) = o4;
+        }
+      }
     }
   }
   __syncthreads();
 
-  const int64_t tile = (int64_t)row * p.H + h;
-  // ---- W (stored negated) and U ----
-  float *Wt = p.W + tile * (int64_t)kChunk * K;
-  for (int idx = tid; idx < kChunk * K; idx += blockDim.x) {
-    int s = idx / K, f = idx % K;
-    float acc = 0.f;
-    for (int j = 0; j <= s; ++j) acc += sm.Tm[s * (kChunk + 1) + j] * sm.wc[j] * sm.ks[j * (K + 1) + f];
-    Wt[idx] = -acc;
+  // ---- T = (I + A)^-1: diagonal 16x16 blocks by forward substitution (warp w: block w) ----
+  if (lane < 16) {
+    const int b0 = warp * 16, cc = lane;
+    float t[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float acc = 0.f;
+#pragma unroll
+      for (int j = 0; j < i; ++j) acc += A[(b0 + i) * kLd + b0 + j] * t[j];
+      t[i] = (i == cc) ? 1.f : (i < cc ? 0.f : -acc);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) Tm[(b0 + i) * kLd + b0 + cc] = t[i];
   }
-  float *Ut = p.U + tile * (int64_t)kChunk * V;
-  for (int idx = tid; idx < kChunk * V; idx += blockDim.x) {
-    int s = idx / V, f = idx % V;
-    float acc = 0.f;
-    for (int j = 0; j <= s; ++j) acc += sm.Tm[s * (kChunk + 1) + j] * sm.uc[j] * sm.vs[j * (V + 1) + f];
-    Ut[idx] = acc;
+  // zero the strictly upper blocks
+  for (int idx = tid; idx < kChunk * kChunk; idx += kWyThreads) {
+    const int i = idx / kChunk, j = idx % kChunk;
+    if ((j >> 4) > (i >> 4)) Tm[i * kLd + j] = 0.f;
   }
-  // ---- masked decayed scores of the readout rows ----
-  float *Pt = p.P + tile * (int64_t)QP * kChunk;
-  for (int idx = tid; idx < QP * kChunk; idx += blockDim.x) {
-    int qi = idx / kChunk, s = idx % kChunk;
-    float val = 0.f;
-    if (qi < nq) {
-      int pr = p0 + qi * M;
-      if (s <= pr) {
-        float d = 0.f;
-        for (int f = 0; f < K; ++f) d += sm.qs[qi * (K + 1) + f] * sm.ks[s * (K + 1) + f];
-        val = p.scale * exp2f(sm.G2[pr] - sm.G2[s]) * sm.rq[qi] * sm.rk[s] * d;
+  __syncthreads();
+  // off-diagonal blocks by distance: T_ij = -T_ii * sum_{x in [16j, 16i)} A[16i + r][x] T[x][16j + c]
+  for (int dist = 1; dist < 4; ++dist) {
+    const int nblk = 4 - dist;
+    for (int idx = tid; idx < nblk * 256; idx += kWyThreads) {
+      const int bi = idx / 256 + dist, bj = bi - dist, r = (idx / 16) & 15, cc = idx & 15;
+      float acc = 0.f;
+      for (int x = 16 * bj; x < 16 * bi; ++x) acc += A[(16 * bi + r) * kLd + x] * Tm[x * kLd + 16 * bj + cc];
+      Y[(idx / 256) * 256 + r * 16 + cc] = acc;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < nblk * 256; idx += kWyThreads) {
+      const int bi = idx / 256 + dist, bj = bi - dist, r = (idx / 16) & 15, cc = idx & 15;
+      float acc = 0.f;
+      for (int m = 0; m <= r; ++m) acc += Tm[(16 * bi + r) * kLd + 16 * bi + m] * Y[(idx / 256) * 256 + m * 16 + cc];
+      Tm[(16 * bi + r) * kLd + 16 * bj + cc] = -acc;
+    }
+    __syncthreads();
+  }
+
+  // ---- T diag(beta gamma rk) and T diag(beta) as hi + lo bf16, K-major swizzled [64 s][64 j] ----
+  for (int idx = tid; idx < kChunk * kChunk; idx += kWyThreads) {
+    const int s = idx / kChunk, j = idx % kChunk;
+    const float t = Tm[s * kLd + j];
+    const float w = t * wc[j], u = t * uc[j];
+    const __nv_bfloat16 wh = __float2bfloat16_rn(w), uh = __float2bfloat16_rn(u);
+    const __nv_bfloat16 wl = __float2bfloat16_rn(w - __bfloat162float(wh));
+    const __nv_bfloat16 ul = __float2bfloat16_rn(u - __bfloat162float(uh));
+    const uint32_t off = swz(s, j * 2u);
+    *reinterpret_cast<__nv_bfloat16 *>(sm + lay.twh + off) = wh;
+    *reinterpret_cast<__nv_bfloat16 *>(sm + lay.twl + off) = wl;
+    *reinterpret_cast<__nv_bfloat16 *>(sm + lay.tuh + off) = uh;
+    *reinterpret_cast<__nv_bfloat16 *>(sm + lay.tul + off) = ul;
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  // ---- W^T = K^T Tw^T and U^T = V^T Tu^T (A operands MN-major from the k / v tiles) ----
+  if (tid == 0) {
+    const uint32_t id = idesc(kFmtBF16, 1, 0, 64, d);
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint32_t ak = smem_u32(kq) + kk * 2048u, av = smem_u32(vt) + kk * 2048u;
+      const uint64_t dak = desc_sw128(ak, 16384, 1024), dav = desc_sw128(av, 8192, 1024);
+      mma_bf16_ss(tW, dak, desc_sw128(smem_u32(sm + lay.twh) + kk * 32u, 16, 1024), id, kk > 0);
+      mma_bf16_ss(tW, dak, desc_sw128(smem_u32(sm + lay.twl) + kk * 32u, 16, 1024), id, 1);
+      mma_bf16_ss(tU, dav, desc_sw128(smem_u32(sm + lay.tuh) + kk * 32u, 16, 1024), id, kk > 0);
+      mma_bf16_ss(tU, dav, desc_sw128(smem_u32(sm + lay.tul) + kk * 32u, 16, 1024), id, 1);
+    }
+    mma_commit(&mma_bar);
+  }
+  const bool ok2 = mbar_wait(&mma_bar, 1);
+  if (!ok2) abort_flag = 1;
+  tc_fence_after();
+  __syncthreads();
+
+  // ---- epilogue: -W image, U (row-major), Ktil^T image, metadata ----
+  {
+    // D row f sits in lane f (M = 128) or in lane 32*(f/16) + f%16 (M = 64).
+    const int f = (d == 128) ? tid : ((lane < 16) ? warp * 16 + lane : -1);
+    float wv[64], uv[64];
+    const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+#pragma unroll
+    for (int c0 = 0; c0 < 64; c0 += 16) {
+      tmem_ld16(tW + lrow + c0, wv + c0);
+      tmem_ld16(tU + lrow + c0, uv + c0);
+    }
+    if (f >= 0 && !abort_flag) {
+      float *Ut = p.U + ((int64_t)row * p.H + h) * (int64_t)kChunk * p.V;
+      for (int s = 0; s < kChunk; ++s) {
+        *reinterpret_cast<float *>(img + il.wn + (f >> 5) * (64u * 128u) + swz(s, (f & 31) * 4u)) = -wv[s];
+        Ut[(int64_t)s * p.V + f] = uv[s];
+      }
+      for (int s0 = 0; s0 < kChunk; s0 += 4) {
+        float4 o4;
+        float *o = &o4.x;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int s = s0 + u;
+          o[u] = (s < len) ? exp2f(G2last - G2[s]) * rk[s] * bf16_at(kq, 128, s, f) : 0.f;
+        }
+        *reinterpret_cast<float4 *>(img + il.kt + (s0 >> 5) * ((uint32_t)d * 128u) + swz(f, (s0 & 31) * 4u)) = o4;
       }
     }
-    Pt[idx] = val;
-  }
-  // ---- metadata for the scan ----
-  ChunkMeta *mt = p.meta + tile;
-  const float G2last = sm.G2[len - 1];
-  if (tid < kChunk) {
-    const int s = tid;
-    mt->kscale[s] = (s < len) ? exp2f(G2last - sm.G2[s]) * sm.rk[s] : 0.f;
-    float qsc = 0.f;
-    if (s < nq) qsc = p.scale * exp2f(sm.G2[p0 + s * M]) * sm.rq[s];
-    mt->qscale[s] = qsc;
   }
   if (tid == 0) {
+    ImageMeta *mt = reinterpret_cast<ImageMeta *>(img + il.meta);
     mt->gamma_last = exp2f(G2last);
     mt->nq = nq;
     mt->p0 = p0;
     mt->len = len;
+    if (abort_flag) set_status(p.status, GDP_DEV_ERR_TIMEOUT);
   }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_free(tbase, 256);
 }
 
 }  // namespace
 
 cudaError_t launch_wy(const Problem &p, cudaStream_t stream) {
   if (p.ntdp_pad == 0) return cudaSuccess;
-  size_t smem = WySmem::bytes(p.K, p.V, p.qpad);
+  const size_t smem = WyLayout(p.K).total + 1024;
   cudaError_t e = cudaFuncSetAttribute(gdp_wy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)p.ntdp_pad, (unsigned)p.H);

@@ -61,6 +61,8 @@ typedef enum gdp_status {
 #define GDP_DEV_ERR_CU_SEQLENS 0x1u /* cu_seqlens not non-decreasing from 0 to T: bad sequences skipped */
 #define GDP_DEV_ERR_SLOT 0x2u       /* state_indices entry outside [-1, num_slots): treated as padding */
 #define GDP_DEV_ERR_DESC 0x4u       /* chunk counts exceed the padded descriptor lengths: tail skipped */
+#define GDP_DEV_ERR_TIMEOUT 0x8u    /* a kernel gave up a bounded wait on its own tensor-core or copy
+                                       completion (about a second); its outputs are undefined */
 
 /*
  * Arguments of one prefill call.  Shapes use T real tokens, N sequences,
