@@ -22,21 +22,33 @@ __host__ __device__ inline int qpad_for(int M) {
 
 // Per-(expanded chunk, head) operand image written by the WY kernel and copied
 // as one block into shared memory by the scan kernel.  Every sub-tile is fp32,
-// K-major with the 128-byte swizzle (gdp_sm100.cuh), 1024-byte aligned:
-//   Wn  [64 rows s][d]   : -W                        (B of V_new  = U - W S^T)
-//   Kt  [d rows f][64 s] : 2^(G2_last-G2_s) khat_s^T (B of S     += V_new^T Ktil)
-//   Qh  [qpad rows][d]   : scale 2^(G2_p) qhat       (B of o      = S qhat...)
-//   Pm  [qpad rows][64 s]: masked decayed scores     (B of o     += P V_new)
-//   meta                 : gamma_last, nq, p0, len
+// K-major with the 128-byte swizzle (gdp_sm100.cuh), 1024-byte aligned.  The
+// B operands that share an A operand are stacked so that one MMA serves both:
+//   b1: d/32 K-blocks of [qpad + 64 rows][32]: rows 0..qpad-1  Qh = scale 2^(G2_p) qhat
+//                                              rows qpad..+63  -W            (A = S)
+//   b2: 2 K-blocks of [d + qpad rows][32]:      rows 0..d-1     Ktil^T = (2^(G2_last-G2_s) khat_s)^T
+//                                              rows d..+qpad-1 P = masked decayed scores (A = V_new^T)
+//   meta: gamma_last, nq, p0, len
 struct ImageLayout {
-  uint32_t wn, kt, qh, pm, meta, bytes;
+  uint32_t b1, b1_block, b2, b2_block, meta, bytes;
   __host__ __device__ ImageLayout(int d, int qpad) {
-    wn = 0;
-    kt = wn + 64u * d * 4u;
-    qh = kt + (uint32_t)d * 64u * 4u;
-    pm = qh + (uint32_t)qpad * d * 4u;
-    meta = pm + (uint32_t)qpad * 64u * 4u;
+    b1 = 0;
+    b1_block = (uint32_t)(qpad + 64) * 128u;
+    b2 = b1 + (uint32_t)(d / 32) * b1_block;
+    b2_block = (uint32_t)(d + qpad) * 128u;
+    meta = b2 + 2u * b2_block;
     bytes = meta + 64u;
+  }
+  // byte offsets of element (row, k) inside a region: K-block k/32, swizzled row
+  __host__ __device__ uint32_t qh(int qi, int f) const { return b1 + (f >> 5) * b1_block + swz_off(qi, f); }
+  __host__ __device__ uint32_t wn(int qpad, int s, int f) const {
+    return b1 + (f >> 5) * b1_block + swz_off(qpad + s, f);
+  }
+  __host__ __device__ uint32_t kt(int f, int s) const { return b2 + (s >> 5) * b2_block + swz_off(f, s); }
+  __host__ __device__ uint32_t pm(int d, int qi, int s) const { return b2 + (s >> 5) * b2_block + swz_off(d + qi, s); }
+  __host__ __device__ static uint32_t swz_off(int r, int k) {  // fp32 element k (mod 32) of row r
+    const uint32_t b = (uint32_t)(k & 31) * 4u;
+    return ((uint32_t)r >> 3) * 1024u + ((uint32_t)r & 7u) * 128u + ((((b >> 4) ^ (uint32_t)r) & 7u) << 4) + (b & 15u);
   }
 };
 struct ImageMeta {
@@ -70,7 +82,7 @@ struct Problem {
   // workspace tiles, indexed by (expanded chunk row r, head h): tile (r * H + h)
   unsigned char *img;  // operand images, img_stride bytes per tile (ImageLayout)
   size_t img_stride;
-  float *U;            // U = T diag(beta) V, [64][V] fp32 per tile, row-major
+  float *U;            // U^T = (T diag(beta) V)^T, [V][64] fp32 per tile, row-major
   uint32_t *status;
   int qpad;
 };

@@ -108,15 +108,38 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
                : "memory");
   return ok != 0;
 }
-// Bounded wait on phase `parity`: false after roughly a second without completion.
+__device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+               : "=r"(ok)
+               : "r"(smem_u32(bar)), "r"(parity)
+               : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait on phase `parity` (try_wait suspends the thread in hardware
+// between polls): false once about a second has passed without completion.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-  for (uint32_t it = 0; it < 64; ++it)
-    if (mbar_test(bar, parity)) return true;
-  for (uint32_t it = 0; it < (1u << 23); ++it) {
-    if (mbar_test(bar, parity)) return true;
-    __nanosleep(100);
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0; it < (1u << 24); ++it) {
+    if (mbar_try(bar, parity)) return true;
+    if ((it & 63u) == 63u && globaltimer_ns() - t0 > 1000000000ull) return false;
   }
   return false;
+}
+
+// 16-byte asynchronous copy global -> shared (zero-fills when src_bytes == 0).
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)), "l"(gsrc), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
 }
 
 // Bulk copy (TMA, non-tensor) global -> shared, completing on `bar` (16-byte aligned, size % 16 == 0).

@@ -67,6 +67,18 @@ __device__ __forceinline__ float bf16_at(const unsigned char *tile, int rows_per
   const uint32_t off = (uint32_t)(f >> 6) * rows_per_block * 128u + swz(r, (uint32_t)(f & 63) * 2u);
   return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + off));
 }
+// Eight consecutive elements f0 .. f0+7 (f0 % 8 == 0) of row r as floats, one 16-byte load.
+__device__ __forceinline__ void bf16x8_at(const unsigned char *tile, int rows_per_block, int r, int f0, float *o) {
+  const uint32_t off = (uint32_t)(f0 >> 6) * rows_per_block * 128u + swz(r, (uint32_t)(f0 & 63) * 2u);
+  const uint4 x = *reinterpret_cast<const uint4 *>(tile + off);
+  const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&x);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f2 = __bfloat1622float2(b[i]);
+    o[2 * i] = f2.x;
+    o[2 * i + 1] = f2.y;
+  }
+}
 
 __global__ void __launch_bounds__(kWyThreads) gdp_wy_kernel(Problem p) {
   const int row = blockIdx.x, h = blockIdx.y;
@@ -78,8 +90,11 @@ __global__ void __launch_bounds__(kWyThreads) gdp_wy_kernel(Problem p) {
   const int M = p.M, d = p.K, QP = p.qpad;
   const int64_t R0 = bos * M + (int64_t)c * kChunk;  // first global expanded row
   const int len = (int)min((int64_t)kChunk, L * M - (int64_t)c * kChunk);
-  const int p0 = (int)((M - 1 - (R0 % M)) % M);
+  const int r0m = (int)(R0 % M);                 // expanded-row phase of the chunk start
+  const int64_t tok0 = (R0 - r0m) / M;           // token of row 0
+  const int p0 = (M - 1 - r0m) % M;              // first readout row (t*M + M - 1)
   const int nq = (p0 < len) ? (len - 1 - p0) / M + 1 : 0;
+  const int64_t tq0 = (R0 + p0) / M;             // token of the first readout row; readout qi is tq0 + qi
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   extern __shared__ __align__(1024) unsigned char wy_smem_raw[];
@@ -103,28 +118,33 @@ __global__ void __launch_bounds__(kWyThreads) gdp_wy_kernel(Problem p) {
     abort_flag = 0;
   }
 
-  // ---- loads: 16-byte chunks into the swizzled bf16 tiles (zero past the chunk end) ----
+  // ---- loads: 16-byte asynchronous copies into the swizzled bf16 tiles (zero past the chunk end) ----
   const int cpr = d / 8;  // 16-byte chunks per row
   for (int idx = tid; idx < 128 * cpr; idx += kWyThreads) {
     const int r = idx / cpr, ch = idx % cpr;
-    uint4 x = make_uint4(0, 0, 0, 0);
+    const __nv_bfloat16 *src = p.k;
+    uint32_t bytes = 0;
     if (r < kChunk) {
-      if (r < len) x = *reinterpret_cast<const uint4 *>(p.k + (R0 + r) * p.k_st + (int64_t)h * p.k_sh + ch * 8);
+      if (r < len) {
+        src = p.k + (R0 + r) * p.k_st + (int64_t)h * p.k_sh + ch * 8;
+        bytes = 16;
+      }
     } else {
       const int qi = r - kChunk;
       if (qi < nq) {
-        const int64_t t = (R0 + p0 + (int64_t)qi * M) / M;
-        x = *reinterpret_cast<const uint4 *>(p.q + t * p.q_st + (int64_t)h * p.q_sh + ch * 8);
+        src = p.q + (tq0 + qi) * p.q_st + (int64_t)h * p.q_sh + ch * 8;
+        bytes = 16;
       }
     }
-    *reinterpret_cast<uint4 *>(kq + (ch >> 3) * 16384u + swz(r, (ch & 7) * 16u)) = x;
+    cp_async16(kq + (ch >> 3) * 16384u + swz(r, (ch & 7) * 16u), src, bytes);
   }
   for (int idx = tid; idx < kChunk * cpr; idx += kWyThreads) {
     const int r = idx / cpr, ch = idx % cpr;
-    uint4 x = make_uint4(0, 0, 0, 0);
-    if (r < len) x = *reinterpret_cast<const uint4 *>(p.v + (R0 + r) * p.v_st + (int64_t)h * p.v_sh + ch * 8);
-    *reinterpret_cast<uint4 *>(vt + (ch >> 3) * 8192u + swz(r, (ch & 7) * 16u)) = x;
+    const bool live = r < len;
+    const __nv_bfloat16 *src = live ? p.v + (R0 + r) * p.v_st + (int64_t)h * p.v_sh + ch * 8 : p.v;
+    cp_async16(vt + (ch >> 3) * 8192u + swz(r, (ch & 7) * 16u), src, live ? 16u : 0u);
   }
+  cp_async_wait_all();
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -147,16 +167,19 @@ __global__ void __launch_bounds__(kWyThreads) gdp_wy_kernel(Problem p) {
     const int r = tid;  // rows 0..63 keys, 64..127 query rows
     float ss = 0.f;
     if (p.l2norm)
-      for (int f = 0; f < d; ++f) {
-        const float x = bf16_at(kq, 128, r, f);
-        ss += x * x;
+      for (int f0 = 0; f0 < d; f0 += 8) {
+        float x[8];
+        bf16x8_at(kq, 128, r, f0, x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss += x[i] * x[i];
       }
     if (r < kChunk) {
       const int64_t gr = R0 + r;
+      const int pos = r0m + r;
       float b = 0.f, gate = 0.f;
       if (r < len) {
         b = p.beta ? p.beta[gr * p.H + h] : 1.f;
-        if (p.g && gr % M == 0) gate = p.g[(gr / M) * p.H + h];
+        if (p.g && pos % M == 0) gate = p.g[(tok0 + pos / M) * p.H + h];
       }
       bt[r] = b;
       rk[r] = p.l2norm ? rsqrtf(ss + kL2Eps) : 1.f;
@@ -217,14 +240,17 @@ __global__ void __launch_bounds__(kWyThreads) gdp_wy_kernel(Problem p) {
             const int s = s0 + u;
             o[u] = (live && s <= pr) ? sc * exp2f(G2[pr] - G2[s]) * rk[s] * dv[s] : 0.f;
           }
-          *reinterpret_cast<float4 *>(img + il.pm + (s0 >> 5) * (QP * 128u) + swz(qi, (s0 & 31) * 4u)) = o4;
+          *reinterpret_cast<float4 *>(img + il.pm(d, qi, s0)) = o4;
         }
-        for (int f0 = 0; f0 < d; f0 += 4) {
-          float4 o4;
-          float *o = &o4.x;
+        for (int f0 = 0; f0 < d; f0 += 8) {
+          float x[8];
+          bf16x8_at(kq, 128, r, f0, x);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) o[u] = qscale * bf16_at(kq, 128, r, f0 + u);
-          *reinterpret_cast<float4 *>(img + il.qh + (f0 >> 5) * (QP * 128u) + swz(qi, (f0 & 31) * 4u)) = o4;
+          for (int hh = 0; hh < 8; hh += 4) {
+            const int f = f0 + hh;
+            *reinterpret_cast<float4 *>(img + il.qh(qi, f)) =
+                make_float4(qscale * x[hh], qscale * x[hh + 1], qscale * x[hh + 2], qscale * x[hh + 3]);
+          }
         }
       }
     }
@@ -319,11 +345,11 @@ __global__ void __launch_bounds__(kWyThreads) gdp_wy_kernel(Problem p) {
       tmem_ld16(tU + lrow + c0, uv + c0);
     }
     if (f >= 0 && !abort_flag) {
-      float *Ut = p.U + ((int64_t)row * p.H + h) * (int64_t)kChunk * p.V;
-      for (int s = 0; s < kChunk; ++s) {
-        *reinterpret_cast<float *>(img + il.wn + (f >> 5) * (64u * 128u) + swz(s, (f & 31) * 4u)) = -wv[s];
-        Ut[(int64_t)s * p.V + f] = uv[s];
-      }
+      float *Ut = p.U + (((int64_t)row * p.H + h) * p.V + f) * kChunk;  // row f of U^T
+      for (int s = 0; s < kChunk; ++s) *reinterpret_cast<float *>(img + il.wn(QP, s, f)) = -wv[s];
+#pragma unroll
+      for (int s0 = 0; s0 < kChunk; s0 += 4)
+        *reinterpret_cast<float4 *>(Ut + s0) = make_float4(uv[s0], uv[s0 + 1], uv[s0 + 2], uv[s0 + 3]);
       for (int s0 = 0; s0 < kChunk; s0 += 4) {
         float4 o4;
         float *o = &o4.x;
@@ -332,7 +358,7 @@ __global__ void __launch_bounds__(kWyThreads) gdp_wy_kernel(Problem p) {
           const int s = s0 + u;
           o[u] = (s < len) ? exp2f(G2last - G2[s]) * rk[s] * bf16_at(kq, 128, s, f) : 0.f;
         }
-        *reinterpret_cast<float4 *>(img + il.kt + (s0 >> 5) * ((uint32_t)d * 128u) + swz(f, (s0 & 31) * 4u)) = o4;
+        *reinterpret_cast<float4 *>(img + il.kt(f, s0)) = o4;
       }
     }
   }
