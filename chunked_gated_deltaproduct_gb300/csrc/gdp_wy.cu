@@ -36,7 +36,10 @@ namespace {
 using namespace sm100;
 
 constexpr int kWyThreads = 128;
-constexpr int kLd = kChunk + 1;  // padded row length of the fp32 A / T scratch
+constexpr int kLd = kChunk + 1;   // row stride of the fp32 A scratch (conflict-free row reads)
+constexpr int kLdT = kChunk + 4;  // row stride of T (16-byte aligned rows for float4 access)
+constexpr int kLdY = 52;          // row stride of the [16][<=48] block-product scratch
+constexpr int kTile = 32 * 68;    // per-warp transpose tile (floats); reuses the A / T / Y region
 
 struct WyLayout {
   uint32_t kq, vt, twh, twl, tuh, tul, A, T, Y, scal, total;
@@ -56,12 +59,13 @@ struct WyLayout {
       tul = tuh + 8192u;
     }
     A = tul + 8192u;                       // fp32 [64][65]
-    T = A + 4u * kChunk * kLd;             // fp32 [64][65]
-    Y = T + 4u * kChunk * kLd;             // fp32 [3][16][16] block products
-    scal = Y + 4u * 3 * 256;               // G2, beta, rk, rq, wc, uc  [6][64]
-    total = scal + 4u * 6 * kChunk;
+    T = A + 4u * kChunk * kLd;             // fp32 [64][68]
+    Y = T + 4u * kChunk * kLdT;            // fp32 [16][52] block products
+    scal = Y + 4u * 16 * kLdY;             // G2, beta, rk, rq, wc, uc, kscale  [7][64]
+    total = scal + 4u * 7 * kChunk;
   }
 };
+static_assert(4 * 64 * (65 + 68) + 4 * 16 * 52 >= 4 * 4 * kTile, "transpose tiles must fit the A/T/Y region");
 
 __device__ __forceinline__ float bf16_at(const unsigned char *tile, int rows_per_block, int r, int f) {
   const uint32_t off = (uint32_t)(f >> 6) * rows_per_block * 128u + swz(r, (uint32_t)(f & 63) * 2u);
@@ -106,6 +110,7 @@ __global__ void __launch_bounds__(kWyThreads) gdp_wy_kernel(Problem p) {
   float *Y = reinterpret_cast<float *>(sm + lay.Y);
   float *G2 = reinterpret_cast<float *>(sm + lay.scal);
   float *bt = G2 + kChunk, *rk = bt + kChunk, *rq = rk + kChunk, *wc = rq + kChunk, *uc = wc + kChunk;
+  float *ks = uc + kChunk;  // 2^(G2_last - G2_s) rk_s (0 past the chunk end)
   __shared__ uint32_t tmem_slot;
   __shared__ __align__(8) uint64_t mma_bar;
   __shared__ float warp_tot;
@@ -205,6 +210,7 @@ __global__ void __launch_bounds__(kWyThreads) gdp_wy_kernel(Problem p) {
   if (tid < kChunk) {
     wc[tid] = bt[tid] * exp2f(G2[tid]) * rk[tid];
     uc[tid] = bt[tid];
+    ks[tid] = (tid < len) ? exp2f(G2[len - 1] - G2[tid]) * rk[tid] : 0.f;
   }
 
   // ---- epilogue of [K;Q]K^T: A rows (lanes 0..63), score rows and query images (lanes 64..127) ----
@@ -269,46 +275,68 @@ __global__ void __launch_bounds__(kWyThreads) gdp_wy_kernel(Problem p) {
       t[i] = (i == cc) ? 1.f : (i < cc ? 0.f : -acc);
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) Tm[(b0 + i) * kLd + b0 + cc] = t[i];
+    for (int i = 0; i < 16; ++i) Tm[(b0 + i) * kLdT + b0 + cc] = t[i];
   }
   // zero the strictly upper blocks
   for (int idx = tid; idx < kChunk * kChunk; idx += kWyThreads) {
     const int i = idx / kChunk, j = idx % kChunk;
-    if ((j >> 4) > (i >> 4)) Tm[i * kLd + j] = 0.f;
+    if ((j >> 4) > (i >> 4)) Tm[i * kLdT + j] = 0.f;
   }
   __syncthreads();
-  // off-diagonal blocks by distance: T_ij = -T_ii * sum_{x in [16j, 16i)} A[16i + r][x] T[x][16j + c]
-  for (int dist = 1; dist < 4; ++dist) {
-    const int nblk = 4 - dist;
-    for (int idx = tid; idx < nblk * 256; idx += kWyThreads) {
-      const int bi = idx / 256 + dist, bj = bi - dist, r = (idx / 16) & 15, cc = idx & 15;
-      float acc = 0.f;
-      for (int x = 16 * bj; x < 16 * bi; ++x) acc += A[(16 * bi + r) * kLd + x] * Tm[x * kLd + 16 * bj + cc];
-      Y[(idx / 256) * 256 + r * 16 + cc] = acc;
+  // block row bi from the rows above it: T_bi,<bi = -T_bi,bi (A_bi,<bi T_<bi,<bi).  The sums
+  // run over all x < 16 bi (T[x][c] = 0 for x < c); each thread owns 4 adjacent columns,
+  // so every shared load feeds 4 independent FMAs.
+  for (int bi = 1; bi < 4; ++bi) {
+    const int ncg = 4 * bi;  // 4-column groups in the 16 bi columns left of the diagonal block
+    for (int it = tid; it < 16 * ncg; it += kWyThreads) {
+      const int m = it / ncg, c = (it % ncg) * 4;
+      const float *arow = A + (16 * bi + m) * kLd;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+      for (int x = 0; x < 16 * bi; ++x) {
+        const float a = arow[x];
+        const float4 t = *reinterpret_cast<const float4 *>(Tm + x * kLdT + c);
+        acc.x += a * t.x; acc.y += a * t.y; acc.z += a * t.z; acc.w += a * t.w;
+      }
+      *reinterpret_cast<float4 *>(Y + m * kLdY + c) = acc;
     }
     __syncthreads();
-    for (int idx = tid; idx < nblk * 256; idx += kWyThreads) {
-      const int bi = idx / 256 + dist, bj = bi - dist, r = (idx / 16) & 15, cc = idx & 15;
-      float acc = 0.f;
-      for (int m = 0; m <= r; ++m) acc += Tm[(16 * bi + r) * kLd + 16 * bi + m] * Y[(idx / 256) * 256 + m * 16 + cc];
-      Tm[(16 * bi + r) * kLd + 16 * bj + cc] = -acc;
+    for (int it = tid; it < 16 * ncg; it += kWyThreads) {
+      const int r = it / ncg, c = (it % ncg) * 4;
+      const float *trow = Tm + (16 * bi + r) * kLdT + 16 * bi;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int m = 0; m <= r; ++m) {
+        const float t = trow[m];
+        const float4 y = *reinterpret_cast<const float4 *>(Y + m * kLdY + c);
+        acc.x += t * y.x; acc.y += t * y.y; acc.z += t * y.z; acc.w += t * y.w;
+      }
+      *reinterpret_cast<float4 *>(Tm + (16 * bi + r) * kLdT + c) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
     __syncthreads();
   }
 
   // ---- T diag(beta gamma rk) and T diag(beta) as hi + lo bf16, K-major swizzled [64 s][64 j] ----
-  for (int idx = tid; idx < kChunk * kChunk; idx += kWyThreads) {
-    const int s = idx / kChunk, j = idx % kChunk;
-    const float t = Tm[s * kLd + j];
-    const float w = t * wc[j], u = t * uc[j];
-    const __nv_bfloat16 wh = __float2bfloat16_rn(w), uh = __float2bfloat16_rn(u);
-    const __nv_bfloat16 wl = __float2bfloat16_rn(w - __bfloat162float(wh));
-    const __nv_bfloat16 ul = __float2bfloat16_rn(u - __bfloat162float(uh));
-    const uint32_t off = swz(s, j * 2u);
-    *reinterpret_cast<__nv_bfloat16 *>(sm + lay.twh + off) = wh;
-    *reinterpret_cast<__nv_bfloat16 *>(sm + lay.twl + off) = wl;
-    *reinterpret_cast<__nv_bfloat16 *>(sm + lay.tuh + off) = uh;
-    *reinterpret_cast<__nv_bfloat16 *>(sm + lay.tul + off) = ul;
+  for (int it = tid; it < kChunk * 8; it += kWyThreads) {  // (row s, 8 consecutive j)
+    const int srow = it >> 3, j0 = (it & 7) * 8;
+    const float4 t0 = *reinterpret_cast<const float4 *>(Tm + srow * kLdT + j0);
+    const float4 t1 = *reinterpret_cast<const float4 *>(Tm + srow * kLdT + j0 + 4);
+    const float t[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+    __nv_bfloat162 wh[4], wl[4], uh[4], ul[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float w0 = t[2 * i] * wc[j0 + 2 * i], w1 = t[2 * i + 1] * wc[j0 + 2 * i + 1];
+      const float u0 = t[2 * i] * uc[j0 + 2 * i], u1 = t[2 * i + 1] * uc[j0 + 2 * i + 1];
+      wh[i] = __floats2bfloat162_rn(w0, w1);
+      uh[i] = __floats2bfloat162_rn(u0, u1);
+      const float2 fw = __bfloat1622float2(wh[i]), fu = __bfloat1622float2(uh[i]);
+      wl[i] = __floats2bfloat162_rn(w0 - fw.x, w1 - fw.y);
+      ul[i] = __floats2bfloat162_rn(u0 - fu.x, u1 - fu.y);
+    }
+    const uint32_t off = swz(srow, j0 * 2u);
+    *reinterpret_cast<uint4 *>(sm + lay.twh + off) = *reinterpret_cast<const uint4 *>(wh);
+    *reinterpret_cast<uint4 *>(sm + lay.twl + off) = *reinterpret_cast<const uint4 *>(wl);
+    *reinterpret_cast<uint4 *>(sm + lay.tuh + off) = *reinterpret_cast<const uint4 *>(uh);
+    *reinterpret_cast<uint4 *>(sm + lay.tul + off) = *reinterpret_cast<const uint4 *>(ul);
   }
   fence_async_smem();
   tc_fence_before();
@@ -333,10 +361,14 @@ __global__ void __launch_bounds__(kWyThreads) gdp_wy_kernel(Problem p) {
   tc_fence_after();
   __syncthreads();
 
-  // ---- epilogue: -W image, U (row-major), Ktil^T image, metadata ----
+  // ---- epilogue: -W image, U^T, Ktil^T image.  Every store goes through a per-warp
+  // shared tile so that each 16-byte store instruction writes whole 128-byte lines. ----
   {
     // D row f sits in lane f (M = 128) or in lane 32*(f/16) + f%16 (M = 64).
-    const int f = (d == 128) ? tid : ((lane < 16) ? warp * 16 + lane : -1);
+    const int rpw = (d == 128) ? 32 : 16;  // feature rows held by this warp
+    const int fbase = warp * rpw;
+    const bool mine = lane < rpw;
+    float *tile = reinterpret_cast<float *>(sm + lay.A) + warp * kTile;
     float wv[64], uv[64];
     const uint32_t lrow = (uint32_t)(warp * 32) << 16;
 #pragma unroll
@@ -344,21 +376,48 @@ __global__ void __launch_bounds__(kWyThreads) gdp_wy_kernel(Problem p) {
       tmem_ld16(tW + lrow + c0, wv + c0);
       tmem_ld16(tU + lrow + c0, uv + c0);
     }
-    if (f >= 0 && !abort_flag) {
-      float *Ut = p.U + (((int64_t)row * p.H + h) * p.V + f) * kChunk;  // row f of U^T
-      for (int s = 0; s < kChunk; ++s) *reinterpret_cast<float *>(img + il.wn(QP, s, f)) = -wv[s];
+    if (!abort_flag) {
+      // U^T rows fbase .. fbase + rpw - 1 (contiguous in global, 256 B each)
+      if (mine) {
 #pragma unroll
-      for (int s0 = 0; s0 < kChunk; s0 += 4)
-        *reinterpret_cast<float4 *>(Ut + s0) = make_float4(uv[s0], uv[s0 + 1], uv[s0 + 2], uv[s0 + 3]);
-      for (int s0 = 0; s0 < kChunk; s0 += 4) {
-        float4 o4;
-        float *o = &o4.x;
+        for (int s0 = 0; s0 < kChunk; s0 += 4)
+          *reinterpret_cast<float4 *>(tile + lane * 68 + s0) = make_float4(uv[s0], uv[s0 + 1], uv[s0 + 2], uv[s0 + 3]);
+      }
+      __syncwarp();
+      float *Ut = p.U + (((int64_t)row * p.H + h) * p.V + fbase) * kChunk;
+      for (int c = lane; c < rpw * 16; c += 32)
+        *reinterpret_cast<float4 *>(Ut + (c >> 4) * kChunk + (c & 15) * 4) =
+            *reinterpret_cast<const float4 *>(tile + (c >> 4) * 68 + (c & 15) * 4);
+      __syncwarp();
+      // -W image: element (s, f) at row qpad + s of K-block f/32; two halves of 32 rows s
+      const int kb = fbase >> 5, ch0 = (fbase & 31) >> 2, nch = rpw >> 2;
+      for (int half = 0; half < 2; ++half) {
+        if (mine) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int s = s0 + u;
-          o[u] = (s < len) ? exp2f(G2last - G2[s]) * rk[s] * bf16_at(kq, 128, s, f) : 0.f;
+          for (int s2 = 0; s2 < 32; ++s2) tile[s2 * 36 + lane] = -wv[half * 32 + s2];
         }
-        *reinterpret_cast<float4 *>(img + il.kt(f, s0)) = o4;
+        __syncwarp();
+        for (int c = lane; c < 32 * nch; c += 32) {
+          const int srow = half * 32 + c / nch, ch = c % nch;
+          *reinterpret_cast<float4 *>(img + il.b1 + kb * il.b1_block + ImageLayout::swz_off(QP + srow, (ch0 + ch) * 4)) =
+              *reinterpret_cast<const float4 *>(tile + (c / nch) * 36 + ch * 4);
+        }
+        __syncwarp();
+      }
+      // Ktil^T image: row f = 2^(G2_last - G2_s) rk_s k[s][f] over s, K-blocks of 32 s
+      if (mine) {
+        const int f = fbase + lane;
+#pragma unroll 4
+        for (int s0 = 0; s0 < kChunk; s0 += 4)
+          *reinterpret_cast<float4 *>(tile + lane * 68 + s0) =
+              make_float4(ks[s0] * bf16_at(kq, 128, s0, f), ks[s0 + 1] * bf16_at(kq, 128, s0 + 1, f),
+                          ks[s0 + 2] * bf16_at(kq, 128, s0 + 2, f), ks[s0 + 3] * bf16_at(kq, 128, s0 + 3, f));
+      }
+      __syncwarp();
+      for (int c = lane; c < rpw * 16; c += 32) {
+        const int r = c >> 4, q = c & 15;  // q: 16-byte chunk of the 64 s values
+        *reinterpret_cast<float4 *>(img + il.b2 + (q >> 3) * il.b2_block + ImageLayout::swz_off(fbase + r, (q & 7) * 4)) =
+            *reinterpret_cast<const float4 *>(tile + r * 68 + q * 4);
       }
     }
   }
