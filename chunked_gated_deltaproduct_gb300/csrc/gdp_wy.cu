@@ -67,6 +67,38 @@ struct WyLayout {
 };
 static_assert(4 * 64 * (65 + 68) + 4 * 16 * 52 >= 4 * 4 * kTile, "transpose tiles must fit the A/T/Y region");
 
+// One block row of the blocked unit-lower-triangular inverse (see the kernel).
+template <int BI>
+__device__ __forceinline__ void inverse_block_row(const float *A, float *Tm, float *Y, int tid) {
+  constexpr int NCG = 4 * BI;  // 4-column groups left of the diagonal block
+  for (int it = tid; it < 16 * NCG; it += kWyThreads) {
+    const int m = it / NCG, c = (it % NCG) * 4;
+    const float *arow = A + (16 * BI + m) * kLd;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int x = 0; x < 16 * BI; ++x) {
+      const float a = arow[x];
+      const float4 t = *reinterpret_cast<const float4 *>(Tm + x * kLdT + c);
+      acc.x += a * t.x; acc.y += a * t.y; acc.z += a * t.z; acc.w += a * t.w;
+    }
+    *reinterpret_cast<float4 *>(Y + m * kLdY + c) = acc;
+  }
+  __syncthreads();
+  for (int it = tid; it < 16 * NCG; it += kWyThreads) {
+    const int r = it / NCG, c = (it % NCG) * 4;
+    const float *trow = Tm + (16 * BI + r) * kLdT + 16 * BI;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      const float t = (m <= r) ? trow[m] : 0.f;
+      const float4 y = *reinterpret_cast<const float4 *>(Y + m * kLdY + c);
+      acc.x += t * y.x; acc.y += t * y.y; acc.z += t * y.z; acc.w += t * y.w;
+    }
+    *reinterpret_cast<float4 *>(Tm + (16 * BI + r) * kLdT + c) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+  }
+  __syncthreads();
+}
+
 __device__ __forceinline__ float bf16_at(const unsigned char *tile, int rows_per_block, int r, int f) {
   const uint32_t off = (uint32_t)(f >> 6) * rows_per_block * 128u + swz(r, (uint32_t)(f & 63) * 2u);
   return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + off));
@@ -285,35 +317,10 @@ __global__ void __launch_bounds__(kWyThreads) gdp_wy_kernel(Problem p) {
   __syncthreads();
   // block row bi from the rows above it: T_bi,<bi = -T_bi,bi (A_bi,<bi T_<bi,<bi).  The sums
   // run over all x < 16 bi (T[x][c] = 0 for x < c); each thread owns 4 adjacent columns,
-  // so every shared load feeds 4 independent FMAs.
-  for (int bi = 1; bi < 4; ++bi) {
-    const int ncg = 4 * bi;  // 4-column groups in the 16 bi columns left of the diagonal block
-    for (int it = tid; it < 16 * ncg; it += kWyThreads) {
-      const int m = it / ncg, c = (it % ncg) * 4;
-      const float *arow = A + (16 * bi + m) * kLd;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-      for (int x = 0; x < 16 * bi; ++x) {
-        const float a = arow[x];
-        const float4 t = *reinterpret_cast<const float4 *>(Tm + x * kLdT + c);
-        acc.x += a * t.x; acc.y += a * t.y; acc.z += a * t.z; acc.w += a * t.w;
-      }
-      *reinterpret_cast<float4 *>(Y + m * kLdY + c) = acc;
-    }
-    __syncthreads();
-    for (int it = tid; it < 16 * ncg; it += kWyThreads) {
-      const int r = it / ncg, c = (it % ncg) * 4;
-      const float *trow = Tm + (16 * bi + r) * kLdT + 16 * bi;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int m = 0; m <= r; ++m) {
-        const float t = trow[m];
-        const float4 y = *reinterpret_cast<const float4 *>(Y + m * kLdY + c);
-        acc.x += t * y.x; acc.y += t * y.y; acc.z += t * y.z; acc.w += t * y.w;
-      }
-      *reinterpret_cast<float4 *>(Tm + (16 * bi + r) * kLdT + c) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-    }
-    __syncthreads();
-  }
+  // so every shared load feeds 4 independent FMAs; trip counts are compile-time.
+  inverse_block_row<1>(A, Tm, Y, tid);
+  inverse_block_row<2>(A, Tm, Y, tid);
+  inverse_block_row<3>(A, Tm, Y, tid);
 
   // ---- T diag(beta gamma rk) and T diag(beta) as hi + lo bf16, K-major swizzled [64 s][64 j] ----
   for (int it = tid; it < kChunk * 8; it += kWyThreads) {  // (row s, 8 consecutive j)
