@@ -98,6 +98,9 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
     return fail(GDP_ERR_INVALID_ARG, "strides describe overlapping rows");
   const uintptr_t align16 = ((uintptr_t)a->q | (uintptr_t)a->k | (uintptr_t)a->v | (uintptr_t)a->output) & 15u;
   if (align16) return fail(GDP_ERR_INVALID_ARG, "q, k, v and output must be 16-byte aligned");
+  const uintptr_t salign = ((uintptr_t)a->initial_state | (uintptr_t)a->state | (uintptr_t)a->output_state |
+                            (uintptr_t)a->chunk_states) & 15u;
+  if (salign) return fail(GDP_ERR_INVALID_ARG, "state buffers must be 16-byte aligned");
   if (a->state && a->initial_state)
     return fail(GDP_ERR_INVALID_ARG, "state (cache mode) and initial_state are mutually exclusive");
   if (a->state && (!a->state_indices || a->num_slots < 1))

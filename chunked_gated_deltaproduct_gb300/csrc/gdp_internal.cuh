@@ -20,24 +20,38 @@ __host__ __device__ inline int qpad_for(int M) {
   return (q + 15) / 16 * 16;
 }
 
+// Per-chunk decay rescaling of the scan.  The scan keeps S_hat = S / Gamma in
+// tensor memory, where Gamma is a running product of chunk decays, so that the
+// per-chunk factor gamma_last never has to be applied to the state on the
+// serial chain.  A chunk whose decay is at least 2^kFastMinLog2Gamma has its -W
+// and Qh operands written pre-divided by gamma_last ("fast" image); a chunk with
+// a smaller decay (including 0) keeps them unscaled and the scan applies its
+// decay to S explicitly.  The scan renormalises S_hat (Gamma -> 1) before Gamma
+// would drop below kRenormMinGamma.
+constexpr float kFastMinLog2Gamma = -20.f;
+constexpr float kRenormMinGamma = 0x1p-40f;
+
 // Per-(expanded chunk, head) operand image written by the WY kernel and copied
-// as one block into shared memory by the scan kernel.  Every sub-tile is fp32,
-// K-major with the 128-byte swizzle (gdp_sm100.cuh), 1024-byte aligned.  The
-// B operands that share an A operand are stacked so that one MMA serves both:
-//   b1: d/32 K-blocks of [qpad + 64 rows][32]: rows 0..qpad-1  Qh = scale 2^(G2_p) qhat
-//                                              rows qpad..+63  -W            (A = S)
+// into shared memory by the scan kernel in two bulk copies (part 1: b1 + meta,
+// part 2: b2).  Every sub-tile is fp32, K-major with the 128-byte swizzle
+// (gdp_sm100.cuh), 1024-byte aligned.  The B operands that share an A operand
+// are stacked so that one MMA serves both (c = 2^-G2_last for a fast image, else 1):
+//   b1: d/32 K-blocks of [qpad + 64 rows][32]: rows 0..qpad-1  c Qh, Qh = scale 2^(G2_p) qhat
+//                                              rows qpad..+63  -c W          (A = S)
+//   meta: gamma_last, nq, p0, len, fast
 //   b2: 2 K-blocks of [d + qpad rows][32]:      rows 0..d-1     Ktil^T = (2^(G2_last-G2_s) khat_s)^T
 //                                              rows d..+qpad-1 P = masked decayed scores (A = V_new^T)
-//   meta: gamma_last, nq, p0, len
 struct ImageLayout {
-  uint32_t b1, b1_block, b2, b2_block, meta, bytes;
+  uint32_t b1, b1_block, meta, part1, b2, b2_block, part2, bytes;
   __host__ __device__ ImageLayout(int d, int qpad) {
     b1 = 0;
     b1_block = (uint32_t)(qpad + 64) * 128u;
-    b2 = b1 + (uint32_t)(d / 32) * b1_block;
+    meta = b1 + (uint32_t)(d / 32) * b1_block;
+    part1 = meta + 64u;
+    b2 = meta + 1024u;
     b2_block = (uint32_t)(d + qpad) * 128u;
-    meta = b2 + 2u * b2_block;
-    bytes = meta + 64u;
+    part2 = 2u * b2_block;
+    bytes = b2 + part2;
   }
   // byte offsets of element (row, k) inside a region: K-block k/32, swizzled row
   __host__ __device__ uint32_t qh(int qi, int f) const { return b1 + (f >> 5) * b1_block + swz_off(qi, f); }
@@ -56,6 +70,7 @@ struct ImageMeta {
   int nq;            // readout rows in the chunk
   int p0;            // local row of the first readout row
   int len;           // rows in the chunk (<= 64)
+  int fast;          // -W and Qh are divided by gamma_last
 };
 
 // Everything a kernel needs about one call (passed by value).
@@ -82,7 +97,10 @@ struct Problem {
   // workspace tiles, indexed by (expanded chunk row r, head h): tile (r * H + h)
   unsigned char *img;  // operand images, img_stride bytes per tile (ImageLayout)
   size_t img_stride;
-  float *U;            // U^T = (T diag(beta) V)^T, [V][64] fp32 per tile, row-major
+  // U^T = (T diag(beta) V)^T, V x 64 fp32 per tile, in 32-row groups: element (v, s) at
+  // ((v / 32) * 16 + s / 4) * 128 + (v % 32) * 4 + s % 4, so that 32 threads reading rows
+  // 32g .. 32g + 31 four columns at a time read 512 contiguous bytes
+  float *U;
   uint32_t *status;
   int qpad;
 };

@@ -11,14 +11,27 @@
 // Every M-th expanded chunk starts a token chunk (64 c tokens = 64 c M rows):
 // its entering state is chunk-state row chunk_offsets[i] + e / M.
 //
-// One CTA per (sequence, head); TMEM lane v = state row v.  S lives in TMEM
-// columns [0, d) for the whole sequence and is read by the MMAs directly as
-// the tf32 A operand, so the recurrence never leaves the SM.  All
-// products are kind::tf32 (fp32 operands truncated to tf32, fp32 accumulate):
-// the state feeds back into every later chunk, and bf16 operands would add a
-// ~2^-9 relative error per chunk.  The B operands come from one operand image
-// per chunk (written by the WY kernel), fetched by a single bulk copy into a
-// double-buffered shared-memory stage while the previous chunk computes.
+// One CTA per (sequence, head); TMEM lane v = state row v.  The state lives in
+// TMEM columns [0, d) for the whole sequence as S_hat = S / Gamma (Gamma: a
+// running product of chunk decays), read by the MMAs directly as the tf32 A
+// operand and updated in place by them, so the recurrence never leaves the
+// SM and no thread touches it on the serial chain.  With the operands of a
+// "fast" image pre-divided by gamma_last (gdp_internal.cuh) and Gamma' = Gamma
+// gamma_last, the chunk's update is the same algebra in scaled form:
+//   Y       = U^T / Gamma' + S_hat (-W / gamma_last)^T    ( = V_new^T / Gamma')
+//   o_hat   = S_hat (Qh / gamma_last)^T + Y P^T           ( = o^T / Gamma')
+//   S_hat  += Y Ktil                                      ( = S_{e+1} / Gamma')
+// Y starts as U^T / Gamma' (written into TMEM by threads ahead of time), so a
+// chunk is two MMA batches back to back on the tensor pipe.  A "slow" image
+// (gamma_last < 2^kFastMinLog2Gamma, e.g. 0) is unscaled: the state is
+// renormalised to Gamma = 1 before it and scaled by gamma_last between its
+// two batches.  Gamma is renormalised to 1 whenever it would fall below
+// kRenormMinGamma.  All products are kind::tf32 (fp32 operands truncated to
+// tf32, fp32 accumulate): the state feeds back into every later chunk, and
+// bf16 operands would add a ~2^-9 relative error per chunk.  The B operands
+// come from one operand image per chunk (written by the WY kernel), fetched by
+// two bulk copies into a double-buffered shared-memory stage while the
+// previous chunk computes.
 #include "gdp_internal.cuh"
 #include "gdp_sm100.cuh"
 
@@ -27,14 +40,14 @@ namespace {
 
 using namespace sm100;
 
-// Warp roles (warp specialisation keeps loads and stores off the serial chain):
+// Warp roles:
 //   warp 8     control : image copies (bulk TMA) and MMA issue
-//   warps 0-3  state   : S <- gamma_last S (+ unscaled copy at token-chunk starts),
-//                        V_new += U^T, then the chunk's o columns -> a 2-slot TMEM ring
-//   warps 4-7  store   : ring -> bf16 outputs, state copy -> chunk_states, final state
-// Per chunk the chain is: batch 1 -> state pass -> batch 2 -> ring copy -> next batch 1.
-// An SM stores only ~30 B/cycle, so outputs and 64 KB state snapshots drain behind it.
-// TMEM lanes: state and store warps w access lanes 32 (w % 4) .. +31.
+//   warps 0-3  prep    : per chunk, Y <- U^T / Gamma' and o_hat <- 0 in the chunk's TMEM
+//                        buffer (two buffers), renormalisation, the state snapshot at
+//                        token-chunk starts (-> TMEM copy) and the slow-image decay
+//   warps 4-7  store   : o_hat * Gamma' -> bf16 outputs, snapshot -> chunk_states,
+//                        final state
+// TMEM lanes: prep and store warps w access lanes 32 (w % 4) .. +31.
 constexpr int kScanThreads = 288;
 constexpr uint32_t kScanSmemBudget = 200u * 1024u;  // operand stages
 constexpr uint32_t kXpose = 32u * 36u * 4u;         // per store warp: 32 x 36 fp32 transpose tile
@@ -51,18 +64,20 @@ __host__ inline size_t scan_smem_bytes(int d, int qpad, int V) {
 }
 
 // Store warp: rows [row0, row0 + 32) of a [V][d] fp32 block from this warp's TMEM
-// lanes (columns from t_lane).  Each 32 x 32 block goes through a shared tile
-// (rows padded to 36 floats: 16-byte aligned, conflict-free) so that every global
+// lanes (columns from t_lane), times mul.  Each 32 x 32 block goes through a shared
+// tile (rows padded to 36 floats: 16-byte aligned, conflict-free) so that every global
 // store instruction writes four full 128-byte row segments with 16-byte stores.
 __device__ __forceinline__ void store_state_rows(uint32_t t_lane, float *xb, int lane, int row0, int V, int d,
-                                                 float *dst) {
+                                                 float mul, float *dst) {
   const int rq = lane >> 3, cq = (lane & 7) * 4;  // this lane's row (of 4) and column in a store
+#pragma unroll 1
   for (int c0 = 0; c0 < d; c0 += 32) {
     float x[32];
     tmem_ld32(t_lane + c0, x);
 #pragma unroll
     for (int j = 0; j < 32; j += 4)
-      *reinterpret_cast<float4 *>(xb + lane * 36 + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+      *reinterpret_cast<float4 *>(xb + lane * 36 + j) =
+          make_float4(mul * x[j], mul * x[j + 1], mul * x[j + 2], mul * x[j + 3]);
     __syncwarp();
 #pragma unroll
     for (int r0 = 0; r0 < 32; r0 += 4) {
@@ -75,6 +90,12 @@ __device__ __forceinline__ void store_state_rows(uint32_t t_lane, float *xb, int
   }
 }
 
+// Per-chunk facts the prep warps hand to the store warps (one slot per TMEM buffer).
+struct ChunkInfo {
+  float out_scale;  // Gamma' of the chunk: o = Gamma' o_hat
+  int nq, p0;
+};
+
 __global__ void __launch_bounds__(kScanThreads, 1) gdp_scan_kernel(Problem p) {
   const int seq = blockIdx.x, h = blockIdx.y;
   int64_t bos, L;
@@ -82,7 +103,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdp_scan_kernel(Problem p) {
   const int d = p.K, V = p.V, M = p.M, QP = p.qpad, H = p.H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q4 = warp & 3;
-  const int v = q4 * 32 + lane;  // state row (TMEM lane) of state and store threads
+  const int v = q4 * 32 + lane;  // state row (TMEM lane) of prep and store threads
   const uint32_t lrow = (uint32_t)(q4 * 32) << 16;
   const ImageLayout il(d, QP);
   const uint32_t sbytes = stage_bytes(d, QP);
@@ -92,10 +113,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdp_scan_kernel(Problem p) {
   unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)scan_smem_raw + 1023) & ~(uintptr_t)1023);
   unsigned char *obuf = sm + nst * sbytes;  // [qpad][V] bf16 output staging
   float *xb = reinterpret_cast<float *>(obuf + obuf_bytes(QP, V)) + q4 * 32 * 36;
-  __shared__ __align__(8) uint64_t full_bar[2], b1_done, b2_done, spass_done, o_free, ring_full[2], ring_free[2],
+  __shared__ __align__(8) uint64_t full1[2], full2[2], yo_ready[2], yo_free[2], b2_done[2], b1_done, mid_done,
       bk_free, fin_bar;
   __shared__ uint32_t tmem_slot;
-  __shared__ int ring_nq[2], ring_p0[2];
+  __shared__ ChunkInfo info[2];
+  __shared__ int st_ok[4];
   __shared__ volatile int abort_flag;
 
   // incoming state source
@@ -117,20 +139,20 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdp_scan_kernel(Problem p) {
   const int64_t co_i = p.chunk_states ? (int64_t)p.co[seq] : 0;
   // chunks whose workspace tile exists (a flagged descriptor overflow truncates the sequence)
   const int64_t nrun = (cod_i < 0) ? 0 : max((int64_t)0, min(nchunks, p.ws_rows - cod_i));
+  // token-chunk starts whose state is requested (a prefix of the chunks e % M == 0)
   auto emits = [&](int64_t e) { return p.chunk_states && (e % M == 0) && co_i >= 0 && co_i + e / M < p.nt_pad; };
 
   if (warp == 8) tmem_alloc(&tmem_slot, 512);
   if (tid == 0) {
-    mbar_init(&full_bar[0], 1);
-    mbar_init(&full_bar[1], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&full1[i], 1);
+      mbar_init(&full2[i], 1);
+      mbar_init(&yo_ready[i], 128);
+      mbar_init(&yo_free[i], 128);
+      mbar_init(&b2_done[i], 1);
+    }
     mbar_init(&b1_done, 1);
-    mbar_init(&b2_done, 1);
-    mbar_init(&spass_done, 128);
-    mbar_init(&o_free, 128);
-    mbar_init(&ring_full[0], 128);
-    mbar_init(&ring_full[1], 128);
-    mbar_init(&ring_free[0], 128);
-    mbar_init(&ring_free[1], 128);
+    mbar_init(&mid_done, 128);
     mbar_init(&bk_free, 128);
     mbar_init(&fin_bar, 1);
     mbar_init_fence();
@@ -139,14 +161,25 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdp_scan_kernel(Problem p) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // TMEM columns: [S: d][o^T: qpad][V_new^T: 64] | 256: o ring 2 x 64 | 384: state copy 128.
-  // [o | V_new] and [S | o] are each contiguous, so one MMA per K step serves both
-  // products that share an A operand.
+  // TMEM columns: [0, d) S_hat | buffer b at 128 + b (qpad + 64): [o_hat: qpad][Y: 64] |
+  // [384, 384 + d) state snapshot.  [o_hat | Y] is contiguous so that one MMA per K step
+  // serves both products of batch 1.
   const uint32_t tb = tmem_slot;
-  const uint32_t tS = tb, tO = tb + d, tVn = tb + d + QP, tRing = tb + 256, tBk = tb + 384;
-  const uint32_t id1 = idesc(kFmtTF32, 0, 0, QP + 64, 128);  // [o | V_new] = S [Qh ; -W]^T
-  const uint32_t id2s = idesc(kFmtTF32, 0, 0, d, 128);       // S += V_new^T Ktil
-  const uint32_t id2o = idesc(kFmtTF32, 0, 0, QP, 128);      // o += V_new^T P^T
+  const uint32_t tS = tb, tBk = tb + 384;
+  auto tO = [&](int b) { return tb + 128u + (uint32_t)b * (uint32_t)(QP + 64); };
+  const uint32_t id1 = idesc(kFmtTF32, 0, 0, QP + 64, 128);  // [o_hat | Y] += S_hat [Qh ; -W]^T
+  const uint32_t id2s = idesc(kFmtTF32, 0, 0, d, 128);       // S_hat += Y Ktil
+  const uint32_t id2o = idesc(kFmtTF32, 0, 0, QP, 128);      // o_hat += Y P^T
+
+  auto load_image = [&](int64_t e) {  // control thread: image of chunk e into stage e % nst
+    const int st = (int)(e % nst);
+    unsigned char *stage = sm + st * sbytes;
+    const unsigned char *g = p.img + (size_t)((cod_i + e) * H + h) * p.img_stride;
+    mbar_arrive_expect_tx(&full1[st], il.part1);
+    bulk_g2s(stage, g, il.part1, &full1[st]);
+    mbar_arrive_expect_tx(&full2[st], il.part2);
+    bulk_g2s(stage + il.b2, g + il.b2, il.part2, &full2[st]);
+  };
 
   if (warp < 4) {
     // S_0 into TMEM (rows >= V stay zero)
@@ -162,155 +195,194 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdp_scan_kernel(Problem p) {
     }
     tmem_st_wait();
   }
-  if (warp == 8 && lane == 0) {
-    for (int s = 0; s < nst && s < nrun; ++s) {
-      mbar_arrive_expect_tx(&full_bar[s], il.bytes);
-      bulk_g2s(sm + s * sbytes, p.img + (size_t)((cod_i + s) * H + h) * p.img_stride, il.bytes, &full_bar[s]);
-    }
-  }
+  if (warp == 8 && lane == 0)
+    for (int64_t e = 0; e < nst && e < nrun; ++e) load_image(e);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
 
   if (warp < 4) {
-    // ---------------- state warps ----------------
+    // ---------------- prep warps ----------------
     float u[64];
-    auto load_u = [&](int64_t e) {
-      const float4 *Ut = reinterpret_cast<const float4 *>(p.U + (((cod_i + e) * H + h) * V + (v < V ? v : 0)) * kChunk);
+    auto load_u = [&](int64_t e) {  // row v of U^T: one 512-byte segment per load instruction of the warp
+      const float4 *Ut = reinterpret_cast<const float4 *>(p.U + ((cod_i + e) * H + h) * (int64_t)V * kChunk) +
+                         (v < V ? q4 * 512 + lane : 0);
 #pragma unroll
       for (int s4 = 0; s4 < 16; ++s4) {
-        const float4 x = (v < V) ? Ut[s4] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 x = (v < V) ? Ut[s4 * 32] : make_float4(0.f, 0.f, 0.f, 0.f);
         u[4 * s4] = x.x; u[4 * s4 + 1] = x.y; u[4 * s4 + 2] = x.z; u[4 * s4 + 3] = x.w;
       }
     };
+    float gam = 1.f;  // Gamma of the state in TMEM
+    int n_emit = 0;
     if (nrun > 0) load_u(0);
     for (int64_t e = 0; e < nrun; ++e) {
-      if (!mbar_wait_or_abort(&b1_done, (uint32_t)(e & 1), &abort_flag)) break;
+      const int st = (int)(e % nst), b = (int)(e & 1);
+      if (!mbar_wait_or_abort(&full1[st], (uint32_t)((e / nst) & 1), &abort_flag)) break;
+      const ImageMeta mt = *reinterpret_cast<const ImageMeta *>(sm + st * sbytes + il.meta);
+      const bool fast = mt.fast != 0, emit = emits(e);
+      const bool renorm = fast ? (gam * mt.gamma_last < kRenormMinGamma) : (gam != 1.f);
+      const float gam_pass = renorm ? 1.f : gam;                  // Gamma during the chunk's products
+      const float gam_next = fast ? gam_pass * mt.gamma_last : 1.f;  // Gamma' after it
+      if (e >= 2 && !mbar_wait_or_abort(&yo_free[b], (uint32_t)(((e >> 1) - 1) & 1), &abort_flag)) break;
       tc_fence_after();
-      const ImageMeta mt = *reinterpret_cast<const ImageMeta *>(sm + (e % nst) * sbytes + il.meta);
-      const bool emit = emits(e);
-      if (emit && e / M >= 1) {  // the store warps have drained the previous state copy
-        if (!mbar_wait_or_abort(&bk_free, (uint32_t)((e / M - 1) & 1), &abort_flag)) break;
+      const uint32_t to = tO(b), ty = to + (uint32_t)QP;
+      const float inv = 1.f / gam_next;
+#pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 16) {
+        float x[16];
+#pragma unroll
+        for (int w = 0; w < 16; ++w) x[w] = u[c0 + w] * inv;
+        tmem_st16(ty + lrow + c0, x);
+      }
+      {
+        float z[16];
+#pragma unroll
+        for (int w = 0; w < 16; ++w) z[w] = 0.f;
+        for (int c0 = 0; c0 < QP; c0 += 16) tmem_st16(to + lrow + c0, z);
+      }
+      if (tid == 0) info[b] = ChunkInfo{gam_next, mt.nq, mt.p0};
+      if ((renorm || emit || !fast) && e >= 1) {  // S_hat of chunk e is final
+        if (!mbar_wait_or_abort(&b2_done[(e - 1) & 1], (uint32_t)(((e - 1) >> 1) & 1), &abort_flag)) break;
         tc_fence_after();
       }
-      for (int c0 = 0; c0 < d; c0 += 32) {
-        float x[32];
-        tmem_ld32(tS + lrow + c0, x);
-        if (emit) {
-          tmem_st16(tBk + lrow + c0, x);
-          tmem_st16(tBk + lrow + c0 + 16, x + 16);
+      if (renorm) {
+        for (int c0 = 0; c0 < d; c0 += 32) {
+          float x[32];
+          tmem_ld32(tS + lrow + c0, x);
+#pragma unroll
+          for (int w = 0; w < 32; ++w) x[w] *= gam;
+          tmem_st16(tS + lrow + c0, x);
+          tmem_st16(tS + lrow + c0 + 16, x + 16);
         }
-#pragma unroll
-        for (int w = 0; w < 32; ++w) x[w] *= mt.gamma_last;
-        tmem_st16(tS + lrow + c0, x);
-        tmem_st16(tS + lrow + c0 + 16, x + 16);
-      }
-#pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        float x[32];
-        tmem_ld32(tVn + lrow + c0, x);
-#pragma unroll
-        for (int w = 0; w < 32; ++w) x[w] += u[c0 + w];
-        tmem_st16(tVn + lrow + c0, x);
-        tmem_st16(tVn + lrow + c0 + 16, x + 16);
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&spass_done);
-      if (e + 1 < nrun) load_u(e + 1);  // next chunk's U^T, in flight while batch 2 runs
-
-      if (!mbar_wait_or_abort(&b2_done, (uint32_t)(e & 1), &abort_flag)) break;
-      tc_fence_after();
-      if (e >= 2 && !mbar_wait_or_abort(&ring_free[e & 1], (uint32_t)(((e >> 1) - 1) & 1), &abort_flag)) break;
-      tc_fence_after();
-      const uint32_t slot_col = tRing + (uint32_t)(e & 1) * 64u;
-      for (int c0 = 0; c0 < QP; c0 += 16) {
-        float x[16];
-        tmem_ld16(tO + lrow + c0, x);
-        tmem_st16(slot_col + lrow + c0, x);
+      mbar_arrive(&yo_ready[b]);
+      if (e + 1 < nrun) load_u(e + 1);  // next chunk's U^T, in flight while this chunk runs
+      if (emit || !fast) {
+        // between the two batches: snapshot S_e = gam_pass S_hat (read alongside batch 1) and,
+        // for a slow image, S_hat <- gamma_last S_hat once batch 1 has read it
+        if (emit && n_emit >= 1 && !mbar_wait_or_abort(&bk_free, (uint32_t)((n_emit - 1) & 1), &abort_flag)) break;
+        if (!fast && !mbar_wait_or_abort(&b1_done, (uint32_t)(e & 1), &abort_flag)) break;
+        tc_fence_after();
+        for (int c0 = 0; c0 < d; c0 += 32) {
+          float x[32];
+          tmem_ld32(tS + lrow + c0, x);
+          if (emit) {
+            float y[32];
+#pragma unroll
+            for (int w = 0; w < 32; ++w) y[w] = x[w] * gam_pass;
+            tmem_st16(tBk + lrow + c0, y);
+            tmem_st16(tBk + lrow + c0 + 16, y + 16);
+          }
+          if (!fast) {
+#pragma unroll
+            for (int w = 0; w < 32; ++w) x[w] *= mt.gamma_last;
+            tmem_st16(tS + lrow + c0, x);
+            tmem_st16(tS + lrow + c0 + 16, x + 16);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&mid_done);
+        if (emit) ++n_emit;
       }
-      if (tid == 0) {
-        ring_nq[e & 1] = mt.nq;
-        ring_p0[e & 1] = mt.p0;
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&o_free);
-      mbar_arrive(&ring_full[e & 1]);
+      gam = gam_next;
     }
   } else if (warp < 8) {
     // ---------------- store warps ----------------
+    float gam_fin = 1.f;
     for (int64_t e = 0; e < nrun; ++e) {
-      if (!mbar_wait_or_abort(&ring_full[e & 1], (uint32_t)((e >> 1) & 1), &abort_flag)) break;
+      const int b = (int)(e & 1);
+      // the four store warps take the same exit decision (they meet at named barriers)
+      const bool ok = mbar_wait_or_abort(&b2_done[b], (uint32_t)((e >> 1) & 1), &abort_flag);
+      if (lane == 0) st_ok[q4] = ok ? 1 : 0;
+      named_sync(1, 128);  // also: every thread has finished reading the previous chunk's staging
+      if (!(st_ok[0] & st_ok[1] & st_ok[2] & st_ok[3])) break;
       tc_fence_after();
-      const int nq = ring_nq[e & 1], p0 = ring_p0[e & 1];
-      float ov[64];
-      const uint32_t slot_col = tRing + (uint32_t)(e & 1) * 64u;
+      const ChunkInfo ci = info[b];
+      gam_fin = ci.out_scale;
+      // outputs: bf16 staging [q][v] (16 readout rows at a time), then full-row 16-byte stores
+#pragma unroll 1
+      for (int c0 = 0; c0 < ci.nq; c0 += 16) {
+        float x[16];
+        tmem_ld16(tO(b) + lrow + c0, x);
+        if (v < V) {
 #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 16)
-        if (c0 < QP) tmem_ld16(slot_col + lrow + c0, ov + c0);
-      tc_fence_before();
-      mbar_arrive(&ring_free[e & 1]);
-      // outputs: bf16 staging [q][v], then full-row 16-byte stores
-      named_sync(1, 128);  // every thread has finished reading the previous chunk's staging
-      if (v < V) {
-#pragma unroll
-        for (int w = 0; w < 64; ++w)
-          if (w < nq) *reinterpret_cast<__nv_bfloat16 *>(obuf + ((uint32_t)w * V + v) * 2u) = __float2bfloat16_rn(ov[w]);
+          for (int w = 0; w < 16; ++w)
+            if (c0 + w < ci.nq)
+              *reinterpret_cast<__nv_bfloat16 *>(obuf + ((uint32_t)(c0 + w) * V + v) * 2u) =
+                  __float2bfloat16_rn(x[w] * ci.out_scale);
+        }
       }
+      tc_fence_before();
+      mbar_arrive(&yo_free[b]);  // the chunk's o_hat columns have been read
       named_sync(1, 128);
-      const int64_t tq0 = (bos * M + e * kChunk + p0) / M;  // readout rows are consecutive tokens
-      const int cpr = V / 8;                                  // 16-byte chunks per output row
-      for (int c = tid - 128; c < nq * cpr; c += 128) {
+      const int64_t tq0 = (bos * M + e * kChunk + ci.p0) / M;  // readout rows are consecutive tokens
+      const int cpr = V / 8;                                     // 16-byte chunks per output row
+      for (int c = tid - 128; c < ci.nq * cpr; c += 128) {
         const int qi = c / cpr, ch = c % cpr;
         *reinterpret_cast<uint4 *>(p.out + ((tq0 + qi) * H + h) * (int64_t)V + ch * 8) =
             *reinterpret_cast<const uint4 *>(obuf + ((uint32_t)qi * V + ch * 8) * 2u);
       }
-      if (emits(e)) {  // the state warps copied S_e before filling this ring slot
+      if (emits(e)) {  // the prep warps copied S_e before batch 2 of this chunk was issued
         float *dst = p.chunk_states + ((co_i + e / M) * H + h) * (int64_t)V * d;
-        store_state_rows(tBk + lrow, xb, lane, q4 * 32, V, d, dst);
+        store_state_rows(tBk + lrow, xb, lane, q4 * 32, V, d, 1.f, dst);
         tc_fence_before();
         mbar_arrive(&bk_free);
       }
     }
-    if (!abort_flag && (nrun == 0 || mbar_wait_or_abort(&b2_done, (uint32_t)((nrun - 1) & 1), &abort_flag))) {
-      tc_fence_after();
+    if (!abort_flag) {  // the last chunk's b2_done was waited for above
       float *dst = nullptr;
       if (p.cache) {
         if (slot >= 0) dst = p.cache + ((int64_t)slot * H + h) * (int64_t)V * d;
       } else if (p.out_state) {
         dst = p.out_state + ((int64_t)seq * H + h) * (int64_t)V * d;
       }
-      if (dst) store_state_rows(tS + lrow, xb, lane, q4 * 32, V, d, dst);
+      if (dst) store_state_rows(tS + lrow, xb, lane, q4 * 32, V, d, gam_fin, dst);
     }
   } else if (lane == 0) {
     // ---------------- control thread: image loads and MMA issue ----------------
+    int n_mid = 0;
     for (int64_t e = 0; e < nrun; ++e) {
-      const int st = (int)(e % nst);
+      const int st = (int)(e % nst), b = (int)(e & 1);
       unsigned char *stage = sm + st * sbytes;
-      if (!mbar_wait_or_abort(&full_bar[st], (uint32_t)((e / nst) & 1), &abort_flag)) break;
-      if (e >= 1 && !mbar_wait_or_abort(&o_free, (uint32_t)((e - 1) & 1), &abort_flag)) break;
+      if (!mbar_wait_or_abort(&full1[st], (uint32_t)((e / nst) & 1), &abort_flag)) break;
+      if (!mbar_wait_or_abort(&yo_ready[b], (uint32_t)((e >> 1) & 1), &abort_flag)) break;
       tc_fence_after();
+      const ImageMeta mt = *reinterpret_cast<const ImageMeta *>(stage + il.meta);
+      const bool mid = emits(e) || mt.fast == 0;
+      const uint32_t to = tO(b), ty = to + (uint32_t)QP;
       const uint32_t sb1 = smem_u32(stage) + il.b1, sb2 = smem_u32(stage) + il.b2;
       for (int kk = 0; kk < d / 8; ++kk)
-        mma_tf32_ts(tO, tS + kk * 8, desc_sw128(sb1 + (kk >> 2) * il.b1_block + (kk & 3) * 32u, 16, 1024), id1,
-                    kk > 0);
+        mma_tf32_ts(to, tS + kk * 8, desc_sw128(sb1 + (kk >> 2) * il.b1_block + (kk & 3) * 32u, 16, 1024), id1, 1);
       mma_commit(&b1_done);
-      if (!mbar_wait_or_abort(&spass_done, (uint32_t)(e & 1), &abort_flag)) break;
-      tc_fence_after();
+      // the previous chunk's stage is free once its batch 2 is done (two stages), refill it
+      // while this chunk's batch 1 runs
+      if (nst == 2 && e >= 1 && e + 1 < nrun) {
+        if (!mbar_wait_or_abort(&b2_done[(e - 1) & 1], (uint32_t)(((e - 1) >> 1) & 1), &abort_flag)) break;
+        fence_async_smem();
+        load_image(e + 1);
+      }
+      if (!mbar_wait_or_abort(&full2[st], (uint32_t)((e / nst) & 1), &abort_flag)) break;
+      if (mid) {
+        if (!mbar_wait_or_abort(&mid_done, (uint32_t)(n_mid & 1), &abort_flag)) break;
+        ++n_mid;
+        tc_fence_after();
+      }
       // two MMAs per K step (N = d and N = qpad): past N = 128 an MMA costs far more than
       // two narrower ones (measured)
       for (int kk = 0; kk < kChunk / 8; ++kk) {
         const uint32_t bk = sb2 + (kk >> 2) * il.b2_block + (kk & 3) * 32u;
-        mma_tf32_ts(tS, tVn + kk * 8, desc_sw128(bk, 16, 1024), id2s, 1);
-        mma_tf32_ts(tO, tVn + kk * 8, desc_sw128(bk + (uint32_t)d * 128u, 16, 1024), id2o, 1);
+        mma_tf32_ts(tS, ty + kk * 8, desc_sw128(bk, 16, 1024), id2s, 1);
+        mma_tf32_ts(to, ty + kk * 8, desc_sw128(bk + (uint32_t)d * 128u, 16, 1024), id2o, 1);
       }
-      mma_commit(&b2_done);
-      if (e + nst < nrun) {  // the stage is free once this chunk's products are done
-        if (!mbar_wait_or_abort(&b2_done, (uint32_t)(e & 1), &abort_flag)) break;
+      mma_commit(&b2_done[b]);
+      if (nst == 1 && e + 1 < nrun) {  // one stage: the next image waits for this chunk
+        if (!mbar_wait_or_abort(&b2_done[b], (uint32_t)((e >> 1) & 1), &abort_flag)) break;
         fence_async_smem();
-        mbar_arrive_expect_tx(&full_bar[st], il.bytes);
-        bulk_g2s(stage, p.img + (size_t)((cod_i + e + nst) * H + h) * p.img_stride, il.bytes, &full_bar[st]);
+        load_image(e + 1);
       }
     }
     if (abort_flag) {
@@ -323,7 +395,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdp_scan_kernel(Problem p) {
   tc_fence_before();
   __syncthreads();
   if (abort_flag && warp == 8 && lane == 0)
-    for (int s = 0; s < nst; ++s) mbar_wait(&full_bar[s], 0);  // bounded; covers a copy still landing
+    for (int s = 0; s < nst; ++s) {  // bounded; covers a copy still landing
+      mbar_wait(&full1[s], 0);
+      mbar_wait(&full2[s], 0);
+    }
   __syncthreads();
   if (warp == 8) tmem_free(tb, 512);
 }

@@ -16,6 +16,8 @@
 // display equation).  The kernel also forms what the output stage needs:
 //   P[q][s] = scale 2^(G2_p - G2_s) (qhat_t . khat_s)   for s <= p  (p = t*M + M - 1)
 //   Qh[q]   = scale 2^(G2_p) qhat_t,    Kt[s] = 2^(G2_last - G2_s) khat_s.
+// When 2^G2_last >= 2^kFastMinLog2Gamma, W and Qh are written divided by
+// 2^G2_last (the scan keeps its state divided by a running decay product).
 // Every exponent is of a difference G2_i - G2_j with i >= j (or of a partial
 // sum <= 0), so no factor exceeds 1.
 //
@@ -239,8 +241,12 @@ __global__ void __launch_bounds__(kWyThreads) gdp_wy_kernel(Problem p) {
     G2[tid] = x;
   }
   __syncthreads();
+  // a fast image carries -W and Qh divided by the chunk decay 2^G2_last
+  const float G2last = G2[len - 1];
+  const bool fast = G2last >= kFastMinLog2Gamma;
+  const float shift = fast ? G2last : 0.f;
   if (tid < kChunk) {
-    wc[tid] = bt[tid] * exp2f(G2[tid]) * rk[tid];
+    wc[tid] = bt[tid] * exp2f(G2[tid] - shift) * rk[tid];
     uc[tid] = bt[tid];
     ks[tid] = (tid < len) ? exp2f(G2[len - 1] - G2[tid]) * rk[tid] : 0.f;
   }
@@ -252,7 +258,6 @@ __global__ void __launch_bounds__(kWyThreads) gdp_wy_kernel(Problem p) {
   __syncthreads();
   const ImageLayout il(d, QP);
   unsigned char *img = p.img + (size_t)((int64_t)row * p.H + h) * p.img_stride;
-  const float G2last = G2[len - 1];
   {
     float dv[64];
     const uint32_t taddr = tD1 + ((uint32_t)(warp * 32) << 16);
@@ -268,7 +273,7 @@ __global__ void __launch_bounds__(kWyThreads) gdp_wy_kernel(Problem p) {
       if (qi < QP) {
         const int pr = p0 + qi * M;
         const bool live = qi < nq;
-        const float qscale = live ? p.scale * exp2f(G2[pr]) * rq[qi] : 0.f;
+        const float qscale = live ? p.scale * exp2f(G2[pr] - shift) * rq[qi] : 0.f;
         const float sc = live ? p.scale * rq[qi] : 0.f;
         for (int s0 = 0; s0 < kChunk; s0 += 4) {
           float4 o4;
@@ -384,18 +389,14 @@ __global__ void __launch_bounds__(kWyThreads) gdp_wy_kernel(Problem p) {
       tmem_ld16(tU + lrow + c0, uv + c0);
     }
     if (!abort_flag) {
-      // U^T rows fbase .. fbase + rpw - 1 (contiguous in global, 256 B each)
+      // U^T rows fbase .. fbase + rpw - 1 in the 32-row-group layout (one float4 per lane and
+      // store instruction, consecutive lanes at consecutive 16 bytes)
       if (mine) {
+        const int f = fbase + lane;
+        float4 *Ut = reinterpret_cast<float4 *>(p.U + ((int64_t)row * p.H + h) * p.V * kChunk) + (f >> 5) * 512 + (f & 31);
 #pragma unroll
-        for (int s0 = 0; s0 < kChunk; s0 += 4)
-          *reinterpret_cast<float4 *>(tile + lane * 68 + s0) = make_float4(uv[s0], uv[s0 + 1], uv[s0 + 2], uv[s0 + 3]);
+        for (int j = 0; j < 16; ++j) Ut[j * 32] = make_float4(uv[4 * j], uv[4 * j + 1], uv[4 * j + 2], uv[4 * j + 3]);
       }
-      __syncwarp();
-      float *Ut = p.U + (((int64_t)row * p.H + h) * p.V + fbase) * kChunk;
-      for (int c = lane; c < rpw * 16; c += 32)
-        *reinterpret_cast<float4 *>(Ut + (c >> 4) * kChunk + (c & 15) * 4) =
-            *reinterpret_cast<const float4 *>(tile + (c >> 4) * 68 + (c & 15) * 4);
-      __syncwarp();
       // -W image: element (s, f) at row qpad + s of K-block f/32; two halves of 32 rows s
       const int kb = fbase >> 5, ch0 = (fbase & 31) >> 2, nch = rpw >> 2;
       for (int half = 0; half < 2; ++half) {
@@ -434,6 +435,7 @@ __global__ void __launch_bounds__(kWyThreads) gdp_wy_kernel(Problem p) {
     mt->nq = nq;
     mt->p0 = p0;
     mt->len = len;
+    mt->fast = fast ? 1 : 0;
     if (abort_flag) set_status(p.status, GDP_DEV_ERR_TIMEOUT);
   }
   tc_fence_before();

@@ -106,7 +106,9 @@ typedef struct gdp_prefill_args {
      PLACE at slot state_indices[i] (int32 [N]); -1 marks a padding sequence,
      which starts from zero, still produces output and writes no slot
      (Megatron page, parameters state and state_indices).  In cache mode
-     output_state must be NULL: the final state goes to the cache only. */
+     output_state must be NULL: the final state goes to the cache only.
+     Every state buffer (initial_state, state, output_state, chunk_states) is
+     contiguous and 16-byte aligned; a misaligned one is GDP_ERR_INVALID_ARG. */
   const float *initial_state;
   float *state;
   const int32_t *state_indices;

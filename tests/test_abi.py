@@ -81,6 +81,8 @@ def _args(**over):
     (dict(q=(1 << 20) + 8), pkg.GDP_ERR_INVALID_ARG),
     (dict(initial_state=1 << 21, state=1 << 22, state_indices=1 << 23, num_slots=4), pkg.GDP_ERR_INVALID_ARG),
     (dict(state=1 << 22), pkg.GDP_ERR_INVALID_ARG),
+    (dict(initial_state=(1 << 21) + 4), pkg.GDP_ERR_INVALID_ARG),
+    (dict(chunk_states=(1 << 21) + 8), pkg.GDP_ERR_INVALID_ARG),
     (dict(state=1 << 22, state_indices=1 << 23, num_slots=4, output_state=1 << 24), pkg.GDP_ERR_INVALID_ARG),
     (dict(initial_state=1 << 24, output_state=(1 << 24) + 4096), pkg.GDP_ERR_ALIAS),
     (dict(chunk_indices=1 << 21), pkg.GDP_ERR_INVALID_ARG),

@@ -147,6 +147,11 @@ EDGE = {
     "empty_sequences": dict(lengths=[0, 17, 0, 0, 70, 0], H=2, d=128, M=2, init_sigma=0.3, chunk_states=True),
     "l2norm_m1": dict(lengths=[300], H=2, d=128, M=1, normalised=False, use_qk_l2norm=True),
     "strong_decay": dict(lengths=[200], H=2, d=128, M=2, decay=8.0, init_sigma=0.3),
+    # chunk decays around 2^-20: a mix of chunks whose state decay is deferred and chunks
+    # whose decay is applied to the state at once, with chunk states requested
+    "mixed_decay": dict(lengths=[700, 333], H=2, d=128, M=2, decay=0.9, init_sigma=0.2, chunk_states=True),
+    # chunk decays ~2^-9: the deferred decay product is renormalised every few chunks
+    "frequent_renorm": dict(lengths=[900], H=2, d=128, M=3, decay=0.6, init_sigma=0.2, chunk_states=True),
     "no_gates": dict(lengths=[90, 33], H=2, d=64, M=2, with_g=False, with_beta=False, init_sigma=0.1),
     "many_short": dict(lengths=[3] * 50 + [1] * 20, H=2, d=128, M=3, chunk_states=True, init_sigma=0.1),
 }
