@@ -41,14 +41,16 @@ namespace {
 using namespace sm100;
 
 // Warp roles:
-//   warp 8     control : image copies (bulk TMA) and MMA issue
+//   warp 8     control : MMA issue
+//   warp 9     producer: image copies (bulk TMA); part 1 of a stage is refilled once batch 1
+//                        has read it, part 2 once batch 2 has
 //   warps 0-3  prep    : per chunk, Y <- U^T / Gamma' and o_hat <- 0 in the chunk's TMEM
 //                        buffer (two buffers), renormalisation, the state snapshot at
 //                        token-chunk starts (-> TMEM copy) and the slow-image decay
 //   warps 4-7  store   : o_hat * Gamma' -> bf16 outputs, snapshot -> chunk_states,
 //                        final state
 // TMEM lanes: prep and store warps w access lanes 32 (w % 4) .. +31.
-constexpr int kScanThreads = 288;
+constexpr int kScanThreads = 320;
 constexpr uint32_t kScanSmemBudget = 200u * 1024u;  // operand stages
 constexpr uint32_t kXpose = 32u * 36u * 4u;         // per store warp: 32 x 36 fp32 transpose tile
 
@@ -113,7 +115,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdp_scan_kernel(Problem p) {
   unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)scan_smem_raw + 1023) & ~(uintptr_t)1023);
   unsigned char *obuf = sm + nst * sbytes;  // [qpad][V] bf16 output staging
   float *xb = reinterpret_cast<float *>(obuf + obuf_bytes(QP, V)) + q4 * 32 * 36;
-  __shared__ __align__(8) uint64_t full1[2], full2[2], yo_ready[2], yo_free[2], b2_done[2], b1_done, mid_done,
+  __shared__ __align__(8) uint64_t full1[2], full2[2], yo_ready[2], yo_free[2], b1_done[2], b2_done[2], mid_done,
       bk_free, fin_bar;
   __shared__ uint32_t tmem_slot;
   __shared__ ChunkInfo info[2];
@@ -149,9 +151,9 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdp_scan_kernel(Problem p) {
       mbar_init(&full2[i], 1);
       mbar_init(&yo_ready[i], 128);
       mbar_init(&yo_free[i], 128);
+      mbar_init(&b1_done[i], 1);
       mbar_init(&b2_done[i], 1);
     }
-    mbar_init(&b1_done, 1);
     mbar_init(&mid_done, 128);
     mbar_init(&bk_free, 128);
     mbar_init(&fin_bar, 1);
@@ -171,14 +173,20 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdp_scan_kernel(Problem p) {
   const uint32_t id2s = idesc(kFmtTF32, 0, 0, d, 128);       // S_hat += Y Ktil
   const uint32_t id2o = idesc(kFmtTF32, 0, 0, QP, 128);      // o_hat += Y P^T
 
-  auto load_image = [&](int64_t e) {  // control thread: image of chunk e into stage e % nst
+  auto image = [&](int64_t e) { return p.img + (size_t)((cod_i + e) * H + h) * p.img_stride; };
+  // producer thread: part 1 / part 2 of chunk e's image into stage e % nst (n1, n2: copies issued)
+  int n1[2] = {0, 0}, n2[2] = {0, 0};
+  auto load_part1 = [&](int64_t e) {
     const int st = (int)(e % nst);
-    unsigned char *stage = sm + st * sbytes;
-    const unsigned char *g = p.img + (size_t)((cod_i + e) * H + h) * p.img_stride;
     mbar_arrive_expect_tx(&full1[st], il.part1);
-    bulk_g2s(stage, g, il.part1, &full1[st]);
+    bulk_g2s(sm + st * sbytes, image(e), il.part1, &full1[st]);
+    ++n1[st];
+  };
+  auto load_part2 = [&](int64_t e) {
+    const int st = (int)(e % nst);
     mbar_arrive_expect_tx(&full2[st], il.part2);
-    bulk_g2s(stage + il.b2, g + il.b2, il.part2, &full2[st]);
+    bulk_g2s(sm + st * sbytes + il.b2, image(e) + il.b2, il.part2, &full2[st]);
+    ++n2[st];
   };
 
   if (warp < 4) {
@@ -195,8 +203,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdp_scan_kernel(Problem p) {
     }
     tmem_st_wait();
   }
-  if (warp == 8 && lane == 0)
-    for (int64_t e = 0; e < nst && e < nrun; ++e) load_image(e);
+  if (warp == 9 && lane == 0)
+    for (int64_t e = 0; e < nst && e < nrun; ++e) {
+      load_part1(e);
+      load_part2(e);
+    }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -215,11 +226,15 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdp_scan_kernel(Problem p) {
     };
     float gam = 1.f;  // Gamma of the state in TMEM
     int n_emit = 0;
-    if (nrun > 0) load_u(0);
+    auto meta_at = [&](int64_t e) { return *reinterpret_cast<const ImageMeta *>(image(e) + il.meta); };
+    ImageMeta mt_next{};
+    if (nrun > 0) {
+      load_u(0);
+      mt_next = meta_at(0);
+    }
     for (int64_t e = 0; e < nrun; ++e) {
-      const int st = (int)(e % nst), b = (int)(e & 1);
-      if (!mbar_wait_or_abort(&full1[st], (uint32_t)((e / nst) & 1), &abort_flag)) break;
-      const ImageMeta mt = *reinterpret_cast<const ImageMeta *>(sm + st * sbytes + il.meta);
+      const int b = (int)(e & 1);
+      const ImageMeta mt = mt_next;  // read from the image in global memory a chunk ahead
       const bool fast = mt.fast != 0, emit = emits(e);
       const bool renorm = fast ? (gam * mt.gamma_last < kRenormMinGamma) : (gam != 1.f);
       const float gam_pass = renorm ? 1.f : gam;                  // Gamma during the chunk's products
@@ -259,12 +274,15 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdp_scan_kernel(Problem p) {
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&yo_ready[b]);
-      if (e + 1 < nrun) load_u(e + 1);  // next chunk's U^T, in flight while this chunk runs
+      if (e + 1 < nrun) {  // next chunk's U^T and meta, in flight while this chunk runs
+        load_u(e + 1);
+        mt_next = meta_at(e + 1);
+      }
       if (emit || !fast) {
         // between the two batches: snapshot S_e = gam_pass S_hat (read alongside batch 1) and,
         // for a slow image, S_hat <- gamma_last S_hat once batch 1 has read it
         if (emit && n_emit >= 1 && !mbar_wait_or_abort(&bk_free, (uint32_t)((n_emit - 1) & 1), &abort_flag)) break;
-        if (!fast && !mbar_wait_or_abort(&b1_done, (uint32_t)(e & 1), &abort_flag)) break;
+        if (!fast && !mbar_wait_or_abort(&b1_done[b], (uint32_t)((e >> 1) & 1), &abort_flag)) break;
         tc_fence_after();
         for (int c0 = 0; c0 < d; c0 += 32) {
           float x[32];
@@ -342,62 +360,61 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdp_scan_kernel(Problem p) {
       }
       if (dst) store_state_rows(tS + lrow, xb, lane, q4 * 32, V, d, gam_fin, dst);
     }
-  } else if (lane == 0) {
-    // ---------------- control thread: image loads and MMA issue ----------------
-    int n_mid = 0;
-    for (int64_t e = 0; e < nrun; ++e) {
-      const int st = (int)(e % nst), b = (int)(e & 1);
-      unsigned char *stage = sm + st * sbytes;
-      if (!mbar_wait_or_abort(&full1[st], (uint32_t)((e / nst) & 1), &abort_flag)) break;
-      if (!mbar_wait_or_abort(&yo_ready[b], (uint32_t)((e >> 1) & 1), &abort_flag)) break;
-      tc_fence_after();
-      const ImageMeta mt = *reinterpret_cast<const ImageMeta *>(stage + il.meta);
-      const bool mid = emits(e) || mt.fast == 0;
-      const uint32_t to = tO(b), ty = to + (uint32_t)QP;
-      const uint32_t sb1 = smem_u32(stage) + il.b1, sb2 = smem_u32(stage) + il.b2;
-      for (int kk = 0; kk < d / 8; ++kk)
-        mma_tf32_ts(to, tS + kk * 8, desc_sw128(sb1 + (kk >> 2) * il.b1_block + (kk & 3) * 32u, 16, 1024), id1, 1);
-      mma_commit(&b1_done);
-      // the previous chunk's stage is free once its batch 2 is done (two stages), refill it
-      // while this chunk's batch 1 runs
-      if (nst == 2 && e >= 1 && e + 1 < nrun) {
-        if (!mbar_wait_or_abort(&b2_done[(e - 1) & 1], (uint32_t)(((e - 1) >> 1) & 1), &abort_flag)) break;
-        fence_async_smem();
-        load_image(e + 1);
-      }
-      if (!mbar_wait_or_abort(&full2[st], (uint32_t)((e / nst) & 1), &abort_flag)) break;
-      if (mid) {
-        if (!mbar_wait_or_abort(&mid_done, (uint32_t)(n_mid & 1), &abort_flag)) break;
-        ++n_mid;
+  } else if (warp == 8) {
+    if (lane == 0) {
+      // ---------------- control thread: MMA issue ----------------
+      int n_mid = 0;
+      for (int64_t e = 0; e < nrun; ++e) {
+        const int st = (int)(e % nst), b = (int)(e & 1);
+        unsigned char *stage = sm + st * sbytes;
+        if (!mbar_wait_or_abort(&full1[st], (uint32_t)((e / nst) & 1), &abort_flag)) break;
+        if (!mbar_wait_or_abort(&yo_ready[b], (uint32_t)((e >> 1) & 1), &abort_flag)) break;
         tc_fence_after();
+        const ImageMeta mt = *reinterpret_cast<const ImageMeta *>(stage + il.meta);
+        const bool mid = emits(e) || mt.fast == 0;
+        const uint32_t to = tO(b), ty = to + (uint32_t)QP;
+        const uint32_t sb1 = smem_u32(stage) + il.b1, sb2 = smem_u32(stage) + il.b2;
+        for (int kk = 0; kk < d / 8; ++kk)
+          mma_tf32_ts(to, tS + kk * 8, desc_sw128(sb1 + (kk >> 2) * il.b1_block + (kk & 3) * 32u, 16, 1024), id1, 1);
+        mma_commit(&b1_done[b]);
+        if (!mbar_wait_or_abort(&full2[st], (uint32_t)((e / nst) & 1), &abort_flag)) break;
+        if (mid) {
+          if (!mbar_wait_or_abort(&mid_done, (uint32_t)(n_mid & 1), &abort_flag)) break;
+          ++n_mid;
+          tc_fence_after();
+        }
+        // two MMAs per K step (N = d and N = qpad): past N = 128 an MMA costs far more than
+        // two narrower ones (measured)
+        for (int kk = 0; kk < kChunk / 8; ++kk) {
+          const uint32_t bk = sb2 + (kk >> 2) * il.b2_block + (kk & 3) * 32u;
+          mma_tf32_ts(tS, ty + kk * 8, desc_sw128(bk, 16, 1024), id2s, 1);
+          mma_tf32_ts(to, ty + kk * 8, desc_sw128(bk + (uint32_t)d * 128u, 16, 1024), id2o, 1);
+        }
+        mma_commit(&b2_done[b]);
       }
-      // two MMAs per K step (N = d and N = qpad): past N = 128 an MMA costs far more than
-      // two narrower ones (measured)
-      for (int kk = 0; kk < kChunk / 8; ++kk) {
-        const uint32_t bk = sb2 + (kk >> 2) * il.b2_block + (kk & 3) * 32u;
-        mma_tf32_ts(tS, ty + kk * 8, desc_sw128(bk, 16, 1024), id2s, 1);
-        mma_tf32_ts(to, ty + kk * 8, desc_sw128(bk + (uint32_t)d * 128u, 16, 1024), id2o, 1);
-      }
-      mma_commit(&b2_done[b]);
-      if (nst == 1 && e + 1 < nrun) {  // one stage: the next image waits for this chunk
-        if (!mbar_wait_or_abort(&b2_done[b], (uint32_t)((e >> 1) & 1), &abort_flag)) break;
-        fence_async_smem();
-        load_image(e + 1);
+      if (abort_flag) {
+        // drain every MMA issued so far before the columns are freed
+        mma_commit(&fin_bar);
+        mbar_wait(&fin_bar, 0);
+        set_status(p.status, GDP_DEV_ERR_TIMEOUT);
       }
     }
-    if (abort_flag) {
-      // drain every MMA issued so far before the columns are freed
-      mma_commit(&fin_bar);
-      mbar_wait(&fin_bar, 0);
-      set_status(p.status, GDP_DEV_ERR_TIMEOUT);
+  } else if (lane == 0) {
+    // ---------------- producer thread: image copies ----------------
+    for (int64_t e = 0; e + nst < nrun; ++e) {
+      const int b = (int)(e & 1);
+      if (!mbar_wait_or_abort(&b1_done[b], (uint32_t)((e >> 1) & 1), &abort_flag)) break;
+      load_part1(e + nst);
+      if (!mbar_wait_or_abort(&b2_done[b], (uint32_t)((e >> 1) & 1), &abort_flag)) break;
+      load_part2(e + nst);
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (abort_flag && warp == 8 && lane == 0)
-    for (int s = 0; s < nst; ++s) {  // bounded; covers a copy still landing
-      mbar_wait(&full1[s], 0);
-      mbar_wait(&full2[s], 0);
+  if (abort_flag && warp == 9 && lane == 0)
+    for (int st = 0; st < nst; ++st) {  // bounded; the last copy issued on each barrier has landed
+      if (n1[st] > 0) mbar_wait(&full1[st], (uint32_t)((n1[st] - 1) & 1));
+      if (n2[st] > 0) mbar_wait(&full2[st], (uint32_t)((n2[st] - 1) & 1));
     }
   __syncthreads();
   if (warp == 8) tmem_free(tb, 512);
