@@ -120,6 +120,9 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
                 (long long)nt_pad, (long long)ntdp_pad, (long long)ntb, (long long)ntdpb);
   if (nprebuilt == 0 && (nt_pad != ntb || ntdp_pad != ntdpb))
     return fail(GDP_ERR_INVALID_ARG, "nt_pad/ntdp_pad other than the bounds need prebuilt descriptors");
+  const int64_t hv = (int64_t)H * V;
+  if (nt_pad * hv > INT32_MAX || N * hv > INT32_MAX || (a->state && a->num_slots * hv > INT32_MAX))
+    return fail(GDP_ERR_UNSUPPORTED, "state arrays above 2^31 rows of K floats");
   const Layout lay = layout_for(T, N, H, K, V, M);
   if (!a->workspace || ((uintptr_t)a->workspace % kAlign) != 0)
     return fail(GDP_ERR_WORKSPACE, "workspace must be non-NULL and %zu-byte aligned", kAlign);

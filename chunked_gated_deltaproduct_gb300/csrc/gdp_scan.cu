@@ -32,6 +32,11 @@
 // come from one operand image per chunk (written by the WY kernel), fetched by
 // two bulk copies into a double-buffered shared-memory stage while the
 // previous chunk computes.
+#include <cuda.h>  // CUtensorMap (types only; the encoder comes from the driver entry point)
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "gdp_internal.cuh"
 #include "gdp_sm100.cuh"
 
@@ -48,11 +53,12 @@ using namespace sm100;
 //                        buffer (two buffers), renormalisation, the state snapshot at
 //                        token-chunk starts (-> TMEM copy) and the slow-image decay
 //   warps 4-7  store   : o_hat * Gamma' -> bf16 outputs, snapshot -> chunk_states,
-//                        final state
+//                        final state (states leave by TMA tensor stores of 32 x 32 blocks,
+//                        so the load/store unit that the control warp shares stays free)
 // TMEM lanes: prep and store warps w access lanes 32 (w % 4) .. +31.
 constexpr int kScanThreads = 320;
 constexpr uint32_t kScanSmemBudget = 200u * 1024u;  // operand stages
-constexpr uint32_t kXpose = 32u * 36u * 4u;         // per store warp: 32 x 36 fp32 transpose tile
+constexpr uint32_t kStTile = 4096u;                 // one 32 x 32 fp32 box, 128-byte swizzle
 
 __host__ __device__ inline uint32_t stage_bytes(int d, int qpad) {
   return (ImageLayout(d, qpad).bytes + 1023u) & ~1023u;
@@ -62,33 +68,36 @@ __host__ __device__ inline int num_stages(int d, int qpad) {
 }
 __host__ __device__ inline uint32_t obuf_bytes(int qpad, int V) { return (uint32_t)qpad * V * 2u; }
 __host__ inline size_t scan_smem_bytes(int d, int qpad, int V) {
-  return (size_t)num_stages(d, qpad) * stage_bytes(d, qpad) + obuf_bytes(qpad, V) + 4u * kXpose + 1024u;
+  return (size_t)num_stages(d, qpad) * stage_bytes(d, qpad) + obuf_bytes(qpad, V) + 4u * 2u * kStTile + 1024u;
 }
 
-// Store warp: rows [row0, row0 + 32) of a [V][d] fp32 block from this warp's TMEM
-// lanes (columns from t_lane), times mul.  Each 32 x 32 block goes through a shared
-// tile (rows padded to 36 floats: 16-byte aligned, conflict-free) so that every global
-// store instruction writes four full 128-byte row segments with 16-byte stores.
-__device__ __forceinline__ void store_state_rows(uint32_t t_lane, float *xb, int lane, int row0, int V, int d,
-                                                 float mul, float *dst) {
-  const int rq = lane >> 3, cq = (lane & 7) * 4;  // this lane's row (of 4) and column in a store
+// Store warp: the state rows held in this warp's TMEM lanes (columns from t_lane), times
+// mul, to map rows [row, row + 32): per 32 columns, one 32 x 32 box staged in shared memory
+// (row r at r * 128 bytes, 16-byte chunk j at position j ^ (r & 7): the map's 128-byte
+// swizzle, conflict-free for a thread per row) and written by one TMA tensor store.  The
+// warp's two tiles alternate; nblk counts the boxes this warp has issued.
+__device__ __forceinline__ void store_state_tma(uint32_t t_lane, unsigned char *tiles, int lane, int d, float mul,
+                                                const CUtensorMap *tm, int row, int &nblk) {
 #pragma unroll 1
   for (int c0 = 0; c0 < d; c0 += 32) {
     float x[32];
     tmem_ld32(t_lane + c0, x);
-#pragma unroll
-    for (int j = 0; j < 32; j += 4)
-      *reinterpret_cast<float4 *>(xb + lane * 36 + j) =
-          make_float4(mul * x[j], mul * x[j + 1], mul * x[j + 2], mul * x[j + 3]);
-    __syncwarp();
-#pragma unroll
-    for (int r0 = 0; r0 < 32; r0 += 4) {
-      const int r = r0 + rq;
-      if (row0 + r < V)
-        *reinterpret_cast<float4 *>(dst + (int64_t)(row0 + r) * d + c0 + cq) =
-            *reinterpret_cast<const float4 *>(xb + r * 36 + cq);
+    unsigned char *tile = tiles + (uint32_t)(nblk & 1) * kStTile;
+    if (nblk >= 2) {  // the store issued from this tile two boxes ago has read it
+      if (lane == 0) bulk_wait_read<1>();
+      __syncwarp();
     }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<float4 *>(tile + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+          make_float4(mul * x[4 * j], mul * x[4 * j + 1], mul * x[4 * j + 2], mul * x[4 * j + 3]);
+    fence_async_smem();
     __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tm, tile, c0, row);
+      bulk_commit();
+    }
+    ++nblk;
   }
 }
 
@@ -98,7 +107,8 @@ struct ChunkInfo {
   int nq, p0;
 };
 
-__global__ void __launch_bounds__(kScanThreads, 1) gdp_scan_kernel(Problem p) {
+__global__ void __launch_bounds__(kScanThreads, 1)
+    gdp_scan_kernel(Problem p, const __grid_constant__ CUtensorMap tm_cs, const __grid_constant__ CUtensorMap tm_fin) {
   const int seq = blockIdx.x, h = blockIdx.y;
   int64_t bos, L;
   if (!seq_bounds(p.cu, p.cu64, p.T, seq, &bos, &L)) return;  // flagged by the descriptor kernel
@@ -114,7 +124,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdp_scan_kernel(Problem p) {
   extern __shared__ __align__(1024) unsigned char scan_smem_raw[];
   unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)scan_smem_raw + 1023) & ~(uintptr_t)1023);
   unsigned char *obuf = sm + nst * sbytes;  // [qpad][V] bf16 output staging
-  float *xb = reinterpret_cast<float *>(obuf + obuf_bytes(QP, V)) + q4 * 32 * 36;
+  unsigned char *sttiles = obuf + obuf_bytes(QP, V) + (uint32_t)q4 * 2u * kStTile;  // this store warp's boxes
   __shared__ __align__(8) uint64_t full1[2], full2[2], yo_ready[2], yo_free[2], b1_done[2], b2_done[2], mid_done,
       bk_free, fin_bar;
   __shared__ uint32_t tmem_slot;
@@ -311,6 +321,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdp_scan_kernel(Problem p) {
   } else if (warp < 8) {
     // ---------------- store warps ----------------
     float gam_fin = 1.f;
+    int nblk = 0;
+    const bool has_rows = q4 * 32 < V;
     for (int64_t e = 0; e < nrun; ++e) {
       const int b = (int)(e & 1);
       // the four store warps take the same exit decision (they meet at named barriers)
@@ -345,21 +357,23 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdp_scan_kernel(Problem p) {
             *reinterpret_cast<const uint4 *>(obuf + ((uint32_t)qi * V + ch * 8) * 2u);
       }
       if (emits(e)) {  // the prep warps copied S_e before batch 2 of this chunk was issued
-        float *dst = p.chunk_states + ((co_i + e / M) * H + h) * (int64_t)V * d;
-        store_state_rows(tBk + lrow, xb, lane, q4 * 32, V, d, 1.f, dst);
+        if (has_rows)
+          store_state_tma(tBk + lrow, sttiles, lane, d, 1.f, &tm_cs, (int)(((co_i + e / M) * H + h) * V + q4 * 32),
+                          nblk);
         tc_fence_before();
-        mbar_arrive(&bk_free);
+        mbar_arrive(&bk_free);  // the snapshot columns have been read
       }
     }
-    if (!abort_flag) {  // the last chunk's b2_done was waited for above
-      float *dst = nullptr;
+    if (!abort_flag && has_rows) {  // the last chunk's b2_done was waited for above
+      int64_t r = -1;
       if (p.cache) {
-        if (slot >= 0) dst = p.cache + ((int64_t)slot * H + h) * (int64_t)V * d;
+        if (slot >= 0) r = ((int64_t)slot * H + h) * V;
       } else if (p.out_state) {
-        dst = p.out_state + ((int64_t)seq * H + h) * (int64_t)V * d;
+        r = ((int64_t)seq * H + h) * V;
       }
-      if (dst) store_state_rows(tS + lrow, xb, lane, q4 * 32, V, d, gam_fin, dst);
+      if (r >= 0) store_state_tma(tS + lrow, sttiles, lane, d, gam_fin, &tm_fin, (int)(r + q4 * 32), nblk);
     }
+    if (lane == 0) bulk_wait_all();  // this warp's tensor stores are complete
   } else if (warp == 8) {
     if (lane == 0) {
       // ---------------- control thread: MMA issue ----------------
@@ -422,13 +436,54 @@ __global__ void __launch_bounds__(kScanThreads, 1) gdp_scan_kernel(Problem p) {
 
 }  // namespace
 
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// Map over a [rows][d] fp32 array (16-byte aligned) in 32 x 32 boxes with the 128-byte swizzle.
+cudaError_t state_map(CUtensorMap *m, float *base, int64_t rows, int d) {
+  if (!base || rows <= 0) return cudaSuccess;  // unused: left zeroed
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)d * sizeof(float)};
+  const cuuint32_t box[2] = {32, 32}, estr[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
 cudaError_t launch_scan(const Problem &p, cudaStream_t stream) {
   if (p.N == 0) return cudaSuccess;
   const size_t smem = scan_smem_bytes(p.K, p.qpad, p.V);
   cudaError_t e = cudaFuncSetAttribute(gdp_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  alignas(64) CUtensorMap tm_cs, tm_fin;
+  memset(&tm_cs, 0, sizeof(tm_cs));
+  memset(&tm_fin, 0, sizeof(tm_fin));
+  const int64_t hv = (int64_t)p.H * p.V;
+  if ((e = state_map(&tm_cs, p.chunk_states, p.nt_pad * hv, p.K)) != cudaSuccess) return e;
+  if (p.cache)
+    e = state_map(&tm_fin, p.cache, p.num_slots * hv, p.K);
+  else
+    e = state_map(&tm_fin, p.out_state, p.N * hv, p.K);
+  if (e != cudaSuccess) return e;
   dim3 grid((unsigned)p.N, (unsigned)p.H);
-  gdp_scan_kernel<<<grid, kScanThreads, smem, stream>>>(p);
+  gdp_scan_kernel<<<grid, kScanThreads, smem, stream>>>(p, tm_cs, tm_fin);
   return cudaGetLastError();
 }
 

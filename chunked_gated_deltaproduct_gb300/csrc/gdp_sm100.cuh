@@ -193,6 +193,13 @@ __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Tensor (TMA) store of one 2-D box from shared memory at coordinates (x, y) of the map
+// `tmap` (a __grid_constant__ kernel parameter), in the calling thread's bulk async-group.
+__device__ __forceinline__ void tma_store_2d(const void *tmap, const void *smem_src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tmap),
+               "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+               : "memory");
+}
 
 }  // namespace sm100
 }  // namespace gdp

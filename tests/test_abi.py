@@ -86,6 +86,8 @@ def _args(**over):
     (dict(state=1 << 22, state_indices=1 << 23, num_slots=4, output_state=1 << 24), pkg.GDP_ERR_INVALID_ARG),
     (dict(initial_state=1 << 24, output_state=(1 << 24) + 4096), pkg.GDP_ERR_ALIAS),
     (dict(chunk_indices=1 << 21), pkg.GDP_ERR_INVALID_ARG),
+    (dict(T=1 << 22, H=4096, q_stride_t=4096 * 64, k_stride_t=4096 * 64, v_stride_t=4096 * 64),
+     pkg.GDP_ERR_UNSUPPORTED),  # chunk-state rows beyond 32-bit tensor coordinates
     (dict(workspace=None), pkg.GDP_ERR_WORKSPACE),
     (dict(workspace=(1 << 20) + 16), pkg.GDP_ERR_WORKSPACE),
     (dict(workspace_bytes=64), pkg.GDP_ERR_WORKSPACE),
