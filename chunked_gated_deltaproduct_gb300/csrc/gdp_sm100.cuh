@@ -116,6 +116,16 @@ __device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity) {
                : "memory");
   return ok != 0;
 }
+// As mbar_try, but the thread may sleep in hardware for up to hint_ns (woken early when the
+// phase completes) instead of returning at once: waiting without polling shared memory.
+__device__ __forceinline__ bool mbar_try_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.u32 %0, 1, 0, p;\n}\n"
+               : "=r"(ok)
+               : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+               : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
@@ -150,14 +160,12 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 0; it < (1u << 24); ++it) {
-    if (mbar_try(bar, parity)) return true;
-    if ((it & 15u) == 15u) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > 1000000000ull) {
-        *abort_flag = 1;
-        return false;
-      }
+  for (uint32_t it = 0; it < (1u << 20); ++it) {
+    if (mbar_try_sleep(bar, parity, 100000u)) return true;  // sleeps up to 0.1 ms per try
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > 1000000000ull) {
+      *abort_flag = 1;
+      return false;
     }
   }
   *abort_flag = 1;
