@@ -129,6 +129,15 @@ cudaError_t launch_descriptors(const void *cu, int cu64, int64_t T, int64_t N, i
 cudaError_t launch_wy(const Problem &p, cudaStream_t stream);
 cudaError_t launch_scan(const Problem &p, cudaStream_t stream);
 
+// TMA tensor maps (gdp_tmap.cu; `map` points at a 64-byte aligned CUtensorMap; a NULL base
+// leaves it zeroed).  All use the 128-byte swizzle.
+//   tmap_state:     [rows][d] fp32, 32 x 32 boxes
+//   tmap_rows_bf16: [rows][H][K] bf16 with element strides (stride_t, stride_h), boxes of
+//                   64 features x 1 head x box_rows rows
+cudaError_t tmap_state(void *map, float *base, int64_t rows, int d);
+cudaError_t tmap_rows_bf16(void *map, const void *base, int64_t rows, int H, int K, int64_t stride_t, int64_t stride_h,
+                           int box_rows);
+
 // Sets the calling thread's gdp_last_error() text (defined in gdp_api.cu).
 void set_last_error(const char *fmt, ...);
 

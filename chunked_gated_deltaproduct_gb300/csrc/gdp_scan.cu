@@ -32,10 +32,7 @@
 // come from one operand image per chunk (written by the WY kernel), fetched by
 // two bulk copies into a double-buffered shared-memory stage while the
 // previous chunk computes.
-#include <cuda.h>  // CUtensorMap (types only; the encoder comes from the driver entry point)
-#include <cudaTypedefs.h>
-
-#include <mutex>
+#include <cuda.h>  // CUtensorMap
 
 #include "gdp_internal.cuh"
 #include "gdp_sm100.cuh"
@@ -436,51 +433,18 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 
 }  // namespace
 
-namespace {
-
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-
-// Map over a [rows][d] fp32 array (16-byte aligned) in 32 x 32 boxes with the 128-byte swizzle.
-cudaError_t state_map(CUtensorMap *m, float *base, int64_t rows, int d) {
-  if (!base || rows <= 0) return cudaSuccess;  // unused: left zeroed
-  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-  if (!enc) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)d * sizeof(float)};
-  const cuuint32_t box[2] = {32, 32}, estr[2] = {1, 1};
-  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
-}  // namespace
-
 cudaError_t launch_scan(const Problem &p, cudaStream_t stream) {
   if (p.N == 0) return cudaSuccess;
   const size_t smem = scan_smem_bytes(p.K, p.qpad, p.V);
   cudaError_t e = cudaFuncSetAttribute(gdp_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   alignas(64) CUtensorMap tm_cs, tm_fin;
-  memset(&tm_cs, 0, sizeof(tm_cs));
-  memset(&tm_fin, 0, sizeof(tm_fin));
   const int64_t hv = (int64_t)p.H * p.V;
-  if ((e = state_map(&tm_cs, p.chunk_states, p.nt_pad * hv, p.K)) != cudaSuccess) return e;
+  if ((e = tmap_state(&tm_cs, p.chunk_states, p.nt_pad * hv, p.K)) != cudaSuccess) return e;
   if (p.cache)
-    e = state_map(&tm_fin, p.cache, p.num_slots * hv, p.K);
+    e = tmap_state(&tm_fin, p.cache, p.num_slots * hv, p.K);
   else
-    e = state_map(&tm_fin, p.out_state, p.N * hv, p.K);
+    e = tmap_state(&tm_fin, p.out_state, p.N * hv, p.K);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)p.N, (unsigned)p.H);
   gdp_scan_kernel<<<grid, kScanThreads, smem, stream>>>(p, tm_cs, tm_fin);

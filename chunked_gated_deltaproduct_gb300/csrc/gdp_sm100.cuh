@@ -187,6 +187,16 @@ __device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gsrc, uint3
                : "memory");
 }
 
+// Tensor (TMA) load of one 3-D box at coordinates (x, y, z) of the map `tmap` into shared
+// memory, completing on `bar` (x * element size must be a multiple of 16 bytes).
+__device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *tmap, int x, int y, int z, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
+          "r"(smem_u32(smem_dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Bulk copy (TMA, non-tensor) shared -> global in the calling thread's bulk async-group
 // (16-byte aligned, size % 16 == 0).  The group is closed by bulk_commit; bulk_wait_read<N>
 // returns once at most N of the thread's newest groups may still be reading shared memory.

@@ -29,6 +29,8 @@
 // The inverse of the unit lower-triangular I + A runs on the CUDA cores in
 // 16 x 16 blocks: the four diagonal blocks by forward substitution (one warp
 // each), then T_ij = -T_ii sum_k A_ik T_kj for the off-diagonal blocks.
+#include <cuda.h>  // CUtensorMap
+
 #include "gdp_internal.cuh"
 #include "gdp_sm100.cuh"
 
@@ -118,7 +120,9 @@ __device__ __forceinline__ void bf16x8_at(const unsigned char *tile, int rows_pe
   }
 }
 
-__global__ void __launch_bounds__(kWyThreads) gdp_wy_kernel(Problem p) {
+__global__ void __launch_bounds__(kWyThreads)
+    gdp_wy_kernel(Problem p, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+                  const __grid_constant__ CUtensorMap tm_v) {
   const int row = blockIdx.x, h = blockIdx.y;
   const int seq = p.cid[2 * row], c = p.cid[2 * row + 1];
   if (seq < 0 || seq >= p.N || row >= p.ws_rows) return;
@@ -146,44 +150,43 @@ __global__ void __launch_bounds__(kWyThreads) gdp_wy_kernel(Problem p) {
   float *bt = G2 + kChunk, *rk = bt + kChunk, *rq = rk + kChunk, *wc = rq + kChunk, *uc = wc + kChunk;
   float *ks = uc + kChunk;  // 2^(G2_last - G2_s) rk_s (0 past the chunk end)
   __shared__ uint32_t tmem_slot;
-  __shared__ __align__(8) uint64_t mma_bar;
+  __shared__ __align__(8) uint64_t mma_bar, ld_bar;
   __shared__ float warp_tot;
   __shared__ int abort_flag;
 
   if (warp == 0) tmem_alloc(&tmem_slot, 256);
   if (tid == 0) {
     mbar_init(&mma_bar, 1);
+    mbar_init(&ld_bar, 1);
     mbar_init_fence();
     abort_flag = 0;
   }
+  __syncthreads();
 
-  // ---- loads: 16-byte asynchronous copies into the swizzled bf16 tiles (zero past the chunk end) ----
-  const int cpr = d / 8;  // 16-byte chunks per row
-  for (int idx = tid; idx < 128 * cpr; idx += kWyThreads) {
-    const int r = idx / cpr, ch = idx % cpr;
-    const __nv_bfloat16 *src = p.k;
-    uint32_t bytes = 0;
-    if (r < kChunk) {
-      if (r < len) {
-        src = p.k + (R0 + r) * p.k_st + (int64_t)h * p.k_sh + ch * 8;
-        bytes = 16;
-      }
-    } else {
-      const int qi = r - kChunk;
-      if (qi < nq) {
-        src = p.q + (tq0 + qi) * p.q_st + (int64_t)h * p.q_sh + ch * 8;
-        bytes = 16;
-      }
+  // ---- loads: TMA boxes of 64 features x rows into the swizzled bf16 tiles: k rows R0.., the
+  // readout q rows tq0.. (rows 64.. of kq), v rows R0..; rows past the chunk (another sequence's
+  // data, or zero past the tensor) are cleared below so that sequences stay independent ----
+  const int nb = d / 64;
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&ld_bar, (uint32_t)nb * (uint32_t)(64 + QP + 64) * 128u);
+    for (int kb = 0; kb < nb; ++kb) {
+      tma_load_3d(kq + kb * 16384u, &tm_k, kb * 64, h, (int)R0, &ld_bar);
+      tma_load_3d(kq + kb * 16384u + 8192u, &tm_q, kb * 64, h, (int)tq0, &ld_bar);
+      tma_load_3d(vt + kb * 8192u, &tm_v, kb * 64, h, (int)R0, &ld_bar);
     }
-    cp_async16(kq + (ch >> 3) * 16384u + swz(r, (ch & 7) * 16u), src, bytes);
   }
-  for (int idx = tid; idx < kChunk * cpr; idx += kWyThreads) {
-    const int r = idx / cpr, ch = idx % cpr;
-    const bool live = r < len;
-    const __nv_bfloat16 *src = live ? p.v + (R0 + r) * p.v_st + (int64_t)h * p.v_sh + ch * 8 : p.v;
-    cp_async16(vt + (ch >> 3) * 8192u + swz(r, (ch & 7) * 16u), src, live ? 16u : 0u);
+  if (!mbar_wait(&ld_bar, 0)) abort_flag = 1;
+  {
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    const int nk = kChunk - len, nqz = QP - nq;  // rows to clear
+    for (int idx = tid; idx < nb * (2 * nk + nqz) * 8; idx += kWyThreads) {
+      const int ch = idx & 7, rr = idx >> 3, kb = rr % nb, r = rr / nb;
+      unsigned char *row = (r < nk) ? kq + kb * 16384u + (uint32_t)(len + r) * 128u
+                           : (r < 2 * nk) ? vt + kb * 8192u + (uint32_t)(len + r - nk) * 128u
+                                          : kq + kb * 16384u + (uint32_t)(64 + nq + r - 2 * nk) * 128u;
+      *reinterpret_cast<uint4 *>(row + ch * 16) = z;
+    }
   }
-  cp_async_wait_all();
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -450,8 +453,13 @@ cudaError_t launch_wy(const Problem &p, cudaStream_t stream) {
   const size_t smem = WyLayout(p.K).total + 1024;
   cudaError_t e = cudaFuncSetAttribute(gdp_wy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  alignas(64) CUtensorMap tm_k, tm_q, tm_v;
+  const int64_t rows = p.T * p.M;
+  if ((e = tmap_rows_bf16(&tm_k, p.k, rows, p.H, p.K, p.k_st, p.k_sh, kChunk)) != cudaSuccess) return e;
+  if ((e = tmap_rows_bf16(&tm_q, p.q, p.T, p.H, p.K, p.q_st, p.q_sh, p.qpad)) != cudaSuccess) return e;
+  if ((e = tmap_rows_bf16(&tm_v, p.v, rows, p.H, p.V, p.v_st, p.v_sh, kChunk)) != cudaSuccess) return e;
   dim3 grid((unsigned)p.ntdp_pad, (unsigned)p.H);
-  gdp_wy_kernel<<<grid, kWyThreads, smem, stream>>>(p);
+  gdp_wy_kernel<<<grid, kWyThreads, smem, stream>>>(p, tm_k, tm_q, tm_v);
   return cudaGetLastError();
 }
 
