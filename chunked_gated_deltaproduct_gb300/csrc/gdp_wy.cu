@@ -42,7 +42,7 @@ using namespace sm100;
 constexpr int kWyThreads = 128;
 constexpr int kLd = kChunk + 1;   // row stride of the fp32 A scratch (conflict-free row reads)
 constexpr int kLdT = kChunk + 4;  // row stride of T (16-byte aligned rows for float4 access)
-constexpr int kLdY = 52;          // row stride of the [16][<=48] block-product scratch
+constexpr int kLdY = 20;          // row stride of the [3 pairs x 16][16] block-product scratch
 constexpr int kTile = 32 * 68;    // per-warp transpose tile (floats); reuses the A / T / Y region
 
 struct WyLayout {
@@ -64,41 +64,48 @@ struct WyLayout {
     }
     A = tul + 8192u;                       // fp32 [64][65]
     T = A + 4u * kChunk * kLd;             // fp32 [64][68]
-    Y = T + 4u * kChunk * kLdT;            // fp32 [16][52] block products
-    scal = Y + 4u * 16 * kLdY;             // G2, beta, rk, rq, wc, uc, kscale  [7][64]
+    Y = T + 4u * kChunk * kLdT;            // fp32 [48][20] block products
+    scal = Y + 4u * 48 * kLdY;             // G2, beta, rk, rq, wc, uc, kscale  [7][64]
     total = scal + 4u * 7 * kChunk;
   }
 };
-static_assert(4 * 64 * (65 + 68) + 4 * 16 * 52 >= 4 * 4 * kTile, "transpose tiles must fit the A/T/Y region");
+static_assert(4 * 64 * (65 + 68) + 4 * 48 * kLdY >= 4 * 4 * kTile, "transpose tiles must fit the A/T/Y region");
 
-// One block row of the blocked unit-lower-triangular inverse (see the kernel).
-template <int BI>
-__device__ __forceinline__ void inverse_block_row(const float *A, float *Tm, float *Y, int tid) {
-  constexpr int NCG = 4 * BI;  // 4-column groups left of the diagonal block
-  for (int it = tid; it < 16 * NCG; it += kWyThreads) {
-    const int m = it / NCG, c = (it % NCG) * 4;
-    const float *arow = A + (16 * BI + m) * kLd;
+// Off-diagonal 16 x 16 blocks of T = (I + A)^-1 for block pairs (i, j), i - j = L: first
+// Y_ij = sum_{k=j}^{i-1} A_ik T_kj over the 16 L columns x of A's block row, then
+// T_ij = -T_ii Y_ij.  The 4 - L pairs of a level are independent; each thread owns 4 adjacent
+// columns of one row of one pair, so every shared load feeds 4 independent FMAs.
+__device__ __forceinline__ void inverse_level(const float *A, float *Tm, float *Y, int tid, int L) {
+  const int items = (4 - L) * 64;
+#pragma unroll 1
+  for (int it = tid; it < items; it += kWyThreads) {
+    const int pr = it >> 6, r = (it >> 2) & 15, c = (it & 3) * 4;
+    const int i = pr + L, j = pr;
+    const float *arow = A + (16 * i + r) * kLd;
+    const float *tcol = Tm + 16 * j + c;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int x = 0; x < 16 * BI; ++x) {
+#pragma unroll 4
+    for (int x = 16 * j; x < 16 * i; ++x) {
       const float a = arow[x];
-      const float4 t = *reinterpret_cast<const float4 *>(Tm + x * kLdT + c);
+      const float4 t = *reinterpret_cast<const float4 *>(tcol + x * kLdT);
       acc.x += a * t.x; acc.y += a * t.y; acc.z += a * t.z; acc.w += a * t.w;
     }
-    *reinterpret_cast<float4 *>(Y + m * kLdY + c) = acc;
+    *reinterpret_cast<float4 *>(Y + (pr * 16 + r) * kLdY + c) = acc;
   }
   __syncthreads();
-  for (int it = tid; it < 16 * NCG; it += kWyThreads) {
-    const int r = it / NCG, c = (it % NCG) * 4;
-    const float *trow = Tm + (16 * BI + r) * kLdT + 16 * BI;
+#pragma unroll 1
+  for (int it = tid; it < items; it += kWyThreads) {
+    const int pr = it >> 6, r = (it >> 2) & 15, c = (it & 3) * 4;
+    const int i = pr + L, j = pr;
+    const float *trow = Tm + (16 * i + r) * kLdT + 16 * i;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const float t = (m <= r) ? trow[m] : 0.f;
-      const float4 y = *reinterpret_cast<const float4 *>(Y + m * kLdY + c);
+#pragma unroll 4
+    for (int m = 0; m <= r; ++m) {
+      const float t = trow[m];
+      const float4 y = *reinterpret_cast<const float4 *>(Y + (pr * 16 + m) * kLdY + c);
       acc.x += t * y.x; acc.y += t * y.y; acc.z += t * y.z; acc.w += t * y.w;
     }
-    *reinterpret_cast<float4 *>(Tm + (16 * BI + r) * kLdT + c) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+    *reinterpret_cast<float4 *>(Tm + (16 * i + r) * kLdT + 16 * j + c) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
   }
   __syncthreads();
 }
@@ -262,41 +269,57 @@ __global__ void __launch_bounds__(kWyThreads)
   const ImageLayout il(d, QP);
   unsigned char *img = p.img + (size_t)((int64_t)row * p.H + h) * p.img_stride;
   {
-    float dv[64];
+    // the TMEM row of this thread in 16-column pieces (rolled loops keep the code small)
     const uint32_t taddr = tD1 + ((uint32_t)(warp * 32) << 16);
-#pragma unroll
-    for (int c0 = 0; c0 < 64; c0 += 16) tmem_ld16(taddr + c0, dv + c0);
     const int r = tid;
     if (r < kChunk) {
       const int i = r;
-      for (int j = 0; j < kChunk; ++j)
-        A[i * kLd + j] = (j < i && i < len) ? bt[i] * exp2f(G2[i] - G2[j]) * rk[i] * rk[j] * dv[j] : 0.f;
+      const bool rowlive = i < len;
+      const float gi = G2[i], si = bt[i] * rk[i];
+#pragma unroll 1
+      for (int c0 = 0; c0 < kChunk; c0 += 16) {
+        float dv[16];
+        tmem_ld16(taddr + c0, dv);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const int j = c0 + u;
+          A[i * kLd + j] = (j < i && rowlive) ? si * exp2f(gi - G2[j]) * rk[j] * dv[u] : 0.f;
+        }
+      }
     } else {
       const int qi = r - kChunk;
-      if (qi < QP) {
-        const int pr = p0 + qi * M;
-        const bool live = qi < nq;
-        const float qscale = live ? p.scale * exp2f(G2[pr] - shift) * rq[qi] : 0.f;
-        const float sc = live ? p.scale * rq[qi] : 0.f;
-        for (int s0 = 0; s0 < kChunk; s0 += 4) {
-          float4 o4;
-          float *o = &o4.x;
+      const int pr = p0 + qi * M;
+      const bool live = qi < nq;
+      const float gp = live ? G2[pr] : 0.f;
+      const float qscale = live ? p.scale * exp2f(gp - shift) * rq[qi] : 0.f;
+      const float sc = live ? p.scale * rq[qi] : 0.f;
+#pragma unroll 1
+      for (int c0 = 0; c0 < kChunk; c0 += 16) {
+        float dv[16];
+        tmem_ld16(taddr + c0, dv);
+        if (qi < QP) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int s = s0 + u;
-            o[u] = (live && s <= pr) ? sc * exp2f(G2[pr] - G2[s]) * rk[s] * dv[s] : 0.f;
+          for (int u4 = 0; u4 < 16; u4 += 4) {
+            float4 o4;
+            float *o = &o4.x;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int s_ = c0 + u4 + u;
+              o[u] = (live && s_ <= pr) ? sc * exp2f(gp - G2[s_]) * rk[s_] * dv[u4 + u] : 0.f;
+            }
+            *reinterpret_cast<float4 *>(img + il.pm(d, qi, c0 + u4)) = o4;
           }
-          *reinterpret_cast<float4 *>(img + il.pm(d, qi, s0)) = o4;
         }
+      }
+      if (qi < QP) {
+#pragma unroll 1
         for (int f0 = 0; f0 < d; f0 += 8) {
           float x[8];
           bf16x8_at(kq, 128, r, f0, x);
-#pragma unroll
-          for (int hh = 0; hh < 8; hh += 4) {
-            const int f = f0 + hh;
-            *reinterpret_cast<float4 *>(img + il.qh(qi, f)) =
-                make_float4(qscale * x[hh], qscale * x[hh + 1], qscale * x[hh + 2], qscale * x[hh + 3]);
-          }
+          *reinterpret_cast<float4 *>(img + il.qh(qi, f0)) =
+              make_float4(qscale * x[0], qscale * x[1], qscale * x[2], qscale * x[3]);
+          *reinterpret_cast<float4 *>(img + il.qh(qi, f0 + 4)) =
+              make_float4(qscale * x[4], qscale * x[5], qscale * x[6], qscale * x[7]);
         }
       }
     }
@@ -323,12 +346,8 @@ __global__ void __launch_bounds__(kWyThreads)
     if ((j >> 4) > (i >> 4)) Tm[i * kLdT + j] = 0.f;
   }
   __syncthreads();
-  // block row bi from the rows above it: T_bi,<bi = -T_bi,bi (A_bi,<bi T_<bi,<bi).  The sums
-  // run over all x < 16 bi (T[x][c] = 0 for x < c); each thread owns 4 adjacent columns,
-  // so every shared load feeds 4 independent FMAs; trip counts are compile-time.
-  inverse_block_row<1>(A, Tm, Y, tid);
-  inverse_block_row<2>(A, Tm, Y, tid);
-  inverse_block_row<3>(A, Tm, Y, tid);
+  // off-diagonal blocks by block diagonals: level L needs only the levels below it
+  for (int L = 1; L < 4; ++L) inverse_level(A, Tm, Y, tid, L);
 
   // ---- T diag(beta gamma rk) and T diag(beta) as hi + lo bf16, K-major swizzled [64 s][64 j] ----
   for (int it = tid; it < kChunk * 8; it += kWyThreads) {  // (row s, 8 consecutive j)
