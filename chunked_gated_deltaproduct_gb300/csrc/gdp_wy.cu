@@ -39,11 +39,10 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kWyThreads = 128;
+constexpr int kWyThreads = 256;  // 8 warps: two per TMEM lane quadrant, splitting the columns
 constexpr int kLd = kChunk + 1;   // row stride of the fp32 A scratch (conflict-free row reads)
 constexpr int kLdT = kChunk + 4;  // row stride of T (16-byte aligned rows for float4 access)
 constexpr int kLdY = 20;          // row stride of the [3 pairs x 16][16] block-product scratch
-constexpr int kTile = 32 * 68;    // per-warp transpose tile (floats); reuses the A / T / Y region
 
 struct WyLayout {
   uint32_t kq, vt, twh, twl, tuh, tul, A, T, Y, scal, total;
@@ -69,7 +68,6 @@ struct WyLayout {
     total = scal + 4u * 7 * kChunk;
   }
 };
-static_assert(4 * 64 * (65 + 68) + 4 * 48 * kLdY >= 4 * 4 * kTile, "transpose tiles must fit the A/T/Y region");
 
 // Off-diagonal 16 x 16 blocks of T = (I + A)^-1 for block pairs (i, j), i - j = L: first
 // Y_ij = sum_{k=j}^{i-1} A_ik T_kj over the 16 L columns x of A's block row, then
@@ -127,7 +125,7 @@ __device__ __forceinline__ void bf16x8_at(const unsigned char *tile, int rows_pe
   }
 }
 
-__global__ void __launch_bounds__(kWyThreads)
+__global__ void __launch_bounds__(kWyThreads, 2)
     gdp_wy_kernel(Problem p, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_v) {
   const int row = blockIdx.x, h = blockIdx.y;
@@ -145,6 +143,7 @@ __global__ void __launch_bounds__(kWyThreads)
   const int nq = (p0 < len) ? (len - 1 - p0) / M + 1 : 0;
   const int64_t tq0 = (R0 + p0) / M;             // token of the first readout row; readout qi is tq0 + qi
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3, chalf = warp >> 2;  // TMEM lane quadrant, column half of this warp
 
   extern __shared__ __align__(1024) unsigned char wy_smem_raw[];
   unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)wy_smem_raw + 1023) & ~(uintptr_t)1023);
@@ -213,16 +212,22 @@ __global__ void __launch_bounds__(kWyThreads)
 
   // ---- per-row scalars: beta, decay gate, inverse norms; base-2 cumsum ----
   {
-    const int r = tid;  // rows 0..63 keys, 64..127 query rows
+    const int r = tid & 127;  // rows 0..63 keys, 64..127 query rows; threads 128.. take the upper features
     float ss = 0.f;
-    if (p.l2norm)
-      for (int f0 = 0; f0 < d; f0 += 8) {
+    if (p.l2norm) {
+#pragma unroll 1
+      for (int f0 = chalf * (d / 2); f0 < (chalf + 1) * (d / 2); f0 += 8) {
         float x[8];
         bf16x8_at(kq, 128, r, f0, x);
 #pragma unroll
         for (int i = 0; i < 8; ++i) ss += x[i] * x[i];
       }
-    if (r < kChunk) {
+      if (chalf) Y[r] = ss;  // the Y scratch is free until the inverse
+      __syncthreads();
+      if (!chalf) ss += Y[r];
+    }
+    if (chalf) {
+    } else if (r < kChunk) {
       const int64_t gr = R0 + r;
       const int pos = r0m + r;
       float b = 0.f, gate = 0.f;
@@ -269,15 +274,16 @@ __global__ void __launch_bounds__(kWyThreads)
   const ImageLayout il(d, QP);
   unsigned char *img = p.img + (size_t)((int64_t)row * p.H + h) * p.img_stride;
   {
-    // the TMEM row of this thread in 16-column pieces (rolled loops keep the code small)
-    const uint32_t taddr = tD1 + ((uint32_t)(warp * 32) << 16);
-    const int r = tid;
+    // the TMEM row of this thread, this warp's half of the columns, in 16-column pieces
+    const uint32_t taddr = tD1 + ((uint32_t)(quad * 32) << 16);
+    const int r = quad * 32 + lane;
+    const int cbeg = chalf * 32;
     if (r < kChunk) {
       const int i = r;
       const bool rowlive = i < len;
       const float gi = G2[i], si = bt[i] * rk[i];
 #pragma unroll 1
-      for (int c0 = 0; c0 < kChunk; c0 += 16) {
+      for (int c0 = cbeg; c0 < cbeg + 32; c0 += 16) {
         float dv[16];
         tmem_ld16(taddr + c0, dv);
 #pragma unroll
@@ -294,7 +300,7 @@ __global__ void __launch_bounds__(kWyThreads)
       const float qscale = live ? p.scale * exp2f(gp - shift) * rq[qi] : 0.f;
       const float sc = live ? p.scale * rq[qi] : 0.f;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kChunk; c0 += 16) {
+      for (int c0 = cbeg; c0 < cbeg + 32; c0 += 16) {
         float dv[16];
         tmem_ld16(taddr + c0, dv);
         if (qi < QP) {
@@ -313,7 +319,7 @@ __global__ void __launch_bounds__(kWyThreads)
       }
       if (qi < QP) {
 #pragma unroll 1
-        for (int f0 = 0; f0 < d; f0 += 8) {
+        for (int f0 = chalf * (d / 2); f0 < (chalf + 1) * (d / 2); f0 += 8) {
           float x[8];
           bf16x8_at(kq, 128, r, f0, x);
           *reinterpret_cast<float4 *>(img + il.qh(qi, f0)) =
@@ -327,7 +333,7 @@ __global__ void __launch_bounds__(kWyThreads)
   __syncthreads();
 
   // ---- T = (I + A)^-1: diagonal 16x16 blocks by forward substitution (warp w: block w) ----
-  if (lane < 16) {
+  if (warp < 4 && lane < 16) {
     const int b0 = warp * 16, cc = lane;
     float t[16];
 #pragma unroll
@@ -395,61 +401,42 @@ __global__ void __launch_bounds__(kWyThreads)
   tc_fence_after();
   __syncthreads();
 
-  // ---- epilogue: -W image, U^T, Ktil^T image.  Every store goes through a per-warp
-  // shared tile so that each 16-byte store instruction writes whole 128-byte lines. ----
-  {
+  // ---- epilogue: -W image, U^T, Ktil^T image; the two warps of a lane quadrant take 32
+  // columns s each.  Stores are arranged so that each warp instruction writes whole
+  // 128-byte (-W, Ktil^T) or 512-byte (U^T) contiguous segments. ----
+  const bool aborted = abort_flag;  // read after the barrier above: the same for every thread
+  if (!aborted) {
     // D row f sits in lane f (M = 128) or in lane 32*(f/16) + f%16 (M = 64).
-    const int rpw = (d == 128) ? 32 : 16;  // feature rows held by this warp
-    const int fbase = warp * rpw;
+    const int rpw = (d == 128) ? 32 : 16;  // feature rows held by this lane quadrant
+    const int f = quad * rpw + lane;
     const bool mine = lane < rpw;
-    float *tile = reinterpret_cast<float *>(sm + lay.A) + warp * kTile;
-    float wv[64], uv[64];
-    const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+    const uint32_t lrow = (uint32_t)(quad * 32) << 16;
+    const int sbeg = chalf * 32;
+    float4 *Ut = reinterpret_cast<float4 *>(p.U + ((int64_t)row * p.H + h) * p.V * kChunk) + (f >> 5) * 512 + (f & 31);
+    unsigned char *wimg = img + il.b1 + (f >> 5) * il.b1_block;
+#pragma unroll 1
+    for (int c0 = sbeg; c0 < sbeg + 32; c0 += 16) {
+      float wv[16], uv[16];
+      tmem_ld16(tW + lrow + c0, wv);
+      tmem_ld16(tU + lrow + c0, uv);
+      if (mine) {
+        // U^T rows in the 32-row-group layout: consecutive lanes at consecutive 16 bytes
 #pragma unroll
-    for (int c0 = 0; c0 < 64; c0 += 16) {
-      tmem_ld16(tW + lrow + c0, wv + c0);
-      tmem_ld16(tU + lrow + c0, uv + c0);
+        for (int j = 0; j < 16; j += 4) Ut[((c0 + j) >> 2) * 32] = make_float4(uv[j], uv[j + 1], uv[j + 2], uv[j + 3]);
+        // -W image: element (s, f) at row qpad + s of K-block f/32 (a row of 32 lanes = 128 bytes)
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          *reinterpret_cast<float *>(wimg + ImageLayout::swz_off(QP + c0 + u, f)) = -wv[u];
+      }
     }
-    if (!abort_flag) {
-      // U^T rows fbase .. fbase + rpw - 1 in the 32-row-group layout (one float4 per lane and
-      // store instruction, consecutive lanes at consecutive 16 bytes)
-      if (mine) {
-        const int f = fbase + lane;
-        float4 *Ut = reinterpret_cast<float4 *>(p.U + ((int64_t)row * p.H + h) * p.V * kChunk) + (f >> 5) * 512 + (f & 31);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) Ut[j * 32] = make_float4(uv[4 * j], uv[4 * j + 1], uv[4 * j + 2], uv[4 * j + 3]);
-      }
-      // -W image: element (s, f) at row qpad + s of K-block f/32; two halves of 32 rows s
-      const int kb = fbase >> 5, ch0 = (fbase & 31) >> 2, nch = rpw >> 2;
-      for (int half = 0; half < 2; ++half) {
-        if (mine) {
-#pragma unroll
-          for (int s2 = 0; s2 < 32; ++s2) tile[s2 * 36 + lane] = -wv[half * 32 + s2];
-        }
-        __syncwarp();
-        for (int c = lane; c < 32 * nch; c += 32) {
-          const int srow = half * 32 + c / nch, ch = c % nch;
-          *reinterpret_cast<float4 *>(img + il.b1 + kb * il.b1_block + ImageLayout::swz_off(QP + srow, (ch0 + ch) * 4)) =
-              *reinterpret_cast<const float4 *>(tile + (c / nch) * 36 + ch * 4);
-        }
-        __syncwarp();
-      }
-      // Ktil^T image: row f = 2^(G2_last - G2_s) rk_s k[s][f] over s, K-blocks of 32 s
-      if (mine) {
-        const int f = fbase + lane;
+    // Ktil^T image: row f = 2^(G2_last - G2_s) rk_s k[s][f], K-block s/32; lane = s, so each
+    // store instruction writes one 128-byte row segment; this warp takes rows f of its quadrant
+    const int s_ = sbeg + lane;
+    const float kss = ks[s_];
+    unsigned char *kimg = img + il.b2 + chalf * il.b2_block;
 #pragma unroll 4
-        for (int s0 = 0; s0 < kChunk; s0 += 4)
-          *reinterpret_cast<float4 *>(tile + lane * 68 + s0) =
-              make_float4(ks[s0] * bf16_at(kq, 128, s0, f), ks[s0 + 1] * bf16_at(kq, 128, s0 + 1, f),
-                          ks[s0 + 2] * bf16_at(kq, 128, s0 + 2, f), ks[s0 + 3] * bf16_at(kq, 128, s0 + 3, f));
-      }
-      __syncwarp();
-      for (int c = lane; c < rpw * 16; c += 32) {
-        const int r = c >> 4, q = c & 15;  // q: 16-byte chunk of the 64 s values
-        *reinterpret_cast<float4 *>(img + il.b2 + (q >> 3) * il.b2_block + ImageLayout::swz_off(fbase + r, (q & 7) * 4)) =
-            *reinterpret_cast<const float4 *>(tile + r * 68 + q * 4);
-      }
-    }
+    for (int fr = quad * (d / 4); fr < (quad + 1) * (d / 4); ++fr)
+      *reinterpret_cast<float *>(kimg + ImageLayout::swz_off(fr, s_)) = kss * bf16_at(kq, 128, s_, fr);
   }
   if (tid == 0) {
     ImageMeta *mt = reinterpret_cast<ImageMeta *>(img + il.meta);
