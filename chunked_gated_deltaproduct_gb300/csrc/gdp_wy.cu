@@ -26,9 +26,11 @@
 //   W^T = K^T (T diag(beta gamma rk))^T, U^T = V^T (T diag(beta))^T : kind::f16,
 //                 M = d, N = 64, K = 64, with T split as hi + lo bf16 (two MMAs
 //                 each) so that T keeps ~16 significant bits.
-// The inverse of the unit lower-triangular I + A runs on the CUDA cores in
-// 16 x 16 blocks: the four diagonal blocks by forward substitution (one warp
-// each), then T_ij = -T_ii sum_k A_ik T_kj for the off-diagonal blocks.
+// The inverse of the unit lower-triangular I + A runs in 16 x 16 blocks: the four
+// diagonal blocks by forward substitution on the CUDA cores (one warp each), then
+// T_ij = -T_ii sum_k A_ik T_kj for the off-diagonal blocks, block diagonal by block
+// diagonal, with warp-level tf32 MMAs in the 3xTF32 split (fp32-level accuracy; these
+// 16 x 16 products are far below the tcgen05 tile size).
 #include <cuda.h>  // CUtensorMap
 
 #include "gdp_internal.cuh"
@@ -69,41 +71,71 @@ struct WyLayout {
   }
 };
 
+// 3xTF32 warp-level products for the 16 x 16 blocks of the inverse: x = hi + lo with hi, lo
+// tf32 (round to nearest), and hi*hi + hi*lo + lo*hi keeps ~fp32 accuracy (lo*lo dropped).
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void tf32_split(float x, uint32_t &hi, uint32_t &lo) {
+  hi = tf32_rna(x);
+  lo = tf32_rna(x - __uint_as_float(hi));
+}
+__device__ __forceinline__ void mma_m16n8k8_tf32(float *c, const uint32_t *a, const uint32_t *b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+// c += X (16 x 8, row stride lx) * Z (8 x 8, row stride lz) with the fragment layout of
+// m16n8k8 (lane = 4 g + t): X rows g, g+8 and columns t, t+4; Z rows t, t+4 and column g.
+__device__ __forceinline__ void mma3_16x8x8(float *c, const float *X, int lx, const float *Z, int lz, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  uint32_t ah[4], al[4], bh[2], bl[2];
+  tf32_split(X[g * lx + t], ah[0], al[0]);
+  tf32_split(X[(g + 8) * lx + t], ah[1], al[1]);
+  tf32_split(X[g * lx + t + 4], ah[2], al[2]);
+  tf32_split(X[(g + 8) * lx + t + 4], ah[3], al[3]);
+  tf32_split(Z[t * lz + g], bh[0], bl[0]);
+  tf32_split(Z[(t + 4) * lz + g], bh[1], bl[1]);
+  mma_m16n8k8_tf32(c, al, bh);
+  mma_m16n8k8_tf32(c, ah, bl);
+  mma_m16n8k8_tf32(c, ah, bh);
+}
+
 // Off-diagonal 16 x 16 blocks of T = (I + A)^-1 for block pairs (i, j), i - j = L: first
-// Y_ij = sum_{k=j}^{i-1} A_ik T_kj over the 16 L columns x of A's block row, then
-// T_ij = -T_ii Y_ij.  The 4 - L pairs of a level are independent; each thread owns 4 adjacent
-// columns of one row of one pair, so every shared load feeds 4 independent FMAs.
-__device__ __forceinline__ void inverse_level(const float *A, float *Tm, float *Y, int tid, int L) {
-  const int items = (4 - L) * 64;
+// Y_ij = sum_{k=j}^{i-1} A_ik T_kj over the 16 L columns of A's block row, then
+// T_ij = -T_ii Y_ij.  The 4 - L pairs of a level are independent; a warp takes one
+// (pair, 8-column half) unit at a time with warp-level tf32 MMAs (3xTF32).
+__device__ __forceinline__ void inverse_level(const float *A, float *Tm, float *Y, int warp, int lane, int L) {
+  constexpr int kWarps = kWyThreads / 32;
+  const int g = lane >> 2, t = lane & 3;
+  const int units = (4 - L) * 2;
+  for (int u = warp; u < units; u += kWarps) {
+    const int pr = u >> 1, nh = u & 1, i = pr + L, j = pr;
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
-  for (int it = tid; it < items; it += kWyThreads) {
-    const int pr = it >> 6, r = (it >> 2) & 15, c = (it & 3) * 4;
-    const int i = pr + L, j = pr;
-    const float *arow = A + (16 * i + r) * kLd;
-    const float *tcol = Tm + 16 * j + c;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int x = 16 * j; x < 16 * i; ++x) {
-      const float a = arow[x];
-      const float4 t = *reinterpret_cast<const float4 *>(tcol + x * kLdT);
-      acc.x += a * t.x; acc.y += a * t.y; acc.z += a * t.z; acc.w += a * t.w;
-    }
-    *reinterpret_cast<float4 *>(Y + (pr * 16 + r) * kLdY + c) = acc;
+    for (int ks = 0; ks < 2 * L; ++ks)
+      mma3_16x8x8(c, A + (16 * i) * kLd + 16 * j + 8 * ks, kLd, Tm + (16 * j + 8 * ks) * kLdT + 16 * j + 8 * nh, kLdT,
+                  lane);
+    float *y = Y + (pr * 16) * kLdY + 8 * nh;
+    y[g * kLdY + 2 * t] = c[0];
+    y[g * kLdY + 2 * t + 1] = c[1];
+    y[(g + 8) * kLdY + 2 * t] = c[2];
+    y[(g + 8) * kLdY + 2 * t + 1] = c[3];
   }
   __syncthreads();
-#pragma unroll 1
-  for (int it = tid; it < items; it += kWyThreads) {
-    const int pr = it >> 6, r = (it >> 2) & 15, c = (it & 3) * 4;
-    const int i = pr + L, j = pr;
-    const float *trow = Tm + (16 * i + r) * kLdT + 16 * i;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int m = 0; m <= r; ++m) {
-      const float t = trow[m];
-      const float4 y = *reinterpret_cast<const float4 *>(Y + (pr * 16 + m) * kLdY + c);
-      acc.x += t * y.x; acc.y += t * y.y; acc.z += t * y.z; acc.w += t * y.w;
-    }
-    *reinterpret_cast<float4 *>(Tm + (16 * i + r) * kLdT + 16 * j + c) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+  for (int u = warp; u < units; u += kWarps) {
+    const int pr = u >> 1, nh = u & 1, i = pr + L, j = pr;
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    mma3_16x8x8(c, Tm + (16 * i) * kLdT + 16 * i, kLdT, Y + (pr * 16) * kLdY + 8 * nh, kLdY, lane);
+    mma3_16x8x8(c, Tm + (16 * i) * kLdT + 16 * i + 8, kLdT, Y + (pr * 16 + 8) * kLdY + 8 * nh, kLdY, lane);
+    float *o = Tm + (16 * i) * kLdT + 16 * j + 8 * nh;
+    o[g * kLdT + 2 * t] = -c[0];
+    o[g * kLdT + 2 * t + 1] = -c[1];
+    o[(g + 8) * kLdT + 2 * t] = -c[2];
+    o[(g + 8) * kLdT + 2 * t + 1] = -c[3];
   }
   __syncthreads();
 }
@@ -353,7 +385,7 @@ __global__ void __launch_bounds__(kWyThreads, 2)
   }
   __syncthreads();
   // off-diagonal blocks by block diagonals: level L needs only the levels below it
-  for (int L = 1; L < 4; ++L) inverse_level(A, Tm, Y, tid, L);
+  for (int L = 1; L < 4; ++L) inverse_level(A, Tm, Y, warp, lane, L);
 
   // ---- T diag(beta gamma rk) and T diag(beta) as hi + lo bf16, K-major swizzled [64 s][64 j] ----
   for (int it = tid; it < kChunk * 8; it += kWyThreads) {  // (row s, 8 consecutive j)
