@@ -213,6 +213,14 @@ __global__ void __launch_bounds__(kWyThreads, 2)
       tma_load_3d(vt + kb * 8192u, &tm_v, kb * 64, h, (int)R0, &ld_bar);
     }
   }
+  // per-row beta and decay gate (the decay of token t sits on its first expanded row t*M),
+  // fetched while the tiles land
+  float b_r = 0.f, gate_r = 0.f;
+  if (tid < kChunk && tid < len) {
+    const int pos = r0m + tid;
+    b_r = p.beta ? p.beta[(R0 + tid) * p.H + h] : 1.f;
+    if (p.g && pos % M == 0) gate_r = p.g[(tok0 + pos / M) * p.H + h];
+  }
   if (!mbar_wait(&ld_bar, 0)) abort_flag = 1;
   {
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
@@ -260,14 +268,8 @@ __global__ void __launch_bounds__(kWyThreads, 2)
     }
     if (chalf) {
     } else if (r < kChunk) {
-      const int64_t gr = R0 + r;
-      const int pos = r0m + r;
-      float b = 0.f, gate = 0.f;
-      if (r < len) {
-        b = p.beta ? p.beta[gr * p.H + h] : 1.f;
-        if (p.g && pos % M == 0) gate = p.g[(tok0 + pos / M) * p.H + h];
-      }
-      bt[r] = b;
+      const float gate = gate_r;
+      bt[r] = b_r;
       rk[r] = p.l2norm ? rsqrtf(ss + kL2Eps) : 1.f;
       // inclusive scan of the gates over the 64 rows (two warps)
       float x = gate;
@@ -364,24 +366,40 @@ __global__ void __launch_bounds__(kWyThreads, 2)
   }
   __syncthreads();
 
-  // ---- T = (I + A)^-1: diagonal 16x16 blocks by forward substitution (warp w: block w) ----
-  if (warp < 4 && lane < 16) {
-    const int b0 = warp * 16, cc = lane;
-    float t[16];
+  // ---- T = (I + A)^-1.  Diagonal 16x16 blocks from 8x8 halves: forward substitution on the
+  // eight 8x8 diagonal blocks (a thread per column), then T_21 = -T_22 A_21 T_11 inside each
+  // 16x16 block; every block above its block diagonal is zero ----
+  if (tid < kChunk) {
+    const int b0 = (tid >> 3) * 8, cc = tid & 7;
+    float t[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 8; ++i) {
       float acc = 0.f;
 #pragma unroll
       for (int j = 0; j < i; ++j) acc += A[(b0 + i) * kLd + b0 + j] * t[j];
       t[i] = (i == cc) ? 1.f : (i < cc ? 0.f : -acc);
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) Tm[(b0 + i) * kLdT + b0 + cc] = t[i];
+    for (int i = 0; i < 8; ++i) Tm[(b0 + i) * kLdT + b0 + cc] = t[i];
   }
-  // zero the strictly upper blocks
+#pragma unroll 1
   for (int idx = tid; idx < kChunk * kChunk; idx += kWyThreads) {
     const int i = idx / kChunk, j = idx % kChunk;
-    if ((j >> 4) > (i >> 4)) Tm[i * kLdT + j] = 0.f;
+    if ((j >> 3) > (i >> 3)) Tm[i * kLdT + j] = 0.f;
+  }
+  __syncthreads();
+  {
+    // thread: block b = tid / 64 (rows 16b+8.., columns 16b..), element (r, c) of the 8x8 block
+    const int b = tid >> 6, r = (tid >> 3) & 7, cc = tid & 7, r0 = 16 * b + 8, c0 = 16 * b;
+    float acc = 0.f;  // (A_21 T_11)[r][cc]
+#pragma unroll
+    for (int x = 0; x < 8; ++x) acc += A[(r0 + r) * kLd + c0 + x] * Tm[(c0 + x) * kLdT + c0 + cc];
+    Y[tid] = acc;
+    __syncthreads();
+    float o = 0.f;  // (T_22 Y)[r][cc], T_22 lower triangular
+#pragma unroll
+    for (int m = 0; m < 8; ++m) o += (m <= r ? Tm[(r0 + r) * kLdT + r0 + m] : 0.f) * Y[(tid & ~63) + m * 8 + cc];
+    Tm[(r0 + r) * kLdT + c0 + cc] = -o;
   }
   __syncthreads();
   // off-diagonal blocks by block diagonals: level L needs only the levels below it
