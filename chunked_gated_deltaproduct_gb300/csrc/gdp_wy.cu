@@ -28,9 +28,9 @@
 //                 each) so that T keeps ~16 significant bits.
 // The inverse of the unit lower-triangular I + A runs in 16 x 16 blocks: the four
 // diagonal blocks by forward substitution on the CUDA cores (one warp each), then
-// T_ij = -T_ii sum_k A_ik T_kj for the off-diagonal blocks, block diagonal by block
-// diagonal, with warp-level tf32 MMAs in the 3xTF32 split (fp32-level accuracy; these
-// 16 x 16 products are far below the tcgen05 tile size).
+// the blocks below the diagonal by recursive doubling (T_21 = -T_22 A_21 T_11 on 16- then
+// 32-row blocks), with warp-level tf32 MMAs in the 3xTF32 split (fp32-level accuracy; these
+// 16 x 16 and 32 x 32 products are far below the tcgen05 tile size).
 #include <cuda.h>  // CUtensorMap
 
 #include "gdp_internal.cuh"
@@ -44,7 +44,7 @@ using namespace sm100;
 constexpr int kWyThreads = 256;  // 8 warps: two per TMEM lane quadrant, splitting the columns
 constexpr int kLd = kChunk + 1;   // row stride of the fp32 A scratch (conflict-free row reads)
 constexpr int kLdT = kChunk + 4;  // row stride of T (16-byte aligned rows for float4 access)
-constexpr int kLdY = 20;          // row stride of the [3 pairs x 16][16] block-product scratch
+constexpr int kLdY = 36;          // row stride of the [32][32] block-product scratch
 
 struct WyLayout {
   uint32_t kq, vt, twh, twl, tuh, tul, A, T, Y, scal, total;
@@ -65,8 +65,8 @@ struct WyLayout {
     }
     A = tul + 8192u;                       // fp32 [64][65]
     T = A + 4u * kChunk * kLd;             // fp32 [64][68]
-    Y = T + 4u * kChunk * kLdT;            // fp32 [48][20] block products
-    scal = Y + 4u * 48 * kLdY;             // G2, beta, rk, rq, wc, uc, kscale  [7][64]
+    Y = T + 4u * kChunk * kLdT;            // fp32 [32][36] block products
+    scal = Y + 4u * 32 * kLdY;             // G2, beta, rk, rq, wc, uc, kscale  [7][64]
     total = scal + 4u * 7 * kChunk;
   }
 };
@@ -104,19 +104,18 @@ __device__ __forceinline__ void mma3_16x8x8(float *c, const float *X, int lx, co
   mma_m16n8k8_tf32(c, ah, bh);
 }
 
-// Off-diagonal 16 x 16 blocks of T = (I + A)^-1 for block pairs (i, j), i - j = L: first
-// Y_ij = sum_{k=j}^{i-1} A_ik T_kj over the 16 L columns of A's block row, then
-// T_ij = -T_ii Y_ij.  The 4 - L pairs of a level are independent; a warp takes one
-// (pair, 8-column half) unit at a time with warp-level tf32 MMAs (3xTF32).
-__device__ __forceinline__ void inverse_level(const float *A, float *Tm, float *Y, int warp, int lane, int L) {
-  constexpr int kWarps = kWyThreads / 32;
+// Off-diagonal blocks of T = (I + A)^-1 by recursive doubling, given the inverted 16x16
+// diagonal blocks: first T_10 and T_32 of the two 32x32 diagonal blocks,
+// T_i,i-1 = -T_ii (A_i,i-1 T_i-1,i-1); then the 32x32 block below the diagonal,
+// T_[23][01] = -T_[23][23] (A_[23][01] T_[01][01]).  Each product is split into 16x8 units,
+// one per warp, computed with warp-level tf32 MMAs (3xTF32); Y holds the inner products.
+__device__ __forceinline__ void inverse_offdiag(const float *A, float *Tm, float *Y, int warp, int lane) {
   const int g = lane >> 2, t = lane & 3;
-  const int units = (4 - L) * 2;
-  for (int u = warp; u < units; u += kWarps) {
-    const int pr = u >> 1, nh = u & 1, i = pr + L, j = pr;
+  // level 1: units (pair p, 8-column half nh): rows 16 i, columns 16 j, i = 2 p + 1, j = 2 p
+  if (warp < 4) {
+    const int pr = warp >> 1, nh = warp & 1, i = 2 * pr + 1, j = 2 * pr;
     float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-    for (int ks = 0; ks < 2 * L; ++ks)
+    for (int ks = 0; ks < 2; ++ks)
       mma3_16x8x8(c, A + (16 * i) * kLd + 16 * j + 8 * ks, kLd, Tm + (16 * j + 8 * ks) * kLdT + 16 * j + 8 * nh, kLdT,
                   lane);
     float *y = Y + (pr * 16) * kLdY + 8 * nh;
@@ -126,12 +125,36 @@ __device__ __forceinline__ void inverse_level(const float *A, float *Tm, float *
     y[(g + 8) * kLdY + 2 * t + 1] = c[3];
   }
   __syncthreads();
-  for (int u = warp; u < units; u += kWarps) {
-    const int pr = u >> 1, nh = u & 1, i = pr + L, j = pr;
+  if (warp < 4) {
+    const int pr = warp >> 1, nh = warp & 1, i = 2 * pr + 1, j = 2 * pr;
     float c[4] = {0.f, 0.f, 0.f, 0.f};
-    mma3_16x8x8(c, Tm + (16 * i) * kLdT + 16 * i, kLdT, Y + (pr * 16) * kLdY + 8 * nh, kLdY, lane);
-    mma3_16x8x8(c, Tm + (16 * i) * kLdT + 16 * i + 8, kLdT, Y + (pr * 16 + 8) * kLdY + 8 * nh, kLdY, lane);
+    for (int ks = 0; ks < 2; ++ks)
+      mma3_16x8x8(c, Tm + (16 * i) * kLdT + 16 * i + 8 * ks, kLdT, Y + (pr * 16 + 8 * ks) * kLdY + 8 * nh, kLdY, lane);
     float *o = Tm + (16 * i) * kLdT + 16 * j + 8 * nh;
+    o[g * kLdT + 2 * t] = -c[0];
+    o[g * kLdT + 2 * t + 1] = -c[1];
+    o[(g + 8) * kLdT + 2 * t] = -c[2];
+    o[(g + 8) * kLdT + 2 * t + 1] = -c[3];
+  }
+  __syncthreads();
+  // level 2: 8 units (16-row tile mt, 8-column tile nt) of the 32x32 block, K = 32
+  const int mt = warp >> 2, nt = warp & 3;
+  {
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int ks = 0; ks < 4; ++ks)
+      mma3_16x8x8(c, A + (32 + 16 * mt) * kLd + 8 * ks, kLd, Tm + (8 * ks) * kLdT + 8 * nt, kLdT, lane);
+    float *y = Y + (16 * mt) * kLdY + 8 * nt;
+    y[g * kLdY + 2 * t] = c[0];
+    y[g * kLdY + 2 * t + 1] = c[1];
+    y[(g + 8) * kLdY + 2 * t] = c[2];
+    y[(g + 8) * kLdY + 2 * t + 1] = c[3];
+  }
+  __syncthreads();
+  {
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int ks = 0; ks < 4; ++ks)
+      mma3_16x8x8(c, Tm + (32 + 16 * mt) * kLdT + 32 + 8 * ks, kLdT, Y + (8 * ks) * kLdY + 8 * nt, kLdY, lane);
+    float *o = Tm + (32 + 16 * mt) * kLdT + 8 * nt;
     o[g * kLdT + 2 * t] = -c[0];
     o[g * kLdT + 2 * t + 1] = -c[1];
     o[(g + 8) * kLdT + 2 * t] = -c[2];
@@ -300,6 +323,11 @@ __global__ void __launch_bounds__(kWyThreads, 2)
     ks[tid] = (tid < len) ? exp2f(G2[len - 1] - G2[tid]) * rk[tid] : 0.f;
   }
 
+  // T starts at zero (its blocks above the diagonal stay so); the area is idle until the inverse
+#pragma unroll 1
+  for (int idx = tid; idx < kChunk * kLdT / 4; idx += kWyThreads)
+    reinterpret_cast<float4 *>(Tm)[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
+
   // ---- epilogue of [K;Q]K^T: A rows (lanes 0..63), score rows and query images (lanes 64..127) ----
   const bool ok1 = mbar_wait(&mma_bar, 0);
   if (!ok1) abort_flag = 1;
@@ -382,11 +410,6 @@ __global__ void __launch_bounds__(kWyThreads, 2)
 #pragma unroll
     for (int i = 0; i < 8; ++i) Tm[(b0 + i) * kLdT + b0 + cc] = t[i];
   }
-#pragma unroll 1
-  for (int idx = tid; idx < kChunk * kChunk; idx += kWyThreads) {
-    const int i = idx / kChunk, j = idx % kChunk;
-    if ((j >> 3) > (i >> 3)) Tm[i * kLdT + j] = 0.f;
-  }
   __syncthreads();
   {
     // thread: block b = tid / 64 (rows 16b+8.., columns 16b..), element (r, c) of the 8x8 block
@@ -402,8 +425,7 @@ __global__ void __launch_bounds__(kWyThreads, 2)
     Tm[(r0 + r) * kLdT + c0 + cc] = -o;
   }
   __syncthreads();
-  // off-diagonal blocks by block diagonals: level L needs only the levels below it
-  for (int L = 1; L < 4; ++L) inverse_level(A, Tm, Y, warp, lane, L);
+  inverse_offdiag(A, Tm, Y, warp, lane);
 
   // ---- T diag(beta gamma rk) and T diag(beta) as hi + lo bf16, K-major swizzled [64 s][64 j] ----
   for (int it = tid; it < kChunk * 8; it += kWyThreads) {  // (row s, 8 consecutive j)
