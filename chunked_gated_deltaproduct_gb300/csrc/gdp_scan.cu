@@ -251,12 +251,9 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       const uint32_t to = tO(b), ty = to + (uint32_t)QP;
       const float inv = 1.f / gam_next;
 #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 16) {
-        float x[16];
-#pragma unroll
-        for (int w = 0; w < 16; ++w) x[w] = u[c0 + w] * inv;
-        tmem_st16(ty + lrow + c0, x);
-      }
+      for (int w = 0; w < 64; ++w) u[w] *= inv;  // u is reloaded for the next chunk below
+      tmem_st32x(ty + lrow, u);
+      tmem_st32x(ty + lrow + 32, u + 32);
       {
         float z[16];
 #pragma unroll
@@ -291,21 +288,19 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         if (emit && n_emit >= 1 && !mbar_wait_or_abort(&bk_free, (uint32_t)((n_emit - 1) & 1), &abort_flag)) break;
         if (!fast && !mbar_wait_or_abort(&b1_done[b], (uint32_t)((e >> 1) & 1), &abort_flag)) break;
         tc_fence_after();
+        // (a slow chunk was renormalised, so gam_pass is 1 there and one array serves both)
         for (int c0 = 0; c0 < d; c0 += 32) {
           float x[32];
-          tmem_ld32(tS + lrow + c0, x);
+          tmem_ld32x(tS + lrow + c0, x);
           if (emit) {
-            float y[32];
 #pragma unroll
-            for (int w = 0; w < 32; ++w) y[w] = x[w] * gam_pass;
-            tmem_st16(tBk + lrow + c0, y);
-            tmem_st16(tBk + lrow + c0 + 16, y + 16);
+            for (int w = 0; w < 32; ++w) x[w] *= gam_pass;
+            tmem_st32x(tBk + lrow + c0, x);
           }
           if (!fast) {
 #pragma unroll
             for (int w = 0; w < 32; ++w) x[w] *= mt.gamma_last;
-            tmem_st16(tS + lrow + c0, x);
-            tmem_st16(tS + lrow + c0 + 16, x + 16);
+            tmem_st32x(tS + lrow + c0, x);
           }
         }
         tmem_st_wait();
