@@ -3,6 +3,7 @@
 // reads device memory, so a call can be captured in a CUDA graph (Megatron-Core
 // API page "core.ssm.ops.gdp.chunk", closing paragraph).
 #include <math.h>
+#include <stdint.h>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -31,9 +32,18 @@ int64_t ntdp_bound(int64_t T, int64_t N, int M) {
   return ((int64_t)M * T + (int64_t)(gdp::kChunk - 1) * N) / gdp::kChunk;
 }
 
+// Number of chunk segments the call runs in (shape-only, see gdp::kSegChunks): more than
+// one only for few (sequence, head) chains and long sequences.
+int seg_count(int64_t T, int64_t N, int H, int M) {
+  if (N * (int64_t)H > gdp::kSegMaxChains) return 1;
+  const int64_t maxc = ((int64_t)M * T + gdp::kChunk - 1) / gdp::kChunk;  // chunks of the longest sequence
+  if (maxc < 3 * gdp::kSegChunks) return 1;
+  return (int)min((maxc + gdp::kSegChunks - 1) / gdp::kSegChunks, (int64_t)gdp::kSegMax);
+}
+
 // Workspace layout; identical for the size query and the carving.
 struct Layout {
-  size_t cod, ci, cid, co, img, img_stride, U, total;
+  size_t cod, ci, cid, co, img, img_stride, U, seg, total;
 };
 
 Layout layout_for(int64_t T, int64_t N, int H, int K, int V, int M) {
@@ -54,6 +64,7 @@ Layout layout_for(int64_t T, int64_t N, int H, int K, int V, int M) {
   l.img_stride = align_up(gdp::ImageLayout(K, qp).bytes);
   l.img = take(l.img_stride * tiles);
   l.U = take(sizeof(float) * tiles * gdp::kChunk * (size_t)V);
+  l.seg = seg_count(T, N, H, M) > 1 ? take(sizeof(float) * (size_t)N * H * (size_t)V * K) : 0;
   l.total = off;
   return l;
 }
@@ -67,6 +78,31 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
   if (!a || !b || na == 0 || nb == 0) return false;
   uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
   return x < y + nb && y < x + na;
+}
+
+// Internal streams of the segmented mode, per host thread and device: WY tiles on a
+// low-priority stream, scan segments on a high-priority one, joined to the caller's stream
+// with events (so a call still captures into one CUDA graph).
+struct SideStreams {
+  bool ok = false;
+  cudaStream_t wy = nullptr, scan = nullptr;
+  cudaEvent_t ev[gdp::kSegMax + 2] = {};
+};
+SideStreams *side_streams() {
+  constexpr int kMaxDev = 16;
+  thread_local SideStreams cache[kMaxDev];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
+  SideStreams &s = cache[dev];
+  if (s.ok) return &s;
+  int least = 0, greatest = 0;
+  if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return nullptr;
+  if (cudaStreamCreateWithPriority(&s.wy, cudaStreamNonBlocking, least) != cudaSuccess) return nullptr;
+  if (cudaStreamCreateWithPriority(&s.scan, cudaStreamNonBlocking, greatest) != cudaSuccess) return nullptr;
+  for (auto &e : s.ev)
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+  s.ok = true;
+  return &s;
 }
 
 gdp_status record(cudaEvent_t ev, cudaStream_t stream) {
@@ -177,6 +213,13 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
   p.U = (float *)(ws + lay.U);
   p.status = a->device_status;
   p.qpad = gdp::qpad_for(M);
+  p.seg_lo = 0;
+  p.seg_hi = INT64_MAX;
+  p.seg_rows = 0;
+  p.seg_state = nullptr;
+  const int nseg = seg_count(T, N, H, M);
+  SideStreams *ss = nseg > 1 ? side_streams() : nullptr;
+  if (nseg > 1 && !ss) return fail(GDP_ERR_CUDA, "could not create the internal streams of the segmented mode");
 
   cudaError_t e;
   if (nprebuilt == 3)  // only the internal expanded-stream offsets
@@ -187,11 +230,46 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
                                 (int32_t *)p.co, (int32_t *)p.cod, p.status, stream);
   if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "descriptor kernel: %s", cudaGetErrorString(e));
   if (ev && (st = record(ev[1], stream)) != GDP_OK) return st;
-  e = gdp::launch_wy(p, stream);
-  if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "WY kernel: %s", cudaGetErrorString(e));
-  if (ev && (st = record(ev[2], stream)) != GDP_OK) return st;
-  e = gdp::launch_scan(p, stream);
-  if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "scan kernel: %s", cudaGetErrorString(e));
+  if (nseg == 1) {
+    e = gdp::launch_wy(p, stream);
+    if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "WY kernel: %s", cudaGetErrorString(e));
+    if (ev && (st = record(ev[2], stream)) != GDP_OK) return st;
+    e = gdp::launch_scan(p, stream);
+    if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "scan kernel: %s", cudaGetErrorString(e));
+    if (ev && (st = record(ev[3], stream)) != GDP_OK) return st;
+    return GDP_OK;
+  }
+  // Segmented: WY(k + 1) on the low-priority stream runs beside scan(k) on the high-priority
+  // one; scan(k) waits for WY(k) by event, and the state crosses segments through seg_state.
+  const int64_t maxc = ((int64_t)M * T + gdp::kChunk - 1) / gdp::kChunk;
+  const int64_t S = (maxc + nseg - 1) / nseg;
+  p.seg_state = (float *)(ws + lay.seg);
+  p.seg_rows = (int)S;
+  auto cuda_fail = [](const char *what, cudaError_t err) {
+    return fail(GDP_ERR_CUDA, "%s: %s", what, cudaGetErrorString(err));
+  };
+  if ((e = cudaEventRecord(ss->ev[0], stream)) != cudaSuccess) return cuda_fail("fork", e);
+  if ((e = cudaStreamWaitEvent(ss->wy, ss->ev[0], 0)) != cudaSuccess) return cuda_fail("fork", e);
+  if ((e = cudaStreamWaitEvent(ss->scan, ss->ev[0], 0)) != cudaSuccess) return cuda_fail("fork", e);
+  for (int k = 0; k <= nseg; ++k) {
+    if (k < nseg) {  // WY tiles of segment k
+      gdp::Problem q = p;
+      q.seg_lo = k * S;
+      q.seg_hi = (k + 1) * S;
+      if ((e = gdp::launch_wy(q, ss->wy)) != cudaSuccess) return cuda_fail("WY kernel", e);
+      if ((e = cudaEventRecord(ss->ev[1 + k], ss->wy)) != cudaSuccess) return cuda_fail("event", e);
+    }
+    if (k > 0) {  // scan of segment k - 1, once its tiles exist
+      gdp::Problem q = p;
+      q.seg_lo = (k - 1) * S;
+      q.seg_hi = (k == nseg) ? INT64_MAX : k * S;
+      if ((e = cudaStreamWaitEvent(ss->scan, ss->ev[k], 0)) != cudaSuccess) return cuda_fail("event", e);
+      if (k == 1 && ev && (st = record(ev[2], ss->scan)) != GDP_OK) return st;
+      if ((e = gdp::launch_scan(q, ss->scan)) != cudaSuccess) return cuda_fail("scan kernel", e);
+    }
+  }
+  if ((e = cudaEventRecord(ss->ev[nseg + 1], ss->scan)) != cudaSuccess) return cuda_fail("join", e);
+  if ((e = cudaStreamWaitEvent(stream, ss->ev[nseg + 1], 0)) != cudaSuccess) return cuda_fail("join", e);
   if (ev && (st = record(ev[3], stream)) != GDP_OK) return st;
   return GDP_OK;
 }

@@ -103,7 +103,20 @@ struct Problem {
   float *U;
   uint32_t *status;
   int qpad;
+  // Chunk segment of this launch: expanded chunks [seg_lo, seg_hi) of every sequence (the
+  // whole sequence is [0, INT64_MAX)).  seg_rows > 0: the WY grid is N x seg_rows tiles
+  // of the segment.  seg_state: [N][H][V][K] fp32 state carried from one segment to the next.
+  int64_t seg_lo, seg_hi;
+  int seg_rows;
+  float *seg_state;
 };
+
+// Long sequences over few (sequence, head) chains are processed in segments of
+// kSegChunks expanded chunks, so that the WY tiles of segment k + 1 are built on the
+// SMs the scan of segment k leaves free (stream-level overlap, no cross-kernel waits).
+constexpr int64_t kSegChunks = 128;
+constexpr int64_t kSegMaxChains = 64;
+constexpr int kSegMax = 64;
 
 __device__ __forceinline__ int64_t load_cu(const void *cu, int cu64, int64_t i) {
   return cu64 ? reinterpret_cast<const int64_t *>(cu)[i] : (int64_t) reinterpret_cast<const int32_t *>(cu)[i];

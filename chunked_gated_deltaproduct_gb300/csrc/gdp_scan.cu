@@ -105,7 +105,8 @@ struct ChunkInfo {
 };
 
 __global__ void __launch_bounds__(kScanThreads, 1)
-    gdp_scan_kernel(Problem p, const __grid_constant__ CUtensorMap tm_cs, const __grid_constant__ CUtensorMap tm_fin) {
+    gdp_scan_kernel(Problem p, const __grid_constant__ CUtensorMap tm_cs, const __grid_constant__ CUtensorMap tm_fin,
+                    const __grid_constant__ CUtensorMap tm_seg) {
   const int seq = blockIdx.x, h = blockIdx.y;
   int64_t bos, L;
   if (!seq_bounds(p.cu, p.cu64, p.T, seq, &bos, &L)) return;  // flagged by the descriptor kernel
@@ -135,7 +136,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   if (p.cache) {
     slot = p.slots[seq];
     if (slot < -1 || slot >= p.num_slots) {
-      if (tid == 0) set_status(p.status, GDP_DEV_ERR_SLOT);
+      if (tid == 0 && p.seg_lo == 0) set_status(p.status, GDP_DEV_ERR_SLOT);
       slot = -1;
     }
     if (slot >= 0) src = p.cache + ((int64_t)slot * H + h) * (int64_t)V * d;
@@ -147,9 +148,18 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   const int64_t cod_i = p.cod[seq];
   const int64_t co_i = p.chunk_states ? (int64_t)p.co[seq] : 0;
   // chunks whose workspace tile exists (a flagged descriptor overflow truncates the sequence)
-  const int64_t nrun = (cod_i < 0) ? 0 : max((int64_t)0, min(nchunks, p.ws_rows - cod_i));
+  const int64_t nall = (cod_i < 0) ? 0 : max((int64_t)0, min(nchunks, p.ws_rows - cod_i));
+  // this launch's chunks: global chunk e0 + e for local e in [0, nrun)
+  const int64_t e0 = min(p.seg_lo, nall);
+  const int64_t nrun = max((int64_t)0, min(p.seg_hi, nall) - e0);
+  if (p.seg_lo > 0 && nrun == 0) return;  // the sequence has no chunk in this segment
+  const bool last_seg = e0 + nrun == nall;
+  if (e0 > 0) src = p.seg_state + ((int64_t)seq * H + h) * (int64_t)V * d;  // carried from the last segment
   // token-chunk starts whose state is requested (a prefix of the chunks e % M == 0)
-  auto emits = [&](int64_t e) { return p.chunk_states && (e % M == 0) && co_i >= 0 && co_i + e / M < p.nt_pad; };
+  auto emits = [&](int64_t e) {
+    const int64_t eg = e0 + e;
+    return p.chunk_states && (eg % M == 0) && co_i >= 0 && co_i + eg / M < p.nt_pad;
+  };
 
   if (warp == 8) tmem_alloc(&tmem_slot, 512);
   if (tid == 0) {
@@ -180,7 +190,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   const uint32_t id2s = idesc(kFmtTF32, 0, 0, d, 128);       // S_hat += Y Ktil
   const uint32_t id2o = idesc(kFmtTF32, 0, 0, QP, 128);      // o_hat += Y P^T
 
-  auto image = [&](int64_t e) { return p.img + (size_t)((cod_i + e) * H + h) * p.img_stride; };
+  auto image = [&](int64_t e) { return p.img + (size_t)((cod_i + e0 + e) * H + h) * p.img_stride; };
   // producer thread: part 1 / part 2 of chunk e's image into stage e % nst (n1, n2: copies issued)
   int n1[2] = {0, 0}, n2[2] = {0, 0};
   auto load_part1 = [&](int64_t e) {
@@ -223,7 +233,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     // ---------------- prep warps ----------------
     float u[64];
     auto load_u = [&](int64_t e) {  // row v of U^T: one 512-byte segment per load instruction of the warp
-      const float4 *Ut = reinterpret_cast<const float4 *>(p.U + ((cod_i + e) * H + h) * (int64_t)V * kChunk) +
+      const float4 *Ut = reinterpret_cast<const float4 *>(p.U + ((cod_i + e0 + e) * H + h) * (int64_t)V * kChunk) +
                          (v < V ? q4 * 512 + lane : 0);
 #pragma unroll
       for (int s4 = 0; s4 < 16; ++s4) {
@@ -341,7 +351,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       tc_fence_before();
       mbar_arrive(&yo_free[b]);  // the chunk's o_hat columns have been read
       named_sync(1, 128);
-      const int64_t tq0 = (bos * M + e * kChunk + ci.p0) / M;  // readout rows are consecutive tokens
+      const int64_t tq0 = (bos * M + (e0 + e) * kChunk + ci.p0) / M;  // readout rows are consecutive tokens
       const int cpr = V / 8;                                     // 16-byte chunks per output row
       for (int c = tid - 128; c < ci.nq * cpr; c += 128) {
         const int qi = c / cpr, ch = c % cpr;
@@ -350,20 +360,24 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       }
       if (emits(e)) {  // the prep warps copied S_e before batch 2 of this chunk was issued
         if (has_rows)
-          store_state_tma(tBk + lrow, sttiles, lane, d, 1.f, &tm_cs, (int)(((co_i + e / M) * H + h) * V + q4 * 32),
-                          nblk);
+          store_state_tma(tBk + lrow, sttiles, lane, d, 1.f, &tm_cs,
+                          (int)(((co_i + (e0 + e) / M) * H + h) * V + q4 * 32), nblk);
         tc_fence_before();
         mbar_arrive(&bk_free);  // the snapshot columns have been read
       }
     }
     if (!abort_flag && has_rows) {  // the last chunk's b2_done was waited for above
       int64_t r = -1;
-      if (p.cache) {
+      const CUtensorMap *tm = &tm_fin;
+      if (!last_seg) {  // carried to the next segment
+        r = ((int64_t)seq * H + h) * V;
+        tm = &tm_seg;
+      } else if (p.cache) {
         if (slot >= 0) r = ((int64_t)slot * H + h) * V;
       } else if (p.out_state) {
         r = ((int64_t)seq * H + h) * V;
       }
-      if (r >= 0) store_state_tma(tS + lrow, sttiles, lane, d, gam_fin, &tm_fin, (int)(r + q4 * 32), nblk);
+      if (r >= 0) store_state_tma(tS + lrow, sttiles, lane, d, gam_fin, tm, (int)(r + q4 * 32), nblk);
     }
     if (lane == 0) bulk_wait_all();  // this warp's tensor stores are complete
   } else if (warp == 8) {
@@ -433,7 +447,7 @@ cudaError_t launch_scan(const Problem &p, cudaStream_t stream) {
   const size_t smem = scan_smem_bytes(p.K, p.qpad, p.V);
   cudaError_t e = cudaFuncSetAttribute(gdp_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  alignas(64) CUtensorMap tm_cs, tm_fin;
+  alignas(64) CUtensorMap tm_cs, tm_fin, tm_seg;
   const int64_t hv = (int64_t)p.H * p.V;
   if ((e = tmap_state(&tm_cs, p.chunk_states, p.nt_pad * hv, p.K)) != cudaSuccess) return e;
   if (p.cache)
@@ -441,8 +455,9 @@ cudaError_t launch_scan(const Problem &p, cudaStream_t stream) {
   else
     e = tmap_state(&tm_fin, p.out_state, p.N * hv, p.K);
   if (e != cudaSuccess) return e;
+  if ((e = tmap_state(&tm_seg, p.seg_state, p.N * hv, p.K)) != cudaSuccess) return e;
   dim3 grid((unsigned)p.N, (unsigned)p.H);
-  gdp_scan_kernel<<<grid, kScanThreads, smem, stream>>>(p, tm_cs, tm_fin);
+  gdp_scan_kernel<<<grid, kScanThreads, smem, stream>>>(p, tm_cs, tm_fin, tm_seg);
   return cudaGetLastError();
 }
 

@@ -183,9 +183,19 @@ __device__ __forceinline__ void bf16x8_at(const unsigned char *tile, int rows_pe
 __global__ void __launch_bounds__(kWyThreads, 2)
     gdp_wy_kernel(Problem p, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_v) {
-  const int row = blockIdx.x, h = blockIdx.y;
-  const int seq = p.cid[2 * row], c = p.cid[2 * row + 1];
-  if (seq < 0 || seq >= p.N || row >= p.ws_rows) return;
+  const int h = blockIdx.y;
+  int row, seq, c;
+  if (p.seg_rows > 0) {  // a segment: tile (sequence, chunk seg_lo + x % seg_rows)
+    seq = blockIdx.x / p.seg_rows;
+    c = (int)(p.seg_lo + blockIdx.x % p.seg_rows);
+    if (seq >= p.N) return;
+    row = p.cod[seq] + c;
+  } else {
+    row = blockIdx.x;
+    seq = p.cid[2 * row];
+    c = p.cid[2 * row + 1];
+  }
+  if (seq < 0 || seq >= p.N || row < 0 || row >= p.ws_rows) return;
   int64_t bos, L;
   if (!seq_bounds(p.cu, p.cu64, p.T, seq, &bos, &L)) return;
   if (c < 0 || L <= 0 || (int64_t)c * kChunk >= L * p.M) return;
@@ -536,7 +546,7 @@ cudaError_t launch_wy(const Problem &p, cudaStream_t stream) {
   if ((e = tmap_rows_bf16(&tm_k, p.k, rows, p.H, p.K, p.k_st, p.k_sh, kChunk)) != cudaSuccess) return e;
   if ((e = tmap_rows_bf16(&tm_q, p.q, p.T, p.H, p.K, p.q_st, p.q_sh, p.qpad)) != cudaSuccess) return e;
   if ((e = tmap_rows_bf16(&tm_v, p.v, rows, p.H, p.V, p.v_st, p.v_sh, kChunk)) != cudaSuccess) return e;
-  dim3 grid((unsigned)p.ntdp_pad, (unsigned)p.H);
+  dim3 grid(p.seg_rows > 0 ? (unsigned)(p.N * p.seg_rows) : (unsigned)p.ntdp_pad, (unsigned)p.H);
   gdp_wy_kernel<<<grid, kWyThreads, smem, stream>>>(p, tm_k, tm_q, tm_v);
   return cudaGetLastError();
 }

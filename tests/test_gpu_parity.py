@@ -136,6 +136,52 @@ def test_workload5_state_cache_graph(cuda_device):
     assert torch.equal(out, o_graph) and torch.equal(d["state"], cache_graph)
 
 
+# ------------------------------------------- segmented mode (few chains, long sequences)
+
+def test_segmented_uneven_lengths(cuda_device):
+    """Chunk segments with the state carried between them; sequences ending in different
+    segments (the shapes qualify: 12 chains, > 3 x 128 expanded chunks)."""
+    w = make_custom([12345, 5000, 30], 4, 128, 2, seed=71, init_sigma=0.1, chunk_states=True)
+    heads = [0, 3]
+    o, fin, cs, _ = run(w, cuda_device)
+    ref = _oracle(w, heads=heads)
+    check_o(o.cpu(), ref["o"], heads=heads)
+    check_state(fin.cpu(), ref["final_state"], heads=heads, label="final_state")
+    check_state(cs[:w.NT].cpu(), ref["chunk_states"], heads=heads, label="chunk_states")
+
+
+def test_segmented_cache_graph(cuda_device):
+    """Segmented mode inside a CUDA graph (internal streams fork from and join the capturing
+    stream) with the state cache, against the oracle and against an eager call."""
+    w = make_custom([12000, 700], 2, 128, 2, seed=72, cache_slots=4, cache_sigma=0.1, padding_slots=1)
+    d = to_dev(w, cuda_device)
+    pristine = d["state"].clone()
+    out = torch.empty((w.T, w.H, w.d), dtype=torch.bfloat16, device=cuda_device)
+    ws = pkg.alloc_workspace(w.T, w.N, w.H, w.d, w.d, w.M, cuda_device)
+    args = pkg.make_args(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu"], w.M, w.scale, None, d["state"],
+                         d["sidx"], out, None, None, None, None, None, None, None, False, ws, None)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g.capture_begin()
+        pkg.gdp_prefill_varlen(args, s.cuda_stream)
+        g.capture_end()
+    torch.cuda.synchronize()
+    assert torch.equal(d["state"], pristine)
+    g.replay()
+    torch.cuda.synchronize()
+    o_graph, cache_graph = out.clone(), d["state"].clone()
+    ref = _oracle(w)
+    check_o(o_graph.cpu(), ref["o"])
+    used = [s_ for s_ in w.state_indices.tolist() if s_ >= 0]
+    check_state(cache_graph.cpu()[used], ref["state_out"][used], label="cache slots")
+    d["state"].copy_(pristine)
+    pkg.gdp_prefill_varlen(args)
+    torch.cuda.synchronize()
+    assert torch.equal(out, o_graph) and torch.equal(d["state"], cache_graph)
+
+
 # ---------------------------------------------------------------- edge cases
 
 EDGE = {
