@@ -217,6 +217,7 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
   p.seg_hi = INT64_MAX;
   p.seg_rows = 0;
   p.seg_state = nullptr;
+  p.prefetch = (N * (int64_t)H <= gdp::kSegMaxChains) ? 1 : 0;
   const int nseg = seg_count(T, N, H, M);
   SideStreams *ss = nseg > 1 ? side_streams() : nullptr;
   if (nseg > 1 && !ss) return fail(GDP_ERR_CUDA, "could not create the internal streams of the segmented mode");

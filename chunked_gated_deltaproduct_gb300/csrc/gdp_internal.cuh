@@ -109,6 +109,8 @@ struct Problem {
   int64_t seg_lo, seg_hi;
   int seg_rows;
   float *seg_state;
+  // scan: prefetch image and U^T tiles into L2 ahead of use (few chains: HBM has headroom)
+  int prefetch;
 };
 
 // Long sequences over few (sequence, head) chains are processed in segments of

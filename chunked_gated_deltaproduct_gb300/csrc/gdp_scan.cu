@@ -421,7 +421,20 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     }
   } else if (lane == 0) {
     // ---------------- producer thread: image copies ----------------
+    // L2 prefetch kPrefetch chunks ahead of the copies (few chains only: with many the scan
+    // already streams at HBM bandwidth): the image and U^T tiles were written by the WY
+    // kernel long before and sit in HBM; the prep warps' U^T loads then hit L2
+    constexpr int kPrefetch = 4;
+    const uint32_t ubytes = (uint32_t)V * kChunk * 4u;
+    auto prefetch = [&](int64_t e) {
+      if (p.prefetch && e < nrun) {
+        bulk_prefetch_l2(image(e), il.bytes & ~15u);
+        bulk_prefetch_l2(p.U + ((cod_i + e0 + e) * H + h) * (int64_t)V * kChunk, ubytes);
+      }
+    };
+    for (int64_t e = 0; e < kPrefetch; ++e) prefetch(nst + e);
     for (int64_t e = 0; e + nst < nrun; ++e) {
+      prefetch(e + nst + kPrefetch);
       const int b = (int)(e & 1);
       if (!mbar_wait_or_abort(&b1_done[b], (uint32_t)((e >> 1) & 1), &abort_flag)) break;
       load_part1(e + nst);
