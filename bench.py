@@ -37,7 +37,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM traffic of the dominant kernel per launch, from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the sha256 of the
 # kernel source it was taken on; reported as null once the source changes.
-NCU_TRAFFIC = {"gdp_scan_kernel": {"sha": "0753aa97819832a0", "bytes_per_launch": 48740352, "workload": 2}}
+NCU_TRAFFIC = {"gdp_scan_kernel": {"sha": "830b7420307e60d2", "bytes_per_launch": 49147136, "workload": 2}}
 
 
 def alg_bytes(w) -> int:
