@@ -19,7 +19,10 @@ from .binding import (  # noqa: F401
     LIB_PATH,
     alloc_workspace,
     chunk_gated_delta_product,
+    decode_args,
+    gated_delta_product_decode,
     gdp_build_descriptors,
+    gdp_decode_step,
     gdp_last_error,
     gdp_nt_pad,
     gdp_ntdp_pad,

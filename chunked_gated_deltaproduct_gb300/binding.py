@@ -70,6 +70,8 @@ def load_library(path: str | None = None):
     lib.gdp_prefill_varlen.argtypes = [ctypes.POINTER(GdpPrefillArgs), _vp]
     lib.gdp_prefill_varlen_profiled.restype = _int
     lib.gdp_prefill_varlen_profiled.argtypes = [ctypes.POINTER(GdpPrefillArgs), _vp, ctypes.POINTER(_vp), _int]
+    lib.gdp_decode_step.restype = _int
+    lib.gdp_decode_step.argtypes = [ctypes.POINTER(GdpPrefillArgs), _vp]
     lib.gdp_prefill_varlen_static_scratch.restype = _int
     lib.gdp_prefill_varlen_static_scratch.argtypes = [ctypes.POINTER(GdpPrefillArgs), _vp]
     lib.gdp_prefill_workspace_bytes.restype = _sz
@@ -213,6 +215,64 @@ def make_args(q, k, v, g, beta, cu_seqlens, num_householder, scale, initial_stat
     a.workspace_bytes = workspace.numel() * workspace.element_size()
     a.device_status = _addr(device_status)
     return a
+
+
+def gdp_decode_step(args: GdpPrefillArgs, stream: int | None = None) -> None:
+    """Enqueue one decode step (one token per sequence, T == N) on ``stream``."""
+    lib = load_library()
+    st = lib.gdp_decode_step(ctypes.byref(args), ctypes.c_void_p(_stream(stream)))
+    if st != GDP_OK:
+        raise GdpError(st, lib.gdp_last_error().decode())
+
+
+def decode_args(q, k, v, g, beta, num_householder, scale, initial_state, state, state_indices, output,
+                output_state, use_qk_l2norm, device_status) -> GdpPrefillArgs:
+    """GdpPrefillArgs of a decode step: q [N,H,K], k/v [N*M,H,K|V] bf16 (no copies)."""
+    N, H, K = q.shape
+    V = v.shape[-1]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or t.stride(-1) != 1:
+            raise GdpError(GDP_ERR_UNSUPPORTED, f"{name} must be bfloat16, contiguous in its last dimension")
+    for name, t in (("g", g), ("beta", beta), ("initial_state", initial_state), ("state", state)):
+        if t is not None and (t.dtype != torch.float32 or not t.is_contiguous()):
+            raise GdpError(GDP_ERR_UNSUPPORTED, f"{name} must be a contiguous float32 tensor")
+    a = GdpPrefillArgs()
+    a.q, a.q_stride_t, a.q_stride_h = q.data_ptr(), q.stride(0), q.stride(1)
+    a.k, a.k_stride_t, a.k_stride_h = k.data_ptr(), k.stride(0), k.stride(1)
+    a.v, a.v_stride_t, a.v_stride_h = v.data_ptr(), v.stride(0), v.stride(1)
+    a.g, a.beta = _addr(g), _addr(beta)
+    a.T, a.N = N, N
+    a.H, a.K, a.V, a.num_householder = H, K, V, int(num_householder)
+    a.scale = 0.0 if scale is None else float(scale)
+    a.use_qk_l2norm = int(bool(use_qk_l2norm))
+    a.initial_state, a.state, a.state_indices = _addr(initial_state), _addr(state), _addr(state_indices)
+    a.num_slots = state.shape[0] if state is not None else 0
+    a.output, a.output_state = output.data_ptr(), _addr(output_state)
+    a.device_status = _addr(device_status)
+    return a
+
+
+def gated_delta_product_decode(q, k, v, g=None, beta=None, num_householder=1, scale=None, initial_state=None,
+                               output_final_state=False, use_qk_l2norm_in_kernel=False, state=None,
+                               state_indices=None, output=None, output_state=None, device_status=None,
+                               stream=None):
+    """One decode step: token i of sequence i, q [N,H,K], k/v [N*M,...] bf16, g [N,H], beta [N*M,H].
+
+    Returns ``o`` [N,H,V] bf16, or ``(o, final_state)`` when output_final_state (dense mode).
+    In state-cache mode the cache is updated in place at ``state_indices``.
+    """
+    N, H, K = q.shape
+    V = v.shape[-1]
+    if output is None:
+        output = torch.empty((N, H, V), dtype=torch.bfloat16, device=q.device)
+    if output_final_state and state is None and output_state is None:
+        output_state = torch.empty((N, H, V, K), dtype=torch.float32, device=q.device)
+    a = decode_args(q, k, v, g, beta, num_householder, scale, initial_state, state, state_indices, output,
+                    output_state, use_qk_l2norm_in_kernel, device_status)
+    gdp_decode_step(a, stream)
+    if output_final_state and state is None:
+        return output, output_state
+    return output
 
 
 def alloc_workspace(T, N, H, K, V, M, device) -> torch.Tensor:

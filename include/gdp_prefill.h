@@ -209,6 +209,25 @@ gdp_status gdp_build_descriptors(const void *cu_seqlens, int cu_seqlens_int64, i
                                  int32_t *chunk_indices_dp, int64_t ntdp_pad, int32_t *chunk_offsets,
                                  int32_t *chunk_offsets_dp, uint32_t *device_status, void *stream);
 
+/*
+ * gdp_decode_step: one token per sequence -- the serving step after prefill
+ * (Attention-Cache-and-Sequence-Parallelism page, section "Prefill and decode"
+ * and the GDN section: decode keeps only the state and advances it token by token
+ * with the recurrent form; Megatron page, parameters state / state_indices).
+ * For token i of sequence i (i < N) and every head: S *= exp(g_i); for j < M:
+ * v_new = beta (v - S k_j), S += v_new (x) k_j; o_i = scale S q_i.
+ *
+ * Arguments: a gdp_prefill_args with T == N (token i belongs to sequence i; k, v
+ * and beta have N*M rows).  cu_seqlens, the descriptor fields, nt_pad/ntdp_pad and
+ * the workspace are ignored; chunk_states must be NULL.  State modes as for the
+ * prefill: the cache `state` is read and written in place at state_indices[i] (-1:
+ * start from zero, write nothing); otherwise initial_state[i] (or zero) is read and
+ * output_state[i] written, and output_state may equal initial_state exactly (an
+ * in-place update) but not partly overlap it (GDP_ERR_ALIAS).  K = V in {64, 128},
+ * 1 <= M <= 16 (GDP_ERR_UNSUPPORTED otherwise).  No workspace; graph-capturable.
+ */
+gdp_status gdp_decode_step(const gdp_prefill_args *args, void *stream);
+
 /* One-line reason for the last non-OK status returned on this thread ("" if none). */
 const char *gdp_last_error(void);
 
