@@ -29,7 +29,7 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from gdp_workloads import WORKLOADS, make_workload  # noqa: E402
+from gdp_workloads import make_custom, WORKLOADS, make_workload  # noqa: E402
 
 METRIC = "GDP prefill real tokens/s on 1 GB300 (device-timed) and % of roofline"
 UNIT = "tokens/s"
@@ -217,6 +217,49 @@ def run_reference(args, w, rank):
     print(json.dumps(line), flush=True)
 
 
+def launches_per_call(w) -> int:
+    """Kernels one call launches: descriptors, then WY + scan, or per segment in the segmented
+    mode (few (sequence, head) chains, long sequences: segments of 128 expanded chunks)."""
+    chains = w.N * w.H
+    maxc = (w.M * w.T + 63) // 64
+    if chains <= 64 and maxc >= 3 * 128:
+        return 1 + 2 * min((maxc + 127) // 128, 64)
+    return 3
+
+
+def measure_decode(pkg, dev, flush, stream, steps=50, warmup=5):
+    """The decode step (one token per sequence, state cache in place) on a serving batch shaped
+    like workload 5: 64 sequences, H=16, d=128, M=4, a 128-slot cache with 8 padding entries.
+    Device time per step with the L2 flushed between steps; algorithmic bytes = the live cache
+    slots read and written + the token's q, M k/v rows, gate, M betas and o."""
+    wd = make_custom([1] * 64, 16, 128, 4, seed=2024, cache_slots=128, cache_sigma=0.1, padding_slots=8)
+    q, k, v, g, b = (t.to(dev) for t in (wd.q, wd.k, wd.v, wd.g, wd.beta))
+    cache, sidx = wd.state.to(dev), wd.state_indices.to(dev)
+    out = torch.empty((wd.N, wd.H, wd.d), dtype=torch.bfloat16, device=dev)
+    a = pkg.decode_args(q, k, v, g, b, wd.M, wd.scale, None, cache, sidx, out, None, False, None)
+    sid = stream.cuda_stream
+    times = []
+    for s in range(warmup + steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            e0.record(stream)
+            pkg.gdp_decode_step(a, sid)
+            e1.record(stream)
+        e1.synchronize()
+        if s >= warmup:
+            times.append(e0.elapsed_time(e1))
+    live = int((wd.state_indices >= 0).sum())
+    d, M, H, N = wd.d, wd.M, wd.H, wd.N
+    ab = live * H * d * d * 4 * 2 + N * H * (2 * d + M * 4 * d + 4 + 4 * M + 2 * d)
+    ms = statistics.median(times)
+    peak, src = measured_peaks()
+    gbs = ab / (ms / 1e3) / 1e9
+    return {"workload": "decode: 64 seqs x 1 token, H16 d128 M4, cache 128 slots (8 padding)",
+            "us_per_step": 1e3 * ms, "tokens_per_s": N / (ms / 1e3), "alg_bytes": ab, "achieved_gbs": gbs,
+            "peak_gbs": peak, "frac": gbs / peak, "peak_source": src, "steps": steps, "l2_flush": True}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -353,6 +396,8 @@ def main():
             e2e_ms.append(e0.elapsed_time(e1))
     e2e_value = world * w.T / (statistics.fmean(e2e_ms) / 1e3)
 
+    decode = measure_decode(pkg, dev, flush, stream) if rank == 0 else None
+
     if rank == 0:
         cpu = None
         if not args.no_cpu_baseline and world == 1:
@@ -371,8 +416,9 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": statistics.fmean(e2e_ms)},
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": launches_per_call(w) * args.steps,
             "clocks": clk.summary(),
+            "decode_step": decode,
             "wall_s_timed": wall,
         }
         print(json.dumps(line), flush=True)

@@ -54,6 +54,31 @@ __global__ void __launch_bounds__(kDecThreads) gdp_decode_kernel(DecodeProblem p
   __shared__ float bt[kDecMaxM];
   __shared__ float red[kDecMaxM + 1];
 
+  // the state row: slot / initial state / zero
+  int slot = -1;
+  const float *src = nullptr;
+  float *dst = nullptr;
+  if (p.cache) {
+    slot = p.slots[i];
+    if (slot < -1 || slot >= p.num_slots) {
+      if (tid == 0 && blockIdx.y == 0 && blockIdx.z == 0) set_status(p.status, GDP_DEV_ERR_SLOT);
+      slot = -1;
+    }
+    if (slot >= 0) src = dst = p.cache + ((int64_t)slot * p.H + h) * (int64_t)p.V * D;
+  } else {
+    if (p.init) src = p.init + ((int64_t)i * p.H + h) * (int64_t)p.V * D;
+    if (p.out_state) dst = p.out_state + ((int64_t)i * p.H + h) * (int64_t)p.V * D;
+  }
+  // thread (row, qd) holds columns 16 g' + 4 qd .. + 3 for g' < G: a warp's 4-thread groups
+  // read 64 contiguous bytes of each of its 8 rows per instruction
+  float s[4 * G];
+  // issued first, so that the state's HBM latency overlaps the input loads below
+#pragma unroll
+  for (int gi = 0; gi < G; ++gi) {
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (src) x = *reinterpret_cast<const float4 *>(src + (int64_t)vrow * D + gi * 16 + qd * 4);
+    s[4 * gi] = x.x; s[4 * gi + 1] = x.y; s[4 * gi + 2] = x.z; s[4 * gi + 3] = x.w;
+  }
   // inputs of the token: k rows i*M + j, q row i, this block's v entries, beta, gate
   for (int idx = tid; idx < (M + 1) * D; idx += kDecThreads) {
     const int j = idx / D, c = idx % D;
@@ -88,31 +113,9 @@ __global__ void __launch_bounds__(kDecThreads) gdp_decode_kernel(DecodeProblem p
     __syncthreads();
   }
 
-  // the state row: slot / initial state / zero
-  int slot = -1;
-  const float *src = nullptr;
-  float *dst = nullptr;
-  if (p.cache) {
-    slot = p.slots[i];
-    if (slot < -1 || slot >= p.num_slots) {
-      if (tid == 0 && blockIdx.y == 0 && blockIdx.z == 0) set_status(p.status, GDP_DEV_ERR_SLOT);
-      slot = -1;
-    }
-    if (slot >= 0) src = dst = p.cache + ((int64_t)slot * p.H + h) * (int64_t)p.V * D;
-  } else {
-    if (p.init) src = p.init + ((int64_t)i * p.H + h) * (int64_t)p.V * D;
-    if (p.out_state) dst = p.out_state + ((int64_t)i * p.H + h) * (int64_t)p.V * D;
-  }
-  // thread (row, qd) holds columns 16 g' + 4 qd .. + 3 for g' < G: a warp's 4-thread groups
-  // read 64 contiguous bytes of each of its 8 rows per instruction
-  float s[4 * G];
   const float decay = p.g ? __expf(p.g[(int64_t)i * p.H + h]) : 1.f;
 #pragma unroll
-  for (int gi = 0; gi < G; ++gi) {
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (src) x = *reinterpret_cast<const float4 *>(src + (int64_t)vrow * D + gi * 16 + qd * 4);
-    s[4 * gi] = x.x * decay; s[4 * gi + 1] = x.y * decay; s[4 * gi + 2] = x.z * decay; s[4 * gi + 3] = x.w * decay;
-  }
+  for (int c = 0; c < 4 * G; ++c) s[c] *= decay;
   for (int j = 0; j < M; ++j) {
     float dot = 0.f;
 #pragma unroll
