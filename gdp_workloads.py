@@ -16,6 +16,14 @@ state_indices):
   * g = -U(0, a) fp32, the natural log of alpha = exp(-U(0, a));
   * beta = sigmoid(N(0, 1)) fp32 on the expanded stream;
   * states sigma * N(0, 1) fp32, V-major [., H, V, K].
+
+Input variants of the same contract (FlashInfer page, parameters q, k, v, g,
+beta, initial_state), all off by default so that the draws above are
+unchanged: q / k / v (and so the output) in float16; the gate drawn as alpha =
+exp(-U(0, a)) itself (linear space) instead of its log; g and beta rounded to
+bfloat16 or float16; the initial state rounded to bfloat16; q, k and v with
+fewer heads than the H state heads (each count divides H; the per-head draws
+simply have that many heads).
 """
 from __future__ import annotations
 
@@ -49,6 +57,7 @@ class Workload:
     return_chunk_states: bool = False
     prebuilt_descriptors: bool = False
     graph: bool = False
+    g_is_alpha: bool = False
     meta: dict = field(default_factory=dict)
 
     @property
@@ -77,26 +86,33 @@ def _normal(gen, shape):
     return torch.randn(*shape, generator=gen, dtype=torch.float32)
 
 
-def _rows(gen, rows, H, d, normalise):
+def _rows(gen, rows, H, d, normalise, dtype=torch.bfloat16):
     x = _normal(gen, (rows, H, d))
     if normalise:
         x = x / x.norm(dim=-1, keepdim=True).clamp_min(1e-30)
-    return x.to(torch.bfloat16)
+    return x.to(dtype)
 
 
 def make_custom(lengths, H, d, M, *, seed=0, normalised=True, use_qk_l2norm=False,
                 decay=0.1, init_sigma=0.0, cache_slots=0, cache_sigma=0.1, padding_slots=0,
                 chunk_states=False, with_g=True, with_beta=True, name="custom",
-                prebuilt_descriptors=False, graph=False, scale=None) -> Workload:
-    """A workload of the given shape drawn with the recipe of this module."""
+                prebuilt_descriptors=False, graph=False, scale=None,
+                qkv_dtype=torch.bfloat16, hq=None, hk=None, hv=None, g_is_alpha=False,
+                g_dtype=torch.float32, beta_dtype=torch.float32, state_dtype=torch.float32) -> Workload:
+    """A workload of the given shape drawn with the recipe of this module (H state heads;
+    hq / hk / hv: head counts of q / k / v, default H)."""
     gen = torch.Generator().manual_seed(int(seed))
     lengths = [int(x) for x in lengths]
     T, N = sum(lengths), len(lengths)
-    q = _rows(gen, T, H, d, normalised)
-    k = _rows(gen, T * M, H, d, normalised)
-    v = _rows(gen, T * M, H, d, False)
+    q = _rows(gen, T, hq or H, d, normalised, qkv_dtype)
+    k = _rows(gen, T * M, hk or H, d, normalised, qkv_dtype)
+    v = _rows(gen, T * M, hv or H, d, False, qkv_dtype)
     g = -torch.rand(T, H, generator=gen, dtype=torch.float32) * decay if with_g else None
+    if g is not None:
+        g = (torch.exp(g) if g_is_alpha else g).to(g_dtype)
     beta = torch.sigmoid(_normal(gen, (T * M, H))) if with_beta else None
+    if beta is not None:
+        beta = beta.to(beta_dtype)
     init = state = sidx = None
     if cache_slots:
         state = _normal(gen, (cache_slots, H, d, d)) * cache_sigma
@@ -106,7 +122,7 @@ def make_custom(lengths, H, d, M, *, seed=0, normalised=True, use_qk_l2norm=Fals
             perm[pos] = -1
         sidx = perm
     elif init_sigma > 0:
-        init = _normal(gen, (N, H, d, d)) * init_sigma
+        init = (_normal(gen, (N, H, d, d)) * init_sigma).to(state_dtype)
     cu = torch.zeros(N + 1, dtype=torch.int32)
     if N:
         cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
@@ -115,7 +131,7 @@ def make_custom(lengths, H, d, M, *, seed=0, normalised=True, use_qk_l2norm=Fals
                     use_qk_l2norm=use_qk_l2norm, initial_state=init, state=state,
                     state_indices=sidx, output_final_state=(state is None),
                     return_chunk_states=chunk_states, prebuilt_descriptors=prebuilt_descriptors,
-                    graph=graph)
+                    graph=graph, g_is_alpha=g_is_alpha)
 
 
 def _loguniform_lengths(gen, n, lo, hi):

@@ -12,4 +12,5 @@ from .oracle import (  # noqa: F401
     descriptors,
     forward,
     oracle_threads,
+    widen_f16,
 )

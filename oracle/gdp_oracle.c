@@ -23,11 +23,23 @@
  *   (parameter return_chunk_states); the state cache is written in place at
  *   state_indices, -1 marking padding (parameters state, state_indices).
  *
- * Everything is computed in float64 from the exact values of the bf16 / fp32
- * inputs (a bf16 bit pattern widened to float is exact).  The only liberty
+ * Everything is computed in float64 from the exact values of the bf16 / f16 /
+ * fp32 inputs (every such bit pattern widens to float64 exactly).  The only liberty
  * taken: the V rows of S are handed to different threads.  Each row of S
  * evolves on its own (row v of v_new only reads row v of S), so every row
  * sees exactly the arithmetic of the unsplit loop, in the same order.
+ *
+ * Input variants (FlashInfer page, parameters q, k, v, g, beta,
+ * initial_state): q / k / v may be float16 instead of bfloat16 (widened
+ * exactly by widen_f16 below, from the IEEE 754 binary16 definition); g may
+ * hold the gate alpha itself in linear space instead of its natural log, in
+ * which case S is multiplied by alpha as given; the head counts of q, k and v
+ * may be smaller than the state head count H.  Reading of the head relation
+ * (the page names the counts but not the map): H is the larger of the q and v
+ * head counts, every count divides H, and state head h reads q head
+ * h / (H / Hq), k head h / (H / Hk) and v head h / (H / Hv), so each head of a
+ * smaller count serves a run of consecutive state heads.  g, beta, the states
+ * and the output have H heads.
  *
  * Readings where the pages are silent (the same list is kept in the design
  * notes): q/k L2 normalisation is x / sqrt(sum x^2 + 1e-6), applied in float64
@@ -53,6 +65,26 @@ static double widen_bf16(uint16_t bits) {
   memcpy(&f, &u, sizeof f);
   return (double)f;
 }
+
+/* IEEE 754 binary16: sign bit, 5-bit exponent with bias 15, 10-bit fraction;
+ * exponent 0 holds zero and the subnormals (fraction * 2^-24), exponent 31
+ * infinity and NaN. */
+static double widen_f16(uint16_t bits) {
+  const int sign = (bits >> 15) & 1, ex = (bits >> 10) & 31, fr = bits & 1023;
+  double mag;
+  if (ex == 0)
+    mag = ldexp((double)fr, -24);
+  else if (ex == 31)
+    mag = fr ? NAN : INFINITY;
+  else
+    mag = ldexp((double)(1024 + fr), ex - 25);
+  return sign ? -mag : mag;
+}
+
+static double widen_half(uint16_t bits, int f16) { return f16 ? widen_f16(bits) : widen_bf16(bits); }
+
+/* Exported for the tests: the binary16 widening above, one bit pattern. */
+double gdp_oracle_widen_f16(uint16_t bits) { return widen_f16(bits); }
 
 static int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -103,14 +135,15 @@ int gdp_oracle_descriptors(const int64_t *cu_seqlens, int64_t N, int M,
   return 0;
 }
 
-/* Load a head-row of a bf16 [rows][H][D] tensor as float64, optionally
- * L2-normalised (FlashInfer page, parameter use_qk_l2norm_in_kernel). */
+/* Load a head-row of a bf16 (f16 = 0) or float16 (f16 = 1) [rows][H][D]
+ * tensor as float64, optionally L2-normalised (FlashInfer page, parameter
+ * use_qk_l2norm_in_kernel). */
 static void load_row(const uint16_t *base, int64_t row, int H, int h, int D,
-                     int normalise, double *out) {
+                     int f16, int normalise, double *out) {
   const uint16_t *p = base + (row * H + h) * (int64_t)D;
   double ss = 0.0;
   for (int d = 0; d < D; ++d) {
-    out[d] = widen_bf16(p[d]);
+    out[d] = widen_half(p[d], f16);
     ss += out[d] * out[d];
   }
   if (normalise) {
@@ -122,8 +155,11 @@ static void load_row(const uint16_t *base, int64_t row, int H, int h, int D,
 /*
  * The forward pass, token by token.
  *
- *   q [T][H][K], k [T*M][H][K], v [T*M][H][V]: bf16 bit patterns.
- *   g [T][H] natural-log decay (NULL: no decay); beta [T*M][H] (NULL: ones).
+ *   q [T][Hq][K], k [T*M][Hk][K], v [T*M][Hv][V]: bf16 (qkv_f16 = 0) or
+ *   float16 (qkv_f16 = 1) bit patterns; state head h reads q head h / (H / Hq),
+ *   k head h / (H / Hk), v head h / (H / Hv) (each count divides H).
+ *   g [T][H]: natural-log decay (g_is_alpha = 0) or alpha itself (g_is_alpha = 1);
+ *   NULL: no decay.  beta [T*M][H] (NULL: ones).
  *   Incoming state: state-cache mode when state_in != NULL (slot = state_indices[i],
  *   slot >= 0 reads state_in[slot], slot -1 starts from zero); otherwise
  *   initial_state[i] when non-NULL; otherwise zero.  States are [..][H][V][K] fp32.
@@ -138,6 +174,7 @@ static void load_row(const uint16_t *base, int64_t row, int H, int h, int D,
  * Returns 0, or a negative code for an argument the definition cannot serve.
  */
 int gdp_oracle_forward(int64_t T, int64_t N, int H, int K, int V, int M,
+                       int Hq, int Hk, int Hv, int qkv_f16, int g_is_alpha,
                        const int64_t *cu_seqlens,
                        const uint16_t *q, const uint16_t *k, const uint16_t *v,
                        const float *g, const float *beta, double scale,
@@ -150,6 +187,7 @@ int gdp_oracle_forward(int64_t T, int64_t N, int H, int K, int V, int M,
                        double *o, double *final_state, double *state_out,
                        double *chunk_states, int num_threads) {
   if (T < 0 || N < 0 || H <= 0 || K <= 0 || V <= 0 || M <= 0) return -1;
+  if (Hq <= 0 || Hk <= 0 || Hv <= 0 || H % Hq || H % Hk || H % Hv) return -6;
   if (chunk_states && !chunk_offsets) return -2;
   if (state_in && !state_indices) return -3;
   if (N > 0 && (cu_seqlens[0] != 0 || cu_seqlens[N] != T)) return -4;
@@ -211,25 +249,25 @@ int gdp_oracle_forward(int64_t T, int64_t N, int H, int K, int V, int M,
               for (int d = 0; d < K; ++d) dst[(int64_t)(v0 + r) * K + d] = S[r * K + d];
           }
           /* decay once per real token, before its updates */
-          const double alpha = g ? exp((double)g[t * H + h]) : 1.0;
+          const double alpha = !g ? 1.0 : g_is_alpha ? (double)g[t * H + h] : exp((double)g[t * H + h]);
           for (int x = 0; x < nv * K; ++x) S[x] *= alpha;
           /* n beta-gated Householder updates on the expanded rows t*M + j */
           for (int j = 0; j < M; ++j) {
             const int64_t row = t * M + j;
-            load_row(k, row, H, h, K, use_qk_l2norm, kr);
+            load_row(k, row, Hk, h / (H / Hk), K, qkv_f16, use_qk_l2norm, kr);
             const double b = beta ? (double)beta[row * H + h] : 1.0;
             for (int r = 0; r < nv; ++r) {
               double *Sr = S + r * K;
               double pred = 0.0;
               for (int d = 0; d < K; ++d) pred += Sr[d] * kr[d];
-              const double vv = widen_bf16(v[(row * H + h) * (int64_t)V + v0 + r]);
+              const double vv = widen_half(v[(row * Hv + h / (H / Hv)) * (int64_t)V + v0 + r], qkv_f16);
               const double vnew = b * (vv - pred);
               for (int d = 0; d < K; ++d) Sr[d] += vnew * kr[d];
             }
           }
           /* readout after the last update */
           if (o) {
-            load_row(q, t, H, h, K, use_qk_l2norm, qt);
+            load_row(q, t, Hq, h / (H / Hq), K, qkv_f16, use_qk_l2norm, qt);
             for (int r = 0; r < nv; ++r) {
               const double *Sr = S + r * K;
               double acc = 0.0;

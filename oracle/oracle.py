@@ -55,6 +55,7 @@ def _load():
             lib.gdp_oracle_forward.restype = ctypes.c_int
             lib.gdp_oracle_forward.argtypes = [
                 i64, i64, i32, i32, i32, i32,  # T N H K V M
+                i32, i32, i32, i32, i32,  # Hq Hk Hv qkv_f16 g_is_alpha
                 P,  # cu_seqlens
                 P, P, P,  # q k v
                 P, P, dbl, i32,  # g beta scale l2norm
@@ -67,6 +68,8 @@ def _load():
             ]
             lib.gdp_oracle_descriptors.restype = ctypes.c_int
             lib.gdp_oracle_descriptors.argtypes = [P, i64, i32, P, i64, P, i64, P, P]
+            lib.gdp_oracle_widen_f16.restype = ctypes.c_double
+            lib.gdp_oracle_widen_f16.argtypes = [ctypes.c_uint16]
             lib.gdp_oracle_decay_cumsum.restype = ctypes.c_int
             lib.gdp_oracle_decay_cumsum.argtypes = [i64, i64, i32, i32, P, P, P]
             _lib = lib
@@ -81,23 +84,42 @@ def oracle_threads() -> int:
         return os.cpu_count() or 1
 
 
-def _bf16_bits(x) -> np.ndarray:
-    """bf16 tensor (torch) or uint16 array -> contiguous uint16 bit patterns."""
+def _half_bits(x):
+    """bf16 / float16 tensor (torch), or a uint16 array of bf16 bit patterns ->
+    (contiguous uint16 bit patterns, 1 if float16 else 0)."""
     if isinstance(x, np.ndarray):
+        if x.dtype == np.float16:
+            return np.ascontiguousarray(x).view(np.uint16), 1
         assert x.dtype == np.uint16
-        return np.ascontiguousarray(x)
+        return np.ascontiguousarray(x), 0
     import torch
 
-    assert x.dtype == torch.bfloat16, x.dtype
-    return np.ascontiguousarray(x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+    assert x.dtype in (torch.bfloat16, torch.float16), x.dtype
+    bits = np.ascontiguousarray(x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+    return bits, int(x.dtype == torch.float16)
+
+
+def _bf16_bits(x) -> np.ndarray:
+    """bf16 tensor (torch) or uint16 array -> contiguous uint16 bit patterns."""
+    bits, f16 = _half_bits(x)
+    assert not f16
+    return bits
 
 
 def _f32(x):
+    """fp32 copy of a float32 / bfloat16 / float16 input (every such value is an
+    fp32 value, so the widening is exact)."""
     if x is None:
         return None
     if isinstance(x, np.ndarray):
+        assert x.dtype in (np.float32, np.float16, np.float64), x.dtype
         return np.ascontiguousarray(x, dtype=np.float32)
     return np.ascontiguousarray(x.detach().cpu().float().numpy())
+
+
+def widen_f16(bits: int) -> float:
+    """The oracle's binary16 -> float64 widening of one bit pattern (for its pin)."""
+    return float(_load().gdp_oracle_widen_f16(int(bits)))
 
 
 def _ptr(a):
@@ -141,24 +163,34 @@ def decay_cumsum(cu_seqlens, g, H: int, M: int) -> np.ndarray:
 def forward(q, k, v, g, beta, cu_seqlens, num_householder: int, scale: float,
             use_qk_l2norm: bool = False, initial_state=None, state=None, state_indices=None,
             chunk_states: bool = False, heads=None, threads: int | None = None,
-            want_o: bool = True, want_final: bool = True):
-    """Run the oracle.  q [T,H,K], k [T*M,H,K], v [T*M,H,V] bf16; g [T,H] and
-    beta [T*M,H] fp32 (or None); states fp32 V-major.  ``heads``: iterable of
-    head indices to compute (default all).  Returns a dict of float64 arrays:
-    o [T,H,V], final_state [N,H,V,K], state_out [S,H,V,K] (cache mode: the
-    pristine cache with every slot >= 0 replaced), chunk_states [NT,H,V,K] and
-    chunk_offsets [N+1]."""
+            want_o: bool = True, want_final: bool = True, g_is_alpha: bool = False):
+    """Run the oracle.  q [T,Hq,K], k [T*M,Hk,K], v [T*M,Hv,V] bf16 or float16
+    (all three the same type); g [T,H] (natural-log decay, or alpha itself when
+    ``g_is_alpha``) and beta [T*M,H] fp32 / bf16 / float16 (or None); states
+    V-major fp32 (an initial state may also be bf16).  H = max(Hq, Hv) and state
+    head h reads q head h // (H // Hq), k head h // (H // Hk), v head
+    h // (H // Hv).  ``heads``: iterable of state-head indices to compute
+    (default all).  Returns a dict of float64 arrays: o [T,H,V], final_state
+    [N,H,V,K], state_out [S,H,V,K] (cache mode: the pristine cache with every
+    slot >= 0 replaced), chunk_states [NT,H,V,K] and chunk_offsets [N+1]."""
     lib = _load()
     M = int(num_householder)
-    qb, kb, vb = _bf16_bits(q), _bf16_bits(k), _bf16_bits(v)
-    T, H, K = qb.shape
-    V = vb.shape[2]
-    assert kb.shape == (T * M, H, K) and vb.shape == (T * M, H, V)
+    (qb, fq), (kb, fk), (vb, fv) = _half_bits(q), _half_bits(k), _half_bits(v)
+    assert fq == fk == fv, "q, k and v must share one element type"
+    T, Hq, K = qb.shape
+    Hk, Hv, V = kb.shape[1], vb.shape[1], vb.shape[2]
+    H = max(Hq, Hv)
+    assert H % Hq == 0 and H % Hk == 0 and H % Hv == 0, (Hq, Hk, Hv)
+    assert kb.shape == (T * M, Hk, K) and vb.shape == (T * M, Hv, V)
     cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
     N = cu.shape[0] - 1
     g32, b32 = _f32(g), _f32(beta)
     init = _f32(initial_state)
     cache = _f32(state)
+    assert g32 is None or g32.shape == (T, H), "g must be [T, H] with H = max(Hq, Hv)"
+    assert b32 is None or b32.shape == (T * M, H), "beta must be [T*M, H]"
+    assert init is None or init.shape == (N, H, V, K)
+    assert cache is None or cache.shape[1:] == (H, V, K)
     sidx = None if state_indices is None else np.ascontiguousarray(np.asarray(state_indices, dtype=np.int32))
     num_slots = 0 if cache is None else cache.shape[0]
     co = None
@@ -175,7 +207,8 @@ def forward(q, k, v, g, beta, cu_seqlens, num_householder: int, scale: float,
     st_out = cache.astype(np.float64) if cache is not None else None
     cs = np.zeros((int(co[-1]), H, V, K), np.float64) if chunk_states else None
     rc = lib.gdp_oracle_forward(
-        T, N, H, K, V, M, _ptr(cu), _ptr(qb), _ptr(kb), _ptr(vb), _ptr(g32), _ptr(b32),
+        T, N, H, K, V, M, Hq, Hk, Hv, fq, int(bool(g_is_alpha)),
+        _ptr(cu), _ptr(qb), _ptr(kb), _ptr(vb), _ptr(g32), _ptr(b32),
         float(scale), int(bool(use_qk_l2norm)), _ptr(init), _ptr(cache), _ptr(sidx), num_slots,
         _ptr(co), _ptr(mask), _ptr(o), _ptr(fin), _ptr(st_out), _ptr(cs),
         int(threads if threads is not None else oracle_threads()))

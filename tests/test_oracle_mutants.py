@@ -18,8 +18,9 @@ from tests import test_oracle_pins as pins
 
 SRC = open(os.path.join(os.path.dirname(orc.__file__), "gdp_oracle.c")).read()
 
-DECAY = ("          const double alpha = g ? exp((double)g[t * H + h]) : 1.0;\n"
-         "          for (int x = 0; x < nv * K; ++x) S[x] *= alpha;\n")
+ALPHA = "          const double alpha = !g ? 1.0 : g_is_alpha ? (double)g[t * H + h] : exp((double)g[t * H + h]);\n"
+DECAY = ALPHA + "          for (int x = 0; x < nv * K; ++x) S[x] *= alpha;\n"
+QLOAD = "load_row(q, t, Hq, h / (H / Hq), K, qkv_f16, use_qk_l2norm, qt);"
 ROW = "            const int64_t row = t * M + j;\n"
 READOUT = "          /* readout after the last update */\n"
 
@@ -28,16 +29,16 @@ MUTANTS = {
     "beta_dropped": [("const double b = beta ? (double)beta[row * H + h] : 1.0;", "const double b = 1.0;")],
     "copies_reversed": [(ROW, "            const int64_t row = t * M + (M - 1 - j);\n")],
     "decay_per_subrow": [(ROW, ROW + "            if (j > 0) for (int x = 0; x < nv * K; ++x) S[x] *= alpha;\n")],
-    "decay_after_updates": [(DECAY, "          const double alpha = g ? exp((double)g[t * H + h]) : 1.0;\n"),
+    "decay_after_updates": [(DECAY, ALPHA),
                             (READOUT, "          for (int x = 0; x < nv * K; ++x) S[x] *= alpha;\n" + READOUT)],
     "decay_base2": [("exp((double)g[t * H + h])", "exp2((double)g[t * H + h])")],
     "scale_dropped": [("= scale * acc;", "= acc;")],
     "state_transposed": [("(double)src[(int64_t)(v0 + r) * K + d]", "(double)src[(int64_t)d * K + v0 + r]")],
-    "q_not_normalised": [("load_row(q, t, H, h, K, use_qk_l2norm, qt);", "load_row(q, t, H, h, K, 0, qt);")],
+    "q_not_normalised": [(QLOAD, QLOAD.replace("use_qk_l2norm", "0"))],
     "readout_before_updates": [(READOUT, ""),
                                ("          /* n beta-gated Householder updates on the expanded rows t*M + j */\n",
                                 READOUT.replace("after the last update", "moved") + "          if (o) {\n"
-                                "            load_row(q, t, H, h, K, use_qk_l2norm, qt);\n"
+                                "            " + QLOAD + "\n"
                                 "            for (int r = 0; r < nv; ++r) {\n"
                                 "              const double *Sr = S + r * K;\n"
                                 "              double acc = 0.0;\n"
@@ -57,6 +58,14 @@ MUTANTS = {
                                  "int64_t n = M * ceil_div64(cu_seqlens[i + 1] - cu_seqlens[i], ORACLE_CHUNK);")],
     "cumsum_no_restart": [("if ((r - r0) % ORACLE_CHUNK == 0) acc = 0.0;", "if (r == r0) acc = 0.0;")],
     "cumsum_every_subrow": [("if (g && r % M == 0)", "if (g)")],
+    # input variants
+    "f16_exponent_bias": [("ldexp((double)(1024 + fr), ex - 25)", "ldexp((double)(1024 + fr), ex - 24)")],
+    "f16_subnormals_flushed": [("mag = ldexp((double)fr, -24);", "mag = 0.0;")],
+    "f16_flag_ignored": [("return f16 ? widen_f16(bits) : widen_bf16(bits);", "return widen_bf16(bits);")],
+    "q_head_modulo": [("load_row(q, t, Hq, h / (H / Hq),", "load_row(q, t, Hq, h % Hq,")],
+    "k_head_modulo": [("load_row(k, row, Hk, h / (H / Hk),", "load_row(k, row, Hk, h % Hk,")],
+    "v_head_modulo": [("v[(row * Hv + h / (H / Hv))", "v[(row * Hv + h % Hv)")],
+    "alpha_exponentiated": [("g_is_alpha ? (double)g[t * H + h]", "g_is_alpha ? exp((double)g[t * H + h])")],
 }
 
 
@@ -89,7 +98,7 @@ def test_mutant_is_caught(mutant, tmp_path):
                    check=True)
     real = orc._load()
     lib = ctypes.CDLL(str(so))
-    for fname in ("gdp_oracle_forward", "gdp_oracle_descriptors", "gdp_oracle_decay_cumsum"):
+    for fname in ("gdp_oracle_forward", "gdp_oracle_descriptors", "gdp_oracle_decay_cumsum", "gdp_oracle_widen_f16"):
         getattr(lib, fname).argtypes = getattr(real, fname).argtypes
         getattr(lib, fname).restype = getattr(real, fname).restype
     caught = []

@@ -288,3 +288,83 @@ def test_decay_cumsum():
     g = f64(w.g)[:, 0]
     assert 2.0 ** G2[63, 0] == pytest.approx(math.exp(g[:32].sum()), rel=1e-12)
     assert 2.0 ** G2[127, 0] == pytest.approx(math.exp(g[32:64].sum()), rel=1e-12)
+
+
+# ---- input variants (FlashInfer page, parameters q, k, v, g, beta, initial_state) ----
+
+def test_f16_widening_exhaustive():
+    """The oracle's binary16 widening equals numpy's float16 -> float64 for all 65536 bit patterns."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.widen_f16(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    np.testing.assert_array_equal(got[~nan], ref[~nan])
+
+
+@pytest.mark.parametrize("M", [1, 3])
+def test_f16_inputs_bruteforce(M):
+    """float16 q / k / v, bf16 g, beta and initial state: the oracle equals the transition-matrix
+    formulation run on the same values (widened by torch)."""
+    w = make_custom([3, 9, 1], 2, 4, M, seed=90 + M, decay=0.5, init_sigma=0.7, normalised=False,
+                    qkv_dtype=torch.float16, g_dtype=torch.bfloat16, beta_dtype=torch.float16,
+                    state_dtype=torch.bfloat16)
+    assert w.q.dtype == torch.float16 and w.initial_state.dtype == torch.bfloat16
+    for l2 in (False, True):
+        res = oracle.forward(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, M, 0.41, use_qk_l2norm=l2,
+                             initial_state=w.initial_state)
+        o_ref, fin_ref, _ = transition_bruteforce(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, M, 0.41,
+                                                  S0_vmajor=w.initial_state, l2norm=l2)
+        assert rel_err(res["o"], o_ref) < 1e-12
+        assert rel_err(res["final_state"], fin_ref) < 1e-12
+    # a float16 pattern read as bf16 is a different number: the element type is honoured
+    res_bf = oracle.forward(w.q.view(torch.bfloat16), w.k.view(torch.bfloat16), w.v.view(torch.bfloat16), w.g,
+                            w.beta, w.cu_seqlens, M, 0.41, initial_state=w.initial_state)
+    assert not np.allclose(res_bf["o"], o_ref)
+
+
+@pytest.mark.parametrize("heads", [(2, 2, 4), (4, 2, 2), (4, 4, 2), (1, 1, 3)])
+def test_grouped_heads_equal_repeated_heads(heads):
+    """Head counts (Hq, Hk, Hv) below the state count H = max(Hq, Hv): the result equals the run on
+    inputs whose heads are repeated explicitly, state head h taking head h // (H // Hx) of each."""
+    hq, hk, hv = heads
+    H = max(hq, hv)
+    w = make_custom([5, 11], H, 4, 2, seed=130 + hq * 7 + hv, decay=0.4, init_sigma=0.5, normalised=False,
+                    hq=hq, hk=hk, hv=hv)
+    assert w.q.shape[1] == hq and w.k.shape[1] == hk and w.v.shape[1] == hv
+    for l2 in (False, True):
+        res = oracle.forward(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, 2, 0.5, use_qk_l2norm=l2,
+                             initial_state=w.initial_state)
+        rep = [t.repeat_interleave(H // t.shape[1], dim=1) for t in (w.q, w.k, w.v)]
+        o_ref, fin_ref, _ = transition_bruteforce(*rep, w.g, w.beta, w.cu_seqlens, 2, 0.5,
+                                                  S0_vmajor=w.initial_state, l2norm=l2)
+        assert rel_err(res["o"], o_ref) < 1e-12
+        assert rel_err(res["final_state"], fin_ref) < 1e-12
+
+
+@pytest.mark.parametrize("g_dtype", [torch.float32, torch.bfloat16, torch.float16])
+def test_linear_alpha_gate(g_dtype):
+    """g given as alpha in linear space multiplies the state by alpha itself: equal to the log-gate
+    formulation at g = ln(alpha), and with beta = 0 to scale * (prod alpha) S0 q."""
+    w = make_custom([6, 20], 2, 4, 2, seed=150, decay=0.6, init_sigma=0.8, normalised=False,
+                    g_is_alpha=True, g_dtype=g_dtype)
+    assert w.g_is_alpha and float(w.g.float().min()) > 0 and float(w.g.float().max()) <= 1
+    res = oracle.forward(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, 2, w.scale, initial_state=w.initial_state,
+                         g_is_alpha=True)
+    log_g = np.log(f64(w.g))
+    o_ref, fin_ref, _ = transition_bruteforce(w.q, w.k, w.v, log_g, w.beta, w.cu_seqlens, 2, w.scale,
+                                              S0_vmajor=w.initial_state)
+    assert rel_err(res["o"], o_ref) < 1e-12
+    assert rel_err(res["final_state"], fin_ref) < 1e-12
+    beta0 = torch.zeros(w.T * 2, 2)
+    res0 = oracle.forward(w.q, w.k, w.v, w.g, beta0, w.cu_seqlens, 2, w.scale, initial_state=w.initial_state,
+                          g_is_alpha=True)
+    a, q, S0 = f64(w.g), f64(w.q), f64(w.initial_state)
+    cu = w.cu_seqlens.tolist()
+    for i in range(w.N):
+        for h in range(2):
+            p = 1.0
+            for t in range(cu[i], cu[i + 1]):
+                p *= a[t, h]
+                np.testing.assert_allclose(res0["o"][t, h], w.scale * p * (S0[i, h] @ q[t, h]), rtol=1e-12,
+                                           atol=1e-14)
