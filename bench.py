@@ -36,7 +36,7 @@ UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 # DRAM traffic of the dominant kernel per launch, from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the sha256 of the
-# kernel source it was taken on; reported as null once the source changes.
+# kernel's sources (KERNEL_SOURCES) it was taken on; reported as null once they change.
 NCU_TRAFFIC = {"gdp_scan_kernel": {"sha": "830b7420307e60d2", "bytes_per_launch": 49147136, "workload": 2}}
 
 
@@ -138,9 +138,18 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def _kernel_sha(name: str) -> str:
-    p = os.path.join(ROOT, "chunked_gated_deltaproduct_gb300", "csrc", name)
-    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16] if os.path.exists(p) else ""
+KERNEL_SOURCES = {"gdp_desc_kernel": ("gdp_desc.cu",), "gdp_wy_kernel": ("gdp_wy.cu", "gdp_wy_body.cuh"),
+                  "gdp_scan_kernel": ("gdp_scan.cu", "gdp_scan_body.cuh")}
+
+
+def _kernel_sha(kernel: str) -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        p = os.path.join(ROOT, "chunked_gated_deltaproduct_gb300", "csrc", name)
+        if not os.path.exists(p):
+            return ""
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
 
 
 def cpu_oracle_baseline(w, budget_s: float):
@@ -364,9 +373,8 @@ def main():
     ab = alg_bytes(w)
     achieved = ab / (kernel_ms[dom] / 1e3) / 1e9
     step_gbs = ab / (statistics.fmean(step_ms) / 1e3) / 1e9
-    src_file = {0: "gdp_desc.cu", 1: "gdp_wy.cu", 2: "gdp_scan.cu"}[dom]
     tr = NCU_TRAFFIC.get(kernel_names[dom])
-    traffic = (tr["bytes_per_launch"] if (tr and tr.get("sha") == _kernel_sha(src_file)
+    traffic = (tr["bytes_per_launch"] if (tr and tr.get("sha") == _kernel_sha(kernel_names[dom])
                                           and tr.get("workload") == args.workload) else None)
 
     # ---- end to end: pinned host inputs -> device -> call -> host outputs

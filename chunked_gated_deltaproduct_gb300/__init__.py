@@ -5,6 +5,11 @@ The computation lives in ``libgdp_gb300.so`` (hand-written CUDA, C ABI in
 binding.
 """
 from .binding import (  # noqa: F401
+    GDP_ABI_VERSION,
+    GDP_DTYPE_BF16,
+    GDP_DTYPE_DEFAULT,
+    GDP_DTYPE_F16,
+    GDP_DTYPE_F32,
     GDP_DEV_ERR_CU_SEQLENS,
     GDP_DEV_ERR_DESC,
     GDP_DEV_ERR_SLOT,

@@ -22,6 +22,9 @@ LIB_PATH = os.path.join(_PKG, "libgdp_gb300.so")
 
 GDP_OK, GDP_ERR_INVALID_ARG, GDP_ERR_UNSUPPORTED, GDP_ERR_ALIAS, GDP_ERR_WORKSPACE, GDP_ERR_CUDA = range(6)
 GDP_DEV_ERR_CU_SEQLENS, GDP_DEV_ERR_SLOT, GDP_DEV_ERR_DESC, GDP_DEV_ERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+GDP_DTYPE_DEFAULT, GDP_DTYPE_F32, GDP_DTYPE_BF16, GDP_DTYPE_F16 = range(4)
+GDP_ABI_VERSION = 2
+_DTYPE_CODE = {torch.float32: GDP_DTYPE_F32, torch.bfloat16: GDP_DTYPE_BF16, torch.float16: GDP_DTYPE_F16}
 STATUS_NAMES = {0: "GDP_OK", 1: "GDP_ERR_INVALID_ARG", 2: "GDP_ERR_UNSUPPORTED", 3: "GDP_ERR_ALIAS",
                 4: "GDP_ERR_WORKSPACE", 5: "GDP_ERR_CUDA"}
 
@@ -45,6 +48,9 @@ class GdpPrefillArgs(ctypes.Structure):
         ("nt_pad", _i64), ("ntdp_pad", _i64),
         ("workspace", _vp), ("workspace_bytes", _sz),
         ("device_status", _vp),
+        # input variants (ABI version 2)
+        ("qkv_dtype", _int), ("g_dtype", _int), ("g_is_alpha", _int), ("beta_dtype", _int),
+        ("initial_state_dtype", _int), ("num_q_heads", _int), ("num_k_heads", _int), ("num_v_heads", _int),
     ]
 
 
@@ -86,7 +92,7 @@ def load_library(path: str | None = None):
     lib.gdp_ntdp_pad.restype = _i64
     lib.gdp_ntdp_pad.argtypes = [_i64, _i64, _int]
     lib.gdp_prefill_args_size.restype = _sz
-    if lib.gdp_prefill_args_size() != ctypes.sizeof(GdpPrefillArgs):
+    if lib.gdp_prefill_args_size() != ctypes.sizeof(GdpPrefillArgs) or lib.gdp_abi_version() != GDP_ABI_VERSION:
         raise RuntimeError("gdp_prefill_args layout mismatch between the binding and the library")
     if path is None:
         _lib = lib
@@ -179,21 +185,37 @@ def _addr(t):
     return t.data_ptr() if t is not None else None
 
 
-def make_args(q, k, v, g, beta, cu_seqlens, num_householder, scale, initial_state, state, state_indices,
-              output, output_state, chunk_states, chunk_indices, chunk_indices_dp, chunk_offsets,
-              nt_pad, ntdp_pad, use_qk_l2norm, workspace, device_status) -> GdpPrefillArgs:
-    """Fill a GdpPrefillArgs from tensors (no copies; the library checks shapes and modes)."""
-    T, H, K = q.shape
-    V = v.shape[-1]
+def _set_variants(a, q, k, v, g, beta, initial_state, state, g_is_alpha):
+    """Element types and head counts of the tensors -> the ABI-version-2 fields (the library
+    checks the combinations)."""
     for name, t in (("q", q), ("k", k), ("v", v)):
-        if t.dtype != torch.bfloat16:
-            raise GdpError(GDP_ERR_UNSUPPORTED, f"{name} must be bfloat16 (got {t.dtype})")
+        if t.dtype not in (torch.bfloat16, torch.float16) or t.dtype != q.dtype:
+            raise GdpError(GDP_ERR_UNSUPPORTED, f"{name} must be bfloat16 or float16, like q (got {t.dtype})")
         if t.stride(-1) != 1:
             raise GdpError(GDP_ERR_INVALID_ARG, f"{name} must be contiguous in its last dimension")
     for name, t in (("g", g), ("beta", beta), ("initial_state", initial_state), ("state", state)):
-        if t is not None and (t.dtype != torch.float32 or not t.is_contiguous()):
-            raise GdpError(GDP_ERR_UNSUPPORTED, f"{name} must be a contiguous float32 tensor")
+        if t is not None and (t.dtype not in _DTYPE_CODE or not t.is_contiguous()):
+            raise GdpError(GDP_ERR_UNSUPPORTED, f"{name} must be a contiguous float32/bfloat16/float16 tensor")
+    if state is not None and state.dtype != torch.float32:
+        raise GdpError(GDP_ERR_UNSUPPORTED, "the state cache is float32")
+    a.qkv_dtype = _DTYPE_CODE[q.dtype]
+    a.g_dtype = _DTYPE_CODE[g.dtype] if g is not None else 0
+    a.g_is_alpha = int(bool(g_is_alpha))
+    a.beta_dtype = _DTYPE_CODE[beta.dtype] if beta is not None else 0
+    a.initial_state_dtype = _DTYPE_CODE[initial_state.dtype] if initial_state is not None else 0
+    a.num_q_heads, a.num_k_heads, a.num_v_heads = q.shape[1], k.shape[1], v.shape[1]
+
+
+def make_args(q, k, v, g, beta, cu_seqlens, num_householder, scale, initial_state, state, state_indices,
+              output, output_state, chunk_states, chunk_indices, chunk_indices_dp, chunk_offsets,
+              nt_pad, ntdp_pad, use_qk_l2norm, workspace, device_status, g_is_alpha=False) -> GdpPrefillArgs:
+    """Fill a GdpPrefillArgs from tensors (no copies; the library checks shapes and modes).
+    q [T,Hq,K], k [T*M,Hk,K], v [T*M,Hv,V]: H = max(Hq, Hv) state heads."""
+    T, K = q.shape[0], q.shape[2]
+    H = max(q.shape[1], v.shape[1])
+    V = v.shape[-1]
     a = GdpPrefillArgs()
+    _set_variants(a, q, k, v, g, beta, initial_state, state, g_is_alpha)
     a.q, a.q_stride_t, a.q_stride_h = q.data_ptr(), q.stride(0), q.stride(1)
     a.k, a.k_stride_t, a.k_stride_h = k.data_ptr(), k.stride(0), k.stride(1)
     a.v, a.v_stride_t, a.v_stride_h = v.data_ptr(), v.stride(0), v.stride(1)
@@ -226,17 +248,13 @@ def gdp_decode_step(args: GdpPrefillArgs, stream: int | None = None) -> None:
 
 
 def decode_args(q, k, v, g, beta, num_householder, scale, initial_state, state, state_indices, output,
-                output_state, use_qk_l2norm, device_status) -> GdpPrefillArgs:
-    """GdpPrefillArgs of a decode step: q [N,H,K], k/v [N*M,H,K|V] bf16 (no copies)."""
-    N, H, K = q.shape
+                output_state, use_qk_l2norm, device_status, g_is_alpha=False) -> GdpPrefillArgs:
+    """GdpPrefillArgs of a decode step: q [N,Hq,K], k/v [N*M,Hk|Hv,K|V] bf16 or f16 (no copies)."""
+    N, K = q.shape[0], q.shape[2]
+    H = max(q.shape[1], v.shape[1])
     V = v.shape[-1]
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        if t.dtype != torch.bfloat16 or t.stride(-1) != 1:
-            raise GdpError(GDP_ERR_UNSUPPORTED, f"{name} must be bfloat16, contiguous in its last dimension")
-    for name, t in (("g", g), ("beta", beta), ("initial_state", initial_state), ("state", state)):
-        if t is not None and (t.dtype != torch.float32 or not t.is_contiguous()):
-            raise GdpError(GDP_ERR_UNSUPPORTED, f"{name} must be a contiguous float32 tensor")
     a = GdpPrefillArgs()
+    _set_variants(a, q, k, v, g, beta, initial_state, state, g_is_alpha)
     a.q, a.q_stride_t, a.q_stride_h = q.data_ptr(), q.stride(0), q.stride(1)
     a.k, a.k_stride_t, a.k_stride_h = k.data_ptr(), k.stride(0), k.stride(1)
     a.v, a.v_stride_t, a.v_stride_h = v.data_ptr(), v.stride(0), v.stride(1)
@@ -255,20 +273,22 @@ def decode_args(q, k, v, g, beta, num_householder, scale, initial_state, state, 
 def gated_delta_product_decode(q, k, v, g=None, beta=None, num_householder=1, scale=None, initial_state=None,
                                output_final_state=False, use_qk_l2norm_in_kernel=False, state=None,
                                state_indices=None, output=None, output_state=None, device_status=None,
-                               stream=None):
-    """One decode step: token i of sequence i, q [N,H,K], k/v [N*M,...] bf16, g [N,H], beta [N*M,H].
+                               stream=None, g_is_alpha=False):
+    """One decode step: token i of sequence i, q [N,Hq,K], k/v [N*M,Hk|Hv,...] bf16 or f16,
+    g [N,H] (natural-log decay, or alpha itself when ``g_is_alpha``), beta [N*M,H]; H = max(Hq, Hv).
 
-    Returns ``o`` [N,H,V] bf16, or ``(o, final_state)`` when output_final_state (dense mode).
-    In state-cache mode the cache is updated in place at ``state_indices``.
+    Returns ``o`` [N,H,V] in q's dtype, or ``(o, final_state)`` when output_final_state (dense
+    mode).  In state-cache mode the cache is updated in place at ``state_indices``.
     """
-    N, H, K = q.shape
+    N, K = q.shape[0], q.shape[2]
+    H = max(q.shape[1], v.shape[1])
     V = v.shape[-1]
     if output is None:
-        output = torch.empty((N, H, V), dtype=torch.bfloat16, device=q.device)
+        output = torch.empty((N, H, V), dtype=q.dtype, device=q.device)
     if output_final_state and state is None and output_state is None:
         output_state = torch.empty((N, H, V, K), dtype=torch.float32, device=q.device)
     a = decode_args(q, k, v, g, beta, num_householder, scale, initial_state, state, state_indices, output,
-                    output_state, use_qk_l2norm_in_kernel, device_status)
+                    output_state, use_qk_l2norm_in_kernel, device_status, g_is_alpha)
     gdp_decode_step(a, stream)
     if output_final_state and state is None:
         return output, output_state
@@ -286,15 +306,18 @@ def chunk_gated_delta_product(q, k, v, g=None, beta=None, cu_seqlens=None, num_h
                               initial_state=None, output_final_state=False, use_qk_l2norm_in_kernel=False,
                               chunk_indices=None, chunk_indices_dp=None, chunk_offsets=None, state=None,
                               state_indices=None, return_chunk_states=False, output=None, output_state=None,
-                              workspace=None, device_status=None, nt_pad=None, ntdp_pad=None, stream=None):
+                              workspace=None, device_status=None, nt_pad=None, ntdp_pad=None, stream=None,
+                              g_is_alpha=False):
     """Chunked Gated DeltaProduct varlen prefill on the GPU.
 
-    q [T,H,K] (or [1,T,H,K]), k/v [T*M,H,K]/[T*M,H,V] bf16; g [T,H] natural-log
-    decays fp32; beta [T*M,H] fp32; cu_seqlens [N+1] int32/int64 (required).
-    Returns ``o`` [T,H,V] bf16, or ``(o, final_state)`` when output_final_state,
-    or ``(o, final_state, chunk_states)`` when return_chunk_states.  In state-cache
-    mode (``state``/``state_indices``) the final state is written into the cache
-    and ``final_state`` is None.
+    q [T,Hq,K] (or [1,T,Hq,K]), k/v [T*M,Hk,K]/[T*M,Hv,V] bf16 or float16 (one type);
+    H = max(Hq, Hv) state heads, Hk equal to Hq or Hv, each dividing H.  g [T,H]
+    natural-log decays (or alpha itself in linear space when ``g_is_alpha``), fp32,
+    bf16 or f16; beta [T*M,H] fp32 or q's dtype; initial_state [N,H,V,K] fp32 or bf16;
+    cu_seqlens [N+1] int32/int64 (required).  Returns ``o`` [T,H,V] in q's dtype, or
+    ``(o, final_state)`` when output_final_state, or ``(o, final_state, chunk_states)``
+    when return_chunk_states (both fp32).  In state-cache mode (``state``/``state_indices``)
+    the final state is written into the cache and ``final_state`` is None.
     """
     if cu_seqlens is None:
         raise GdpError(GDP_ERR_INVALID_ARG, "cu_seqlens is required (packed THD input only)")
@@ -304,13 +327,14 @@ def chunk_gated_delta_product(q, k, v, g=None, beta=None, cu_seqlens=None, num_h
         g = g[0]
     if beta is not None and beta.dim() == 3:
         beta = beta[0]
-    T, H, K = q.shape
+    T, K = q.shape[0], q.shape[2]
+    H = max(q.shape[1], v.shape[1])
     V = v.shape[-1]
     M = int(num_householder)
     N = cu_seqlens.numel() - 1
     dev = q.device
     if output is None:
-        output = torch.empty((T, H, V), dtype=torch.bfloat16, device=dev)
+        output = torch.empty((T, H, V), dtype=q.dtype, device=dev)
     if output_final_state and state is None and output_state is None:
         output_state = torch.empty((N, H, V, K), dtype=torch.float32, device=dev)
     cs = None
@@ -321,7 +345,7 @@ def chunk_gated_delta_product(q, k, v, g=None, beta=None, cu_seqlens=None, num_h
         workspace = alloc_workspace(T, N, H, K, V, M, dev)
     a = make_args(q, k, v, g, beta, cu_seqlens, M, scale, initial_state, state, state_indices, output,
                   output_state if state is None else None, cs, chunk_indices, chunk_indices_dp, chunk_offsets,
-                  nt_pad, ntdp_pad, use_qk_l2norm_in_kernel, workspace, device_status)
+                  nt_pad, ntdp_pad, use_qk_l2norm_in_kernel, workspace, device_status, g_is_alpha)
     gdp_prefill_varlen(a, stream)
     final = output_state if (output_final_state and state is None) else None
     if return_chunk_states:

@@ -111,6 +111,50 @@ gdp_status record(cudaEvent_t ev, cudaStream_t stream) {
   return e == cudaSuccess ? GDP_OK : fail(GDP_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(e));
 }
 
+}  // namespace
+
+// The input-variant tail of gdp_prefill_args (FlashInfer page, parameters q, k, v, g,
+// beta, initial_state): checks it and fills the matching Problem fields.
+gdp_status gdp::resolve_variants(const gdp_prefill_args *a, Problem *p) {
+  const int H = a->H;
+  const int hq = a->num_q_heads ? a->num_q_heads : H, hk = a->num_k_heads ? a->num_k_heads : H,
+            hv = a->num_v_heads ? a->num_v_heads : H;
+  if (hq < 1 || hk < 1 || hv < 1 || H % hq || H % hk || H % hv || H != (hq > hv ? hq : hv) || (hk != hq && hk != hv))
+    return fail(GDP_ERR_INVALID_ARG,
+                "head counts q=%d k=%d v=%d: each must divide H=%d, H must equal max(q, v), k must equal q or v",
+                hq, hk, hv, H);
+  if (H > 65535) return fail(GDP_ERR_UNSUPPORTED, "H=%d above the 65535 heads one launch grid holds", H);
+  p->Hq = hq;
+  p->Hk = hk;
+  p->Hv = hv;
+  p->hmul_q = head_mul(H / hq);
+  p->hmul_k = head_mul(H / hk);
+  p->hmul_v = head_mul(H / hv);
+  const int qt = a->qkv_dtype ? a->qkv_dtype : GDP_DTYPE_BF16;
+  if (qt != GDP_DTYPE_BF16 && qt != GDP_DTYPE_F16)
+    return fail(GDP_ERR_UNSUPPORTED, "qkv_dtype %d: q, k, v are bfloat16 or float16", a->qkv_dtype);
+  p->f16 = qt == GDP_DTYPE_F16;
+  auto type_of = [](int dt) { return dt == GDP_DTYPE_BF16 ? kTypeBF16 : dt == GDP_DTYPE_F16 ? kTypeF16 : kTypeF32; };
+  const int gt = a->g_dtype ? a->g_dtype : GDP_DTYPE_F32;
+  if (gt != GDP_DTYPE_F32 && gt != GDP_DTYPE_BF16 && gt != GDP_DTYPE_F16)
+    return fail(GDP_ERR_UNSUPPORTED, "g_dtype %d: g is float32, bfloat16 or float16", a->g_dtype);
+  p->g_type = type_of(gt);
+  const int bt = a->beta_dtype ? a->beta_dtype : GDP_DTYPE_F32;
+  if (bt != GDP_DTYPE_F32 && bt != qt)
+    return fail(GDP_ERR_UNSUPPORTED, "beta_dtype %d: beta is float32 or the q/k/v type", a->beta_dtype);
+  p->beta_type = type_of(bt);
+  if (a->g_is_alpha != 0 && a->g_is_alpha != 1) return fail(GDP_ERR_INVALID_ARG, "g_is_alpha must be 0 or 1");
+  p->g_alpha = a->g_is_alpha;
+  const int st = a->initial_state_dtype ? a->initial_state_dtype : GDP_DTYPE_F32;
+  if (st != GDP_DTYPE_F32 && st != GDP_DTYPE_BF16)
+    return fail(GDP_ERR_UNSUPPORTED, "initial_state_dtype %d: the initial state is float32 or bfloat16",
+                a->initial_state_dtype);
+  p->init_bf16 = st == GDP_DTYPE_BF16;
+  return GDP_OK;
+}
+
+namespace {
+
 // Checks + launches shared by gdp_prefill_varlen and its profiled form.
 gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t const *ev) {
   g_last_error[0] = 0;
@@ -125,12 +169,15 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
   if (!a->cu_seqlens && N > 0) return fail(GDP_ERR_INVALID_ARG, "cu_seqlens is NULL");
   if (T > 0 && (!a->q || !a->k || !a->v || !a->output))
     return fail(GDP_ERR_INVALID_ARG, "q, k, v and output are required");
+  gdp::Problem p{};
+  gdp_status vst = gdp::resolve_variants(a, &p);
+  if (vst != GDP_OK) return vst;
   const int64_t strides[6] = {a->q_stride_t, a->q_stride_h, a->k_stride_t, a->k_stride_h, a->v_stride_t, a->v_stride_h};
   for (int i = 0; i < 6; ++i)
     if (T > 0 && (strides[i] <= 0 || strides[i] % 8 != 0))
       return fail(GDP_ERR_INVALID_ARG, "strides must be positive multiples of 8 elements (16 bytes)");
-  if (T > 0 && (a->q_stride_h < K || a->k_stride_h < K || a->v_stride_h < V || a->q_stride_t < (int64_t)H * K ||
-                a->k_stride_t < (int64_t)H * K || a->v_stride_t < (int64_t)H * V))
+  if (T > 0 && (a->q_stride_h < K || a->k_stride_h < K || a->v_stride_h < V || a->q_stride_t < (int64_t)p.Hq * K ||
+                a->k_stride_t < (int64_t)p.Hk * K || a->v_stride_t < (int64_t)p.Hv * V))
     return fail(GDP_ERR_INVALID_ARG, "strides describe overlapping rows");
   const uintptr_t align16 = ((uintptr_t)a->q | (uintptr_t)a->k | (uintptr_t)a->v | (uintptr_t)a->output) & 15u;
   if (align16) return fail(GDP_ERR_INVALID_ARG, "q, k, v and output must be 16-byte aligned");
@@ -144,7 +191,7 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
   if (a->state && a->output_state)
     return fail(GDP_ERR_INVALID_ARG, "in cache mode the final state is written to the cache; output_state must be NULL");
   const size_t state_bytes = sizeof(float) * (size_t)N * H * (size_t)V * K;
-  if (overlaps(a->output_state, state_bytes, a->initial_state, state_bytes))
+  if (overlaps(a->output_state, state_bytes, a->initial_state, p.init_bf16 ? state_bytes / 2 : state_bytes))
     return fail(GDP_ERR_ALIAS, "output_state must not alias initial_state");
   const int nprebuilt = (a->chunk_indices != nullptr) + (a->chunk_indices_dp != nullptr) + (a->chunk_offsets != nullptr);
   if (nprebuilt != 0 && nprebuilt != 3)
@@ -174,10 +221,9 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
   }
 
   char *ws = (char *)a->workspace;
-  gdp::Problem p{};
-  p.q = (const __nv_bfloat16 *)a->q;
-  p.k = (const __nv_bfloat16 *)a->k;
-  p.v = (const __nv_bfloat16 *)a->v;
+  p.q = a->q;
+  p.k = a->k;
+  p.v = a->v;
   p.q_st = a->q_stride_t; p.q_sh = a->q_stride_h;
   p.k_st = a->k_stride_t; p.k_sh = a->k_stride_h;
   p.v_st = a->v_stride_t; p.v_sh = a->v_stride_h;
@@ -192,7 +238,7 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
   p.cache = a->state;
   p.slots = a->state_indices;
   p.num_slots = a->num_slots;
-  p.out = (__nv_bfloat16 *)a->output;
+  p.out = a->output;
   p.out_state = a->output_state;
   p.chunk_states = a->chunk_states;
   p.nt_pad = nt_pad;

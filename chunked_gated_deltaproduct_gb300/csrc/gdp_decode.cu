@@ -8,7 +8,10 @@
 // sequence i and every head:
 //   S *= exp(g_t);  for j < M:  v_new = beta_j (v_j - S k_j),  S += v_new (x) k_j;
 //   o_t = scale S q_t
-// (k_j, q optionally L2-normalised: x / sqrt(sum x^2 + 1e-6)).
+// (k_j, q optionally L2-normalised: x / sqrt(sum x^2 + 1e-6)).  The input variants of the
+// prefill apply (FlashInfer page, parameters q, k, v, g, beta, initial_state): float16
+// q / k / v / output, a linear-space alpha gate (multiplied in directly), bf16 / f16 g and
+// beta, a bf16 initial state, and q / k / v heads grouped over the state heads.
 //
 // The step is bandwidth-bound: per (sequence, head) it reads and writes the 64 KB fp32
 // state and touches only M + 1 vectors of inputs.  One CTA per (sequence, head, 32 state
@@ -25,21 +28,28 @@ constexpr int kDecThreads = kDecRows * 4;  // four threads per row
 constexpr int kDecMaxM = 16;             // sub-token updates per token served by this kernel
 
 struct DecodeProblem {
-  const __nv_bfloat16 *q, *k, *v;
+  const void *q, *k, *v;  // bf16, or f16 when f16 != 0
   int64_t q_st, q_sh, k_st, k_sh, v_st, v_sh;
-  const float *g, *beta;
+  const void *g, *beta;   // element types g_type, beta_type
   int64_t N;
   int H, K, V, M;
+  uint64_t hmul_q, hmul_k, hmul_v;  // state head h reads head input_head(h, hmul_x) of q, k, v
+  int f16, g_type, beta_type, g_alpha, init_bf16;
   float scale;
   int l2norm;
-  const float *init;
+  const void *init;       // fp32, or bf16 when init_bf16 != 0
   float *cache;
   const int32_t *slots;
   int64_t num_slots;
-  __nv_bfloat16 *out;
+  void *out;              // the q / k / v type
   float *out_state;
   uint32_t *status;
 };
+
+__device__ __forceinline__ float load16(const void *base, int64_t i, int f16) {
+  return f16 ? __half2float(static_cast<const __half *>(base)[i])
+             : __bfloat162float(static_cast<const __nv_bfloat16 *>(base)[i]);
+}
 
 template <int D>
 __global__ void __launch_bounds__(kDecThreads) gdp_decode_kernel(DecodeProblem p) {
@@ -48,6 +58,7 @@ __global__ void __launch_bounds__(kDecThreads) gdp_decode_kernel(DecodeProblem p
   const int tid = threadIdx.x, r = tid >> 2, qd = tid & 3;
   const int vrow = blockIdx.z * kDecRows + r;
   const int M = p.M;
+  const int hq = input_head(h, p.hmul_q), hk = input_head(h, p.hmul_k), hv = input_head(h, p.hmul_v);
   __shared__ float kf[kDecMaxM][D];
   __shared__ float qf[D];
   __shared__ float vv[kDecMaxM][kDecRows];
@@ -57,6 +68,7 @@ __global__ void __launch_bounds__(kDecThreads) gdp_decode_kernel(DecodeProblem p
   // the state row: slot / initial state / zero
   int slot = -1;
   const float *src = nullptr;
+  const __nv_bfloat16 *src16 = nullptr;  // a bf16 initial state
   float *dst = nullptr;
   if (p.cache) {
     slot = p.slots[i];
@@ -66,7 +78,10 @@ __global__ void __launch_bounds__(kDecThreads) gdp_decode_kernel(DecodeProblem p
     }
     if (slot >= 0) src = dst = p.cache + ((int64_t)slot * p.H + h) * (int64_t)p.V * D;
   } else {
-    if (p.init) src = p.init + ((int64_t)i * p.H + h) * (int64_t)p.V * D;
+    if (p.init && p.init_bf16)
+      src16 = static_cast<const __nv_bfloat16 *>(p.init) + ((int64_t)i * p.H + h) * (int64_t)p.V * D;
+    else if (p.init)
+      src = static_cast<const float *>(p.init) + ((int64_t)i * p.H + h) * (int64_t)p.V * D;
     if (p.out_state) dst = p.out_state + ((int64_t)i * p.H + h) * (int64_t)p.V * D;
   }
   // thread (row, qd) holds columns 16 g' + 4 qd .. + 3 for g' < G: a warp's 4-thread groups
@@ -76,7 +91,14 @@ __global__ void __launch_bounds__(kDecThreads) gdp_decode_kernel(DecodeProblem p
 #pragma unroll
   for (int gi = 0; gi < G; ++gi) {
     float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (src) x = *reinterpret_cast<const float4 *>(src + (int64_t)vrow * D + gi * 16 + qd * 4);
+    if (src) {
+      x = *reinterpret_cast<const float4 *>(src + (int64_t)vrow * D + gi * 16 + qd * 4);
+    } else if (src16) {
+      const uint2 y = *reinterpret_cast<const uint2 *>(src16 + (int64_t)vrow * D + gi * 16 + qd * 4);
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&y.x));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&y.y));
+      x = make_float4(a.x, a.y, b.x, b.y);
+    }
     s[4 * gi] = x.x; s[4 * gi + 1] = x.y; s[4 * gi + 2] = x.z; s[4 * gi + 3] = x.w;
   }
   // inputs of the token: k rows i*M + j, q row i, this block's v entries, beta, gate
@@ -84,16 +106,16 @@ __global__ void __launch_bounds__(kDecThreads) gdp_decode_kernel(DecodeProblem p
     const int j = idx / D, c = idx % D;
     float x;
     if (j < M)
-      x = __bfloat162float(p.k[((int64_t)i * M + j) * p.k_st + (int64_t)h * p.k_sh + c]);
+      x = load16(p.k, ((int64_t)i * M + j) * p.k_st + (int64_t)hk * p.k_sh + c, p.f16);
     else
-      x = __bfloat162float(p.q[(int64_t)i * p.q_st + (int64_t)h * p.q_sh + c]);
+      x = load16(p.q, (int64_t)i * p.q_st + (int64_t)hq * p.q_sh + c, p.f16);
     if (j < M) kf[j][c] = x; else qf[c] = x;
   }
   for (int idx = tid; idx < M * kDecRows; idx += kDecThreads) {
     const int j = idx / kDecRows, rr = idx % kDecRows;
-    vv[j][rr] = __bfloat162float(p.v[((int64_t)i * M + j) * p.v_st + (int64_t)h * p.v_sh + blockIdx.z * kDecRows + rr]);
+    vv[j][rr] = load16(p.v, ((int64_t)i * M + j) * p.v_st + (int64_t)hv * p.v_sh + blockIdx.z * kDecRows + rr, p.f16);
   }
-  if (tid < M) bt[tid] = p.beta ? p.beta[((int64_t)i * M + tid) * p.H + h] : 1.f;
+  if (tid < M) bt[tid] = p.beta ? load_typed(p.beta, ((int64_t)i * M + tid) * p.H + h, p.beta_type) : 1.f;
   __syncthreads();
   if (p.l2norm) {  // one warp per vector: 1 / sqrt(sum x^2 + eps)
     const int warp = tid >> 5, lane = tid & 31;
@@ -113,7 +135,12 @@ __global__ void __launch_bounds__(kDecThreads) gdp_decode_kernel(DecodeProblem p
     __syncthreads();
   }
 
-  const float decay = p.g ? __expf(p.g[(int64_t)i * p.H + h]) : 1.f;
+  // alpha_t = exp(g_t), or g_t itself for a linear-space gate (floored like the prefill's)
+  float decay = 1.f;
+  if (p.g) {
+    const float x = load_typed(p.g, (int64_t)i * p.H + h, p.g_type);
+    decay = p.g_alpha ? fmaxf(x, __expf(kMinLogAlpha)) : __expf(x);
+  }
 #pragma unroll
   for (int c = 0; c < 4 * G; ++c) s[c] *= decay;
   for (int j = 0; j < M; ++j) {
@@ -137,7 +164,10 @@ __global__ void __launch_bounds__(kDecThreads) gdp_decode_kernel(DecodeProblem p
     for (int u = 0; u < 4; ++u) o += s[4 * gi + u] * qf[gi * 16 + qd * 4 + u];
   o += __shfl_xor_sync(0xffffffffu, o, 1);
   o += __shfl_xor_sync(0xffffffffu, o, 2);
-  if (qd == 0) p.out[((int64_t)i * p.H + h) * p.V + vrow] = __float2bfloat16_rn(p.scale * o);
+  if (qd == 0) {
+    uint16_t *out = static_cast<uint16_t *>(p.out) + ((int64_t)i * p.H + h) * p.V + vrow;
+    *out = p.f16 ? __half_as_ushort(__float2half_rn(p.scale * o)) : __bfloat16_as_ushort(__float2bfloat16_rn(p.scale * o));
+  }
   if (dst) {
 #pragma unroll
     for (int gi = 0; gi < G; ++gi)
@@ -176,15 +206,21 @@ GDP_EXPORT gdp_status gdp_decode_step(const gdp_prefill_args *a, void *stream) {
   if (a->state && a->output_state)
     return fail(GDP_ERR_INVALID_ARG, "in cache mode the final state is written to the cache; output_state must be NULL");
   if (a->chunk_states) return fail(GDP_ERR_INVALID_ARG, "chunk_states has no meaning for a decode step");
+  gdp::Problem vp{};
+  const gdp_status vst = gdp::resolve_variants(a, &vp);
+  if (vst != GDP_OK) return vst;
   if (a->initial_state && a->output_state) {
     const size_t bytes = sizeof(float) * (size_t)N * H * (size_t)V * K;
+    const size_t ibytes = vp.init_bf16 ? bytes / 2 : bytes;
     const uintptr_t x = (uintptr_t)a->initial_state, y = (uintptr_t)a->output_state;
-    if (x != y && x < y + bytes && y < x + bytes)
-      return fail(GDP_ERR_ALIAS, "output_state overlaps initial_state (only an exact in-place update is allowed)");
+    if ((x != y || vp.init_bf16) && x < y + bytes && y < x + ibytes)
+      return fail(GDP_ERR_ALIAS, "output_state overlaps initial_state (only an exact in-place fp32 update is allowed)");
   }
   if (N == 0) return GDP_OK;
   gdp::DecodeProblem p{};
-  p.q = (const __nv_bfloat16 *)a->q; p.k = (const __nv_bfloat16 *)a->k; p.v = (const __nv_bfloat16 *)a->v;
+  p.q = a->q; p.k = a->k; p.v = a->v;
+  p.hmul_q = vp.hmul_q; p.hmul_k = vp.hmul_k; p.hmul_v = vp.hmul_v;
+  p.f16 = vp.f16; p.g_type = vp.g_type; p.beta_type = vp.beta_type; p.g_alpha = vp.g_alpha; p.init_bf16 = vp.init_bf16;
   p.q_st = a->q_stride_t; p.q_sh = a->q_stride_h;
   p.k_st = a->k_stride_t; p.k_sh = a->k_stride_h;
   p.v_st = a->v_stride_t; p.v_sh = a->v_stride_h;
@@ -193,7 +229,7 @@ GDP_EXPORT gdp_status gdp_decode_step(const gdp_prefill_args *a, void *stream) {
   p.scale = (a->scale > 0.f && a->scale == a->scale) ? a->scale : 1.0f / sqrtf((float)K);
   p.l2norm = a->use_qk_l2norm ? 1 : 0;
   p.init = a->initial_state; p.cache = a->state; p.slots = a->state_indices; p.num_slots = a->num_slots;
-  p.out = (__nv_bfloat16 *)a->output; p.out_state = a->output_state; p.status = a->device_status;
+  p.out = a->output; p.out_state = a->output_state; p.status = a->device_status;
   dim3 grid((unsigned)N, (unsigned)H, (unsigned)(V / gdp::kDecRows));
   cudaStream_t s = (cudaStream_t)stream;
   if (K == 128)

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -74,21 +75,26 @@ struct ImageMeta {
 };
 
 // Everything a kernel needs about one call (passed by value).
+// Element types of g, beta and the initial state (q, k, v and the output: bf16 or f16).
+constexpr int kTypeF32 = 0, kTypeBF16 = 1, kTypeF16 = 2;
+// An alpha gate is read as max(log(alpha), kMinLogAlpha): alpha <= 0 stays finite.
+constexpr float kMinLogAlpha = -80.f;
+
 struct Problem {
-  const __nv_bfloat16 *q, *k, *v;
+  const void *q, *k, *v;  // bf16, or f16 when f16 != 0
   int64_t q_st, q_sh, k_st, k_sh, v_st, v_sh;
-  const float *g, *beta;
+  const void *g, *beta;   // element types g_type, beta_type
   const void *cu;
   int cu64;
   int64_t T, N;
   int H, K, V, M;
   float scale;
   int l2norm;
-  const float *init;
+  const void *init;  // fp32, or bf16 when init_bf16 != 0
   float *cache;
   const int32_t *slots;
   int64_t num_slots;
-  __nv_bfloat16 *out;
+  void *out;  // same type as q, k, v
   float *out_state;
   float *chunk_states;
   const int32_t *ci, *cid, *co, *cod;
@@ -111,7 +117,33 @@ struct Problem {
   float *seg_state;
   // scan: prefetch image and U^T tiles into L2 ahead of use (few chains: HBM has headroom)
   int prefetch;
+  // input variants: head counts of q, k, v (each divides H; state head h reads head
+  // h / (H / Hx), computed as input_head(h, hmul_x)), element types, linear-space gate
+  int Hq, Hk, Hv;
+  uint64_t hmul_q, hmul_k, hmul_v;  // ceil(2^32 / (H / Hx))
+  int f16;               // q, k, v and the output are float16 (else bfloat16)
+  int g_type, beta_type;  // kType*
+  int g_alpha;           // g holds alpha itself (else its natural log)
+  int init_bf16;         // the dense initial state is bfloat16 (else fp32)
 };
+
+// Input head h / r of state head h, with m = ceil(2^32 / r): (h m) >> 32 equals h / r for
+// every h < 2^16 and r <= 2^16 (the rounding excess of m stays below 2^-16 <= 1 / r), and it
+// takes one wide multiply instead of a division.
+__device__ __forceinline__ int input_head(int h, uint64_t m) { return (int)(((uint64_t)h * m) >> 32); }
+__host__ inline uint64_t head_mul(int ratio) { return ((1ull << 32) + (uint64_t)ratio - 1) / (uint64_t)ratio; }
+
+// One element of a g / beta array of element type `type`, as fp32.
+__device__ __forceinline__ float load_typed(const void *base, int64_t i, int type) {
+  if (type == kTypeF32) return reinterpret_cast<const float *>(base)[i];
+  const uint32_t u = reinterpret_cast<const uint16_t *>(base)[i];
+  return type == kTypeBF16 ? __uint_as_float(u << 16) : __half2float(__ushort_as_half((unsigned short)u));
+}
+// The natural-log decay of token row i of g (alpha = exp of it).
+__device__ __forceinline__ float load_log_gate(const Problem &p, int64_t i) {
+  const float x = load_typed(p.g, i, p.g_type);
+  return p.g_alpha ? fmaxf(logf(x), kMinLogAlpha) : x;  // fmaxf also maps NaN (alpha < 0) to the floor
+}
 
 // Long sequences over few (sequence, head) chains are processed in segments of
 // kSegChunks expanded chunks, so that the WY tiles of segment k + 1 are built on the
@@ -142,18 +174,24 @@ cudaError_t launch_descriptors(const void *cu, int cu64, int64_t T, int64_t N, i
                                int32_t *cid, int64_t ntdp_pad, int32_t *co, int32_t *cod, uint32_t *status,
                                cudaStream_t stream);
 cudaError_t launch_wy(const Problem &p, cudaStream_t stream);
+// The WY kernel for float16 inputs (f16) and / or 16-bit or linear-space gates (typed).
+cudaError_t launch_wy_variant(const Problem &p, cudaStream_t stream, bool f16, bool typed);
 cudaError_t launch_scan(const Problem &p, cudaStream_t stream);
+// The scan for float16 inputs (f16) and / or a bfloat16 dense initial state (init16).
+cudaError_t launch_scan_variant(const Problem &p, cudaStream_t stream, bool f16, bool init16);
 
 // TMA tensor maps (gdp_tmap.cu; `map` points at a 64-byte aligned CUtensorMap; a NULL base
 // leaves it zeroed).  All use the 128-byte swizzle.
 //   tmap_state:     [rows][d] fp32, 32 x 32 boxes
-//   tmap_rows_bf16: [rows][H][K] bf16 with element strides (stride_t, stride_h), boxes of
-//                   64 features x 1 head x box_rows rows
+//   tmap_rows_16:   [rows][H][K] bf16 (f16 = 0) or float16 (f16 = 1) with element strides
+//                   (stride_t, stride_h), boxes of 64 features x 1 head x box_rows rows
 cudaError_t tmap_state(void *map, float *base, int64_t rows, int d);
-cudaError_t tmap_rows_bf16(void *map, const void *base, int64_t rows, int H, int K, int64_t stride_t, int64_t stride_h,
-                           int box_rows);
+cudaError_t tmap_rows_16(void *map, const void *base, int64_t rows, int H, int K, int64_t stride_t, int64_t stride_h,
+                         int box_rows, int f16);
 
 // Sets the calling thread's gdp_last_error() text (defined in gdp_api.cu).
 void set_last_error(const char *fmt, ...);
+// Checks the input-variant fields of the arguments and fills p's Hq/Hk/Hv and type fields.
+gdp_status resolve_variants(const gdp_prefill_args *a, Problem *p);
 
 }  // namespace gdp

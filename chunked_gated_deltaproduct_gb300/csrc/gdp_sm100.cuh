@@ -29,13 +29,14 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr, uint32_t lbo, uint
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-// Instruction descriptor for kind::f16 / kind::tf32: D fp32; a/b format 1 = bf16, 2 = tf32;
+// Instruction descriptor for kind::f16 / kind::tf32: D fp32; a/b format 0 = f16, 1 = bf16, 2 = tf32
+// (A and B always of one type);
 // major 0 = K-major, 1 = MN-major; N >> 3 at bit 17; M >> 4 at bit 24.
 __host__ __device__ constexpr uint32_t idesc(int afmt, int amaj, int bmaj, int N, int M) {
   return (1u << 4) | ((uint32_t)afmt << 7) | ((uint32_t)afmt << 10) | ((uint32_t)amaj << 15) |
          ((uint32_t)bmaj << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
-constexpr int kFmtBF16 = 1, kFmtTF32 = 2;
+constexpr int kFmtF16 = 0, kFmtBF16 = 1, kFmtTF32 = 2;
 
 __device__ __forceinline__ void mma_bf16_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
   asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"

@@ -47,15 +47,16 @@ cudaError_t tmap_state(void *map, float *base, int64_t rows, int d) {
   return encode(static_cast<CUtensorMap *>(map), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box);
 }
 
-cudaError_t tmap_rows_bf16(void *map, const void *base, int64_t rows, int H, int K, int64_t stride_t, int64_t stride_h,
-                           int box_rows) {
+cudaError_t tmap_rows_16(void *map, const void *base, int64_t rows, int H, int K, int64_t stride_t, int64_t stride_h,
+                         int box_rows, int f16) {
   memset(map, 0, sizeof(CUtensorMap));
   if (!base || rows <= 0) return cudaSuccess;
   const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)H, (cuuint64_t)rows};
   const cuuint64_t strides[2] = {(cuuint64_t)stride_h * 2u, (cuuint64_t)stride_t * 2u};
   const cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
-  return encode(static_cast<CUtensorMap *>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
-                strides, box);
+  return encode(static_cast<CUtensorMap *>(map),
+                f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base),
+                dims, strides, box);
 }
 
 }  // namespace gdp

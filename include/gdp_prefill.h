@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define GDP_ABI_VERSION 1
+#define GDP_ABI_VERSION 2 /* 2: the input-variant fields at the end of gdp_prefill_args */
 #define GDP_CHUNK 64 /* chunk size of both streams (Megatron page, stage list) */
 
 typedef enum gdp_status {
@@ -57,6 +57,14 @@ typedef enum gdp_status {
   GDP_ERR_CUDA = 5         /* a CUDA launch/attribute call failed (reason in gdp_last_error) */
 } gdp_status;
 
+/* Element types of the input-variant fields (gdp_prefill_args, ABI version 2). */
+typedef enum gdp_dtype {
+  GDP_DTYPE_DEFAULT = 0, /* the field's version-1 type */
+  GDP_DTYPE_F32 = 1,
+  GDP_DTYPE_BF16 = 2,
+  GDP_DTYPE_F16 = 3
+} gdp_dtype;
+
 /* Bits OR-ed into *device_status by the kernels. */
 #define GDP_DEV_ERR_CU_SEQLENS 0x1u /* cu_seqlens not non-decreasing from 0 to T: bad sequences skipped */
 #define GDP_DEV_ERR_SLOT 0x2u       /* state_indices entry outside [-1, num_slots): treated as padding */
@@ -66,19 +74,22 @@ typedef enum gdp_status {
 
 /*
  * Arguments of one prefill call.  Shapes use T real tokens, N sequences,
- * H heads (q, k, v and the gates share one head count), K = V = head size,
- * M = num_householder.  Element strides are in ELEMENTS; the innermost
- * dimension is always contiguous (FlashInfer page, parameter q).
+ * H state heads (the heads of g, beta, the states and the output; q, k and v
+ * have H heads unless the head-count fields at the end say otherwise),
+ * K = V = head size, M = num_householder.  Element strides are in ELEMENTS;
+ * the innermost dimension is always contiguous (FlashInfer page, parameter q).
+ * The types named below are those of a zero-filled variant tail (the fields
+ * after device_status); those fields widen them.
  */
 typedef struct gdp_prefill_args {
-  /* q [T, H, K] bf16 at real-token rows (FlashInfer page, parameter q). */
+  /* q [T, Hq, K] bf16 at real-token rows (FlashInfer page, parameter q). */
   const void *q;
   int64_t q_stride_t, q_stride_h;
-  /* k [T*M, H, K] bf16 on the expanded stream: token t's M updates are rows
+  /* k [T*M, Hk, K] bf16 on the expanded stream: token t's M updates are rows
      t*M .. t*M+M-1 (FlashInfer page, parameter k; Megatron page, parameter k). */
   const void *k;
   int64_t k_stride_t, k_stride_h;
-  /* v [T*M, H, V] bf16, same rows as k (FlashInfer page, parameter v). */
+  /* v [T*M, Hv, V] bf16, same rows as k (FlashInfer page, parameter v). */
   const void *v;
   int64_t v_stride_t, v_stride_h;
   /* g [T, H] fp32, contiguous: natural-log decay, alpha_t = exp(g_t)
@@ -147,6 +158,37 @@ typedef struct gdp_prefill_args {
   size_t workspace_bytes;
   /* Optional uint32 status word; GDP_DEV_ERR_* bits are OR-ed in. */
   uint32_t *device_status;
+
+  /* ---- Input variants (ABI version 2; zero keeps every type and head count
+     above).  FlashInfer page, parameters q, k, v, g, beta, initial_state. ---- */
+  /* Type of q, k, v and output: GDP_DTYPE_BF16 (DEFAULT) or GDP_DTYPE_F16
+     (parameters q, k, v: float16 or bfloat16).  The output takes this type. */
+  int qkv_dtype;
+  /* Type of g: GDP_DTYPE_F32 (DEFAULT), GDP_DTYPE_BF16 or GDP_DTYPE_F16
+     (parameter g).  Contiguous [T, H] in every type. */
+  int g_dtype;
+  /* 0: g holds natural-log decays, alpha_t = exp(g_t) (Megatron page,
+     parameter g).  1: g holds alpha_t itself, the forget gate in linear space,
+     in (0, 1] (FlashInfer page, parameter g).  An alpha outside that range is
+     read as max(alpha, exp(-80)): zero or a negative value decays the state to
+     about 1e-35 of itself instead of producing NaN. */
+  int g_is_alpha;
+  /* Type of beta: GDP_DTYPE_F32 (DEFAULT) or the q/k/v type (parameter beta:
+     float32 or q.dtype).  Contiguous [T*M, H]. */
+  int beta_dtype;
+  /* Type of initial_state: GDP_DTYPE_F32 (DEFAULT) or GDP_DTYPE_BF16
+     (parameter initial_state).  The cache `state`, output_state and
+     chunk_states are always fp32. */
+  int initial_state_dtype;
+  /* Head counts of q, k and v; 0 means H.  Every count divides H,
+     H = max(num_q_heads, num_v_heads), and num_k_heads equals num_q_heads or
+     num_v_heads (parameters k, v).  State head h reads q head
+     h / (H / num_q_heads), k head h / (H / num_k_heads) and v head
+     h / (H / num_v_heads): a head of a smaller count serves a run of
+     consecutive state heads (the page names the counts but not the map; this
+     is the reading taken).  The head strides above are per head of each
+     tensor.  Any other combination is GDP_ERR_INVALID_ARG. */
+  int num_q_heads, num_k_heads, num_v_heads;
 } gdp_prefill_args;
 
 /* Shape-only descriptor bounds: floor((T + 63 N) / 64) and floor((M T + 63 N) / 64). */

@@ -30,7 +30,7 @@ def run(w, dev, d=None, prebuilt=False, status=None, scale=None, **kw):
         initial_state=d["init"], output_final_state=w.output_final_state,
         use_qk_l2norm_in_kernel=w.use_qk_l2norm, chunk_indices=ci, chunk_indices_dp=cid, chunk_offsets=co,
         state=d["state"], state_indices=d["sidx"], return_chunk_states=w.return_chunk_states,
-        device_status=status, **kw)
+        device_status=status, g_is_alpha=w.g_is_alpha, **kw)
     torch.cuda.synchronize()
     if isinstance(res, tuple):
         o = res[0]

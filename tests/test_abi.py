@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(lib):
     assert "gdp_prefill_varlen" in declared and "gdp_build_descriptors" in declared
     for name in declared:
         assert hasattr(lib, name), f"{name} declared in include/ but not exported"
-    assert lib.gdp_abi_version() == 1
+    assert lib.gdp_abi_version() == pkg.GDP_ABI_VERSION == 2
 
 
 def test_args_struct_layout(lib):
@@ -93,6 +93,21 @@ def _args(**over):
     (dict(workspace_bytes=64), pkg.GDP_ERR_WORKSPACE),
     (dict(T=200, nt_pad=1, ntdp_pad=1, chunk_indices=1 << 21, chunk_indices_dp=1 << 21, chunk_offsets=1 << 21),
      pkg.GDP_ERR_INVALID_ARG),
+    # input variants (ABI version 2)
+    (dict(qkv_dtype=pkg.GDP_DTYPE_F32), pkg.GDP_ERR_UNSUPPORTED),
+    (dict(qkv_dtype=7), pkg.GDP_ERR_UNSUPPORTED),
+    (dict(g_dtype=9), pkg.GDP_ERR_UNSUPPORTED),
+    (dict(beta_dtype=pkg.GDP_DTYPE_F16), pkg.GDP_ERR_UNSUPPORTED),  # neither fp32 nor the (bf16) q type
+    (dict(qkv_dtype=pkg.GDP_DTYPE_F16, beta_dtype=pkg.GDP_DTYPE_BF16), pkg.GDP_ERR_UNSUPPORTED),
+    (dict(initial_state_dtype=pkg.GDP_DTYPE_F16), pkg.GDP_ERR_UNSUPPORTED),
+    (dict(g_is_alpha=2), pkg.GDP_ERR_INVALID_ARG),
+    (dict(H=4, num_q_heads=3, num_k_heads=3), pkg.GDP_ERR_INVALID_ARG),  # 3 does not divide 4
+    (dict(H=4, num_q_heads=2, num_k_heads=2, num_v_heads=2), pkg.GDP_ERR_INVALID_ARG),  # H != max(q, v)
+    (dict(H=4, num_q_heads=4, num_k_heads=1, num_v_heads=2), pkg.GDP_ERR_INVALID_ARG),  # k neither q nor v
+    (dict(H=4, num_q_heads=2, num_k_heads=2, num_v_heads=4, q_stride_t=64, k_stride_t=128, v_stride_t=256),
+     pkg.GDP_ERR_INVALID_ARG),  # q rows of 2 heads need a stride of 128
+    (dict(initial_state=1 << 24, initial_state_dtype=pkg.GDP_DTYPE_BF16, output_state=(1 << 24) + 4096),
+     pkg.GDP_ERR_ALIAS),  # the bf16 state spans 8 KB
 ])
 def test_host_validation(lib, over, status):
     a = _args(**over)
@@ -117,3 +132,17 @@ def test_empty_batch_is_ok_without_launch(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError):
         pkg.load_library(str(tmp_path / "nope.so"))
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(qkv_dtype=pkg.GDP_DTYPE_F32), pkg.GDP_ERR_UNSUPPORTED),
+    (dict(H=4, num_q_heads=3, num_k_heads=3), pkg.GDP_ERR_INVALID_ARG),
+    (dict(g_is_alpha=-1), pkg.GDP_ERR_INVALID_ARG),
+    # an exact in-place update exists only for an fp32 initial state
+    (dict(initial_state=1 << 24, output_state=1 << 24, initial_state_dtype=pkg.GDP_DTYPE_BF16), pkg.GDP_ERR_ALIAS),
+])
+def test_decode_host_validation(lib, over, status):
+    a = _args(T=1, N=1, **over)
+    st = lib.gdp_decode_step(ctypes.byref(a), None)
+    assert st == status, (st, pkg.gdp_last_error())
+    assert pkg.gdp_last_error() != ""
