@@ -265,8 +265,11 @@ gdp_status gdp_build_descriptors(const void *cu_seqlens, int cu_seqlens_int64, i
  * prefill: the cache `state` is read and written in place at state_indices[i] (-1:
  * start from zero, write nothing); otherwise initial_state[i] (or zero) is read and
  * output_state[i] written, and output_state may equal initial_state exactly (an
- * in-place update) but not partly overlap it (GDP_ERR_ALIAS).  K = V in {64, 128},
- * 1 <= M <= 16 (GDP_ERR_UNSUPPORTED otherwise).  No workspace; graph-capturable.
+ * in-place update, fp32 initial state only) but not partly overlap it
+ * (GDP_ERR_ALIAS).  The input-variant fields (types, alpha gate, head counts)
+ * apply as for the prefill; with g_is_alpha the state is multiplied by
+ * max(alpha, exp(-80)) directly.  K = V in {64, 128}, 1 <= M <= 16
+ * (GDP_ERR_UNSUPPORTED otherwise).  No workspace; graph-capturable.
  */
 gdp_status gdp_decode_step(const gdp_prefill_args *args, void *stream);
 
