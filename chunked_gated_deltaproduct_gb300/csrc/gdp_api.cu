@@ -265,6 +265,9 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
   p.seg_state = nullptr;
   p.prefetch = (N * (int64_t)H <= gdp::kSegMaxChains) ? 1 : 0;
   const int nseg = seg_count(T, N, H, M);
+  // desc -> WY -> scan on one stream overlap their launches (programmatic dependent launch);
+  // the profiled form records events between them, so there each kernel runs alone
+  p.pdl = (nseg == 1 && !ev) ? 1 : 0;
   SideStreams *ss = nseg > 1 ? side_streams() : nullptr;
   if (nseg > 1 && !ss) return fail(GDP_ERR_CUDA, "could not create the internal streams of the segmented mode");
 

@@ -8,14 +8,17 @@
 // makes the call capturable).
 //
 // One CTA: a block-wide exclusive scan over the sequences (tiles of 1024),
-// then every padded row finds its sequence by binary search over the offsets.
-// Grid and block sizes depend on nothing but the padded lengths.
+// then every padded row finds its sequence by binary search over the offsets
+// (kept in shared memory up to kDescSmemSeqs sequences, else read back from
+// global memory).  Grid and block sizes depend on nothing but the padded lengths.
 #include "gdp_internal.cuh"
+#include "gdp_sm100.cuh"
 
 namespace gdp {
 namespace {
 
 constexpr int kDescThreads = 1024;
+constexpr int kDescSmemSeqs = 2048;  // offsets of up to this many sequences stay in shared memory
 
 __device__ __forceinline__ int block_exclusive_scan(int x, int *warp_sums, int *total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -70,6 +73,9 @@ __global__ void __launch_bounds__(kDescThreads) gdp_desc_kernel(const void *cu, 
   __shared__ int warp_sums[32];
   __shared__ int tot_a, tot_b;
   __shared__ int carry_a, carry_b;
+  __shared__ int32_t s_co[kDescSmemSeqs + 1], s_cod[kDescSmemSeqs + 1];
+  const bool in_smem = N <= kDescSmemSeqs;
+  sm100::pdl_trigger();  // the WY kernel may start launching; it waits for these descriptors
   if (threadIdx.x == 0) {
     carry_a = carry_b = 0;
     if (N > 0 && (load_cu(cu, cu64, 0) != 0 || load_cu(cu, cu64, N) != T)) set_status(status, GDP_DEV_ERR_CU_SEQLENS);
@@ -89,6 +95,10 @@ __global__ void __launch_bounds__(kDescThreads) gdp_desc_kernel(const void *cu, 
     if (i < N) {
       if (co) co[i] = carry_a + ea;
       if (cod) cod[i] = carry_b + eb;
+      if (in_smem) {
+        s_co[i] = carry_a + ea;
+        s_cod[i] = carry_b + eb;
+      }
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -102,10 +112,14 @@ __global__ void __launch_bounds__(kDescThreads) gdp_desc_kernel(const void *cu, 
     if ((ci && a > nt_pad) || (cid && b > ntdp_pad)) set_status(status, GDP_DEV_ERR_DESC);
     if (co) co[N] = a;
     if (cod) cod[N] = b;
+    if (in_smem) {
+      s_co[N] = a;
+      s_cod[N] = b;
+    }
   }
   __syncthreads();  // makes the offsets written above visible to the whole block
-  if (ci) fill_rows(ci, nt_pad, co, N);
-  if (cid) fill_rows(cid, ntdp_pad, cod, N);
+  if (ci) fill_rows(ci, nt_pad, in_smem ? s_co : co, N);
+  if (cid) fill_rows(cid, ntdp_pad, in_smem ? s_cod : cod, N);
 }
 
 }  // namespace

@@ -125,7 +125,27 @@ struct Problem {
   int g_type, beta_type;  // kType*
   int g_alpha;           // g holds alpha itself (else its natural log)
   int init_bf16;         // the dense initial state is bfloat16 (else fp32)
+  // launch the WY and scan kernels with programmatic stream serialization: each may start while
+  // its predecessor finishes and waits (griddepcontrol.wait) before reading that one's outputs
+  int pdl;
 };
+
+// Launch `kern` on `stream`, with programmatic stream serialization when `pdl`.
+template <typename... Params, typename... Args>
+cudaError_t launch_kernel(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                          Args &&...args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
 
 // Input head h / r of state head h, with m = ceil(2^32 / r): (h m) >> 32 equals h / r for
 // every h < 2^16 and r <= 2^16 (the rounding excess of m stays below 2^-16 <= 1 / r), and it

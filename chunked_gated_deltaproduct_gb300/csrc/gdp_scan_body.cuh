@@ -153,19 +153,30 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
       src = static_cast<const float *>(p.init) + ((int64_t)seq * H + h) * (int64_t)V * d;
   }
 
+  // Descriptors, workspace tiles and a carried state come from earlier kernels of the stream:
+  // read only after pdl_wait().  The first segment (the whole sequence when unsegmented) loads
+  // its incoming state, which is the caller's, before waiting.
   const int64_t nchunks = (L * M + kChunk - 1) / kChunk;
-  const int64_t cod_i = p.cod[seq];
-  const int64_t co_i = p.chunk_states ? (int64_t)p.co[seq] : 0;
-  // chunks whose workspace tile exists (a flagged descriptor overflow truncates the sequence)
-  const int64_t nall = (cod_i < 0) ? 0 : max((int64_t)0, min(nchunks, p.ws_rows - cod_i));
-  // this launch's chunks: global chunk e0 + e for local e in [0, nrun)
-  const int64_t e0 = min(p.seg_lo, nall);
-  const int64_t nrun = max((int64_t)0, min(p.seg_hi, nall) - e0);
-  if (p.seg_lo > 0 && nrun == 0) return;  // the sequence has no chunk in this segment
-  const bool last_seg = e0 + nrun == nall;
-  if (e0 > 0) {  // carried from the last segment (fp32)
-    src = p.seg_state + ((int64_t)seq * H + h) * (int64_t)V * d;
-    if constexpr (INIT16) src16 = nullptr;
+  int64_t cod_i = 0, co_i = 0, nall = 0, e0 = 0, nrun = 0;
+  bool last_seg = true;
+  auto resolve = [&]() {
+    cod_i = p.cod[seq];
+    co_i = p.chunk_states ? (int64_t)p.co[seq] : 0;
+    // chunks whose workspace tile exists (a flagged descriptor overflow truncates the sequence)
+    nall = (cod_i < 0) ? 0 : max((int64_t)0, min(nchunks, p.ws_rows - cod_i));
+    // this launch's chunks: global chunk e0 + e for local e in [0, nrun)
+    e0 = min(p.seg_lo, nall);
+    nrun = max((int64_t)0, min(p.seg_hi, nall) - e0);
+    last_seg = e0 + nrun == nall;
+    if (e0 > 0) {  // carried from the last segment (fp32)
+      src = p.seg_state + ((int64_t)seq * H + h) * (int64_t)V * d;
+      if constexpr (INIT16) src16 = nullptr;
+    }
+  };
+  if (p.seg_lo > 0) {
+    pdl_wait();
+    resolve();
+    if (nrun == 0) return;  // the sequence has no chunk in this segment
   }
   // token-chunk starts whose state is requested (a prefix of the chunks e % M == 0)
   auto emits = [&](int64_t e) {
@@ -246,6 +257,10 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
       tmem_st16(tS + lrow + c0, x);
     }
     tmem_st_wait();
+  }
+  if (p.seg_lo == 0) {
+    pdl_wait();
+    resolve();
   }
   if (warp == 9 && lane == 0)
     for (int64_t e = 0; e < nst && e < nrun; ++e) {
@@ -503,7 +518,9 @@ cudaError_t launch_scan_kernel(Kern kern, const Problem &p, cudaStream_t stream)
   if (e != cudaSuccess) return e;
   if ((e = tmap_state(&tm_seg, p.seg_state, p.N * hv, p.K)) != cudaSuccess) return e;
   dim3 grid((unsigned)p.N, (unsigned)p.H);
-  kern<<<grid, kScanThreads, smem, stream>>>(p, tm_cs, tm_fin, tm_seg);
+  if ((e = launch_kernel(kern, grid, dim3(kScanThreads), smem, stream, p.pdl != 0, p, tm_cs, tm_fin, tm_seg)) !=
+      cudaSuccess)
+    return e;
   return cudaGetLastError();
 }
 

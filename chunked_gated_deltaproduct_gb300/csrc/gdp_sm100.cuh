@@ -29,6 +29,12 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr, uint32_t lbo, uint
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// Programmatic dependent launch: wait until the previous kernel in the stream has completed and
+// its memory is visible (returns at once when the kernel was launched without the attribute), and
+// allow the next kernel of the stream to start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Instruction descriptor for kind::f16 / kind::tf32: D fp32; a/b format 0 = f16, 1 = bf16, 2 = tf32
 // (A and B always of one type);
 // major 0 = K-major, 1 = MN-major; N >> 3 at bit 17; M >> 4 at bit 24.

@@ -225,6 +225,8 @@ template <bool F16, bool TYPED>
 __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_k, const CUtensorMap &tm_q,
                                         const CUtensorMap &tm_v) {
   using In = In16<F16>;
+  pdl_wait();     // the descriptors (and, in a segmented call, nothing else) come from the kernel before
+  pdl_trigger();  // the scan may start launching: it waits for this grid before reading its tiles
   const int h = blockIdx.y;
   const int hq = input_head(h, p.hmul_q), hk = input_head(h, p.hmul_k), hv = input_head(h, p.hmul_v);
   int row, seq, c;
@@ -625,7 +627,8 @@ cudaError_t launch_wy_kernel(Kern kern, const Problem &p, cudaStream_t stream) {
   if ((e = tmap_rows_16(&tm_q, p.q, p.T, p.Hq, p.K, p.q_st, p.q_sh, p.qpad, p.f16)) != cudaSuccess) return e;
   if ((e = tmap_rows_16(&tm_v, p.v, rows, p.Hv, p.V, p.v_st, p.v_sh, kChunk, p.f16)) != cudaSuccess) return e;
   dim3 grid(p.seg_rows > 0 ? (unsigned)(p.N * p.seg_rows) : (unsigned)p.ntdp_pad, (unsigned)p.H);
-  kern<<<grid, kWyThreads, smem, stream>>>(p, tm_k, tm_q, tm_v);
+  if ((e = launch_kernel(kern, grid, dim3(kWyThreads), smem, stream, p.pdl != 0, p, tm_k, tm_q, tm_v)) != cudaSuccess)
+    return e;
   return cudaGetLastError();
 }
 
