@@ -40,7 +40,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM traffic of the dominant kernel per launch, from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the sha256 of the
 # kernel's sources (KERNEL_SOURCES) it was taken on; reported as null once they change.
-NCU_TRAFFIC = {"gdp_scan_kernel": {"sha": "830b7420307e60d2", "bytes_per_launch": 49147136, "workload": 2}}
+NCU_TRAFFIC = {"gdp_scan_kernel": {"sha": "1e3f3a2aa11249c9", "bytes_per_launch": 49039616, "workload": 2}}
 
 
 def alg_bytes(w) -> int:
