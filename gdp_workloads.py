@@ -174,3 +174,19 @@ def make_workload(wid: int, seed: int | None = None) -> Workload:
                         graph=True)
         return w
     raise KeyError(wid)
+
+
+def make_cotangents(w: Workload, *, seed=0, dfin_sigma=1.0, d_final_state=True, quantum=None):
+    """Seeded upstream gradients for the backward pass of workload ``w``: d_output [T, H, V]
+    bf16 ~ N(0, 1) (the type of the output) and d_final_state [N, H, V, K] fp32 ~ dfin_sigma N(0, 1)
+    (None when ``d_final_state`` is False).  ``quantum``: when given, g, beta and the initial
+    state of ``w`` are replaced by their values rounded to multiples of it (a grid on which
+    finite-difference steps that are multiples of ``quantum`` stay exact in fp32)."""
+    gen = torch.Generator().manual_seed(int(seed) + 77)
+    d_out = _normal(gen, (w.T, w.H, w.d)).to(torch.bfloat16)
+    d_fin = _normal(gen, (w.N, w.H, w.d, w.d)) * dfin_sigma if d_final_state else None
+    if quantum is not None:
+        def snap(x):
+            return None if x is None else (torch.round(x.double() / quantum) * quantum).to(x.dtype)
+        w.g, w.beta, w.initial_state = snap(w.g), snap(w.beta), snap(w.initial_state)
+    return d_out, d_fin

@@ -316,3 +316,226 @@ int gdp_oracle_decay_cumsum(int64_t T, int64_t N, int H, int M,
   }
   return 0;
 }
+
+/*
+ * The backward pass (reverse mode of the recurrence above), for training.
+ *
+ * The blog post "Attention Cache and Sequence Parallelism" (GDN section and the
+ * section on passing state instead of KV) notes that training runs the same
+ * recurrence in chunks and that its backward dependence runs the other way
+ * round; the pages print no backward formula, so this function is the
+ * derivative of the forward definition taken step by step, nothing else.
+ * For a loss L with dL/do = d_output and dL/dS_final = d_final_state, walking
+ * the expanded rows of each sequence backwards with D = dL/dS:
+ *
+ *   readout row r = t*M + M-1:  D += scale do_t qhat_t^T;  dqhat_t = scale S_r^T do_t
+ *   update row r (P_r = the state before the update, e_r = v_r - P_r khat_r):
+ *       delta = D khat_r;  dv_r = beta_r delta;  dbeta_r = e_r . delta
+ *       dkhat_r = beta_r D^T e_r - P_r^T dv_r;   D <- D - dv_r khat_r^T
+ *   first row of token t (the decay S <- alpha_t S, alpha_t = exp(g_t)):
+ *       dg_t = <D, P_r> (Frobenius);  D <- alpha_t D
+ *   start of the sequence: d_initial_state = D.
+ * With use_qk_l2norm, xhat = x / n, n = sqrt(|x|^2 + eps), and
+ *   dx = dxhat / n - x (x . dxhat) / n^3.
+ *
+ * Inputs are float64 (the caller widens bf16 / fp32 values exactly); heads are
+ * one-to-one (Hq = Hk = Hv = H) and g is a natural-log decay.  The states P_r
+ * of one 64-token block are recomputed from a checkpoint taken in a forward
+ * sweep (the same arithmetic, in the same order, as that sweep).  One task per
+ * (sequence, head).  Optional o and final_state receive the forward values.
+ * Returns 0, or a negative code for an argument it cannot serve.
+ */
+int gdp_oracle_backward(int64_t T, int64_t N, int H, int K, int V, int M,
+                        const int64_t *cu_seqlens,
+                        const double *q, const double *k, const double *v,
+                        const double *g, const double *beta, double scale,
+                        int use_qk_l2norm, const double *initial_state,
+                        const double *d_output, const double *d_final_state,
+                        double *dq, double *dk, double *dv, double *dg,
+                        double *dbeta, double *d_initial_state,
+                        double *o, double *final_state, int num_threads) {
+  if (T < 0 || N < 0 || H <= 0 || K <= 0 || V <= 0 || M <= 0) return -1;
+  if (N > 0 && (cu_seqlens[0] != 0 || cu_seqlens[N] != T)) return -4;
+  for (int64_t i = 0; i < N; ++i)
+    if (cu_seqlens[i + 1] < cu_seqlens[i]) return -4;
+  if (!d_output) return -2;
+  const int64_t KV = (int64_t)K * V;
+  const int B = ORACLE_CHUNK;  /* tokens per checkpoint block */
+  const int64_t ntasks = N * (int64_t)H;
+  int rc = 0;
+
+#ifdef _OPENMP
+  if (num_threads > 0) omp_set_num_threads(num_threads);
+#pragma omp parallel
+#endif
+  {
+    double *S = (double *)malloc(sizeof(double) * KV);
+    double *D = (double *)malloc(sizeof(double) * KV);
+    double *Pst = (double *)malloc(sizeof(double) * KV * (size_t)B * M);  /* P_r of one block */
+    double *kh = (double *)malloc(sizeof(double) * K);
+    double *qh = (double *)malloc(sizeof(double) * K);
+    double *dkh = (double *)malloc(sizeof(double) * K);
+    double *e = (double *)malloc(sizeof(double) * V);
+    double *dl = (double *)malloc(sizeof(double) * V);
+    double *dvv = (double *)malloc(sizeof(double) * V);
+    if (!S || !D || !Pst || !kh || !qh || !dkh || !e || !dl || !dvv) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+      rc = -10;
+    } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+      for (int64_t task = 0; task < ntasks; ++task) {
+        const int64_t i = task / H;
+        const int h = (int)(task % H);
+        const int64_t bos = cu_seqlens[i], eos = cu_seqlens[i + 1], L = eos - bos;
+        const int64_t nblk = (L + B - 1) / B;
+        double *ck = (double *)malloc(sizeof(double) * KV * (size_t)(nblk + 1));
+        if (!ck) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+          rc = -10;
+          continue;
+        }
+        /* row loaders: khat_r and qhat_t of head h (optionally L2-normalised) */
+#define ORACLE_HAT(src, row, out)                                             \
+  do {                                                                        \
+    const double *p_ = (src) + ((int64_t)(row) * H + h) * (int64_t)K;         \
+    double ss_ = 0.0;                                                         \
+    for (int d_ = 0; d_ < K; ++d_) ss_ += p_[d_] * p_[d_];                    \
+    const double inv_ = use_qk_l2norm ? 1.0 / sqrt(ss_ + ORACLE_L2_EPS) : 1.0; \
+    for (int d_ = 0; d_ < K; ++d_) (out)[d_] = p_[d_] * inv_;                 \
+  } while (0)
+
+        /* one token of the forward recurrence on S; with Pout, stores P_r of every row */
+#define ORACLE_TOKEN(t, Pout)                                                                   \
+  do {                                                                                          \
+    const double a_ = g ? exp(g[(t) * H + h]) : 1.0;                                            \
+    for (int64_t x_ = 0; x_ < KV; ++x_) S[x_] *= a_;                                            \
+    for (int j_ = 0; j_ < M; ++j_) {                                                            \
+      const int64_t r_ = (t) * M + j_;                                                          \
+      ORACLE_HAT(k, r_, kh);                                                                    \
+      if (Pout) memcpy((Pout) + (size_t)j_ * KV, S, sizeof(double) * KV);                       \
+      const double b_ = beta ? beta[r_ * H + h] : 1.0;                                          \
+      for (int vv_ = 0; vv_ < V; ++vv_) {                                                       \
+        double *Sr_ = S + (int64_t)vv_ * K, pred_ = 0.0;                                        \
+        for (int d_ = 0; d_ < K; ++d_) pred_ += Sr_[d_] * kh[d_];                               \
+        const double vn_ = b_ * (v[(r_ * H + h) * (int64_t)V + vv_] - pred_);                   \
+        for (int d_ = 0; d_ < K; ++d_) Sr_[d_] += vn_ * kh[d_];                                 \
+      }                                                                                         \
+    }                                                                                           \
+  } while (0)
+
+        /* forward sweep: checkpoints at the start of every block, outputs, final state */
+        for (int64_t x = 0; x < KV; ++x) S[x] = initial_state ? initial_state[(i * H + h) * KV + x] : 0.0;
+        for (int64_t t = bos; t < eos; ++t) {
+          if ((t - bos) % B == 0) memcpy(ck + (size_t)((t - bos) / B) * KV, S, sizeof(double) * KV);
+          ORACLE_TOKEN(t, (double *)NULL);
+          if (o) {
+            ORACLE_HAT(q, t, qh);
+            for (int vv = 0; vv < V; ++vv) {
+              double acc = 0.0;
+              for (int d = 0; d < K; ++d) acc += S[(int64_t)vv * K + d] * qh[d];
+              o[(t * H + h) * (int64_t)V + vv] = scale * acc;
+            }
+          }
+        }
+        if (final_state) memcpy(final_state + (i * H + h) * KV, S, sizeof(double) * KV);
+
+        /* backward sweep */
+        for (int64_t x = 0; x < KV; ++x) D[x] = d_final_state ? d_final_state[(i * H + h) * KV + x] : 0.0;
+        for (int64_t blk = nblk - 1; blk >= 0; --blk) {
+          const int64_t t0 = bos + blk * B, t1 = (t0 + B < eos) ? t0 + B : eos;
+          memcpy(S, ck + (size_t)blk * KV, sizeof(double) * KV);
+          for (int64_t t = t0; t < t1; ++t) ORACLE_TOKEN(t, Pst + (size_t)(t - t0) * M * KV);
+          for (int64_t t = t1 - 1; t >= t0; --t) {
+            for (int j = M - 1; j >= 0; --j) {
+              const int64_t r = t * M + j;
+              const double *P = Pst + ((size_t)(t - t0) * M + j) * KV;
+              const double b = beta ? beta[r * H + h] : 1.0;
+              ORACLE_HAT(k, r, kh);
+              for (int vv = 0; vv < V; ++vv) {  /* e_r = v_r - P_r khat_r */
+                double pred = 0.0;
+                for (int d = 0; d < K; ++d) pred += P[(int64_t)vv * K + d] * kh[d];
+                e[vv] = v[(r * H + h) * (int64_t)V + vv] - pred;
+              }
+              if (j == M - 1) {  /* readout after row r: S_r = P_r + beta e khat^T */
+                ORACLE_HAT(q, t, qh);
+                const double *dOt = d_output + (t * H + h) * (int64_t)V;
+                for (int d = 0; d < K; ++d) {
+                  double acc = 0.0;
+                  for (int vv = 0; vv < V; ++vv) acc += (P[(int64_t)vv * K + d] + b * e[vv] * kh[d]) * dOt[vv];
+                  dkh[d] = scale * acc;  /* dqhat_t, staged in dkh */
+                }
+                if (dq) {
+                  const double *qr = q + (t * H + h) * (int64_t)K;
+                  double ss = 0.0, dot = 0.0;
+                  for (int d = 0; d < K; ++d) ss += qr[d] * qr[d];
+                  const double n = use_qk_l2norm ? sqrt(ss + ORACLE_L2_EPS) : 1.0;
+                  for (int d = 0; d < K; ++d) dot += qr[d] * dkh[d];
+                  for (int d = 0; d < K; ++d)
+                    dq[(t * H + h) * (int64_t)K + d] = use_qk_l2norm ? dkh[d] / n - qr[d] * dot / (n * n * n) : dkh[d];
+                }
+                for (int vv = 0; vv < V; ++vv)
+                  for (int d = 0; d < K; ++d) D[(int64_t)vv * K + d] += scale * dOt[vv] * qh[d];
+              }
+              /* the update S_r = P_r + beta e khat^T, reversed */
+              double db = 0.0;
+              for (int vv = 0; vv < V; ++vv) {
+                double acc = 0.0;
+                for (int d = 0; d < K; ++d) acc += D[(int64_t)vv * K + d] * kh[d];
+                dl[vv] = acc;
+                dvv[vv] = b * acc;
+                db += e[vv] * acc;
+              }
+              for (int d = 0; d < K; ++d) {
+                double acc = 0.0;
+                for (int vv = 0; vv < V; ++vv)
+                  acc += b * D[(int64_t)vv * K + d] * e[vv] - P[(int64_t)vv * K + d] * dvv[vv];
+                dkh[d] = acc;
+              }
+              if (dbeta) dbeta[r * H + h] = db;
+              if (dv)
+                for (int vv = 0; vv < V; ++vv) dv[(r * H + h) * (int64_t)V + vv] = dvv[vv];
+              if (dk) {
+                const double *kr = k + (r * H + h) * (int64_t)K;
+                double ss = 0.0, dot = 0.0;
+                for (int d = 0; d < K; ++d) ss += kr[d] * kr[d];
+                const double n = use_qk_l2norm ? sqrt(ss + ORACLE_L2_EPS) : 1.0;
+                for (int d = 0; d < K; ++d) dot += kr[d] * dkh[d];
+                for (int d = 0; d < K; ++d)
+                  dk[(r * H + h) * (int64_t)K + d] = use_qk_l2norm ? dkh[d] / n - kr[d] * dot / (n * n * n) : dkh[d];
+              }
+              for (int vv = 0; vv < V; ++vv)
+                for (int d = 0; d < K; ++d) D[(int64_t)vv * K + d] -= dvv[vv] * kh[d];
+              if (j == 0) {  /* the decay S <- alpha_t S before row t*M */
+                double acc = 0.0;
+                for (int64_t x = 0; x < KV; ++x) acc += D[x] * P[x];
+                if (dg) dg[t * H + h] = g ? acc : 0.0;
+                const double a = g ? exp(g[t * H + h]) : 1.0;
+                for (int64_t x = 0; x < KV; ++x) D[x] *= a;
+              }
+            }
+          }
+        }
+        if (d_initial_state) memcpy(d_initial_state + (i * H + h) * KV, D, sizeof(double) * KV);
+        free(ck);
+#undef ORACLE_TOKEN
+#undef ORACLE_HAT
+      }
+    }
+    free(S);
+    free(D);
+    free(Pst);
+    free(kh);
+    free(qh);
+    free(dkh);
+    free(e);
+    free(dl);
+    free(dvv);
+  }
+  return rc;
+}

@@ -72,6 +72,16 @@ def _load():
             lib.gdp_oracle_widen_f16.argtypes = [ctypes.c_uint16]
             lib.gdp_oracle_decay_cumsum.restype = ctypes.c_int
             lib.gdp_oracle_decay_cumsum.argtypes = [i64, i64, i32, i32, P, P, P]
+            lib.gdp_oracle_backward.restype = ctypes.c_int
+            lib.gdp_oracle_backward.argtypes = [
+                i64, i64, i32, i32, i32, i32,  # T N H K V M
+                P,  # cu_seqlens
+                P, P, P, P, P, dbl, i32,  # q k v g beta scale l2norm
+                P, P, P,  # initial_state d_output d_final_state
+                P, P, P, P, P, P,  # dq dk dv dg dbeta d_initial_state
+                P, P,  # o final_state
+                i32,
+            ]
             _lib = lib
     return _lib
 
@@ -215,3 +225,51 @@ def forward(q, k, v, g, beta, cu_seqlens, num_householder: int, scale: float,
     if rc != 0:
         raise ValueError(f"gdp_oracle_forward rejected its arguments ({rc})")
     return {"o": o, "final_state": fin, "state_out": st_out, "chunk_states": cs, "chunk_offsets": co}
+
+
+def _f64(x):
+    """float64 copy of a bf16 / float16 / fp32 / float64 tensor or array (exact widening), or None."""
+    if x is None:
+        return None
+    if isinstance(x, np.ndarray):
+        return np.ascontiguousarray(x, dtype=np.float64)
+    return np.ascontiguousarray(x.detach().cpu().double().numpy())
+
+
+def backward(q, k, v, g, beta, cu_seqlens, num_householder: int, scale: float, d_output,
+             use_qk_l2norm: bool = False, initial_state=None, d_final_state=None,
+             threads: int | None = None):
+    """Reverse mode of the recurrence (``gdp_oracle_backward``): the gradients of a loss L
+    with dL/do = d_output [T,H,V] and dL/dS_final = d_final_state [N,H,V,K] (None: 0) with
+    respect to q [T,H,K], k [T*M,H,K], v [T*M,H,V], g [T,H] (natural-log decay), beta
+    [T*M,H] and the initial state [N,H,V,K].  Heads are one-to-one.  Returns a dict of
+    float64 arrays: dq, dk, dv, dg, dbeta, d_initial_state, plus the forward values o and
+    final_state."""
+    lib = _load()
+    M = int(num_householder)
+    qd, kd, vd = _f64(q), _f64(k), _f64(v)
+    T, H, K = qd.shape
+    V = vd.shape[2]
+    assert kd.shape == (T * M, H, K) and vd.shape == (T * M, H, V)
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
+    N = cu.shape[0] - 1
+    gd, bd, init, dout, dfin = _f64(g), _f64(beta), _f64(initial_state), _f64(d_output), _f64(d_final_state)
+    assert dout.shape == (T, H, V)
+    assert gd is None or gd.shape == (T, H)
+    assert bd is None or bd.shape == (T * M, H)
+    assert init is None or init.shape == (N, H, V, K)
+    assert dfin is None or dfin.shape == (N, H, V, K)
+    out = {
+        "dq": np.zeros((T, H, K)), "dk": np.zeros((T * M, H, K)), "dv": np.zeros((T * M, H, V)),
+        "dg": np.zeros((T, H)), "dbeta": np.zeros((T * M, H)), "d_initial_state": np.zeros((N, H, V, K)),
+        "o": np.zeros((T, H, V)), "final_state": np.zeros((N, H, V, K)),
+    }
+    rc = lib.gdp_oracle_backward(
+        T, N, H, K, V, M, _ptr(cu), _ptr(qd), _ptr(kd), _ptr(vd), _ptr(gd), _ptr(bd), float(scale),
+        int(bool(use_qk_l2norm)), _ptr(init), _ptr(dout), _ptr(dfin),
+        _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]), _ptr(out["dbeta"]),
+        _ptr(out["d_initial_state"]), _ptr(out["o"]), _ptr(out["final_state"]),
+        int(threads if threads is not None else oracle_threads()))
+    if rc != 0:
+        raise ValueError(f"gdp_oracle_backward rejected its arguments ({rc})")
+    return out
