@@ -272,6 +272,64 @@ def measure_decode(pkg, dev, flush, stream, steps=50, warmup=5):
             "peak_gbs": peak, "frac": gbs / peak, "peak_source": src, "steps": steps, "l2_flush": True}
 
 
+def backward_alg_bytes(w, with_dfin: bool) -> int:
+    """Algorithmic bytes of one backward call: q, k, v, d_output (bf16), g, beta (fp32) and the
+    initial state / final-state gradient (fp32) read once; dq, dk, dv, dg, dbeta and the
+    initial-state gradient (fp32) written once."""
+    d, M, H, T, N = w.d, w.M, w.H, w.T, w.N
+    rd = T * H * (2 * d * (2 + 2 * M) + 4 + 4 * M)
+    wr = T * H * (4 * d * (1 + 2 * M) + 4 + 4 * M)
+    st = N * H * d * d * 4
+    return int(rd + wr + (st if w.initial_state is not None else 0) * 2 + (st if with_dfin else 0))
+
+
+def backward_launches(w) -> int:
+    """Kernels one backward call launches: the forward recompute, two memsets (the sums and
+    dbeta), the reverse scan, the per-chunk gradients, the row pass and the decay pass."""
+    return launches_per_call(w) + 2 + 4
+
+
+def measure_backward(pkg, dev, flush, stream, w, steps=20, warmup=3):
+    """The backward pass of the same workload: upstream gradients d_output (bf16) and
+    d_final_state (fp32) drawn by gdp_workloads.make_cotangents; device time per call with the
+    L2 flushed between calls."""
+    from gdp_workloads import make_cotangents
+
+    d_out, d_fin = make_cotangents(w, seed=1, dfin_sigma=0.5)
+    dd = lambda x: None if x is None else x.to(dev)
+    q, k, v, g, beta, init = (dd(t) for t in (w.q, w.k, w.v, w.g, w.beta, w.initial_state))
+    cu, dout, dfin = w.cu_seqlens.to(dev), d_out.to(dev), d_fin.to(dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    T, H, d, M, N = w.T, w.H, w.d, w.M, w.N
+    dq, dk, dv = torch.empty((T, H, d), **f32), torch.empty((T * M, H, d), **f32), torch.empty((T * M, H, d), **f32)
+    dg, db = torch.empty((T, H), **f32), torch.empty((T * M, H), **f32)
+    dinit = torch.empty((N, H, d, d), **f32) if init is not None else None
+    ws = torch.empty(pkg.gdp_backward_workspace_bytes(T, N, H, d, d, M), dtype=torch.uint8, device=dev)
+    fa = pkg.make_args(q, k, v, g, beta, cu, M, w.scale, init, None, None, None, None, None, None, None, None, None,
+                       None, w.use_qk_l2norm, None, None)
+    b = pkg.backward_args(fa, dout, dfin, dq, dk, dv, dg, db, dinit, ws)
+    sid = stream.cuda_stream
+    times = []
+    for s in range(warmup + steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            e0.record(stream)
+            pkg.gdp_prefill_varlen_backward(b, sid)
+            e1.record(stream)
+        e1.synchronize()
+        if s >= warmup:
+            times.append(e0.elapsed_time(e1))
+    ms = statistics.fmean(times)
+    ab = backward_alg_bytes(w, True)
+    peak, src = measured_peaks()
+    gbs = ab / (ms / 1e3) / 1e9
+    return {"workload": w.name, "ms_per_call": ms, "tokens_per_s": T / (ms / 1e3), "alg_bytes": ab,
+            "achieved_gbs": gbs, "peak_gbs": peak, "frac": gbs / peak, "peak_source": src, "steps": steps,
+            "l2_flush": True, "launches_per_call": backward_launches(w),
+            "note": "includes the forward recompute (the backward keeps nothing from a forward call)"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -282,6 +340,7 @@ def main():
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-backward", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -428,6 +487,7 @@ def main():
     e2e_value = world * w.T / (statistics.fmean(e2e_ms) / 1e3)
 
     decode = measure_decode(pkg, dev, flush, stream) if rank == 0 else None
+    bwd = measure_backward(pkg, dev, flush, stream, w) if (rank == 0 and not args.no_backward) else None
 
     if rank == 0:
         cpu = None
@@ -451,6 +511,7 @@ def main():
             "gpu_launches": launches_per_call(w) * args.steps,
             "clocks": clk.summary(),
             "decode_step": decode,
+            "backward": bwd,
             "wall_s_timed": wall,
         }
         print(json.dumps(line), flush=True)

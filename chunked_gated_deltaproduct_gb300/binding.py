@@ -2,6 +2,7 @@
 
 The names mirror the C ABI in ``include/gdp_prefill.h``: ``gdp_prefill_varlen``,
 ``gdp_prefill_varlen_profiled``, ``gdp_prefill_workspace_bytes``,
+``gdp_prefill_varlen_backward``, ``gdp_backward_workspace_bytes``,
 ``gdp_build_descriptors``, ``gdp_last_error``, ``gdp_nt_pad``, ``gdp_ntdp_pad``.
 ``chunk_gated_delta_product`` wraps them with the keyword signature of the
 pages (FlashInfer API page "flashinfer.gdp_prefill.chunk_gated_delta_product";
@@ -54,6 +55,15 @@ class GdpPrefillArgs(ctypes.Structure):
     ]
 
 
+class GdpBackwardArgs(ctypes.Structure):
+    """Mirror of ``gdp_backward_args``."""
+    _fields_ = [
+        ("fwd", ctypes.POINTER(GdpPrefillArgs)), ("d_output", _vp), ("d_final_state", _vp),
+        ("dq", _vp), ("dk", _vp), ("dv", _vp), ("dg", _vp), ("dbeta", _vp), ("d_initial_state", _vp),
+        ("workspace", _vp), ("workspace_bytes", _sz), ("device_status", _vp),
+    ]
+
+
 class GdpError(RuntimeError):
     def __init__(self, status: int, msg: str):
         super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
@@ -80,6 +90,10 @@ def load_library(path: str | None = None):
     lib.gdp_decode_step.argtypes = [ctypes.POINTER(GdpPrefillArgs), _vp]
     lib.gdp_prefill_varlen_static_scratch.restype = _int
     lib.gdp_prefill_varlen_static_scratch.argtypes = [ctypes.POINTER(GdpPrefillArgs), _vp]
+    lib.gdp_prefill_varlen_backward.restype = _int
+    lib.gdp_prefill_varlen_backward.argtypes = [ctypes.POINTER(GdpBackwardArgs), _vp]
+    lib.gdp_backward_workspace_bytes.restype = _sz
+    lib.gdp_backward_workspace_bytes.argtypes = [_i64, _i64, _int, _int, _int, _int]
     lib.gdp_prefill_workspace_bytes.restype = _sz
     lib.gdp_prefill_workspace_bytes.argtypes = [_i64, _i64, _int, _int, _int, _int]
     lib.gdp_build_descriptors.restype = _int
@@ -228,15 +242,74 @@ def make_args(q, k, v, g, beta, cu_seqlens, num_householder, scale, initial_stat
     a.use_qk_l2norm = int(bool(use_qk_l2norm))
     a.initial_state, a.state, a.state_indices = _addr(initial_state), _addr(state), _addr(state_indices)
     a.num_slots = state.shape[0] if state is not None else 0
-    a.output, a.output_state, a.chunk_states = output.data_ptr(), _addr(output_state), _addr(chunk_states)
+    a.output, a.output_state, a.chunk_states = _addr(output), _addr(output_state), _addr(chunk_states)
     a.chunk_indices, a.chunk_indices_dp, a.chunk_offsets = _addr(chunk_indices), _addr(chunk_indices_dp), _addr(
         chunk_offsets)
     a.nt_pad = int(nt_pad or 0)
     a.ntdp_pad = int(ntdp_pad or 0)
-    a.workspace = workspace.data_ptr()
-    a.workspace_bytes = workspace.numel() * workspace.element_size()
+    a.workspace = _addr(workspace)
+    a.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     a.device_status = _addr(device_status)
     return a
+
+
+def gdp_backward_workspace_bytes(T: int, N: int, H: int, K: int, V: int, M: int) -> int:
+    return int(load_library().gdp_backward_workspace_bytes(T, N, H, K, V, M))
+
+
+def gdp_prefill_varlen_backward(args: GdpBackwardArgs, stream: int | None = None) -> None:
+    """Enqueue the backward pass on ``stream`` (default: torch's current stream).  The
+    forward arguments ``args.fwd`` must stay alive during the call."""
+    lib = load_library()
+    st = lib.gdp_prefill_varlen_backward(ctypes.byref(args), ctypes.c_void_p(_stream(stream)))
+    if st != GDP_OK:
+        raise GdpError(st, lib.gdp_last_error().decode())
+
+
+def backward_args(fwd: GdpPrefillArgs, d_output, d_final_state, dq, dk, dv, dg, dbeta, d_initial_state, workspace,
+                  device_status=None) -> GdpBackwardArgs:
+    """Fill a GdpBackwardArgs from tensors (no copies); keep ``fwd`` alive while it is used."""
+    b = GdpBackwardArgs()
+    b.fwd = ctypes.pointer(fwd)
+    b.d_output, b.d_final_state = _addr(d_output), _addr(d_final_state)
+    b.dq, b.dk, b.dv, b.dg, b.dbeta = _addr(dq), _addr(dk), _addr(dv), _addr(dg), _addr(dbeta)
+    b.d_initial_state = _addr(d_initial_state)
+    b.workspace = workspace.data_ptr()
+    b.workspace_bytes = workspace.numel() * workspace.element_size()
+    b.device_status = _addr(device_status)
+    return b
+
+
+def chunk_gated_delta_product_backward(q, k, v, g, beta, cu_seqlens, num_householder, d_output, scale=None,
+                                       initial_state=None, d_final_state=None, use_qk_l2norm_in_kernel=False,
+                                       workspace=None, device_status=None, stream=None):
+    """Gradients of the prefill for a loss with dL/do = ``d_output`` [T,H,V] (bf16) and
+    dL/dS_final = ``d_final_state`` [N,H,V,K] (fp32, or None).  q [T,H,K], k [T*M,H,K],
+    v [T*M,H,V] bf16; g [T,H] natural-log decay fp32 (or None); beta [T*M,H] fp32 (or None);
+    initial_state [N,H,V,K] fp32 (or None).  Returns a dict of fp32 tensors dq, dk, dv, dg
+    (None without g), dbeta and d_initial_state (None without an initial state)."""
+    T, H, K = q.shape
+    V = v.shape[-1]
+    M = int(num_householder)
+    N = cu_seqlens.numel() - 1
+    dev = q.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = {"dq": torch.empty((T, H, K), **f32), "dk": torch.empty((T * M, H, K), **f32),
+           "dv": torch.empty((T * M, H, V), **f32),
+           "dg": torch.empty((T, H), **f32) if g is not None else None,
+           "dbeta": torch.empty((T * M, H), **f32),
+           "d_initial_state": torch.empty((N, H, V, K), **f32) if initial_state is not None else None}
+    if workspace is None:
+        nbytes = gdp_backward_workspace_bytes(T, N, H, K, V, M)
+        if nbytes == 0:
+            raise GdpError(GDP_ERR_INVALID_ARG, "invalid shape for the workspace query")
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    fa = make_args(q, k, v, g, beta, cu_seqlens, M, scale, initial_state, None, None, None, None, None, None, None,
+                   None, None, None, use_qk_l2norm_in_kernel, None, None)
+    b = backward_args(fa, d_output, d_final_state, out["dq"], out["dk"], out["dv"], out["dg"], out["dbeta"],
+                      out["d_initial_state"], workspace, device_status)
+    gdp_prefill_varlen_backward(b, stream)
+    return out
 
 
 def gdp_decode_step(args: GdpPrefillArgs, stream: int | None = None) -> None:

@@ -155,8 +155,17 @@ gdp_status gdp::resolve_variants(const gdp_prefill_args *a, Problem *p) {
 
 namespace {
 
-// Checks + launches shared by gdp_prefill_varlen and its profiled form.
-gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t const *ev) {
+// The forward recompute of the backward pass: the scan writes the state entering EVERY
+// expanded chunk to `states` (row chunk_offsets_dp[i] + e), the final state to `final_state`
+// (or nothing when NULL) and no output; args->output, output_state and chunk_states are ignored.
+struct Recompute {
+  float *states;
+  float *final_state;
+};
+
+// Checks + launches shared by gdp_prefill_varlen, its profiled form and the backward pass.
+gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t const *ev,
+                   const Recompute *rc = nullptr) {
   g_last_error[0] = 0;
   if (!a) return fail(GDP_ERR_INVALID_ARG, "args is NULL");
   const int64_t T = a->T, N = a->N;
@@ -167,7 +176,7 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
   if (K != V || (K != 64 && K != 128))
     return fail(GDP_ERR_UNSUPPORTED, "head sizes K=%d V=%d: this build serves K == V in {64, 128}", K, V);
   if (!a->cu_seqlens && N > 0) return fail(GDP_ERR_INVALID_ARG, "cu_seqlens is NULL");
-  if (T > 0 && (!a->q || !a->k || !a->v || !a->output))
+  if (T > 0 && (!a->q || !a->k || !a->v || (!a->output && !rc)))
     return fail(GDP_ERR_INVALID_ARG, "q, k, v and output are required");
   gdp::Problem p{};
   gdp_status vst = gdp::resolve_variants(a, &p);
@@ -259,6 +268,16 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
   p.U = (float *)(ws + lay.U);
   p.status = a->device_status;
   p.qpad = gdp::qpad_for(M);
+  p.cs_div = M;
+  int32_t *const co_desc = (int32_t *)p.co;  // where the descriptor kernel writes chunk_offsets
+  if (rc) {  // backward recompute: a state row per expanded chunk, no outputs
+    p.out = nullptr;
+    p.out_state = rc->final_state;
+    p.chunk_states = rc->states;
+    p.co = p.cod;
+    p.nt_pad = ntdp_pad;
+    p.cs_div = 1;
+  }
   p.seg_lo = 0;
   p.seg_hi = INT64_MAX;
   p.seg_rows = 0;
@@ -277,7 +296,7 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
                                 stream);
   else
     e = gdp::launch_descriptors(p.cu, p.cu64, T, N, M, (int32_t *)p.ci, nt_pad, (int32_t *)p.cid, ntdp_pad,
-                                (int32_t *)p.co, (int32_t *)p.cod, p.status, stream);
+                                co_desc, (int32_t *)p.cod, p.status, stream);
   if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "descriptor kernel: %s", cudaGetErrorString(e));
   if (ev && (st = record(ev[1], stream)) != GDP_OK) return st;
   if (nseg == 1) {
@@ -373,6 +392,152 @@ GDP_EXPORT gdp_status gdp_build_descriptors(const void *cu_seqlens, int cu_seqle
 
 GDP_EXPORT gdp_status gdp_prefill_varlen(const gdp_prefill_args *a, void *stream) {
   return prefill(a, (cudaStream_t)stream, nullptr);
+}
+
+namespace {
+
+// Backward workspace: the forward's layout (recompute) followed by the backward's buffers;
+// [acc, acc_end) is zeroed at the start of every call.
+struct BwdLayout {
+  size_t Sx, Dx, fin, tot, dkh, dqh, sig, rho, acc, acc_end, total;
+};
+
+BwdLayout bwd_layout_for(int64_t T, int64_t N, int H, int K, int V, int M) {
+  BwdLayout l{};
+  size_t off = layout_for(T, N, H, K, V, M).total;
+  auto take = [&](size_t bytes) {
+    size_t at = off;
+    off = align_up(off + bytes);
+    return at;
+  };
+  const size_t kv = (size_t)K * V * sizeof(float);
+  const int64_t ntdp = ntdp_bound(T, N, M);
+  l.Sx = take((size_t)ntdp * H * kv);
+  l.Dx = take((size_t)ntdp * H * kv);
+  l.fin = take((size_t)N * H * kv);
+  l.tot = take((size_t)N * H * sizeof(float));
+  l.acc = off;
+  l.dkh = take((size_t)T * M * H * K * sizeof(float));
+  l.dqh = take((size_t)T * H * K * sizeof(float));
+  l.sig = take((size_t)T * M * H * sizeof(float));
+  l.rho = take((size_t)T * H * sizeof(float));
+  l.acc_end = off;
+  l.total = off;
+  return l;
+}
+
+gdp_status backward(const gdp_backward_args *b, cudaStream_t stream) {
+  g_last_error[0] = 0;
+  if (!b || !b->fwd) return fail(GDP_ERR_INVALID_ARG, "args and args->fwd are required");
+  const gdp_prefill_args *a = b->fwd;
+  const int64_t T = a->T, N = a->N;
+  const int H = a->H, K = a->K, V = a->V, M = a->num_householder;
+  if (!shape_ok(T, N, H, K, V, M))
+    return fail(GDP_ERR_INVALID_ARG, "bad shape T=%lld N=%lld H=%d K=%d V=%d M=%d", (long long)T, (long long)N, H, K,
+                V, M);
+  if (K != V || (K != 64 && K != 128))
+    return fail(GDP_ERR_UNSUPPORTED, "head sizes K=%d V=%d: the backward serves K == V in {64, 128}", K, V);
+  if ((a->qkv_dtype && a->qkv_dtype != GDP_DTYPE_BF16) || (a->g_dtype && a->g_dtype != GDP_DTYPE_F32) ||
+      a->g_is_alpha || (a->beta_dtype && a->beta_dtype != GDP_DTYPE_F32) ||
+      (a->initial_state_dtype && a->initial_state_dtype != GDP_DTYPE_F32))
+    return fail(GDP_ERR_UNSUPPORTED,
+                "the backward serves bf16 q/k/v, fp32 natural-log g, fp32 beta and an fp32 initial state");
+  if ((a->num_q_heads && a->num_q_heads != H) || (a->num_k_heads && a->num_k_heads != H) ||
+      (a->num_v_heads && a->num_v_heads != H))
+    return fail(GDP_ERR_UNSUPPORTED, "the backward serves one-to-one heads (num_q/k/v_heads 0 or H)");
+  if (a->state || a->state_indices)
+    return fail(GDP_ERR_UNSUPPORTED, "the backward serves the dense state mode (initial_state), not the cache");
+  if (T > 0 && (!b->d_output || !b->dq || !b->dk || !b->dv))
+    return fail(GDP_ERR_INVALID_ARG, "d_output, dq, dk and dv are required");
+  const uintptr_t al = ((uintptr_t)b->d_output | (uintptr_t)b->dq | (uintptr_t)b->dk | (uintptr_t)b->dv |
+                        (uintptr_t)b->d_final_state | (uintptr_t)b->d_initial_state | (uintptr_t)b->dg |
+                        (uintptr_t)b->dbeta) & 15u;
+  if (al) return fail(GDP_ERR_INVALID_ARG, "d_output and every gradient buffer must be 16-byte aligned");
+  const int64_t ntdpb = ntdp_bound(T, N, M);
+  if (ntdpb * (int64_t)H * V > INT32_MAX)
+    return fail(GDP_ERR_UNSUPPORTED, "per-chunk state arrays above 2^31 rows of K floats");
+  const BwdLayout bl = bwd_layout_for(T, N, H, K, V, M);
+  if (!b->workspace || ((uintptr_t)b->workspace % kAlign) != 0)
+    return fail(GDP_ERR_WORKSPACE, "workspace must be non-NULL and %zu-byte aligned", kAlign);
+  if (b->workspace_bytes < bl.total)
+    return fail(GDP_ERR_WORKSPACE, "workspace of %zu bytes < required %zu", b->workspace_bytes, bl.total);
+  char *ws = (char *)b->workspace;
+
+  // 1. forward recompute: descriptors, WY images, and the state entering every expanded chunk
+  gdp_prefill_args f = *a;
+  f.output = nullptr;
+  f.output_state = nullptr;
+  f.chunk_states = nullptr;
+  f.chunk_indices = f.chunk_indices_dp = f.chunk_offsets = nullptr;
+  f.nt_pad = f.ntdp_pad = 0;
+  f.workspace = ws;
+  f.workspace_bytes = layout_for(T, N, H, K, V, M).total;
+  f.device_status = b->device_status;
+  Recompute rc{(float *)(ws + bl.Sx), b->d_final_state ? (float *)(ws + bl.fin) : nullptr};
+  gdp_status st = prefill(&f, stream, nullptr, &rc);
+  if (st != GDP_OK) return st;
+  if (N == 0) return GDP_OK;
+
+  // 2. zero the sums
+  cudaError_t e = cudaMemsetAsync(ws + bl.acc, 0, bl.acc_end - bl.acc, stream);
+  if (e == cudaSuccess && b->dbeta && T > 0)
+    e = cudaMemsetAsync(b->dbeta, 0, sizeof(float) * (size_t)T * M * H, stream);
+  if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
+
+  // 3. reverse state scan, per-chunk gradients, finishing passes
+  const Layout fl = layout_for(T, N, H, K, V, M);
+  gdp::BwdProblem p{};
+  p.q = (const __nv_bfloat16 *)a->q;
+  p.k = (const __nv_bfloat16 *)a->k;
+  p.v = (const __nv_bfloat16 *)a->v;
+  p.q_st = a->q_stride_t; p.q_sh = a->q_stride_h;
+  p.k_st = a->k_stride_t; p.k_sh = a->k_stride_h;
+  p.v_st = a->v_stride_t; p.v_sh = a->v_stride_h;
+  p.g = a->g;
+  p.beta = a->beta;
+  p.cu = a->cu_seqlens;
+  p.cu64 = a->cu_seqlens_int64 ? 1 : 0;
+  p.T = T; p.N = N; p.H = H; p.D = K; p.M = M;
+  p.qpad = gdp::qpad_for(M);
+  p.scale = (a->scale > 0.f && !isnan(a->scale)) ? a->scale : 1.0f / sqrtf((float)K);
+  p.l2norm = a->use_qk_l2norm ? 1 : 0;
+  p.cid = (const int32_t *)(ws + fl.cid);
+  p.cod = (const int32_t *)(ws + fl.cod);
+  p.ntdp_pad = ntdpb;
+  p.ws_rows = ntdpb;
+  p.img = (const unsigned char *)(ws + fl.img);
+  p.img_stride = fl.img_stride;
+  p.Sx = (const float *)(ws + bl.Sx);
+  p.Dx = (float *)(ws + bl.Dx);
+  p.dout = (const __nv_bfloat16 *)b->d_output;
+  p.dfin = b->d_final_state;
+  p.fin = b->d_final_state ? (const float *)(ws + bl.fin) : nullptr;
+  p.dinit = b->d_initial_state;
+  p.tot = (float *)(ws + bl.tot);
+  p.dkh = (float *)(ws + bl.dkh);
+  p.dqh = (float *)(ws + bl.dqh);
+  p.sig = (float *)(ws + bl.sig);
+  p.rho = (float *)(ws + bl.rho);
+  p.dq = b->dq;
+  p.dk = b->dk;
+  p.dv = b->dv;
+  p.dg = b->dg;
+  p.dbeta = b->dbeta;
+  p.status = b->device_status;
+  if ((e = gdp::launch_backward(p, stream)) != cudaSuccess)
+    return fail(GDP_ERR_CUDA, "backward kernels: %s", cudaGetErrorString(e));
+  return GDP_OK;
+}
+
+}  // namespace
+
+GDP_EXPORT size_t gdp_backward_workspace_bytes(int64_t T, int64_t N, int H, int K, int V, int M) {
+  if (!shape_ok(T, N, H, K, V, M)) return 0;
+  return bwd_layout_for(T, N, H, K, V, M).total;
+}
+
+GDP_EXPORT gdp_status gdp_prefill_varlen_backward(const gdp_backward_args *args, void *stream) {
+  return backward(args, (cudaStream_t)stream);
 }
 
 GDP_EXPORT gdp_status gdp_prefill_varlen_profiled(const gdp_prefill_args *a, void *stream, void *const *events,

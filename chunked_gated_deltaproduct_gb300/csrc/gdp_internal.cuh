@@ -128,7 +128,43 @@ struct Problem {
   // launch the WY and scan kernels with programmatic stream serialization: each may start while
   // its predecessor finishes and waits (griddepcontrol.wait) before reading that one's outputs
   int pdl;
+  // chunk_states row spacing: the scan emits the state entering expanded chunk e when
+  // e % cs_div == 0, at row co[seq] + e / cs_div (M: token-chunk starts; 1: every expanded
+  // chunk, with co = the expanded-chunk offsets, for the backward pass).  A NULL `out` skips
+  // the output stores.
+  int cs_div;
 };
+
+// Everything the backward kernels need about one call (gdp_backward.cu).  Heads are
+// one-to-one, q / k / v / d_output bf16, g natural-log fp32, beta fp32, K = V = D.
+struct BwdProblem {
+  const __nv_bfloat16 *q, *k, *v;
+  int64_t q_st, q_sh, k_st, k_sh, v_st, v_sh;
+  const float *g, *beta;  // NULL: no decay / all ones
+  const void *cu;
+  int cu64;
+  int64_t T, N;
+  int H, D, M, qpad;
+  float scale;
+  int l2norm;
+  const int32_t *cid, *cod;  // expanded-chunk descriptors and offsets (forward recompute)
+  int64_t ntdp_pad, ws_rows;
+  const unsigned char *img;  // the forward's operand images (ImageLayout), img_stride apart
+  size_t img_stride;
+  const float *Sx;           // [ntdp][H][V][K] state entering each expanded chunk
+  float *Dx;                 // [ntdp][H][V][K] dL/dS at each expanded chunk's exit
+  const __nv_bfloat16 *dout; // [T][H][V] dL/do
+  const float *dfin;         // [N][H][V][K] dL/dS_final or NULL
+  const float *fin;          // [N][H][V][K] recomputed final state (when dfin)
+  float *dinit;              // [N][H][V][K] dL/dS_initial or NULL
+  float *tot;                // [N][H] <dS_final, S_final>
+  float *dkh, *dqh;          // [T*M][H][K], [T][H][K] gradients of the normalised rows (summed)
+  float *sig, *rho;          // [T*M][H] sum_v dv v, [T][H] do . o (summed)
+  float *dq, *dk, *dv, *dg, *dbeta;
+  uint32_t *status;
+};
+cudaError_t launch_backward(const BwdProblem &p, cudaStream_t stream);
+size_t backward_chunk_smem(int d, int qpad);
 
 // Launch `kern` on `stream`, with programmatic stream serialization when `pdl`.
 template <typename... Params, typename... Args>

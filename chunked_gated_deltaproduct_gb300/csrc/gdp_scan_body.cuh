@@ -178,10 +178,12 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
     resolve();
     if (nrun == 0) return;  // the sequence has no chunk in this segment
   }
-  // token-chunk starts whose state is requested (a prefix of the chunks e % M == 0)
+  // token-chunk starts whose state is requested (a prefix of the chunks e % M == 0; every
+  // chunk when cs_div is 1, the backward pass's recompute)
+  const int csd = p.cs_div;
   auto emits = [&](int64_t e) {
     const int64_t eg = e0 + e;
-    return p.chunk_states && (eg % M == 0) && co_i >= 0 && co_i + eg / M < p.nt_pad;
+    return p.chunk_states && (eg % csd == 0) && co_i >= 0 && co_i + eg / csd < p.nt_pad;
   };
 
   if (warp == 8) tmem_alloc(&tmem_slot, 512);
@@ -400,7 +402,7 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
       named_sync(1, 128);
       const int64_t tq0 = (bos * M + (e0 + e) * kChunk + ci.p0) / M;  // readout rows are consecutive tokens
       const int cpr = V / 8;                                     // 16-byte chunks per output row
-      for (int c = tid - 128; c < ci.nq * cpr; c += 128) {
+      for (int c = tid - 128; p.out && c < ci.nq * cpr; c += 128) {
         const int qi = c / cpr, ch = c % cpr;
         *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + ((tq0 + qi) * H + h) * (int64_t)V + ch * 8) =
             *reinterpret_cast<const uint4 *>(obuf + ((uint32_t)qi * V + ch * 8) * 2u);
@@ -408,7 +410,7 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
       if (emits(e)) {  // the prep warps copied S_e before batch 2 of this chunk was issued
         if (has_rows)
           store_state_tma(tBk + lrow, sttiles, lane, d, 1.f, &tm_cs,
-                          (int)(((co_i + (e0 + e) / M) * H + h) * V + q4 * 32), nblk);
+                          (int)(((co_i + (e0 + e) / csd) * H + h) * V + q4 * 32), nblk);
         tc_fence_before();
         mbar_arrive(&bk_free);  // the snapshot columns have been read
       }

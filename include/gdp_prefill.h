@@ -273,6 +273,57 @@ gdp_status gdp_build_descriptors(const void *cu_seqlens, int cu_seqlens_int64, i
  */
 gdp_status gdp_decode_step(const gdp_prefill_args *args, void *stream);
 
+/*
+ * gdp_prefill_varlen_backward: the backward pass of the prefill, for training.
+ *
+ * The pages print the forward recurrence only (FlashInfer page, display equation);
+ * the blog post "Attention Cache and Sequence Parallelism" (section on passing state
+ * instead of KV) notes that training runs it in chunks and that the backward
+ * dependence runs the other way round.  This entry point returns the exact derivative
+ * of that recurrence: for a loss L with dL/do = d_output and dL/dS_final =
+ * d_final_state, the gradients of L with respect to q, k, v, g, beta and the initial
+ * state.  It recomputes the forward pass from the inputs (nothing from a forward call
+ * is kept), then runs the state scan backwards over 64-row chunks.
+ *
+ *   fwd            the forward call's arguments: q, k, v, g, beta, cu_seqlens, the
+ *                  shapes, scale, use_qk_l2norm, initial_state (as for
+ *                  gdp_prefill_varlen).  Its output, output_state, chunk_states,
+ *                  descriptor, workspace and device_status fields are ignored.
+ *                  Served: bf16 q/k/v with one-to-one heads, fp32 natural-log g (or
+ *                  NULL), fp32 beta (or NULL), dense state mode (initial_state or
+ *                  NULL; no state cache), K = V in {64, 128}; anything else is
+ *                  GDP_ERR_UNSUPPORTED.
+ *   d_output       [T, H, V] bf16, contiguous: dL/do.
+ *   d_final_state  [N, H, V, K] fp32 or NULL (= 0): dL/dS_final.
+ *   dq             [T, H, K] fp32, contiguous, written (with use_qk_l2norm: the
+ *                  gradient with respect to the unnormalised rows).
+ *   dk             [T*M, H, K] fp32, likewise.
+ *   dv             [T*M, H, V] fp32, written.
+ *   dg             [T, H] fp32 or NULL; all zeros when fwd->g is NULL.
+ *   dbeta          [T*M, H] fp32 or NULL (the gradient at beta = 1 when fwd->beta is NULL).
+ *   d_initial_state [N, H, V, K] fp32 or NULL: dL/dS_initial.
+ *   workspace      at least gdp_backward_workspace_bytes(...) bytes, 256-byte aligned,
+ *                  contents undefined on entry and exit.
+ *   device_status  optional, as for the prefill.
+ * Every buffer is a device pointer, 16-byte aligned.  Nothing is allocated and
+ * nothing synchronises.  dq, dk and dbeta are sums of per-slice shares added with
+ * atomics, so their last bits may differ from call to call.
+ */
+typedef struct gdp_backward_args {
+  const gdp_prefill_args *fwd; /* host pointer, read during the call only */
+  const void *d_output;
+  const float *d_final_state;
+  float *dq, *dk, *dv, *dg, *dbeta, *d_initial_state;
+  void *workspace;
+  size_t workspace_bytes;
+  uint32_t *device_status;
+} gdp_backward_args;
+
+/* Workspace bytes of gdp_prefill_varlen_backward for this shape (0 for an invalid shape). */
+size_t gdp_backward_workspace_bytes(int64_t T, int64_t N, int H, int K, int V, int num_householder);
+
+gdp_status gdp_prefill_varlen_backward(const gdp_backward_args *args, void *stream);
+
 /* One-line reason for the last non-OK status returned on this thread ("" if none). */
 const char *gdp_last_error(void);
 

@@ -146,3 +146,47 @@ def test_decode_host_validation(lib, over, status):
     st = lib.gdp_decode_step(ctypes.byref(a), None)
     assert st == status, (st, pkg.gdp_last_error())
     assert pkg.gdp_last_error() != ""
+
+
+def _bwd(lib, fwd_over=None, **over):
+    a = _args(**(fwd_over or {}))
+    fake = 1 << 20
+    b = pkg.GdpBackwardArgs()
+    b.fwd = ctypes.pointer(a)
+    b.d_output = b.dq = b.dk = b.dv = fake
+    b.workspace = fake
+    b.workspace_bytes = pkg.gdp_backward_workspace_bytes(a.T, a.N, a.H, a.K, a.V, a.num_householder)
+    for k, v in over.items():
+        setattr(b, k, v)
+    return lib.gdp_prefill_varlen_backward(ctypes.byref(b), None), a
+
+
+@pytest.mark.parametrize("fwd_over,over,status", [
+    (dict(qkv_dtype=pkg.GDP_DTYPE_F16), {}, pkg.GDP_ERR_UNSUPPORTED),
+    (dict(g_is_alpha=1), {}, pkg.GDP_ERR_UNSUPPORTED),
+    (dict(g_dtype=pkg.GDP_DTYPE_BF16), {}, pkg.GDP_ERR_UNSUPPORTED),
+    (dict(initial_state_dtype=pkg.GDP_DTYPE_BF16), {}, pkg.GDP_ERR_UNSUPPORTED),
+    (dict(H=4, num_q_heads=2, num_k_heads=2, num_v_heads=4), {}, pkg.GDP_ERR_UNSUPPORTED),
+    (dict(state=1 << 22, state_indices=1 << 23, num_slots=4), {}, pkg.GDP_ERR_UNSUPPORTED),
+    (dict(K=96, V=96), {}, pkg.GDP_ERR_UNSUPPORTED),
+    ({}, dict(d_output=None), pkg.GDP_ERR_INVALID_ARG),
+    ({}, dict(dk=None), pkg.GDP_ERR_INVALID_ARG),
+    ({}, dict(dq=(1 << 20) + 4), pkg.GDP_ERR_INVALID_ARG),
+    ({}, dict(workspace_bytes=64), pkg.GDP_ERR_WORKSPACE),
+    ({}, dict(workspace=None), pkg.GDP_ERR_WORKSPACE),
+])
+def test_backward_host_validation(lib, fwd_over, over, status):
+    st, _ = _bwd(lib, fwd_over, **over)
+    assert st == status, (st, pkg.gdp_last_error())
+    assert pkg.gdp_last_error() != ""
+
+
+def test_backward_null_forward_args(lib):
+    b = pkg.GdpBackwardArgs()
+    assert lib.gdp_prefill_varlen_backward(ctypes.byref(b), None) == pkg.GDP_ERR_INVALID_ARG
+
+
+def test_backward_workspace_covers_forward():
+    for shape in [(1421, 4, 8, 128, 128, 2), (65536, 1, 32, 128, 128, 2), (256, 1, 2, 64, 64, 1)]:
+        assert pkg.gdp_backward_workspace_bytes(*shape) > pkg.gdp_prefill_workspace_bytes(*shape) > 0
+    assert pkg.gdp_backward_workspace_bytes(10, 1, 1, 64, 64, 0) == 0
