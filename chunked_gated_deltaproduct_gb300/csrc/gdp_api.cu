@@ -396,10 +396,9 @@ GDP_EXPORT gdp_status gdp_prefill_varlen(const gdp_prefill_args *a, void *stream
 
 namespace {
 
-// Backward workspace: the forward's layout (recompute) followed by the backward's buffers;
-// [acc, acc_end) is zeroed at the start of every call.
+// Backward workspace: the forward's layout (recompute) followed by the backward's buffers.
 struct BwdLayout {
-  size_t Sx, Dx, fin, tot, dkh, dqh, sig, rho, acc, acc_end, total;
+  size_t Sx, Dx, fin, tot, sig, rho, total;
 };
 
 BwdLayout bwd_layout_for(int64_t T, int64_t N, int H, int K, int V, int M) {
@@ -416,12 +415,8 @@ BwdLayout bwd_layout_for(int64_t T, int64_t N, int H, int K, int V, int M) {
   l.Dx = take((size_t)ntdp * H * kv);
   l.fin = take((size_t)N * H * kv);
   l.tot = take((size_t)N * H * sizeof(float));
-  l.acc = off;
-  l.dkh = take((size_t)T * M * H * K * sizeof(float));
-  l.dqh = take((size_t)T * H * K * sizeof(float));
   l.sig = take((size_t)T * M * H * sizeof(float));
   l.rho = take((size_t)T * H * sizeof(float));
-  l.acc_end = off;
   l.total = off;
   return l;
 }
@@ -478,13 +473,8 @@ gdp_status backward(const gdp_backward_args *b, cudaStream_t stream) {
   if (st != GDP_OK) return st;
   if (N == 0) return GDP_OK;
 
-  // 2. zero the sums
-  cudaError_t e = cudaMemsetAsync(ws + bl.acc, 0, bl.acc_end - bl.acc, stream);
-  if (e == cudaSuccess && b->dbeta && T > 0)
-    e = cudaMemsetAsync(b->dbeta, 0, sizeof(float) * (size_t)T * M * H, stream);
-  if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
-
-  // 3. reverse state scan, per-chunk gradients, finishing passes
+  // 2. reverse state scan, per-chunk gradients, decay gradient
+  cudaError_t e;
   const Layout fl = layout_for(T, N, H, K, V, M);
   gdp::BwdProblem p{};
   p.q = (const __nv_bfloat16 *)a->q;
@@ -514,8 +504,6 @@ gdp_status backward(const gdp_backward_args *b, cudaStream_t stream) {
   p.fin = b->d_final_state ? (const float *)(ws + bl.fin) : nullptr;
   p.dinit = b->d_initial_state;
   p.tot = (float *)(ws + bl.tot);
-  p.dkh = (float *)(ws + bl.dkh);
-  p.dqh = (float *)(ws + bl.dqh);
   p.sig = (float *)(ws + bl.sig);
   p.rho = (float *)(ws + bl.rho);
   p.dq = b->dq;

@@ -26,15 +26,15 @@
 // Everything above follows from the row recurrence by algebra alone; the float64 oracle
 // takes the derivative step by step instead and the parity tests compare the two.
 //
-// Kernels (warp-level tf32 MMAs, fp32 accumulation; the dense chunk products are small
-// and varied, the serial part is the state scan):
-//   gdp_bwd_scan_kernel   one CTA per (sequence, head): D = dL/dS in registers, chunks in
-//                         reverse, operands from the forward's per-chunk images (TMA bulk
-//                         copies, double-buffered), writes D_C of every chunk
-//   gdp_bwd_chunk_kernel  one CTA per (expanded chunk, head, 32-column slice of V): the
-//                         per-row gradients above; the slice's shares of dkhat, dqhat,
-//                         dbeta and the dg terms are summed with atomics
-//   gdp_bwd_rows_kernel   L2-norm chain rule: dx = dxhat / n - x (x . dxhat) / n^3
+// Kernels (warp-level tf32 MMAs, fp32 accumulation -- the triangular solves in the 3xTF32
+// split; the dense chunk products are small and varied, the serial part is the state scan):
+//   gdp_bwd_scan_kernel   one CTA per (sequence, head): D = dL/dS in registers (two warps
+//                         per 16 state rows, one per column half), chunks in reverse,
+//                         operands from the forward's per-chunk images (TMA bulk copies,
+//                         double-buffered), writes D_C of every chunk
+//   gdp_bwd_chunk_kernel  one CTA per (expanded chunk, head), V in 16- (or 8-) column
+//                         slices: the per-row gradients above, the L2-norm chain rule
+//                         dx = dxhat / n - x (x . dxhat) / n^3, dq / dk / dv / dbeta stores
 //   gdp_bwd_dg_kernel     reverse cumulative sum of the decay gradient per (sequence, head)
 #include "gdp_internal.cuh"
 #include "gdp_sm100.cuh"
@@ -70,63 +70,74 @@ __device__ __forceinline__ void mma_tile(float *c, int ks, int g, int t, FA a, F
   }
 }
 
-__device__ __forceinline__ float bf(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
-
 // ---------------------------------------------------------------------------------------
 // Reverse state scan.
 // ---------------------------------------------------------------------------------------
-constexpr uint32_t kBwdScanBudget = 190u * 1024u;
+constexpr uint32_t kBwdScanLimit = 227u * 1024u;
 
 __host__ __device__ inline uint32_t bwd_stage_bytes(int d, int qpad) {
   return (ImageLayout(d, qpad).bytes + 1023u) & ~1023u;
 }
+// d_output rows of a chunk, bf16 [qpad][d + 8]; the Z exchange buffer, fp32 [d][64]
+__host__ __device__ inline uint32_t bwd_dos_bytes(int d, int qpad) { return (uint32_t)qpad * (d + 8) * 2u; }
+__host__ __device__ inline uint32_t bwd_zbuf_bytes(int d) { return (uint32_t)d * kChunk * 4u; }
 __host__ __device__ inline int bwd_scan_stages(int d, int qpad) {
-  return 2u * bwd_stage_bytes(d, qpad) + (uint32_t)qpad * (d + 8) * 4u <= kBwdScanBudget ? 2 : 1;
+  return 2u * bwd_stage_bytes(d, qpad) + bwd_dos_bytes(d, qpad) + bwd_zbuf_bytes(d) + 1024u <= kBwdScanLimit ? 2 : 1;
 }
 __host__ inline size_t bwd_scan_smem(int d, int qpad) {
-  return (size_t)bwd_scan_stages(d, qpad) * bwd_stage_bytes(d, qpad) + (size_t)qpad * (d + 8) * 4u + 1024u;
+  return (size_t)bwd_scan_stages(d, qpad) * bwd_stage_bytes(d, qpad) + bwd_dos_bytes(d, qpad) + bwd_zbuf_bytes(d) +
+         1024u;
 }
 
-template <int D>
-__global__ void __launch_bounds__(2 * D, 1) gdp_bwd_scan_kernel(BwdProblem p) {
-  constexpr int NW = D / 16;  // warps; warp w holds state rows 16 w .. 16 w + 15
-  constexpr int LDO = D + 8;  // row stride of the staged d_output rows (conflict-free A loads)
+// Warp w holds state rows 16 (w % (D / 16)) .. +15 and the column half w / (D / 16) of D in
+// the m16n8 accumulator layout.  Per chunk, each half forms its share of Z = D Ktil^T
+// (plus dO^T P on half 0), the halves are summed through shared memory, and each half
+// updates its own columns of D.
+template <int D, int QP>
+__global__ void __launch_bounds__(4 * D, 1) gdp_bwd_scan_kernel(BwdProblem p) {
+  constexpr int NR = D / 16;     // row groups
+  constexpr int NW = 2 * NR;     // warps
+  constexpr int HC = D / 2;      // columns per half
+  constexpr int LDO = D + 8;     // row stride (bf16 elements) of the staged d_output rows
   const int seq = blockIdx.x, h = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int rg = warp % NR, ch = warp / NR;
   int64_t bos, L;
   if (!seq_bounds(p.cu, p.cu64, p.T, seq, &bos, &L)) return;
-  const int M = p.M, QP = p.qpad, H = p.H;
+  const int M = p.M, H = p.H;
   const ImageLayout il(D, QP);
   const uint32_t sbytes = bwd_stage_bytes(D, QP);
   const int nst = bwd_scan_stages(D, QP);
   extern __shared__ __align__(1024) unsigned char bwd_scan_raw[];
   unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)bwd_scan_raw + 1023) & ~(uintptr_t)1023);
-  float *dos = reinterpret_cast<float *>(sm + nst * sbytes);
+  __nv_bfloat16 *dos = reinterpret_cast<__nv_bfloat16 *>(sm + nst * sbytes);
+  float *zbuf = reinterpret_cast<float *>(sm + nst * sbytes + bwd_dos_bytes(D, QP));
   __shared__ __align__(8) uint64_t full[2];
   __shared__ float red[NW];
   const int64_t KV = (int64_t)D * D, sh = (int64_t)seq * H + h;
   const int64_t nchunks = (L * M + kChunk - 1) / kChunk;
   const int64_t cod_i = p.cod[seq];
   const int64_t nall = (cod_i < 0) ? 0 : max((int64_t)0, min(nchunks, p.ws_rows - cod_i));
-  const int r0 = 16 * warp + g;  // this thread's rows r0 and r0 + 8
+  const int r0 = 16 * rg + g;  // this thread's rows r0 and r0 + 8
+  const int c0 = HC * ch;      // first column of this warp's half
 
   // D = dL/dS_final; <dS_final, S_final> for the decay gradient
-  float dacc[D / 8][4];
+  float dacc[HC / 8][4];
   {
     const float *src = p.dfin ? p.dfin + sh * KV : nullptr;
     const float *fin = (p.dfin && p.fin) ? p.fin + sh * KV : nullptr;
     float part = 0.f;
 #pragma unroll
-    for (int j = 0; j < D / 8; ++j)
+    for (int j = 0; j < HC / 8; ++j)
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        const int64_t off = (int64_t)(r0 + 8 * hf) * D + 8 * j + 2 * t;
+        const int64_t off = (int64_t)(r0 + 8 * hf) * D + c0 + 8 * j + 2 * t;
         const float2 x = src ? *reinterpret_cast<const float2 *>(src + off) : make_float2(0.f, 0.f);
         dacc[j][2 * hf] = x.x;
         dacc[j][2 * hf + 1] = x.y;
         if (fin) {
-          const float2 s = *reinterpret_cast<const float2 *>(fin + off);
-          part += x.x * s.x + x.y * s.y;
+          const float2 s2 = *reinterpret_cast<const float2 *>(fin + off);
+          part += x.x * s2.x + x.y * s2.y;
         }
       }
 #pragma unroll
@@ -140,9 +151,9 @@ __global__ void __launch_bounds__(2 * D, 1) gdp_bwd_scan_kernel(BwdProblem p) {
   }
   __syncthreads();
   if (tid == 0 && p.tot) {
-    float s = 0.f;
-    for (int w = 0; w < NW; ++w) s += red[w];
-    p.tot[sh] = s;
+    float s2 = 0.f;
+    for (int w = 0; w < NW; ++w) s2 += red[w];
+    p.tot[sh] = s2;
   }
   auto image = [&](int64_t e) { return p.img + (size_t)((cod_i + e) * H + h) * p.img_stride; };
   int issued[2] = {0, 0};
@@ -154,6 +165,7 @@ __global__ void __launch_bounds__(2 * D, 1) gdp_bwd_scan_kernel(BwdProblem p) {
   };
   if (tid == 0)
     for (int64_t i = 0; i < nst && i < nall; ++i) issue(i);
+  auto dO = [&](int qi, int v) { return __bfloat162float(dos[qi * LDO + v]); };
 
   bool aborted = false;
   for (int64_t i = 0; i < nall; ++i) {
@@ -163,89 +175,123 @@ __global__ void __launch_bounds__(2 * D, 1) gdp_bwd_scan_kernel(BwdProblem p) {
     // the gradient at chunk e's exit
     float *dst = p.Dx + ((cod_i + e) * H + h) * KV;
 #pragma unroll
-    for (int j = 0; j < D / 8; ++j)
+    for (int j = 0; j < HC / 8; ++j)
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf)
-        *reinterpret_cast<float2 *>(dst + (int64_t)(r0 + 8 * hf) * D + 8 * j + 2 * t) =
+        *reinterpret_cast<float2 *>(dst + (int64_t)(r0 + 8 * hf) * D + c0 + 8 * j + 2 * t) =
             make_float2(dacc[j][2 * hf], dacc[j][2 * hf + 1]);
-    // d_output rows of the chunk's readouts (fp32, zero past the readout count)
+    // d_output rows of the chunk's readouts (bf16, zero past the readout count)
     const ImageMeta mt = *reinterpret_cast<const ImageMeta *>(image(e) + il.meta);
     const int64_t tq0 = (bos * M + e * kChunk + mt.p0) / M;
-    for (int idx = tid; idx < QP * (D / 4); idx += 32 * NW) {
-      const int qi = idx / (D / 4), c4 = (idx % (D / 4)) * 4;
-      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (qi < mt.nq) {
-        const __nv_bfloat16 *src = p.dout + ((tq0 + qi) * H + h) * (int64_t)D + c4;
-        const uint2 u = *reinterpret_cast<const uint2 *>(src);
-        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
-        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
-        x = make_float4(a.x, a.y, b.x, b.y);
-      }
-      *reinterpret_cast<float4 *>(dos + qi * LDO + c4) = x;
+    for (int idx = tid; idx < QP * (D / 8); idx += 32 * NW) {
+      const int qi = idx / (D / 8), c8 = (idx % (D / 8)) * 8;
+      uint4 x = make_uint4(0u, 0u, 0u, 0u);
+      if (qi < mt.nq) x = *reinterpret_cast<const uint4 *>(p.dout + ((tq0 + qi) * H + h) * (int64_t)D + c8);
+      *reinterpret_cast<uint4 *>(dos + qi * LDO + c8) = x;
     }
     const bool ok = mbar_wait(&full[st], (uint32_t)((i / nst) & 1));
     if (!__syncthreads_and(ok)) {
       aborted = true;
       break;
     }
-    auto ld = [&](uint32_t off) { return *reinterpret_cast<const float *>(im + off); };
-    // Z = D Ktil^T + dO^T P  (rows v of this warp x 64 chunk rows s).  The D fragments serve
-    // as A with the k order permuted within each 8-column step (logical k = t <-> column
-    // 2t, k = t + 4 <-> column 2t + 1); B is read in the same order.
+    const float *imf = reinterpret_cast<const float *>(im);
+    // this half's share of Z = D Ktil^T (+ dO^T P on half 0): rows v x 64 chunk rows s.  The D
+    // fragments serve as A with the k order permuted within each 8-column step (logical
+    // k = t <-> column 2t, k = t + 4 <-> 2t + 1); B is read in the same order.  Operand
+    // addresses in the swizzled image (row r, column k: 1024-byte atoms of 8 rows, 16-byte
+    // chunk (k % 32) / 4 of row r at chunk position ((k % 32) / 4) ^ (r % 8)) are a per-thread
+    // base (ko, po, wo, qo below, in floats) plus compile-time steps.
     float z[8][4];
 #pragma unroll
     for (int n = 0; n < 8; ++n) z[n][0] = z[n][1] = z[n][2] = z[n][3] = 0.f;
 #pragma unroll
-    for (int j = 0; j < D / 8; ++j) {
-      const uint32_t a0 = tf32r(dacc[j][0]), a1 = tf32r(dacc[j][2]), a2 = tf32r(dacc[j][1]), a3 = tf32r(dacc[j][3]);
-      const int f0 = 8 * j + 2 * t;
+    for (int n = 0; n < 8; ++n) {
+      const uint32_t cq = 2u * (n & 3) + (g >> 2);  // chunk of column s = 8 n + g in its row
+      const uint32_t blk = (il.b2 + (uint32_t)(n >> 2) * il.b2_block) / 4u + (uint32_t)(g & 3);
+      // Ktil^T rows f = c0 + 8 j + 2 t (+1): atom (c0 / 8 + j), row-in-atom 2t (+1)
+      const uint32_t ko0 = blk + (uint32_t)(c0 / 8) * 256u + 2u * t * 32u + (((cq ^ (2u * t)) & 7u) << 2);
+      const uint32_t ko1 = blk + (uint32_t)(c0 / 8) * 256u + (2u * t + 1u) * 32u + (((cq ^ (2u * t + 1u)) & 7u) << 2);
 #pragma unroll
-      for (int n = 0; n < 8; ++n) {
-        const int s = 8 * n + g;
-        mma8(z[n], a0, a1, a2, a3, tf32r(ld(il.kt(f0, s))), tf32r(ld(il.kt(f0 + 1, s))));
+      for (int j = 0; j < HC / 8; ++j) {
+        const uint32_t a0 = tf32r(dacc[j][0]), a1 = tf32r(dacc[j][2]), a2 = tf32r(dacc[j][1]),
+                       a3 = tf32r(dacc[j][3]);
+        mma8(z[n], a0, a1, a2, a3, tf32r(imf[ko0 + 256u * j]), tf32r(imf[ko1 + 256u * j]));
+      }
+      if (ch == 0) {
+        // P rows d + k0 + t (+4): atom (d + k0) / 8, row-in-atom t (+4)
+        const uint32_t po0 = blk + (uint32_t)(D / 8) * 256u + t * 32u + (((cq ^ t) & 7u) << 2);
+        const uint32_t po1 = blk + (uint32_t)(D / 8) * 256u + (t + 4u) * 32u + (((cq ^ (t + 4u)) & 7u) << 2);
+#pragma unroll
+        for (int k = 0; k < QP / 8; ++k) {
+          const int k0 = 8 * k;
+          mma8(z[n], tf32r(dO(k0 + t, r0)), tf32r(dO(k0 + t, r0 + 8)), tf32r(dO(k0 + t + 4, r0)),
+               tf32r(dO(k0 + t + 4, r0 + 8)), tf32r(imf[po0 + 256u * k]), tf32r(imf[po1 + 256u * k]));
+        }
       }
     }
-    for (int k0 = 0; k0 < QP; k0 += 8) {
-      const uint32_t a0 = tf32r(dos[(k0 + t) * LDO + r0]), a1 = tf32r(dos[(k0 + t) * LDO + r0 + 8]),
-                     a2 = tf32r(dos[(k0 + t + 4) * LDO + r0]), a3 = tf32r(dos[(k0 + t + 4) * LDO + r0 + 8]);
+    // sum the halves: half 1 posts, half 0 adds and posts the sum, half 1 reads it
+    auto zput = [&]() {
 #pragma unroll
-      for (int n = 0; n < 8; ++n) {
-        const int s = 8 * n + g;
-        mma8(z[n], a0, a1, a2, a3, tf32r(ld(il.pm(D, k0 + t, s))), tf32r(ld(il.pm(D, k0 + t + 4, s))));
-      }
+      for (int n = 0; n < 8; ++n)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+          *reinterpret_cast<float2 *>(zbuf + (r0 + 8 * hf) * kChunk + 8 * n + 2 * t) =
+              make_float2(z[n][2 * hf], z[n][2 * hf + 1]);
+    };
+    auto zget = [&](bool add) {
+#pragma unroll
+      for (int n = 0; n < 8; ++n)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const float2 x = *reinterpret_cast<const float2 *>(zbuf + (r0 + 8 * hf) * kChunk + 8 * n + 2 * t);
+          z[n][2 * hf] = add ? z[n][2 * hf] + x.x : x.x;
+          z[n][2 * hf + 1] = add ? z[n][2 * hf + 1] + x.y : x.y;
+        }
+    };
+    if (ch == 1) zput();
+    __syncthreads();
+    if (ch == 0) {
+      zget(true);
+      zput();
     }
-    // D_in = gamma_C D + Z (-W) + dO^T Qh; a fast image holds -W and Qh divided by gamma_C
+    __syncthreads();
+    if (ch == 1) zget(false);
+    // D_in = gamma_C D + Z (-W) + dO^T Qh on this half's columns; a fast image holds -W and Qh
+    // divided by gamma_C
     const float gam = mt.gamma_last;
     if (!mt.fast)
 #pragma unroll
-      for (int j = 0; j < D / 8; ++j)
+      for (int j = 0; j < HC / 8; ++j)
 #pragma unroll
         for (int x = 0; x < 4; ++x) dacc[j][x] *= gam;
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const uint32_t a0 = tf32r(z[ks][0]), a1 = tf32r(z[ks][2]), a2 = tf32r(z[ks][1]), a3 = tf32r(z[ks][3]);
-      const int s0 = 8 * ks + 2 * t;
+    for (int j = 0; j < HC / 8; ++j) {
+      // column f = c0 + 8 j + g: K-block f / 32, chunk ((8 j + g) % 32) / 4 (c0 is a multiple of 32)
+      const uint32_t cq = 2u * (j & 3) + (g >> 2);
+      const uint32_t blk = (il.b1 + (uint32_t)(c0 / 32 + (j >> 2)) * il.b1_block) / 4u + (uint32_t)(g & 3);
+      // -c W rows qp + 8 ks + 2 t (+1): atom qp / 8 + ks, row-in-atom 2t (+1)
+      const uint32_t wo0 = blk + (uint32_t)(QP / 8) * 256u + 2u * t * 32u + (((cq ^ (2u * t)) & 7u) << 2);
+      const uint32_t wo1 = blk + (uint32_t)(QP / 8) * 256u + (2u * t + 1u) * 32u + (((cq ^ (2u * t + 1u)) & 7u) << 2);
 #pragma unroll
-      for (int j = 0; j < D / 8; ++j) {
-        const int f = 8 * j + g;
-        mma8(dacc[j], a0, a1, a2, a3, tf32r(ld(il.wn(QP, s0, f))), tf32r(ld(il.wn(QP, s0 + 1, f))));
-      }
-    }
-    for (int k0 = 0; k0 < QP; k0 += 8) {
-      const uint32_t a0 = tf32r(dos[(k0 + t) * LDO + r0]), a1 = tf32r(dos[(k0 + t) * LDO + r0 + 8]),
-                     a2 = tf32r(dos[(k0 + t + 4) * LDO + r0]), a3 = tf32r(dos[(k0 + t + 4) * LDO + r0 + 8]);
+      for (int ks = 0; ks < 8; ++ks)
+        mma8(dacc[j], tf32r(z[ks][0]), tf32r(z[ks][2]), tf32r(z[ks][1]), tf32r(z[ks][3]), tf32r(imf[wo0 + 256u * ks]),
+             tf32r(imf[wo1 + 256u * ks]));
+      // c Qh rows k0 + t (+4): atom k0 / 8, row-in-atom t (+4)
+      const uint32_t qo0 = blk + t * 32u + (((cq ^ t) & 7u) << 2);
+      const uint32_t qo1 = blk + (t + 4u) * 32u + (((cq ^ (t + 4u)) & 7u) << 2);
 #pragma unroll
-      for (int j = 0; j < D / 8; ++j) {
-        const int f = 8 * j + g;
-        mma8(dacc[j], a0, a1, a2, a3, tf32r(ld(il.qh(k0 + t, f))), tf32r(ld(il.qh(k0 + t + 4, f))));
+      for (int k = 0; k < QP / 8; ++k) {
+        const int k0 = 8 * k;
+        mma8(dacc[j], tf32r(dO(k0 + t, r0)), tf32r(dO(k0 + t, r0 + 8)), tf32r(dO(k0 + t + 4, r0)),
+             tf32r(dO(k0 + t + 4, r0 + 8)), tf32r(imf[qo0 + 256u * k]), tf32r(imf[qo1 + 256u * k]));
       }
     }
     if (mt.fast)
 #pragma unroll
-      for (int j = 0; j < D / 8; ++j)
+      for (int j = 0; j < HC / 8; ++j)
 #pragma unroll
         for (int x = 0; x < 4; ++x) dacc[j][x] *= gam;
-    __syncthreads();  // every warp is done with this stage and with dos
+    __syncthreads();  // every warp is done with this stage, dos and zbuf
     if (tid == 0 && i + nst < nall) issue(i + nst);
   }
   if (aborted) {
@@ -260,10 +306,10 @@ __global__ void __launch_bounds__(2 * D, 1) gdp_bwd_scan_kernel(BwdProblem p) {
   if (p.dinit) {
     float *dst = p.dinit + sh * KV;
 #pragma unroll
-    for (int j = 0; j < D / 8; ++j)
+    for (int j = 0; j < HC / 8; ++j)
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf)
-        *reinterpret_cast<float2 *>(dst + (int64_t)(r0 + 8 * hf) * D + 8 * j + 2 * t) =
+        *reinterpret_cast<float2 *>(dst + (int64_t)(r0 + 8 * hf) * D + c0 + 8 * j + 2 * t) =
             make_float2(dacc[j][2 * hf], dacc[j][2 * hf + 1]);
   }
 }
@@ -271,38 +317,150 @@ __global__ void __launch_bounds__(2 * D, 1) gdp_bwd_scan_kernel(BwdProblem p) {
 // ---------------------------------------------------------------------------------------
 // Per-chunk gradients.
 // ---------------------------------------------------------------------------------------
-constexpr int kVS = 32;        // V columns per CTA
-constexpr int kLS = kVS + 4;   // row stride of [rows][kVS] tiles
-constexpr int kLC = kChunk + 4;  // row stride of [rows][64] tiles
+// acc[16 x 8] += A[16 x 8 ks] B[8 ks x 8] for one output tile (m16n8k8 tf32, fp32 accumulate).
+// A is read as At[k][m] when AT (else row-major [m][k]); B as Bt[n][k] when BT (else
+// row-major [k][n]); pointers are at the tile origin.  arow (per tile row) and bk (per k)
+// scale the operands when given.  Within every 8-wide k step the logical k order is
+// permuted (logical k = t <-> physical 2t, k = t + 4 <-> 2t + 1) for A and B alike, so
+// that row-major A and Bt fragments load as float2.  SPLIT: 3xTF32 (x = hi + lo, the
+// lo*lo product dropped), about fp32 accuracy.
+template <bool AT, bool BT, bool SPLIT>
+__device__ __forceinline__ void tile_mma(float *c, const float *A, int lda, const float *B, int ldb, int ks,
+                                         const float *arow, const float *bk, int g, int t) {
+  const float sa0 = arow ? arow[g] : 1.f, sa1 = arow ? arow[g + 8] : 1.f;
+#pragma unroll 2
+  for (int kk = 0; kk < ks; ++kk) {
+    const int k0 = 8 * kk + 2 * t;
+    float a0, a1, a2, a3, b0, b1;
+    if (!AT) {
+      const float2 x = *reinterpret_cast<const float2 *>(A + g * lda + k0);
+      const float2 y = *reinterpret_cast<const float2 *>(A + (g + 8) * lda + k0);
+      a0 = x.x; a2 = x.y; a1 = y.x; a3 = y.y;
+    } else {
+      a0 = A[k0 * lda + g]; a2 = A[(k0 + 1) * lda + g]; a1 = A[k0 * lda + g + 8]; a3 = A[(k0 + 1) * lda + g + 8];
+    }
+    if (BT) {
+      const float2 x = *reinterpret_cast<const float2 *>(B + g * ldb + k0);
+      b0 = x.x; b1 = x.y;
+    } else {
+      b0 = B[k0 * ldb + g]; b1 = B[(k0 + 1) * ldb + g];
+    }
+    a0 *= sa0; a2 *= sa0; a1 *= sa1; a3 *= sa1;
+    if (bk) {
+      b0 *= bk[k0];
+      b1 *= bk[k0 + 1];
+    }
+    if (SPLIT) {
+      const uint32_t ah0 = tf32r(a0), ah1 = tf32r(a1), ah2 = tf32r(a2), ah3 = tf32r(a3), bh0 = tf32r(b0),
+                     bh1 = tf32r(b1);
+      const uint32_t al0 = tf32r(a0 - __uint_as_float(ah0)), al1 = tf32r(a1 - __uint_as_float(ah1)),
+                     al2 = tf32r(a2 - __uint_as_float(ah2)), al3 = tf32r(a3 - __uint_as_float(ah3)),
+                     bl0 = tf32r(b0 - __uint_as_float(bh0)), bl1 = tf32r(b1 - __uint_as_float(bh1));
+      mma8(c, al0, al1, al2, al3, bh0, bh1);
+      mma8(c, ah0, ah1, ah2, ah3, bl0, bl1);
+      mma8(c, ah0, ah1, ah2, ah3, bh0, bh1);
+    } else {
+      mma8(c, tf32r(a0), tf32r(a1), tf32r(a2), tf32r(a3), tf32r(b0), tf32r(b1));
+    }
+  }
+}
+// As tile_mma for NT adjacent output tiles (columns 8 n .. 8 n + 7 of B for n < NT) that
+// share the A fragments: A is loaded, scaled and rounded once per k step.
+template <int NT, bool AT, bool BT, bool SPLIT>
+__device__ __forceinline__ void tiles_mma(float (*c)[4], const float *A, int lda, const float *B, int ldb, int ks,
+                                          const float *arow, const float *bk, int g, int t) {
+  const float sa0 = arow ? arow[g] : 1.f, sa1 = arow ? arow[g + 8] : 1.f;
+#pragma unroll 1
+  for (int kk = 0; kk < ks; ++kk) {
+    const int k0 = 8 * kk + 2 * t;
+    float a0, a1, a2, a3;
+    if (!AT) {
+      const float2 x = *reinterpret_cast<const float2 *>(A + g * lda + k0);
+      const float2 y = *reinterpret_cast<const float2 *>(A + (g + 8) * lda + k0);
+      a0 = x.x; a2 = x.y; a1 = y.x; a3 = y.y;
+    } else {
+      a0 = A[k0 * lda + g]; a2 = A[(k0 + 1) * lda + g]; a1 = A[k0 * lda + g + 8]; a3 = A[(k0 + 1) * lda + g + 8];
+    }
+    a0 *= sa0; a2 *= sa0; a1 *= sa1; a3 *= sa1;
+    const float s0 = bk ? bk[k0] : 1.f, s1 = bk ? bk[k0 + 1] : 1.f;
+    uint32_t ah[4] = {tf32r(a0), tf32r(a1), tf32r(a2), tf32r(a3)};
+    uint32_t al[4] = {0u, 0u, 0u, 0u};
+    if (SPLIT) {
+      al[0] = tf32r(a0 - __uint_as_float(ah[0]));
+      al[1] = tf32r(a1 - __uint_as_float(ah[1]));
+      al[2] = tf32r(a2 - __uint_as_float(ah[2]));
+      al[3] = tf32r(a3 - __uint_as_float(ah[3]));
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      float b0, b1;
+      if (BT) {
+        const float2 x = *reinterpret_cast<const float2 *>(B + (8 * n + g) * ldb + k0);
+        b0 = x.x; b1 = x.y;
+      } else {
+        b0 = B[k0 * ldb + 8 * n + g]; b1 = B[(k0 + 1) * ldb + 8 * n + g];
+      }
+      b0 *= s0;
+      b1 *= s1;
+      const uint32_t bh0 = tf32r(b0), bh1 = tf32r(b1);
+      if (SPLIT) {
+        const uint32_t bl0 = tf32r(b0 - __uint_as_float(bh0)), bl1 = tf32r(b1 - __uint_as_float(bh1));
+        mma8(c[n], al[0], al[1], al[2], al[3], bh0, bh1);
+        mma8(c[n], ah[0], ah[1], ah[2], ah[3], bl0, bl1);
+      }
+      mma8(c[n], ah[0], ah[1], ah[2], ah[3], bh0, bh1);
+    }
+  }
+}
+// Row / column of element x of an m16n8 accumulator tile.
+__device__ __forceinline__ int trow(int x, int g) { return g + 8 * (x >> 1); }
+__device__ __forceinline__ int tcol(int x, int t) { return 2 * t + (x & 1); }
+
+constexpr int kChunkThreads = 512;  // 16 warps
+constexpr int kLC = kChunk + 8;     // row stride of [rows][64] tiles (8 mod 32: conflict-free float2)
 
 struct ChunkSmem {
-  uint32_t kh, qh, vs, dos, ss, dcs, lm, pm, et, vt, dl, qs, m1, m3, scal, total;
-  __host__ __device__ ChunkSmem(int d, int qp) {
-    const uint32_t ld = (uint32_t)(d + 4) * 4u;
+  int ldd, ldv, ldq;
+  uint32_t kh, qh, lm, tm, pm, g1, g23, g4, ss, dcs, vs, dos, rhs, qs, zt, dl, vt, scal, total;
+  __host__ __device__ ChunkSmem(int d, int qp, int vsl) {
+    ldd = d + 8;
+    ldv = vsl + 8;
+    ldq = qp + 8;
     uint32_t o = 0;
-    kh = o; o += kChunk * ld;           // khat [64][d]
-    qh = o; o += qp * ld;               // qhat readout rows [qp][d]
-    vs = o; o += kChunk * kLS * 4u;     // v slice [64][32]
-    dos = o; o += qp * kLS * 4u;        // d_output slice [qp][32]
-    ss = o; o += kVS * ld;              // S slice [32][d]
-    dcs = o; o += kVS * ld;             // D_C slice [32][d]
-    lm = o; o += kChunk * kLC * 4u;     // L, then M2 [64][64]
-    pm = o; o += qp * kLC * 4u;         // P, then M4 [qp][64]
-    et = o; o += kChunk * kLS * 4u;     // rhs, then e [64][32]
-    vt = o; o += kChunk * kLS * 4u;     // vt [64][32]
-    dl = o; o += kChunk * kLS * 4u;     // Zt, then Delta [64][32]
-    qs = o; o += qp * kLS * 4u;         // qhat S^T [qp][32]
-    m1 = o; o += kChunk * (qp + 4) * 4u;  // M1 [64][qp]
-    m3 = o; o += kChunk * kLC * 4u;     // M3 [64][64]
-    scal = o; o += 5u * kChunk * 4u;    // G, beta, rk, rq, gamma
+    auto take = [&](uint32_t floats) {
+      const uint32_t at = o;
+      o += (floats * 4u + 15u) & ~15u;
+      return at;
+    };
+    kh = take(kChunk * ldd);    // khat [64][d]
+    qh = take(qp * ldd);        // qhat readout rows [qp][d]
+    lm = take(kChunk * kLC);    // L [64][64] (decayed Gram, strictly lower)
+    tm = take(kChunk * kLC);    // T = (I + diag(beta) L)^-1 (adjacent to L: together the dkhat staging)
+    pm = take(qp * kLC);        // P [qp][64]
+    g1 = take(kChunk * ldq);    // sum over V of e dO^T [64][qp]
+    g23 = take(kChunk * kLC);   // upper: sum e dv^T, lower: sum dv vt^T [64][64]
+    g4 = take(qp * kLC);        // sum dO vt^T [qp][64]
+    ss = take(vsl * ldd);       // S slice [vsl][d]
+    dcs = take(vsl * ldd);      // D_C slice [vsl][d]
+    vs = take(kChunk * ldv);    // v slice [64][vsl]
+    dos = take(qp * ldv);       // d_output slice [qp][vsl]
+    rhs = take(kChunk * ldv);   // rhs, then e [64][vsl]
+    qs = take(qp * ldv);        // qhat S^T [qp][vsl]
+    zt = take(kChunk * ldv);    // Ktil D_C^T + P^T dO [64][vsl]
+    dl = take(kChunk * ldv);    // Delta [64][vsl]
+    vt = take(kChunk * ldv);    // vt [64][vsl]
+    scal = take(14 * kChunk);   // per-row factors and sums
     total = o;
   }
 };
 
-template <int D>
-__global__ void __launch_bounds__(256, 1) gdp_bwd_chunk_kernel(BwdProblem p) {
-  constexpr int LD = D + 4;
-  const int row = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * kVS;
+// One CTA per (expanded chunk, head); V in slices of VSL columns.  T = (I + A)^-1 is formed
+// once, so the two triangular solves of every slice are small matrix products (3xTF32).
+// dkhat and dqhat sum over the slices in registers and leave through the L2-norm chain
+// rule; dbeta, sum_v dv v and do . o are complete per chunk and stored as they are.
+template <int D, int VSL>
+__global__ void __launch_bounds__(kChunkThreads, 1) gdp_bwd_chunk_kernel(BwdProblem p) {
+  const int row = blockIdx.x, h = blockIdx.y;
   const int seq = p.cid[2 * row], c = p.cid[2 * row + 1];
   if (seq < 0 || seq >= p.N || row >= p.ws_rows) return;
   int64_t bos, L;
@@ -317,27 +475,25 @@ __global__ void __launch_bounds__(256, 1) gdp_bwd_chunk_kernel(BwdProblem p) {
   const int p0 = (M - 1 - r0m) % M;
   const int nq = (p0 < len) ? (len - 1 - p0) / M + 1 : 0;
   const int64_t tq0 = (R0 + p0) / M;
-  const int64_t srow = (int64_t)p.cod[seq] + c;  // state rows of this chunk in Sx / Dx
+  const int64_t srow = (int64_t)p.cod[seq] + c;
 
   extern __shared__ __align__(16) unsigned char bwd_chunk_raw[];
-  const ChunkSmem lay(D, QP);
+  const ChunkSmem lay(D, QP, VSL);
+  const int LDD = lay.ldd, LDV = lay.ldv, LDQ = lay.ldq;
   unsigned char *sm = bwd_chunk_raw;
-  float *kh = reinterpret_cast<float *>(sm + lay.kh), *qh = reinterpret_cast<float *>(sm + lay.qh);
-  float *vs = reinterpret_cast<float *>(sm + lay.vs), *dos = reinterpret_cast<float *>(sm + lay.dos);
-  float *ss = reinterpret_cast<float *>(sm + lay.ss), *dcs = reinterpret_cast<float *>(sm + lay.dcs);
-  float *lm = reinterpret_cast<float *>(sm + lay.lm), *pm = reinterpret_cast<float *>(sm + lay.pm);
-  float *et = reinterpret_cast<float *>(sm + lay.et), *vt = reinterpret_cast<float *>(sm + lay.vt);
-  float *dl = reinterpret_cast<float *>(sm + lay.dl), *qs = reinterpret_cast<float *>(sm + lay.qs);
-  float *m1 = reinterpret_cast<float *>(sm + lay.m1), *m3 = reinterpret_cast<float *>(sm + lay.m3);
-  float *G = reinterpret_cast<float *>(sm + lay.scal), *bt = G + kChunk, *rk = bt + kChunk, *rq = rk + kChunk,
-        *gm = rq + kChunk;
-  const int LM1 = QP + 4;
+  auto F = [&](uint32_t off) { return reinterpret_cast<float *>(sm + off); };
+  float *kh = F(lay.kh), *qh = F(lay.qh), *lm = F(lay.lm), *tm = F(lay.tm), *pm = F(lay.pm);
+  float *g1 = F(lay.g1), *g23 = F(lay.g23), *g4 = F(lay.g4), *ss = F(lay.ss), *dcs = F(lay.dcs);
+  float *vs = F(lay.vs), *dos = F(lay.dos), *rhs = F(lay.rhs), *qs = F(lay.qs), *zt = F(lay.zt), *dl = F(lay.dl),
+        *vt = F(lay.vt);
+  float *G = F(lay.scal), *bt = G + kChunk, *gm = bt + kChunk, *fc = gm + kChunk, *bfc = fc + kChunk,
+        *gb = bfc + kChunk, *rk = gb + kChunk, *rq = rk + kChunk, *gq = rq + kChunk, *sdb = gq + kChunk,
+        *ssg = sdb + kChunk, *srho = ssg + kChunk, *scq = srho + kChunk, *mgb = scq + kChunk;
   __shared__ float carry;
 
   // ---- scalars: beta, gates, within-chunk cumulative log decay ----
   if (tid < kChunk) {
-    const int r = tid;
-    const int pos = r0m + r;
+    const int r = tid, pos = r0m + r;
     float b = 0.f, gate = 0.f;
     if (r < len) {
       b = p.beta ? p.beta[(R0 + r) * H + h] : 1.f;
@@ -352,385 +508,396 @@ __global__ void __launch_bounds__(256, 1) gdp_bwd_chunk_kernel(BwdProblem p) {
     }
     if (r == 31) carry = x;
     G[r] = x;
+    sdb[r] = ssg[r] = srho[r] = 0.f;
   }
-  // ---- khat rows (4 threads per row), qhat readout rows, slices of v, d_output, S, D_C ----
-  {
-    const int r = tid >> 2, part = tid & 3;  // 64 rows x 4 parts of D / 4 features
-    float x[D / 4];
-    float ss2 = 0.f;
-    const bool live = r < len;
-    const __nv_bfloat16 *src = p.k + (R0 + r) * p.k_st + (int64_t)h * p.k_sh + part * (D / 4);
+  // ---- khat and qhat rows (8 threads per row) ----
+  for (int r = tid >> 3; r < kChunk + QP; r += kChunkThreads / 8) {
+    const int part = tid & 7;
+    const bool isk = r < kChunk;
+    const int rr = isk ? r : r - kChunk;
+    const bool live = isk ? rr < len : rr < nq;
+    const __nv_bfloat16 *src = isk ? p.k + (R0 + rr) * p.k_st + (int64_t)h * p.k_sh
+                                   : p.q + (tq0 + rr) * p.q_st + (int64_t)h * p.q_sh;
+    float x[D / 8];
+    float s2 = 0.f;
 #pragma unroll
-    for (int i = 0; i < D / 4; i += 8) {
+    for (int i = 0; i < D / 8; i += 8) {
       uint4 u = make_uint4(0u, 0u, 0u, 0u);
-      if (live) u = *reinterpret_cast<const uint4 *>(src + i);
+      if (live) u = *reinterpret_cast<const uint4 *>(src + part * (D / 8) + i);
       const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&u);
 #pragma unroll
       for (int q2 = 0; q2 < 4; ++q2) {
         const float2 f = __bfloat1622float2(b2[q2]);
         x[i + 2 * q2] = f.x;
         x[i + 2 * q2 + 1] = f.y;
-        ss2 += f.x * f.x + f.y * f.y;
+        s2 += f.x * f.x + f.y * f.y;
       }
     }
-    ss2 += __shfl_xor_sync(0xffffffffu, ss2, 1);
-    ss2 += __shfl_xor_sync(0xffffffffu, ss2, 2);
-    const float inv = p.l2norm ? rsqrtf(ss2 + kL2Eps) : 1.f;
-    if (part == 0) rk[r] = inv;
+    s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
+    s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
+    s2 += __shfl_xor_sync(0xffffffffu, s2, 4);
+    const float inv = p.l2norm ? rsqrtf(s2 + kL2Eps) : 1.f;
+    if (part == 0) (isk ? rk : rq)[rr] = inv;
+    float *dst = (isk ? kh : qh) + rr * LDD + part * (D / 8);
 #pragma unroll
-    for (int i = 0; i < D / 4; i += 4)
-      *reinterpret_cast<float4 *>(kh + r * LD + part * (D / 4) + i) =
-          make_float4(x[i] * inv, x[i + 1] * inv, x[i + 2] * inv, x[i + 3] * inv);
-  }
-  for (int r = tid >> 2; r < QP; r += 64) {
-    const int part = tid & 3;
-    float x[D / 4];
-    float ss2 = 0.f;
-    const bool live = r < nq;
-    const __nv_bfloat16 *src = p.q + (tq0 + r) * p.q_st + (int64_t)h * p.q_sh + part * (D / 4);
-#pragma unroll
-    for (int i = 0; i < D / 4; i += 8) {
-      uint4 u = make_uint4(0u, 0u, 0u, 0u);
-      if (live) u = *reinterpret_cast<const uint4 *>(src + i);
-      const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&u);
-#pragma unroll
-      for (int q2 = 0; q2 < 4; ++q2) {
-        const float2 f = __bfloat1622float2(b2[q2]);
-        x[i + 2 * q2] = f.x;
-        x[i + 2 * q2 + 1] = f.y;
-        ss2 += f.x * f.x + f.y * f.y;
-      }
-    }
-    ss2 += __shfl_xor_sync(0xffffffffu, ss2, 1);
-    ss2 += __shfl_xor_sync(0xffffffffu, ss2, 2);
-    const float inv = p.l2norm ? rsqrtf(ss2 + kL2Eps) : 1.f;
-    if (part == 0) rq[r] = inv;
-#pragma unroll
-    for (int i = 0; i < D / 4; i += 4)
-      *reinterpret_cast<float4 *>(qh + r * LD + part * (D / 4) + i) =
-          make_float4(x[i] * inv, x[i + 1] * inv, x[i + 2] * inv, x[i + 3] * inv);
-  }
-  for (int idx = tid; idx < kChunk * (kVS / 4); idx += 256) {  // v slice
-    const int r = idx / (kVS / 4), c4 = (idx % (kVS / 4)) * 4;
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (r < len) {
-      const uint2 u = *reinterpret_cast<const uint2 *>(p.v + (R0 + r) * p.v_st + (int64_t)h * p.v_sh + v0 + c4);
-      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
-      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
-      x = make_float4(a.x, a.y, b.x, b.y);
-    }
-    *reinterpret_cast<float4 *>(vs + r * kLS + c4) = x;
-  }
-  for (int idx = tid; idx < QP * (kVS / 4); idx += 256) {  // d_output slice
-    const int r = idx / (kVS / 4), c4 = (idx % (kVS / 4)) * 4;
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (r < nq) {
-      const uint2 u = *reinterpret_cast<const uint2 *>(p.dout + ((tq0 + r) * H + h) * (int64_t)D + v0 + c4);
-      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
-      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
-      x = make_float4(a.x, a.y, b.x, b.y);
-    }
-    *reinterpret_cast<float4 *>(dos + r * kLS + c4) = x;
-  }
-  {
-    const int64_t KV = (int64_t)D * D;
-    const float *S = p.Sx + (srow * H + h) * KV + (int64_t)v0 * D;
-    const float *Dc = p.Dx + (srow * H + h) * KV + (int64_t)v0 * D;
-    for (int idx = tid; idx < kVS * (D / 4); idx += 256) {
-      const int r = idx / (D / 4), c4 = (idx % (D / 4)) * 4;
-      *reinterpret_cast<float4 *>(ss + r * LD + c4) = *reinterpret_cast<const float4 *>(S + (int64_t)r * D + c4);
-      *reinterpret_cast<float4 *>(dcs + r * LD + c4) = *reinterpret_cast<const float4 *>(Dc + (int64_t)r * D + c4);
-    }
+    for (int i = 0; i < D / 8; i += 4)
+      *reinterpret_cast<float4 *>(dst + i) = make_float4(x[i] * inv, x[i + 1] * inv, x[i + 2] * inv, x[i + 3] * inv);
   }
   __syncthreads();
   if (tid < kChunk) {
     const float x = (tid >= 32 ? G[tid] + carry : G[tid]);
     G[tid] = x;
-    gm[tid] = expf(x);
   }
   __syncthreads();
   const float GC = G[len - 1], scale = p.scale;
   auto pr = [&](int qi) { return p0 + qi * M; };  // local row of readout qi
+  if (tid < kChunk) {
+    const int r = tid;
+    const float gr = expf(G[r]), f = expf(GC - G[r]), b = bt[r];
+    gm[r] = gr;           // gamma_r
+    fc[r] = f;            // gamma_C / gamma_r
+    bfc[r] = b * f;       // beta_r gamma_C / gamma_r
+    gb[r] = gr * b;       // gamma_r beta_r
+    mgb[r] = -gr * b;     // -gamma_r beta_r
+    gq[r] = (r < nq) ? scale * expf(G[pr(r)]) : 0.f;  // scale gamma_p of readout r
+    scq[r] = scale;
+  }
+  __syncthreads();
 
-  // ---- Gram products: L (64 x 64) and P (qp x 64) ----
-  for (int u = warp; u < 4 * 8 + (QP / 16) * 8; u += 8) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    const bool isL = u < 32;
-    const int uu = isL ? u : u - 32;
-    const int m0 = 16 * (uu >> 3), n0 = 8 * (uu & 7);
-    const float *A = isL ? kh : qh;
-    mma_tile(acc, D / 8, g, t, [&](int r, int k) { return A[(m0 + r) * LD + k]; },
-             [&](int k, int n) { return kh[(n0 + n) * LD + k]; });
+  // ---- L [64 x 64] and P [qp x 64] ----
+  for (int u = warp; u < 2 * (4 + QP / 16); u += kChunkThreads / 32) {  // (m-tile, 4 n-tiles) units
+    float acc[4][4] = {};
+    const bool isL = u < 8;
+    const int uu = isL ? u : u - 8, m0 = 16 * (uu >> 1), n0 = 32 * (uu & 1);
+    tiles_mma<4, false, true, false>(acc, (isL ? kh : qh) + m0 * LDD, LDD, kh + n0 * LDD, LDD, D / 8, nullptr,
+                                     nullptr, g, t);
 #pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      const int r = m0 + g + 8 * (x >> 1), j = n0 + 2 * t + (x & 1);
-      if (isL) {
-        lm[r * kLC + j] = (j < r) ? expf(G[r] - G[j]) * acc[x] : 0.f;
-      } else {
-        const int pp = pr(r);
-        pm[r * kLC + j] = (r < nq && j <= pp) ? scale * expf(G[pp] - G[j]) * acc[x] : 0.f;
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int r = m0 + trow(x, g), j = n0 + 8 * n + tcol(x, t);
+        if (isL) {
+          lm[r * kLC + j] = (j < r) ? expf(G[r] - G[j]) * acc[n][x] : 0.f;
+        } else {
+          const bool ok = r < nq && j <= pr(r);
+          pm[r * kLC + j] = ok ? scale * expf(G[pr(r)] - G[j]) * acc[n][x] : 0.f;
+        }
       }
-    }
   }
+  // zero the slice sums of the Gram matrices
+  for (int i = tid; i < kChunk * LDQ; i += kChunkThreads) g1[i] = 0.f;
+  for (int i = tid; i < kChunk * kLC; i += kChunkThreads) g23[i] = 0.f;
+  for (int i = tid; i < QP * kLC; i += kChunkThreads) g4[i] = 0.f;
   __syncthreads();
-  // ---- rhs = v - gamma (Khat S^T);  qhat S^T;  Zt = Ktil D_C^T + P^T dO ----
-  for (int u = warp; u < 16 + (QP / 16) * 4 + 16; u += 8) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (u < 16) {
-      const int m0 = 16 * (u >> 2), n0 = 8 * (u & 3);
-      mma_tile(acc, D / 8, g, t, [&](int r, int k) { return kh[(m0 + r) * LD + k]; },
-               [&](int k, int n) { return ss[(n0 + n) * LD + k]; });
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const int r = m0 + g + 8 * (x >> 1), j = n0 + 2 * t + (x & 1);
-        et[r * kLS + j] = vs[r * kLS + j] - gm[r] * acc[x];
-      }
-    } else if (u < 16 + (QP / 16) * 4) {
-      const int uu = u - 16, m0 = 16 * (uu >> 2), n0 = 8 * (uu & 3);
-      mma_tile(acc, D / 8, g, t, [&](int r, int k) { return qh[(m0 + r) * LD + k]; },
-               [&](int k, int n) { return ss[(n0 + n) * LD + k]; });
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const int r = m0 + g + 8 * (x >> 1), j = n0 + 2 * t + (x & 1);
-        qs[r * kLS + j] = acc[x];
-      }
-    } else {
-      const int uu = u - 16 - (QP / 16) * 4, m0 = 16 * (uu >> 2), n0 = 8 * (uu & 3);
-      mma_tile(acc, D / 8, g, t, [&](int r, int k) { return expf(GC - G[m0 + r]) * kh[(m0 + r) * LD + k]; },
-               [&](int k, int n) { return dcs[(n0 + n) * LD + k]; });
-      mma_tile(acc, QP / 8, g, t, [&](int r, int k) { return pm[k * kLC + m0 + r]; },
-               [&](int k, int n) { return dos[k * kLS + n0 + n]; });
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const int r = m0 + g + 8 * (x >> 1), j = n0 + 2 * t + (x & 1);
-        dl[r * kLS + j] = acc[x];
-      }
-    }
-  }
-  __syncthreads();
-  // ---- substitutions, per column (8 threads per column, row terms split by j mod 8) ----
+  // ---- T = (I + A)^-1, A = diag(beta) L: column c by forward substitution, 8 threads per column ----
   {
     const int col = tid >> 3, i = tid & 7;
     float hist[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    // e_r = rhs_r - sum_{j<r} L_rj vt_j;  vt_r = beta_r e_r
 #pragma unroll
     for (int r = 0; r < kChunk; ++r) {
       float part = 0.f;
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj)
-        if (8 * jj < r) {  // rows j = 8 jj + i < r (the entries of L at j >= r are zero)
-          part += lm[r * kLC + 8 * jj + i] * hist[jj];
-        }
+        if (8 * jj < r) part += lm[r * kLC + 8 * jj + i] * hist[jj];  // L_rj = 0 for j >= r
       part += __shfl_xor_sync(0xffffffffu, part, 1);
       part += __shfl_xor_sync(0xffffffffu, part, 2);
       part += __shfl_xor_sync(0xffffffffu, part, 4);
-      const float e = et[r * kLS + col] - part;
-      const float vv = bt[r] * e;
+      const float val = (r == col ? 1.f : 0.f) - bt[r] * part;
       if ((r & 7) == i) {
-        hist[r >> 3] = vv;
-        et[r * kLS + col] = e;
-        vt[r * kLS + col] = vv;
-      }
-    }
-    // Delta_r = Zt_r - sum_{j>r} beta_j L_jr Delta_j
-#pragma unroll
-    for (int jj = 0; jj < 8; ++jj) hist[jj] = 0.f;
-#pragma unroll
-    for (int r = kChunk - 1; r >= 0; --r) {
-      float part = 0.f;
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj)
-        if (8 * jj + 7 > r) {
-          const int j = 8 * jj + i;
-          part += (j > r) ? bt[j] * lm[j * kLC + r] * hist[jj] : 0.f;
-        }
-      part += __shfl_xor_sync(0xffffffffu, part, 1);
-      part += __shfl_xor_sync(0xffffffffu, part, 2);
-      part += __shfl_xor_sync(0xffffffffu, part, 4);
-      const float dd = dl[r * kLS + col] - part;
-      if ((r & 7) == i) {
-        hist[r >> 3] = dd;
-        dl[r * kLS + col] = dd;
+        hist[r >> 3] = val;
+        tm[r * kLC + col] = val;
       }
     }
   }
   __syncthreads();
-  // ---- dv (this slice), and the slice's shares of dbeta and of sum_v dv v ----
-  for (int r = warp; r < len; r += 8) {
-    const float d = dl[r * kLS + lane], b = bt[r];
-    p.dv[((R0 + r) * H + h) * (int64_t)D + v0 + lane] = b * d;
-    float sdb = et[r * kLS + lane] * d, ssg = b * d * vs[r * kLS + lane];
+
+  // dkhat / dqhat accumulators: warp w owns output tiles of a fixed m-tile and a run of n-tiles
+  constexpr int NTK = (kChunk / 16) * (D / 8) / (kChunkThreads / 32);  // dkhat tiles per warp
+  const int mk = warp % 4, nk0 = (warp / 4) * NTK;
+  float dk_acc[NTK][4];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      sdb += __shfl_xor_sync(0xffffffffu, sdb, o);
-      ssg += __shfl_xor_sync(0xffffffffu, ssg, o);
+  for (int i = 0; i < NTK; ++i) dk_acc[i][0] = dk_acc[i][1] = dk_acc[i][2] = dk_acc[i][3] = 0.f;
+  const int nqt = (QP / 16) * (D / 8);  // dqhat tiles, dealt round robin: tile warp + 16 i
+  constexpr int NTQ = (4 * (D / 8) + kChunkThreads / 32 - 1) / (kChunkThreads / 32);  // qp <= 64
+  float dq_acc[NTQ][4];
+#pragma unroll
+  for (int i = 0; i < NTQ; ++i) dq_acc[i][0] = dq_acc[i][1] = dq_acc[i][2] = dq_acc[i][3] = 0.f;
+  auto dq_tile = [&](int i, int &m0, int &n0) {
+    const int u = warp + (kChunkThreads / 32) * i;
+    m0 = 16 * (u / (D / 8));
+    n0 = 8 * (u % (D / 8));
+    return u < nqt;
+  };
+
+  const int64_t KV = (int64_t)D * D;
+  const float *Sg = p.Sx + (srow * H + h) * KV;
+  const float *Dg = p.Dx + (srow * H + h) * KV;
+  constexpr int NVS = VSL / 8;  // n-tiles per slice
+#pragma unroll 1
+  for (int v0 = 0; v0 < D; v0 += VSL) {
+    // ---- slice loads: S and D_C rows v0 .., v and d_output columns v0 .. ----
+    for (int idx = tid; idx < VSL * (D / 4); idx += kChunkThreads) {
+      const int r = idx / (D / 4), c4 = (idx % (D / 4)) * 4;
+      *reinterpret_cast<float4 *>(ss + r * LDD + c4) =
+          *reinterpret_cast<const float4 *>(Sg + (int64_t)(v0 + r) * D + c4);
+      *reinterpret_cast<float4 *>(dcs + r * LDD + c4) =
+          *reinterpret_cast<const float4 *>(Dg + (int64_t)(v0 + r) * D + c4);
     }
-    if (lane == 0) {
-      if (p.dbeta) atomicAdd(p.dbeta + (R0 + r) * H + h, sdb);
-      atomicAdd(p.sig + (R0 + r) * H + h, ssg);
+    for (int idx = tid; idx < (kChunk + QP) * (VSL / 4); idx += kChunkThreads) {
+      const int r = idx / (VSL / 4), c4 = (idx % (VSL / 4)) * 4;
+      const bool isv = r < kChunk;
+      const int rr = isv ? r : r - kChunk;
+      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (isv ? rr < len : rr < nq) {
+        const __nv_bfloat16 *src = isv ? p.v + (R0 + rr) * p.v_st + (int64_t)h * p.v_sh + v0 + c4
+                                       : p.dout + ((tq0 + rr) * H + h) * (int64_t)D + v0 + c4;
+        const uint2 u = *reinterpret_cast<const uint2 *>(src);
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+        x = make_float4(a.x, a.y, b.x, b.y);
+      }
+      *reinterpret_cast<float4 *>((isv ? vs : dos) + rr * LDV + c4) = x;
     }
+    __syncthreads();
+    // ---- rhs = v - gamma (Khat S^T);  QS = qhat S^T;  Zt = Ktil D_C^T + P^T dO ----
+    for (int u = warp; u < 8 + QP / 16; u += kChunkThreads / 32) {  // (m-tile, all NVS n-tiles) units
+      float acc[NVS][4] = {};
+      if (u < 4) {
+        const int m0 = 16 * u;
+        tiles_mma<NVS, false, true, false>(acc, kh + m0 * LDD, LDD, ss, LDD, D / 8, nullptr, nullptr, g, t);
+#pragma unroll
+        for (int n = 0; n < NVS; ++n)
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const int r = m0 + trow(x, g), j = 8 * n + tcol(x, t);
+            rhs[r * LDV + j] = vs[r * LDV + j] - gm[r] * acc[n][x];
+          }
+      } else if (u < 8) {
+        const int m0 = 16 * (u - 4);
+        tiles_mma<NVS, false, true, false>(acc, kh + m0 * LDD, LDD, dcs, LDD, D / 8, fc + m0, nullptr, g, t);
+        tiles_mma<NVS, true, false, false>(acc, pm + m0, kLC, dos, LDV, QP / 8, nullptr, nullptr, g, t);
+#pragma unroll
+        for (int n = 0; n < NVS; ++n)
+#pragma unroll
+          for (int x = 0; x < 4; ++x) zt[(m0 + trow(x, g)) * LDV + 8 * n + tcol(x, t)] = acc[n][x];
+      } else {
+        const int m0 = 16 * (u - 8);
+        tiles_mma<NVS, false, true, false>(acc, qh + m0 * LDD, LDD, ss, LDD, D / 8, nullptr, nullptr, g, t);
+#pragma unroll
+        for (int n = 0; n < NVS; ++n)
+#pragma unroll
+          for (int x = 0; x < 4; ++x) qs[(m0 + trow(x, g)) * LDV + 8 * n + tcol(x, t)] = acc[n][x];
+      }
+    }
+    __syncthreads();
+    // ---- vt = T diag(beta) rhs;  Delta = T^T Zt  (3xTF32) ----
+    for (int u = warp; u < 8; u += kChunkThreads / 32) {
+      float acc[NVS][4] = {};
+      const bool isv = u < 4;
+      const int m0 = 16 * (isv ? u : u - 4);
+      if (isv)
+        tiles_mma<NVS, false, false, true>(acc, tm + m0 * kLC, kLC, rhs, LDV, kChunk / 8, nullptr, bt, g, t);
+      else
+        tiles_mma<NVS, true, false, true>(acc, tm + m0, kLC, zt, LDV, kChunk / 8, nullptr, nullptr, g, t);
+#pragma unroll
+      for (int n = 0; n < NVS; ++n)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) (isv ? vt : dl)[(m0 + trow(x, g)) * LDV + 8 * n + tcol(x, t)] = acc[n][x];
+    }
+    __syncthreads();
+    // ---- e = rhs - L vt (in place);  o = scale gamma_p QS + P vt -> do . o;  dv out ----
+    for (int u = warp; u < 4 + QP / 16; u += kChunkThreads / 32) {
+      float acc[NVS][4] = {};
+      if (u < 4) {
+        const int m0 = 16 * u;
+        tiles_mma<NVS, false, false, false>(acc, lm + m0 * kLC, kLC, vt, LDV, kChunk / 8, nullptr, nullptr, g, t);
+#pragma unroll
+        for (int n = 0; n < NVS; ++n)
+#pragma unroll
+          for (int x = 0; x < 4; ++x) rhs[(m0 + trow(x, g)) * LDV + 8 * n + tcol(x, t)] -= acc[n][x];
+      } else {
+        const int m0 = 16 * (u - 4);
+        tiles_mma<NVS, false, false, false>(acc, pm + m0 * kLC, kLC, vt, LDV, kChunk / 8, nullptr, nullptr, g, t);
+        float part[2] = {0.f, 0.f};
+#pragma unroll
+        for (int n = 0; n < NVS; ++n)
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const int r = m0 + trow(x, g), j = 8 * n + tcol(x, t);
+            part[x >> 1] += (gq[r] * qs[r * LDV + j] + acc[n][x]) * dos[r * LDV + j];
+          }
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {  // the unit covers the slice: one plain add per row
+          float s = part[hf];
+          s += __shfl_xor_sync(0xffffffffu, s, 1);
+          s += __shfl_xor_sync(0xffffffffu, s, 2);
+          if (t == 0) srho[m0 + g + 8 * hf] += s;
+        }
+      }
+    }
+    for (int idx = tid; idx < len * VSL; idx += kChunkThreads) {
+      const int r = idx / VSL, j = idx % VSL;
+      p.dv[((R0 + r) * H + h) * (int64_t)D + v0 + j] = bt[r] * dl[r * LDV + j];
+    }
+    __syncthreads();
+    // ---- row sums: dbeta += e . Delta, sum dv v;  Gram sums over V;  dkhat, dqhat shares ----
+    if (tid < 2 * kChunk) {
+      const int r = tid >> 1, hf = tid & 1;
+      float a = 0.f, b = 0.f;
+#pragma unroll
+      for (int j = hf * (VSL / 2); j < (hf + 1) * (VSL / 2); ++j) {
+        a += rhs[r * LDV + j] * dl[r * LDV + j];
+        b += dl[r * LDV + j] * vs[r * LDV + j];
+      }
+      a += __shfl_xor_sync(0xffffffffu, a, 1);
+      b += __shfl_xor_sync(0xffffffffu, b, 1);
+      if (hf == 0) {
+        sdb[r] += a;
+        ssg[r] += bt[r] * b;
+      }
+    }
+    {
+      // G1 += e dO^T [64 x qp]; G23 += (upper) e dv^T, (lower) dv vt^T; G4 += dO vt^T [qp x 64]
+      // units: G1 (m-tile, qp/8 n-tiles), G23 (m-tile, 4 n-tiles, upper and lower products), G4
+      // (m-tile, 4 n-tiles); the A rows of G23's lower product are dv = beta Delta
+      const int n1 = 4, n4 = 2 * (QP / 16);
+      for (int u = warp; u < n1 + 8 + n4; u += kChunkThreads / 32) {
+        if (u < n1) {
+          const int m0 = 16 * u;
+          float acc[8][4] = {};
+          if (QP == 16)
+            tiles_mma<2, false, true, false>(acc, rhs + m0 * LDV, LDV, dos, LDV, VSL / 8, nullptr, nullptr, g, t);
+          else if (QP == 32)
+            tiles_mma<4, false, true, false>(acc, rhs + m0 * LDV, LDV, dos, LDV, VSL / 8, nullptr, nullptr, g, t);
+          else
+            tiles_mma<8, false, true, false>(acc, rhs + m0 * LDV, LDV, dos, LDV, VSL / 8, nullptr, nullptr, g, t);
+#pragma unroll
+          for (int n = 0; n < 8; ++n)
+            if (n < QP / 8)
+#pragma unroll
+              for (int x = 0; x < 4; ++x) g1[(m0 + trow(x, g)) * LDQ + 8 * n + tcol(x, t)] += acc[n][x];
+        } else if (u < n1 + 8) {
+          const int uu = u - n1, m0 = 16 * (uu >> 1), n0 = 32 * (uu & 1);
+          float up[4][4] = {}, lo[4][4] = {};
+          tiles_mma<4, false, true, false>(up, rhs + m0 * LDV, LDV, dl + n0 * LDV, LDV, VSL / 8, nullptr, nullptr, g, t);
+          tiles_mma<4, false, true, false>(lo, dl + m0 * LDV, LDV, vt + n0 * LDV, LDV, VSL / 8, bt + m0, nullptr, g, t);
+#pragma unroll
+          for (int n = 0; n < 4; ++n)
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              const int r = m0 + trow(x, g), j = n0 + 8 * n + tcol(x, t);
+              g23[r * kLC + j] += (j > r) ? bt[j] * up[n][x] : (j < r) ? lo[n][x] : 0.f;
+            }
+        } else {
+          const int uu = u - n1 - 8, m0 = 16 * (uu >> 1), n0 = 32 * (uu & 1);
+          float acc[4][4] = {};
+          tiles_mma<4, false, true, false>(acc, dos + m0 * LDV, LDV, vt + n0 * LDV, LDV, VSL / 8, nullptr, nullptr, g, t);
+#pragma unroll
+          for (int n = 0; n < 4; ++n)
+#pragma unroll
+            for (int x = 0; x < 4; ++x) g4[(m0 + trow(x, g)) * kLC + n0 + 8 * n + tcol(x, t)] += acc[n][x];
+        }
+      }
+    }
+    // dkhat += (beta gamma_C / gamma) e D_C - (gamma beta Delta) S
+    tiles_mma<NTK, false, false, false>(dk_acc, rhs + 16 * mk * LDV, LDV, dcs + 8 * nk0, LDD, VSL / 8, bfc + 16 * mk,
+                                        nullptr, g, t);
+    tiles_mma<NTK, false, false, false>(dk_acc, dl + 16 * mk * LDV, LDV, ss + 8 * nk0, LDD, VSL / 8, mgb + 16 * mk,
+                                        nullptr, g, t);
+    // dqhat += (scale gamma_p dO) S
+#pragma unroll
+    for (int i = 0; i < NTQ; ++i)
+      if (int m0, n0; dq_tile(i, m0, n0)) {
+        tile_mma<false, false, false>(dq_acc[i], dos + m0 * LDV, LDV, ss + n0, LDD, VSL / 8, gq + m0, nullptr, g, t);
+      }
+    __syncthreads();
   }
-  // ---- o (this slice) = scale gamma_p (qhat S^T) + P vt, and the slice's share of do . o ----
-  for (int u = warp; u < (QP / 16) * 4; u += 8) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    const int m0 = 16 * (u >> 2), n0 = 8 * (u & 3);
-    mma_tile(acc, kChunk / 8, g, t, [&](int r, int k) { return pm[(m0 + r) * kLC + k]; },
-             [&](int k, int n) { return vt[k * kLS + n0 + n]; });
-    float part[2] = {0.f, 0.f};
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      const int r = m0 + g + 8 * (x >> 1), j = n0 + 2 * t + (x & 1);
-      const float o = (r < nq) ? scale * gm[pr(r)] * qs[r * kLS + j] + acc[x] : 0.f;
-      part[x >> 1] += o * dos[r * kLS + j];
-    }
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      float s = part[hf];
-      s += __shfl_xor_sync(0xffffffffu, s, 1);
-      s += __shfl_xor_sync(0xffffffffu, s, 2);
-      const int r = m0 + g + 8 * hf;
-      if (t == 0 && r < nq) atomicAdd(p.rho + (tq0 + r) * H + h, s);
-    }
+
+  // ---- masks and decays of the Gram sums: M1 (times beta_r), beta M2 (upper) + M3 (lower), M4 ----
+  for (int i = tid; i < kChunk * QP; i += kChunkThreads) {
+    const int r = i / QP, qi = i % QP;
+    const bool ok = qi < nq && r <= pr(qi);
+    g1[r * LDQ + qi] = ok ? bt[r] * scale * expf(G[pr(qi)] - G[r]) * g1[r * LDQ + qi] : 0.f;
+  }
+  for (int i = tid; i < kChunk * kChunk; i += kChunkThreads) {
+    const int r = i >> 6, j = i & 63;
+    const float x = g23[r * kLC + j];
+    g23[r * kLC + j] = (j > r) ? bt[r] * expf(G[j] - G[r]) * x : (j < r) ? expf(G[r] - G[j]) * x : 0.f;
+  }
+  for (int i = tid; i < QP * kChunk; i += kChunkThreads) {
+    const int qi = i >> 6, j = i & 63;
+    const bool ok = qi < nq && j <= pr(qi);
+    g4[qi * kLC + j] = ok ? scale * expf(G[pr(qi)] - G[j]) * g4[qi * kLC + j] : 0.f;
   }
   __syncthreads();
-  // ---- M1 [64 x qp], M2 [64 x 64] (into L), M3 [64 x 64], M4 [qp x 64] (into P) ----
+  // dkhat += (beta M1) qhat - (beta M2 + M3) khat;  dqhat += scale M4 khat
+  tiles_mma<NTK, false, false, false>(dk_acc, g1 + 16 * mk * LDQ, LDQ, qh + 8 * nk0, LDD, QP / 8, nullptr, nullptr, g,
+                                      t);
   {
-    const int n1 = 4 * (QP / 8), n2 = 32, n3 = 32, n4 = (QP / 16) * 8;
-    for (int u = warp; u < n1 + n2 + n3 + n4; u += 8) {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      if (u < n1) {  // e dO^T
-        const int m0 = 16 * (u / (QP / 8)), c0 = 8 * (u % (QP / 8));
-        mma_tile(acc, kVS / 8, g, t, [&](int r, int k) { return et[(m0 + r) * kLS + k]; },
-                 [&](int k, int n) { return dos[(c0 + n) * kLS + k]; });
+    float neg[NTK][4] = {};
+    tiles_mma<NTK, false, false, false>(neg, g23 + 16 * mk * kLC, kLC, kh + 8 * nk0, LDD, kChunk / 8, nullptr, nullptr,
+                                        g, t);
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const int r = m0 + g + 8 * (x >> 1), qi = c0 + 2 * t + (x & 1);
-          const int pp = pr(qi);
-          m1[r * LM1 + qi] = (qi < nq && r <= pp) ? scale * expf(G[pp] - G[r]) * acc[x] : 0.f;
-        }
-      } else if (u < n1 + n2) {  // e dv^T
-        const int uu = u - n1, m0 = 16 * (uu >> 3), c0 = 8 * (uu & 7);
-        mma_tile(acc, kVS / 8, g, t, [&](int r, int k) { return et[(m0 + r) * kLS + k]; },
-                 [&](int k, int n) { return bt[c0 + n] * dl[(c0 + n) * kLS + k]; });
+    for (int i = 0; i < NTK; ++i)
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const int r = m0 + g + 8 * (x >> 1), j = c0 + 2 * t + (x & 1);
-          lm[r * kLC + j] = (j > r) ? expf(G[j] - G[r]) * acc[x] : 0.f;
-        }
-      } else if (u < n1 + n2 + n3) {  // dv vt^T
-        const int uu = u - n1 - n2, m0 = 16 * (uu >> 3), c0 = 8 * (uu & 7);
-        mma_tile(acc, kVS / 8, g, t, [&](int r, int k) { return bt[m0 + r] * dl[(m0 + r) * kLS + k]; },
-                 [&](int k, int n) { return vt[(c0 + n) * kLS + k]; });
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const int r = m0 + g + 8 * (x >> 1), j = c0 + 2 * t + (x & 1);
-          m3[r * kLC + j] = (j < r) ? expf(G[r] - G[j]) * acc[x] : 0.f;
-        }
-      } else {  // dO vt^T
-        const int uu = u - n1 - n2 - n3, m0 = 16 * (uu >> 3), c0 = 8 * (uu & 7);
-        mma_tile(acc, kVS / 8, g, t, [&](int r, int k) { return dos[(m0 + r) * kLS + k]; },
-                 [&](int k, int n) { return vt[(c0 + n) * kLS + k]; });
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const int qi = m0 + g + 8 * (x >> 1), j = c0 + 2 * t + (x & 1);
-          const int pp = pr(qi);
-          pm[qi * kLC + j] = (qi < nq && j <= pp) ? expf(G[pp] - G[j]) * acc[x] : 0.f;
-        }
-      }
-    }
+      for (int x = 0; x < 4; ++x) dk_acc[i][x] -= neg[i][x];
   }
+#pragma unroll
+  for (int i = 0; i < NTQ; ++i)
+    if (int m0, n0; dq_tile(i, m0, n0)) {
+      tile_mma<false, false, false>(dq_acc[i], g4 + m0 * kLC, kLC, kh + n0, LDD, kChunk / 8, nullptr, nullptr, g, t);
+    }
+  __syncthreads();  // L and T are free: they stage dkhat; the Gram sums stage dqhat
+  float *stk = lm;   // [64][LDD] over L and T (2 x 64 x 72 >= 64 x (D + 8) floats)
+  float *stq = g23;  // [qp][LDD] over G23 and G4 when they suffice, else over P .. G4
+#pragma unroll
+  for (int i = 0; i < NTK; ++i)
+#pragma unroll
+    for (int x = 0; x < 4; ++x) stk[(16 * mk + trow(x, g)) * LDD + 8 * (nk0 + i) + tcol(x, t)] = dk_acc[i][x];
+  const bool q_in_g = (uint32_t)QP * LDD * 4u <= lay.ss - lay.g23;
+  if (!q_in_g) stq = pm;
+#pragma unroll
+  for (int i = 0; i < NTQ; ++i)
+    if (int m0, n0; dq_tile(i, m0, n0)) {
+#pragma unroll
+      for (int x = 0; x < 4; ++x) stq[(m0 + trow(x, g)) * LDD + n0 + tcol(x, t)] = dq_acc[i][x];
+    }
   __syncthreads();
-  // ---- the slice's shares of dkhat [64 x D] and dqhat [qp x D] ----
-  for (int u = warp; u < 4 * (D / 8) + (QP / 16) * (D / 8); u += 8) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (u < 4 * (D / 8)) {
-      const int m0 = 16 * (u / (D / 8)), f0 = 8 * (u % (D / 8));
-      // (beta gamma_C / gamma) e D_C
-      mma_tile(acc, kVS / 8, g, t,
-               [&](int r, int k) { return bt[m0 + r] * expf(GC - G[m0 + r]) * et[(m0 + r) * kLS + k]; },
-               [&](int k, int n) { return dcs[k * LD + f0 + n]; });
-      // - gamma dv S
-      mma_tile(acc, kVS / 8, g, t,
-               [&](int r, int k) { return -gm[m0 + r] * bt[m0 + r] * dl[(m0 + r) * kLS + k]; },
-               [&](int k, int n) { return ss[k * LD + f0 + n]; });
-      // beta M1 qhat
-      mma_tile(acc, QP / 8, g, t, [&](int r, int k) { return bt[m0 + r] * m1[(m0 + r) * LM1 + k]; },
-               [&](int k, int n) { return qh[k * LD + f0 + n]; });
-      // - (beta M2 + M3) khat
-      mma_tile(acc, kChunk / 8, g, t,
-               [&](int r, int k) { return -(bt[m0 + r] * lm[(m0 + r) * kLC + k] + m3[(m0 + r) * kLC + k]); },
-               [&](int k, int n) { return kh[k * LD + f0 + n]; });
+  // ---- L2-norm chain rule (dx = rx (dxhat - (xhat . dxhat) xhat)), stores, row sums ----
+  for (int r = warp; r < len + nq; r += kChunkThreads / 32) {
+    const bool isk = r < len;
+    const int rr = isk ? r : r - len;
+    const float *dh = (isk ? stk : stq) + rr * LDD, *xh = (isk ? kh : qh) + rr * LDD;
+    constexpr int PER = D / 32;
+    float a[PER], xv[PER], dot = 0.f;
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int r = m0 + g + 8 * hf;
-        if (r < len)
-          atomicAdd(reinterpret_cast<float2 *>(p.dkh + ((R0 + r) * H + h) * (int64_t)D + f0 + 2 * t),
-                    make_float2(acc[2 * hf], acc[2 * hf + 1]));
-      }
+    for (int i = 0; i < PER; ++i) {
+      a[i] = dh[lane + 32 * i];
+      xv[i] = xh[lane + 32 * i];
+      dot += a[i] * xv[i];
+    }
+    float *out = isk ? p.dk + ((R0 + rr) * H + h) * (int64_t)D : p.dq + ((tq0 + rr) * H + h) * (int64_t)D;
+    if (p.l2norm) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+      const float rx = (isk ? rk : rq)[rr];
+#pragma unroll
+      for (int i = 0; i < PER; ++i) out[lane + 32 * i] = rx * (a[i] - dot * xv[i]);
     } else {
-      const int uu = u - 4 * (D / 8), m0 = 16 * (uu / (D / 8)), f0 = 8 * (uu % (D / 8));
-      // scale gamma_p dO S
-      mma_tile(acc, kVS / 8, g, t,
-               [&](int r, int k) {
-                 const int qi = m0 + r;
-                 return qi < nq ? scale * gm[pr(qi)] * dos[qi * kLS + k] : 0.f;
-               },
-               [&](int k, int n) { return ss[k * LD + f0 + n]; });
-      // scale M4 khat
-      mma_tile(acc, kChunk / 8, g, t, [&](int r, int k) { return scale * pm[(m0 + r) * kLC + k]; },
-               [&](int k, int n) { return kh[k * LD + f0 + n]; });
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int qi = m0 + g + 8 * hf;
-        if (qi < nq)
-          atomicAdd(reinterpret_cast<float2 *>(p.dqh + ((tq0 + qi) * H + h) * (int64_t)D + f0 + 2 * t),
-                    make_float2(acc[2 * hf], acc[2 * hf + 1]));
-      }
+      for (int i = 0; i < PER; ++i) out[lane + 32 * i] = a[i];
     }
   }
+  if (tid < len) {
+    if (p.dbeta) p.dbeta[(R0 + tid) * H + h] = sdb[tid];
+    p.sig[(R0 + tid) * H + h] = ssg[tid];
+  }
+  if (tid < nq) p.rho[(tq0 + tid) * H + h] = srho[tid];
 }
 
 // ---------------------------------------------------------------------------------------
 // Finishing passes.
 // ---------------------------------------------------------------------------------------
-// One warp per (row, head): dx = dxhat / n - x (x . dxhat) / n^3 with n = sqrt(|x|^2 + eps)
-// (or dx = dxhat without the L2 norm).  blockIdx.y: 0 = k rows (T*M), 1 = q rows (T).
-template <int D>
-__global__ void __launch_bounds__(256) gdp_bwd_rows_kernel(BwdProblem p) {
-  const int which = blockIdx.y;
-  const int64_t rows = (which == 0 ? p.T * p.M : p.T) * p.H;
-  const int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (w >= rows) return;
-  const int64_t r = w / p.H;
-  const int h = (int)(w % p.H);
-  const float *acc = (which == 0 ? p.dkh : p.dqh) + w * D;
-  float *out = (which == 0 ? p.dk : p.dq) + w * D;
-  const __nv_bfloat16 *x = which == 0 ? p.k + r * p.k_st + (int64_t)h * p.k_sh : p.q + r * p.q_st + (int64_t)h * p.q_sh;
-  constexpr int PER = D / 32;
-  float a[PER], xv[PER], ss = 0.f, dot = 0.f;
-#pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    a[i] = acc[lane * PER + i];
-    xv[i] = bf(x + lane * PER + i);
-    ss += xv[i] * xv[i];
-    dot += xv[i] * a[i];
-  }
-  if (p.l2norm) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      dot += __shfl_xor_sync(0xffffffffu, dot, o);
-    }
-    const float inv = rsqrtf(ss + kL2Eps), inv3 = inv * inv * inv;
-#pragma unroll
-    for (int i = 0; i < PER; ++i) out[lane * PER + i] = a[i] * inv - xv[i] * dot * inv3;
-  } else {
-#pragma unroll
-    for (int i = 0; i < PER; ++i) out[lane * PER + i] = a[i];
-  }
-}
-
 // One CTA per (sequence, head): dg_t = <dS_T, S_T> + sum_{t' >= t} (rho_t' - sum_j sig_{t'M+j}).
 __global__ void __launch_bounds__(256) gdp_bwd_dg_kernel(BwdProblem p) {
   const int seq = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
@@ -769,59 +936,56 @@ __global__ void __launch_bounds__(256) gdp_bwd_dg_kernel(BwdProblem p) {
   }
 }
 
+// Slice width of the per-chunk kernel: 16 V columns when the shared memory allows, else 8.
+int chunk_slice(int d, int qpad) { return ChunkSmem(d, qpad, 16).total <= 227u * 1024u ? 16 : 8; }
+
+template <int D, int QP>
+cudaError_t launch_bscan(const BwdProblem &p, cudaStream_t stream) {
+  const size_t smem = bwd_scan_smem(D, QP);
+  cudaError_t e = cudaFuncSetAttribute(gdp_bwd_scan_kernel<D, QP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  gdp_bwd_scan_kernel<D, QP><<<dim3((unsigned)p.N, (unsigned)p.H), 4 * D, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D, int VSL>
+cudaError_t launch_chunk(const BwdProblem &p, cudaStream_t stream) {
+  const size_t smem = ChunkSmem(D, p.qpad, VSL).total;
+  cudaError_t e = cudaFuncSetAttribute(gdp_bwd_chunk_kernel<D, VSL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  gdp_bwd_chunk_kernel<D, VSL><<<dim3((unsigned)p.ntdp_pad, (unsigned)p.H), kChunkThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_backward(const BwdProblem &p, cudaStream_t stream) {
   cudaError_t e;
   const int D = p.D, QP = p.qpad;
   if (p.N > 0) {
-    const size_t smem = bwd_scan_smem(D, QP);
-    dim3 grid((unsigned)p.N, (unsigned)p.H);
-    if (D == 128) {
-      if ((e = cudaFuncSetAttribute(gdp_bwd_scan_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)smem)) != cudaSuccess)
-        return e;
-      gdp_bwd_scan_kernel<128><<<grid, 256, smem, stream>>>(p);
-    } else {
-      if ((e = cudaFuncSetAttribute(gdp_bwd_scan_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)smem)) != cudaSuccess)
-        return e;
-      gdp_bwd_scan_kernel<64><<<grid, 128, smem, stream>>>(p);
-    }
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (D == 128)
+      e = QP == 16 ? launch_bscan<128, 16>(p, stream) : QP == 32 ? launch_bscan<128, 32>(p, stream)
+                                                    : launch_bscan<128, 64>(p, stream);
+    else
+      e = QP == 16 ? launch_bscan<64, 16>(p, stream) : QP == 32 ? launch_bscan<64, 32>(p, stream)
+                                                   : launch_bscan<64, 64>(p, stream);
+    if (e != cudaSuccess) return e;
   }
   if (p.ntdp_pad > 0) {
-    const size_t smem = ChunkSmem(D, QP).total;
-    dim3 grid((unsigned)p.ntdp_pad, (unsigned)p.H, (unsigned)(D / kVS));
-    if (D == 128) {
-      if ((e = cudaFuncSetAttribute(gdp_bwd_chunk_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)smem)) != cudaSuccess)
-        return e;
-      gdp_bwd_chunk_kernel<128><<<grid, 256, smem, stream>>>(p);
-    } else {
-      if ((e = cudaFuncSetAttribute(gdp_bwd_chunk_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)smem)) != cudaSuccess)
-        return e;
-      gdp_bwd_chunk_kernel<64><<<grid, 256, smem, stream>>>(p);
-    }
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  if (p.T > 0) {
-    const int64_t rows = p.T * p.M * p.H;
-    dim3 grid((unsigned)((rows + 7) / 8), 2);
+    const int vsl = chunk_slice(D, QP);
     if (D == 128)
-      gdp_bwd_rows_kernel<128><<<grid, 256, 0, stream>>>(p);
+      e = vsl == 16 ? launch_chunk<128, 16>(p, stream) : launch_chunk<128, 8>(p, stream);
     else
-      gdp_bwd_rows_kernel<64><<<grid, 256, 0, stream>>>(p);
+      e = vsl == 16 ? launch_chunk<64, 16>(p, stream) : launch_chunk<64, 8>(p, stream);
+    if (e != cudaSuccess) return e;
+  }
+  if (p.T > 0 && p.dg) {
+    gdp_bwd_dg_kernel<<<dim3((unsigned)p.N, (unsigned)p.H), 256, 0, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if (p.dg) {
-      gdp_bwd_dg_kernel<<<dim3((unsigned)p.N, (unsigned)p.H), 256, 0, stream>>>(p);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
   }
   return cudaSuccess;
 }
-
-size_t backward_chunk_smem(int d, int qpad) { return ChunkSmem(d, qpad).total; }
 
 }  // namespace gdp

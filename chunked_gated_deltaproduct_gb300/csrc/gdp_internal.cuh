@@ -158,13 +158,11 @@ struct BwdProblem {
   const float *fin;          // [N][H][V][K] recomputed final state (when dfin)
   float *dinit;              // [N][H][V][K] dL/dS_initial or NULL
   float *tot;                // [N][H] <dS_final, S_final>
-  float *dkh, *dqh;          // [T*M][H][K], [T][H][K] gradients of the normalised rows (summed)
-  float *sig, *rho;          // [T*M][H] sum_v dv v, [T][H] do . o (summed)
+  float *sig, *rho;          // [T*M][H] sum_v dv v, [T][H] do . o
   float *dq, *dk, *dv, *dg, *dbeta;
   uint32_t *status;
 };
 cudaError_t launch_backward(const BwdProblem &p, cudaStream_t stream);
-size_t backward_chunk_smem(int d, int qpad);
 
 // Launch `kern` on `stream`, with programmatic stream serialization when `pdl`.
 template <typename... Params, typename... Args>

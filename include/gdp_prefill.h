@@ -306,8 +306,8 @@ gdp_status gdp_decode_step(const gdp_prefill_args *args, void *stream);
  *                  contents undefined on entry and exit.
  *   device_status  optional, as for the prefill.
  * Every buffer is a device pointer, 16-byte aligned.  Nothing is allocated and
- * nothing synchronises.  dq, dk and dbeta are sums of per-slice shares added with
- * atomics, so their last bits may differ from call to call.
+ * nothing synchronises; a call can be captured in a CUDA graph.  Results do not
+ * depend on scheduling: every sum runs in a fixed order.
  */
 typedef struct gdp_backward_args {
   const gdp_prefill_args *fwd; /* host pointer, read during the call only */
