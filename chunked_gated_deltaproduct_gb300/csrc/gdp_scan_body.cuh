@@ -181,8 +181,8 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
   // token-chunk starts whose state is requested (a prefix of the chunks e % M == 0; every
   // chunk when cs_div is 1, the backward pass's recompute)
   const int csd = p.cs_div;
-  auto emits = [&](int64_t e) {
-    const int64_t eg = e0 + e;
+  auto emits = [&](int64_t e) {  // chunk indices fit 32 bits (the host checks T * M)
+    const int eg = (int)(e0 + e);
     return p.chunk_states && (eg % csd == 0) && co_i >= 0 && co_i + eg / csd < p.nt_pad;
   };
 
@@ -315,7 +315,7 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
         for (int c0 = 0; c0 < QP; c0 += 16) tmem_st16(to + lrow + c0, z);
       }
       if (tid == 0) info[b] = ChunkInfo{gam_next, mt.nq, mt.p0};
-      if ((renorm || emit || !fast) && e >= 1) {  // S_hat of chunk e is final
+      if (renorm && e >= 1) {  // the renormalisation rewrites the final S_hat of chunk e
         if (!mbar_wait_or_abort(&b2_done[(e - 1) & 1], (uint32_t)(((e - 1) >> 1) & 1), &abort_flag)) break;
         tc_fence_after();
       }
@@ -340,7 +340,12 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
         // between the two batches: snapshot S_e = gam_pass S_hat (read alongside batch 1) and,
         // for a slow image, S_hat <- gamma_last S_hat once batch 1 has read it
         if (emit && n_emit >= 1 && !mbar_wait_or_abort(&bk_free, (uint32_t)((n_emit - 1) & 1), &abort_flag)) break;
-        if (!fast && !mbar_wait_or_abort(&b1_done[b], (uint32_t)((e >> 1) & 1), &abort_flag)) break;
+        if (!fast) {  // batch 1 has read S_hat (so chunk e - 1's batch 2 is complete too)
+          if (!mbar_wait_or_abort(&b1_done[b], (uint32_t)((e >> 1) & 1), &abort_flag)) break;
+        } else if (!renorm && e >= 1) {  // S_hat of chunk e is final; waited for only now, so that
+          // batch 1 (issued on yo_ready above) is not held back by this round trip
+          if (!mbar_wait_or_abort(&b2_done[(e - 1) & 1], (uint32_t)(((e - 1) >> 1) & 1), &abort_flag)) break;
+        }
         tc_fence_after();
         // (a slow chunk was renormalised, so gam_pass is 1 there and one array serves both)
         for (int c0 = 0; c0 < d; c0 += 32) {
