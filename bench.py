@@ -11,7 +11,9 @@ resident in HBM.  Between timed steps a 256 MiB buffer is written to flush the
 by CUDA events on the launching stream (its kernels overlap their launches);
 a second pass of the same steps through gdp_prefill_varlen_profiled, whose
 events sit between the kernels (so each kernel runs alone), gives the
-per-kernel durations of the roofline.  Under torchrun every rank
+per-kernel durations of the roofline.  Two more legs are reported beside the headline: the
+decode step (key decode_step) and the backward pass of the same workload (key backward: device
+time per gdp_prefill_varlen_backward call, which includes its forward recompute).  Under torchrun every rank
 runs its own independent batch of the same shape (weak scaling, no
 collective); rank 0 prints one JSON line.
 """
@@ -40,7 +42,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM traffic of the dominant kernel per launch, from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the sha256 of the
 # kernel's sources (KERNEL_SOURCES) it was taken on; reported as null once they change.
-NCU_TRAFFIC = {"gdp_scan_kernel": {"sha": "1e3f3a2aa11249c9", "bytes_per_launch": 49039616, "workload": 2}}
+NCU_TRAFFIC = {"gdp_scan_kernel": {"sha": "13e68d499a1788d5", "bytes_per_launch": 49113088, "workload": 2}}
 
 
 def alg_bytes(w) -> int:

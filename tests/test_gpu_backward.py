@@ -154,3 +154,13 @@ def test_backward_repeatable_and_graph_capturable(cuda_device):
     torch.cuda.synchronize()
     for n in ("dq", "dk", "dv", "dg", "dbeta", "d_initial_state"):
         assert torch.allclose(out[n], a[n], rtol=1e-4, atol=1e-5), n
+
+
+def test_backward_workload2_full_size(cuda_device):
+    """The bench's backward workload at full size (workload 2: N=4, L={100,257,64,1000}, H=8,
+    d=128, M=2, initial state), every head, with the bench's upstream gradients."""
+    from gdp_workloads import make_workload
+
+    w = make_workload(2)
+    d_out, d_fin = make_cotangents(w, seed=1, dfin_sigma=0.5)
+    _compare(w, cuda_device, d_out, d_fin)
