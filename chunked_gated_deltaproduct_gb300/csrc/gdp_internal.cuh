@@ -128,6 +128,9 @@ struct Problem {
   // launch the WY and scan kernels with programmatic stream serialization: each may start while
   // its predecessor finishes and waits (griddepcontrol.wait) before reading that one's outputs
   int pdl;
+  // scan: the two output tensor maps (boxes of 64 / M and ceil(64 / M) token rows) are encoded:
+  // a chunk with that many readout rows leaves through one TMA store
+  int out_tma;
   // chunk_states row spacing: the scan emits the state entering expanded chunk e when
   // e % cs_div == 0, at row co[seq] + e / cs_div (M: token-chunk starts; 1: every expanded
   // chunk, with co = the expanded-chunk offsets, for the backward pass).  A NULL `out` skips
@@ -242,6 +245,9 @@ cudaError_t launch_scan_variant(const Problem &p, cudaStream_t stream, bool f16,
 cudaError_t tmap_state(void *map, float *base, int64_t rows, int d);
 cudaError_t tmap_rows_16(void *map, const void *base, int64_t rows, int H, int K, int64_t stride_t, int64_t stride_h,
                          int box_rows, int f16);
+//   tmap_out_rows:  the output [T][H][V] (bf16 or float16), unswizzled boxes of V features x
+//                   1 head x box_rows tokens
+cudaError_t tmap_out_rows(void *map, void *base, int64_t T, int H, int V, int box_rows, int f16);
 
 // Sets the calling thread's gdp_last_error() text (defined in gdp_api.cu).
 void set_last_error(const char *fmt, ...);

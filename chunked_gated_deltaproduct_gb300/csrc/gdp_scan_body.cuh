@@ -70,32 +70,46 @@ __host__ inline size_t scan_smem_bytes(int d, int qpad, int V) {
 }
 
 // Store warp: the state rows held in this warp's TMEM lanes (columns from t_lane), times
-// mul, to map rows [row, row + 32): per 32 columns, one 32 x 32 box staged in shared memory
-// (row r at r * 128 bytes, 16-byte chunk j at position j ^ (r & 7): the map's 128-byte
-// swizzle, conflict-free for a thread per row) and written by one TMA tensor store.  The
-// warp's two tiles alternate; nblk counts the boxes this warp has issued.
+// mul, to map rows [row, row + 32).  The columns are read from TMEM 64 at a time under one
+// wait; `read` (when given) is arrived on once the last of them is in registers, since the
+// columns may be overwritten from there on.  Per 32 columns the rows leave as one 32 x 32 box
+// staged in shared memory (row r at r * 128 bytes, 16-byte chunk j at position j ^ (r & 7):
+// the map's 128-byte swizzle, conflict-free for a thread per row) and written by one TMA
+// tensor store.  The warp's two tiles alternate; nblk counts the boxes this warp has issued.
 __device__ __forceinline__ void store_state_tma(uint32_t t_lane, unsigned char *tiles, int lane, int d, float mul,
-                                                const CUtensorMap *tm, int row, int &nblk) {
+                                                const CUtensorMap *tm, int row, int &nblk, uint64_t *read) {
 #pragma unroll 1
-  for (int c0 = 0; c0 < d; c0 += 32) {
-    float x[32];
-    tmem_ld32(t_lane + c0, x);
-    unsigned char *tile = tiles + (uint32_t)(nblk & 1) * kStTile;
-    if (nblk >= 2) {  // the store issued from this tile two boxes ago has read it
-      if (lane == 0) bulk_wait_read<1>();
-      __syncwarp();
+  for (int c0 = 0; c0 < d; c0 += 64) {
+    uint32_t x[64];
+    tmem_ld32x_nw(t_lane + c0, x);
+    tmem_ld32x_nw(t_lane + c0 + 32, x + 32);
+    tmem_ld_wait();
+    if (read && c0 + 64 >= d) {
+      tc_fence_before();
+      mbar_arrive(read);
     }
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      *reinterpret_cast<float4 *>(tile + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-          make_float4(mul * x[4 * j], mul * x[4 * j + 1], mul * x[4 * j + 2], mul * x[4 * j + 3]);
-    fence_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      tma_store_2d(tm, tile, c0, row);
-      bulk_commit();
+    for (int c = 0; c < 2; ++c) {
+      unsigned char *tile = tiles + (uint32_t)(nblk & 1) * kStTile;
+      if (nblk >= 2) {  // the store issued from this tile two boxes ago has read it
+        if (lane == 0) bulk_wait_read<1>();
+        __syncwarp();
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t *y = x + 32 * c + 4 * j;
+        *reinterpret_cast<float4 *>(tile + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+            make_float4(mul * __uint_as_float(y[0]), mul * __uint_as_float(y[1]), mul * __uint_as_float(y[2]),
+                        mul * __uint_as_float(y[3]));
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(tm, tile, c0 + 32 * c, row);
+        bulk_commit();
+      }
+      ++nblk;
     }
-    ++nblk;
   }
 }
 
@@ -111,7 +125,8 @@ struct ChunkInfo {
 // came out larger than the same body in a plain one).
 template <bool F16, bool INIT16>
 __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &tm_cs, const CUtensorMap &tm_fin,
-                                          const CUtensorMap &tm_seg) {
+                                          const CUtensorMap &tm_seg, const CUtensorMap &tm_out_a,
+                                          const CUtensorMap &tm_out_b) {
   const int seq = blockIdx.x, h = blockIdx.y;
   int64_t bos, L;
   if (!seq_bounds(p.cu, p.cu64, p.T, seq, &bos, &L)) return;  // flagged by the descriptor kernel
@@ -379,45 +394,59 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
       // the four store warps take the same exit decision (they meet at named barriers)
       const bool ok = mbar_wait_or_abort(&b2_done[b], (uint32_t)((e >> 1) & 1), &abort_flag);
       if (lane == 0) st_ok[q4] = ok ? 1 : 0;
+      if (tid == 128) bulk_wait_read<0>();  // the output staging's TMA store (if any) has read it
       named_sync(1, 128);  // also: every thread has finished reading the previous chunk's staging
       if (!(st_ok[0] & st_ok[1] & st_ok[2] & st_ok[3])) break;
       tc_fence_after();
       const ChunkInfo ci = info[b];
       gam_fin = ci.out_scale;
-      // outputs: 16-bit staging [q][v] (16 readout rows at a time), then full-row 16-byte stores
+      // outputs: the chunk's o_hat columns (read under one wait), 16-bit staging [q][v]
 #pragma unroll 1
-      for (int c0 = 0; c0 < ci.nq; c0 += 16) {
-        float x[16];
-        tmem_ld16(tO(b) + lrow + c0, x);
+      for (int q0 = 0; q0 < ci.nq; q0 += 32) {  // 32 readout rows per wait
+        uint32_t xo[32];
+        tmem_ld16_nw(tO(b) + lrow + q0, xo);
+        if (q0 + 16 < ci.nq) tmem_ld16_nw(tO(b) + lrow + q0 + 16, xo + 16);
+        tmem_ld_wait();
         if (v < V) {
 #pragma unroll
-          for (int w = 0; w < 16; ++w)
-            if (c0 + w < ci.nq) {
+          for (int w = 0; w < 32; ++w)
+            if (q0 + w < ci.nq) {
+              const float o = __uint_as_float(xo[w]) * ci.out_scale;
               if constexpr (F16)
-                *reinterpret_cast<__half *>(obuf + ((uint32_t)(c0 + w) * V + v) * 2u) =
-                    __float2half_rn(x[w] * ci.out_scale);
+                *reinterpret_cast<__half *>(obuf + ((uint32_t)(q0 + w) * V + v) * 2u) = __float2half_rn(o);
               else
-                *reinterpret_cast<__nv_bfloat16 *>(obuf + ((uint32_t)(c0 + w) * V + v) * 2u) =
-                    __float2bfloat16_rn(x[w] * ci.out_scale);
+                *reinterpret_cast<__nv_bfloat16 *>(obuf + ((uint32_t)(q0 + w) * V + v) * 2u) =
+                    __float2bfloat16_rn(o);
             }
         }
       }
+      fence_async_smem();  // the staging may leave by a TMA store
       tc_fence_before();
       mbar_arrive(&yo_free[b]);  // the chunk's o_hat columns have been read
       named_sync(1, 128);
       const int64_t tq0 = (bos * M + (e0 + e) * kChunk + ci.p0) / M;  // readout rows are consecutive tokens
-      const int cpr = V / 8;                                     // 16-byte chunks per output row
-      for (int c = tid - 128; p.out && c < ci.nq * cpr; c += 128) {
-        const int qi = c / cpr, ch = c % cpr;
-        *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + ((tq0 + qi) * H + h) * (int64_t)V + ch * 8) =
-            *reinterpret_cast<const uint4 *>(obuf + ((uint32_t)qi * V + ch * 8) * 2u);
+      if (p.out && p.out_tma && (ci.nq == kChunk / M || ci.nq == (kChunk + M - 1) / M)) {
+        // one box of exactly nq token rows (x = 0, head h, token tq0)
+        if (tid == 128) {
+          tma_store_3d(ci.nq == kChunk / M ? &tm_out_a : &tm_out_b, obuf, 0, h, (int)tq0);
+          bulk_commit();
+        }
+      } else {
+        const int cpr = V / 8;  // 16-byte chunks per output row
+        for (int c = tid - 128; p.out && c < ci.nq * cpr; c += 128) {
+          const int qi = c / cpr, ch = c % cpr;
+          *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + ((tq0 + qi) * H + h) * (int64_t)V + ch * 8) =
+              *reinterpret_cast<const uint4 *>(obuf + ((uint32_t)qi * V + ch * 8) * 2u);
+        }
       }
       if (emits(e)) {  // the prep warps copied S_e before batch 2 of this chunk was issued
-        if (has_rows)
+        if (has_rows) {  // bk_free: the snapshot columns have been read
           store_state_tma(tBk + lrow, sttiles, lane, d, 1.f, &tm_cs,
-                          (int)(((co_i + (e0 + e) / csd) * H + h) * V + q4 * 32), nblk);
-        tc_fence_before();
-        mbar_arrive(&bk_free);  // the snapshot columns have been read
+                          (int)(((co_i + (e0 + e) / csd) * H + h) * V + q4 * 32), nblk, &bk_free);
+        } else {
+          tc_fence_before();
+          mbar_arrive(&bk_free);
+        }
       }
     }
     if (!abort_flag && has_rows) {  // the last chunk's b2_done was waited for above
@@ -431,7 +460,7 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
       } else if (p.out_state) {
         r = ((int64_t)seq * H + h) * V;
       }
-      if (r >= 0) store_state_tma(tS + lrow, sttiles, lane, d, gam_fin, tm, (int)(r + q4 * 32), nblk);
+      if (r >= 0) store_state_tma(tS + lrow, sttiles, lane, d, gam_fin, tm, (int)(r + q4 * 32), nblk, nullptr);
     }
     if (lane == 0) bulk_wait_all();  // this warp's tensor stores are complete
   } else if (warp == 8) {
@@ -524,9 +553,16 @@ cudaError_t launch_scan_kernel(Kern kern, const Problem &p, cudaStream_t stream)
     e = tmap_state(&tm_fin, p.out_state, p.N * hv, p.K);
   if (e != cudaSuccess) return e;
   if ((e = tmap_state(&tm_seg, p.seg_state, p.N * hv, p.K)) != cudaSuccess) return e;
+  // output boxes of 64 / M and ceil(64 / M) token rows: the readout counts of a full chunk
+  alignas(64) CUtensorMap tm_out_a, tm_out_b;
+  Problem q = p;
+  const int na = kChunk / p.M, nb = (kChunk + p.M - 1) / p.M;
+  q.out_tma = (p.out && p.T >= nb) ? 1 : 0;
+  if ((e = tmap_out_rows(&tm_out_a, q.out_tma ? p.out : nullptr, p.T, p.H, p.V, na, p.f16)) != cudaSuccess) return e;
+  if ((e = tmap_out_rows(&tm_out_b, q.out_tma ? p.out : nullptr, p.T, p.H, p.V, nb, p.f16)) != cudaSuccess) return e;
   dim3 grid((unsigned)p.N, (unsigned)p.H);
-  if ((e = launch_kernel(kern, grid, dim3(kScanThreads), smem, stream, p.pdl != 0, p, tm_cs, tm_fin, tm_seg)) !=
-      cudaSuccess)
+  if ((e = launch_kernel(kern, grid, dim3(kScanThreads), smem, stream, p.pdl != 0, q, tm_cs, tm_fin, tm_seg, tm_out_a,
+                         tm_out_b)) != cudaSuccess)
     return e;
   return cudaGetLastError();
 }
@@ -534,8 +570,9 @@ cudaError_t launch_scan_kernel(Kern kern, const Problem &p, cudaStream_t stream)
 #define GDP_SCAN_KERNEL(name, f16, init16)                                                                       \
   __global__ void __launch_bounds__(kScanThreads, 1)                                                            \
       name(Problem p, const __grid_constant__ CUtensorMap tm_cs, const __grid_constant__ CUtensorMap tm_fin,     \
-           const __grid_constant__ CUtensorMap tm_seg) {                                                          \
-    scan_body<f16, init16>(p, tm_cs, tm_fin, tm_seg);                                                           \
+           const __grid_constant__ CUtensorMap tm_seg, const __grid_constant__ CUtensorMap tm_out_a,              \
+           const __grid_constant__ CUtensorMap tm_out_b) {                                                        \
+    scan_body<f16, init16>(p, tm_cs, tm_fin, tm_seg, tm_out_a, tm_out_b);                                       \
   }
 
 }  // namespace

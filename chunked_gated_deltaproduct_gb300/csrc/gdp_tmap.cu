@@ -27,12 +27,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 }
 
 cudaError_t encode(CUtensorMap *m, CUtensorMapDataType type, cuuint32_t rank, void *base, const cuuint64_t *dims,
-                   const cuuint64_t *strides, const cuuint32_t *box) {
+                   const cuuint64_t *strides, const cuuint32_t *box,
+                   CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
   if (!enc) return cudaErrorNotSupported;
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = enc(m, type, rank, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = enc(m, type, rank, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -57,6 +58,17 @@ cudaError_t tmap_rows_16(void *map, const void *base, int64_t rows, int H, int K
   return encode(static_cast<CUtensorMap *>(map),
                 f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base),
                 dims, strides, box);
+}
+
+cudaError_t tmap_out_rows(void *map, void *base, int64_t T, int H, int V, int box_rows, int f16) {
+  memset(map, 0, sizeof(CUtensorMap));
+  if (!base || T <= 0) return cudaSuccess;
+  const cuuint64_t dims[3] = {(cuuint64_t)V, (cuuint64_t)H, (cuuint64_t)T};
+  const cuuint64_t strides[2] = {(cuuint64_t)V * 2u, (cuuint64_t)H * V * 2u};
+  const cuuint32_t box[3] = {(cuuint32_t)V, 1, (cuuint32_t)box_rows};
+  return encode(static_cast<CUtensorMap *>(map),
+                f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 }  // namespace gdp
