@@ -274,6 +274,21 @@ def measure_decode(pkg, dev, flush, stream, steps=50, warmup=5):
             "peak_gbs": peak, "frac": gbs / peak, "peak_source": src, "steps": steps, "l2_flush": True}
 
 
+def rank_seed(workload: int, rank: int):
+    """Input seed of a rank: rank 0 draws the workload's own inputs, every other rank an
+    independent batch of the same shape (replicas, weak scaling)."""
+    return 1000 + workload + 7919 * rank if rank else None
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest value of x over the ranks of the process group (x itself without one)."""
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def backward_alg_bytes(w, with_dfin: bool) -> int:
     """Algorithmic bytes of one backward call: q, k, v, d_output (bf16), g, beta (fp32) and the
     initial state / final-state gradient (fp32) read once; dq, dk, dv, dg, dbeta and the
@@ -356,8 +371,7 @@ def main():
         dist = dist_mod
         dist.init_process_group("nccl" if args.impl == "gdp" else "gloo")
 
-    seed = 1000 + args.workload + 7919 * rank if rank else None
-    w = make_workload(args.workload, seed=seed)
+    w = make_workload(args.workload, seed=rank_seed(args.workload, rank))
 
     if args.impl == "reference":
         run_reference(args, w, rank)
@@ -444,11 +458,7 @@ def main():
     torch.cuda.synchronize()
     stage = [[ev[i].elapsed_time(ev[i + 1]) for i in range(3)] for ev in events]
     profiled_step_ms = statistics.fmean(ev[0].elapsed_time(ev[3]) for ev in events)
-    total_s = sum(step_ms) / 1e3
-    if dist:
-        t = torch.tensor([total_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_s = float(t.item())
+    total_s = max_over_ranks(sum(step_ms) / 1e3, dist, dev)
     value = world * w.T * args.steps / total_s
     kernel_names = ["gdp_desc_kernel", "gdp_wy_kernel", "gdp_scan_kernel"]
     kernel_ms = [statistics.fmean(x[i] for x in stage) for i in range(3)]
