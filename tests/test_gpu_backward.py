@@ -164,3 +164,12 @@ def test_backward_workload2_full_size(cuda_device):
     w = make_workload(2)
     d_out, d_fin = make_cotangents(w, seed=1, dfin_sigma=0.5)
     _compare(w, cuda_device, d_out, d_fin)
+
+
+def test_backward_empty_batch(cuda_device):
+    """No tokens at all: the initial-state gradient is the final-state gradient passed through."""
+    w = make_custom([0, 0], 2, 64, 2, seed=13, init_sigma=0.1)
+    d_out, d_fin = make_cotangents(w, seed=14)
+    res = _run(w, cuda_device, d_out, d_fin)
+    assert res["dq"].numel() == 0 and res["dv"].numel() == 0
+    assert torch.equal(res["d_initial_state"].cpu(), d_fin)
