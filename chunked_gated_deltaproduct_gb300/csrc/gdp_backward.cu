@@ -28,10 +28,10 @@
 //
 // Kernels (warp-level tf32 MMAs, fp32 accumulation -- the triangular solves in the 3xTF32
 // split; the dense chunk products are small and varied, the serial part is the state scan):
-//   gdp_bwd_scan_kernel   one CTA per (sequence, head): D = dL/dS in registers (two warps
-//                         per 16 state rows, one per column half), chunks in reverse,
-//                         operands from the forward's per-chunk images (TMA bulk copies,
-//                         double-buffered), writes D_C of every chunk
+//   gdp_bwd_scan_kernel   one CTA per (sequence, head): D = dL/dS in registers (a warp per
+//                         16 state rows), chunks in reverse, operands from the forward's
+//                         per-chunk images (TMA bulk copies, double-buffered), writes D_C of
+//                         every chunk
 //   gdp_bwd_chunk_kernel  one CTA per (expanded chunk, head), V in 16- (or 8-) column
 //                         slices: the per-row gradients above, the L2-norm chain rule
 //                         dx = dxhat / n - x (x . dxhat) / n^3, dq / dk / dv / dbeta stores
@@ -78,30 +78,23 @@ constexpr uint32_t kBwdScanLimit = 227u * 1024u;
 __host__ __device__ inline uint32_t bwd_stage_bytes(int d, int qpad) {
   return (ImageLayout(d, qpad).bytes + 1023u) & ~1023u;
 }
-// d_output rows of a chunk, bf16 [qpad][d + 8]; the Z exchange buffer, fp32 [d][64]
+// d_output rows of a chunk, bf16 [qpad][d + 8]
 __host__ __device__ inline uint32_t bwd_dos_bytes(int d, int qpad) { return (uint32_t)qpad * (d + 8) * 2u; }
-__host__ __device__ inline uint32_t bwd_zbuf_bytes(int d) { return (uint32_t)d * kChunk * 4u; }
 __host__ __device__ inline int bwd_scan_stages(int d, int qpad) {
-  return 2u * bwd_stage_bytes(d, qpad) + bwd_dos_bytes(d, qpad) + bwd_zbuf_bytes(d) + 1024u <= kBwdScanLimit ? 2 : 1;
+  return 2u * bwd_stage_bytes(d, qpad) + bwd_dos_bytes(d, qpad) + 1024u <= kBwdScanLimit ? 2 : 1;
 }
 __host__ inline size_t bwd_scan_smem(int d, int qpad) {
-  return (size_t)bwd_scan_stages(d, qpad) * bwd_stage_bytes(d, qpad) + bwd_dos_bytes(d, qpad) + bwd_zbuf_bytes(d) +
-         1024u;
+  return (size_t)bwd_scan_stages(d, qpad) * bwd_stage_bytes(d, qpad) + bwd_dos_bytes(d, qpad) + 1024u;
 }
 
-// Warp w holds state rows 16 (w % (D / 16)) .. +15 and the column half w / (D / 16) of D in
-// the m16n8 accumulator layout.  Per chunk, each half forms its share of Z = D Ktil^T
-// (plus dO^T P on half 0), the halves are summed through shared memory, and each half
-// updates its own columns of D.
+// Warp w holds state rows 16 w .. 16 w + 15 of D (all columns) in the m16n8 accumulator layout.
+// Per chunk it forms its rows of Z = D Ktil^T + dO^T P, then D_in = gamma_C D - Z W + dO^T Qh.
 template <int D, int QP>
-__global__ void __launch_bounds__(4 * D, 1) gdp_bwd_scan_kernel(BwdProblem p) {
-  constexpr int NR = D / 16;     // row groups
-  constexpr int NW = 2 * NR;     // warps
-  constexpr int HC = D / 2;      // columns per half
+__global__ void __launch_bounds__(2 * D, 1) gdp_bwd_scan_kernel(BwdProblem p) {
+  constexpr int NW = D / 16;     // warps
   constexpr int LDO = D + 8;     // row stride (bf16 elements) of the staged d_output rows
   const int seq = blockIdx.x, h = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
-  const int rg = warp % NR, ch = warp / NR;
   int64_t bos, L;
   if (!seq_bounds(p.cu, p.cu64, p.T, seq, &bos, &L)) return;
   const int M = p.M, H = p.H;
@@ -111,27 +104,25 @@ __global__ void __launch_bounds__(4 * D, 1) gdp_bwd_scan_kernel(BwdProblem p) {
   extern __shared__ __align__(1024) unsigned char bwd_scan_raw[];
   unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)bwd_scan_raw + 1023) & ~(uintptr_t)1023);
   __nv_bfloat16 *dos = reinterpret_cast<__nv_bfloat16 *>(sm + nst * sbytes);
-  float *zbuf = reinterpret_cast<float *>(sm + nst * sbytes + bwd_dos_bytes(D, QP));
   __shared__ __align__(8) uint64_t full[2];
   __shared__ float red[NW];
   const int64_t KV = (int64_t)D * D, sh = (int64_t)seq * H + h;
   const int64_t nchunks = (L * M + kChunk - 1) / kChunk;
   const int64_t cod_i = p.cod[seq];
   const int64_t nall = (cod_i < 0) ? 0 : max((int64_t)0, min(nchunks, p.ws_rows - cod_i));
-  const int r0 = 16 * rg + g;  // this thread's rows r0 and r0 + 8
-  const int c0 = HC * ch;      // first column of this warp's half
+  const int r0 = 16 * warp + g;  // this thread's rows r0 and r0 + 8
 
   // D = dL/dS_final; <dS_final, S_final> for the decay gradient
-  float dacc[HC / 8][4];
+  float dacc[D / 8][4];
   {
     const float *src = p.dfin ? p.dfin + sh * KV : nullptr;
     const float *fin = (p.dfin && p.fin) ? p.fin + sh * KV : nullptr;
     float part = 0.f;
 #pragma unroll
-    for (int j = 0; j < HC / 8; ++j)
+    for (int j = 0; j < D / 8; ++j)
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        const int64_t off = (int64_t)(r0 + 8 * hf) * D + c0 + 8 * j + 2 * t;
+        const int64_t off = (int64_t)(r0 + 8 * hf) * D + 8 * j + 2 * t;
         const float2 x = src ? *reinterpret_cast<const float2 *>(src + off) : make_float2(0.f, 0.f);
         dacc[j][2 * hf] = x.x;
         dacc[j][2 * hf + 1] = x.y;
@@ -166,19 +157,23 @@ __global__ void __launch_bounds__(4 * D, 1) gdp_bwd_scan_kernel(BwdProblem p) {
   if (tid == 0)
     for (int64_t i = 0; i < nst && i < nall; ++i) issue(i);
   auto dO = [&](int qi, int v) { return __bfloat162float(dos[qi * LDO + v]); };
+  // per-thread parts of the operand addresses in the swizzled image (row r, column k: 1024-byte
+  // atoms of 8 rows; the 16-byte chunk (k % 32) / 4 of row r sits at chunk position
+  // ((k % 32) / 4) ^ (r % 8)), in floats; the rest are compile-time steps
+  const uint32_t gq = (uint32_t)(g & 3), gh = (uint32_t)(g >> 2);
 
   bool aborted = false;
   for (int64_t i = 0; i < nall; ++i) {
     const int64_t e = nall - 1 - i;
     const int st = (int)(i % nst);
-    const unsigned char *im = sm + st * sbytes;
+    const float *imf = reinterpret_cast<const float *>(sm + st * sbytes);
     // the gradient at chunk e's exit
     float *dst = p.Dx + ((cod_i + e) * H + h) * KV;
 #pragma unroll
-    for (int j = 0; j < HC / 8; ++j)
+    for (int j = 0; j < D / 8; ++j)
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf)
-        *reinterpret_cast<float2 *>(dst + (int64_t)(r0 + 8 * hf) * D + c0 + 8 * j + 2 * t) =
+        *reinterpret_cast<float2 *>(dst + (int64_t)(r0 + 8 * hf) * D + 8 * j + 2 * t) =
             make_float2(dacc[j][2 * hf], dacc[j][2 * hf + 1]);
     // d_output rows of the chunk's readouts (bf16, zero past the readout count)
     const ImageMeta mt = *reinterpret_cast<const ImageMeta *>(image(e) + il.meta);
@@ -194,81 +189,44 @@ __global__ void __launch_bounds__(4 * D, 1) gdp_bwd_scan_kernel(BwdProblem p) {
       aborted = true;
       break;
     }
-    const float *imf = reinterpret_cast<const float *>(im);
-    // this half's share of Z = D Ktil^T (+ dO^T P on half 0): rows v x 64 chunk rows s.  The D
-    // fragments serve as A with the k order permuted within each 8-column step (logical
-    // k = t <-> column 2t, k = t + 4 <-> 2t + 1); B is read in the same order.  Operand
-    // addresses in the swizzled image (row r, column k: 1024-byte atoms of 8 rows, 16-byte
-    // chunk (k % 32) / 4 of row r at chunk position ((k % 32) / 4) ^ (r % 8)) are a per-thread
-    // base (ko, po, wo, qo below, in floats) plus compile-time steps.
+    // Z = D Ktil^T + dO^T P (rows of this warp x 64 chunk rows s).  The D fragments serve as A
+    // with the k order permuted within each 8-column step (logical k = t <-> column 2t,
+    // k = t + 4 <-> 2t + 1); B is read in the same order.
     float z[8][4];
 #pragma unroll
-    for (int n = 0; n < 8; ++n) z[n][0] = z[n][1] = z[n][2] = z[n][3] = 0.f;
-#pragma unroll
     for (int n = 0; n < 8; ++n) {
-      const uint32_t cq = 2u * (n & 3) + (g >> 2);  // chunk of column s = 8 n + g in its row
-      const uint32_t blk = (il.b2 + (uint32_t)(n >> 2) * il.b2_block) / 4u + (uint32_t)(g & 3);
-      // Ktil^T rows f = c0 + 8 j + 2 t (+1): atom (c0 / 8 + j), row-in-atom 2t (+1)
-      const uint32_t ko0 = blk + (uint32_t)(c0 / 8) * 256u + 2u * t * 32u + (((cq ^ (2u * t)) & 7u) << 2);
-      const uint32_t ko1 = blk + (uint32_t)(c0 / 8) * 256u + (2u * t + 1u) * 32u + (((cq ^ (2u * t + 1u)) & 7u) << 2);
+      z[n][0] = z[n][1] = z[n][2] = z[n][3] = 0.f;
+      const uint32_t cq = 2u * (n & 3) + gh;  // chunk of column s = 8 n + g in its row
+      const uint32_t blk = (il.b2 + (uint32_t)(n >> 2) * il.b2_block) / 4u + gq;
+      // Ktil^T rows f = 8 j + 2 t (+1): atom j, row-in-atom 2t (+1)
+      const uint32_t ko0 = blk + 2u * t * 32u + (((cq ^ (2u * t)) & 7u) << 2);
+      const uint32_t ko1 = blk + (2u * t + 1u) * 32u + (((cq ^ (2u * t + 1u)) & 7u) << 2);
 #pragma unroll
-      for (int j = 0; j < HC / 8; ++j) {
-        const uint32_t a0 = tf32r(dacc[j][0]), a1 = tf32r(dacc[j][2]), a2 = tf32r(dacc[j][1]),
-                       a3 = tf32r(dacc[j][3]);
-        mma8(z[n], a0, a1, a2, a3, tf32r(imf[ko0 + 256u * j]), tf32r(imf[ko1 + 256u * j]));
-      }
-      if (ch == 0) {
-        // P rows d + k0 + t (+4): atom (d + k0) / 8, row-in-atom t (+4)
-        const uint32_t po0 = blk + (uint32_t)(D / 8) * 256u + t * 32u + (((cq ^ t) & 7u) << 2);
-        const uint32_t po1 = blk + (uint32_t)(D / 8) * 256u + (t + 4u) * 32u + (((cq ^ (t + 4u)) & 7u) << 2);
+      for (int j = 0; j < D / 8; ++j)
+        mma8(z[n], tf32r(dacc[j][0]), tf32r(dacc[j][2]), tf32r(dacc[j][1]), tf32r(dacc[j][3]),
+             tf32r(imf[ko0 + 256u * j]), tf32r(imf[ko1 + 256u * j]));
+      // P rows d + k0 + t (+4): atom (d + k0) / 8, row-in-atom t (+4)
+      const uint32_t po0 = blk + (uint32_t)(D / 8) * 256u + t * 32u + (((cq ^ t) & 7u) << 2);
+      const uint32_t po1 = blk + (uint32_t)(D / 8) * 256u + (t + 4u) * 32u + (((cq ^ (t + 4u)) & 7u) << 2);
 #pragma unroll
-        for (int k = 0; k < QP / 8; ++k) {
-          const int k0 = 8 * k;
-          mma8(z[n], tf32r(dO(k0 + t, r0)), tf32r(dO(k0 + t, r0 + 8)), tf32r(dO(k0 + t + 4, r0)),
-               tf32r(dO(k0 + t + 4, r0 + 8)), tf32r(imf[po0 + 256u * k]), tf32r(imf[po1 + 256u * k]));
-        }
+      for (int k = 0; k < QP / 8; ++k) {
+        const int k0 = 8 * k;
+        mma8(z[n], tf32r(dO(k0 + t, r0)), tf32r(dO(k0 + t, r0 + 8)), tf32r(dO(k0 + t + 4, r0)),
+             tf32r(dO(k0 + t + 4, r0 + 8)), tf32r(imf[po0 + 256u * k]), tf32r(imf[po1 + 256u * k]));
       }
     }
-    // sum the halves: half 1 posts, half 0 adds and posts the sum, half 1 reads it
-    auto zput = [&]() {
-#pragma unroll
-      for (int n = 0; n < 8; ++n)
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
-          *reinterpret_cast<float2 *>(zbuf + (r0 + 8 * hf) * kChunk + 8 * n + 2 * t) =
-              make_float2(z[n][2 * hf], z[n][2 * hf + 1]);
-    };
-    auto zget = [&](bool add) {
-#pragma unroll
-      for (int n = 0; n < 8; ++n)
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const float2 x = *reinterpret_cast<const float2 *>(zbuf + (r0 + 8 * hf) * kChunk + 8 * n + 2 * t);
-          z[n][2 * hf] = add ? z[n][2 * hf] + x.x : x.x;
-          z[n][2 * hf + 1] = add ? z[n][2 * hf + 1] + x.y : x.y;
-        }
-    };
-    if (ch == 1) zput();
-    __syncthreads();
-    if (ch == 0) {
-      zget(true);
-      zput();
-    }
-    __syncthreads();
-    if (ch == 1) zget(false);
-    // D_in = gamma_C D + Z (-W) + dO^T Qh on this half's columns; a fast image holds -W and Qh
-    // divided by gamma_C
+    // D_in = gamma_C D + Z (-W) + dO^T Qh; a fast image holds -W and Qh divided by gamma_C
     const float gam = mt.gamma_last;
     if (!mt.fast)
 #pragma unroll
-      for (int j = 0; j < HC / 8; ++j)
+      for (int j = 0; j < D / 8; ++j)
 #pragma unroll
         for (int x = 0; x < 4; ++x) dacc[j][x] *= gam;
 #pragma unroll
-    for (int j = 0; j < HC / 8; ++j) {
-      // column f = c0 + 8 j + g: K-block f / 32, chunk ((8 j + g) % 32) / 4 (c0 is a multiple of 32)
-      const uint32_t cq = 2u * (j & 3) + (g >> 2);
-      const uint32_t blk = (il.b1 + (uint32_t)(c0 / 32 + (j >> 2)) * il.b1_block) / 4u + (uint32_t)(g & 3);
+    for (int j = 0; j < D / 8; ++j) {
+      // column f = 8 j + g: K-block j / 4, chunk 2 (j % 4) + g / 4
+      const uint32_t cq = 2u * (j & 3) + gh;
+      const uint32_t blk = (il.b1 + (uint32_t)(j >> 2) * il.b1_block) / 4u + gq;
       // -c W rows qp + 8 ks + 2 t (+1): atom qp / 8 + ks, row-in-atom 2t (+1)
       const uint32_t wo0 = blk + (uint32_t)(QP / 8) * 256u + 2u * t * 32u + (((cq ^ (2u * t)) & 7u) << 2);
       const uint32_t wo1 = blk + (uint32_t)(QP / 8) * 256u + (2u * t + 1u) * 32u + (((cq ^ (2u * t + 1u)) & 7u) << 2);
@@ -288,10 +246,10 @@ __global__ void __launch_bounds__(4 * D, 1) gdp_bwd_scan_kernel(BwdProblem p) {
     }
     if (mt.fast)
 #pragma unroll
-      for (int j = 0; j < HC / 8; ++j)
+      for (int j = 0; j < D / 8; ++j)
 #pragma unroll
         for (int x = 0; x < 4; ++x) dacc[j][x] *= gam;
-    __syncthreads();  // every warp is done with this stage, dos and zbuf
+    __syncthreads();  // every warp is done with this stage and dos
     if (tid == 0 && i + nst < nall) issue(i + nst);
   }
   if (aborted) {
@@ -306,10 +264,10 @@ __global__ void __launch_bounds__(4 * D, 1) gdp_bwd_scan_kernel(BwdProblem p) {
   if (p.dinit) {
     float *dst = p.dinit + sh * KV;
 #pragma unroll
-    for (int j = 0; j < HC / 8; ++j)
+    for (int j = 0; j < D / 8; ++j)
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf)
-        *reinterpret_cast<float2 *>(dst + (int64_t)(r0 + 8 * hf) * D + c0 + 8 * j + 2 * t) =
+        *reinterpret_cast<float2 *>(dst + (int64_t)(r0 + 8 * hf) * D + 8 * j + 2 * t) =
             make_float2(dacc[j][2 * hf], dacc[j][2 * hf + 1]);
   }
 }
@@ -945,7 +903,7 @@ cudaError_t launch_bscan(const BwdProblem &p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(gdp_bwd_scan_kernel<D, QP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  gdp_bwd_scan_kernel<D, QP><<<dim3((unsigned)p.N, (unsigned)p.H), 4 * D, smem, stream>>>(p);
+  gdp_bwd_scan_kernel<D, QP><<<dim3((unsigned)p.N, (unsigned)p.H), 2 * D, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
