@@ -39,9 +39,10 @@ from gdp_workloads import make_custom, WORKLOADS, make_workload  # noqa: E402
 METRIC = "GDP prefill real tokens/s on 1 GB300 (device-timed) and % of roofline"
 UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
-# DRAM traffic of the dominant kernel per launch, from one ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the sha256 of the
-# kernel's sources (KERNEL_SOURCES) it was taken on; reported as null once they change.
+# DRAM traffic of the dominant stage per call, from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum, summed over the stage's kernels), keyed by
+# the sha256 of the stage's sources (KERNEL_SOURCES) it was taken on; reported as null once
+# they change.
 NCU_TRAFFIC = {"gdp_scan_kernel": {"sha": "13e68d499a1788d5", "bytes_per_launch": 49113088, "workload": 2}}
 
 
@@ -144,7 +145,9 @@ class ClockSampler:
 
 
 KERNEL_SOURCES = {"gdp_desc_kernel": ("gdp_desc.cu",), "gdp_wy_kernel": ("gdp_wy.cu", "gdp_wy_body.cuh"),
-                  "gdp_scan_kernel": ("gdp_scan.cu", "gdp_scan_body.cuh")}
+                  "gdp_scan_kernel": ("gdp_scan.cu", "gdp_scan_body.cuh"),
+                  "gdp_scan_kernel x2 + gdp_piece_combine_kernel": ("gdp_scan.cu", "gdp_scan_body.cuh",
+                                                                    "gdp_pieces.cu")}
 
 
 def _kernel_sha(kernel: str) -> str:
@@ -232,13 +235,19 @@ def run_reference(args, w, rank):
 
 
 def launches_per_call(w) -> int:
-    """Kernels one call launches: descriptors, then WY + scan, or per segment in the segmented
-    mode (few (sequence, head) chains, long sequences: segments of 128 expanded chunks)."""
-    chains = w.N * w.H
-    maxc = (w.M * w.T + 63) // 64
-    if chains <= 64 and maxc >= 3 * 128:
-        return 1 + 2 * min((maxc + 127) // 128, 64)
-    return 3
+    """Kernels one call launches (the library's shape-only plan): descriptors, WY and scan; WY +
+    scan per segment in the segmented mode; or, with split chains, the scan's two passes and the
+    combine kernel between them."""
+    import chunked_gated_deltaproduct_gb300 as pkg
+    return pkg.gdp_prefill_plan(w.T, w.N, w.H, w.d, w.d, w.M)["launches"]
+
+
+def scan_stage_name(w) -> str:
+    """The kernels between the WY stage and the end of a call."""
+    import chunked_gated_deltaproduct_gb300 as pkg
+    if pkg.gdp_prefill_plan(w.T, w.N, w.H, w.d, w.d, w.M)["piece_chunks"] > 0:
+        return "gdp_scan_kernel x2 + gdp_piece_combine_kernel"
+    return "gdp_scan_kernel"
 
 
 def measure_decode(pkg, dev, flush, stream, steps=50, warmup=5):
@@ -460,7 +469,7 @@ def main():
     profiled_step_ms = statistics.fmean(ev[0].elapsed_time(ev[3]) for ev in events)
     total_s = max_over_ranks(sum(step_ms) / 1e3, dist, dev)
     value = world * w.T * args.steps / total_s
-    kernel_names = ["gdp_desc_kernel", "gdp_wy_kernel", "gdp_scan_kernel"]
+    kernel_names = ["gdp_desc_kernel", "gdp_wy_kernel", scan_stage_name(w)]
     kernel_ms = [statistics.fmean(x[i] for x in stage) for i in range(3)]
     dom = max(range(3), key=lambda i: kernel_ms[i])
     peak, peak_src = measured_peaks()

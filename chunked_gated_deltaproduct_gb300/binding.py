@@ -96,6 +96,8 @@ def load_library(path: str | None = None):
     lib.gdp_backward_workspace_bytes.argtypes = [_i64, _i64, _int, _int, _int, _int]
     lib.gdp_prefill_workspace_bytes.restype = _sz
     lib.gdp_prefill_workspace_bytes.argtypes = [_i64, _i64, _int, _int, _int, _int]
+    lib.gdp_prefill_plan.restype = _int
+    lib.gdp_prefill_plan.argtypes = [_i64, _i64, _int, _int, _int, _int] + [ctypes.POINTER(_i64)] * 4
     lib.gdp_build_descriptors.restype = _int
     lib.gdp_build_descriptors.argtypes = [_vp, _int, _i64, _i64, _int, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _vp]
     lib.gdp_last_error.restype = ctypes.c_char_p
@@ -129,6 +131,17 @@ def gdp_ntdp_pad(T: int, N: int, M: int) -> int:
 
 def gdp_prefill_workspace_bytes(T: int, N: int, H: int, K: int, V: int, M: int) -> int:
     return int(load_library().gdp_prefill_workspace_bytes(T, N, H, K, V, M))
+
+
+def gdp_prefill_plan(T: int, N: int, H: int, K: int, V: int, M: int) -> dict:
+    """How a call of this shape runs: segments, piece_chunks (0 unless the chains are split),
+    piece_rows and the number of kernel launches (shape-only)."""
+    lib = load_library()
+    out = [ctypes.c_int64() for _ in range(4)]
+    st = lib.gdp_prefill_plan(T, N, H, K, V, M, *[ctypes.byref(x) for x in out])
+    if st != GDP_OK:
+        raise GdpError(st, lib.gdp_last_error().decode())
+    return dict(zip(("segments", "piece_chunks", "piece_rows", "launches"), (int(x.value) for x in out)))
 
 
 def _stream(stream):

@@ -41,9 +41,32 @@ int seg_count(int64_t T, int64_t N, int H, int M) {
   return (int)min((maxc + gdp::kSegChunks - 1) / gdp::kSegChunks, (int64_t)gdp::kSegMax);
 }
 
+// Split chains (shape-only, see gdp::Problem::piece_len): in a one-segment call over few
+// sequences, the shortest piece length (at least kPieceMinChunks expanded chunks) whose
+// piece-row bound N + ceil(C / len) (C: the expanded-chunk bound; a sequence of n chunks has
+// max(1, ceil(n / len)) pieces) times H stays within kPieceCtas; off (len 0) when no piece
+// would be shorter than the longest possible sequence.
+struct PiecePlan {
+  int64_t len, rows;
+};
+PiecePlan piece_plan(int64_t T, int64_t N, int H, int M) {
+  PiecePlan pl{0, 0};
+  if (N < 1 || N > gdp::kPieceMaxSeqs || seg_count(T, N, H, M) != 1) return pl;
+  const int64_t C = ntdp_bound(T, N, M), maxc = ((int64_t)M * T + gdp::kChunk - 1) / gdp::kChunk;
+  for (int64_t len = gdp::kPieceMinChunks; len < maxc; ++len) {
+    const int64_t rows = N + (C + len - 1) / len;
+    if (rows * H <= gdp::kPieceCtas) {
+      pl.len = len;
+      pl.rows = rows;
+      break;
+    }
+  }
+  return pl;
+}
+
 // Workspace layout; identical for the size query and the carving.
 struct Layout {
-  size_t cod, ci, cid, co, img, img_stride, U, seg, total;
+  size_t cod, ci, cid, co, img, img_stride, U, seg, piece, total;
 };
 
 Layout layout_for(int64_t T, int64_t N, int H, int K, int V, int M) {
@@ -65,6 +88,8 @@ Layout layout_for(int64_t T, int64_t N, int H, int K, int V, int M) {
   l.img = take(l.img_stride * tiles);
   l.U = take(sizeof(float) * tiles * gdp::kChunk * (size_t)V);
   l.seg = seg_count(T, N, H, M) > 1 ? take(sizeof(float) * (size_t)N * H * (size_t)V * K) : 0;
+  const PiecePlan pp = piece_plan(T, N, H, M);
+  l.piece = pp.len > 0 ? take(sizeof(float) * 3 * (size_t)pp.rows * H * (size_t)V * K) : 0;
   l.total = off;
   return l;
 }
@@ -284,6 +309,11 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
   p.seg_state = nullptr;
   p.prefetch = (N * (int64_t)H <= gdp::kSegMaxChains) ? 1 : 0;
   const int nseg = seg_count(T, N, H, M);
+  const PiecePlan pp = piece_plan(T, N, H, M);
+  p.piece_len = (int)pp.len;
+  p.piece_rows = (int)pp.rows;
+  p.piece_pass1 = 0;
+  p.piece_buf = pp.len > 0 ? (float *)(ws + lay.piece) : nullptr;
   // desc -> WY -> scan on one stream overlap their launches (programmatic dependent launch);
   // the profiled form records events between them, so there each kernel runs alone
   p.pdl = (nseg == 1 && !ev) ? 1 : 0;
@@ -303,6 +333,17 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
     e = gdp::launch_wy(p, stream);
     if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "WY kernel: %s", cudaGetErrorString(e));
     if (ev && (st = record(ev[2], stream)) != GDP_OK) return st;
+    if (pp.len > 0) {  // split chains: B and Phi of the pieces, their entering states, the pieces
+      gdp::Problem q = p;
+      q.piece_pass1 = 1;
+      q.out = nullptr;
+      q.out_state = nullptr;
+      q.chunk_states = nullptr;
+      e = gdp::launch_scan(q, stream);
+      if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "scan kernel (pieces): %s", cudaGetErrorString(e));
+      e = gdp::launch_piece_combine(p, stream);
+      if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "piece combine kernel: %s", cudaGetErrorString(e));
+    }
     e = gdp::launch_scan(p, stream);
     if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "scan kernel: %s", cudaGetErrorString(e));
     if (ev && (st = record(ev[3], stream)) != GDP_OK) return st;
@@ -359,6 +400,21 @@ GDP_EXPORT int64_t gdp_ntdp_pad(int64_t T, int64_t N, int M) { return ntdp_bound
 GDP_EXPORT size_t gdp_prefill_workspace_bytes(int64_t T, int64_t N, int H, int K, int V, int M) {
   if (!shape_ok(T, N, H, K, V, M)) return 0;
   return layout_for(T, N, H, K, V, M).total;
+}
+
+GDP_EXPORT gdp_status gdp_prefill_plan(int64_t T, int64_t N, int H, int K, int V, int M, int64_t *segments,
+                                       int64_t *piece_chunks, int64_t *piece_rows, int64_t *launches) {
+  g_last_error[0] = 0;
+  if (!shape_ok(T, N, H, K, V, M))
+    return fail(GDP_ERR_INVALID_ARG, "bad shape T=%lld N=%lld H=%d K=%d V=%d M=%d", (long long)T, (long long)N, H, K,
+                V, M);
+  const int nseg = seg_count(T, N, H, M);
+  const PiecePlan pp = piece_plan(T, N, H, M);
+  if (segments) *segments = nseg;
+  if (piece_chunks) *piece_chunks = pp.len;
+  if (piece_rows) *piece_rows = pp.rows;
+  if (launches) *launches = N == 0 ? 0 : 1 + (nseg > 1 ? 2 * nseg : (pp.len > 0 ? 4 : 2));
+  return GDP_OK;
 }
 
 GDP_EXPORT const char *gdp_last_error(void) { return g_last_error; }

@@ -136,6 +136,18 @@ struct Problem {
   // chunk, with co = the expanded-chunk offsets, for the backward pass).  A NULL `out` skips
   // the output stores.
   int cs_div;
+  // Split chains (few long chains; 0: off): a sequence of n chunks runs as
+  // max(1, ceil(n / piece_len)) pieces of piece_len expanded chunks, numbered sequence by
+  // sequence (piece rows).  The state recurrence is affine in the state, S' = S Phi + B, so
+  // a piece's entering state follows from its predecessors' (Phi, B) alone.  piece_pass1 = 1:
+  // for every piece but a sequence's last, grid row r < piece_rows runs the piece from a zero
+  // state (its B) and row piece_rows + r from the identity with V = 0 (its Phi), each leaving
+  // its end state in piece_buf row (grid row); no outputs.  piece_pass1 = 0: piece r of a
+  // split sequence enters with piece_buf row 2 piece_rows + r (the combine kernel's S_in)
+  // and writes outputs, chunk states and, as its sequence's last piece, the final state.
+  // piece_buf: [3 piece_rows][H][V][K] fp32.
+  int piece_len, piece_rows, piece_pass1;
+  float *piece_buf;
 };
 
 // Everything the backward kernels need about one call (gdp_backward.cu).  Heads are
@@ -222,6 +234,51 @@ __device__ __forceinline__ bool seq_bounds(const void *cu, int cu64, int64_t T, 
   return ok;
 }
 
+// Split chains: the number of pieces of sequence i, from its chunks whose workspace tile
+// exists; at least one, so that an empty sequence still passes its state through.
+constexpr int kPieceMaxSeqs = 32;    // sequences a split call may hold (one warp finds a piece)
+constexpr int kPieceCtas = 128;      // piece rows x heads of a split call
+constexpr int kPieceMinChunks = 6;   // shortest piece (measured: 4 to 7 within 2 %, 6 best)
+__device__ __forceinline__ int seq_pieces(const Problem &p, int64_t i) {
+  int64_t bos, L;
+  seq_bounds(p.cu, p.cu64, p.T, i, &bos, &L);
+  const int64_t nch = (L * p.M + kChunk - 1) / kChunk, cod = p.cod[i];
+  const int64_t nall = (cod < 0) ? 0 : max((int64_t)0, min(nch, p.ws_rows - cod));
+  return (int)max((int64_t)1, (nall + p.piece_len - 1) / p.piece_len);
+}
+// Warp-wide (all 32 lanes, N <= kPieceMaxSeqs): lane i < N holds its sequence's piece count
+// n and the inclusive prefix sum of the counts.
+__device__ __forceinline__ void piece_prefix(const Problem &p, int lane, int *n, int *incl) {
+  const int c = (lane < p.N) ? seq_pieces(p, lane) : 0;
+  int x = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  *n = c;
+  *incl = x;
+}
+// Warp-wide: the sequence holding piece row r, the piece's index in it and the sequence's
+// piece count; seq = -1 past the last piece.
+__device__ __forceinline__ void piece_of_row(const Problem &p, int r, int lane, int *seq, int *pi, int *np) {
+  int n, incl;
+  piece_prefix(p, lane, &n, &incl);
+  // the counts are positive, so the sequences ending at or before r are a prefix
+  const int s = __popc(__ballot_sync(0xffffffffu, lane < p.N && incl <= r));
+  const int first = __shfl_sync(0xffffffffu, incl - n, s & 31), cnt = __shfl_sync(0xffffffffu, n, s & 31);
+  *seq = (s < p.N) ? s : -1;
+  *pi = r - first;
+  *np = cnt;
+}
+// Warp-wide: sequence i's first piece row and piece count.
+__device__ __forceinline__ void pieces_of_seq(const Problem &p, int i, int lane, int *first, int *np) {
+  int n, incl;
+  piece_prefix(p, lane, &n, &incl);
+  *first = __shfl_sync(0xffffffffu, incl - n, i & 31);
+  *np = __shfl_sync(0xffffffffu, n, i & 31);
+}
+
 __device__ __forceinline__ void set_status(uint32_t *status, uint32_t bits) {
   if (status) atomicOr(status, bits);
 }
@@ -236,6 +293,8 @@ cudaError_t launch_wy_variant(const Problem &p, cudaStream_t stream, bool f16, b
 cudaError_t launch_scan(const Problem &p, cudaStream_t stream);
 // The scan for float16 inputs (f16) and / or a bfloat16 dense initial state (init16).
 cudaError_t launch_scan_variant(const Problem &p, cudaStream_t stream, bool f16, bool init16);
+// Split chains: the entering state of every piece of a split sequence (gdp_pieces.cu).
+cudaError_t launch_piece_combine(const Problem &p, cudaStream_t stream);
 
 // TMA tensor maps (gdp_tmap.cu; `map` points at a 64-byte aligned CUtensorMap; a NULL base
 // leaves it zeroed).  All use the 128-byte swizzle.

@@ -1,0 +1,245 @@
+// gdp_pieces.cu -- split chains: the entering state of every piece of a split sequence.
+//
+// Over its expanded chunks a sequence's state follows the affine recurrence
+// S_{e+1} = S_e A_e + B_e (V-major state, right multiplication by K x K maps; the
+// decay, the delta-rule updates and the readouts of Megatron-Core API page
+// "core.ssm.ops.gdp.chunk", stages 3 and 4).  Cut into pieces of piece_len chunks, piece j
+// maps its entering state to S_in(j) Phi_j + B_j, where B_j is the piece run from a zero
+// state and Phi_j the piece run from the identity with V = 0 -- the scan kernel's first
+// pass computes both for every piece but a sequence's last, all pieces at once.  This
+// kernel chains them,
+//   S_in(0) = the sequence's initial state,   S_in(j + 1) = S_in(j) Phi_j + B_j,
+// on warp-level tf32 MMAs in the 3xTF32 split, and stores every S_in for the scan's second
+// pass, which then runs all pieces at once from their own entering states.  Rows of the state
+// are independent: one CTA per (sequence, head, 16 state rows), one CTA per SM, so a
+// (sequence, head) spreads over V / 16 SMs.  Phi_{j+2} and B_{j+2} arrive by TMA while step j
+// computes.
+#include <cuda.h>  // CUtensorMap
+
+#include "gdp_internal.cuh"
+#include "gdp_sm100.cuh"
+
+namespace gdp {
+namespace {
+
+constexpr int kCmbThreads = 256;    // 8 warps, each owning D / 8 columns of the CTA's rows
+constexpr int kCmbRows = 16;        // state rows per CTA (the MMA's M)
+constexpr size_t kCmbMinSmem = 116u * 1024u;  // at most one CTA per SM: the steps are serial, an SM each
+
+__device__ __forceinline__ uint32_t tf32r(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+// c[16 x 8] += A[16 x 8] B[8 x 8] (m16n8k8, tf32 in, fp32 out).  Fragments (lane = 4 g + t):
+// A (g, t), (g+8, t), (g, t+4), (g+8, t+4); B (t, g), (t+4, g); C (g, 2t), (g, 2t+1),
+// (g+8, 2t), (g+8, 2t+1).
+__device__ __forceinline__ void mma8(float *c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                     uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Shared memory: Phi_j in two stages as 32 x 32 boxes of the state map (128-byte swizzle: row r
+// of a box at r * 128 bytes, its 16-byte chunk q at position q ^ (r % 8)); B_j (this CTA's 16
+// rows) in two stages; S_in(j) split into tf32 high and low parts, [16][D + 4] each, in two
+// buffers (the row pad spreads the A-fragment loads over all banks).
+__host__ __device__ constexpr uint32_t cmb_phi_bytes(int d) { return (uint32_t)d * d * 4u; }
+__host__ __device__ constexpr uint32_t cmb_b_bytes(int d) { return (uint32_t)kCmbRows * d * 4u; }
+__host__ __device__ constexpr uint32_t cmb_s_floats(int d) { return (uint32_t)kCmbRows * (d + 4); }
+__host__ inline size_t cmb_smem(int d) {
+  const size_t need = 2 * (size_t)cmb_phi_bytes(d) + 2 * (size_t)cmb_b_bytes(d) + 4 * 4 * (size_t)cmb_s_floats(d) + 1024;
+  return need > kCmbMinSmem ? need : kCmbMinSmem;
+}
+
+// Step j: S_in(j + 1) = S_in(j) Phi_j + B_j on warp-level tf32 MMAs with the 3xTF32 split
+// (hi hi + lo hi + hi lo: about fp32 accuracy, since the product replaces the whole state
+// every step).  Warp w owns columns [w D / 8, (w + 1) D / 8) of the CTA's 16 rows: NT n-tiles
+// of 8, with separate accumulators per split term and k-step parity (independent MMA chains),
+// summed with B_j at the end.  Thread 0 brings Phi_j (tensor boxes) and B_j (one bulk copy)
+// in two steps ahead.  (Sharing Phi_j among the row blocks of a (sequence, head) by cluster
+// multicast was slower: clusters of 8 whole-SM CTAs start later.)
+template <int D, bool INIT16>
+__global__ void __launch_bounds__(kCmbThreads, 1) gdp_piece_combine_kernel(Problem p,
+                                                                        const __grid_constant__ CUtensorMap tm_phi) {
+  constexpr int NT = D / 64, NB = D / 32, SP = D + 4;
+  constexpr uint32_t PB = cmb_phi_bytes(D), BB = cmb_b_bytes(D), SF = cmb_s_floats(D);
+  extern __shared__ __align__(1024) unsigned char cmb_smem_raw[];
+  unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)cmb_smem_raw + 1023) & ~(uintptr_t)1023);
+  float *bst = reinterpret_cast<float *>(sm + 2 * PB);  // B_j stages, [2][16][D]
+  float *sb = bst + 2 * BB / 4;                          // S_in(j): [buffer][hi, lo][16][D + 4]
+  __shared__ __align__(8) uint64_t full[2];
+  __shared__ int sh[2];
+  const int seq = blockIdx.x, h = blockIdx.y, r0 = kCmbRows * (int)blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
+
+  // B and Phi come from the grid before; wait before any exit so that this grid's
+  // completion implies its predecessors'
+  sm100::pdl_wait();
+  sm100::pdl_trigger();
+  if (warp == 0) {
+    int first, np;
+    pieces_of_seq(p, seq, lane, &first, &np);
+    if (lane == 0) {
+      sh[0] = first;
+      sh[1] = np;
+    }
+  }
+  if (tid == 0) {
+    sm100::mbar_init(&full[0], 1);
+    sm100::mbar_init(&full[1], 1);
+    sm100::mbar_init_fence();
+  }
+  __syncthreads();
+  const int first = sh[0], np = sh[1];
+  if (np <= 1) return;  // one piece: the scan reads the caller's state itself
+  const int64_t KV = (int64_t)D * D, R = p.piece_rows;
+  auto rows_of = [&](int64_t prow) { return p.piece_buf + (prow * p.H + h) * KV; };
+  int issued[2] = {0, 0};
+  auto issue = [&](int j) {  // Phi_j and B_j (rows r0 ..) into stage j % 2 (thread 0)
+    const int sg = j & 1;
+    unsigned char *dst = sm + sg * PB;
+    sm100::mbar_arrive_expect_tx(&full[sg], PB + BB);
+    const int y0 = (int)(((R + first + j) * p.H + h) * D);  // Phi_j's first row in the map
+#pragma unroll
+    for (int kb = 0; kb < NB; ++kb)
+#pragma unroll
+      for (int cb = 0; cb < NB; ++cb)
+        sm100::tma_load_2d(dst + (kb * NB + cb) * 4096, &tm_phi, 32 * cb, y0 + 32 * kb, &full[sg]);
+    sm100::bulk_g2s(bst + sg * (BB / 4), rows_of(first + j) + (int64_t)r0 * D, BB, &full[sg]);
+    ++issued[sg];
+  };
+  if (tid == 0)
+    for (int j = 0; j < 2 && j + 1 < np; ++j) issue(j);
+
+  // S_in(j) -> piece_buf row 2 R + first + j (fp32) and S buffer j % 2 (tf32 hi / lo)
+  auto put2 = [&](int j, int row, int col, float x0, float x1) {
+    *reinterpret_cast<float2 *>(rows_of(2 * R + first + j) + (int64_t)(r0 + row) * D + col) = make_float2(x0, x1);
+    float *hi = sb + (j & 1) * 2 * SF, *lo = hi + SF;
+    const float h0 = __uint_as_float(tf32r(x0)), h1 = __uint_as_float(tf32r(x1));
+    *reinterpret_cast<float2 *>(hi + row * SP + col) = make_float2(h0, h1);
+    *reinterpret_cast<float2 *>(lo + row * SP + col) =
+        make_float2(__uint_as_float(tf32r(x0 - h0)), __uint_as_float(tf32r(x1 - h1)));
+  };
+  {  // S_in(0): the caller's state (cache slot, dense fp32 / bf16, or zero)
+    const float *src = nullptr;
+    const __nv_bfloat16 *src16 = nullptr;
+    if (p.cache) {  // an out-of-range slot reads as no state (the scan reports it)
+      const int slot = p.slots[seq];
+      if (slot >= 0 && slot < p.num_slots) src = p.cache + ((int64_t)slot * p.H + h) * KV;
+    } else if (p.init) {
+      if constexpr (INIT16)
+        src16 = static_cast<const __nv_bfloat16 *>(p.init) + ((int64_t)seq * p.H + h) * KV;
+      else
+        src = static_cast<const float *>(p.init) + ((int64_t)seq * p.H + h) * KV;
+    }
+    for (int idx = tid; idx < kCmbRows * D / 2; idx += kCmbThreads) {
+      const int row = idx / (D / 2), col = 2 * (idx % (D / 2));
+      const int64_t off = (int64_t)(r0 + row) * D + col;
+      float2 x = make_float2(0.f, 0.f);
+      if (src) x = *reinterpret_cast<const float2 *>(src + off);
+      if constexpr (INIT16) {
+        if (src16) x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(src16 + off));
+      }
+      put2(0, row, col, x.x, x.y);
+    }
+  }
+  // per-thread parts of the B-fragment offsets (floats) inside a stage: column c = n0 + g of
+  // n-tile n0 sits in box column c / 32, chunk (c % 32) / 4, at (c % 4); rows k0 + t and
+  // k0 + t + 4 of the k-step are box rows 8 (ks % 4) + t (+ 4), with chunk position chunk ^ row % 8
+  uint32_t bo0[NT], bo1[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int n0 = warp * 8 * NT + 8 * nt;
+    const uint32_t cq = (uint32_t)(((n0 & 31) >> 2) + (g >> 2));
+    const uint32_t base = (uint32_t)(n0 >> 5) * 1024u + (uint32_t)(g & 3);
+    bo0[nt] = base + (uint32_t)t * 32u + (((cq ^ (uint32_t)t) & 7u) << 2);
+    bo1[nt] = base + (uint32_t)(t + 4) * 32u + (((cq ^ (uint32_t)(t + 4)) & 7u) << 2);
+  }
+  bool ok = true;
+#pragma unroll 1
+  for (int j = 0; j + 1 < np; ++j) {
+    const int sg = j & 1;
+    // also publishes S_in(j) (written before this point)
+    ok = __syncthreads_and(sm100::mbar_wait(&full[sg], (uint32_t)((j >> 1) & 1)));
+    if (!ok) break;
+    const float *phi = reinterpret_cast<const float *>(sm + sg * PB);
+    const float *bj = bst + sg * (BB / 4);
+    const float *hi = sb + sg * 2 * SF, *lo = hi + SF;
+    float acc[2][NT][3][4];  // [k-step parity][n-tile][hi hi, lo hi, hi lo]
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int x = 0; x < 3; ++x) acc[e][nt][x][0] = acc[e][nt][x][1] = acc[e][nt][x][2] = acc[e][nt][x][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < D / 8; ++ks) {
+      const int k0 = 8 * ks, e = ks & 1;
+      const uint32_t ah0 = __float_as_uint(hi[g * SP + k0 + t]), ah1 = __float_as_uint(hi[(g + 8) * SP + k0 + t]);
+      const uint32_t ah2 = __float_as_uint(hi[g * SP + k0 + t + 4]),
+                     ah3 = __float_as_uint(hi[(g + 8) * SP + k0 + t + 4]);
+      const uint32_t al0 = __float_as_uint(lo[g * SP + k0 + t]), al1 = __float_as_uint(lo[(g + 8) * SP + k0 + t]);
+      const uint32_t al2 = __float_as_uint(lo[g * SP + k0 + t + 4]),
+                     al3 = __float_as_uint(lo[(g + 8) * SP + k0 + t + 4]);
+      const uint32_t kofs = (uint32_t)(ks >> 2) * (uint32_t)NB * 1024u + (uint32_t)(ks & 3) * 256u;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float b0 = phi[kofs + bo0[nt]], b1 = phi[kofs + bo1[nt]];
+        const uint32_t bh0 = tf32r(b0), bh1 = tf32r(b1);
+        const uint32_t bl0 = tf32r(b0 - __uint_as_float(bh0)), bl1 = tf32r(b1 - __uint_as_float(bh1));
+        mma8(acc[e][nt][0], ah0, ah1, ah2, ah3, bh0, bh1);
+        mma8(acc[e][nt][1], al0, al1, al2, al3, bh0, bh1);
+        mma8(acc[e][nt][2], ah0, ah1, ah2, ah3, bl0, bl1);
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int c = warp * 8 * NT + 8 * nt + 2 * t;
+      const float2 u0 = *reinterpret_cast<const float2 *>(bj + g * D + c);
+      const float2 u1 = *reinterpret_cast<const float2 *>(bj + (g + 8) * D + c);
+      float y[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)  // small terms first
+        y[q] = ((acc[0][nt][1][q] + acc[1][nt][1][q]) + (acc[0][nt][2][q] + acc[1][nt][2][q])) +
+               (acc[0][nt][0][q] + acc[1][nt][0][q]);
+      put2(j + 1, g, c, y[0] + u0.x, y[1] + u0.y);
+      put2(j + 1, g + 8, c, y[2] + u1.x, y[3] + u1.y);
+    }
+    __syncthreads();  // stage sg and S buffer j % 2 are consumed
+    if (tid == 0 && j + 3 < np) issue(j + 2);
+  }
+  if (!ok && tid == 0) {
+    set_status(p.status, GDP_DEV_ERR_TIMEOUT);
+    for (int sg = 0; sg < 2; ++sg)  // bounded: the last copies issued on each stage have landed
+      if (issued[sg] > 0) sm100::mbar_wait(&full[sg], (uint32_t)((issued[sg] - 1) & 1));
+  }
+}
+
+template <int D, bool INIT16>
+cudaError_t launch_combine_d(const Problem &p, cudaStream_t stream) {
+  const size_t smem = cmb_smem(D);
+  cudaError_t e = cudaFuncSetAttribute(gdp_piece_combine_kernel<D, INIT16>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  alignas(64) CUtensorMap tm_phi;  // the piece states, [3 piece_rows][H][V][K] fp32, 32 x 32 boxes
+  if ((e = tmap_state(&tm_phi, p.piece_buf, 3 * (int64_t)p.piece_rows * p.H * p.V, p.K)) != cudaSuccess) return e;
+  e = launch_kernel(gdp_piece_combine_kernel<D, INIT16>, dim3((unsigned)p.N, (unsigned)p.H, (unsigned)(D / kCmbRows)),
+                    dim3(kCmbThreads), smem, stream, p.pdl != 0, p, tm_phi);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_piece_combine(const Problem &p, cudaStream_t stream) {
+  if (p.N == 0 || p.piece_len <= 0) return cudaSuccess;
+  const bool init16 = p.init && p.init_bf16 && !p.cache;
+  if (p.K == 64) return init16 ? launch_combine_d<64, true>(p, stream) : launch_combine_d<64, false>(p, stream);
+  if (p.K == 128) return init16 ? launch_combine_d<128, true>(p, stream) : launch_combine_d<128, false>(p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace gdp

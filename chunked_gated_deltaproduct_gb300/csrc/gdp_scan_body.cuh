@@ -127,11 +127,36 @@ template <bool F16, bool INIT16>
 __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &tm_cs, const CUtensorMap &tm_fin,
                                           const CUtensorMap &tm_seg, const CUtensorMap &tm_out_a,
                                           const CUtensorMap &tm_out_b) {
-  const int seq = blockIdx.x, h = blockIdx.y;
+  const int h = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // split chains: this CTA's piece (pass 1: grid row r and piece_rows + r run the same piece)
+  const bool pieces = p.piece_len > 0, pass1 = pieces && p.piece_pass1;
+  const bool transfer = pass1 && (int)blockIdx.x >= p.piece_rows;  // from the identity, V = 0
+  int seq = blockIdx.x, pc_i = 0, pc_n = 1;
+  if (pieces) {
+    // the piece table comes from the descriptors; every CTA waits for its predecessor grid
+    // before it may exit, so that this grid's completion implies the predecessors'
+    pdl_wait();
+    pdl_trigger();
+    __shared__ int pc_sh[3];
+    if (warp == 0) {
+      int sq, pi, np;
+      piece_of_row(p, (int)blockIdx.x - (transfer ? p.piece_rows : 0), lane, &sq, &pi, &np);
+      if (lane == 0) {
+        pc_sh[0] = sq;
+        pc_sh[1] = pi;
+        pc_sh[2] = np;
+      }
+    }
+    __syncthreads();
+    seq = pc_sh[0];
+    pc_i = pc_sh[1];
+    pc_n = pc_sh[2];
+    if (seq < 0 || (pass1 && pc_i == pc_n - 1)) return;  // past the last piece; a last piece has no pass 1
+  }
   int64_t bos, L;
   if (!seq_bounds(p.cu, p.cu64, p.T, seq, &bos, &L)) return;  // flagged by the descriptor kernel
   const int d = p.K, V = p.V, M = p.M, QP = p.qpad, H = p.H;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q4 = warp & 3;
   const int v = q4 * 32 + lane;  // state row (TMEM lane) of prep and store threads
   const uint32_t lrow = (uint32_t)(q4 * 32) << 16;
@@ -157,7 +182,7 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
   if (p.cache) {
     slot = p.slots[seq];
     if (slot < -1 || slot >= p.num_slots) {
-      if (tid == 0 && p.seg_lo == 0) set_status(p.status, GDP_DEV_ERR_SLOT);
+      if (tid == 0 && p.seg_lo == 0 && !pass1 && pc_i == 0) set_status(p.status, GDP_DEV_ERR_SLOT);
       slot = -1;
     }
     if (slot >= 0) src = p.cache + ((int64_t)slot * H + h) * (int64_t)V * d;
@@ -166,6 +191,10 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
       src16 = static_cast<const __nv_bfloat16 *>(p.init) + ((int64_t)seq * H + h) * (int64_t)V * d;
     else
       src = static_cast<const float *>(p.init) + ((int64_t)seq * H + h) * (int64_t)V * d;
+  }
+  if (pass1 || pc_n > 1) {  // pass 1 starts from zero (or the identity); a split piece from its S_in
+    src = pass1 ? nullptr : p.piece_buf + ((int64_t)(2 * p.piece_rows + (int)blockIdx.x) * H + h) * (int64_t)V * d;
+    if constexpr (INIT16) src16 = nullptr;
   }
 
   // Descriptors, workspace tiles and a carried state come from earlier kernels of the stream:
@@ -180,6 +209,12 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
     // chunks whose workspace tile exists (a flagged descriptor overflow truncates the sequence)
     nall = (cod_i < 0) ? 0 : max((int64_t)0, min(nchunks, p.ws_rows - cod_i));
     // this launch's chunks: global chunk e0 + e for local e in [0, nrun)
+    if (pieces) {
+      e0 = min((int64_t)pc_i * p.piece_len, nall);
+      nrun = max((int64_t)0, min(e0 + p.piece_len, nall) - e0);
+      last_seg = pc_i == pc_n - 1;
+      return;
+    }
     e0 = min(p.seg_lo, nall);
     nrun = max((int64_t)0, min(p.seg_hi, nall) - e0);
     last_seg = e0 + nrun == nall;
@@ -227,6 +262,7 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
   const uint32_t tS = tb, tBk = tb + 384;
   auto tO = [&](int b) { return tb + 128u + (uint32_t)b * (uint32_t)(QP + 64); };
   const uint32_t id1 = idesc(kFmtTF32, 0, 0, QP + 64, 128);  // [o_hat | Y] += S_hat [Qh ; -W]^T
+  const uint32_t id1y = idesc(kFmtTF32, 0, 0, 64, 128);      // Y += S_hat (-W)^T (no outputs)
   const uint32_t id2s = idesc(kFmtTF32, 0, 0, d, 128);       // S_hat += Y Ktil
   const uint32_t id2o = idesc(kFmtTF32, 0, 0, QP, 128);      // o_hat += Y P^T
 
@@ -256,6 +292,9 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
         if (src && v < V) y = *reinterpret_cast<const float4 *>(src + (int64_t)v * d + c0 + u4);
         x[u4] = y.x; x[u4 + 1] = y.y; x[u4 + 2] = y.z; x[u4 + 3] = y.w;
       }
+      if (transfer)  // the identity (V == K)
+#pragma unroll
+        for (int u = 0; u < 16; ++u) x[u] = (c0 + u == v) ? 1.f : 0.f;
       if constexpr (INIT16) {
         if (src16 && v < V) {  // eight bf16 per 16-byte load
 #pragma unroll
@@ -296,7 +335,7 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
                          (v < V ? q4 * 512 + lane : 0);
 #pragma unroll
       for (int s4 = 0; s4 < 16; ++s4) {
-        const float4 x = (v < V) ? Ut[s4 * 32] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 x = (v < V && !transfer) ? Ut[s4 * 32] : make_float4(0.f, 0.f, 0.f, 0.f);
         u[4 * s4] = x.x; u[4 * s4 + 1] = x.y; u[4 * s4 + 2] = x.z; u[4 * s4 + 3] = x.w;
       }
     };
@@ -323,7 +362,7 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
       for (int w = 0; w < 64; ++w) u[w] *= inv;  // u is reloaded for the next chunk below
       tmem_st32x(ty + lrow, u);
       tmem_st32x(ty + lrow + 32, u + 32);
-      {
+      if (p.out) {  // without outputs the MMAs leave o_hat alone
         float z[16];
 #pragma unroll
         for (int w = 0; w < 16; ++w) z[w] = 0.f;
@@ -402,7 +441,7 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
       gam_fin = ci.out_scale;
       // outputs: the chunk's o_hat columns (read under one wait), 16-bit staging [q][v]
 #pragma unroll 1
-      for (int q0 = 0; q0 < ci.nq; q0 += 32) {  // 32 readout rows per wait
+      for (int q0 = 0; p.out && q0 < ci.nq; q0 += 32) {  // 32 readout rows per wait
         uint32_t xo[32];
         tmem_ld16_nw(tO(b) + lrow + q0, xo);
         if (q0 + 16 < ci.nq) tmem_ld16_nw(tO(b) + lrow + q0 + 16, xo + 16);
@@ -452,8 +491,11 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
     if (!abort_flag && has_rows) {  // the last chunk's b2_done was waited for above
       int64_t r = -1;
       const CUtensorMap *tm = &tm_fin;
-      if (!last_seg) {  // carried to the next segment
-        r = ((int64_t)seq * H + h) * V;
+      if (pass1) {  // B or Phi of the piece (piece_buf through the segment map)
+        r = ((int64_t)blockIdx.x * H + h) * V;
+        tm = &tm_seg;
+      } else if (!last_seg) {  // carried to the next segment (a split piece leaves nothing)
+        if (!pieces) r = ((int64_t)seq * H + h) * V;
         tm = &tm_seg;
       } else if (p.cache) {
         if (slot >= 0) r = ((int64_t)slot * H + h) * V;
@@ -477,8 +519,16 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
         const bool mid = emits(e) || mt.fast == 0;
         const uint32_t to = tO(b), ty = to + (uint32_t)QP;
         const uint32_t sb1 = smem_u32(stage) + il.b1, sb2 = smem_u32(stage) + il.b2;
-        for (int kk = 0; kk < d / 8; ++kk)
-          mma_tf32_ts(to, tS + kk * 8, desc_sw128(sb1 + (kk >> 2) * il.b1_block + (kk & 3) * 32u, 16, 1024), id1, 1);
+        if (p.out) {
+          for (int kk = 0; kk < d / 8; ++kk)
+            mma_tf32_ts(to, tS + kk * 8, desc_sw128(sb1 + (kk >> 2) * il.b1_block + (kk & 3) * 32u, 16, 1024), id1,
+                        1);
+        } else {  // the -W rows only: they start qpad rows (whole 1024-byte atoms) into each K-block
+          for (int kk = 0; kk < d / 8; ++kk)
+            mma_tf32_ts(ty, tS + kk * 8,
+                        desc_sw128(sb1 + (kk >> 2) * il.b1_block + (uint32_t)QP * 128u + (kk & 3) * 32u, 16, 1024),
+                        id1y, 1);
+        }
         mma_commit(&b1_done[b]);
         if (!mbar_wait_or_abort(&full2[st], (uint32_t)((e / nst) & 1), &abort_flag)) break;
         if (mid) {
@@ -491,7 +541,7 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
         for (int kk = 0; kk < kChunk / 8; ++kk) {
           const uint32_t bk = sb2 + (kk >> 2) * il.b2_block + (kk & 3) * 32u;
           mma_tf32_ts(tS, ty + kk * 8, desc_sw128(bk, 16, 1024), id2s, 1);
-          mma_tf32_ts(to, ty + kk * 8, desc_sw128(bk + (uint32_t)d * 128u, 16, 1024), id2o, 1);
+          if (p.out) mma_tf32_ts(to, ty + kk * 8, desc_sw128(bk + (uint32_t)d * 128u, 16, 1024), id2o, 1);
         }
         mma_commit(&b2_done[b]);
       }
@@ -512,7 +562,7 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
     auto prefetch = [&](int64_t e) {
       if (p.prefetch && e < nrun) {
         bulk_prefetch_l2(image(e), il.bytes & ~15u);
-        bulk_prefetch_l2(p.U + ((cod_i + e0 + e) * H + h) * (int64_t)V * kChunk, ubytes);
+        if (!transfer) bulk_prefetch_l2(p.U + ((cod_i + e0 + e) * H + h) * (int64_t)V * kChunk, ubytes);
       }
     };
     for (int64_t e = 0; e < kPrefetch; ++e) prefetch(nst + e);
@@ -552,7 +602,11 @@ cudaError_t launch_scan_kernel(Kern kern, const Problem &p, cudaStream_t stream)
   else
     e = tmap_state(&tm_fin, p.out_state, p.N * hv, p.K);
   if (e != cudaSuccess) return e;
-  if ((e = tmap_state(&tm_seg, p.seg_state, p.N * hv, p.K)) != cudaSuccess) return e;
+  if (p.piece_len > 0)  // the piece states (pass 1 writes B and Phi through it)
+    e = tmap_state(&tm_seg, p.piece_buf, 3 * (int64_t)p.piece_rows * hv, p.K);
+  else
+    e = tmap_state(&tm_seg, p.seg_state, p.N * hv, p.K);
+  if (e != cudaSuccess) return e;
   // output boxes of 64 / M and ceil(64 / M) token rows: the readout counts of a full chunk
   alignas(64) CUtensorMap tm_out_a, tm_out_b;
   Problem q = p;
@@ -560,7 +614,9 @@ cudaError_t launch_scan_kernel(Kern kern, const Problem &p, cudaStream_t stream)
   q.out_tma = (p.out && p.T >= nb) ? 1 : 0;
   if ((e = tmap_out_rows(&tm_out_a, q.out_tma ? p.out : nullptr, p.T, p.H, p.V, na, p.f16)) != cudaSuccess) return e;
   if ((e = tmap_out_rows(&tm_out_b, q.out_tma ? p.out : nullptr, p.T, p.H, p.V, nb, p.f16)) != cudaSuccess) return e;
-  dim3 grid((unsigned)p.N, (unsigned)p.H);
+  // one CTA per (sequence, head), or per (piece row, head) -- pass 1 runs two per piece
+  const int64_t rows = p.piece_len > 0 ? (p.piece_pass1 ? 2 : 1) * (int64_t)p.piece_rows : p.N;
+  dim3 grid((unsigned)rows, (unsigned)p.H);
   if ((e = launch_kernel(kern, grid, dim3(kScanThreads), smem, stream, p.pdl != 0, q, tm_cs, tm_fin, tm_seg, tm_out_a,
                          tm_out_b)) != cudaSuccess)
     return e;

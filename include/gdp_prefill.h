@@ -200,6 +200,29 @@ int64_t gdp_ntdp_pad(int64_t T, int64_t N, int num_householder);
 size_t gdp_prefill_workspace_bytes(int64_t T, int64_t N, int H, int K, int V, int num_householder);
 
 /*
+ * How a call of this shape runs (shape-only, like the workspace size; no
+ * device access).  The scan of each (sequence, head) is a serial chain over
+ * its 64-row expanded chunks (Megatron-Core API page "core.ssm.ops.gdp.chunk",
+ * stage 3), so a call runs in one of three ways:
+ *   - plain: descriptors, WY, scan (3 launches);
+ *   - segmented (few long chains): the chunks in *segments of about 128, the
+ *     WY of segment k + 1 beside the scan of segment k (1 + 2 segments launches);
+ *   - split chains (few sequences, N <= 32, over few heads): every sequence
+ *     cut into pieces of *piece_chunks expanded chunks that run side by side.
+ *     The recurrence is affine in the state, S' = S Phi + B, so a first scan
+ *     pass finds each piece's B (from a zero state) and Phi (from the identity
+ *     with V = 0), a combine kernel chains the pieces' entering states, and a
+ *     second scan pass runs every piece from its own (5 launches).
+ *     *piece_rows bounds the number of pieces.  The results agree with the
+ *     plain form to rounding (fp32 state arithmetic in a different order).
+ * Outputs (any may be NULL): segments (1 unless segmented), piece_chunks (0
+ * unless split), piece_rows, launches (kernels one call enqueues; 0 for
+ * N = 0).  GDP_ERR_INVALID_ARG for an invalid shape.
+ */
+gdp_status gdp_prefill_plan(int64_t T, int64_t N, int H, int K, int V, int num_householder, int64_t *segments,
+                            int64_t *piece_chunks, int64_t *piece_rows, int64_t *launches);
+
+/*
  * The prefill forward pass: enqueue descriptors (unless prebuilt), the prep
  * + WY kernel and the state-scan / output kernel on `stream`.
  * Returns GDP_OK once enqueued.
@@ -210,7 +233,8 @@ gdp_status gdp_prefill_varlen(const gdp_prefill_args *args, void *stream);
  * Same as gdp_prefill_varlen, and records `events` (cudaEvent_t handles
  * created by the caller with timing enabled) on `stream` around the stages:
  * events[0] before the descriptor kernel, [1] after it, [2] after the WY
- * kernel, [3] after the scan/output kernel.  num_events must be 4.  Used by
+ * kernel, [3] after the scan/output kernel (in a split-chains call, after
+ * its two scan passes and the combine kernel).  num_events must be 4.  Used by
  * the bench to time each kernel on its own stream; the results are identical
  * to gdp_prefill_varlen.
  */

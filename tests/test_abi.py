@@ -190,3 +190,42 @@ def test_backward_workspace_covers_forward():
     for shape in [(1421, 4, 8, 128, 128, 2), (65536, 1, 32, 128, 128, 2), (256, 1, 2, 64, 64, 1)]:
         assert pkg.gdp_backward_workspace_bytes(*shape) > pkg.gdp_prefill_workspace_bytes(*shape) > 0
     assert pkg.gdp_backward_workspace_bytes(10, 1, 1, 64, 64, 0) == 0
+
+
+def test_prefill_plan(lib):
+    """The shape-only plan: plain, segmented or split chains, and the launches each enqueues."""
+    plain = pkg.gdp_prefill_plan(256, 1, 2, 64, 64, 1)  # four chunks: nothing to split
+    assert plain == {"segments": 1, "piece_chunks": 0, "piece_rows": 0, "launches": 3}
+    split = pkg.gdp_prefill_plan(1421, 4, 8, 128, 128, 2)  # 4 sequences x 8 heads
+    assert split["segments"] == 1 and split["piece_chunks"] == 6 and split["launches"] == 5
+    assert split["piece_rows"] * 8 <= 128
+    assert pkg.gdp_prefill_plan(32768, 8, 16, 128, 128, 3)["piece_chunks"] == 0  # 128 chains fill the GPU
+    seg = pkg.gdp_prefill_plan(65536, 1, 32, 128, 128, 2)
+    assert seg["segments"] == 16 and seg["piece_chunks"] == 0 and seg["launches"] == 33
+    assert pkg.gdp_prefill_plan(5000, 33, 1, 64, 64, 2)["piece_chunks"] == 0  # more than 32 sequences
+    assert pkg.gdp_prefill_plan(0, 0, 4, 64, 64, 2)["launches"] == 0
+    with pytest.raises(pkg.GdpError):
+        pkg.gdp_prefill_plan(10, 1, 1, 64, 64, 0)
+    # a split call needs workspace for the pieces' B, Phi and entering states
+    assert (pkg.gdp_prefill_workspace_bytes(1421, 4, 8, 128, 128, 2)
+            >= 3 * split["piece_rows"] * 8 * 128 * 128 * 4)
+
+
+@pytest.mark.parametrize("T,N,H,M", [(1421, 4, 8, 2), (3000, 1, 1, 1), (1143, 4, 2, 3), (5000, 32, 1, 2),
+                                     (700, 3, 4, 4)])
+def test_piece_rows_bound_every_length_mix(lib, T, N, H, M):
+    """The kernels number pieces row by row up to piece_rows: for any split of T tokens over N
+    sequences, sum_i max(1, ceil(ceil(L_i M / 64) / len)) stays within that bound."""
+    import numpy as np
+    plan = pkg.gdp_prefill_plan(T, N, H, 64, 64, M)
+    ln, rows = plan["piece_chunks"], plan["piece_rows"]
+    assert ln > 0 and rows * H <= 128
+    rng = np.random.default_rng(T + N)
+    mixes = [np.full(N, T // N) + (np.arange(N) < T % N), np.eye(N, dtype=int)[0] * T]
+    for _ in range(200):
+        cuts = np.sort(rng.integers(0, T + 1, N - 1))
+        mixes.append(np.diff(np.concatenate([[0], cuts, [T]])))
+    for L in mixes:
+        assert L.sum() == T and (L >= 0).all()
+        pieces = sum(max(1, -(-(-(-int(x) * M // 64)) // ln)) for x in L)
+        assert pieces <= rows, (list(L), pieces, rows)
