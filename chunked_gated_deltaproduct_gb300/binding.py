@@ -96,6 +96,10 @@ def load_library(path: str | None = None):
     lib.gdp_backward_workspace_bytes.argtypes = [_i64, _i64, _int, _int, _int, _int]
     lib.gdp_prefill_workspace_bytes.restype = _sz
     lib.gdp_prefill_workspace_bytes.argtypes = [_i64, _i64, _int, _int, _int, _int]
+    lib.gdp_prefill_transfer.restype = _int
+    lib.gdp_prefill_transfer.argtypes = [ctypes.POINTER(GdpPrefillArgs), _vp, _vp]
+    lib.gdp_chain_states.restype = _int
+    lib.gdp_chain_states.argtypes = [_vp, _vp, _vp, _i64, _i64, _int, _int, _vp, _vp, _vp]
     lib.gdp_prefill_plan.restype = _int
     lib.gdp_prefill_plan.argtypes = [_i64, _i64, _int, _int, _int, _int] + [ctypes.POINTER(_i64)] * 4
     lib.gdp_build_descriptors.restype = _int
@@ -439,3 +443,104 @@ def chunk_gated_delta_product(q, k, v, g=None, beta=None, cu_seqlens=None, num_h
     if output_final_state:
         return output, final
     return output
+
+
+# ---- sequence-sharded prefill by state passing ----------------------------------------------
+
+def gdp_prefill_transfer(args: GdpPrefillArgs, pairs: int, stream: int | None = None) -> None:
+    """Enqueue the transfer pairs (B, Phi) of every sequence of ``args`` into ``pairs``."""
+    lib = load_library()
+    st = lib.gdp_prefill_transfer(ctypes.byref(args), ctypes.c_void_p(pairs), ctypes.c_void_p(_stream(stream)))
+    if st != GDP_OK:
+        raise GdpError(st, lib.gdp_last_error().decode())
+
+
+def gdp_chain_states(s0, phi, b, steps: int, N: int, H: int, d: int, s_out, device_status=None,
+                     stream: int | None = None) -> None:
+    """Enqueue S_{j+1} = S_j Phi_j + B_j (j < steps) from S_0 = s0 (None: zero) into s_out."""
+    lib = load_library()
+    st = lib.gdp_chain_states(_ptr(s0), _ptr(phi), _ptr(b), steps, N, H, d, _ptr(s_out), _ptr(device_status),
+                              ctypes.c_void_p(_stream(stream)))
+    if st != GDP_OK:
+        raise GdpError(st, lib.gdp_last_error().decode())
+
+
+def chunk_gated_delta_product_transfer(q, k, v, g=None, beta=None, cu_seqlens=None, num_householder=1, scale=None,
+                                       use_qk_l2norm_in_kernel=False, workspace=None, device_status=None,
+                                       stream=None, g_is_alpha=False):
+    """The transfer pairs of a shard: returns ``pairs`` [2, N, H, V, K] fp32 with pairs[0] = B (the
+    state after each sequence from a zero state) and pairs[1] = Phi (from the identity with v = 0),
+    so that the final state from any initial state S_0 is S_0 @ Phi + B.  Inputs as for
+    chunk_gated_delta_product."""
+    if cu_seqlens is None:
+        raise GdpError(GDP_ERR_INVALID_ARG, "cu_seqlens is required (packed THD input only)")
+    T, K = q.shape[0], q.shape[2]
+    H = max(q.shape[1], v.shape[1])
+    V = v.shape[-1]
+    M = int(num_householder)
+    N = cu_seqlens.numel() - 1
+    pairs = torch.empty((2, N, H, V, K), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(T, N, H, K, V, M, q.device)
+    a = make_args(q, k, v, g, beta, cu_seqlens, M, scale, None, None, None, None, None, None, None, None, None,
+                  None, None, use_qk_l2norm_in_kernel, workspace, device_status, g_is_alpha)
+    gdp_prefill_transfer(a, pairs.data_ptr(), stream)
+    return pairs
+
+
+def chain_states(s0, phi, b, device_status=None, stream=None):
+    """S_out [steps+1, N, H, d, d] with S_out[0] = s0 (None: zero), S_out[j+1] = S_out[j] @ phi[j] + b[j]."""
+    steps, N, H, d = phi.shape[0], phi.shape[1], phi.shape[2], phi.shape[-1]
+    for x in (phi, b) + ((s0,) if s0 is not None else ()):
+        if x.dtype != torch.float32 or not x.is_contiguous():
+            raise GdpError(GDP_ERR_INVALID_ARG, "chain_states takes contiguous fp32 tensors")
+    s_out = torch.empty((steps + 1, N, H, d, d), dtype=torch.float32, device=phi.device)
+    gdp_chain_states(s0, phi, b, steps, N, H, d, s_out, device_status, stream)
+    return s_out
+
+
+def gather_transfer_pairs(pairs, group=None):
+    """All ranks' transfer pairs in rank order: [R, 2, N, H, V, K] (the one exchange of the
+    sequence-sharded prefill; any torch.distributed backend)."""
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    out = [torch.empty_like(pairs) for _ in range(world)]
+    dist.all_gather(out, pairs.contiguous(), group=group)
+    return torch.stack(out)
+
+
+def sequence_parallel_steps(transfer, chain, run, initial_state, group=None):
+    """The host logic of the sequence-sharded prefill over its three device steps:
+    ``transfer()`` gives this rank's pairs [2, N, H, V, K], the pairs of all ranks are
+    all-gathered, ``chain(s0, phi, b)`` ([steps + 1, ...]) chains those of the ranks before this
+    one onto ``initial_state``, and ``run(s_in)`` runs the shard from the result."""
+    import torch.distributed as dist
+    rank = dist.get_rank(group)
+    allp = gather_transfer_pairs(transfer(), group)  # [R, 2, N, H, V, K]
+    if rank == 0:
+        return run(initial_state)
+    s0 = None if initial_state is None else initial_state.to(torch.float32).contiguous()
+    return run(chain(s0, allp[:rank, 1].contiguous(), allp[:rank, 0].contiguous())[rank])
+
+
+def chunk_gated_delta_product_sequence_parallel(q, k, v, g=None, beta=None, cu_seqlens=None, num_householder=1,
+                                                scale=None, initial_state=None, use_qk_l2norm_in_kernel=False,
+                                                return_chunk_states=False, group=None, g_is_alpha=False):
+    """Prefill of sequences whose tokens are split over the ranks of ``group`` in rank order:
+    this rank holds every sequence's shard r (consecutive whole tokens; empty shards allowed),
+    packed with its own ``cu_seqlens``.  ``initial_state`` [N, H, V, K] is the state before
+    shard 0 (the same on every rank, or None).  Each rank computes its shard's transfer pairs on
+    the GPU, the pairs are all-gathered (the one exchange), each rank chains the pairs of the ranks
+    before it onto the initial state (GPU) and runs its shard from there (GPU).  Returns
+    ``(o, final_state)`` (``chunk_states`` third when asked): final_state is the state after this
+    rank's shard, the sequence's final state on the last rank; chunk-state rows are per shard."""
+    def transfer():
+        return chunk_gated_delta_product_transfer(q, k, v, g, beta, cu_seqlens, num_householder, scale,
+                                                  use_qk_l2norm_in_kernel, g_is_alpha=g_is_alpha)
+
+    def run(s_in):
+        return chunk_gated_delta_product(q, k, v, g, beta, cu_seqlens, num_householder, scale, initial_state=s_in,
+                                         output_final_state=True, use_qk_l2norm_in_kernel=use_qk_l2norm_in_kernel,
+                                         return_chunk_states=return_chunk_states, g_is_alpha=g_is_alpha)
+
+    return sequence_parallel_steps(transfer, chain_states, run, initial_state, group)

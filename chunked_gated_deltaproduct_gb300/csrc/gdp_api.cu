@@ -188,9 +188,11 @@ struct Recompute {
   float *final_state;
 };
 
-// Checks + launches shared by gdp_prefill_varlen, its profiled form and the backward pass.
+// Checks + launches shared by gdp_prefill_varlen, its profiled form, the backward pass and the
+// transfer pairs (xfer_out != NULL: B and Phi of every sequence into xfer_out, [2][N][H][V][K];
+// output, output_state, chunk_states, initial_state and the state cache are ignored).
 gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t const *ev,
-                   const Recompute *rc = nullptr) {
+                   const Recompute *rc = nullptr, float *xfer_out = nullptr) {
   g_last_error[0] = 0;
   if (!a) return fail(GDP_ERR_INVALID_ARG, "args is NULL");
   const int64_t T = a->T, N = a->N;
@@ -201,7 +203,7 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
   if (K != V || (K != 64 && K != 128))
     return fail(GDP_ERR_UNSUPPORTED, "head sizes K=%d V=%d: this build serves K == V in {64, 128}", K, V);
   if (!a->cu_seqlens && N > 0) return fail(GDP_ERR_INVALID_ARG, "cu_seqlens is NULL");
-  if (T > 0 && (!a->q || !a->k || !a->v || (!a->output && !rc)))
+  if (T > 0 && (!a->q || !a->k || !a->v || (!a->output && !rc && !xfer_out)))
     return fail(GDP_ERR_INVALID_ARG, "q, k, v and output are required");
   gdp::Problem p{};
   gdp_status vst = gdp::resolve_variants(a, &p);
@@ -308,12 +310,26 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
   p.seg_rows = 0;
   p.seg_state = nullptr;
   p.prefetch = (N * (int64_t)H <= gdp::kSegMaxChains) ? 1 : 0;
-  const int nseg = seg_count(T, N, H, M);
-  const PiecePlan pp = piece_plan(T, N, H, M);
+  // a transfer-pair call runs whole sequences in one segment
+  const int nseg = xfer_out ? 1 : seg_count(T, N, H, M);
+  const PiecePlan pp = xfer_out ? PiecePlan{0, 0} : piece_plan(T, N, H, M);
   p.piece_len = (int)pp.len;
   p.piece_rows = (int)pp.rows;
   p.piece_pass1 = 0;
   p.piece_buf = pp.len > 0 ? (float *)(ws + lay.piece) : nullptr;
+  p.xfer = 0;
+  p.xfer_out = nullptr;
+  if (xfer_out) {  // B (rows 0 .. N-1) and Phi (rows N .. 2N-1) of every sequence, no outputs
+    p.xfer = 1;
+    p.xfer_out = xfer_out;
+    p.out = nullptr;
+    p.out_state = nullptr;
+    p.chunk_states = nullptr;
+    p.init = nullptr;
+    p.cache = nullptr;
+    p.slots = nullptr;
+    p.num_slots = 0;
+  }
   // desc -> WY -> scan on one stream overlap their launches (programmatic dependent launch);
   // the profiled form records events between them, so there each kernel runs alone
   p.pdl = (nseg == 1 && !ev) ? 1 : 0;
@@ -448,6 +464,36 @@ GDP_EXPORT gdp_status gdp_build_descriptors(const void *cu_seqlens, int cu_seqle
 
 GDP_EXPORT gdp_status gdp_prefill_varlen(const gdp_prefill_args *a, void *stream) {
   return prefill(a, (cudaStream_t)stream, nullptr);
+}
+
+GDP_EXPORT gdp_status gdp_prefill_transfer(const gdp_prefill_args *a, float *pairs, void *stream) {
+  g_last_error[0] = 0;
+  if (!a) return fail(GDP_ERR_INVALID_ARG, "args is NULL");
+  if (a->N > 0 && !pairs) return fail(GDP_ERR_INVALID_ARG, "pairs is NULL");
+  if (((uintptr_t)pairs & 15u) != 0) return fail(GDP_ERR_INVALID_ARG, "pairs must be 16-byte aligned");
+  if (a->N > 0 && a->H > 0 && 2 * a->N * (int64_t)a->H * a->V > INT32_MAX)
+    return fail(GDP_ERR_UNSUPPORTED, "transfer pairs above 2^31 rows of K floats");
+  return prefill(a, (cudaStream_t)stream, nullptr, nullptr, pairs);
+}
+
+GDP_EXPORT gdp_status gdp_chain_states(const float *s0, const float *phi, const float *b, int64_t steps, int64_t N,
+                                       int H, int d, float *s_out, uint32_t *device_status, void *stream) {
+  g_last_error[0] = 0;
+  if (steps < 0 || N < 0 || H < 1 || (d != 64 && d != 128))
+    return fail(GDP_ERR_INVALID_ARG, "bad shape steps=%lld N=%lld H=%d d=%d (d is 64 or 128)", (long long)steps,
+                (long long)N, H, d);
+  if (N == 0) return GDP_OK;
+  if (!s_out || (steps > 0 && (!phi || !b))) return fail(GDP_ERR_INVALID_ARG, "s_out, phi and b are required");
+  if ((((uintptr_t)s0 | (uintptr_t)phi | (uintptr_t)b | (uintptr_t)s_out) & 15u) != 0)
+    return fail(GDP_ERR_INVALID_ARG, "state buffers must be 16-byte aligned");
+  const size_t one = sizeof(float) * (size_t)N * H * (size_t)d * d;
+  if (steps * N * (int64_t)H * d > INT32_MAX) return fail(GDP_ERR_UNSUPPORTED, "Phi above 2^31 rows of d floats");
+  if (overlaps(s_out, one * (size_t)(steps + 1), s0, one) || overlaps(s_out, one * (size_t)(steps + 1), phi, one * steps) ||
+      overlaps(s_out, one * (size_t)(steps + 1), b, one * steps))
+    return fail(GDP_ERR_ALIAS, "s_out must not overlap s0, phi or b");
+  cudaError_t e = gdp::launch_chain_states(s0, phi, b, steps, N, H, d, s_out, device_status, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "chain kernel: %s", cudaGetErrorString(e));
+  return GDP_OK;
 }
 
 namespace {

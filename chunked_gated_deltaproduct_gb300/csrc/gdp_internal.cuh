@@ -148,6 +148,12 @@ struct Problem {
   // piece_buf: [3 piece_rows][H][V][K] fp32.
   int piece_len, piece_rows, piece_pass1;
   float *piece_buf;
+  // Transfer pair of every sequence (xfer = 1; no pieces, one segment): grid row i < N runs
+  // sequence i from a zero state, row N + i from the identity with V = 0, each writing its end
+  // state (B_i, Phi_i: S_end = S_0 Phi_i + B_i for any S_0) to xfer_out row (grid row); no
+  // outputs.  xfer_out: [2][N][H][V][K] fp32.
+  int xfer;
+  float *xfer_out;
 };
 
 // Everything the backward kernels need about one call (gdp_backward.cu).  Heads are
@@ -295,6 +301,10 @@ cudaError_t launch_scan(const Problem &p, cudaStream_t stream);
 cudaError_t launch_scan_variant(const Problem &p, cudaStream_t stream, bool f16, bool init16);
 // Split chains: the entering state of every piece of a split sequence (gdp_pieces.cu).
 cudaError_t launch_piece_combine(const Problem &p, cudaStream_t stream);
+// S_{j+1} = S_j Phi_j + B_j for j < steps from S_0 (NULL: zero), Phi / B [steps][N][H][d][d],
+// S_out [steps + 1][N][H][d][d] (S_out[0] = S_0) (gdp_pieces.cu).
+cudaError_t launch_chain_states(const float *s0, const float *phi, const float *b, int64_t steps, int64_t N, int H,
+                                int d, float *s_out, uint32_t *status, cudaStream_t stream);
 
 // TMA tensor maps (gdp_tmap.cu; `map` points at a 64-byte aligned CUtensorMap; a NULL base
 // leaves it zeroed).  All use the 128-byte swizzle.

@@ -54,97 +54,69 @@ __host__ inline size_t cmb_smem(int d) {
   return need > kCmbMinSmem ? need : kCmbMinSmem;
 }
 
-// Step j: S_in(j + 1) = S_in(j) Phi_j + B_j on warp-level tf32 MMAs with the 3xTF32 split
-// (hi hi + lo hi + hi lo: about fp32 accuracy, since the product replaces the whole state
-// every step).  Warp w owns columns [w D / 8, (w + 1) D / 8) of the CTA's 16 rows: NT n-tiles
-// of 8, with separate accumulators per split term and k-step parity (independent MMA chains),
-// summed with B_j at the end.  Thread 0 brings Phi_j (tensor boxes) and B_j (one bulk copy)
-// in two steps ahead.  (Sharing Phi_j among the row blocks of a (sequence, head) by cluster
-// multicast was slower: clusters of 8 whole-SM CTAs start later.)
+// One chain of steps for a CTA's 16 state rows: S_{j+1} = S_j Phi_j + B_j for j < steps.
+// Pointers are already offset to the CTA's rows.
+struct ChainRows {
+  int steps;
+  int64_t phi_row0, phi_row_step;  // first row of Phi_j in the tensor map: phi_row0 + j phi_row_step
+  const float *b0;                 // B_j's rows: b0 + j b_step
+  int64_t b_step;
+  float *s0;                       // S_j's rows (j = 0 .. steps): s0 + j s_step
+  int64_t s_step;
+  const float *src;                // S_0's rows, fp32, or
+  const __nv_bfloat16 *src16;      // bf16; both NULL: zero
+};
+
+// The steps on warp-level tf32 MMAs with the 3xTF32 split (hi hi + lo hi + hi lo: about fp32
+// accuracy, since the product replaces the whole state every step).  Warp w owns columns
+// [w D / 8, (w + 1) D / 8) of the 16 rows: NT n-tiles of 8, with separate accumulators per split
+// term and k-step parity (independent MMA chains), summed with B_j at the end.  Thread 0 brings
+// Phi_j (tensor boxes) and B_j (one bulk copy) in two steps ahead.  (Sharing Phi_j among the row
+// blocks of a (sequence, head) by cluster multicast was slower: clusters of 8 whole-SM CTAs
+// start later.)  Called by all threads after the mbarriers are initialised and visible.
 template <int D, bool INIT16>
-__global__ void __launch_bounds__(kCmbThreads, 1) gdp_piece_combine_kernel(Problem p,
-                                                                        const __grid_constant__ CUtensorMap tm_phi) {
+__device__ __forceinline__ void run_chain(const ChainRows &c, const CUtensorMap *tm_phi, unsigned char *sm,
+                                          uint64_t *full, uint32_t *status) {
   constexpr int NT = D / 64, NB = D / 32, SP = D + 4;
   constexpr uint32_t PB = cmb_phi_bytes(D), BB = cmb_b_bytes(D), SF = cmb_s_floats(D);
-  extern __shared__ __align__(1024) unsigned char cmb_smem_raw[];
-  unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)cmb_smem_raw + 1023) & ~(uintptr_t)1023);
   float *bst = reinterpret_cast<float *>(sm + 2 * PB);  // B_j stages, [2][16][D]
-  float *sb = bst + 2 * BB / 4;                          // S_in(j): [buffer][hi, lo][16][D + 4]
-  __shared__ __align__(8) uint64_t full[2];
-  __shared__ int sh[2];
-  const int seq = blockIdx.x, h = blockIdx.y, r0 = kCmbRows * (int)blockIdx.z;
+  float *sb = bst + 2 * BB / 4;                          // S_j: [buffer][hi, lo][16][D + 4]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
-
-  // B and Phi come from the grid before; wait before any exit so that this grid's
-  // completion implies its predecessors'
-  sm100::pdl_wait();
-  sm100::pdl_trigger();
-  if (warp == 0) {
-    int first, np;
-    pieces_of_seq(p, seq, lane, &first, &np);
-    if (lane == 0) {
-      sh[0] = first;
-      sh[1] = np;
-    }
-  }
-  if (tid == 0) {
-    sm100::mbar_init(&full[0], 1);
-    sm100::mbar_init(&full[1], 1);
-    sm100::mbar_init_fence();
-  }
-  __syncthreads();
-  const int first = sh[0], np = sh[1];
-  if (np <= 1) return;  // one piece: the scan reads the caller's state itself
-  const int64_t KV = (int64_t)D * D, R = p.piece_rows;
-  auto rows_of = [&](int64_t prow) { return p.piece_buf + (prow * p.H + h) * KV; };
   int issued[2] = {0, 0};
-  auto issue = [&](int j) {  // Phi_j and B_j (rows r0 ..) into stage j % 2 (thread 0)
+  auto issue = [&](int j) {  // Phi_j and B_j into stage j % 2 (thread 0)
     const int sg = j & 1;
     unsigned char *dst = sm + sg * PB;
     sm100::mbar_arrive_expect_tx(&full[sg], PB + BB);
-    const int y0 = (int)(((R + first + j) * p.H + h) * D);  // Phi_j's first row in the map
+    const int y0 = (int)(c.phi_row0 + (int64_t)j * c.phi_row_step);
 #pragma unroll
     for (int kb = 0; kb < NB; ++kb)
 #pragma unroll
       for (int cb = 0; cb < NB; ++cb)
-        sm100::tma_load_2d(dst + (kb * NB + cb) * 4096, &tm_phi, 32 * cb, y0 + 32 * kb, &full[sg]);
-    sm100::bulk_g2s(bst + sg * (BB / 4), rows_of(first + j) + (int64_t)r0 * D, BB, &full[sg]);
+        sm100::tma_load_2d(dst + (kb * NB + cb) * 4096, tm_phi, 32 * cb, y0 + 32 * kb, &full[sg]);
+    sm100::bulk_g2s(bst + sg * (BB / 4), c.b0 + (int64_t)j * c.b_step, BB, &full[sg]);
     ++issued[sg];
   };
   if (tid == 0)
-    for (int j = 0; j < 2 && j + 1 < np; ++j) issue(j);
+    for (int j = 0; j < 2 && j < c.steps; ++j) issue(j);
 
-  // S_in(j) -> piece_buf row 2 R + first + j (fp32) and S buffer j % 2 (tf32 hi / lo)
+  // S_j -> global (fp32) and S buffer j % 2 (tf32 hi / lo)
   auto put2 = [&](int j, int row, int col, float x0, float x1) {
-    *reinterpret_cast<float2 *>(rows_of(2 * R + first + j) + (int64_t)(r0 + row) * D + col) = make_float2(x0, x1);
+    *reinterpret_cast<float2 *>(c.s0 + (int64_t)j * c.s_step + (int64_t)row * D + col) = make_float2(x0, x1);
     float *hi = sb + (j & 1) * 2 * SF, *lo = hi + SF;
     const float h0 = __uint_as_float(tf32r(x0)), h1 = __uint_as_float(tf32r(x1));
     *reinterpret_cast<float2 *>(hi + row * SP + col) = make_float2(h0, h1);
     *reinterpret_cast<float2 *>(lo + row * SP + col) =
         make_float2(__uint_as_float(tf32r(x0 - h0)), __uint_as_float(tf32r(x1 - h1)));
   };
-  {  // S_in(0): the caller's state (cache slot, dense fp32 / bf16, or zero)
-    const float *src = nullptr;
-    const __nv_bfloat16 *src16 = nullptr;
-    if (p.cache) {  // an out-of-range slot reads as no state (the scan reports it)
-      const int slot = p.slots[seq];
-      if (slot >= 0 && slot < p.num_slots) src = p.cache + ((int64_t)slot * p.H + h) * KV;
-    } else if (p.init) {
-      if constexpr (INIT16)
-        src16 = static_cast<const __nv_bfloat16 *>(p.init) + ((int64_t)seq * p.H + h) * KV;
-      else
-        src = static_cast<const float *>(p.init) + ((int64_t)seq * p.H + h) * KV;
+  for (int idx = tid; idx < kCmbRows * D / 2; idx += kCmbThreads) {  // S_0
+    const int row = idx / (D / 2), col = 2 * (idx % (D / 2));
+    const int64_t off = (int64_t)row * D + col;
+    float2 x = make_float2(0.f, 0.f);
+    if (c.src) x = *reinterpret_cast<const float2 *>(c.src + off);
+    if constexpr (INIT16) {
+      if (c.src16) x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(c.src16 + off));
     }
-    for (int idx = tid; idx < kCmbRows * D / 2; idx += kCmbThreads) {
-      const int row = idx / (D / 2), col = 2 * (idx % (D / 2));
-      const int64_t off = (int64_t)(r0 + row) * D + col;
-      float2 x = make_float2(0.f, 0.f);
-      if (src) x = *reinterpret_cast<const float2 *>(src + off);
-      if constexpr (INIT16) {
-        if (src16) x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(src16 + off));
-      }
-      put2(0, row, col, x.x, x.y);
-    }
+    put2(0, row, col, x.x, x.y);
   }
   // per-thread parts of the B-fragment offsets (floats) inside a stage: column c = n0 + g of
   // n-tile n0 sits in box column c / 32, chunk (c % 32) / 4, at (c % 4); rows k0 + t and
@@ -160,9 +132,9 @@ __global__ void __launch_bounds__(kCmbThreads, 1) gdp_piece_combine_kernel(Probl
   }
   bool ok = true;
 #pragma unroll 1
-  for (int j = 0; j + 1 < np; ++j) {
+  for (int j = 0; j < c.steps; ++j) {
     const int sg = j & 1;
-    // also publishes S_in(j) (written before this point)
+    // also publishes S_j (written before this point)
     ok = __syncthreads_and(sm100::mbar_wait(&full[sg], (uint32_t)((j >> 1) & 1)));
     if (!ok) break;
     const float *phi = reinterpret_cast<const float *>(sm + sg * PB);
@@ -197,25 +169,115 @@ __global__ void __launch_bounds__(kCmbThreads, 1) gdp_piece_combine_kernel(Probl
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int c = warp * 8 * NT + 8 * nt + 2 * t;
-      const float2 u0 = *reinterpret_cast<const float2 *>(bj + g * D + c);
-      const float2 u1 = *reinterpret_cast<const float2 *>(bj + (g + 8) * D + c);
+      const int col = warp * 8 * NT + 8 * nt + 2 * t;
+      const float2 u0 = *reinterpret_cast<const float2 *>(bj + g * D + col);
+      const float2 u1 = *reinterpret_cast<const float2 *>(bj + (g + 8) * D + col);
       float y[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q)  // small terms first
         y[q] = ((acc[0][nt][1][q] + acc[1][nt][1][q]) + (acc[0][nt][2][q] + acc[1][nt][2][q])) +
                (acc[0][nt][0][q] + acc[1][nt][0][q]);
-      put2(j + 1, g, c, y[0] + u0.x, y[1] + u0.y);
-      put2(j + 1, g + 8, c, y[2] + u1.x, y[3] + u1.y);
+      put2(j + 1, g, col, y[0] + u0.x, y[1] + u0.y);
+      put2(j + 1, g + 8, col, y[2] + u1.x, y[3] + u1.y);
     }
     __syncthreads();  // stage sg and S buffer j % 2 are consumed
-    if (tid == 0 && j + 3 < np) issue(j + 2);
+    if (tid == 0 && j + 2 < c.steps) issue(j + 2);
   }
   if (!ok && tid == 0) {
-    set_status(p.status, GDP_DEV_ERR_TIMEOUT);
+    set_status(status, GDP_DEV_ERR_TIMEOUT);
     for (int sg = 0; sg < 2; ++sg)  // bounded: the last copies issued on each stage have landed
       if (issued[sg] > 0) sm100::mbar_wait(&full[sg], (uint32_t)((issued[sg] - 1) & 1));
   }
+}
+
+__device__ __forceinline__ unsigned char *cmb_smem_base() {
+  extern __shared__ __align__(1024) unsigned char cmb_smem_raw[];
+  return reinterpret_cast<unsigned char *>(((uintptr_t)cmb_smem_raw + 1023) & ~(uintptr_t)1023);
+}
+
+// Split chains: the pieces of sequence blockIdx.x, head blockIdx.y, state rows 16 blockIdx.z ..:
+// S_in(0) is the caller's state (cache slot, dense fp32 / bf16, or zero), S_in(j) goes to
+// piece_buf row 2 piece_rows + first + j, Phi_j / B_j come from rows piece_rows + first + j / first + j.
+template <int D, bool INIT16>
+__global__ void __launch_bounds__(kCmbThreads, 1) gdp_piece_combine_kernel(Problem p,
+                                                                        const __grid_constant__ CUtensorMap tm_phi) {
+  __shared__ __align__(8) uint64_t full[2];
+  __shared__ int sh[2];
+  const int seq = blockIdx.x, h = blockIdx.y, r0 = kCmbRows * (int)blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // B and Phi come from the grid before; wait before any exit so that this grid's
+  // completion implies its predecessors'
+  sm100::pdl_wait();
+  sm100::pdl_trigger();
+  if (warp == 0) {
+    int first, np;
+    pieces_of_seq(p, seq, lane, &first, &np);
+    if (lane == 0) {
+      sh[0] = first;
+      sh[1] = np;
+    }
+  }
+  if (tid == 0) {
+    sm100::mbar_init(&full[0], 1);
+    sm100::mbar_init(&full[1], 1);
+    sm100::mbar_init_fence();
+  }
+  __syncthreads();
+  const int first = sh[0], np = sh[1];
+  if (np <= 1) return;  // one piece: the scan reads the caller's state itself
+  const int64_t KV = (int64_t)D * D, R = p.piece_rows, step = (int64_t)p.H * KV;
+  auto rows_of = [&](int64_t prow) { return p.piece_buf + (prow * p.H + h) * KV + (int64_t)r0 * D; };
+  ChainRows c{};
+  c.steps = np - 1;
+  c.phi_row0 = ((R + first) * p.H + h) * D;
+  c.phi_row_step = (int64_t)p.H * D;
+  c.b0 = rows_of(first);
+  c.b_step = step;
+  c.s0 = rows_of(2 * R + first);
+  c.s_step = step;
+  if (p.cache) {  // an out-of-range slot reads as no state (the scan reports it)
+    const int slot = p.slots[seq];
+    if (slot >= 0 && slot < p.num_slots) c.src = p.cache + ((int64_t)slot * p.H + h) * KV + (int64_t)r0 * D;
+  } else if (p.init) {
+    if constexpr (INIT16)
+      c.src16 = static_cast<const __nv_bfloat16 *>(p.init) + ((int64_t)seq * p.H + h) * KV + (int64_t)r0 * D;
+    else
+      c.src = static_cast<const float *>(p.init) + ((int64_t)seq * p.H + h) * KV + (int64_t)r0 * D;
+  }
+  run_chain<D, INIT16>(c, &tm_phi, cmb_smem_base(), full, p.status);
+}
+
+// The general chain (gdp_chain_states): sequence blockIdx.x, head blockIdx.y, rows 16 blockIdx.z ..;
+// Phi / B / S_out indexed [step][N][H][D][D].
+struct ChainArgs {
+  const float *s0, *b;
+  float *s_out;
+  int64_t steps, N;
+  int H;
+  uint32_t *status;
+};
+template <int D>
+__global__ void __launch_bounds__(kCmbThreads, 1) gdp_chain_states_kernel(ChainArgs a,
+                                                                       const __grid_constant__ CUtensorMap tm_phi) {
+  __shared__ __align__(8) uint64_t full[2];
+  const int seq = blockIdx.x, h = blockIdx.y, r0 = kCmbRows * (int)blockIdx.z;
+  if (threadIdx.x == 0) {
+    sm100::mbar_init(&full[0], 1);
+    sm100::mbar_init(&full[1], 1);
+    sm100::mbar_init_fence();
+  }
+  __syncthreads();
+  const int64_t KV = (int64_t)D * D, step = a.N * a.H * KV, base = ((int64_t)seq * a.H + h) * KV + (int64_t)r0 * D;
+  ChainRows c{};
+  c.steps = (int)a.steps;
+  c.phi_row0 = ((int64_t)seq * a.H + h) * D;
+  c.phi_row_step = a.N * a.H * D;
+  c.b0 = a.b + base;
+  c.b_step = step;
+  c.s0 = a.s_out + base;
+  c.s_step = step;
+  c.src = a.s0 ? a.s0 + base : nullptr;
+  run_chain<D, false>(c, &tm_phi, cmb_smem_base(), full, a.status);
 }
 
 template <int D, bool INIT16>
@@ -232,7 +294,29 @@ cudaError_t launch_combine_d(const Problem &p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <int D>
+cudaError_t launch_chain_d(const ChainArgs &a, const float *phi, cudaStream_t stream) {
+  const size_t smem = cmb_smem(D);
+  cudaError_t e = cudaFuncSetAttribute(gdp_chain_states_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  alignas(64) CUtensorMap tm_phi;  // Phi, [steps][N][H][D][D] fp32, 32 x 32 boxes
+  if ((e = tmap_state(&tm_phi, const_cast<float *>(phi), a.steps * a.N * a.H * D, D)) != cudaSuccess) return e;
+  gdp_chain_states_kernel<D><<<dim3((unsigned)a.N, (unsigned)a.H, (unsigned)(D / kCmbRows)), kCmbThreads, smem,
+                               stream>>>(a, tm_phi);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_chain_states(const float *s0, const float *phi, const float *b, int64_t steps, int64_t N, int H,
+                                int d, float *s_out, uint32_t *status, cudaStream_t stream) {
+  if (N == 0) return cudaSuccess;
+  const ChainArgs a{s0, b, s_out, steps, N, H, status};
+  if (d == 64) return launch_chain_d<64>(a, phi, stream);
+  if (d == 128) return launch_chain_d<128>(a, phi, stream);
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_piece_combine(const Problem &p, cudaStream_t stream) {
   if (p.N == 0 || p.piece_len <= 0) return cudaSuccess;

@@ -130,9 +130,10 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
   const int h = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // split chains: this CTA's piece (pass 1: grid row r and piece_rows + r run the same piece)
-  const bool pieces = p.piece_len > 0, pass1 = pieces && p.piece_pass1;
-  const bool transfer = pass1 && (int)blockIdx.x >= p.piece_rows;  // from the identity, V = 0
-  int seq = blockIdx.x, pc_i = 0, pc_n = 1;
+  const bool pieces = p.piece_len > 0, pass1 = pieces && p.piece_pass1, xfer = p.xfer != 0;
+  // from the identity with V = 0: the second half of the rows of a pass 1 or a transfer-pair launch
+  const bool transfer = (pass1 && (int)blockIdx.x >= p.piece_rows) || (xfer && (int64_t)blockIdx.x >= p.N);
+  int seq = (xfer && transfer) ? (int)(blockIdx.x - p.N) : (int)blockIdx.x, pc_i = 0, pc_n = 1;
   if (pieces) {
     // the piece table comes from the descriptors; every CTA waits for its predecessor grid
     // before it may exit, so that this grid's completion implies the predecessors'
@@ -182,7 +183,7 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
   if (p.cache) {
     slot = p.slots[seq];
     if (slot < -1 || slot >= p.num_slots) {
-      if (tid == 0 && p.seg_lo == 0 && !pass1 && pc_i == 0) set_status(p.status, GDP_DEV_ERR_SLOT);
+      if (tid == 0 && p.seg_lo == 0 && !pass1 && !xfer && pc_i == 0) set_status(p.status, GDP_DEV_ERR_SLOT);
       slot = -1;
     }
     if (slot >= 0) src = p.cache + ((int64_t)slot * H + h) * (int64_t)V * d;
@@ -192,8 +193,9 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
     else
       src = static_cast<const float *>(p.init) + ((int64_t)seq * H + h) * (int64_t)V * d;
   }
-  if (pass1 || pc_n > 1) {  // pass 1 starts from zero (or the identity); a split piece from its S_in
-    src = pass1 ? nullptr : p.piece_buf + ((int64_t)(2 * p.piece_rows + (int)blockIdx.x) * H + h) * (int64_t)V * d;
+  if (pass1 || xfer || pc_n > 1) {  // zero (or the identity) for B / Phi; a split piece from its S_in
+    src = (pass1 || xfer) ? nullptr
+                          : p.piece_buf + ((int64_t)(2 * p.piece_rows + (int)blockIdx.x) * H + h) * (int64_t)V * d;
     if constexpr (INIT16) src16 = nullptr;
   }
 
@@ -491,7 +493,7 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
     if (!abort_flag && has_rows) {  // the last chunk's b2_done was waited for above
       int64_t r = -1;
       const CUtensorMap *tm = &tm_fin;
-      if (pass1) {  // B or Phi of the piece (piece_buf through the segment map)
+      if (pass1 || xfer) {  // B or Phi of the piece / sequence (piece_buf or xfer_out: the segment map)
         r = ((int64_t)blockIdx.x * H + h) * V;
         tm = &tm_seg;
       } else if (!last_seg) {  // carried to the next segment (a split piece leaves nothing)
@@ -604,6 +606,8 @@ cudaError_t launch_scan_kernel(Kern kern, const Problem &p, cudaStream_t stream)
   if (e != cudaSuccess) return e;
   if (p.piece_len > 0)  // the piece states (pass 1 writes B and Phi through it)
     e = tmap_state(&tm_seg, p.piece_buf, 3 * (int64_t)p.piece_rows * hv, p.K);
+  else if (p.xfer)  // the transfer pairs
+    e = tmap_state(&tm_seg, p.xfer_out, 2 * p.N * hv, p.K);
   else
     e = tmap_state(&tm_seg, p.seg_state, p.N * hv, p.K);
   if (e != cudaSuccess) return e;
@@ -615,7 +619,7 @@ cudaError_t launch_scan_kernel(Kern kern, const Problem &p, cudaStream_t stream)
   if ((e = tmap_out_rows(&tm_out_a, q.out_tma ? p.out : nullptr, p.T, p.H, p.V, na, p.f16)) != cudaSuccess) return e;
   if ((e = tmap_out_rows(&tm_out_b, q.out_tma ? p.out : nullptr, p.T, p.H, p.V, nb, p.f16)) != cudaSuccess) return e;
   // one CTA per (sequence, head), or per (piece row, head) -- pass 1 runs two per piece
-  const int64_t rows = p.piece_len > 0 ? (p.piece_pass1 ? 2 : 1) * (int64_t)p.piece_rows : p.N;
+  const int64_t rows = p.piece_len > 0 ? (p.piece_pass1 ? 2 : 1) * (int64_t)p.piece_rows : (p.xfer ? 2 : 1) * p.N;
   dim3 grid((unsigned)rows, (unsigned)p.H);
   if ((e = launch_kernel(kern, grid, dim3(kScanThreads), smem, stream, p.pdl != 0, q, tm_cs, tm_fin, tm_seg, tm_out_a,
                          tm_out_b)) != cudaSuccess)

@@ -242,6 +242,39 @@ gdp_status gdp_prefill_varlen_profiled(const gdp_prefill_args *args, void *strea
                                        int num_events);
 
 /*
+ * Sequence-sharded prefill by state passing (blog post "Attention Cache and
+ * Sequence Parallelism", section on passing state instead of KV): when the
+ * tokens of a sequence are split over ranks, the state the previous ranks
+ * leave is the next rank's initial state.  Over a shard the state map is
+ * affine, S_end = S_0 Phi + B (the decay and the delta-rule updates of the
+ * FlashInfer page's display equation, right-multiplying the V-major state),
+ * so every rank finds its (B, Phi) at once, the pairs are exchanged, and each
+ * rank chains those of the ranks before it into its initial state.
+ *
+ * gdp_prefill_transfer: for every sequence i and head h of args (the shard,
+ * packed as for gdp_prefill_varlen), pairs[0][i][h] = B (the state after the
+ * sequence from a zero state) and pairs[1][i][h] = Phi (the state after it
+ * from the identity with v = 0), each [V][K] fp32: the final state from any
+ * S_0 is S_0 Phi + B.  pairs: [2][N][H][V][K] fp32 device memory, 16-byte
+ * aligned, written whole (B = 0, Phi = I for an empty sequence).  Needs
+ * q, k, v, g, beta, cu_seqlens, the workspace and the scalars of args;
+ * output, output_state, chunk_states, initial_state and the state cache are
+ * ignored.  Runs whole sequences in one segment (no split chains).  Errors
+ * as gdp_prefill_varlen.
+ *
+ * gdp_chain_states: S_{j+1} = S_j Phi_j + B_j for j < steps, per (sequence,
+ * head), from S_0 = s0 (NULL: zero).  phi, b: [steps][N][H][d][d] fp32 (the
+ * pairs of consecutive shards in order), s_out: [steps + 1][N][H][d][d] fp32,
+ * s_out[0] = S_0; d is 64 or 128; all device pointers, 16-byte aligned;
+ * s_out must not overlap the inputs (GDP_ERR_ALIAS).  The products run on
+ * warp-level tf32 MMAs in the 3xTF32 split (about fp32 accuracy).  A bounded
+ * wait that runs out sets GDP_DEV_ERR_TIMEOUT in *device_status (may be NULL).
+ */
+gdp_status gdp_prefill_transfer(const gdp_prefill_args *args, float *pairs, void *stream);
+gdp_status gdp_chain_states(const float *s0, const float *phi, const float *b, int64_t steps, int64_t N, int H,
+                            int d, float *s_out, uint32_t *device_status, void *stream);
+
+/*
  * gdp_prefill_varlen_static_scratch: the same prefill for callers that cannot
  * allocate device memory.  No counterpart on the pages: it exists because the
  * main entry point needs a caller-owned workspace, and some callers cannot

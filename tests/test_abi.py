@@ -229,3 +229,21 @@ def test_piece_rows_bound_every_length_mix(lib, T, N, H, M):
         assert L.sum() == T and (L >= 0).all()
         pieces = sum(max(1, -(-(-(-int(x) * M // 64)) // ln)) for x in L)
         assert pieces <= rows, (list(L), pieces, rows)
+
+
+def test_transfer_and_chain_host_validation(lib):
+    """The sequence-sharded prefill's entry points reject bad arguments before any launch."""
+    vp = ctypes.c_void_p
+    assert lib.gdp_prefill_transfer(None, None, None) == pkg.GDP_ERR_INVALID_ARG
+    a = _args()
+    assert lib.gdp_prefill_transfer(ctypes.byref(a), None, None) == pkg.GDP_ERR_INVALID_ARG  # pairs missing
+    assert lib.gdp_prefill_transfer(ctypes.byref(a), vp(0x1008), None) == pkg.GDP_ERR_INVALID_ARG  # misaligned
+    ch = lib.gdp_chain_states
+    assert ch(None, None, None, 1, 1, 1, 96, vp(0x1000), None, None) == pkg.GDP_ERR_INVALID_ARG  # d not 64 / 128
+    assert ch(None, None, None, -1, 1, 1, 64, vp(0x1000), None, None) == pkg.GDP_ERR_INVALID_ARG
+    assert ch(None, None, None, 2, 1, 1, 64, vp(0x1000), None, None) == pkg.GDP_ERR_INVALID_ARG  # phi, b missing
+    assert ch(None, None, None, 0, 1, 1, 64, None, None, None) == pkg.GDP_ERR_INVALID_ARG  # s_out missing
+    assert ch(vp(0x1004), None, None, 0, 1, 1, 64, vp(0x2000), None, None) == pkg.GDP_ERR_INVALID_ARG
+    assert ch(vp(0x1000), None, None, 0, 1, 1, 64, vp(0x1000), None, None) == pkg.GDP_ERR_ALIAS
+    assert ch(None, vp(0x10000), vp(0x20000), 1, 1, 1, 64, vp(0x20000 + 4096), None, None) == pkg.GDP_ERR_ALIAS
+    assert ch(None, None, None, 0, 0, 1, 64, None, None, None) == pkg.GDP_OK  # N = 0: nothing to do

@@ -68,3 +68,99 @@ def test_reference_arm_under_torchrun_two_ranks():
     line = lines[0]
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["steps"] == 2 and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+# ------------------------------------------------- sequence-sharded prefill: the host exchange
+
+def _shard_tensors(w, cuts, r):
+    """Rank r's packed shard: tokens [cuts[i][r], cuts[i][r+1]) of every sequence i."""
+    M, cu = w.M, w.cu_seqlens.tolist()
+    idx_t, idx_e, lens = [], [], []
+    for i in range(len(cu) - 1):
+        a, b = cu[i] + cuts[i][r], cu[i] + cuts[i][r + 1]
+        idx_t += list(range(a, b))
+        idx_e += list(range(M * a, M * b))
+        lens.append(b - a)
+    it, ie = torch.tensor(idx_t, dtype=torch.long), torch.tensor(idx_e, dtype=torch.long)
+    cu_l = torch.tensor([0] + list(torch.tensor(lens).cumsum(0).tolist()), dtype=torch.int32)
+    return dict(q=w.q[it], k=w.k[ie], v=w.v[ie], g=w.g[it], beta=w.beta[ie], cu=cu_l)
+
+
+SEQPAR_LENGTHS = [90, 40, 0]
+
+
+def _seqpar_cuts(world):
+    # per sequence, the token boundaries of the shards of ranks 0 .. world-1 (an empty shard included)
+    return {2: [[0, 37, 90], [0, 0, 40], [0, 0, 0]], 3: [[0, 20, 63, 90], [0, 40, 40, 40], [0, 0, 0, 0]]}[world]
+
+
+def _seqpar_main(rank, world, port, out):
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import oracle
+    import chunked_gated_deltaproduct_gb300 as pkg
+    from gdp_workloads import make_custom
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        M, H, d = 2, 2, 8
+        w = make_custom(SEQPAR_LENGTHS, H, d, M, seed=150, decay=0.1, init_sigma=0.5)  # every rank draws the same
+        sh = _shard_tensors(w, _seqpar_cuts(world), rank)
+        N = len(SEQPAR_LENGTHS)
+
+        def transfer():  # the oracle stands in for the GPU's transfer pairs
+            b = oracle.forward(sh["q"], sh["k"], sh["v"], sh["g"], sh["beta"], sh["cu"], M, w.scale)["final_state"]
+            eye = torch.eye(d).expand(N, H, d, d).contiguous()
+            phi = oracle.forward(sh["q"], sh["k"], torch.zeros_like(sh["v"]), sh["g"], sh["beta"], sh["cu"], M,
+                                 w.scale, initial_state=eye)["final_state"]
+            return torch.from_numpy(np.stack([b, phi])).float()
+
+        def chain(s0, phi, b):  # the plain definition stands in for the GPU chain
+            s = [np.zeros((N, H, d, d)) if s0 is None else s0.double().numpy()]
+            for j in range(phi.shape[0]):
+                s.append(s[-1] @ phi[j].double().numpy() + b[j].double().numpy())
+            return torch.from_numpy(np.stack(s)).float()
+
+        def run(s_in):
+            return oracle.forward(sh["q"], sh["k"], sh["v"], sh["g"], sh["beta"], sh["cu"], M, w.scale,
+                                  initial_state=s_in)
+
+        res = pkg.sequence_parallel_steps(transfer, chain, run, w.initial_state)
+        out[rank] = (res["o"].tolist(), res["final_state"].tolist())
+    finally:
+        dist.destroy_process_group()
+
+
+import pytest  # noqa: E402
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_sequence_sharded_prefill_host_exchange(world):
+    """world ranks hold consecutive token shards of every sequence; the pairs exchange and the
+    chaining of the ranks before each one (the library's host logic, with the oracle standing in
+    for the device steps) reproduce the unsharded run: outputs in token order, the last rank's
+    state = the final state."""
+    import numpy as np
+    import oracle
+    from gdp_workloads import make_custom
+    from tests._pins import rel_err
+
+    port = _free_port()
+    mgr = mp.get_context("spawn").Manager()
+    out = mgr.dict()
+    mp.start_processes(_seqpar_main, args=(world, port, out), nprocs=world, start_method="spawn", join=True)
+    w = make_custom(SEQPAR_LENGTHS, 2, 8, 2, seed=150, decay=0.1, init_sigma=0.5)
+    whole = oracle.forward(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, 2, w.scale, initial_state=w.initial_state)
+    cuts, cu = _seqpar_cuts(world), w.cu_seqlens.tolist()
+    o = np.zeros_like(whole["o"])
+    for r in range(world):
+        o_r = np.asarray(out[r][0])
+        pos = 0
+        for i in range(len(SEQPAR_LENGTHS)):
+            n = cuts[i][r + 1] - cuts[i][r]
+            o[cu[i] + cuts[i][r]:cu[i] + cuts[i][r + 1]] = o_r[pos:pos + n]
+            pos += n
+    # each shard starts from the fp32 rounding of the chained state, hence the tolerance
+    assert rel_err(o, whole["o"]) < 1e-6
+    assert rel_err(np.asarray(out[world - 1][1]), whole["final_state"]) < 1e-6

@@ -368,3 +368,61 @@ def test_linear_alpha_gate(g_dtype):
                 p *= a[t, h]
                 np.testing.assert_allclose(res0["o"][t, h], w.scale * p * (S0[i, h] @ q[t, h]), rtol=1e-12,
                                            atol=1e-14)
+
+
+def test_transfer_pair_affine_in_state():
+    """Over a sequence the state map is affine: S_end(S0) = S0 Phi + B, B the run from a zero
+    state and Phi the run from the identity with v = 0 (the pair a sequence-sharded prefill
+    exchanges; blog post "Attention Cache and Sequence Parallelism", passing state instead of
+    KV).  Phi is checked against the product of the per-token transition matrices
+    alpha_t prod_j (I - beta_j k_j k_j^T), built here directly; an empty sequence has B = 0,
+    Phi = I."""
+    M, H, d = 3, 2, 8
+    w = make_custom([37, 0, 70], H, d, M, seed=140, decay=0.2, init_sigma=0.5)
+    N = 3
+    whole = oracle.forward(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, M, w.scale, initial_state=w.initial_state)
+    B = oracle.forward(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, M, w.scale)["final_state"]
+    eye = torch.eye(d).expand(N, H, d, d).contiguous()
+    Phi = oracle.forward(w.q, w.k, torch.zeros_like(w.v), w.g, w.beta, w.cu_seqlens, M, w.scale,
+                         initial_state=eye)["final_state"]
+    S0 = f64(w.initial_state)
+    np.testing.assert_allclose(whole["final_state"], S0 @ Phi + B, rtol=1e-10, atol=1e-12)
+    np.testing.assert_array_equal(B[1], 0.0)
+    np.testing.assert_array_equal(Phi[1], np.broadcast_to(np.eye(d), (H, d, d)))
+    k, g, beta = f64(w.k), f64(w.g), f64(w.beta)
+    cu = w.cu_seqlens.tolist()
+    for i in (0, 2):
+        for h in range(H):
+            P = np.eye(d)
+            for t in range(cu[i], cu[i + 1]):
+                A = math.exp(g[t, h]) * np.eye(d)
+                for j in range(M):
+                    r = t * M + j
+                    A = A @ (np.eye(d) - beta[r, h] * np.outer(k[r, h], k[r, h]))
+                P = P @ A
+            np.testing.assert_allclose(Phi[i, h], P, rtol=1e-10, atol=1e-13)
+
+
+def test_transfer_pairs_chain_over_shards():
+    """Cutting a sequence into consecutive shards at token boundaries: chaining the shards'
+    pairs, S_{r+1} = S_r Phi_r + B_r from the initial state, gives every shard's entering state,
+    and running each shard from it reproduces the whole run."""
+    M, H, d, L = 2, 2, 8, 150
+    w = make_custom([L], H, d, M, seed=141, decay=0.1, init_sigma=0.5)
+    whole = oracle.forward(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, M, w.scale, initial_state=w.initial_state)
+    cuts = [0, 41, 41, 97, L]  # one empty shard
+    S = f64(w.initial_state)
+    outs = []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        sl = dict(q=w.q[a:b], k=w.k[M * a:M * b], v=w.v[M * a:M * b], g=w.g[a:b], beta=w.beta[M * a:M * b])
+        run = oracle.forward(sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"], [0, b - a], M, w.scale,
+                             initial_state=torch.from_numpy(S).float())
+        outs.append(run["o"])
+        Bs = oracle.forward(sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"], [0, b - a], M, w.scale)["final_state"]
+        eye = torch.eye(d).expand(1, H, d, d).contiguous()
+        Ph = oracle.forward(sl["q"], sl["k"], torch.zeros_like(sl["v"]), sl["g"], sl["beta"], [0, b - a], M, w.scale,
+                            initial_state=eye)["final_state"]
+        S = S @ Ph + Bs
+    # the shards start from fp32 roundings of the chained state, hence the tolerance
+    assert rel_err(np.concatenate(outs), whole["o"]) < 1e-6
+    assert rel_err(S, whole["final_state"]) < 1e-6
