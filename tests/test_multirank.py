@@ -1,11 +1,15 @@
-"""The bench's multi-GPU path on the CPU: world_size-2 process groups on gloo.
+"""Multi-rank host logic on the CPU: gloo process groups.
 
-The path partitions into independent problems (every (sequence, head) chain is independent),
-so N GPUs run N independent batches of the same shape with no collective on the data path
-(weak scaling); the only exchange is the maximum of the ranks' timed durations.  These tests
-run that host logic -- per-rank inputs and the max-over-ranks reduction -- in two CPU
-processes, and launch the bench's reference arm under torch.distributed.run with two ranks
+The bench's multi-GPU path partitions into independent problems (every (sequence, head) chain
+is independent), so N GPUs run N independent batches of the same shape with no collective on
+the data path (weak scaling); the only exchange is the maximum of the ranks' timed durations.
+These tests run that host logic -- per-rank inputs and the max-over-ranks reduction -- in two
+CPU processes, and launch the bench's reference arm under torch.distributed.run with two ranks
 (rank 0 alone runs and prints; the other exits without work).
+
+The sequence-sharded prefill has one real exchange: the ranks' transfer pairs (B, Phi) are
+all-gathered and each rank chains those of the ranks before it.  Its host logic runs here in
+groups of 2 and 3 ranks, with the float64 oracle standing in for the three device steps.
 """
 import json
 import os
