@@ -43,8 +43,8 @@ FALLBACK_HBM_GBS = 6800.0
 # (dram__bytes_read.sum + dram__bytes_write.sum, summed over the stage's kernels), keyed by
 # the sha256 of the stage's sources (KERNEL_SOURCES) it was taken on; reported as null once
 # they change.
-NCU_TRAFFIC = {"gdp_scan_kernel x2 + gdp_piece_combine_kernel": {"sha": "930425cac61a23b8",
-                                                                  "bytes_per_launch": 95152128, "workload": 2}}
+NCU_TRAFFIC = {"gdp_scan_kernel x2 + gdp_piece_combine_kernel": {"sha": "251e60bd817b26c4",
+                                                                  "bytes_per_launch": 94883840, "workload": 2}}
 
 
 def alg_bytes(w) -> int:

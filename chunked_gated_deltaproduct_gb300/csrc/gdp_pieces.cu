@@ -9,7 +9,7 @@
 // pass computes both for every piece but a sequence's last, all pieces at once.  This
 // kernel chains them,
 //   S_in(0) = the sequence's initial state,   S_in(j + 1) = S_in(j) Phi_j + B_j,
-// on warp-level tf32 MMAs in the 3xTF32 split, and stores every S_in for the scan's second
+// in fp32 FMA, and stores every S_in for the scan's second
 // pass, which then runs all pieces at once from their own entering states.  Rows of the state
 // are independent: one CTA per (sequence, head, 16 state rows), one CTA per SM, so a
 // (sequence, head) spreads over V / 16 SMs.  Phi_{j+2} and B_{j+2} arrive by TMA while step j
@@ -22,35 +22,22 @@
 namespace gdp {
 namespace {
 
-constexpr int kCmbThreads = 256;    // 8 warps, each owning D / 8 columns of the CTA's rows
-constexpr int kCmbRows = 16;        // state rows per CTA (the MMA's M)
+constexpr int kCmbThreads = 512;    // 16 warps: k splits x 4 row groups x D / 4 column groups
+constexpr int kCmbRows = 16;        // state rows per CTA
+constexpr int kCmbStStride = 20;    // floats per k row of the transposed rows (16 + 4 pad)
 constexpr size_t kCmbMinSmem = 116u * 1024u;  // at most one CTA per SM: the steps are serial, an SM each
 
-__device__ __forceinline__ uint32_t tf32r(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
-// c[16 x 8] += A[16 x 8] B[8 x 8] (m16n8k8, tf32 in, fp32 out).  Fragments (lane = 4 g + t):
-// A (g, t), (g+8, t), (g, t+4), (g+8, t+4); B (t, g), (t+4, g); C (g, 2t), (g, 2t+1),
-// (g+8, 2t), (g+8, 2t+1).
-__device__ __forceinline__ void mma8(float *c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
-                                     uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
+__host__ __device__ constexpr int cmb_splits(int d) { return kCmbThreads / d; }  // k splits
 // Shared memory: Phi_j in two stages as 32 x 32 boxes of the state map (128-byte swizzle: row r
 // of a box at r * 128 bytes, its 16-byte chunk q at position q ^ (r % 8)); B_j (this CTA's 16
-// rows) in two stages; S_in(j) split into tf32 high and low parts, [16][D + 4] each, in two
-// buffers (the row pad spreads the A-fragment loads over all banks).
+// rows) in two stages; S_j transposed, [D][kCmbStStride], in two buffers; the partial products
+// of the k splits after the first, [KS - 1][16][D].
 __host__ __device__ constexpr uint32_t cmb_phi_bytes(int d) { return (uint32_t)d * d * 4u; }
 __host__ __device__ constexpr uint32_t cmb_b_bytes(int d) { return (uint32_t)kCmbRows * d * 4u; }
-__host__ __device__ constexpr uint32_t cmb_s_floats(int d) { return (uint32_t)kCmbRows * (d + 4); }
+__host__ __device__ constexpr uint32_t cmb_st_floats(int d) { return (uint32_t)d * kCmbStStride; }
 __host__ inline size_t cmb_smem(int d) {
-  const size_t need = 2 * (size_t)cmb_phi_bytes(d) + 2 * (size_t)cmb_b_bytes(d) + 4 * 4 * (size_t)cmb_s_floats(d) + 1024;
+  const size_t need = 2 * (size_t)cmb_phi_bytes(d) + 2 * (size_t)cmb_b_bytes(d) + 2 * 4 * (size_t)cmb_st_floats(d) +
+                      4 * (size_t)(cmb_splits(d) - 1) * kCmbRows * d + 1024;
   return need > kCmbMinSmem ? need : kCmbMinSmem;
 }
 
@@ -67,21 +54,24 @@ struct ChainRows {
   const __nv_bfloat16 *src16;      // bf16; both NULL: zero
 };
 
-// The steps on warp-level tf32 MMAs with the 3xTF32 split (hi hi + lo hi + hi lo: about fp32
-// accuracy, since the product replaces the whole state every step).  Warp w owns columns
-// [w D / 8, (w + 1) D / 8) of the 16 rows: NT n-tiles of 8, with separate accumulators per split
-// term and k-step parity (independent MMA chains), summed with B_j at the end.  Thread 0 brings
-// Phi_j (tensor boxes) and B_j (one bulk copy) in two steps ahead.  (Sharing Phi_j among the row
-// blocks of a (sequence, head) by cluster multicast was slower: clusters of 8 whole-SM CTAs
-// start later.)  Called by all threads after the mbarriers are initialised and visible.
+// The steps in fp32 FMA.  Thread (ks, rg, cg) sums k split ks (D / KS values of k) for rows
+// 4 rg .. 4 rg + 3 and columns 4 cg .. 4 cg + 3; split 0 adds the other splits' partial products
+// and B_j and owns S_{j+1}.  Thread 0 brings Phi_j (tensor boxes) and B_j (one bulk copy) in two
+// steps ahead.  Measured on this part: warp-level tf32 MMAs in the 3xTF32 split took ~1.7 us per
+// step (the legacy MMA path runs at about the FFMA rate, and the split needs three products);
+// sharing Phi_j among a (sequence, head)'s row blocks by cluster multicast was slower (clusters
+// of 8 whole-SM CTAs start late).  Called by all threads once the mbarriers are initialised.
 template <int D, bool INIT16>
 __device__ __forceinline__ void run_chain(const ChainRows &c, const CUtensorMap *tm_phi, unsigned char *sm,
                                           uint64_t *full, uint32_t *status) {
-  constexpr int NT = D / 64, NB = D / 32, SP = D + 4;
-  constexpr uint32_t PB = cmb_phi_bytes(D), BB = cmb_b_bytes(D), SF = cmb_s_floats(D);
+  constexpr int NB = D / 32, CG = D / 4, KS = cmb_splits(D), KL = D / KS;
+  constexpr uint32_t PB = cmb_phi_bytes(D), BB = cmb_b_bytes(D), STF = cmb_st_floats(D);
+  static_assert(KS * D == kCmbThreads && KL * KS == D, "thread layout");
   float *bst = reinterpret_cast<float *>(sm + 2 * PB);  // B_j stages, [2][16][D]
-  float *sb = bst + 2 * BB / 4;                          // S_j: [buffer][hi, lo][16][D + 4]
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
+  float *sts = bst + 2 * BB / 4;                         // S_j^T buffers, [2][D][kCmbStStride]
+  float *part = sts + 2 * STF;                           // [KS - 1][16][D]
+  const int tid = threadIdx.x;
+  const int ks = tid / D, tt = tid % D, rg = tt / CG, cg = tt % CG;
   int issued[2] = {0, 0};
   auto issue = [&](int j) {  // Phi_j and B_j into stage j % 2 (thread 0)
     const int sg = j & 1;
@@ -99,16 +89,7 @@ __device__ __forceinline__ void run_chain(const ChainRows &c, const CUtensorMap 
   if (tid == 0)
     for (int j = 0; j < 2 && j < c.steps; ++j) issue(j);
 
-  // S_j -> global (fp32) and S buffer j % 2 (tf32 hi / lo)
-  auto put2 = [&](int j, int row, int col, float x0, float x1) {
-    *reinterpret_cast<float2 *>(c.s0 + (int64_t)j * c.s_step + (int64_t)row * D + col) = make_float2(x0, x1);
-    float *hi = sb + (j & 1) * 2 * SF, *lo = hi + SF;
-    const float h0 = __uint_as_float(tf32r(x0)), h1 = __uint_as_float(tf32r(x1));
-    *reinterpret_cast<float2 *>(hi + row * SP + col) = make_float2(h0, h1);
-    *reinterpret_cast<float2 *>(lo + row * SP + col) =
-        make_float2(__uint_as_float(tf32r(x0 - h0)), __uint_as_float(tf32r(x1 - h1)));
-  };
-  for (int idx = tid; idx < kCmbRows * D / 2; idx += kCmbThreads) {  // S_0
+  for (int idx = tid; idx < kCmbRows * D / 2; idx += kCmbThreads) {  // S_0 -> global, S^T buffer 0
     const int row = idx / (D / 2), col = 2 * (idx % (D / 2));
     const int64_t off = (int64_t)row * D + col;
     float2 x = make_float2(0.f, 0.f);
@@ -116,72 +97,72 @@ __device__ __forceinline__ void run_chain(const ChainRows &c, const CUtensorMap 
     if constexpr (INIT16) {
       if (c.src16) x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(c.src16 + off));
     }
-    put2(0, row, col, x.x, x.y);
+    *reinterpret_cast<float2 *>(c.s0 + off) = x;
+    sts[col * kCmbStStride + row] = x.x;
+    sts[(col + 1) * kCmbStStride + row] = x.y;
   }
-  // per-thread parts of the B-fragment offsets (floats) inside a stage: column c = n0 + g of
-  // n-tile n0 sits in box column c / 32, chunk (c % 32) / 4, at (c % 4); rows k0 + t and
-  // k0 + t + 4 of the k-step are box rows 8 (ks % 4) + t (+ 4), with chunk position chunk ^ row % 8
-  uint32_t bo0[NT], bo1[NT];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int n0 = warp * 8 * NT + 8 * nt;
-    const uint32_t cq = (uint32_t)(((n0 & 31) >> 2) + (g >> 2));
-    const uint32_t base = (uint32_t)(n0 >> 5) * 1024u + (uint32_t)(g & 3);
-    bo0[nt] = base + (uint32_t)t * 32u + (((cq ^ (uint32_t)t) & 7u) << 2);
-    bo1[nt] = base + (uint32_t)(t + 4) * 32u + (((cq ^ (uint32_t)(t + 4)) & 7u) << 2);
-  }
+  // Phi element (k, 4 cg .. 4 cg + 3), one 16-byte chunk: box (k / 32, col / 32), row k % 32,
+  // chunk position ((col % 32) / 4) ^ (k % 8); the part that depends on the thread only
+  const uint32_t cbase = (uint32_t)(cg >> 3) * 1024u;  // floats
+  const uint32_t cq = (uint32_t)(cg & 7);
   bool ok = true;
 #pragma unroll 1
   for (int j = 0; j < c.steps; ++j) {
     const int sg = j & 1;
-    // also publishes S_j (written before this point)
+    // also publishes S_j^T and frees the partial products of the step before
     ok = __syncthreads_and(sm100::mbar_wait(&full[sg], (uint32_t)((j >> 1) & 1)));
     if (!ok) break;
     const float *phi = reinterpret_cast<const float *>(sm + sg * PB);
-    const float *bj = bst + sg * (BB / 4);
-    const float *hi = sb + sg * 2 * SF, *lo = hi + SF;
-    float acc[2][NT][3][4];  // [k-step parity][n-tile][hi hi, lo hi, hi lo]
+    const float *st = sts + (j & 1) * STF;
+    float acc[4][4];
+    if (ks == 0) {  // B_j now: the stage is refilled once everyone has passed the barrier below
+      const float *bj = bst + sg * (BB / 4);
 #pragma unroll
-    for (int e = 0; e < 2; ++e)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int x = 0; x < 3; ++x) acc[e][nt][x][0] = acc[e][nt][x][1] = acc[e][nt][x][2] = acc[e][nt][x][3] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < D / 8; ++ks) {
-      const int k0 = 8 * ks, e = ks & 1;
-      const uint32_t ah0 = __float_as_uint(hi[g * SP + k0 + t]), ah1 = __float_as_uint(hi[(g + 8) * SP + k0 + t]);
-      const uint32_t ah2 = __float_as_uint(hi[g * SP + k0 + t + 4]),
-                     ah3 = __float_as_uint(hi[(g + 8) * SP + k0 + t + 4]);
-      const uint32_t al0 = __float_as_uint(lo[g * SP + k0 + t]), al1 = __float_as_uint(lo[(g + 8) * SP + k0 + t]);
-      const uint32_t al2 = __float_as_uint(lo[g * SP + k0 + t + 4]),
-                     al3 = __float_as_uint(lo[(g + 8) * SP + k0 + t + 4]);
-      const uint32_t kofs = (uint32_t)(ks >> 2) * (uint32_t)NB * 1024u + (uint32_t)(ks & 3) * 256u;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const float b0 = phi[kofs + bo0[nt]], b1 = phi[kofs + bo1[nt]];
-        const uint32_t bh0 = tf32r(b0), bh1 = tf32r(b1);
-        const uint32_t bl0 = tf32r(b0 - __uint_as_float(bh0)), bl1 = tf32r(b1 - __uint_as_float(bh1));
-        mma8(acc[e][nt][0], ah0, ah1, ah2, ah3, bh0, bh1);
-        mma8(acc[e][nt][1], al0, al1, al2, al3, bh0, bh1);
-        mma8(acc[e][nt][2], ah0, ah1, ah2, ah3, bl0, bl1);
+      for (int i = 0; i < 4; ++i) {
+        const float4 bv = *reinterpret_cast<const float4 *>(bj + (4 * rg + i) * D + 4 * cg);
+        acc[i][0] = bv.x; acc[i][1] = bv.y; acc[i][2] = bv.z; acc[i][3] = bv.w;
       }
-    }
+    } else {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int col = warp * 8 * NT + 8 * nt + 2 * t;
-      const float2 u0 = *reinterpret_cast<const float2 *>(bj + g * D + col);
-      const float2 u1 = *reinterpret_cast<const float2 *>(bj + (g + 8) * D + col);
-      float y[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q)  // small terms first
-        y[q] = ((acc[0][nt][1][q] + acc[1][nt][1][q]) + (acc[0][nt][2][q] + acc[1][nt][2][q])) +
-               (acc[0][nt][0][q] + acc[1][nt][0][q]);
-      put2(j + 1, g, col, y[0] + u0.x, y[1] + u0.y);
-      put2(j + 1, g + 8, col, y[2] + u1.x, y[3] + u1.y);
+      for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     }
-    __syncthreads();  // stage sg and S buffer j % 2 are consumed
+#pragma unroll 8
+    for (int k = ks * KL; k < ks * KL + KL; ++k) {
+      const float4 sv = *reinterpret_cast<const float4 *>(st + k * kCmbStStride + 4 * rg);
+      const float4 pv = *reinterpret_cast<const float4 *>(
+          phi + (uint32_t)(k >> 5) * (uint32_t)NB * 1024u + cbase + (uint32_t)(k & 31) * 32u + ((cq ^ (uint32_t)(k & 7)) << 2));
+      const float sa[4] = {sv.x, sv.y, sv.z, sv.w}, pa[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[i][q] = fmaf(sa[i], pa[q], acc[i][q]);
+    }
+    if (ks > 0)
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<float4 *>(part + ((ks - 1) * kCmbRows + 4 * rg + i) * D + 4 * cg) =
+            make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    __syncthreads();  // stage sg (Phi_j, B_j) and S_j^T are read; the partial products are in place
     if (tid == 0 && j + 2 < c.steps) issue(j + 2);
+    if (ks == 0) {
+      float *nst = sts + ((j + 1) & 1) * STF;
+      float *dst = c.s0 + (int64_t)(j + 1) * c.s_step;
+#pragma unroll
+      for (int x = 0; x < KS - 1; ++x)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 y = *reinterpret_cast<const float4 *>(part + (x * kCmbRows + 4 * rg + i) * D + 4 * cg);
+          acc[i][0] += y.x; acc[i][1] += y.y; acc[i][2] += y.z; acc[i][3] += y.w;
+        }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<float4 *>(dst + (int64_t)(4 * rg + i) * D + 4 * cg) =
+            make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<float4 *>(nst + (4 * cg + q) * kCmbStStride + 4 * rg) =
+            make_float4(acc[0][q], acc[1][q], acc[2][q], acc[3][q]);
+    }
   }
   if (!ok && tid == 0) {
     set_status(status, GDP_DEV_ERR_TIMEOUT);

@@ -266,9 +266,9 @@ gdp_status gdp_prefill_varlen_profiled(const gdp_prefill_args *args, void *strea
  * head), from S_0 = s0 (NULL: zero).  phi, b: [steps][N][H][d][d] fp32 (the
  * pairs of consecutive shards in order), s_out: [steps + 1][N][H][d][d] fp32,
  * s_out[0] = S_0; d is 64 or 128; all device pointers, 16-byte aligned;
- * s_out must not overlap the inputs (GDP_ERR_ALIAS).  The products run on
- * warp-level tf32 MMAs in the 3xTF32 split (about fp32 accuracy).  A bounded
- * wait that runs out sets GDP_DEV_ERR_TIMEOUT in *device_status (may be NULL).
+ * s_out must not overlap the inputs (GDP_ERR_ALIAS).  The products run in
+ * fp32 FMA.  A bounded wait that runs out sets GDP_DEV_ERR_TIMEOUT in
+ * *device_status (may be NULL).
  */
 gdp_status gdp_prefill_transfer(const gdp_prefill_args *args, float *pairs, void *stream);
 gdp_status gdp_chain_states(const float *s0, const float *phi, const float *b, int64_t steps, int64_t N, int H,

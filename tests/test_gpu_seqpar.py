@@ -113,7 +113,7 @@ def test_transfer_pairs_against_oracle(cuda_device):
 
 @pytest.mark.parametrize("d,steps", [(128, 5), (64, 3), (128, 0)])
 def test_chain_states_against_float64(cuda_device, d, steps):
-    """S_{j+1} = S_j Phi_j + B_j in the 3xTF32 split against the same chain in float64."""
+    """S_{j+1} = S_j Phi_j + B_j (fp32 FMA) against the same chain in float64."""
     gen = torch.Generator().manual_seed(430 + d + steps)
     N, H = 3, 2
     phi = torch.randn((steps, N, H, d, d), generator=gen) / d ** 0.5
