@@ -43,7 +43,7 @@ FALLBACK_HBM_GBS = 6800.0
 # (dram__bytes_read.sum + dram__bytes_write.sum, summed over the stage's kernels), keyed by
 # the sha256 of the stage's sources (KERNEL_SOURCES) it was taken on; reported as null once
 # they change.
-NCU_TRAFFIC = {"gdp_scan_kernel x2 + gdp_piece_combine_kernel": {"sha": "251e60bd817b26c4",
+NCU_TRAFFIC = {"gdp_scan_kernel x2 + gdp_piece_combine_kernel": {"sha": "4e25b41a91e3db0c",
                                                                   "bytes_per_launch": 94883840, "workload": 2}}
 
 

@@ -32,6 +32,13 @@
 // come from one operand image per chunk (written by the WY kernel), fetched by
 // two bulk copies into a double-buffered shared-memory stage while the
 // previous chunk computes.
+//
+// The same kernel runs three other grids (Problem fields piece_len, piece_pass1, xfer):
+// the two passes of split chains (one CTA per piece of a sequence: pass 1 from a zero
+// state and from the identity with U^T read as zero, storing the piece's B and Phi;
+// pass 2 from the piece's entering state), and the transfer pairs of whole sequences
+// (one CTA per sequence from zero, one from the identity).  A launch without outputs
+// skips the o_hat products and stores.
 #pragma once
 #include <cuda.h>  // CUtensorMap
 
