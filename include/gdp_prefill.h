@@ -259,8 +259,9 @@ gdp_status gdp_prefill_varlen_profiled(const gdp_prefill_args *args, void *strea
  * aligned, written whole (B = 0, Phi = I for an empty sequence).  Needs
  * q, k, v, g, beta, cu_seqlens, the workspace and the scalars of args;
  * output, output_state, chunk_states, initial_state and the state cache are
- * ignored.  Runs whole sequences in one segment (no split chains).  Errors
- * as gdp_prefill_varlen.
+ * not used (they are checked as for gdp_prefill_varlen when given).  Runs
+ * whole sequences in one segment (no split chains).  N = 0 returns GDP_OK
+ * without a launch.  Errors as gdp_prefill_varlen.
  *
  * gdp_chain_states: S_{j+1} = S_j Phi_j + B_j for j < steps, per (sequence,
  * head), from S_0 = s0 (NULL: zero).  phi, b: [steps][N][H][d][d] fp32 (the

@@ -247,3 +247,6 @@ def test_transfer_and_chain_host_validation(lib):
     assert ch(vp(0x1000), None, None, 0, 1, 1, 64, vp(0x1000), None, None) == pkg.GDP_ERR_ALIAS
     assert ch(None, vp(0x10000), vp(0x20000), 1, 1, 1, 64, vp(0x20000 + 4096), None, None) == pkg.GDP_ERR_ALIAS
     assert ch(None, None, None, 0, 0, 1, 64, None, None, None) == pkg.GDP_OK  # N = 0: nothing to do
+    empty = _args(N=0, T=0)
+    assert lib.gdp_prefill_transfer(ctypes.byref(empty), None, None) == pkg.GDP_OK  # no sequences, no launch
+    assert lib.gdp_prefill_transfer(ctypes.byref(_args(K=96, V=96)), vp(0x1000), None) == pkg.GDP_ERR_UNSUPPORTED
