@@ -32,6 +32,10 @@ CASES = {
                                init_sigma=0.1),
     "grouped_heads": dict(lengths=[1000, 260], H=4, d=64, M=2, hq=2, hk=2, hv=4, init_sigma=0.1,
                           chunk_states=True),
+    # M does not divide the piece length: token-chunk starts fall at different local chunks per piece
+    "m4_chunk_states_unaligned": dict(lengths=[900, 70], H=2, d=64, M=4, init_sigma=0.1, chunk_states=True),
+    # both sequences are split, so the padded slot belongs to a split sequence
+    "cache_padding_on_split": dict(lengths=[900, 700], H=2, d=128, M=2, cache_slots=4, padding_slots=1),
 }
 PLAIN_H = 64
 
