@@ -26,6 +26,7 @@ import math
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -96,13 +97,14 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, folder: str | None = None):
         self.index, self.proc, self.path = index, None, None
+        self.folder = folder or tempfile.gettempdir()  # where the raw samples go (--clocks-dir)
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+            os.makedirs(self.folder, exist_ok=True)
+            self.path = os.path.join(self.folder, f"clocks_bench_{os.getpid()}.csv")
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
@@ -368,6 +370,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--clocks-dir", default=None, help="folder for the raw clock samples (default: a temp folder)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -452,7 +455,7 @@ def main():
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    with ClockSampler(local, args.clocks_dir) as clk:
         wall0 = time.perf_counter()
         for s in range(args.steps):
             step_plain(*plain[s])
