@@ -250,3 +250,15 @@ def test_transfer_and_chain_host_validation(lib):
     empty = _args(N=0, T=0)
     assert lib.gdp_prefill_transfer(ctypes.byref(empty), None, None) == pkg.GDP_OK  # no sequences, no launch
     assert lib.gdp_prefill_transfer(ctypes.byref(_args(K=96, V=96)), vp(0x1000), None) == pkg.GDP_ERR_UNSUPPORTED
+
+
+def test_sequence_parallel_wrappers_reject_bad_tensors():
+    """The binding's checks that run before any library call."""
+    import torch
+    with pytest.raises(pkg.GdpError):
+        pkg.chain_states(None, torch.zeros((1, 1, 1, 64, 64), dtype=torch.float16), torch.zeros((1, 1, 1, 64, 64)))
+    with pytest.raises(pkg.GdpError):
+        pkg.chain_states(None, torch.zeros((1, 1, 1, 64, 64)).transpose(-1, -2), torch.zeros((1, 1, 1, 64, 64)))
+    with pytest.raises(pkg.GdpError):
+        q = torch.zeros((4, 1, 64), dtype=torch.bfloat16)
+        pkg.chunk_gated_delta_product_transfer(q, q, q, cu_seqlens=None)
