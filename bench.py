@@ -1,21 +1,26 @@
 """Bench: real tokens/s of the GDP varlen prefill on one GB300 (device-timed),
-with the dominant kernel's roofline fraction, an end-to-end leg through host
-buffers, and the float64 CPU oracle as the reported CPU baseline.
+with the roofline fractions, an end-to-end leg through host buffers, and the
+float64 CPU oracle as the reported CPU baseline.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 2] [--impl gdp|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 4] [--impl gdp|reference]
 
-A step is one full gdp_prefill_varlen call (descriptor kernel, prep + WY
-kernel, scan/output kernel) over one batch of the synthetic workload, inputs
-resident in HBM.  Between timed steps a 256 MiB buffer is written to flush the
-129 MB L2.  The timed steps are plain gdp_prefill_varlen calls, each bracketed
-by CUDA events on the launching stream (its kernels overlap their launches);
-a second pass of the same steps through gdp_prefill_varlen_profiled, whose
-events sit between the kernels (so each kernel runs alone), gives the
-per-kernel durations of the roofline.  Two more legs are reported beside the headline: the
-decode step (key decode_step) and the backward pass of the same workload (key backward: device
-time per gdp_prefill_varlen_backward call, which includes its forward recompute).  Under torchrun every rank
-runs its own independent batch of the same shape (weak scaling, no
-collective); rank 0 prints one JSON line.
+The headline workload is the largest single-GPU configuration: one sequence of
+65536 tokens (131072 expanded rows), H=32, d=128, M=2, initial state, final
+state and per-chunk states.  A step is one full gdp_prefill_varlen call over
+that batch, inputs resident in HBM.  Between timed steps a 256 MiB buffer is
+written to flush the 129 MB L2.  The timed steps are plain gdp_prefill_varlen
+calls, each bracketed by CUDA events on the launching stream; a second pass of
+the same steps through gdp_prefill_varlen_profiled, whose events sit between
+the stages (so each stage runs alone), gives the per-stage durations.
+
+Reported beside the headline (key per_workload): the other benchmark
+configurations -- the four-sequence varlen batch (1421 tokens, H8, M2, chunk
+states), the 8 x 4096 batch (H16, M3, in-kernel L2 norm) and the serving step
+(64 log-uniform sequences, H16, M4, state cache in place, prebuilt descriptors)
+timed as a CUDA-graph replay.  Also reported: the decode step (key
+decode_step) and the backward pass of the headline workload (key backward).
+Under torchrun every rank runs its own independent batch of the same shape
+(weak scaling, no collective); rank 0 prints one JSON line.
 """
 from __future__ import annotations
 
@@ -39,13 +44,15 @@ from gdp_workloads import make_custom, WORKLOADS, make_workload  # noqa: E402
 
 METRIC = "GDP prefill real tokens/s on 1 GB300 (device-timed) and % of roofline"
 UNIT = "tokens/s"
+HEADLINE_WORKLOAD = 4
+PER_WORKLOAD = (2, 3, 5)
 FALLBACK_HBM_GBS = 6800.0
-# DRAM traffic of the dominant stage per call, from one ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum, summed over the stage's kernels), keyed by
-# the sha256 of the stage's sources (KERNEL_SOURCES) it was taken on; reported as null once
-# they change.
-NCU_TRAFFIC = {"gdp_scan_kernel x2 + gdp_piece_combine_kernel": {"sha": "4e25b41a91e3db0c",
-                                                                  "bytes_per_launch": 94883840, "workload": 2}}
+# DRAM traffic of a stage per call, from one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum summed over the stage's kernels, scaled to the full call where the
+# capture ran a reduced shape), keyed by (stage, workload id); each entry names the source
+# files of the stage's kernels and the sha256 of those files when the capture was taken, and is
+# reported as null once they change.
+NCU_TRAFFIC = {}
 
 
 def alg_bytes(w) -> int:
@@ -147,15 +154,10 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-KERNEL_SOURCES = {"gdp_desc_kernel": ("gdp_desc.cu",), "gdp_wy_kernel": ("gdp_wy.cu", "gdp_wy_body.cuh"),
-                  "gdp_scan_kernel": ("gdp_scan.cu", "gdp_scan_body.cuh"),
-                  "gdp_scan_kernel x2 + gdp_piece_combine_kernel": ("gdp_scan.cu", "gdp_scan_body.cuh",
-                                                                    "gdp_pieces.cu")}
-
-
-def _kernel_sha(kernel: str) -> str:
+def sources_sha(files) -> str:
+    """sha256 (16 hex digits) of the given files under the package's csrc/ folder."""
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES[kernel]:
+    for name in files:
         p = os.path.join(ROOT, "chunked_gated_deltaproduct_gb300", "csrc", name)
         if not os.path.exists(p):
             return ""
@@ -163,71 +165,77 @@ def _kernel_sha(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
+# ------------------------------------------------------------------------- the oracle's sample
+
+def oracle_sample(w, frac: float) -> dict:
+    """Every head, each sequence cut to its first ceil(frac * L) tokens: the bounded sample of
+    the workload that the CPU baseline and the reference arm time (all heads, so that the
+    oracle's parallel loop over (sequence, head, V-row block) has the workload's own width)."""
+    lens = [min(L, max(1, int(math.ceil(L * frac)))) if L else 0 for L in w.lengths]
+    cu = w.cu_seqlens.tolist()
+    parts = [torch.arange(cu[i], cu[i] + lens[i]) for i in range(w.N)]
+    tok = torch.cat(parts) if parts else torch.arange(0)
+    rows = (tok[:, None] * w.M + torch.arange(w.M)[None]).reshape(-1)
+    sub_cu = [0]
+    for L in lens:
+        sub_cu.append(sub_cu[-1] + L)
+    return {"q": w.q[tok], "k": w.k[rows], "v": w.v[rows], "g": None if w.g is None else w.g[tok],
+            "beta": None if w.beta is None else w.beta[rows], "cu": sub_cu, "T": int(tok.numel())}
+
+
+def _oracle_run(oracle, w, s, threads):
+    oracle.forward(s["q"], s["k"], s["v"], s["g"], s["beta"], s["cu"], w.M, w.scale, use_qk_l2norm=w.use_qk_l2norm,
+                   initial_state=w.initial_state, state=w.state, state_indices=w.state_indices,
+                   chunk_states=w.return_chunk_states, threads=threads)
+
+
+def oracle_fraction(oracle, w, budget_s: float, threads: int) -> float:
+    """The token fraction whose all-heads sample takes about budget_s on the host cores
+    (calibrated on a small probe; the oracle's cost is linear in the tokens)."""
+    f = min(1.0, 256.0 / max(max(w.lengths), 1))
+    s = oracle_sample(w, f)
+    t0 = time.perf_counter()
+    _oracle_run(oracle, w, s, threads)
+    el = max(time.perf_counter() - t0, 1e-4)
+    return min(1.0, f * budget_s / el)
+
+
 def cpu_oracle_baseline(w, budget_s: float):
-    """The oracle as it stands on this host's cores, over a bounded sample:
-    whole-workload repetitions, or a subset of heads when one run is too long."""
+    """The oracle as it stands on this host's cores over a bounded sample of the workload."""
     import oracle
 
     threads = oracle.oracle_threads()
-    heads = list(range(w.H))
+    frac = oracle_fraction(oracle, w, budget_s, threads)
+    s = oracle_sample(w, frac)
     t0 = time.perf_counter()
-    oracle.forward(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, w.M, w.scale, use_qk_l2norm=w.use_qk_l2norm,
-                   initial_state=w.initial_state, state=w.state, state_indices=w.state_indices,
-                   chunk_states=w.return_chunk_states, heads=[0], threads=threads)
-    per_head = time.perf_counter() - t0
-    nh = max(1, min(w.H, int(budget_s / max(per_head, 1e-6))))
-    heads = heads[:nh]
-    reps = max(1, int(budget_s / max(per_head * nh, 1e-6))) if nh == w.H else 1
-    t0 = time.perf_counter()
-    for _ in range(reps):
-        oracle.forward(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, w.M, w.scale, use_qk_l2norm=w.use_qk_l2norm,
-                       initial_state=w.initial_state, state=w.state, state_indices=w.state_indices,
-                       chunk_states=w.return_chunk_states, heads=heads, threads=threads)
+    _oracle_run(oracle, w, s, threads)
     el = time.perf_counter() - t0
-    value = w.T * (nh / w.H) * reps / el
-    return {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{reps} run(s) of heads 0..{nh - 1} of {w.H} over all {w.T} tokens, {el:.1f} s"}
+    return {"value": s["T"] / el, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"all {w.H} heads, first {frac:.4f} of each sequence ({s['T']} of {w.T} tokens), "
+                      f"one run, {el:.1f} s"}
 
 
 def run_reference(args, w, rank):
-    """Reference arm: the float64 oracle on the host cores, a bounded sample per step."""
+    """Reference arm: the float64 oracle on the host cores, timed on the same kind of sample as
+    the CPU baseline (all heads, a prefix of every sequence), one sample per step."""
     import oracle
 
     if rank != 0:
         return
     threads = oracle.oracle_threads()
     total_steps = args.steps + args.warmup
-    per_step_budget = max(0.02, min(5.0, 150.0 / max(total_steps, 1)))
-    t0 = time.perf_counter()
-    oracle.forward(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, w.M, w.scale, use_qk_l2norm=w.use_qk_l2norm,
-                   initial_state=w.initial_state, state=w.state, state_indices=w.state_indices,
-                   chunk_states=w.return_chunk_states, heads=[0], threads=threads)
-    per_head = time.perf_counter() - t0
-    frac = min(1.0, per_step_budget / max(per_head, 1e-9))
-    # sample: head h (rotating), every sequence truncated to its first `frac` share of tokens
-    lens = [max(1, int(math.ceil(L * frac))) if L else 0 for L in w.lengths]
-    cu = w.cu_seqlens.tolist()
-    tok = torch.cat([torch.arange(cu[i], cu[i] + lens[i]) for i in range(w.N)]) if w.T else torch.arange(0)
-    rows = (tok[:, None] * w.M + torch.arange(w.M)[None]).reshape(-1)
-    sub_cu = [0]
-    for L in lens:
-        sub_cu.append(sub_cu[-1] + L)
-    q, k, v = w.q[tok], w.k[rows], w.v[rows]
-    g = None if w.g is None else w.g[tok]
-    beta = None if w.beta is None else w.beta[rows]
-    Ts = len(tok)
+    per_step_budget = max(0.05, min(5.0, 150.0 / max(total_steps, 1)))
+    frac = oracle_fraction(oracle, w, per_step_budget, threads)
+    s = oracle_sample(w, frac)
     times = []
-    for s in range(total_steps):
-        h = s % w.H
+    for i in range(total_steps):
         t0 = time.perf_counter()
-        oracle.forward(q, k, v, g, beta, sub_cu, w.M, w.scale, use_qk_l2norm=w.use_qk_l2norm,
-                       initial_state=w.initial_state, state=w.state, state_indices=w.state_indices,
-                       chunk_states=w.return_chunk_states, heads=[h], threads=threads)
-        if s >= args.warmup:
+        _oracle_run(oracle, w, s, threads)
+        if i >= args.warmup:
             times.append(time.perf_counter() - t0)
     el = sum(times)
-    value = Ts * (1.0 / w.H) * len(times) / el if el > 0 else 0.0
-    sample = f"per step: 1 of {w.H} heads (rotating), first {frac:.3f} of each sequence ({Ts} of {w.T} tokens)"
+    value = s["T"] * len(times) / el if el > 0 else 0.0
+    sample = (f"per step: all {w.H} heads, first {frac:.4f} of each sequence ({s['T']} of {w.T} tokens)")
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * el / max(len(times), 1), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -237,27 +245,179 @@ def run_reference(args, w, rank):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------------- the GPU legs
+
 def launches_per_call(w) -> int:
-    """Kernels one call launches (the library's shape-only plan): descriptors, WY and scan; WY +
-    scan per segment in the segmented mode; or, with split chains, the scan's two passes and the
-    combine kernel between them."""
+    """Kernels one call launches (the library's shape-only plan)."""
     import chunked_gated_deltaproduct_gb300 as pkg
     return pkg.gdp_prefill_plan(w.T, w.N, w.H, w.d, w.d, w.M)["launches"]
 
 
-def scan_stage_name(w) -> str:
-    """The kernels between the WY stage and the end of a call."""
+def stage_names(w):
+    """The three stages the profiled entry point separates by events."""
     import chunked_gated_deltaproduct_gb300 as pkg
-    if pkg.gdp_prefill_plan(w.T, w.N, w.H, w.d, w.d, w.M)["piece_chunks"] > 0:
-        return "gdp_scan_kernel x2 + gdp_piece_combine_kernel"
-    return "gdp_scan_kernel"
+    plan = pkg.gdp_prefill_plan(w.T, w.N, w.H, w.d, w.d, w.M)
+    if plan["piece_chunks"] > 0:
+        scan = "gdp_scan_kernel x2 + gdp_piece_combine_kernel"
+    elif plan["segments"] > 1:
+        scan = f"gdp_scan_kernel x{plan['segments']} (segmented, WY segments 2.. beside it)"
+    else:
+        scan = "gdp_scan_kernel"
+    wy = "gdp_wy_kernel" if plan["segments"] == 1 else "gdp_wy_kernel (segment 1)"
+    return ["gdp_desc_kernel", wy, scan]
+
+
+class Call:
+    """Device tensors and arguments of one workload's call."""
+
+    def __init__(self, pkg, w, dev):
+        self.w = w
+        self.q, self.k, self.v = w.q.to(dev), w.k.to(dev), w.v.to(dev)
+        self.g = None if w.g is None else w.g.to(dev)
+        self.beta = None if w.beta is None else w.beta.to(dev)
+        self.cu = w.cu_seqlens.to(dev)
+        self.init = None if w.initial_state is None else w.initial_state.to(dev)
+        self.cache = None if w.state is None else w.state.to(dev)
+        self.sidx = None if w.state_indices is None else w.state_indices.to(dev)
+        self.out = torch.empty((w.T, w.H, w.d), dtype=torch.bfloat16, device=dev)
+        self.fin = torch.empty((w.N, w.H, w.d, w.d), dtype=torch.float32, device=dev) if (
+            w.output_final_state and self.cache is None) else None
+        self.cs = torch.zeros((pkg.gdp_nt_pad(w.T, w.N), w.H, w.d, w.d), dtype=torch.float32, device=dev) if (
+            w.return_chunk_states) else None
+        self.ci = self.cid = self.co = None
+        if w.prebuilt_descriptors:
+            self.ci, self.cid, self.co = pkg.gdp_build_descriptors(self.cu, w.T, w.M)
+        self.ws = pkg.alloc_workspace(w.T, w.N, w.H, w.d, w.d, w.M, dev)
+        self.args = pkg.make_args(self.q, self.k, self.v, self.g, self.beta, self.cu, w.M, w.scale, self.init,
+                                  self.cache, self.sidx, self.out, self.fin, self.cs, self.ci, self.cid, self.co,
+                                  None, None, w.use_qk_l2norm, self.ws, None)
+
+    def inputs(self):
+        return [t for t in (self.q, self.k, self.v, self.g, self.beta, self.cu, self.init, self.cache, self.sidx)
+                if t is not None]
+
+    def outputs(self):
+        return [t for t in (self.out, self.fin, self.cs, self.cache) if t is not None]
+
+
+def time_call(pkg, c, stream, flush, steps, warmup, clk_folder=None, sample_clocks=False):
+    """Plain calls (events around each, L2 flushed before each), then the same number of calls
+    through the profiled entry point (events between the stages).  Returns step times (ms), the
+    mean per-stage times (ms), the profiled step time and the clock summary."""
+    sid = stream.cuda_stream
+
+    def new_events():
+        # torch creates the CUDA event lazily at its first record(); record once so the raw
+        # handle exists and torch accepts elapsed_time(); the library then re-records it.
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        for e in evs:
+            e.record(stream)
+        return evs
+
+    def step_profiled(evs):
+        with torch.cuda.stream(stream):
+            flush.zero_()
+        pkg.gdp_prefill_varlen_profiled(c.args, evs, sid)
+
+    def step_plain(e0, e1):
+        with torch.cuda.stream(stream):
+            flush.zero_()
+        e0.record(stream)
+        pkg.gdp_prefill_varlen(c.args, sid)
+        e1.record(stream)
+
+    def pair():
+        return [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    for _ in range(warmup):
+        step_plain(*pair())
+        step_profiled(new_events())
+    torch.cuda.synchronize()
+    plain = [pair() for _ in range(steps)]
+    clk = None
+    t_wall = 0.0
+    if sample_clocks:
+        with ClockSampler(torch.cuda.current_device(), clk_folder) as sampler:
+            w0 = time.perf_counter()
+            for s in range(steps):
+                step_plain(*plain[s])
+            torch.cuda.synchronize()
+            t_wall = time.perf_counter() - w0
+        clk = sampler.summary()
+    else:
+        for s in range(steps):
+            step_plain(*plain[s])
+        torch.cuda.synchronize()
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in plain]
+    events = [new_events() for _ in range(steps)]
+    for s in range(steps):
+        step_profiled(events[s])
+    torch.cuda.synchronize()
+    stage = [[ev[i].elapsed_time(ev[i + 1]) for i in range(3)] for ev in events]
+    stage_ms = [statistics.fmean(x[i] for x in stage) for i in range(3)]
+    prof_ms = statistics.fmean(ev[0].elapsed_time(ev[3]) for ev in events)
+    return step_ms, stage_ms, prof_ms, clk, t_wall
+
+
+def roofline_of(w, step_ms_mean, stage_ms, names, workload_id):
+    """Whole-call and dominant-stage fractions of the HBM roofline (algorithmic bytes over the
+    measured time; every workload is HBM-bound by its algorithmic count)."""
+    peak, src = measured_peaks()
+    ab = alg_bytes(w)
+    dom = max(range(3), key=lambda i: stage_ms[i])
+    stage_gbs = ab / (stage_ms[dom] / 1e3) / 1e9
+    step_gbs = ab / (step_ms_mean / 1e3) / 1e9
+    tr = NCU_TRAFFIC.get((names[dom], workload_id))
+    traffic = tr["bytes_per_call"] if (tr and tr["sha"] == sources_sha(tr["sources"])) else None
+    return {"bound": "hbm", "kernel": names[dom], "achieved": stage_gbs, "peak": peak, "peak_source": src,
+            "unit": "GB/s", "frac": stage_gbs / peak, "traffic": traffic, "alg_bytes_per_launch": ab,
+            "kernel_ms": stage_ms[dom], "step_achieved": step_gbs, "step_frac": step_gbs / peak,
+            "roofline_us": ab / (peak * 1e9) * 1e6, "alg_gflop_per_step": alg_flops(w) / 1e9}
+
+
+def measure_graph(pkg, w, dev, stream, flush, replays=50, warmup=10):
+    """A CUDA-graph replay of one call (prebuilt descriptors, the state cache in place): median
+    of `replays` replays after `warmup`, the L2 flushed outside the graph before each.  Replays
+    keep updating the cache in place (beta in (0, 1) and unit-norm k keep it bounded)."""
+    c = Call(pkg, w, dev)
+    sid = stream.cuda_stream
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        graph.capture_begin()
+        pkg.gdp_prefill_varlen(c.args, sid)
+        graph.capture_end()
+    torch.cuda.synchronize()
+    times = []
+    for i in range(warmup + replays):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+        e1.synchronize()
+        if i >= warmup:
+            times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    peak, src = measured_peaks()
+    ab = alg_bytes(w)
+    live = int((w.state_indices >= 0).sum()) if w.state_indices is not None else w.N
+    live_tokens = sum(L for L, s in zip(w.lengths, w.state_indices.tolist()) if s >= 0) if (
+        w.state_indices is not None) else w.T
+    del graph, c
+    return {"workload": w.name, "timing": f"CUDA-graph replay, median of {replays} after {warmup}, L2 flushed",
+            "ms_per_call": ms, "tokens_per_s": w.T / (ms / 1e3), "tokens": w.T,
+            "live_tokens_per_s": live_tokens / (ms / 1e3), "live_sequences": live,
+            "alg_bytes": ab, "achieved_gbs": ab / (ms / 1e3) / 1e9, "frac": ab / (ms / 1e3) / 1e9 / peak,
+            "roofline_us": ab / (peak * 1e9) * 1e6, "launches_per_call": launches_per_call(w)}
 
 
 def measure_decode(pkg, dev, flush, stream, steps=50, warmup=5):
     """The decode step (one token per sequence, state cache in place) on a serving batch shaped
-    like workload 5: 64 sequences, H=16, d=128, M=4, a 128-slot cache with 8 padding entries.
-    Device time per step with the L2 flushed between steps; algorithmic bytes = the live cache
-    slots read and written + the token's q, M k/v rows, gate, M betas and o."""
+    like the serving workload: 64 sequences, H=16, d=128, M=4, a 128-slot cache with 8 padding
+    entries.  Device time per step with the L2 flushed between steps; algorithmic bytes = the
+    live cache slots read and written + the token's q, M k/v rows, gate, M betas and o."""
     wd = make_custom([1] * 64, 16, 128, 4, seed=2024, cache_slots=128, cache_sigma=0.1, padding_slots=8)
     q, k, v, g, b = (t.to(dev) for t in (wd.q, wd.k, wd.v, wd.g, wd.beta))
     cache, sidx = wd.state.to(dev), wd.state_indices.to(dev)
@@ -318,7 +478,7 @@ def backward_launches(w) -> int:
     return launches_per_call(w) + 2 + 4
 
 
-def measure_backward(pkg, dev, flush, stream, w, steps=20, warmup=3):
+def measure_backward(pkg, dev, flush, stream, w, steps=5, warmup=3):
     """The backward pass of the same workload: upstream gradients d_output (bf16) and
     d_final_state (fp32) drawn by gdp_workloads.make_cotangents; device time per call with the
     L2 flushed between calls."""
@@ -353,23 +513,44 @@ def measure_backward(pkg, dev, flush, stream, w, steps=20, warmup=3):
     ab = backward_alg_bytes(w, True)
     peak, src = measured_peaks()
     gbs = ab / (ms / 1e3) / 1e9
+    del ws, b, fa
     return {"workload": w.name, "ms_per_call": ms, "tokens_per_s": T / (ms / 1e3), "alg_bytes": ab,
             "achieved_gbs": gbs, "peak_gbs": peak, "frac": gbs / peak, "peak_source": src, "steps": steps,
             "l2_flush": True, "launches_per_call": backward_launches(w),
             "note": "includes the forward recompute (the backward keeps nothing from a forward call)"}
 
 
+def measure_other(pkg, wid, dev, stream, flush, steps=20, warmup=5):
+    """One of the other benchmark configurations: plain calls (or a graph replay for the
+    serving step), with the same roofline arithmetic as the headline."""
+    w = make_workload(wid)
+    if w.graph:
+        return measure_graph(pkg, w, dev, stream, flush)
+    c = Call(pkg, w, dev)
+    step_ms, stage_ms, prof_ms, _, _ = time_call(pkg, c, stream, flush, steps, warmup)
+    names = stage_names(w)
+    rf = roofline_of(w, statistics.fmean(step_ms), stage_ms, names, wid)
+    del c
+    return {"workload": w.name, "timing": f"plain calls, mean of {steps} after {warmup}, L2 flushed",
+            "ms_per_call": statistics.fmean(step_ms), "tokens_per_s": w.T / (statistics.fmean(step_ms) / 1e3),
+            "step_frac": rf["step_frac"], "stage_frac": rf["frac"], "dominant_stage": rf["kernel"],
+            "stages_ms": dict(zip(names, stage_ms)), "profiled_ms_per_call": prof_ms,
+            "alg_bytes": rf["alg_bytes_per_launch"], "roofline_us": rf["roofline_us"],
+            "launches_per_call": launches_per_call(w)}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", type=int, default=2, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", type=int, default=HEADLINE_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="gdp", choices=["gdp", "reference"])
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--no-others", action="store_true", help="skip the per_workload legs")
     ap.add_argument("--clocks-dir", default=None, help="folder for the raw clock samples (default: a temp folder)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -398,102 +579,30 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream(dev)
-    q, k, v = w.q.to(dev), w.k.to(dev), w.v.to(dev)
-    g = None if w.g is None else w.g.to(dev)
-    beta = None if w.beta is None else w.beta.to(dev)
-    cu = w.cu_seqlens.to(dev)
-    init = None if w.initial_state is None else w.initial_state.to(dev)
-    cache = None if w.state is None else w.state.to(dev)
-    sidx = None if w.state_indices is None else w.state_indices.to(dev)
-    out = torch.empty((w.T, w.H, w.d), dtype=torch.bfloat16, device=dev)
-    fin = torch.empty((w.N, w.H, w.d, w.d), dtype=torch.float32, device=dev) if (
-        w.output_final_state and cache is None) else None
-    cs = torch.zeros((pkg.gdp_nt_pad(w.T, w.N), w.H, w.d, w.d), dtype=torch.float32, device=dev) if (
-        w.return_chunk_states) else None
-    ci = cid = co = None
-    if w.prebuilt_descriptors:
-        ci, cid, co = pkg.gdp_build_descriptors(cu, w.T, w.M)
-    ws = pkg.alloc_workspace(w.T, w.N, w.H, w.d, w.d, w.M, dev)
-    a = pkg.make_args(q, k, v, g, beta, cu, w.M, w.scale, init, cache, sidx, out, fin, cs, ci, cid, co, None, None,
-                      w.use_qk_l2norm, ws, None)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    sid = stream.cuda_stream
+    c = Call(pkg, w, dev)
     torch.cuda.synchronize()
 
-    def new_events():
-        # torch creates the CUDA event lazily at its first record(); record once so the raw
-        # handle exists and torch accepts elapsed_time(); the library then re-records it.
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-        for e in evs:
-            e.record(stream)
-        return evs
-
-    def step(evs):
-        # the profiled form: events between the kernels, so each kernel runs alone (no
-        # programmatic overlap); gives the per-kernel durations
-        with torch.cuda.stream(stream):
-            flush.zero_()
-        pkg.gdp_prefill_varlen_profiled(a, evs, sid)
-
-    def step_plain(e0, e1):
-        # the call as a user makes it (its kernels overlap their launches); timed as a whole
-        with torch.cuda.stream(stream):
-            flush.zero_()
-        e0.record(stream)
-        pkg.gdp_prefill_varlen(a, sid)
-        e1.record(stream)
-
-    def timing_events():
-        return [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-
-    for _ in range(args.warmup):
-        step_plain(*timing_events())
-        step(new_events())
-    torch.cuda.synchronize()
-
-    plain = [timing_events() for _ in range(args.steps)]
     if dist:
         dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local, args.clocks_dir) as clk:
-        wall0 = time.perf_counter()
-        for s in range(args.steps):
-            step_plain(*plain[s])
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - wall0
+    step_ms, stage_ms, prof_ms, clk, wall = time_call(pkg, c, stream, flush, args.steps, args.warmup,
+                                                       args.clocks_dir, sample_clocks=True)
     if dist:
         dist.barrier()
-    step_ms = [e0.elapsed_time(e1) for e0, e1 in plain]
-    # per-kernel durations: a second pass of the same steps through the profiled form
-    events = [new_events() for _ in range(args.steps)]
-    for s in range(args.steps):
-        step(events[s])
-    torch.cuda.synchronize()
-    stage = [[ev[i].elapsed_time(ev[i + 1]) for i in range(3)] for ev in events]
-    profiled_step_ms = statistics.fmean(ev[0].elapsed_time(ev[3]) for ev in events)
     total_s = max_over_ranks(sum(step_ms) / 1e3, dist, dev)
     value = world * w.T * args.steps / total_s
-    kernel_names = ["gdp_desc_kernel", "gdp_wy_kernel", scan_stage_name(w)]
-    kernel_ms = [statistics.fmean(x[i] for x in stage) for i in range(3)]
-    dom = max(range(3), key=lambda i: kernel_ms[i])
-    peak, peak_src = measured_peaks()
-    ab = alg_bytes(w)
-    achieved = ab / (kernel_ms[dom] / 1e3) / 1e9
-    step_gbs = ab / (statistics.fmean(step_ms) / 1e3) / 1e9
-    tr = NCU_TRAFFIC.get(kernel_names[dom])
-    traffic = (tr["bytes_per_launch"] if (tr and tr.get("sha") == _kernel_sha(kernel_names[dom])
-                                          and tr.get("workload") == args.workload) else None)
+    names = stage_names(w)
+    rf = roofline_of(w, statistics.fmean(step_ms), stage_ms, names, args.workload)
 
-    # ---- end to end: pinned host inputs -> device -> call -> host outputs
+    # ---- end to end: pinned host inputs -> device -> call -> host outputs, same stream
     host_in = [t.pin_memory() for t in (w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, w.initial_state, w.state,
                                         w.state_indices) if t is not None]
-    dev_in = [t for t in (q, k, v, g, beta, cu, init, cache, sidx) if t is not None]
-    dev_out = [t for t in (out, fin, cs) if t is not None]
-    if cache is not None:
-        dev_out.append(cache)
+    dev_in = c.inputs()
+    dev_out = c.outputs()
     host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_out]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
+    sid = stream.cuda_stream
     e2e_ms = []
     for s in range(args.e2e_steps + 2):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -502,7 +611,7 @@ def main():
             e0.record(stream)
             for hsrc, ddst in zip(host_in, dev_in):
                 ddst.copy_(hsrc, non_blocking=True)
-            pkg.gdp_prefill_varlen(a, sid)
+            pkg.gdp_prefill_varlen(c.args, sid)
             for dsrc, hdst in zip(dev_out, host_out):
                 hdst.copy_(dsrc, non_blocking=True)
             e1.record(stream)
@@ -510,7 +619,15 @@ def main():
         if s >= 2:
             e2e_ms.append(e0.elapsed_time(e1))
     e2e_value = world * w.T / (statistics.fmean(e2e_ms) / 1e3)
+    del host_in, host_out, c
+    torch.cuda.empty_cache()
 
+    others = {}
+    if rank == 0 and not args.no_others:
+        for wid in PER_WORKLOAD:
+            if wid != args.workload:
+                others[str(wid)] = measure_other(pkg, wid, dev, stream, flush)
+                torch.cuda.empty_cache()
     decode = measure_decode(pkg, dev, flush, stream) if rank == 0 else None
     bwd = measure_backward(pkg, dev, flush, stream, w) if (rank == 0 and not args.no_backward) else None
 
@@ -523,18 +640,17 @@ def main():
             "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16/tf32 MMA, f32 state", "data": "synthetic",
             "config": {**w.describe(), "l2_flush": True, "flush_bytes": flush.numel()},
-            "roofline": {"bound": "hbm", "kernel": kernel_names[dom], "achieved": achieved, "peak": peak,
-                         "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
-                         "alg_bytes_per_launch": ab, "kernel_ms": kernel_ms[dom],
-                         "step_achieved": step_gbs, "step_frac": step_gbs / peak,
-                         "alg_gflop_per_step": alg_flops(w) / 1e9},
-            "kernels_ms": dict(zip(kernel_names, kernel_ms)),
-            "profiled_ms_per_step": profiled_step_ms,
+            "roofline": rf,
+            "step_roofline": {"achieved": rf["step_achieved"], "frac": rf["step_frac"], "unit": "GB/s",
+                              "scope": "whole call (all kernels), algorithmic bytes / mean step time"},
+            "stages_ms": dict(zip(names, stage_ms)),
+            "profiled_ms_per_step": prof_ms,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": statistics.fmean(e2e_ms)},
             "gpu_launches": launches_per_call(w) * args.steps,
-            "clocks": clk.summary(),
+            "clocks": clk,
+            "per_workload": others,
             "decode_step": decode,
             "backward": bwd,
             "wall_s_timed": wall,

@@ -90,6 +90,10 @@ def load_library(path: str | None = None):
     lib.gdp_decode_step.argtypes = [ctypes.POINTER(GdpPrefillArgs), _vp]
     lib.gdp_prefill_varlen_static_scratch.restype = _int
     lib.gdp_prefill_varlen_static_scratch.argtypes = [ctypes.POINTER(GdpPrefillArgs), _vp]
+    lib.gdp_static_scratch_bytes.restype = _sz
+    lib.gdp_arm_wait_expiry_test.restype = _int
+    lib.gdp_arm_wait_expiry_test.argtypes = [ctypes.c_uint64]
+    lib.gdp_static_scratch_bytes.argtypes = []
     lib.gdp_prefill_varlen_backward.restype = _int
     lib.gdp_prefill_varlen_backward.argtypes = [ctypes.POINTER(GdpBackwardArgs), _vp]
     lib.gdp_backward_workspace_bytes.restype = _sz
@@ -172,12 +176,24 @@ def gdp_prefill_varlen_profiled(args: GdpPrefillArgs, events, stream: int | None
         raise GdpError(st, lib.gdp_last_error().decode())
 
 
-GDP_STATIC_SCRATCH_BYTES = 64 << 20
+def gdp_static_scratch_bytes() -> int:
+    """Size of the library's static scratch array (the largest workspace the
+    static-scratch entry point serves)."""
+    return int(load_library().gdp_static_scratch_bytes())
+
+
+def gdp_arm_wait_expiry_test(limit_ns: int) -> None:
+    """Arm the calling thread's next prefill call to exercise the bounded-wait failure path
+    (its scan waits give up after limit_ns; one of them runs out); see the header."""
+    lib = load_library()
+    st = lib.gdp_arm_wait_expiry_test(int(limit_ns))
+    if st != GDP_OK:
+        raise GdpError(st, lib.gdp_last_error().decode())
 
 
 def gdp_prefill_varlen_static_scratch(args: GdpPrefillArgs, stream: int | None = None) -> None:
     """The prefill without a caller workspace: the library's own static scratch
-    (GDP_STATIC_SCRATCH_BYTES) is used instead, for callers that cannot allocate
+    (gdp_static_scratch_bytes()) is used instead, for callers that cannot allocate
     device memory; args.workspace is ignored.  Calls that overlap on the GPU race."""
     lib = load_library()
     st = lib.gdp_prefill_varlen_static_scratch(ctypes.byref(args), ctypes.c_void_p(_stream(stream)))

@@ -15,6 +15,8 @@
 namespace {
 
 thread_local char g_last_error[512] = "";
+// gdp_arm_wait_expiry_test: the wait limit (ns) of the calling thread's next prefill, 0 = not armed
+thread_local uint64_t g_expiry_test_ns = 0;
 
 gdp_status fail(gdp_status st, const char *fmt, ...) {
   va_list ap;
@@ -319,6 +321,13 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
   p.piece_buf = pp.len > 0 ? (float *)(ws + lay.piece) : nullptr;
   p.xfer = 0;
   p.xfer_out = nullptr;
+  p.wait_limit_ns = 1000000000ull;
+  p.test_withhold_copy = 0;
+  if (g_expiry_test_ns) {  // armed by gdp_arm_wait_expiry_test: this call only
+    p.wait_limit_ns = g_expiry_test_ns;
+    p.test_withhold_copy = 1;
+    g_expiry_test_ns = 0;
+  }
   if (xfer_out) {  // B (rows 0 .. N-1) and Phi (rows N .. 2N-1) of every sequence, no outputs
     p.xfer = 1;
     p.xfer_out = xfer_out;
@@ -434,6 +443,14 @@ GDP_EXPORT gdp_status gdp_prefill_plan(int64_t T, int64_t N, int H, int K, int V
 }
 
 GDP_EXPORT const char *gdp_last_error(void) { return g_last_error; }
+
+GDP_EXPORT gdp_status gdp_arm_wait_expiry_test(uint64_t limit_ns) {
+  g_last_error[0] = 0;
+  if (limit_ns < 100000ull || limit_ns > 1000000000ull)
+    return fail(GDP_ERR_INVALID_ARG, "limit_ns %llu outside [1e5, 1e9]", (unsigned long long)limit_ns);
+  g_expiry_test_ns = limit_ns;
+  return GDP_OK;
+}
 
 GDP_EXPORT int gdp_abi_version(void) { return GDP_ABI_VERSION; }
 

@@ -154,6 +154,11 @@ struct Problem {
   // outputs.  xfer_out: [2][N][H][V][K] fp32.
   int xfer;
   float *xfer_out;
+  // Limit of every bounded wait of the scan (kWaitLimitNs, about a second, unless a test of the
+  // failure path shortened it) and that test's switch: CTA (0, 0) withholds the first image copy,
+  // so that one of its waits runs out (gdp_arm_wait_expiry_test).
+  uint64_t wait_limit_ns;
+  int test_withhold_copy;
 };
 
 // Everything the backward kernels need about one call (gdp_backward.cu).  Heads are

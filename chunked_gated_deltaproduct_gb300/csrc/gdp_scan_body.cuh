@@ -182,6 +182,8 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
   __shared__ ChunkInfo info[2];
   __shared__ int st_ok[4];
   __shared__ volatile int abort_flag;
+  // every wait of this launch gives up after wl (about a second unless a test shortened it)
+  const uint64_t wl = p.wait_limit_ns;
 
   // incoming state source
   int slot = -1;
@@ -329,7 +331,8 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
   }
   if (warp == 9 && lane == 0)
     for (int64_t e = 0; e < nst && e < nrun; ++e) {
-      load_part1(e);
+      // (a test of the bounded waits withholds the first copy of CTA (0, 0): its wait runs out)
+      if (!(p.test_withhold_copy && e == 0 && blockIdx.x == 0 && blockIdx.y == 0)) load_part1(e);
       load_part2(e);
     }
   tc_fence_before();
@@ -363,7 +366,7 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
       const bool renorm = fast ? (gam * mt.gamma_last < kRenormMinGamma) : (gam != 1.f);
       const float gam_pass = renorm ? 1.f : gam;                  // Gamma during the chunk's products
       const float gam_next = fast ? gam_pass * mt.gamma_last : 1.f;  // Gamma' after it
-      if (e >= 2 && !mbar_wait_or_abort(&yo_free[b], (uint32_t)(((e >> 1) - 1) & 1), &abort_flag)) break;
+      if (e >= 2 && !mbar_wait_or_abort(&yo_free[b], (uint32_t)(((e >> 1) - 1) & 1), &abort_flag, wl)) break;
       tc_fence_after();
       const uint32_t to = tO(b), ty = to + (uint32_t)QP;
       const float inv = 1.f / gam_next;
@@ -379,7 +382,7 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
       }
       if (tid == 0) info[b] = ChunkInfo{gam_next, mt.nq, mt.p0};
       if (renorm && e >= 1) {  // the renormalisation rewrites the final S_hat of chunk e
-        if (!mbar_wait_or_abort(&b2_done[(e - 1) & 1], (uint32_t)(((e - 1) >> 1) & 1), &abort_flag)) break;
+        if (!mbar_wait_or_abort(&b2_done[(e - 1) & 1], (uint32_t)(((e - 1) >> 1) & 1), &abort_flag, wl)) break;
         tc_fence_after();
       }
       if (renorm) {
@@ -402,12 +405,12 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
       if (emit || !fast) {
         // between the two batches: snapshot S_e = gam_pass S_hat (read alongside batch 1) and,
         // for a slow image, S_hat <- gamma_last S_hat once batch 1 has read it
-        if (emit && n_emit >= 1 && !mbar_wait_or_abort(&bk_free, (uint32_t)((n_emit - 1) & 1), &abort_flag)) break;
+        if (emit && n_emit >= 1 && !mbar_wait_or_abort(&bk_free, (uint32_t)((n_emit - 1) & 1), &abort_flag, wl)) break;
         if (!fast) {  // batch 1 has read S_hat (so chunk e - 1's batch 2 is complete too)
-          if (!mbar_wait_or_abort(&b1_done[b], (uint32_t)((e >> 1) & 1), &abort_flag)) break;
+          if (!mbar_wait_or_abort(&b1_done[b], (uint32_t)((e >> 1) & 1), &abort_flag, wl)) break;
         } else if (!renorm && e >= 1) {  // S_hat of chunk e is final; waited for only now, so that
           // batch 1 (issued on yo_ready above) is not held back by this round trip
-          if (!mbar_wait_or_abort(&b2_done[(e - 1) & 1], (uint32_t)(((e - 1) >> 1) & 1), &abort_flag)) break;
+          if (!mbar_wait_or_abort(&b2_done[(e - 1) & 1], (uint32_t)(((e - 1) >> 1) & 1), &abort_flag, wl)) break;
         }
         tc_fence_after();
         // (a slow chunk was renormalised, so gam_pass is 1 there and one array serves both)
@@ -432,6 +435,7 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
       }
       gam = gam_next;
     }
+    tmem_st_wait();  // (an aborted chunk may leave stores in flight; the columns are freed below)
   } else if (warp < 8) {
     // ---------------- store warps ----------------
     float gam_fin = 1.f;
@@ -440,7 +444,7 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
     for (int64_t e = 0; e < nrun; ++e) {
       const int b = (int)(e & 1);
       // the four store warps take the same exit decision (they meet at named barriers)
-      const bool ok = mbar_wait_or_abort(&b2_done[b], (uint32_t)((e >> 1) & 1), &abort_flag);
+      const bool ok = mbar_wait_or_abort(&b2_done[b], (uint32_t)((e >> 1) & 1), &abort_flag, wl);
       if (lane == 0) st_ok[q4] = ok ? 1 : 0;
       if (tid == 128) bulk_wait_read<0>();  // the output staging's TMA store (if any) has read it
       named_sync(1, 128);  // also: every thread has finished reading the previous chunk's staging
@@ -521,8 +525,8 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
       for (int64_t e = 0; e < nrun; ++e) {
         const int st = (int)(e % nst), b = (int)(e & 1);
         unsigned char *stage = sm + st * sbytes;
-        if (!mbar_wait_or_abort(&full1[st], (uint32_t)((e / nst) & 1), &abort_flag)) break;
-        if (!mbar_wait_or_abort(&yo_ready[b], (uint32_t)((e >> 1) & 1), &abort_flag)) break;
+        if (!mbar_wait_or_abort(&full1[st], (uint32_t)((e / nst) & 1), &abort_flag, wl)) break;
+        if (!mbar_wait_or_abort(&yo_ready[b], (uint32_t)((e >> 1) & 1), &abort_flag, wl)) break;
         tc_fence_after();
         const ImageMeta mt = *reinterpret_cast<const ImageMeta *>(stage + il.meta);
         const bool mid = emits(e) || mt.fast == 0;
@@ -539,9 +543,9 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
                         id1y, 1);
         }
         mma_commit(&b1_done[b]);
-        if (!mbar_wait_or_abort(&full2[st], (uint32_t)((e / nst) & 1), &abort_flag)) break;
+        if (!mbar_wait_or_abort(&full2[st], (uint32_t)((e / nst) & 1), &abort_flag, wl)) break;
         if (mid) {
-          if (!mbar_wait_or_abort(&mid_done, (uint32_t)(n_mid & 1), &abort_flag)) break;
+          if (!mbar_wait_or_abort(&mid_done, (uint32_t)(n_mid & 1), &abort_flag, wl)) break;
           ++n_mid;
           tc_fence_after();
         }
@@ -578,9 +582,9 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
     for (int64_t e = 0; e + nst < nrun; ++e) {
       prefetch(e + nst + kPrefetch);
       const int b = (int)(e & 1);
-      if (!mbar_wait_or_abort(&b1_done[b], (uint32_t)((e >> 1) & 1), &abort_flag)) break;
+      if (!mbar_wait_or_abort(&b1_done[b], (uint32_t)((e >> 1) & 1), &abort_flag, wl)) break;
       load_part1(e + nst);
-      if (!mbar_wait_or_abort(&b2_done[b], (uint32_t)((e >> 1) & 1), &abort_flag)) break;
+      if (!mbar_wait_or_abort(&b2_done[b], (uint32_t)((e >> 1) & 1), &abort_flag, wl)) break;
       load_part2(e + nst);
     }
   }

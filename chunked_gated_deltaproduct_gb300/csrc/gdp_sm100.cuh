@@ -213,20 +213,24 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 // As mbar_wait, but gives up at once when *abort_flag is set by another thread
-// (and sets it when its own time runs out), so a stuck CTA leaves all roles quickly.
+// (and sets it when its own time, limit_ns, runs out), so a stuck CTA leaves all roles quickly.
 // The slow path of mbar_wait_or_abort, out of line: kernels wait at many places, and one
 // copy of the sleep/timeout loop keeps their code small.
-static __device__ __noinline__ bool mbar_wait_or_abort_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag);
-__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // about a second
+static __device__ __noinline__ bool mbar_wait_or_abort_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                                            uint64_t limit_ns);
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                                   uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try(bar, parity)) return true;
-  return mbar_wait_or_abort_slow(bar, parity, abort_flag);
+  return mbar_wait_or_abort_slow(bar, parity, abort_flag, limit_ns);
 }
-static __device__ __noinline__ bool mbar_wait_or_abort_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+static __device__ __noinline__ bool mbar_wait_or_abort_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                                            uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0; it < (1u << 20); ++it) {
     if (mbar_try_sleep(bar, parity, 100000u)) return true;  // sleeps up to 0.1 ms per try
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > 1000000000ull) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       *abort_flag = 1;
       return false;
     }

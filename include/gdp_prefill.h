@@ -276,6 +276,23 @@ gdp_status gdp_chain_states(const float *s0, const float *phi, const float *b, i
                             int d, float *s_out, uint32_t *device_status, void *stream);
 
 /*
+ * gdp_arm_wait_expiry_test: a test of the failure path (no counterpart on the
+ * pages).  Every spin-wait of the kernels is bounded: a wait that does not
+ * complete within its limit (about a second) sets GDP_DEV_ERR_TIMEOUT in
+ * *device_status, drains the CTA's own tensor-core work and copies, frees its
+ * tensor memory and returns, so the CUDA context stays usable and the host
+ * reads the status after the stream completes.  This call arms the calling
+ * host thread's NEXT gdp_prefill_varlen* call to exercise that path: its scan
+ * waits give up after limit_ns (1e5 .. 1e9 ns), and the scan CTA of sequence
+ * 0, head 0 withholds its first operand copy, so one of its waits runs out.
+ * That call's outputs are undefined (those of sequence 0, head 0 at least) and
+ * its status word gets GDP_DEV_ERR_TIMEOUT; later calls are unaffected.  No
+ * fault, trap or endless loop is involved.  GDP_ERR_INVALID_ARG for a limit
+ * outside the range.
+ */
+gdp_status gdp_arm_wait_expiry_test(uint64_t limit_ns);
+
+/*
  * gdp_prefill_varlen_static_scratch: the same prefill for callers that cannot
  * allocate device memory.  No counterpart on the pages: it exists because the
  * main entry point needs a caller-owned workspace, and some callers cannot
@@ -288,14 +305,19 @@ gdp_status gdp_chain_states(const float *s0, const float *phi, const float *b, i
  * (64 MiB) array inside the library, held by every GPU that loads the library
  * until the process exits.  A shape whose gdp_prefill_workspace_bytes exceeds
  * it is rejected with GDP_ERR_WORKSPACE before any launch.  Nothing is
- * allocated.  The first call on each device looks the array's device address
- * up (cudaGetSymbolAddress, that device current) and caches it; make that
- * first call outside any stream capture.  All calls share the array, so calls
- * whose kernels overlap on the GPU (other streams, other threads) race:
- * serialise them.  Nothing in the array needs to start at zero.
+ * allocated.  Each CUDA context holds its own copy of the array: the first call
+ * made in a context (with it current) looks the array's device address up
+ * (cudaGetSymbolAddress) and caches it under the context's unique ID, so a
+ * context created later -- another runtime's own context, or the primary
+ * context that replaces one destroyed by cudaDeviceReset -- gets its own lookup.
+ * Make the first call in each context outside any stream capture.  All calls
+ * share the array, so calls whose kernels overlap on the GPU (other streams,
+ * other threads) race: serialise them.  Nothing in the array needs to start at
+ * zero.  gdp_static_scratch_bytes() returns the array's size.
  */
 #define GDP_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
 gdp_status gdp_prefill_varlen_static_scratch(const gdp_prefill_args *args, void *stream);
+size_t gdp_static_scratch_bytes(void);
 
 /*
  * Build the varlen descriptors on the device (Megatron page, parameters

@@ -262,3 +262,11 @@ def test_sequence_parallel_wrappers_reject_bad_tensors():
     with pytest.raises(pkg.GdpError):
         q = torch.zeros((4, 1, 64), dtype=torch.bfloat16)
         pkg.chunk_gated_delta_product_transfer(q, q, q, cu_seqlens=None)
+
+
+def test_static_scratch_size_matches_header(lib):
+    """The static-scratch size the library reports is the header's GDP_STATIC_SCRATCH_BYTES."""
+    text = open(os.path.join(HEADER_DIR, "gdp_prefill.h")).read()
+    m = re.search(r"#define\s+GDP_STATIC_SCRATCH_BYTES\s+\(\(size_t\)(\d+)\s*<<\s*(\d+)\)", text)
+    assert m, "GDP_STATIC_SCRATCH_BYTES not found in the header"
+    assert pkg.gdp_static_scratch_bytes() == int(m.group(1)) << int(m.group(2))

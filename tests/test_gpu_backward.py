@@ -129,13 +129,15 @@ def test_backward_segmented_recompute(cuda_device):
 
 
 def test_backward_repeatable_and_graph_capturable(cuda_device):
-    """Two calls agree to the atomics' rounding, and the call captures into a CUDA graph."""
+    """Two calls give identical bits (the kernels use no atomics: every gradient element is
+    written once by one thread, in a fixed order), and the call captures into a CUDA graph whose
+    replay gives those same bits."""
     w = make_custom([100, 180], 2, 128, 2, seed=11, init_sigma=0.1)
     d_out, d_fin = make_cotangents(w, seed=12)
     a = _run(w, cuda_device, d_out, d_fin)
     b = _run(w, cuda_device, d_out, d_fin)
     for n in ("dq", "dk", "dv", "dg", "dbeta", "d_initial_state"):
-        assert torch.allclose(a[n], b[n], rtol=1e-4, atol=1e-5), n
+        assert torch.equal(a[n], b[n]), n
     dev = cuda_device
     dd = lambda x: None if x is None else x.to(dev)
     args = [dd(w.q), dd(w.k), dd(w.v), dd(w.g), dd(w.beta), w.cu_seqlens.to(dev), w.M, dd(d_out)]
@@ -153,7 +155,7 @@ def test_backward_repeatable_and_graph_capturable(cuda_device):
     graph.replay()
     torch.cuda.synchronize()
     for n in ("dq", "dk", "dv", "dg", "dbeta", "d_initial_state"):
-        assert torch.allclose(out[n], a[n], rtol=1e-4, atol=1e-5), n
+        assert torch.equal(out[n], a[n]), n
 
 
 def test_backward_workload2_full_size(cuda_device):

@@ -25,13 +25,13 @@ def _oracle(w, heads=None, **kw):
 
 
 def _compare(w, o, fin, cs, ref, heads=None):
-    check_o(o.cpu(), ref["o"], heads=heads)
+    check_o(o.cpu(), ref["o"], heads=heads, cu_seqlens=w.cu_seqlens)
     if fin is not None and ref["final_state"] is not None:
         check_state(fin.cpu(), ref["final_state"], heads=heads, label="final_state")
     if cs is not None:
         nt = ref["chunk_states"].shape[0]
         assert nt == w.NT
-        check_state(cs[:nt].cpu(), ref["chunk_states"], heads=heads, label="chunk_states")
+        check_state(cs[:nt].cpu(), ref["chunk_states"], heads=heads, label="chunk_states", seq_offsets=ref["chunk_offsets"])
         if cs.shape[0] > nt:  # rows past the real count are not written
             assert torch.count_nonzero(cs[nt:]).item() == 0
 
@@ -94,7 +94,7 @@ def test_workload4_long_context(cuda_device):
     ref = _oracle(w, heads=heads)
     check_o(o, ref["o"][:, heads])
     check_state(fin, ref["final_state"][:, heads], label="final_state")
-    check_state(cs[:w.NT], ref["chunk_states"][:, heads], label="chunk_states")
+    check_state(cs[:w.NT], ref["chunk_states"][:, heads], label="chunk_states", seq_offsets=ref["chunk_offsets"])
 
 
 @pytest.mark.slow
@@ -147,7 +147,7 @@ def test_segmented_uneven_lengths(cuda_device):
     ref = _oracle(w, heads=heads)
     check_o(o.cpu(), ref["o"], heads=heads)
     check_state(fin.cpu(), ref["final_state"], heads=heads, label="final_state")
-    check_state(cs[:w.NT].cpu(), ref["chunk_states"], heads=heads, label="chunk_states")
+    check_state(cs[:w.NT].cpu(), ref["chunk_states"], heads=heads, label="chunk_states", seq_offsets=ref["chunk_offsets"])
 
 
 def test_segmented_cache_graph(cuda_device):

@@ -52,7 +52,7 @@ def _check(w, o, fin, cs, d, heads=None):
     if fin is not None and ref["final_state"] is not None:
         check_state(fin.cpu(), ref["final_state"], heads=heads, label="final_state")
     if cs is not None:
-        check_state(cs[:w.NT].cpu(), ref["chunk_states"], heads=heads, label="chunk_states")
+        check_state(cs[:w.NT].cpu(), ref["chunk_states"], heads=heads, label="chunk_states", seq_offsets=ref["chunk_offsets"])
     if w.state is not None:
         used = [s for s in w.state_indices.tolist() if s >= 0]
         unused = [s for s in range(w.state.shape[0]) if s not in used]
@@ -126,6 +126,6 @@ def test_split_chains_repeatable_and_graph_capturable(cuda_device):
     assert torch.equal(out, o1) and torch.equal(cs, c1) and torch.equal(d["state"], s1)
     ref = _oracle(w)
     check_o(o1.float().cpu(), ref["o"])
-    check_state(c1[:w.NT].cpu(), ref["chunk_states"], label="chunk_states")
+    check_state(c1[:w.NT].cpu(), ref["chunk_states"], label="chunk_states", seq_offsets=ref["chunk_offsets"])
     used = [x for x in w.state_indices.tolist() if x >= 0]
     check_state(s1.cpu()[used], ref["state_out"][used], label="cache slots")

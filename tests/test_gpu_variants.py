@@ -35,7 +35,7 @@ def _check_prefill(w, dev):
         check_state(fin.cpu(), ref["final_state"], label="final_state")
     if cs is not None:
         nt = ref["chunk_states"].shape[0]
-        check_state(cs[:nt].cpu(), ref["chunk_states"], label="chunk_states")
+        check_state(cs[:nt].cpu(), ref["chunk_states"], label="chunk_states", seq_offsets=ref["chunk_offsets"])
     return ref
 
 
