@@ -104,6 +104,8 @@ def load_library(path: str | None = None):
     lib.gdp_prefill_transfer.argtypes = [ctypes.POINTER(GdpPrefillArgs), _vp, _vp]
     lib.gdp_chain_states.restype = _int
     lib.gdp_chain_states.argtypes = [_vp, _vp, _vp, _i64, _i64, _int, _int, _vp, _vp, _vp]
+    lib.gdp_prefill_fused.restype = _int
+    lib.gdp_prefill_fused.argtypes = [_i64, _i64, _int, _int, _int, _int]
     lib.gdp_prefill_plan.restype = _int
     lib.gdp_prefill_plan.argtypes = [_i64, _i64, _int, _int, _int, _int] + [ctypes.POINTER(_i64)] * 4
     lib.gdp_build_descriptors.restype = _int
@@ -150,6 +152,11 @@ def gdp_prefill_plan(T: int, N: int, H: int, K: int, V: int, M: int) -> dict:
     if st != GDP_OK:
         raise GdpError(st, lib.gdp_last_error().decode())
     return dict(zip(("segments", "piece_chunks", "piece_rows", "launches"), (int(x.value) for x in out)))
+
+
+def gdp_prefill_fused(T: int, N: int, H: int, K: int, V: int, M: int) -> bool:
+    """Whether a common-contract call of this shape runs as the one fused kernel (shape-only)."""
+    return bool(load_library().gdp_prefill_fused(T, N, H, K, V, M))
 
 
 def _stream(stream):

@@ -339,11 +339,14 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
     p.slots = nullptr;
     p.num_slots = 0;
   }
+  // the fused kernel (WY work, scan and outputs in one launch) serves the common contract of a
+  // plain forward call whose chains are not split
+  const bool fused = !rc && !xfer_out && pp.len == 0 && gdp::fused_serves(p);
   // desc -> WY -> scan on one stream overlap their launches (programmatic dependent launch);
   // the profiled form records events between them, so there each kernel runs alone
-  p.pdl = (nseg == 1 && !ev) ? 1 : 0;
-  SideStreams *ss = nseg > 1 ? side_streams() : nullptr;
-  if (nseg > 1 && !ss) return fail(GDP_ERR_CUDA, "could not create the internal streams of the segmented mode");
+  p.pdl = ((nseg == 1 || fused) && !ev) ? 1 : 0;
+  SideStreams *ss = (nseg > 1 && !fused) ? side_streams() : nullptr;
+  if (nseg > 1 && !fused && !ss) return fail(GDP_ERR_CUDA, "could not create the internal streams of the segmented mode");
 
   cudaError_t e;
   if (nprebuilt == 3)  // only the internal expanded-stream offsets
@@ -354,6 +357,13 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
                                 co_desc, (int32_t *)p.cod, p.status, stream);
   if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "descriptor kernel: %s", cudaGetErrorString(e));
   if (ev && (st = record(ev[1], stream)) != GDP_OK) return st;
+  if (fused) {  // no WY stage of its own: events 1 and 2 mark the same point
+    if (ev && (st = record(ev[2], stream)) != GDP_OK) return st;
+    e = gdp::launch_fused(p, stream);
+    if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "fused kernel: %s", cudaGetErrorString(e));
+    if (ev && (st = record(ev[3], stream)) != GDP_OK) return st;
+    return GDP_OK;
+  }
   if (nseg == 1) {
     e = gdp::launch_wy(p, stream);
     if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "WY kernel: %s", cudaGetErrorString(e));
@@ -438,8 +448,14 @@ GDP_EXPORT gdp_status gdp_prefill_plan(int64_t T, int64_t N, int H, int K, int V
   if (segments) *segments = nseg;
   if (piece_chunks) *piece_chunks = pp.len;
   if (piece_rows) *piece_rows = pp.rows;
-  if (launches) *launches = N == 0 ? 0 : 1 + (nseg > 1 ? 2 * nseg : (pp.len > 0 ? 4 : 2));
+  const bool fused = pp.len == 0 && gdp::fused_shape(K, V, M);
+  if (launches) *launches = N == 0 ? 0 : 1 + (fused ? 1 : (nseg > 1 ? 2 * nseg : (pp.len > 0 ? 4 : 2)));
   return GDP_OK;
+}
+
+GDP_EXPORT int gdp_prefill_fused(int64_t T, int64_t N, int H, int K, int V, int M) {
+  if (!shape_ok(T, N, H, K, V, M)) return 0;
+  return piece_plan(T, N, H, M).len == 0 && gdp::fused_shape(K, V, M) ? 1 : 0;
 }
 
 GDP_EXPORT const char *gdp_last_error(void) { return g_last_error; }

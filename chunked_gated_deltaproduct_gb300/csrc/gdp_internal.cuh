@@ -304,6 +304,12 @@ cudaError_t launch_wy_variant(const Problem &p, cudaStream_t stream, bool f16, b
 cudaError_t launch_scan(const Problem &p, cudaStream_t stream);
 // The scan for float16 inputs (f16) and / or a bfloat16 dense initial state (init16).
 cudaError_t launch_scan_variant(const Problem &p, cudaStream_t stream, bool f16, bool init16);
+// The fused prefill (gdp_fused.cu): WY work, scan, outputs and state scatter in one kernel, one
+// CTA per (sequence, head), for the common contract (bf16 q / k / v, fp32 natural-log g and
+// beta, fp32 states, K = V = 128, qpad <= 32); fused_serves says whether a call is served.
+bool fused_serves(const Problem &p);
+bool fused_shape(int K, int V, int M);
+cudaError_t launch_fused(const Problem &p, cudaStream_t stream);
 // Split chains: the entering state of every piece of a split sequence (gdp_pieces.cu).
 cudaError_t launch_piece_combine(const Problem &p, cudaStream_t stream);
 // S_{j+1} = S_j Phi_j + B_j for j < steps from S_0 (NULL: zero), Phi / B [steps][N][H][d][d],

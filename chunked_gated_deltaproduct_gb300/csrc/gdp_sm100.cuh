@@ -276,6 +276,13 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *tmap, in
       : "memory");
 }
 
+// Prefetch of one 3-D box of the map `tmap` at (x, y, z) into L2 (no shared-memory destination,
+// no completion; x * element size a multiple of 16 bytes).
+__device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 // Bulk copy (TMA, non-tensor) shared -> global in the calling thread's bulk async-group
 // (16-byte aligned, size % 16 == 0).  The group is closed by bulk_commit; bulk_wait_read<N>
 // returns once at most N of the thread's newest groups may still be reading shared memory.

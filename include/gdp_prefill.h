@@ -223,6 +223,16 @@ gdp_status gdp_prefill_plan(int64_t T, int64_t N, int H, int K, int V, int num_h
                             int64_t *piece_chunks, int64_t *piece_rows, int64_t *launches);
 
 /*
+ * 1 when a call of this shape over the common contract (bf16 q/k/v, fp32 natural-log g and
+ * beta, fp32 states, chains not split into pieces) runs as one fused kernel after the
+ * descriptor kernel -- the WY work, the state scan, the outputs and the state scatter of every
+ * (sequence, head) in one CTA, with no operand images in the workspace -- and 0 when it runs
+ * the staged kernels (gdp_prefill_plan).  Served: K = V = 128 and num_householder >= 2.
+ * Shape-only; 0 for a bad shape.
+ */
+int gdp_prefill_fused(int64_t T, int64_t N, int H, int K, int V, int num_householder);
+
+/*
  * The prefill forward pass: enqueue descriptors (unless prebuilt), the prep
  * + WY kernel and the state-scan / output kernel on `stream`.
  * Returns GDP_OK once enqueued.

@@ -200,8 +200,15 @@ def test_prefill_plan(lib):
     assert split["segments"] == 1 and split["piece_chunks"] == 6 and split["launches"] == 5
     assert split["piece_rows"] * 8 <= 128
     assert pkg.gdp_prefill_plan(32768, 8, 16, 128, 128, 3)["piece_chunks"] == 0  # 128 chains fill the GPU
-    seg = pkg.gdp_prefill_plan(65536, 1, 32, 128, 128, 2)
+    seg = pkg.gdp_prefill_plan(65536, 1, 32, 64, 64, 2)  # head size 64: the staged kernels
     assert seg["segments"] == 16 and seg["piece_chunks"] == 0 and seg["launches"] == 33
+    # head size 128, M >= 2: descriptors + the fused kernel (segments no longer matter)
+    fused = pkg.gdp_prefill_plan(65536, 1, 32, 128, 128, 2)
+    assert fused["piece_chunks"] == 0 and fused["launches"] == 2
+    assert pkg.gdp_prefill_fused(65536, 1, 32, 128, 128, 2) and pkg.gdp_prefill_fused(32768, 8, 16, 128, 128, 3)
+    assert not pkg.gdp_prefill_fused(65536, 1, 32, 128, 128, 1)  # M = 1: its tensor memory does not fit
+    assert not pkg.gdp_prefill_fused(1421, 4, 8, 128, 128, 2)  # split chains
+    assert not pkg.gdp_prefill_fused(4096, 2, 2, 64, 64, 2)  # head size 64
     assert pkg.gdp_prefill_plan(5000, 33, 1, 64, 64, 2)["piece_chunks"] == 0  # more than 32 sequences
     assert pkg.gdp_prefill_plan(0, 0, 4, 64, 64, 2)["launches"] == 0
     with pytest.raises(pkg.GdpError):
