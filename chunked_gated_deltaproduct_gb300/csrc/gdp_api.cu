@@ -66,6 +66,29 @@ PiecePlan piece_plan(int64_t T, int64_t N, int H, int M) {
   return pl;
 }
 
+// The split-chains plan of the fused kernel (gdp_fused.cu): as piece_plan, but a fused call runs
+// whole sequences in one launch whatever their length, so long chains split as well.
+PiecePlan fused_piece_plan(int64_t T, int64_t N, int H, int M) {
+  PiecePlan pl{0, 0};
+  if (N < 1 || N > gdp::kPieceMaxSeqs) return pl;
+  const int64_t C = ntdp_bound(T, N, M), maxc = ((int64_t)M * T + gdp::kChunk - 1) / gdp::kChunk;
+  for (int64_t len = gdp::kPieceMinChunks; len < maxc; ++len) {
+    const int64_t rows = N + (C + len - 1) / len;
+    if (rows * H <= gdp::kPieceCtas) {
+      pl.len = len;
+      pl.rows = rows;
+      break;
+    }
+  }
+  return pl;
+}
+
+// The plan a common-contract call of this shape takes (the fused kernel's where it serves the
+// shape, else the staged kernels').
+PiecePlan plan_for(int64_t T, int64_t N, int H, int K, int V, int M) {
+  return gdp::fused_shape(K, V, M) ? fused_piece_plan(T, N, H, M) : piece_plan(T, N, H, M);
+}
+
 // Workspace layout; identical for the size query and the carving.
 struct Layout {
   size_t cod, ci, cid, co, img, img_stride, U, seg, piece, total;
@@ -90,8 +113,11 @@ Layout layout_for(int64_t T, int64_t N, int H, int K, int V, int M) {
   l.img = take(l.img_stride * tiles);
   l.U = take(sizeof(float) * tiles * gdp::kChunk * (size_t)V);
   l.seg = seg_count(T, N, H, M) > 1 ? take(sizeof(float) * (size_t)N * H * (size_t)V * K) : 0;
+  // the pieces of either plan (a call over another input type on a fused shape runs the staged one)
   const PiecePlan pp = piece_plan(T, N, H, M);
-  l.piece = pp.len > 0 ? take(sizeof(float) * 3 * (size_t)pp.rows * H * (size_t)V * K) : 0;
+  const PiecePlan pf = gdp::fused_shape(K, V, M) ? fused_piece_plan(T, N, H, M) : PiecePlan{0, 0};
+  const int64_t prow = pp.rows > pf.rows ? pp.rows : pf.rows;
+  l.piece = prow > 0 ? take(sizeof(float) * 3 * (size_t)prow * H * (size_t)V * K) : 0;
   l.total = off;
   return l;
 }
@@ -312,9 +338,12 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
   p.seg_rows = 0;
   p.seg_state = nullptr;
   p.prefetch = (N * (int64_t)H <= gdp::kSegMaxChains) ? 1 : 0;
+  // the fused kernel (WY work, scan and outputs in one launch) serves the common contract of a
+  // plain forward call
+  const bool fused = !rc && !xfer_out && gdp::fused_serves(p);
   // a transfer-pair call runs whole sequences in one segment
   const int nseg = xfer_out ? 1 : seg_count(T, N, H, M);
-  const PiecePlan pp = xfer_out ? PiecePlan{0, 0} : piece_plan(T, N, H, M);
+  const PiecePlan pp = xfer_out ? PiecePlan{0, 0} : (fused ? fused_piece_plan(T, N, H, M) : piece_plan(T, N, H, M));
   p.piece_len = (int)pp.len;
   p.piece_rows = (int)pp.rows;
   p.piece_pass1 = 0;
@@ -339,9 +368,6 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
     p.slots = nullptr;
     p.num_slots = 0;
   }
-  // the fused kernel (WY work, scan and outputs in one launch) serves the common contract of a
-  // plain forward call whose chains are not split
-  const bool fused = !rc && !xfer_out && pp.len == 0 && gdp::fused_serves(p);
   // desc -> WY -> scan on one stream overlap their launches (programmatic dependent launch);
   // the profiled form records events between them, so there each kernel runs alone
   p.pdl = ((nseg == 1 || fused) && !ev) ? 1 : 0;
@@ -359,6 +385,17 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
   if (ev && (st = record(ev[1], stream)) != GDP_OK) return st;
   if (fused) {  // no WY stage of its own: events 1 and 2 mark the same point
     if (ev && (st = record(ev[2], stream)) != GDP_OK) return st;
+    if (pp.len > 0) {  // split chains: B and Phi of the pieces, their entering states, the pieces
+      gdp::Problem q = p;
+      q.piece_pass1 = 1;
+      q.out = nullptr;
+      q.out_state = nullptr;
+      q.chunk_states = nullptr;
+      e = gdp::launch_fused(q, stream);
+      if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "fused kernel (pieces): %s", cudaGetErrorString(e));
+      e = gdp::launch_piece_combine(p, stream);
+      if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "piece combine kernel: %s", cudaGetErrorString(e));
+    }
     e = gdp::launch_fused(p, stream);
     if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "fused kernel: %s", cudaGetErrorString(e));
     if (ev && (st = record(ev[3], stream)) != GDP_OK) return st;
@@ -443,19 +480,20 @@ GDP_EXPORT gdp_status gdp_prefill_plan(int64_t T, int64_t N, int H, int K, int V
   if (!shape_ok(T, N, H, K, V, M))
     return fail(GDP_ERR_INVALID_ARG, "bad shape T=%lld N=%lld H=%d K=%d V=%d M=%d", (long long)T, (long long)N, H, K,
                 V, M);
-  const int nseg = seg_count(T, N, H, M);
-  const PiecePlan pp = piece_plan(T, N, H, M);
+  const bool fused = gdp::fused_shape(K, V, M);
+  const int nseg = fused ? 1 : seg_count(T, N, H, M);
+  const PiecePlan pp = plan_for(T, N, H, K, V, M);
   if (segments) *segments = nseg;
   if (piece_chunks) *piece_chunks = pp.len;
   if (piece_rows) *piece_rows = pp.rows;
-  const bool fused = pp.len == 0 && gdp::fused_shape(K, V, M);
-  if (launches) *launches = N == 0 ? 0 : 1 + (fused ? 1 : (nseg > 1 ? 2 * nseg : (pp.len > 0 ? 4 : 2)));
+  if (launches)
+    *launches = N == 0 ? 0 : 1 + (fused ? (pp.len > 0 ? 3 : 1) : (nseg > 1 ? 2 * nseg : (pp.len > 0 ? 4 : 2)));
   return GDP_OK;
 }
 
 GDP_EXPORT int gdp_prefill_fused(int64_t T, int64_t N, int H, int K, int V, int M) {
   if (!shape_ok(T, N, H, K, V, M)) return 0;
-  return piece_plan(T, N, H, M).len == 0 && gdp::fused_shape(K, V, M) ? 1 : 0;
+  return gdp::fused_shape(K, V, M) ? 1 : 0;
 }
 
 GDP_EXPORT const char *gdp_last_error(void) { return g_last_error; }

@@ -199,16 +199,50 @@ __device__ __forceinline__ void store_state_one_tile(uint32_t t_lane, unsigned c
 
 __device__ __forceinline__ void fused_body(const Problem &p, const CUtensorMap &tm_k, const CUtensorMap &tm_q,
                                            const CUtensorMap &tm_v, const CUtensorMap &tm_cs,
-                                           const CUtensorMap &tm_fin, const CUtensorMap &tm_out_a,
-                                           const CUtensorMap &tm_out_b) {
+                                           const CUtensorMap &tm_fin, const CUtensorMap &tm_seg,
+                                           const CUtensorMap &tm_out_a, const CUtensorMap &tm_out_b) {
   using In = In16<false>;
-  const int h = blockIdx.y, seq = blockIdx.x;
+  const int h = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int M = p.M, QP = p.qpad, H = p.H;
   constexpr int d = kFusedD;
+  // Split chains (Problem::piece_len > 0): this CTA runs one piece.  Pass 1 (piece_pass1): grid
+  // row r < piece_rows runs piece r from a zero state (its B), row piece_rows + r from the
+  // identity with U = 0 (its Phi), no outputs, the end state to piece_buf row (grid row); a
+  // sequence's last piece has no pass 1.  Pass 2: piece r of a split sequence enters with
+  // piece_buf row 2 piece_rows + r (the combine kernel's S_in) and writes its outputs, chunk
+  // states and, as its sequence's last piece, the final state.
+  const bool pieces = p.piece_len > 0, pass1 = pieces && p.piece_pass1;
+  const bool transfer = pass1 && (int)blockIdx.x >= p.piece_rows;  // the Phi row of a piece
+  const bool outs = !pass1;
+  int seq = (int)blockIdx.x, pc_i = 0, pc_n = 1;
+  if (pieces) {
+    // the piece table comes from the descriptors (chunk_offsets_dp); every CTA waits for its
+    // predecessor grid before it may exit, so that this grid's completion implies theirs
+    pdl_wait();
+    __shared__ int pc_sh[3];
+    if (warp == 0) {
+      int sq, pi, np;
+      piece_of_row(p, (int)blockIdx.x - (transfer ? p.piece_rows : 0), lane, &sq, &pi, &np);
+      if (lane == 0) {
+        pc_sh[0] = sq;
+        pc_sh[1] = pi;
+        pc_sh[2] = np;
+      }
+    }
+    __syncthreads();
+    seq = pc_sh[0];
+    pc_i = pc_sh[1];
+    pc_n = pc_sh[2];
+    if (seq < 0 || (pass1 && pc_i == pc_n - 1)) return;  // past the last piece; a last piece has no pass 1
+  }
   int64_t bos, L;
   const bool seq_ok = seq_bounds(p.cu, p.cu64, p.T, seq, &bos, &L);  // flagged by the descriptor kernel
-  const int64_t n = seq_ok ? (L * M + kChunk - 1) / kChunk : 0;
+  const int64_t nseq = seq_ok ? (L * M + kChunk - 1) / kChunk : 0;  // the sequence's expanded chunks
+  // this launch's chunks: global chunk e0 + c for local c in [0, n)
+  const int64_t e0 = pieces ? min((int64_t)pc_i * p.piece_len, nseq) : 0;
+  const int64_t n = pieces ? max((int64_t)0, min(e0 + p.piece_len, nseq) - e0) : nseq;
+  const bool last_piece = pc_i == pc_n - 1;
   const int hq = input_head(h, p.hmul_q), hk = input_head(h, p.hmul_k), hv = input_head(h, p.hmul_v);
   const uint64_t wl = p.wait_limit_ns;
 
@@ -268,13 +302,15 @@ __device__ __forceinline__ void fused_body(const Problem &p, const CUtensorMap &
   if (p.cache) {
     slot = p.slots[seq];
     if (slot < -1 || slot >= p.num_slots) {
-      if (tid == 0) set_status(p.status, GDP_DEV_ERR_SLOT);
+      if (tid == 0 && !pass1 && pc_i == 0) set_status(p.status, GDP_DEV_ERR_SLOT);
       slot = -1;
     }
     if (slot >= 0) src = p.cache + ((int64_t)slot * H + h) * (int64_t)p.V * d;
   } else if (p.init) {
     src = static_cast<const float *>(p.init) + ((int64_t)seq * H + h) * (int64_t)p.V * d;
   }
+  if (pass1 || pc_n > 1)  // zero (or the identity) for B / Phi; a split piece from its S_in
+    src = pass1 ? nullptr : p.piece_buf + ((int64_t)(2 * p.piece_rows + (int)blockIdx.x) * H + h) * (int64_t)p.V * d;
 
   const int q4 = warp & 3;                 // TMEM lane quadrant of math and store warps
   const int v = q4 * 32 + lane;            // state row / feature of this thread's TMEM lane
@@ -283,8 +319,8 @@ __device__ __forceinline__ void fused_body(const Problem &p, const CUtensorMap &
   bool load_pending = false;               // (thread 0) a tile load is in flight on tl_full
   int n_loads = 0;
 
-  auto issue_tiles = [&](int64_t c) {  // thread 0: the k, q, v tiles of chunk c
-    const ChunkGeo g = chunk_geo(bos, L, M, c);
+  auto issue_tiles = [&](int64_t c) {  // thread 0: the k, q, v tiles of local chunk c
+    const ChunkGeo g = chunk_geo(bos, L, M, e0 + c);
     mbar_arrive_expect_tx(&tl_full, 2u * (uint32_t)(64 + QP + 64) * 128u);
     for (int kb = 0; kb < 2; ++kb) {
       tma_load_3d(kq + kb * 16384u, &tm_k, kb * 64, hk, (int)g.R0, &tl_full);
@@ -294,7 +330,7 @@ __device__ __forceinline__ void fused_body(const Problem &p, const CUtensorMap &
     load_pending = true;
     ++n_loads;
     if (c + 2 < n) {  // the tiles two chunks ahead into L2
-      const ChunkGeo g2 = chunk_geo(bos, L, M, c + 2);
+      const ChunkGeo g2 = chunk_geo(bos, L, M, e0 + c + 2);
       for (int kb = 0; kb < 2; ++kb) {
         tma_prefetch_3d(&tm_k, kb * 64, hk, (int)g2.R0);
         tma_prefetch_3d(&tm_q, kb * 64, hq, (int)g2.tq0);
@@ -313,6 +349,9 @@ __device__ __forceinline__ void fused_body(const Problem &p, const CUtensorMap &
         if (src) y = *reinterpret_cast<const float4 *>(src + (int64_t)v * d + c0 + u4);
         x[u4] = y.x; x[u4 + 1] = y.y; x[u4 + 2] = y.z; x[u4 + 3] = y.w;
       }
+      if (transfer)  // the identity
+#pragma unroll
+        for (int u = 0; u < 16; ++u) x[u] = (c0 + u == v) ? 1.f : 0.f;
       tmem_st16(tS + lrow + c0, x);
     }
     float z[16];
@@ -320,13 +359,15 @@ __device__ __forceinline__ void fused_body(const Problem &p, const CUtensorMap &
     for (int w = 0; w < 16; ++w) z[w] = 0.f;
     for (int c0 = 0; c0 < QP; c0 += 16) tmem_st16(tO(hf) + lrow + c0, z);
     tmem_st_wait();
-    if (tid == 0 && n > 0) issue_tiles(0);
+    // (a test of the bounded waits withholds the first load of CTA (0, 0): its wait runs out)
+    if (tid == 0 && n > 0 && !(p.test_withhold_copy && blockIdx.x == 0 && blockIdx.y == 0)) issue_tiles(0);
   }
   // chunk_offsets (chunk-state rows) come from the descriptor kernel
-  pdl_wait();
+  if (!pieces) pdl_wait();
   const int64_t co_i = p.chunk_states ? (int64_t)p.co[seq] : 0;
-  auto emits = [&](int64_t c) {
-    return p.chunk_states && (c % M == 0) && co_i >= 0 && co_i + c / M < p.nt_pad;
+  auto emits = [&](int64_t c) {  // local chunk c
+    const int64_t eg = e0 + c;
+    return p.chunk_states && (eg % M == 0) && co_i >= 0 && co_i + eg / M < p.nt_pad;
   };
   tc_fence_before();
   __syncthreads();
@@ -350,7 +391,7 @@ __device__ __forceinline__ void fused_body(const Problem &p, const CUtensorMap &
     };
     for (int64_t c = 0; c < n; ++c) {
       const int b = (int)(c & 1);
-      const ChunkGeo g = chunk_geo(bos, L, M, c);
+      const ChunkGeo g = chunk_geo(bos, L, M, e0 + c);
       // per-row beta and decay gate (the decay of token t sits on its first expanded row t*M)
       float b_r = 0.f, gate_r = 0.f;
       if (tid < kChunk && tid < g.len) {
@@ -419,7 +460,7 @@ __device__ __forceinline__ void fused_body(const Problem &p, const CUtensorMap &
       const float gam_next = fast ? gam_pass * gamma_last : 1.f;
       if (tid < kChunk) {
         wc[tid] = bt[tid] * exp2f(G2[tid]) * rk[tid];
-        uc[tid] = bt[tid];
+        uc[tid] = transfer ? 0.f : bt[tid];
         ks[tid] = (tid < g.len) ? exp2f(G2last - G2[tid]) * rk[tid] : 0.f;
         const int pr = g.p0 + tid * M;
         qs[tid] = (tid < g.nq) ? p.scale * exp2f(G2[pr]) * rq[tid] : 0.f;
@@ -446,9 +487,11 @@ __device__ __forceinline__ void fused_body(const Problem &p, const CUtensorMap &
               A[r * kLd + j] = (j < r && rowlive) ? si * exp2f(gi - G2[j]) * rk[j] * dv[u] : 0.f;
             }
           }
-        } else if (r < kChunk + QP) {
+        } else if (outs) {
+          // lanes 64..127: the TMEM load is warp-wide (.sync.aligned), so every lane of these
+          // quadrants issues it; only the qpad readout rows store
           const int qi = r - kChunk, pr = g.p0 + qi * M;
-          const bool live = qi < g.nq;
+          const bool inq = qi < QP, live = qi < g.nq;
           const float gp = live ? G2[pr] : 0.f;
           const float sc = live ? p.scale * rq[qi] : 0.f;
           unsigned char *pb = sm + lay.P + (uint32_t)hf * (uint32_t)QP * 128u;  // K-block s / 32 = hf
@@ -456,16 +499,18 @@ __device__ __forceinline__ void fused_body(const Problem &p, const CUtensorMap &
           for (int c0 = cbeg; c0 < cbeg + 32; c0 += 16) {
             float dv[16];
             tmem_ld16(tW + lrow + c0, dv);
+            if (inq) {
 #pragma unroll
-            for (int u4 = 0; u4 < 16; u4 += 4) {
-              float4 o4;
-              float *o = &o4.x;
+              for (int u4 = 0; u4 < 16; u4 += 4) {
+                float4 o4;
+                float *o = &o4.x;
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int s_ = c0 + u4 + u;
-                o[u] = (live && s_ <= pr) ? sc * exp2f(gp - G2[s_]) * rk[s_] * dv[u4 + u] : 0.f;
+                for (int u = 0; u < 4; ++u) {
+                  const int s_ = c0 + u4 + u;
+                  o[u] = (live && s_ <= pr) ? sc * exp2f(gp - G2[s_]) * rk[s_] * dv[u4 + u] : 0.f;
+                }
+                *reinterpret_cast<float4 *>(pb + ImageLayout::swz_off(qi, c0 + u4)) = o4;
               }
-              *reinterpret_cast<float4 *>(pb + ImageLayout::swz_off(qi, c0 + u4)) = o4;
             }
           }
         }
@@ -570,7 +615,7 @@ __device__ __forceinline__ void fused_body(const Problem &p, const CUtensorMap &
           *reinterpret_cast<float4 *>(row + ((j ^ (f & 7)) << 4)) = o4;
         }
         // b2: P rows (same in-row swizzle: 128 + qi and qi agree mod 8)
-        const uint32_t pchunks = (uint32_t)QP * 8u;
+        const uint32_t pchunks = outs ? (uint32_t)QP * 8u : 0u;
         for (uint32_t idx = tid; idx < 2u * pchunks; idx += kMathThreads) {
           const uint32_t kb = idx / pchunks, rem = idx % pchunks;
           *reinterpret_cast<uint4 *>(sm + lay.b2 + kb * lay.b2_block + (uint32_t)d * 128u + rem * 16u) =
@@ -585,7 +630,7 @@ __device__ __forceinline__ void fused_body(const Problem &p, const CUtensorMap &
           for (int u = 0; u < 32; ++u)
             *reinterpret_cast<float *>(b1 + ImageLayout::swz_off(QP + hf * 32 + u, f)) = -gam_pass * w[u];
         }
-        const int qh = QP / 2;
+        const int qh = outs ? QP / 2 : 0;
 #pragma unroll 4
         for (int qi = hf * qh; qi < hf * qh + qh; ++qi)
           *reinterpret_cast<float *>(b1 + ImageLayout::swz_off(qi, f)) =
@@ -635,20 +680,21 @@ __device__ __forceinline__ void fused_body(const Problem &p, const CUtensorMap &
       named_sync(kBarStore, 128);
       if (!(st_ok[0] & st_ok[1] & st_ok[2] & st_ok[3])) break;
       tc_fence_after();
-      const ChunkGeo g = chunk_geo(bos, L, M, c);
+      const ChunkGeo g = chunk_geo(bos, L, M, e0 + c);
+      const int nqo = outs ? g.nq : 0;
 #pragma unroll 1
-      for (int q0 = 0; q0 < g.nq; q0 += 32) {
+      for (int q0 = 0; q0 < nqo; q0 += 32) {
         uint32_t xo[32];
         tmem_ld16_nw(tO(b) + lrow + q0, xo);
-        if (q0 + 16 < g.nq) tmem_ld16_nw(tO(b) + lrow + q0 + 16, xo + 16);
+        if (q0 + 16 < nqo) tmem_ld16_nw(tO(b) + lrow + q0 + 16, xo + 16);
         tmem_ld_wait();
 #pragma unroll
         for (int w = 0; w < 32; ++w)
-          if (q0 + w < g.nq)
+          if (q0 + w < nqo)
             *reinterpret_cast<__nv_bfloat16 *>(obuf + ((uint32_t)(q0 + w) * d + v) * 2u) =
                 __float2bfloat16_rn(__uint_as_float(xo[w]));
       }
-      {  // the buffer's o columns start the chunk after next at zero
+      if (outs) {  // the buffer's o columns start the chunk after next at zero
         float z[16];
 #pragma unroll
         for (int w = 0; w < 16; ++w) z[w] = 0.f;
@@ -659,7 +705,8 @@ __device__ __forceinline__ void fused_body(const Problem &p, const CUtensorMap &
       tc_fence_before();
       mbar_arrive(&yo_free[b]);
       named_sync(kBarStore, 128);
-      if (p.out_tma && (g.nq == kChunk / M || g.nq == (kChunk + M - 1) / M)) {
+      if (!outs) {
+      } else if (p.out_tma && (g.nq == kChunk / M || g.nq == (kChunk + M - 1) / M)) {
         if (tid == 256) {
           tma_store_3d(g.nq == kChunk / M ? &tm_out_a : &tm_out_b, obuf, 0, h, (int)g.tq0);
           bulk_commit();
@@ -673,16 +720,21 @@ __device__ __forceinline__ void fused_body(const Problem &p, const CUtensorMap &
       }
       if (emits(c))  // the math warps copied S_c before batch 2 of this chunk was issued
         store_state_one_tile(tBk + lrow, tile, lane, 1.f, &tm_cs,
-                             (int)(((co_i + c / M) * H + h) * d + q4 * 32), pending, &bk_free);
+                             (int)(((co_i + (e0 + c) / M) * H + h) * d + q4 * 32), pending, &bk_free);
     }
     if (seq_ok && !abort_flag) {  // the last chunk's b2_done was waited for above
       int64_t r = -1;
-      if (p.cache) {
+      const CUtensorMap *tm = &tm_fin;
+      if (pass1) {  // B or Phi of the piece
+        r = ((int64_t)blockIdx.x * H + h) * d;
+        tm = &tm_seg;
+      } else if (!last_piece) {  // a split piece leaves no state
+      } else if (p.cache) {
         if (slot >= 0) r = ((int64_t)slot * H + h) * d;
       } else if (p.out_state) {
         r = ((int64_t)seq * H + h) * d;
       }
-      if (r >= 0) store_state_one_tile(tS + lrow, tile, lane, gam_fin_sh, &tm_fin, (int)(r + q4 * 32), pending, nullptr);
+      if (r >= 0) store_state_one_tile(tS + lrow, tile, lane, gam_fin_sh, tm, (int)(r + q4 * 32), pending, nullptr);
     }
     if (lane == 0) bulk_wait_all();
   } else if (lane == 0) {
@@ -690,6 +742,7 @@ __device__ __forceinline__ void fused_body(const Problem &p, const CUtensorMap &
     const uint32_t gram_id = idesc(kFmtBF16, 0, 0, 64, 128);
     const uint32_t wu_id = idesc(kFmtBF16, 1, 0, 64, d);
     const uint32_t id1 = idesc(kFmtTF32, 0, 0, QP + 64, 128);
+    const uint32_t id1y = idesc(kFmtTF32, 0, 0, 64, 128);  // Y only (no outputs)
     const uint32_t id2s = idesc(kFmtTF32, 0, 0, d, 128);
     const uint32_t id2o = idesc(kFmtTF32, 0, 0, QP, 128);
     const uint32_t skq = smem_u32(kq), svt = smem_u32(vt);
@@ -727,8 +780,16 @@ __device__ __forceinline__ void fused_body(const Problem &p, const CUtensorMap &
       if (c >= 2 && !mbar_wait_or_abort(&yo_free[b], (uint32_t)(((c >> 1) - 1) & 1), &abort_flag, wl)) break;
       tc_fence_after();
       const bool slow = slow_sh[b] != 0;
-      for (int kk = 0; kk < d / 8; ++kk)
-        mma_tf32_ts(tO(b), tS + kk * 8, desc_sw128(sb1 + (kk >> 2) * lay.b1_block + (kk & 3) * 32u, 16, 1024), id1, 1);
+      if (outs) {
+        for (int kk = 0; kk < d / 8; ++kk)
+          mma_tf32_ts(tO(b), tS + kk * 8, desc_sw128(sb1 + (kk >> 2) * lay.b1_block + (kk & 3) * 32u, 16, 1024), id1,
+                      1);
+      } else {  // the -W rows only: they start qpad rows (whole 1024-byte atoms) into each K-block
+        for (int kk = 0; kk < d / 8; ++kk)
+          mma_tf32_ts(ty, tS + kk * 8,
+                      desc_sw128(sb1 + (kk >> 2) * lay.b1_block + (uint32_t)QP * 128u + (kk & 3) * 32u, 16, 1024),
+                      id1y, 1);
+      }
       mma_commit(&b1_done[b]);
       // the next chunk's Gram runs between the batches (the math warps need it first)
       if (c + 1 < n) {
@@ -745,7 +806,7 @@ __device__ __forceinline__ void fused_body(const Problem &p, const CUtensorMap &
       for (int kk = 0; kk < kChunk / 8; ++kk) {
         const uint32_t bk = sb2 + (kk >> 2) * lay.b2_block + (kk & 3) * 32u;
         mma_tf32_ts(tS, ty + kk * 8, desc_sw128(bk, 16, 1024), id2s, 1);
-        mma_tf32_ts(tO(b), ty + kk * 8, desc_sw128(bk + (uint32_t)d * 128u, 16, 1024), id2o, 1);
+        if (outs) mma_tf32_ts(tO(b), ty + kk * 8, desc_sw128(bk + (uint32_t)d * 128u, 16, 1024), id2o, 1);
       }
       mma_commit(&b2_done[b]);
     }
@@ -766,9 +827,9 @@ __device__ __forceinline__ void fused_body(const Problem &p, const CUtensorMap &
 __global__ void __launch_bounds__(kFusedThreads, 1)
     gdp_fused_kernel(Problem p, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_cs,
-                     const __grid_constant__ CUtensorMap tm_fin, const __grid_constant__ CUtensorMap tm_out_a,
-                     const __grid_constant__ CUtensorMap tm_out_b) {
-  fused_body(p, tm_k, tm_q, tm_v, tm_cs, tm_fin, tm_out_a, tm_out_b);
+                     const __grid_constant__ CUtensorMap tm_fin, const __grid_constant__ CUtensorMap tm_seg,
+                     const __grid_constant__ CUtensorMap tm_out_a, const __grid_constant__ CUtensorMap tm_out_b) {
+  fused_body(p, tm_k, tm_q, tm_v, tm_cs, tm_fin, tm_seg, tm_out_a, tm_out_b);
 }
 
 }  // namespace
@@ -787,7 +848,7 @@ cudaError_t launch_fused(const Problem &p, cudaStream_t stream) {
   const size_t smem = fused_smem_bytes(p.qpad);
   cudaError_t e = cudaFuncSetAttribute(gdp_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  alignas(64) CUtensorMap tm_k, tm_q, tm_v, tm_cs, tm_fin, tm_out_a, tm_out_b;
+  alignas(64) CUtensorMap tm_k, tm_q, tm_v, tm_cs, tm_fin, tm_seg, tm_out_a, tm_out_b;
   const int64_t rows = p.T * p.M;
   if ((e = tmap_rows_16(&tm_k, p.k, rows, p.Hk, p.K, p.k_st, p.k_sh, kChunk, 0)) != cudaSuccess) return e;
   if ((e = tmap_rows_16(&tm_q, p.q, p.T, p.Hq, p.K, p.q_st, p.q_sh, p.qpad, 0)) != cudaSuccess) return e;
@@ -799,14 +860,20 @@ cudaError_t launch_fused(const Problem &p, cudaStream_t stream) {
   else
     e = tmap_state(&tm_fin, p.out_state, p.N * hv, p.K);
   if (e != cudaSuccess) return e;
+  // the pieces' states (pass 1 writes B and Phi through it)
+  if ((e = tmap_state(&tm_seg, p.piece_len > 0 ? p.piece_buf : nullptr, 3 * (int64_t)p.piece_rows * hv, p.K)) !=
+      cudaSuccess)
+    return e;
   Problem q = p;
   const int na = kChunk / p.M, nb = (kChunk + p.M - 1) / p.M;
   q.out_tma = (p.out && p.T >= nb) ? 1 : 0;
   if ((e = tmap_out_rows(&tm_out_a, q.out_tma ? p.out : nullptr, p.T, p.H, p.V, na, 0)) != cudaSuccess) return e;
   if ((e = tmap_out_rows(&tm_out_b, q.out_tma ? p.out : nullptr, p.T, p.H, p.V, nb, 0)) != cudaSuccess) return e;
-  dim3 grid((unsigned)p.N, (unsigned)p.H);
+  // one CTA per (sequence, head), or per (piece row, head) -- pass 1 runs two per piece
+  const int64_t grid_rows = p.piece_len > 0 ? (p.piece_pass1 ? 2 : 1) * (int64_t)p.piece_rows : p.N;
+  dim3 grid((unsigned)grid_rows, (unsigned)p.H);
   if ((e = launch_kernel(gdp_fused_kernel, grid, dim3(kFusedThreads), smem, stream, p.pdl != 0, q, tm_k, tm_q, tm_v,
-                         tm_cs, tm_fin, tm_out_a, tm_out_b)) != cudaSuccess)
+                         tm_cs, tm_fin, tm_seg, tm_out_a, tm_out_b)) != cudaSuccess)
     return e;
   return cudaGetLastError();
 }

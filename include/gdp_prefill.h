@@ -292,9 +292,10 @@ gdp_status gdp_chain_states(const float *s0, const float *phi, const float *b, i
  * *device_status, drains the CTA's own tensor-core work and copies, frees its
  * tensor memory and returns, so the CUDA context stays usable and the host
  * reads the status after the stream completes.  This call arms the calling
- * host thread's NEXT gdp_prefill_varlen* call to exercise that path: its scan
- * waits give up after limit_ns (1e5 .. 1e9 ns), and the scan CTA of sequence
- * 0, head 0 withholds its first operand copy, so one of its waits runs out.
+ * host thread's NEXT gdp_prefill_varlen* call to exercise that path: the waits
+ * of its scan (or fused) kernel give up after limit_ns (1e5 .. 1e9 ns), and that
+ * kernel's CTA of sequence 0, head 0 withholds its first copy, so one of its
+ * waits runs out.
  * That call's outputs are undefined (those of sequence 0, head 0 at least) and
  * its status word gets GDP_DEV_ERR_TIMEOUT; later calls are unaffected.  No
  * fault, trap or endless loop is involved.  GDP_ERR_INVALID_ARG for a limit

@@ -3,8 +3,8 @@
 Every output buffer (o, the final state, the chunk states) and the workspace is
 carved out of a larger allocation whose guard bands before and after it hold a
 fixed byte pattern; after the call the bands must be unchanged, so no kernel
-writes outside the buffers it was given.  Each of the three ways a call runs
-(plain, split chains, segmented; gdp_prefill_plan names which) is covered, and
+writes outside the buffers it was given.  Each way a call runs (the fused kernel whole or
+split into pieces; the staged kernels plain, split or segmented) is covered, and
 the outputs are checked against the oracle as well.
 """
 import pytest
@@ -36,16 +36,20 @@ class Guarded:
         return bool((lo == PATTERN).all()) and bool((hi == PATTERN).all())
 
 
-@pytest.mark.parametrize("lengths,H,M,kind", [
-    ([5 * i + 3 for i in range(40)], 2, 3, "plain"),
-    ([100, 257, 64, 300], 4, 2, "split"),
-    ([12288], 1, 2, "segmented"),
+@pytest.mark.parametrize("lengths,H,d,M,kind", [
+    ([5 * i + 3 for i in range(40)], 2, 128, 3, "fused"),
+    ([100, 257, 64, 300], 4, 128, 2, "fused split"),
+    ([5 * i + 3 for i in range(40)], 2, 64, 2, "staged"),
+    ([100, 257, 64, 300], 4, 64, 2, "staged split"),
+    ([12288], 1, 64, 2, "staged segmented"),
 ])
-def test_no_write_outside_the_given_buffers(cuda_device, lengths, H, M, kind):
+def test_no_write_outside_the_given_buffers(cuda_device, lengths, H, d, M, kind):
     dev = cuda_device
-    w = make_custom(lengths, H, 128, M, seed=123, init_sigma=0.1, chunk_states=True)
+    w = make_custom(lengths, H, d, M, seed=123, init_sigma=0.1, chunk_states=True)
     plan = pkg.gdp_prefill_plan(w.T, w.N, w.H, w.d, w.d, w.M)
-    assert kind == ("segmented" if plan["segments"] > 1 else "split" if plan["piece_chunks"] else "plain")
+    got = "fused" if pkg.gdp_prefill_fused(w.T, w.N, w.H, w.d, w.d, w.M) else "staged"
+    got += " segmented" if plan["segments"] > 1 else " split" if plan["piece_chunks"] else ""
+    assert kind == got
     nt = pkg.gdp_nt_pad(w.T, w.N)
     g_out = Guarded(w.T * w.H * w.d * 2, dev)
     g_fin = Guarded(w.N * w.H * w.d * w.d * 4, dev)

@@ -1,8 +1,8 @@
 """Failure detection on the GPU without a GPU fault: the bounded waits.
 
 Every spin-wait of the kernels is bounded.  gdp_arm_wait_expiry_test arms one
-call so that its scan waits give up after a few milliseconds and the scan CTA
-of sequence 0, head 0 withholds its first operand copy: one wait runs out (a
+call so that its waits give up after a few milliseconds and the CTA of sequence
+0, head 0 (of the fused kernel, or of the staged scan) withholds its first copy: one wait runs out (a
 flag that nothing sets), the CTA drains its own tensor-core work and copies,
 frees its tensor memory and returns.  The test checks that the call completes
 promptly, that the status word carries GDP_DEV_ERR_TIMEOUT, and that the
@@ -23,9 +23,13 @@ from tests.gpu_helpers import run, to_dev
 pytestmark = pytest.mark.gpu
 
 
-def test_wait_expiry_sets_timeout_and_context_survives(cuda_device):
-    w = make_custom([100, 37], 2, 128, 2, seed=31, init_sigma=0.1)
-    assert pkg.gdp_prefill_plan(w.T, w.N, w.H, w.d, w.d, w.M)["launches"] == 3  # one scan launch
+@pytest.mark.parametrize("d,fused", [(128, True), (64, False)])
+def test_wait_expiry_sets_timeout_and_context_survives(cuda_device, d, fused):
+    """The fused kernel (head size 128) and the staged scan (head size 64) each withhold one copy."""
+    w = make_custom([100, 37], 2, d, 2, seed=31, init_sigma=0.1)
+    assert pkg.gdp_prefill_fused(w.T, w.N, w.H, w.d, w.d, w.M) == fused
+    plan = pkg.gdp_prefill_plan(w.T, w.N, w.H, w.d, w.d, w.M)
+    assert plan["piece_chunks"] == 0 and plan["segments"] == 1  # one launch of the kernel under test
     d = to_dev(w, cuda_device)
     status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
     pkg.gdp_arm_wait_expiry_test(2_000_000)  # 2 ms

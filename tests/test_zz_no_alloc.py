@@ -3,8 +3,9 @@ allocate device memory (a plugin inside a runtime that owns all device memory,
 or a host program that may not call cudaMalloc in its serving loop).
 
 The entry point is called through the C ABI twice in a row on the same inputs,
-once for each of the three ways a call runs (plain, split chains, segmented;
-gdp_prefill_plan names which), and each result must equal, bit for bit, the
+once for each way a call runs (the fused kernel whole or split into pieces; the
+staged kernels plain, split or segmented; gdp_prefill_fused and gdp_prefill_plan
+name which), and each result must equal, bit for bit, the
 main entry point's result with a caller-owned workspace: the two run the same
 kernels in the same order, only the scratch memory differs.  One call of each
 shape is also checked against the float64 oracle with the parity tolerances.
@@ -24,17 +25,25 @@ from tests._parity import check_o, check_state
 
 pytestmark = pytest.mark.gpu
 
-# (lengths, H, M, the plan the shape takes)
+# (lengths, H, head size, M, the plan the shape takes): the fused kernel whole and split into
+# pieces, the staged kernels plain, split and segmented
 SHAPES = [
-    ([5 * i + 3 for i in range(40)], 2, 3, "plain"),      # 40 sequences: no split chains
-    ([100, 257, 64, 300], 4, 2, "split"),                 # few short sequences: split chains
-    ([12288], 1, 2, "segmented"),                         # one long chain: segmented
+    ([5 * i + 3 for i in range(40)], 2, 128, 3, "fused"),
+    ([100, 257, 64, 300], 4, 128, 2, "fused split"),
+    ([5 * i + 3 for i in range(40)], 2, 64, 2, "staged"),
+    ([100, 257, 64, 300], 4, 64, 2, "staged split"),
+    ([12288], 1, 64, 2, "staged segmented"),
 ]
 
 
 def _plan_kind(w):
     plan = pkg.gdp_prefill_plan(w.T, w.N, w.H, w.d, w.d, w.M)
-    return "segmented" if plan["segments"] > 1 else ("split" if plan["piece_chunks"] > 0 else "plain")
+    kind = "fused" if pkg.gdp_prefill_fused(w.T, w.N, w.H, w.d, w.d, w.M) else "staged"
+    if plan["segments"] > 1:
+        kind += " segmented"
+    elif plan["piece_chunks"] > 0:
+        kind += " split"
+    return kind
 
 
 def _args(w, d, out, fin, cs, workspace):
@@ -42,9 +51,9 @@ def _args(w, d, out, fin, cs, workspace):
                          out, fin, cs, None, None, None, None, None, w.use_qk_l2norm, workspace, None)
 
 
-@pytest.mark.parametrize("lengths,H,M,kind", SHAPES)
-def test_static_scratch_matches_caller_workspace(cuda_device, lengths, H, M, kind):
-    w = make_custom(lengths, H, 128, M, seed=77, init_sigma=0.1, chunk_states=True)
+@pytest.mark.parametrize("lengths,H,d,M,kind", SHAPES)
+def test_static_scratch_matches_caller_workspace(cuda_device, lengths, H, d, M, kind):
+    w = make_custom(lengths, H, d, M, seed=77, init_sigma=0.1, chunk_states=True)
     assert pkg.gdp_prefill_workspace_bytes(w.T, w.N, w.H, w.d, w.d, w.M) <= pkg.gdp_static_scratch_bytes()
     assert _plan_kind(w) == kind
     dev = cuda_device
