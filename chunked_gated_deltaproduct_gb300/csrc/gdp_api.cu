@@ -91,7 +91,7 @@ PiecePlan plan_for(int64_t T, int64_t N, int H, int K, int V, int M) {
 
 // Workspace layout; identical for the size query and the carving.
 struct Layout {
-  size_t cod, ci, cid, co, img, img_stride, U, seg, piece, total;
+  size_t cod, ci, cid, co, ord, img, img_stride, U, seg, piece, total;
 };
 
 Layout layout_for(int64_t T, int64_t N, int H, int K, int V, int M) {
@@ -108,6 +108,7 @@ Layout layout_for(int64_t T, int64_t N, int H, int K, int V, int M) {
   l.ci = take(sizeof(int32_t) * 2 * (size_t)ntp);
   l.cid = take(sizeof(int32_t) * 2 * (size_t)ntdp);
   l.co = take(sizeof(int32_t) * (size_t)(N + 1));
+  l.ord = take(sizeof(int32_t) * (size_t)(N + 1));
   const size_t tiles = (size_t)ntdp * (size_t)H;
   l.img_stride = align_up(gdp::ImageLayout(K, qp).bytes);
   l.img = take(l.img_stride * tiles);
@@ -350,6 +351,7 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
   p.piece_buf = pp.len > 0 ? (float *)(ws + lay.piece) : nullptr;
   p.xfer = 0;
   p.xfer_out = nullptr;
+  p.order = nullptr;
   p.wait_limit_ns = 1000000000ull;
   p.test_withhold_copy = 0;
   if (g_expiry_test_ns) {  // armed by gdp_arm_wait_expiry_test: this call only
@@ -374,13 +376,16 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
   SideStreams *ss = (nseg > 1 && !fused) ? side_streams() : nullptr;
   if (nseg > 1 && !fused && !ss) return fail(GDP_ERR_CUDA, "could not create the internal streams of the segmented mode");
 
+  // a fused call over whole sequences runs them longest first (the descriptor kernel's order)
+  int32_t *ord = (fused && pp.len == 0 && N > 1) ? (int32_t *)(ws + lay.ord) : nullptr;
+  p.order = ord;
   cudaError_t e;
   if (nprebuilt == 3)  // only the internal expanded-stream offsets
     e = gdp::launch_descriptors(p.cu, p.cu64, T, N, M, nullptr, 0, nullptr, 0, nullptr, (int32_t *)p.cod, p.status,
-                                stream);
+                                stream, ord);
   else
     e = gdp::launch_descriptors(p.cu, p.cu64, T, N, M, (int32_t *)p.ci, nt_pad, (int32_t *)p.cid, ntdp_pad,
-                                co_desc, (int32_t *)p.cod, p.status, stream);
+                                co_desc, (int32_t *)p.cod, p.status, stream, ord);
   if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "descriptor kernel: %s", cudaGetErrorString(e));
   if (ev && (st = record(ev[1], stream)) != GDP_OK) return st;
   if (fused) {  // no WY stage of its own: events 1 and 2 mark the same point

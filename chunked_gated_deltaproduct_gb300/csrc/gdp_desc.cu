@@ -66,10 +66,14 @@ __device__ void fill_rows(int32_t *rows, int64_t pad, const int32_t *offs, int64
   }
 }
 
+// Sequences the longest-first order is computed for (one thread per sequence, a count over all
+// of them); larger batches keep their own order.
+constexpr int64_t kOrderMaxSeqs = kDescThreads;
+
 __global__ void __launch_bounds__(kDescThreads) gdp_desc_kernel(const void *cu, int cu64, int64_t T, int64_t N,
                                                                 int M, int32_t *ci, int64_t nt_pad, int32_t *cid,
                                                                 int64_t ntdp_pad, int32_t *co, int32_t *cod,
-                                                                uint32_t *status) {
+                                                                int32_t *order, uint32_t *status) {
   __shared__ int warp_sums[32];
   __shared__ int tot_a, tot_b;
   __shared__ int carry_a, carry_b;
@@ -120,14 +124,33 @@ __global__ void __launch_bounds__(kDescThreads) gdp_desc_kernel(const void *cu, 
   __syncthreads();  // makes the offsets written above visible to the whole block
   if (ci) fill_rows(ci, nt_pad, in_smem ? s_co : co, N);
   if (cid) fill_rows(cid, ntdp_pad, in_smem ? s_cod : cod, N);
+  if (order) {
+    // longest first: sequence i goes to position #{j : n_j > n_i} + #{j < i : n_j == n_i}, n the
+    // expanded-chunk counts (a permutation: ties keep the sequences' own order)
+    if (N <= kOrderMaxSeqs && in_smem) {
+      const int64_t i = threadIdx.x;
+      if (i < N) {
+        const int ni = s_cod[i + 1] - s_cod[i];
+        int rank = 0;
+        for (int64_t j = 0; j < N; ++j) {
+          const int nj = s_cod[j + 1] - s_cod[j];
+          rank += (nj > ni) || (nj == ni && j < i);
+        }
+        order[rank] = (int32_t)i;
+      }
+    } else {
+      for (int64_t i = threadIdx.x; i < N; i += blockDim.x) order[i] = (int32_t)i;
+    }
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_descriptors(const void *cu, int cu64, int64_t T, int64_t N, int M, int32_t *ci, int64_t nt_pad,
                                int32_t *cid, int64_t ntdp_pad, int32_t *co, int32_t *cod, uint32_t *status,
-                               cudaStream_t stream) {
-  gdp_desc_kernel<<<1, kDescThreads, 0, stream>>>(cu, cu64, T, N, M, ci, nt_pad, cid, ntdp_pad, co, cod, status);
+                               cudaStream_t stream, int32_t *order) {
+  gdp_desc_kernel<<<1, kDescThreads, 0, stream>>>(cu, cu64, T, N, M, ci, nt_pad, cid, ntdp_pad, co, cod, order,
+                                                  status);
   return cudaGetLastError();
 }
 

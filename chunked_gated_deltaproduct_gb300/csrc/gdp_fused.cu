@@ -202,7 +202,6 @@ __device__ __forceinline__ void fused_body(const Problem &p, const CUtensorMap &
                                            const CUtensorMap &tm_fin, const CUtensorMap &tm_seg,
                                            const CUtensorMap &tm_out_a, const CUtensorMap &tm_out_b) {
   using In = In16<false>;
-  const int h = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int M = p.M, QP = p.qpad, H = p.H;
   constexpr int d = kFusedD;
@@ -216,6 +215,15 @@ __device__ __forceinline__ void fused_body(const Problem &p, const CUtensorMap &
   const bool transfer = pass1 && (int)blockIdx.x >= p.piece_rows;  // the Phi row of a piece
   const bool outs = !pass1;
   int seq = (int)blockIdx.x, pc_i = 0, pc_n = 1;
+  int h = (int)blockIdx.y;
+  if (!pieces && p.order) {
+    // longest first: linear CTA index l (the order CTAs start in) runs sequence order[l / H],
+    // head l % H; the order comes from the descriptor kernel
+    pdl_wait();
+    const int64_t l = (int64_t)blockIdx.x + (int64_t)blockIdx.y * gridDim.x;
+    seq = p.order[l / H];
+    h = (int)(l % H);
+  }
   if (pieces) {
     // the piece table comes from the descriptors (chunk_offsets_dp); every CTA waits for its
     // predecessor grid before it may exit, so that this grid's completion implies theirs
@@ -363,7 +371,7 @@ __device__ __forceinline__ void fused_body(const Problem &p, const CUtensorMap &
     if (tid == 0 && n > 0 && !(p.test_withhold_copy && blockIdx.x == 0 && blockIdx.y == 0)) issue_tiles(0);
   }
   // chunk_offsets (chunk-state rows) come from the descriptor kernel
-  if (!pieces) pdl_wait();
+  if (!pieces && !p.order) pdl_wait();
   const int64_t co_i = p.chunk_states ? (int64_t)p.co[seq] : 0;
   auto emits = [&](int64_t c) {  // local chunk c
     const int64_t eg = e0 + c;

@@ -159,6 +159,9 @@ struct Problem {
   // so that one of its waits runs out (gdp_arm_wait_expiry_test).
   uint64_t wait_limit_ns;
   int test_withhold_copy;
+  // The fused kernel's CTA order (NULL: sequence by sequence): linear CTA index l runs sequence
+  // order[l / H], head l % H, so the longest sequences start first (the descriptor kernel's order)
+  const int32_t *order;
 };
 
 // Everything the backward kernels need about one call (gdp_backward.cu).  Heads are
@@ -295,9 +298,11 @@ __device__ __forceinline__ void set_status(uint32_t *status, uint32_t bits) {
 }
 
 // Kernel launchers (defined in their .cu files).  Each returns a CUDA error.
+// order (optional, [N]): the sequences longest first (by expanded chunks; ties in their own
+// order) for batches of up to 1024 sequences, the identity beyond.
 cudaError_t launch_descriptors(const void *cu, int cu64, int64_t T, int64_t N, int M, int32_t *ci, int64_t nt_pad,
                                int32_t *cid, int64_t ntdp_pad, int32_t *co, int32_t *cod, uint32_t *status,
-                               cudaStream_t stream);
+                               cudaStream_t stream, int32_t *order = nullptr);
 cudaError_t launch_wy(const Problem &p, cudaStream_t stream);
 // The WY kernel for float16 inputs (f16) and / or 16-bit or linear-space gates (typed).
 cudaError_t launch_wy_variant(const Problem &p, cudaStream_t stream, bool f16, bool typed);
