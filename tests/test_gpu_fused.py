@@ -34,7 +34,12 @@ CASES = {
     "no_gates": dict(lengths=[90, 33, 64] * 11, H=2, M=2, with_g=False, with_beta=False, init_sigma=0.1),
     "zero_state_chunks": dict(lengths=[128, 129, 1] * 11, H=2, M=2, chunk_states=True),
     "long_chain": dict(lengths=[20000], H=2, M=2, decay=0.02, init_sigma=0.05, chunk_states=True),
+    # few chains: the fused kernel splits them into pieces (pass 1, combine, pass 2)
+    "split_varlen": dict(lengths=[100, 257, 64, 1000], H=8, M=2, decay=0.05, init_sigma=0.1, chunk_states=True),
+    "split_long_m3": dict(lengths=[8192, 5], H=4, M=3, decay=0.02, init_sigma=0.05, chunk_states=True),
+    "split_strong_decay": dict(lengths=[3000, 70], H=2, M=2, decay=2.0, init_sigma=0.3, chunk_states=True),
 }
+SPLIT = {"long_chain", "split_varlen", "split_long_m3", "split_strong_decay"}
 
 
 def _oracle(w):
@@ -58,6 +63,8 @@ def _check(w, o, fin, cs, ref):
 def test_fused_parity(cuda_device, name):
     w = make_custom(seed=sorted(CASES).index(name) + 900, d=128, name=name, **CASES[name])
     assert pkg.gdp_prefill_fused(w.T, w.N, w.H, w.d, w.d, w.M), "shape should take the fused kernel"
+    split = pkg.gdp_prefill_plan(w.T, w.N, w.H, w.d, w.d, w.M)["piece_chunks"] > 0
+    assert split == (name in SPLIT)
     status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
     o, fin, cs, _ = run(w, cuda_device, status=status)
     assert int(status.item()) == 0
@@ -79,6 +86,31 @@ def test_fused_state_cache_in_place(cuda_device):
         if s not in used:
             assert torch.equal(cache[s], w.state[s]), f"slot {s} was touched"
     check_state(cache[sorted(used)], ref["state_out"][sorted(used)], label="cache slots")
+
+
+def test_fused_split_state_cache(cuda_device):
+    """Split chains with the state cache: pieces read the slot through the combine kernel, the
+    last piece writes it; padding sequences start from zero and write nothing."""
+    w = make_custom([1500, 3, 700, 0], 4, 128, 2, seed=78, cache_slots=8, cache_sigma=0.1, padding_slots=1)
+    assert pkg.gdp_prefill_plan(w.T, w.N, w.H, w.d, w.d, w.M)["piece_chunks"] > 0
+    o, fin, cs, d = run(w, cuda_device)
+    ref = _oracle(w)
+    check_o(o.cpu(), ref["o"], cu_seqlens=w.cu_seqlens)
+    cache = d["state"].cpu()
+    used = set(int(s) for s in w.state_indices.tolist() if s >= 0)
+    for s in range(w.state.shape[0]):
+        if s not in used:
+            assert torch.equal(cache[s], w.state[s]), f"slot {s} was touched"
+    check_state(cache[sorted(used)], ref["state_out"][sorted(used)], label="cache slots")
+
+
+def test_fused_longest_first_order(cuda_device):
+    """Over whole sequences the fused kernel runs them longest first (a device-built order);
+    lengths in rising order, equal lengths and an empty sequence come out right."""
+    w = make_custom(list(range(1, 40)) + [0, 600, 600, 2000], 2, 128, 2, seed=79, init_sigma=0.1, chunk_states=True)
+    assert pkg.gdp_prefill_plan(w.T, w.N, w.H, w.d, w.d, w.M)["piece_chunks"] == 0
+    o, fin, cs, _ = run(w, cuda_device)
+    _check(w, o, fin, cs, _oracle(w))
 
 
 def test_fused_grouped_heads(cuda_device):
