@@ -520,6 +520,30 @@ def measure_backward(pkg, dev, flush, stream, w, steps=5, warmup=3):
             "note": "includes the forward recompute (the backward keeps nothing from a forward call)"}
 
 
+def time_fused(pkg, c, stream, flush, steps=10, warmup=3):
+    """Mean ms per call of the same arguments through gdp_prefill_varlen_fused (L2 flushed), or
+    None when the fused kernel does not serve the workload."""
+    w = c.w
+    if pkg.gdp_prefill_fused(w.T, w.N, w.H, w.d, w.d, w.M) is None:
+        return None
+    sid = stream.cuda_stream
+    times = []
+    for s in range(warmup + steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            e0.record(stream)
+            pkg.gdp_prefill_varlen_fused(c.args, sid)
+            e1.record(stream)
+        e1.synchronize()
+        if s >= warmup:
+            times.append(e0.elapsed_time(e1))
+    ms = statistics.fmean(times)
+    peak, _ = measured_peaks()
+    return {"ms_per_call": ms, "tokens_per_s": w.T / (ms / 1e3),
+            "step_frac": alg_bytes(w) / (ms / 1e3) / 1e9 / peak, "steps": steps}
+
+
 def measure_other(pkg, wid, dev, stream, flush, steps=20, warmup=5):
     """One of the other benchmark configurations: plain calls (or a graph replay for the
     serving step), with the same roofline arithmetic as the headline."""
@@ -530,13 +554,14 @@ def measure_other(pkg, wid, dev, stream, flush, steps=20, warmup=5):
     step_ms, stage_ms, prof_ms, _, _ = time_call(pkg, c, stream, flush, steps, warmup)
     names = stage_names(w)
     rf = roofline_of(w, statistics.fmean(step_ms), stage_ms, names, wid)
+    fused = time_fused(pkg, c, stream, flush)
     del c
     return {"workload": w.name, "timing": f"plain calls, mean of {steps} after {warmup}, L2 flushed",
             "ms_per_call": statistics.fmean(step_ms), "tokens_per_s": w.T / (statistics.fmean(step_ms) / 1e3),
             "step_frac": rf["step_frac"], "stage_frac": rf["frac"], "dominant_stage": rf["kernel"],
             "stages_ms": dict(zip(names, stage_ms)), "profiled_ms_per_call": prof_ms,
             "alg_bytes": rf["alg_bytes_per_launch"], "roofline_us": rf["roofline_us"],
-            "launches_per_call": launches_per_call(w)}
+            "launches_per_call": launches_per_call(w), "fused_entry_point": fused}
 
 
 def main():
@@ -593,6 +618,8 @@ def main():
     value = world * w.T * args.steps / total_s
     names = stage_names(w)
     rf = roofline_of(w, statistics.fmean(step_ms), stage_ms, names, args.workload)
+
+    fused_head = time_fused(pkg, c, stream, flush) if rank == 0 else None
 
     # ---- end to end: pinned host inputs -> device -> call -> host outputs, same stream
     host_in = [t.pin_memory() for t in (w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, w.initial_state, w.state,
@@ -651,6 +678,7 @@ def main():
             "gpu_launches": launches_per_call(w) * args.steps,
             "clocks": clk,
             "per_workload": others,
+            "fused_entry_point": fused_head,
             "decode_step": decode,
             "backward": bwd,
             "wall_s_timed": wall,

@@ -105,7 +105,11 @@ def load_library(path: str | None = None):
     lib.gdp_chain_states.restype = _int
     lib.gdp_chain_states.argtypes = [_vp, _vp, _vp, _i64, _i64, _int, _int, _vp, _vp, _vp]
     lib.gdp_prefill_fused.restype = _int
-    lib.gdp_prefill_fused.argtypes = [_i64, _i64, _int, _int, _int, _int]
+    lib.gdp_prefill_fused.argtypes = [_i64, _i64, _int, _int, _int, _int] + [ctypes.POINTER(_i64)] * 3
+    lib.gdp_prefill_varlen_fused.restype = _int
+    lib.gdp_prefill_varlen_fused.argtypes = [ctypes.POINTER(GdpPrefillArgs), _vp]
+    lib.gdp_prefill_varlen_fused_profiled.restype = _int
+    lib.gdp_prefill_varlen_fused_profiled.argtypes = [ctypes.POINTER(GdpPrefillArgs), _vp, ctypes.POINTER(_vp), _int]
     lib.gdp_prefill_plan.restype = _int
     lib.gdp_prefill_plan.argtypes = [_i64, _i64, _int, _int, _int, _int] + [ctypes.POINTER(_i64)] * 4
     lib.gdp_build_descriptors.restype = _int
@@ -154,9 +158,34 @@ def gdp_prefill_plan(T: int, N: int, H: int, K: int, V: int, M: int) -> dict:
     return dict(zip(("segments", "piece_chunks", "piece_rows", "launches"), (int(x.value) for x in out)))
 
 
-def gdp_prefill_fused(T: int, N: int, H: int, K: int, V: int, M: int) -> bool:
-    """Whether a common-contract call of this shape runs as the one fused kernel (shape-only)."""
-    return bool(load_library().gdp_prefill_fused(T, N, H, K, V, M))
+def gdp_prefill_fused(T: int, N: int, H: int, K: int, V: int, M: int):
+    """The plan of gdp_prefill_varlen_fused for a common-contract call of this shape (dict with
+    piece_chunks, piece_rows, launches), or None when it does not serve the shape."""
+    out = [ctypes.c_int64() for _ in range(3)]
+    ok = load_library().gdp_prefill_fused(T, N, H, K, V, M, *[ctypes.byref(x) for x in out])
+    if not ok:
+        return None
+    return dict(zip(("piece_chunks", "piece_rows", "launches"), (int(x.value) for x in out)))
+
+
+def gdp_prefill_varlen_fused(args: GdpPrefillArgs, stream: int | None = None) -> None:
+    """Enqueue one prefill as the fused kernel (see the header) on ``stream``."""
+    lib = load_library()
+    st = lib.gdp_prefill_varlen_fused(ctypes.byref(args), ctypes.c_void_p(_stream(stream)))
+    if st != GDP_OK:
+        raise GdpError(st, lib.gdp_last_error().decode())
+
+
+def gdp_prefill_varlen_fused_profiled(args: GdpPrefillArgs, events, stream: int | None = None) -> None:
+    """As gdp_prefill_varlen_fused, recording the 4 torch.cuda.Event objects around the stages."""
+    lib = load_library()
+    handles = [e.cuda_event for e in events]
+    if len(handles) != 4 or not all(handles):
+        raise GdpError(GDP_ERR_INVALID_ARG, "need 4 created events (record each once before passing it)")
+    arr = (_vp * 4)(*[ctypes.c_void_p(h) for h in handles])
+    st = lib.gdp_prefill_varlen_fused_profiled(ctypes.byref(args), ctypes.c_void_p(_stream(stream)), arr, 4)
+    if st != GDP_OK:
+        raise GdpError(st, lib.gdp_last_error().decode())
 
 
 def _stream(stream):
@@ -420,8 +449,9 @@ def chunk_gated_delta_product(q, k, v, g=None, beta=None, cu_seqlens=None, num_h
                               chunk_indices=None, chunk_indices_dp=None, chunk_offsets=None, state=None,
                               state_indices=None, return_chunk_states=False, output=None, output_state=None,
                               workspace=None, device_status=None, nt_pad=None, ntdp_pad=None, stream=None,
-                              g_is_alpha=False):
-    """Chunked Gated DeltaProduct varlen prefill on the GPU.
+                              g_is_alpha=False, fused=False):
+    """Chunked Gated DeltaProduct varlen prefill on the GPU (``fused``: through
+    gdp_prefill_varlen_fused instead of gdp_prefill_varlen).
 
     q [T,Hq,K] (or [1,T,Hq,K]), k/v [T*M,Hk,K]/[T*M,Hv,V] bf16 or float16 (one type);
     H = max(Hq, Hv) state heads, Hk equal to Hq or Hv, each dividing H.  g [T,H]
@@ -459,7 +489,7 @@ def chunk_gated_delta_product(q, k, v, g=None, beta=None, cu_seqlens=None, num_h
     a = make_args(q, k, v, g, beta, cu_seqlens, M, scale, initial_state, state, state_indices, output,
                   output_state if state is None else None, cs, chunk_indices, chunk_indices_dp, chunk_offsets,
                   nt_pad, ntdp_pad, use_qk_l2norm_in_kernel, workspace, device_status, g_is_alpha)
-    gdp_prefill_varlen(a, stream)
+    (gdp_prefill_varlen_fused if fused else gdp_prefill_varlen)(a, stream)
     final = output_state if (output_final_state and state is None) else None
     if return_chunk_states:
         return output, final, cs

@@ -83,12 +83,6 @@ PiecePlan fused_piece_plan(int64_t T, int64_t N, int H, int M) {
   return pl;
 }
 
-// The plan a common-contract call of this shape takes (the fused kernel's where it serves the
-// shape, else the staged kernels').
-PiecePlan plan_for(int64_t T, int64_t N, int H, int K, int V, int M) {
-  return gdp::fused_shape(K, V, M) ? fused_piece_plan(T, N, H, M) : piece_plan(T, N, H, M);
-}
-
 // Workspace layout; identical for the size query and the carving.
 struct Layout {
   size_t cod, ci, cid, co, ord, img, img_stride, U, seg, piece, total;
@@ -221,7 +215,7 @@ struct Recompute {
 // transfer pairs (xfer_out != NULL: B and Phi of every sequence into xfer_out, [2][N][H][V][K];
 // output, output_state, chunk_states, initial_state and the state cache are ignored).
 gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t const *ev,
-                   const Recompute *rc = nullptr, float *xfer_out = nullptr) {
+                   const Recompute *rc = nullptr, float *xfer_out = nullptr, bool want_fused = false) {
   g_last_error[0] = 0;
   if (!a) return fail(GDP_ERR_INVALID_ARG, "args is NULL");
   const int64_t T = a->T, N = a->N;
@@ -339,9 +333,12 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
   p.seg_rows = 0;
   p.seg_state = nullptr;
   p.prefetch = (N * (int64_t)H <= gdp::kSegMaxChains) ? 1 : 0;
-  // the fused kernel (WY work, scan and outputs in one launch) serves the common contract of a
-  // plain forward call
-  const bool fused = !rc && !xfer_out && gdp::fused_serves(p);
+  // the fused kernel (WY work, scan and outputs in one launch; gdp_prefill_varlen_fused) serves
+  // the common contract of a plain forward call
+  if (want_fused && (rc || xfer_out || !gdp::fused_serves(p)))
+    return fail(GDP_ERR_UNSUPPORTED,
+                "the fused kernel serves bf16 q/k/v, fp32 natural-log g and beta, fp32 states, K = V = 128, M >= 2");
+  const bool fused = want_fused;
   // a transfer-pair call runs whole sequences in one segment
   const int nseg = xfer_out ? 1 : seg_count(T, N, H, M);
   const PiecePlan pp = xfer_out ? PiecePlan{0, 0} : (fused ? fused_piece_plan(T, N, H, M) : piece_plan(T, N, H, M));
@@ -485,20 +482,23 @@ GDP_EXPORT gdp_status gdp_prefill_plan(int64_t T, int64_t N, int H, int K, int V
   if (!shape_ok(T, N, H, K, V, M))
     return fail(GDP_ERR_INVALID_ARG, "bad shape T=%lld N=%lld H=%d K=%d V=%d M=%d", (long long)T, (long long)N, H, K,
                 V, M);
-  const bool fused = gdp::fused_shape(K, V, M);
-  const int nseg = fused ? 1 : seg_count(T, N, H, M);
-  const PiecePlan pp = plan_for(T, N, H, K, V, M);
+  const int nseg = seg_count(T, N, H, M);
+  const PiecePlan pp = piece_plan(T, N, H, M);
   if (segments) *segments = nseg;
   if (piece_chunks) *piece_chunks = pp.len;
   if (piece_rows) *piece_rows = pp.rows;
-  if (launches)
-    *launches = N == 0 ? 0 : 1 + (fused ? (pp.len > 0 ? 3 : 1) : (nseg > 1 ? 2 * nseg : (pp.len > 0 ? 4 : 2)));
+  if (launches) *launches = N == 0 ? 0 : 1 + (nseg > 1 ? 2 * nseg : (pp.len > 0 ? 4 : 2));
   return GDP_OK;
 }
 
-GDP_EXPORT int gdp_prefill_fused(int64_t T, int64_t N, int H, int K, int V, int M) {
-  if (!shape_ok(T, N, H, K, V, M)) return 0;
-  return gdp::fused_shape(K, V, M) ? 1 : 0;
+GDP_EXPORT int gdp_prefill_fused(int64_t T, int64_t N, int H, int K, int V, int M, int64_t *piece_chunks,
+                                 int64_t *piece_rows, int64_t *launches) {
+  if (!shape_ok(T, N, H, K, V, M) || !gdp::fused_shape(K, V, M)) return 0;
+  const PiecePlan pp = fused_piece_plan(T, N, H, M);
+  if (piece_chunks) *piece_chunks = pp.len;
+  if (piece_rows) *piece_rows = pp.rows;
+  if (launches) *launches = N == 0 ? 0 : 1 + (pp.len > 0 ? 3 : 1);
+  return 1;
 }
 
 GDP_EXPORT const char *gdp_last_error(void) { return g_last_error; }
@@ -540,6 +540,21 @@ GDP_EXPORT gdp_status gdp_build_descriptors(const void *cu_seqlens, int cu_seqle
 
 GDP_EXPORT gdp_status gdp_prefill_varlen(const gdp_prefill_args *a, void *stream) {
   return prefill(a, (cudaStream_t)stream, nullptr);
+}
+
+GDP_EXPORT gdp_status gdp_prefill_varlen_fused(const gdp_prefill_args *a, void *stream) {
+  return prefill(a, (cudaStream_t)stream, nullptr, nullptr, nullptr, true);
+}
+
+GDP_EXPORT gdp_status gdp_prefill_varlen_fused_profiled(const gdp_prefill_args *a, void *stream, void *const *events,
+                                                        int num_events) {
+  if (!events || num_events != 4) {
+    g_last_error[0] = 0;
+    return fail(GDP_ERR_INVALID_ARG, "gdp_prefill_varlen_fused_profiled needs exactly 4 events");
+  }
+  cudaEvent_t ev[4];
+  for (int i = 0; i < 4; ++i) ev[i] = (cudaEvent_t)events[i];
+  return prefill(a, (cudaStream_t)stream, ev, nullptr, nullptr, true);
 }
 
 GDP_EXPORT gdp_status gdp_prefill_transfer(const gdp_prefill_args *a, float *pairs, void *stream) {

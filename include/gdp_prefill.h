@@ -223,14 +223,31 @@ gdp_status gdp_prefill_plan(int64_t T, int64_t N, int H, int K, int V, int num_h
                             int64_t *piece_chunks, int64_t *piece_rows, int64_t *launches);
 
 /*
- * 1 when a call of this shape over the common contract (bf16 q/k/v, fp32 natural-log g and
- * beta, fp32 states, chains not split into pieces) runs as one fused kernel after the
- * descriptor kernel -- the WY work, the state scan, the outputs and the state scatter of every
- * (sequence, head) in one CTA, with no operand images in the workspace -- and 0 when it runs
- * the staged kernels (gdp_prefill_plan).  Served: K = V = 128 and num_householder >= 2.
- * Shape-only; 0 for a bad shape.
+ * gdp_prefill_varlen_fused: the same prefill as one fused kernel per (sequence, head) -- the
+ * WY work, the state scan, the outputs and the state scatter of every expanded chunk in one
+ * CTA, so no operand image or U^T reaches the workspace or HBM (Megatron page, stages 1-4 as
+ * one pipeline) -- after the descriptor kernel.  Over few sequences (N <= 32) the chains are
+ * split into pieces as in gdp_prefill_plan (a pass from zero and from the identity, the
+ * combine, a pass from the entering states).  Arguments, results and tolerances are those of
+ * gdp_prefill_varlen; the workspace is the same size.  Served: bf16 q/k/v (heads may be
+ * grouped), fp32 natural-log g (or NULL), fp32 beta (or NULL), an fp32 dense initial state or
+ * the cache, K = V = 128, num_householder >= 2; anything else is GDP_ERR_UNSUPPORTED before any
+ * launch.  Measured on one GB300 it is slower than gdp_prefill_varlen on every benchmark
+ * workload (its chunks' WY work lies on the serial state chain), which is why
+ * gdp_prefill_varlen does not route calls here.  The _profiled form records 4 events like
+ * gdp_prefill_varlen_profiled (the third equal to the second: no WY stage).
  */
-int gdp_prefill_fused(int64_t T, int64_t N, int H, int K, int V, int num_householder);
+gdp_status gdp_prefill_varlen_fused(const gdp_prefill_args *args, void *stream);
+gdp_status gdp_prefill_varlen_fused_profiled(const gdp_prefill_args *args, void *stream, void *const *events,
+                                             int num_events);
+
+/*
+ * 1 when gdp_prefill_varlen_fused serves a common-contract call of this shape (K = V = 128,
+ * num_householder >= 2), with its plan: piece_chunks (0 unless the chains are split),
+ * piece_rows and launches (any may be NULL); 0 otherwise (nothing written).  Shape-only.
+ */
+int gdp_prefill_fused(int64_t T, int64_t N, int H, int K, int V, int num_householder, int64_t *piece_chunks,
+                      int64_t *piece_rows, int64_t *launches);
 
 /*
  * The prefill forward pass: enqueue descriptors (unless prebuilt), the prep

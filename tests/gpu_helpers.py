@@ -20,7 +20,8 @@ def to_dev(w, dev, cu_dtype=torch.int32):
 
 
 def run(w, dev, d=None, prebuilt=False, status=None, scale=None, **kw):
-    """One call through the library; returns (o, final_state, chunk_states, device tensors)."""
+    """One call through the library (``fused=True``: the fused entry point); returns
+    (o, final_state, chunk_states, device tensors)."""
     d = d or to_dev(w, dev)
     ci = cid = co = None
     if prebuilt:

@@ -201,18 +201,16 @@ def test_prefill_plan(lib):
     assert split["segments"] == 1 and split["piece_chunks"] == 6 and split["launches"] == 5
     assert split["piece_rows"] * 8 <= 128
     assert pkg.gdp_prefill_plan(32768, 8, 16, 128, 128, 3)["piece_chunks"] == 0  # 128 chains fill the GPU
-    seg = pkg.gdp_prefill_plan(65536, 1, 32, 64, 64, 2)  # head size 64: the staged kernels, segmented
+    seg = pkg.gdp_prefill_plan(65536, 1, 32, 128, 128, 2)
     assert seg["segments"] == 16 and seg["piece_chunks"] == 0 and seg["launches"] == 33
-    # head size 128, M >= 2: the fused kernel; one long chain per head splits into pieces
-    # (descriptors, pass 1, combine, pass 2)
-    fused = pkg.gdp_prefill_plan(65536, 1, 32, 128, 128, 2)
-    assert fused["segments"] == 1 and fused["piece_chunks"] == 683 and fused["launches"] == 4
-    assert fused["piece_rows"] * 32 <= 128
-    assert pkg.gdp_prefill_plan(32768, 8, 16, 128, 128, 3)["launches"] == 2  # descriptors + fused
-    assert pkg.gdp_prefill_fused(65536, 1, 32, 128, 128, 2) and pkg.gdp_prefill_fused(32768, 8, 16, 128, 128, 3)
-    assert pkg.gdp_prefill_fused(1421, 4, 8, 128, 128, 2)
-    assert not pkg.gdp_prefill_fused(65536, 1, 32, 128, 128, 1)  # M = 1: its tensor memory does not fit
-    assert not pkg.gdp_prefill_fused(4096, 2, 2, 64, 64, 2)  # head size 64
+    # gdp_prefill_varlen_fused's plan: one long chain per head splits into pieces (descriptors,
+    # pass 1, combine, pass 2); many chains run whole (descriptors + the fused kernel)
+    fused = pkg.gdp_prefill_fused(65536, 1, 32, 128, 128, 2)
+    assert fused == {"piece_chunks": 683, "piece_rows": 4, "launches": 4}
+    assert pkg.gdp_prefill_fused(32768, 8, 16, 128, 128, 3) == {"piece_chunks": 0, "piece_rows": 0, "launches": 2}
+    assert pkg.gdp_prefill_fused(1421, 4, 8, 128, 128, 2)["piece_chunks"] == 6
+    assert pkg.gdp_prefill_fused(65536, 1, 32, 128, 128, 1) is None  # M = 1: its tensor memory does not fit
+    assert pkg.gdp_prefill_fused(4096, 2, 2, 64, 64, 2) is None  # head size 64
     assert pkg.gdp_prefill_plan(5000, 33, 1, 64, 64, 2)["piece_chunks"] == 0  # more than 32 sequences
     assert pkg.gdp_prefill_plan(0, 0, 4, 64, 64, 2)["launches"] == 0
     with pytest.raises(pkg.GdpError):
@@ -221,7 +219,7 @@ def test_prefill_plan(lib):
     assert (pkg.gdp_prefill_workspace_bytes(1421, 4, 8, 64, 64, 2)
             >= 3 * split["piece_rows"] * 8 * 64 * 64 * 4)
     assert (pkg.gdp_prefill_workspace_bytes(65536, 1, 32, 128, 128, 2)
-            >= 3 * fused["piece_rows"] * 32 * 128 * 128 * 4)
+            >= 3 * fused["piece_rows"] * 32 * 128 * 128 * 4)  # the fused entry point's pieces
 
 
 @pytest.mark.parametrize("T,N,H,M", [(1421, 4, 8, 2), (3000, 1, 1, 1), (1143, 4, 2, 3), (5000, 32, 1, 2),

@@ -3,8 +3,8 @@
 Every output buffer (o, the final state, the chunk states) and the workspace is
 carved out of a larger allocation whose guard bands before and after it hold a
 fixed byte pattern; after the call the bands must be unchanged, so no kernel
-writes outside the buffers it was given.  Each way a call runs (the fused kernel whole or
-split into pieces; the staged kernels plain, split or segmented) is covered, and
+writes outside the buffers it was given.  Each way a call runs (gdp_prefill_varlen plain,
+split or segmented; gdp_prefill_varlen_fused whole or split into pieces) is covered, and
 the outputs are checked against the oracle as well.
 """
 import pytest
@@ -37,18 +37,20 @@ class Guarded:
 
 
 @pytest.mark.parametrize("lengths,H,d,M,kind", [
+    ([5 * i + 3 for i in range(40)], 2, 128, 3, "staged"),
+    ([100, 257, 64, 300], 4, 128, 2, "staged split"),
+    ([12288], 1, 128, 2, "staged segmented"),
     ([5 * i + 3 for i in range(40)], 2, 128, 3, "fused"),
     ([100, 257, 64, 300], 4, 128, 2, "fused split"),
-    ([5 * i + 3 for i in range(40)], 2, 64, 2, "staged"),
-    ([100, 257, 64, 300], 4, 64, 2, "staged split"),
-    ([12288], 1, 64, 2, "staged segmented"),
 ])
 def test_no_write_outside_the_given_buffers(cuda_device, lengths, H, d, M, kind):
     dev = cuda_device
     w = make_custom(lengths, H, d, M, seed=123, init_sigma=0.1, chunk_states=True)
-    plan = pkg.gdp_prefill_plan(w.T, w.N, w.H, w.d, w.d, w.M)
-    got = "fused" if pkg.gdp_prefill_fused(w.T, w.N, w.H, w.d, w.d, w.M) else "staged"
-    got += " segmented" if plan["segments"] > 1 else " split" if plan["piece_chunks"] else ""
+    fused = kind.startswith("fused")
+    plan = pkg.gdp_prefill_fused(w.T, w.N, w.H, w.d, w.d, w.M) if fused else pkg.gdp_prefill_plan(
+        w.T, w.N, w.H, w.d, w.d, w.M)
+    got = ("fused" if fused else "staged") + (" segmented" if plan.get("segments", 1) > 1 else
+                                              " split" if plan["piece_chunks"] else "")
     assert kind == got
     nt = pkg.gdp_nt_pad(w.T, w.N)
     g_out = Guarded(w.T * w.H * w.d * 2, dev)
@@ -64,7 +66,7 @@ def test_no_write_outside_the_given_buffers(cuda_device, lengths, H, d, M, kind)
     q, k, v, g, beta, cu, init = (t.to(dev) for t in (w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, w.initial_state))
     a = pkg.make_args(q, k, v, g, beta, cu, w.M, w.scale, init, None, None, out, fin, cs, None, None, None, None,
                       None, False, ws, status)
-    pkg.gdp_prefill_varlen(a)
+    (pkg.gdp_prefill_varlen_fused if fused else pkg.gdp_prefill_varlen)(a)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     for name, gb in (("output", g_out), ("final state", g_fin), ("chunk states", g_cs), ("workspace", g_ws)):

@@ -23,18 +23,19 @@ from tests.gpu_helpers import run, to_dev
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("d,fused", [(128, True), (64, False)])
-def test_wait_expiry_sets_timeout_and_context_survives(cuda_device, d, fused):
-    """The fused kernel (head size 128) and the staged scan (head size 64) each withhold one copy."""
-    w = make_custom([100, 37], 2, d, 2, seed=31, init_sigma=0.1)
-    assert pkg.gdp_prefill_fused(w.T, w.N, w.H, w.d, w.d, w.M) == fused
-    plan = pkg.gdp_prefill_plan(w.T, w.N, w.H, w.d, w.d, w.M)
-    assert plan["piece_chunks"] == 0 and plan["segments"] == 1  # one launch of the kernel under test
+@pytest.mark.parametrize("fused", [False, True])
+def test_wait_expiry_sets_timeout_and_context_survives(cuda_device, fused):
+    """The staged scan (gdp_prefill_varlen) and the fused kernel (gdp_prefill_varlen_fused) each
+    withhold one copy."""
+    w = make_custom([100, 37], 2, 128, 2, seed=31, init_sigma=0.1)
+    plan = pkg.gdp_prefill_fused(w.T, w.N, w.H, w.d, w.d, w.M) if fused else pkg.gdp_prefill_plan(
+        w.T, w.N, w.H, w.d, w.d, w.M)
+    assert plan["piece_chunks"] == 0  # one launch of the kernel under test
     d = to_dev(w, cuda_device)
     status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
     pkg.gdp_arm_wait_expiry_test(2_000_000)  # 2 ms
     t0 = time.perf_counter()
-    run(w, cuda_device, d=d, status=status)  # synchronises
+    run(w, cuda_device, d=d, status=status, fused=fused)  # synchronises
     took = time.perf_counter() - t0
     st = int(status.item())
     assert st & pkg.GDP_DEV_ERR_TIMEOUT, f"status {st:#x}: the withheld copy's wait did not run out"
@@ -42,7 +43,7 @@ def test_wait_expiry_sets_timeout_and_context_survives(cuda_device, d, fused):
     assert took < 5.0, f"the expired call took {took:.2f} s"
     # the context is usable and the next (unarmed) call is correct
     status.zero_()
-    o, fin, _, _ = run(w, cuda_device, d=d, status=status)
+    o, fin, _, _ = run(w, cuda_device, d=d, status=status, fused=fused)
     assert int(status.item()) == 0
     ref = oracle.forward(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, w.M, w.scale, initial_state=w.initial_state)
     check_o(o.cpu(), ref["o"])

@@ -1,7 +1,7 @@
 """GPU parity of the fused prefill kernel (WY work, state scan, outputs and state scatter in one
 CTA per (sequence, head)) against the float64 oracle.
 
-Every case below asserts that its shape takes the fused plan (gdp_prefill_fused), so these
+Every case runs through gdp_prefill_varlen_fused (the plan of gdp_prefill_fused), so these
 tests hold the fused kernel itself to the parity bar: per-head relative L2 <= 5e-3 on o and
 <= 2e-3 on final and chunk states (and per (sequence, head) on states), max |delta o| <= 2e-2,
 untouched cache slots bit for bit.  The cases cover ragged chunk tails, empty and one-token
@@ -62,11 +62,11 @@ def _check(w, o, fin, cs, ref):
 @pytest.mark.parametrize("name", sorted(CASES))
 def test_fused_parity(cuda_device, name):
     w = make_custom(seed=sorted(CASES).index(name) + 900, d=128, name=name, **CASES[name])
-    assert pkg.gdp_prefill_fused(w.T, w.N, w.H, w.d, w.d, w.M), "shape should take the fused kernel"
-    split = pkg.gdp_prefill_plan(w.T, w.N, w.H, w.d, w.d, w.M)["piece_chunks"] > 0
-    assert split == (name in SPLIT)
+    plan = pkg.gdp_prefill_fused(w.T, w.N, w.H, w.d, w.d, w.M)
+    assert plan is not None, "the fused kernel should serve this shape"
+    assert (plan["piece_chunks"] > 0) == (name in SPLIT)
     status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
-    o, fin, cs, _ = run(w, cuda_device, status=status)
+    o, fin, cs, _ = run(w, cuda_device, status=status, fused=True)
     assert int(status.item()) == 0
     _check(w, o, fin, cs, _oracle(w))
 
@@ -76,8 +76,8 @@ def test_fused_state_cache_in_place(cuda_device):
     write nothing, untouched slots bit-identical."""
     w = make_custom([100, 0, 513, 64, 1, 300] * 6, 2, 128, 4, seed=77, cache_slots=48, cache_sigma=0.1,
                     padding_slots=5)
-    assert pkg.gdp_prefill_fused(w.T, w.N, w.H, w.d, w.d, w.M)
-    o, fin, cs, d = run(w, cuda_device)
+    assert pkg.gdp_prefill_fused(w.T, w.N, w.H, w.d, w.d, w.M) is not None
+    o, fin, cs, d = run(w, cuda_device, fused=True)
     ref = _oracle(w)
     check_o(o.cpu(), ref["o"], cu_seqlens=w.cu_seqlens)
     cache = d["state"].cpu()
@@ -92,8 +92,8 @@ def test_fused_split_state_cache(cuda_device):
     """Split chains with the state cache: pieces read the slot through the combine kernel, the
     last piece writes it; padding sequences start from zero and write nothing."""
     w = make_custom([1500, 3, 700, 0], 4, 128, 2, seed=78, cache_slots=8, cache_sigma=0.1, padding_slots=1)
-    assert pkg.gdp_prefill_plan(w.T, w.N, w.H, w.d, w.d, w.M)["piece_chunks"] > 0
-    o, fin, cs, d = run(w, cuda_device)
+    assert pkg.gdp_prefill_fused(w.T, w.N, w.H, w.d, w.d, w.M)["piece_chunks"] > 0
+    o, fin, cs, d = run(w, cuda_device, fused=True)
     ref = _oracle(w)
     check_o(o.cpu(), ref["o"], cu_seqlens=w.cu_seqlens)
     cache = d["state"].cpu()
@@ -108,16 +108,16 @@ def test_fused_longest_first_order(cuda_device):
     """Over whole sequences the fused kernel runs them longest first (a device-built order);
     lengths in rising order, equal lengths and an empty sequence come out right."""
     w = make_custom(list(range(1, 40)) + [0, 600, 600, 2000], 2, 128, 2, seed=79, init_sigma=0.1, chunk_states=True)
-    assert pkg.gdp_prefill_plan(w.T, w.N, w.H, w.d, w.d, w.M)["piece_chunks"] == 0
-    o, fin, cs, _ = run(w, cuda_device)
+    assert pkg.gdp_prefill_fused(w.T, w.N, w.H, w.d, w.d, w.M)["piece_chunks"] == 0
+    o, fin, cs, _ = run(w, cuda_device, fused=True)
     _check(w, o, fin, cs, _oracle(w))
 
 
 def test_fused_grouped_heads(cuda_device):
     """q, k with 2 heads serving 8 state heads (GVA): each input head feeds a run of state heads."""
     w = make_custom([300, 77, 1000] * 11, 8, 128, 2, seed=31, hq=2, hk=2, init_sigma=0.1, chunk_states=True)
-    assert pkg.gdp_prefill_fused(w.T, w.N, w.H, w.d, w.d, w.M)
-    o, fin, cs, _ = run(w, cuda_device)
+    assert pkg.gdp_prefill_fused(w.T, w.N, w.H, w.d, w.d, w.M) is not None
+    o, fin, cs, _ = run(w, cuda_device, fused=True)
     _check(w, o, fin, cs, _oracle(w))
 
 
@@ -134,16 +134,27 @@ def test_fused_graph_replay_bit_identical(cuda_device):
                       False, ws, None)
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
-        pkg.gdp_prefill_varlen(a, s.cuda_stream)
+        pkg.gdp_prefill_varlen_fused(a, s.cuda_stream)
     torch.cuda.synchronize()
     eager = (out.clone(), fin.clone(), cs.clone())
     out.zero_(), fin.zero_(), cs.zero_()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.stream(s):
         graph.capture_begin()
-        pkg.gdp_prefill_varlen(a, s.cuda_stream)
+        pkg.gdp_prefill_varlen_fused(a, s.cuda_stream)
         graph.capture_end()
     graph.replay()
     torch.cuda.synchronize()
     for x, y in zip((out, fin, cs), eager):
         assert torch.equal(x, y)
+
+
+def test_fused_rejects_what_it_does_not_serve(cuda_device):
+    """Another input type or head size is refused before any launch (the staged kernels serve it)."""
+    w = make_custom([100, 37], 2, 64, 2, seed=3)
+    assert pkg.gdp_prefill_fused(w.T, w.N, w.H, w.d, w.d, w.M) is None
+    with pytest.raises(pkg.GdpError):
+        run(w, cuda_device, fused=True)
+    w16 = make_custom([100, 37], 2, 128, 2, seed=3, qkv_dtype=torch.float16)
+    with pytest.raises(pkg.GdpError):
+        run(w16, cuda_device, fused=True)

@@ -3,9 +3,8 @@ allocate device memory (a plugin inside a runtime that owns all device memory,
 or a host program that may not call cudaMalloc in its serving loop).
 
 The entry point is called through the C ABI twice in a row on the same inputs,
-once for each way a call runs (the fused kernel whole or split into pieces; the
-staged kernels plain, split or segmented; gdp_prefill_fused and gdp_prefill_plan
-name which), and each result must equal, bit for bit, the
+once for each of the three ways a call runs (plain, split chains, segmented;
+gdp_prefill_plan names which), and each result must equal, bit for bit, the
 main entry point's result with a caller-owned workspace: the two run the same
 kernels in the same order, only the scratch memory differs.  One call of each
 shape is also checked against the float64 oracle with the parity tolerances.
@@ -25,25 +24,18 @@ from tests._parity import check_o, check_state
 
 pytestmark = pytest.mark.gpu
 
-# (lengths, H, head size, M, the plan the shape takes): the fused kernel whole and split into
-# pieces, the staged kernels plain, split and segmented
+# (lengths, H, head size, M, the plan the shape takes)
 SHAPES = [
-    ([5 * i + 3 for i in range(40)], 2, 128, 3, "fused"),
-    ([100, 257, 64, 300], 4, 128, 2, "fused split"),
-    ([5 * i + 3 for i in range(40)], 2, 64, 2, "staged"),
-    ([100, 257, 64, 300], 4, 64, 2, "staged split"),
-    ([12288], 1, 64, 2, "staged segmented"),
+    ([5 * i + 3 for i in range(40)], 2, 128, 3, "plain"),
+    ([100, 257, 64, 300], 4, 128, 2, "split"),
+    ([12288], 1, 128, 2, "segmented"),
+    ([100, 257, 64, 300], 4, 64, 1, "split"),
 ]
 
 
 def _plan_kind(w):
     plan = pkg.gdp_prefill_plan(w.T, w.N, w.H, w.d, w.d, w.M)
-    kind = "fused" if pkg.gdp_prefill_fused(w.T, w.N, w.H, w.d, w.d, w.M) else "staged"
-    if plan["segments"] > 1:
-        kind += " segmented"
-    elif plan["piece_chunks"] > 0:
-        kind += " split"
-    return kind
+    return "segmented" if plan["segments"] > 1 else ("split" if plan["piece_chunks"] > 0 else "plain")
 
 
 def _args(w, d, out, fin, cs, workspace):
