@@ -73,8 +73,8 @@ struct WyLayout {
     A = tul + 8192u;                       // fp32 [64][65]
     T = A + 4u * kChunk * kLd;             // fp32 [64][68]
     Y = T + 4u * kChunk * kLdT;            // fp32 [32][36] block products
-    scal = Y + 4u * 32 * kLdY;             // G2, beta, rk, rq, wc, uc, kscale  [7][64]
-    total = scal + 4u * 7 * kChunk;
+    scal = Y + 4u * 32 * kLdY;             // G2, beta, rk, rq, wc, uc, kscale, colf  [8][64]
+    total = scal + 4u * 8 * kChunk;
   }
 };
 
@@ -265,6 +265,7 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
   float *G2 = reinterpret_cast<float *>(sm + lay.scal);
   float *bt = G2 + kChunk, *rk = bt + kChunk, *rq = rk + kChunk, *wc = rq + kChunk, *uc = wc + kChunk;
   float *ks = uc + kChunk;  // 2^(G2_last - G2_s) rk_s (0 past the chunk end)
+  float *colf = ks + kChunk;  // 2^(m - G2_j) rk_j: the column factor of the separable decay
   __shared__ uint32_t tmem_slot;
   __shared__ __align__(8) uint64_t mma_bar, ld_bar;
   __shared__ float warp_tot;
@@ -377,10 +378,18 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
   const float G2last = G2[len - 1];
   const bool fast = G2last >= kFastMinLog2Gamma;
   const float shift = fast ? G2last : 0.f;
+  // The decay factor 2^(G2_i - G2_j) of A and P splits into 2^(G2_i - m) 2^(m - G2_j) with m the
+  // middle of the chunk's G2 range (G2 falls from G2[0] to G2[len - 1]) whenever that range is
+  // at most 120: every factor then stays within 2^+-60, far inside fp32, and one exp2 per row
+  // and per column replaces one per element.  A wider range (a decay of more than ~1.3 per
+  // row) keeps the exact per-element form.
+  const bool sep = G2[0] - G2last <= 120.f;
+  const float mid = 0.5f * (G2[0] + G2last);
   if (tid < kChunk) {
     wc[tid] = bt[tid] * exp2f(G2[tid] - shift) * rk[tid];
     uc[tid] = bt[tid];
     ks[tid] = (tid < len) ? exp2f(G2[len - 1] - G2[tid]) * rk[tid] : 0.f;
+    colf[tid] = (sep && tid < len) ? exp2f(mid - G2[tid]) * rk[tid] : 0.f;
   }
 
   // T starts at zero (its blocks above the diagonal stay so); the area is idle until the inverse
@@ -404,14 +413,23 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
       const int i = r;
       const bool rowlive = i < len;
       const float gi = G2[i], si = bt[i] * rk[i];
+      const float rowf = sep ? si * exp2f(gi - mid) : 0.f;
 #pragma unroll 1
       for (int c0 = cbeg; c0 < cbeg + 32; c0 += 16) {
         float dv[16];
         tmem_ld16(taddr + c0, dv);
+        if (sep) {
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const int j = c0 + u;
-          A[i * kLd + j] = (j < i && rowlive) ? si * exp2f(gi - G2[j]) * rk[j] * dv[u] : 0.f;
+          for (int u = 0; u < 16; ++u) {
+            const int j = c0 + u;
+            A[i * kLd + j] = (j < i && rowlive) ? rowf * colf[j] * dv[u] : 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const int j = c0 + u;
+            A[i * kLd + j] = (j < i && rowlive) ? si * exp2f(gi - G2[j]) * rk[j] * dv[u] : 0.f;
+          }
         }
       }
     } else {
@@ -421,6 +439,7 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
       const float gp = live ? G2[pr] : 0.f;
       const float qscale = live ? p.scale * exp2f(gp - shift) * rq[qi] : 0.f;
       const float sc = live ? p.scale * rq[qi] : 0.f;
+      const float rowf = (live && sep) ? sc * exp2f(gp - mid) : 0.f;
 #pragma unroll 1
       for (int c0 = cbeg; c0 < cbeg + 32; c0 += 16) {
         float dv[16];
@@ -433,7 +452,9 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const int s_ = c0 + u4 + u;
-              o[u] = (live && s_ <= pr) ? sc * exp2f(gp - G2[s_]) * rk[s_] * dv[u4 + u] : 0.f;
+              o[u] = (live && s_ <= pr)
+                         ? (sep ? rowf * colf[s_] * dv[u4 + u] : sc * exp2f(gp - G2[s_]) * rk[s_] * dv[u4 + u])
+                         : 0.f;
             }
             *reinterpret_cast<float4 *>(img + il.pm(d, qi, c0 + u4)) = o4;
           }
@@ -585,20 +606,36 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
 #pragma unroll
         for (int j = 0; j < 16; j += 4)
           Ut[((c0 + j) >> 2) * 32] = make_float4(uv[j] * isu, uv[j + 1] * isu, uv[j + 2] * isu, uv[j + 3] * isu);
-        // -W image: element (s, f) at row qpad + s of K-block f/32 (a row of 32 lanes = 128 bytes)
+        // -W image: element (s, f) at row qpad + s of K-block f/32 (a row of 32 lanes = 128
+        // bytes).  Rows qpad + c0 + u share (row / 8) for u < 8 and u >= 8, and their in-atom
+        // offset depends on u % 8 only: eight offsets per thread, computed once
+        uint32_t xo[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) xo[k] = ImageLayout::swz_off(k, f);
+        unsigned char *w0 = wimg + (uint32_t)((QP + c0) >> 3) * 1024u;
 #pragma unroll
         for (int u = 0; u < 16; ++u)
-          *reinterpret_cast<float *>(wimg + ImageLayout::swz_off(QP + c0 + u, f)) = -wv[u] * isw;
+          *reinterpret_cast<float *>(w0 + (uint32_t)(u >> 3) * 1024u + xo[u & 7]) = -wv[u] * isw;
       }
     }
     // Ktil^T image: row f = 2^(G2_last - G2_s) rk_s k[s][f], K-block s/32; lane = s, so each
-    // store instruction writes one 128-byte row segment; this warp takes rows f of its quadrant
+    // store instruction writes one 128-byte row segment.  This warp takes the rows f of its
+    // quadrant eight at a time: one 16-byte load of k row s gives features f0 .. f0 + 7, each
+    // stored to its own row at the swizzled column s (eight offsets per thread, computed once)
     const int s_ = sbeg + lane;
     const float kss = ks[s_];
     unsigned char *kimg = img + il.b2 + chalf * il.b2_block;
-#pragma unroll 4
-    for (int fr = quad * (d / 4); fr < (quad + 1) * (d / 4); ++fr)
-      *reinterpret_cast<float *>(kimg + ImageLayout::swz_off(fr, s_)) = kss * in_at<F16>(kq, 128, s_, fr);
+    uint32_t yo[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) yo[j] = ImageLayout::swz_off(j, s_);
+#pragma unroll 1
+    for (int f0 = quad * (d / 4); f0 < (quad + 1) * (d / 4); f0 += 8) {
+      float x[8];
+      in8_at<F16>(kq, 128, s_, f0, x);
+      unsigned char *r0 = kimg + (uint32_t)(f0 >> 3) * 1024u;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) *reinterpret_cast<float *>(r0 + yo[j]) = kss * x[j];
+    }
   }
   if (tid == 0) {
     ImageMeta *mt = reinterpret_cast<ImageMeta *>(img + il.meta);
