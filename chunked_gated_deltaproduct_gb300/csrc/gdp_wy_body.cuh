@@ -73,8 +73,8 @@ struct WyLayout {
     A = tul + 8192u;                       // fp32 [64][65]
     T = A + 4u * kChunk * kLd;             // fp32 [64][68]
     Y = T + 4u * kChunk * kLdT;            // fp32 [32][36] block products
-    scal = Y + 4u * 32 * kLdY;             // G2, beta, rk, rq, wc, uc, kscale, colf  [8][64]
-    total = scal + 4u * 8 * kChunk;
+    scal = Y + 4u * 32 * kLdY;             // G2, beta, rk, rq, wc, uc, kscale  [7][64]
+    total = scal + 4u * 7 * kChunk;
   }
 };
 
@@ -265,7 +265,6 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
   float *G2 = reinterpret_cast<float *>(sm + lay.scal);
   float *bt = G2 + kChunk, *rk = bt + kChunk, *rq = rk + kChunk, *wc = rq + kChunk, *uc = wc + kChunk;
   float *ks = uc + kChunk;  // 2^(G2_last - G2_s) rk_s (0 past the chunk end)
-  float *colf = ks + kChunk;  // 2^(m - G2_j) rk_j: the column factor of the separable decay
   __shared__ uint32_t tmem_slot;
   __shared__ __align__(8) uint64_t mma_bar, ld_bar;
   __shared__ float warp_tot;
@@ -378,18 +377,10 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
   const float G2last = G2[len - 1];
   const bool fast = G2last >= kFastMinLog2Gamma;
   const float shift = fast ? G2last : 0.f;
-  // The decay factor 2^(G2_i - G2_j) of A and P splits into 2^(G2_i - m) 2^(m - G2_j) with m the
-  // middle of the chunk's G2 range (G2 falls from G2[0] to G2[len - 1]) whenever that range is
-  // at most 120: every factor then stays within 2^+-60, far inside fp32, and one exp2 per row
-  // and per column replaces one per element.  A wider range (a decay of more than ~1.3 per
-  // row) keeps the exact per-element form.
-  const bool sep = G2[0] - G2last <= 120.f;
-  const float mid = 0.5f * (G2[0] + G2last);
   if (tid < kChunk) {
     wc[tid] = bt[tid] * exp2f(G2[tid] - shift) * rk[tid];
     uc[tid] = bt[tid];
     ks[tid] = (tid < len) ? exp2f(G2[len - 1] - G2[tid]) * rk[tid] : 0.f;
-    colf[tid] = (sep && tid < len) ? exp2f(mid - G2[tid]) * rk[tid] : 0.f;
   }
 
   // T starts at zero (its blocks above the diagonal stay so); the area is idle until the inverse
@@ -413,23 +404,14 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
       const int i = r;
       const bool rowlive = i < len;
       const float gi = G2[i], si = bt[i] * rk[i];
-      const float rowf = sep ? si * exp2f(gi - mid) : 0.f;
 #pragma unroll 1
       for (int c0 = cbeg; c0 < cbeg + 32; c0 += 16) {
         float dv[16];
         tmem_ld16(taddr + c0, dv);
-        if (sep) {
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const int j = c0 + u;
-            A[i * kLd + j] = (j < i && rowlive) ? rowf * colf[j] * dv[u] : 0.f;
-          }
-        } else {
-#pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const int j = c0 + u;
-            A[i * kLd + j] = (j < i && rowlive) ? si * exp2f(gi - G2[j]) * rk[j] * dv[u] : 0.f;
-          }
+        for (int u = 0; u < 16; ++u) {
+          const int j = c0 + u;
+          A[i * kLd + j] = (j < i && rowlive) ? si * exp2f(gi - G2[j]) * rk[j] * dv[u] : 0.f;
         }
       }
     } else {
@@ -439,7 +421,6 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
       const float gp = live ? G2[pr] : 0.f;
       const float qscale = live ? p.scale * exp2f(gp - shift) * rq[qi] : 0.f;
       const float sc = live ? p.scale * rq[qi] : 0.f;
-      const float rowf = (live && sep) ? sc * exp2f(gp - mid) : 0.f;
 #pragma unroll 1
       for (int c0 = cbeg; c0 < cbeg + 32; c0 += 16) {
         float dv[16];
@@ -452,9 +433,7 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const int s_ = c0 + u4 + u;
-              o[u] = (live && s_ <= pr)
-                         ? (sep ? rowf * colf[s_] * dv[u4 + u] : sc * exp2f(gp - G2[s_]) * rk[s_] * dv[u4 + u])
-                         : 0.f;
+              o[u] = (live && s_ <= pr) ? sc * exp2f(gp - G2[s_]) * rk[s_] * dv[u4 + u] : 0.f;
             }
             *reinterpret_cast<float4 *>(img + il.pm(d, qi, c0 + u4)) = o4;
           }
