@@ -332,7 +332,6 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
   p.seg_hi = INT64_MAX;
   p.seg_rows = 0;
   p.seg_state = nullptr;
-  p.prefetch = (N * (int64_t)H <= gdp::kSegMaxChains) ? 1 : 0;
   // the fused kernel (WY work, scan and outputs in one launch; gdp_prefill_varlen_fused) serves
   // the common contract of a plain forward call
   if (want_fused && (rc || xfer_out || !gdp::fused_serves(p)))

@@ -115,8 +115,6 @@ struct Problem {
   int64_t seg_lo, seg_hi;
   int seg_rows;
   float *seg_state;
-  // scan: prefetch image and U^T tiles into L2 ahead of use (few chains: HBM has headroom)
-  int prefetch;
   // input variants: head counts of q, k, v (each divides H; state head h reads head
   // h / (H / Hx), computed as input_head(h, hmul_x)), element types, linear-space gate
   int Hq, Hk, Hv;

@@ -567,20 +567,10 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
     }
   } else if (lane == 0) {
     // ---------------- producer thread: image copies ----------------
-    // L2 prefetch kPrefetch chunks ahead of the copies (few chains only: with many the scan
-    // already streams at HBM bandwidth): the image and U^T tiles were written by the WY
-    // kernel long before and sit in HBM; the prep warps' U^T loads then hit L2
-    constexpr int kPrefetch = 4;
-    const uint32_t ubytes = (uint32_t)V * kChunk * 4u;
-    auto prefetch = [&](int64_t e) {
-      if (p.prefetch && e < nrun) {
-        bulk_prefetch_l2(image(e), il.bytes & ~15u);
-        if (!transfer) bulk_prefetch_l2(p.U + ((cod_i + e0 + e) * H + h) * (int64_t)V * kChunk, ubytes);
-      }
-    };
-    for (int64_t e = 0; e < kPrefetch; ++e) prefetch(nst + e);
+    // (no L2 prefetch ahead of the copies: with the WY kernel writing the next segment's images
+    // beside the scan, prefetching 2 / 4 / 8 / 16 chunks ahead measured 0 / 3 / 5 / 8 % slower on
+    // the 65536-token sequence than none: the prefetched lines are evicted before their copy)
     for (int64_t e = 0; e + nst < nrun; ++e) {
-      prefetch(e + nst + kPrefetch);
       const int b = (int)(e & 1);
       if (!mbar_wait_or_abort(&b1_done[b], (uint32_t)((e >> 1) & 1), &abort_flag, wl)) break;
       load_part1(e + nst);

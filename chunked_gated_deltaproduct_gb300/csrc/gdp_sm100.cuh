@@ -254,10 +254,6 @@ __device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gsrc, uint3
                : "memory");
 }
 
-// Bulk prefetch of [gsrc, gsrc + bytes) into L2 (16-byte aligned, bytes % 16 == 0); no completion.
-__device__ __forceinline__ void bulk_prefetch_l2(const void *gsrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
-}
 
 // Tensor (TMA) load of one 3-D box at coordinates (x, y, z) of the map `tmap` into shared
 // memory, completing on `bar` (x * element size must be a multiple of 16 bytes).
