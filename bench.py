@@ -52,7 +52,18 @@ FALLBACK_HBM_GBS = 6800.0
 # capture ran a reduced shape), keyed by (stage, workload id); each entry names the source
 # files of the stage's kernels and the sha256 of those files when the capture was taken, and is
 # reported as null once they change.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # the 65536-token sequence: its segmented stage runs 16 scan launches of 128 expanded chunks x
+    # 32 heads and 15 WY segments of 4096 tiles beside them.  Captured on the 12288-token cut of
+    # the same shape (profile_case w4): one middle-segment scan launch, 506061312 + 145573888 B,
+    # and one WY segment, 171823616 + 443181824 B (both launches cover exactly one full segment).
+    ("gdp_scan_kernel x16 (segmented, WY segments 2.. beside it)", 4): {
+        "sources": ["gdp_scan_body.cuh", "gdp_scan.cu", "gdp_wy_body.cuh", "gdp_wy.cu", "gdp_sm100.cuh",
+                    "gdp_internal.cuh"],
+        "sha": "bf78901b10ca42ae",
+        "bytes_per_call": 16 * (506061312 + 145573888) + 15 * (171823616 + 443181824),
+    },
+}
 
 
 def alg_bytes(w) -> int:
@@ -576,6 +587,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-others", action="store_true", help="skip the per_workload legs")
+    ap.add_argument("--no-fused", action="store_true", help="skip the fused entry point's timing")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode step's timing")
     ap.add_argument("--clocks-dir", default=None, help="folder for the raw clock samples (default: a temp folder)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -619,7 +632,7 @@ def main():
     names = stage_names(w)
     rf = roofline_of(w, statistics.fmean(step_ms), stage_ms, names, args.workload)
 
-    fused_head = time_fused(pkg, c, stream, flush) if rank == 0 else None
+    fused_head = time_fused(pkg, c, stream, flush) if (rank == 0 and not args.no_fused) else None
 
     # ---- end to end: pinned host inputs -> device -> call -> host outputs, same stream
     host_in = [t.pin_memory() for t in (w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, w.initial_state, w.state,
@@ -655,7 +668,7 @@ def main():
             if wid != args.workload:
                 others[str(wid)] = measure_other(pkg, wid, dev, stream, flush)
                 torch.cuda.empty_cache()
-    decode = measure_decode(pkg, dev, flush, stream) if rank == 0 else None
+    decode = measure_decode(pkg, dev, flush, stream) if (rank == 0 and not args.no_decode) else None
     bwd = measure_backward(pkg, dev, flush, stream, w) if (rank == 0 and not args.no_backward) else None
 
     if rank == 0:
