@@ -372,8 +372,9 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
   SideStreams *ss = (nseg > 1 && !fused) ? side_streams() : nullptr;
   if (nseg > 1 && !fused && !ss) return fail(GDP_ERR_CUDA, "could not create the internal streams of the segmented mode");
 
-  // a fused call over whole sequences runs them longest first (the descriptor kernel's order)
-  int32_t *ord = (fused && pp.len == 0 && N > 1) ? (int32_t *)(ws + lay.ord) : nullptr;
+  // a call over whole sequences in one launch runs them longest first (the descriptor kernel's
+  // order); split chains and segments keep the grid order
+  int32_t *ord = (pp.len == 0 && N > 1 && !xfer_out && (fused || nseg == 1)) ? (int32_t *)(ws + lay.ord) : nullptr;
   p.order = ord;
   cudaError_t e;
   if (nprebuilt == 3)  // only the internal expanded-stream offsets

@@ -134,13 +134,22 @@ template <bool F16, bool INIT16>
 __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &tm_cs, const CUtensorMap &tm_fin,
                                           const CUtensorMap &tm_seg, const CUtensorMap &tm_out_a,
                                           const CUtensorMap &tm_out_b) {
-  const int h = blockIdx.y;
+  int h = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // split chains: this CTA's piece (pass 1: grid row r and piece_rows + r run the same piece)
   const bool pieces = p.piece_len > 0, pass1 = pieces && p.piece_pass1, xfer = p.xfer != 0;
   // from the identity with V = 0: the second half of the rows of a pass 1 or a transfer-pair launch
   const bool transfer = (pass1 && (int)blockIdx.x >= p.piece_rows) || (xfer && (int64_t)blockIdx.x >= p.N);
   int seq = (xfer && transfer) ? (int)(blockIdx.x - p.N) : (int)blockIdx.x, pc_i = 0, pc_n = 1;
+  if (p.order && !pieces && !xfer) {
+    // longest first: linear CTA index l (the order CTAs start in) runs sequence order[l / H],
+    // head l % H, so that the longest chains do not start in the last wave; the order comes
+    // from the descriptor kernel
+    pdl_wait();
+    const int64_t l = (int64_t)blockIdx.x + (int64_t)blockIdx.y * gridDim.x;
+    seq = p.order[l / p.H];
+    h = (int)(l % p.H);
+  }
   if (pieces) {
     // the piece table comes from the descriptors; every CTA waits for its predecessor grid
     // before it may exit, so that this grid's completion implies the predecessors'
