@@ -49,32 +49,33 @@ namespace {
 using namespace sm100;
 
 constexpr int kWyThreads = 256;  // 8 warps: two per TMEM lane quadrant, splitting the columns
-constexpr int kLd = kChunk + 1;   // row stride of the fp32 A scratch (conflict-free row reads)
-constexpr int kLdT = kChunk + 4;  // row stride of T (16-byte aligned rows for float4 access)
+constexpr int kWyCtasPerSm = 3;   // shared memory (~68 KB), TMEM (128 columns) and 80 registers each
+constexpr int kLd = kChunk + 1;   // row stride of an fp32 [64][65] scratch (conflict-free row reads)
+constexpr int kLdT = kChunk + 4;  // row stride of A / T (16-byte aligned rows for float4 access)
 constexpr int kLdY = 36;          // row stride of the [32][32] block-product scratch
 
+// Shared memory of one tile, small enough for three CTAs per SM.  Lifetimes: the query rows of
+// kq die with the [K;Q]K^T epilogue and then hold the inverse's block products (Y) and, after
+// the inverse, the hi and lo tiles of one T split at a time (W's, then U's once W's MMAs have
+// read them); T is computed in place over A (A strictly lower, T unit lower: the zeros above
+// the diagonal serve both).
 struct WyLayout {
-  uint32_t kq, vt, twh, twl, tuh, tul, A, T, Y, scal, total;
+  uint32_t kq, vt, th, tl, Y, A, scal, total;
   __host__ __device__ WyLayout(int d) {
     const uint32_t nb = (uint32_t)d / 64;  // 64-element (128-byte) K blocks of a 16-bit row
     kq = 0;                                // [nb][128 rows][128 B]: rows 0..63 k, 64..127 q
     vt = kq + nb * 16384u;                 // [nb][64 rows][128 B]
-    if (d == 128) {                        // reuse the query half of kq once [K;Q]K^T is done
-      twh = kq + 8192u;
-      twl = kq + 16384u + 8192u;
-      tuh = vt + nb * 8192u;
-      tul = tuh + 8192u;
+    th = kq + 8192u;                       // the query rows of K block 0
+    Y = th;                                // fp32 [32][36] block products (during the inverse)
+    if (d == 128) {
+      tl = kq + 16384u + 8192u;            // the query rows of K block 1
+      A = vt + nb * 8192u;
     } else {
-      twh = vt + nb * 8192u;
-      twl = twh + 8192u;
-      tuh = twl + 8192u;
-      tul = tuh + 8192u;
+      tl = vt + nb * 8192u;
+      A = tl + 8192u;
     }
-    A = tul + 8192u;                       // fp32 [64][65]
-    T = A + 4u * kChunk * kLd;             // fp32 [64][68]
-    Y = T + 4u * kChunk * kLdT;            // fp32 [32][36] block products
-    scal = Y + 4u * 32 * kLdY;             // G2, beta, rk, rq, wc, uc, kscale  [7][64]
-    total = scal + 4u * 7 * kChunk;
+    scal = A + 4u * kChunk * kLdT;         // A / T: fp32 [64][68]
+    total = scal + 4u * 9 * kChunk;        // G2, beta, rk, rq, wc, uc, kscale [7][64]; [128] norms
   }
 };
 
@@ -116,6 +117,8 @@ __device__ __forceinline__ void mma3_16x8x8(float *c, const float *X, int lx, co
 // T_i,i-1 = -T_ii (A_i,i-1 T_i-1,i-1); then the 32x32 block below the diagonal,
 // T_[23][01] = -T_[23][23] (A_[23][01] T_[01][01]).  Each product is split into 16x8 units,
 // one per warp, computed with warp-level tf32 MMAs (3xTF32); Y holds the inner products.
+// A and Tm may be the same array (row stride kLdT): a block of A is read only before the
+// barrier after which its T block is written, and no later step reads it.
 __device__ __forceinline__ void inverse_offdiag(const float *A, float *Tm, float *Y, int warp, int lane) {
   const int g = lane >> 2, t = lane & 3;
   // level 1: units (pair p, 8-column half nh): rows 16 i, columns 16 j, i = 2 p + 1, j = 2 p
@@ -123,8 +126,8 @@ __device__ __forceinline__ void inverse_offdiag(const float *A, float *Tm, float
     const int pr = warp >> 1, nh = warp & 1, i = 2 * pr + 1, j = 2 * pr;
     float c[4] = {0.f, 0.f, 0.f, 0.f};
     for (int ks = 0; ks < 2; ++ks)
-      mma3_16x8x8(c, A + (16 * i) * kLd + 16 * j + 8 * ks, kLd, Tm + (16 * j + 8 * ks) * kLdT + 16 * j + 8 * nh, kLdT,
-                  lane);
+      mma3_16x8x8(c, A + (16 * i) * kLdT + 16 * j + 8 * ks, kLdT, Tm + (16 * j + 8 * ks) * kLdT + 16 * j + 8 * nh,
+                  kLdT, lane);
     float *y = Y + (pr * 16) * kLdY + 8 * nh;
     y[g * kLdY + 2 * t] = c[0];
     y[g * kLdY + 2 * t + 1] = c[1];
@@ -149,7 +152,7 @@ __device__ __forceinline__ void inverse_offdiag(const float *A, float *Tm, float
   {
     float c[4] = {0.f, 0.f, 0.f, 0.f};
     for (int ks = 0; ks < 4; ++ks)
-      mma3_16x8x8(c, A + (32 + 16 * mt) * kLd + 8 * ks, kLd, Tm + (8 * ks) * kLdT + 8 * nt, kLdT, lane);
+      mma3_16x8x8(c, A + (32 + 16 * mt) * kLdT + 8 * ks, kLdT, Tm + (8 * ks) * kLdT + 8 * nt, kLdT, lane);
     float *y = Y + (16 * mt) * kLdY + 8 * nt;
     y[g * kLdY + 2 * t] = c[0];
     y[g * kLdY + 2 * t + 1] = c[1];
@@ -260,17 +263,18 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
   const WyLayout lay(d);
   unsigned char *kq = sm + lay.kq, *vt = sm + lay.vt;
   float *A = reinterpret_cast<float *>(sm + lay.A);
-  float *Tm = reinterpret_cast<float *>(sm + lay.T);
+  float *Tm = A;  // T = (I + A)^-1 replaces A in place
   float *Y = reinterpret_cast<float *>(sm + lay.Y);
   float *G2 = reinterpret_cast<float *>(sm + lay.scal);
   float *bt = G2 + kChunk, *rk = bt + kChunk, *rq = rk + kChunk, *wc = rq + kChunk, *uc = wc + kChunk;
   float *ks = uc + kChunk;  // 2^(G2_last - G2_s) rk_s (0 past the chunk end)
+  float *l2s = ks + kChunk;  // [128] partial squared norms of the key and query rows
   __shared__ uint32_t tmem_slot;
   __shared__ __align__(8) uint64_t mma_bar, ld_bar;
   __shared__ float warp_tot;
   __shared__ int abort_flag;
 
-  if (warp == 0) tmem_alloc(&tmem_slot, 256);
+  if (warp == 0) tmem_alloc(&tmem_slot, 128);
   if (tid == 0) {
     mbar_init(&mma_bar, 1);
     mbar_init(&ld_bar, 1);
@@ -321,7 +325,8 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = tmem_slot;
-  const uint32_t tD1 = tbase, tW = tbase + 64, tU = tbase + 128;
+  // [K;Q]K^T in columns 0..63 until its epilogue; then W^T there and U^T in 64..127
+  const uint32_t tD1 = tbase, tW = tbase, tU = tbase + 64;
 
   // ---- [K; Q] K^T on the tensor cores (issued first, overlaps the scalar prologue) ----
   if (tid == 0) {
@@ -345,9 +350,9 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
 #pragma unroll
         for (int i = 0; i < 8; ++i) ss += x[i] * x[i];
       }
-      if (chalf) Y[r] = ss;  // the Y scratch is free until the inverse
+      if (chalf) l2s[r] = ss;
       __syncthreads();
-      if (!chalf) ss += Y[r];
+      if (!chalf) ss += l2s[r];
     }
     if (chalf) {
     } else if (r < kChunk) {
@@ -383,11 +388,6 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
     ks[tid] = (tid < len) ? exp2f(G2[len - 1] - G2[tid]) * rk[tid] : 0.f;
   }
 
-  // T starts at zero (its blocks above the diagonal stay so); the area is idle until the inverse
-#pragma unroll 1
-  for (int idx = tid; idx < kChunk * kLdT / 4; idx += kWyThreads)
-    reinterpret_cast<float4 *>(Tm)[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
-
   // ---- epilogue of [K;Q]K^T: A rows (lanes 0..63), score rows and query images (lanes 64..127) ----
   const bool ok1 = mbar_wait(&mma_bar, 0);
   if (!ok1) abort_flag = 1;
@@ -411,7 +411,7 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
           const int j = c0 + u;
-          A[i * kLd + j] = (j < i && rowlive) ? si * exp2f(gi - G2[j]) * rk[j] * dv[u] : 0.f;
+          A[i * kLdT + j] = (j < i && rowlive) ? si * exp2f(gi - G2[j]) * rk[j] * dv[u] : 0.f;
         }
       }
     } else {
@@ -454,9 +454,9 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
   }
   __syncthreads();
 
-  // ---- T = (I + A)^-1.  Diagonal 16x16 blocks from 8x8 halves: forward substitution on the
-  // eight 8x8 diagonal blocks (a thread per column), then T_21 = -T_22 A_21 T_11 inside each
-  // 16x16 block; every block above its block diagonal is zero ----
+  // ---- T = (I + A)^-1 in place.  Diagonal 16x16 blocks from 8x8 halves: forward substitution
+  // on the eight 8x8 diagonal blocks (a thread per column), then T_21 = -T_22 A_21 T_11 inside
+  // each 16x16 block; every block above its block diagonal is zero in A and in T ----
   if (tid < kChunk) {
     const int b0 = (tid >> 3) * 8, cc = tid & 7;
     float t[8];
@@ -464,9 +464,10 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
     for (int i = 0; i < 8; ++i) {
       float acc = 0.f;
 #pragma unroll
-      for (int j = 0; j < i; ++j) acc += A[(b0 + i) * kLd + b0 + j] * t[j];
+      for (int j = 0; j < i; ++j) acc += A[(b0 + i) * kLdT + b0 + j] * t[j];
       t[i] = (i == cc) ? 1.f : (i < cc ? 0.f : -acc);
     }
+    __syncwarp();  // the block's eight threads (one warp) have read A's block before T replaces it
 #pragma unroll
     for (int i = 0; i < 8; ++i) Tm[(b0 + i) * kLdT + b0 + cc] = t[i];
   }
@@ -476,7 +477,7 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
     const int b = tid >> 6, r = (tid >> 3) & 7, cc = tid & 7, r0 = 16 * b + 8, c0 = 16 * b;
     float acc = 0.f;  // (A_21 T_11)[r][cc]
 #pragma unroll
-    for (int x = 0; x < 8; ++x) acc += A[(r0 + r) * kLd + c0 + x] * Tm[(c0 + x) * kLdT + c0 + cc];
+    for (int x = 0; x < 8; ++x) acc += A[(r0 + r) * kLdT + c0 + x] * Tm[(c0 + x) * kLdT + c0 + cc];
     Y[tid] = acc;
     __syncthreads();
     float o = 0.f;  // (T_22 Y)[r][cc], T_22 lower triangular
@@ -517,48 +518,51 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
     sw = f16_split_scale(mw, &isw);
     su = f16_split_scale(mu, &isu);
   }
-  for (int it = tid; it < kChunk * 8; it += kWyThreads) {  // (row s, 8 consecutive j)
-    const int srow = it >> 3, j0 = (it & 7) * 8;
-    const float4 t0 = *reinterpret_cast<const float4 *>(Tm + srow * kLdT + j0);
-    const float4 t1 = *reinterpret_cast<const float4 *>(Tm + srow * kLdT + j0 + 4);
-    const float t[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
-    typename In::T2 wh[4], wl[4], uh[4], ul[4];
+  // T diag(c) sc as hi + lo of the input type into the split tiles (row s, 8 consecutive j
+  // per item)
+  unsigned char *th = sm + lay.th, *tl = sm + lay.tl;
+  auto split = [&](const float *cv, float sc) {
+    for (int it = tid; it < kChunk * 8; it += kWyThreads) {
+      const int srow = it >> 3, j0 = (it & 7) * 8;
+      const float4 t0 = *reinterpret_cast<const float4 *>(Tm + srow * kLdT + j0);
+      const float4 t1 = *reinterpret_cast<const float4 *>(Tm + srow * kLdT + j0 + 4);
+      const float t[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+      typename In::T2 hi[4], lo[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float w0 = t[2 * i] * wc[j0 + 2 * i] * sw, w1 = t[2 * i + 1] * wc[j0 + 2 * i + 1] * sw;
-      const float u0 = t[2 * i] * uc[j0 + 2 * i] * su, u1 = t[2 * i + 1] * uc[j0 + 2 * i + 1] * su;
-      wh[i] = In::from_f2(w0, w1);
-      uh[i] = In::from_f2(u0, u1);
-      const float2 fw = In::to_f2(wh[i]), fu = In::to_f2(uh[i]);
-      wl[i] = In::from_f2(w0 - fw.x, w1 - fw.y);
-      ul[i] = In::from_f2(u0 - fu.x, u1 - fu.y);
+      for (int i = 0; i < 4; ++i) {
+        const float a0 = t[2 * i] * cv[j0 + 2 * i] * sc, a1 = t[2 * i + 1] * cv[j0 + 2 * i + 1] * sc;
+        hi[i] = In::from_f2(a0, a1);
+        const float2 f = In::to_f2(hi[i]);
+        lo[i] = In::from_f2(a0 - f.x, a1 - f.y);
+      }
+      const uint32_t off = swz(srow, j0 * 2u);
+      *reinterpret_cast<uint4 *>(th + off) = *reinterpret_cast<const uint4 *>(hi);
+      *reinterpret_cast<uint4 *>(tl + off) = *reinterpret_cast<const uint4 *>(lo);
     }
-    const uint32_t off = swz(srow, j0 * 2u);
-    *reinterpret_cast<uint4 *>(sm + lay.twh + off) = *reinterpret_cast<const uint4 *>(wh);
-    *reinterpret_cast<uint4 *>(sm + lay.twl + off) = *reinterpret_cast<const uint4 *>(wl);
-    *reinterpret_cast<uint4 *>(sm + lay.tuh + off) = *reinterpret_cast<const uint4 *>(uh);
-    *reinterpret_cast<uint4 *>(sm + lay.tul + off) = *reinterpret_cast<const uint4 *>(ul);
-  }
-  fence_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-
-  // ---- W^T = K^T Tw^T and U^T = V^T Tu^T (A operands MN-major from the k / v tiles) ----
-  if (tid == 0) {
-    const uint32_t id = idesc(In::kFmt, 1, 0, 64, d);
-    for (int kk = 0; kk < 4; ++kk) {
-      const uint32_t ak = smem_u32(kq) + kk * 2048u, av = smem_u32(vt) + kk * 2048u;
-      const uint64_t dak = desc_sw128(ak, 16384, 1024), dav = desc_sw128(av, 8192, 1024);
-      mma_bf16_ss(tW, dak, desc_sw128(smem_u32(sm + lay.twh) + kk * 32u, 16, 1024), id, kk > 0);
-      mma_bf16_ss(tW, dak, desc_sw128(smem_u32(sm + lay.twl) + kk * 32u, 16, 1024), id, 1);
-      mma_bf16_ss(tU, dav, desc_sw128(smem_u32(sm + lay.tuh) + kk * 32u, 16, 1024), id, kk > 0);
-      mma_bf16_ss(tU, dav, desc_sw128(smem_u32(sm + lay.tul) + kk * 32u, 16, 1024), id, 1);
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  };
+  // ---- W^T = K^T Tw^T, then U^T = V^T Tu^T through the same split tiles (A operands MN-major
+  // from the k / v tiles); each split waits for the MMAs that read the tiles before it ----
+  const uint32_t idwu = idesc(In::kFmt, 1, 0, 64, d);
+  auto issue_wu = [&](uint32_t tD, const unsigned char *src, uint32_t lbo) {
+    if (tid == 0) {
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t da = desc_sw128(smem_u32(src) + kk * 2048u, lbo, 1024);
+        mma_bf16_ss(tD, da, desc_sw128(smem_u32(th) + kk * 32u, 16, 1024), idwu, kk > 0);
+        mma_bf16_ss(tD, da, desc_sw128(smem_u32(tl) + kk * 32u, 16, 1024), idwu, 1);
+      }
+      mma_commit(&mma_bar);
     }
-    mma_commit(&mma_bar);
-  }
-  const bool ok2 = mbar_wait(&mma_bar, 1);
-  if (!ok2) abort_flag = 1;
+  };
+  split(wc, sw);
+  issue_wu(tW, kq, 16384u);
+  if (!mbar_wait(&mma_bar, 1)) abort_flag = 1;
+  split(uc, su);
+  issue_wu(tU, vt, 8192u);
+  if (!mbar_wait(&mma_bar, 0)) abort_flag = 1;
   tc_fence_after();
   __syncthreads();
 
@@ -627,14 +631,17 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_free(tbase, 256);
+  if (warp == 0) tmem_free(tbase, 128);
 }
 
 // Shared by the WY kernels of every type combination (one translation unit for the common
 // kernel, one for the rest): tensor maps of k, q, v and the grid (expanded chunk, head).
 template <typename Kern>
 cudaError_t launch_wy_kernel(Kern kern, const Problem &p, cudaStream_t stream) {
-  const size_t smem = WyLayout(p.K).total + 1024;
+  // Beside the scan (a segmented call) the tiles run two per SM, asked for by the shared memory
+  // size: with three, the scan beside them ran 2.5 % slower on the 65536-token sequence than the
+  // WY tiles gained (A/B on one GB300)
+  const size_t smem = p.seg_rows > 0 ? (size_t)100 * 1024 : WyLayout(p.K).total + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   alignas(64) CUtensorMap tm_k, tm_q, tm_v;
@@ -649,7 +656,7 @@ cudaError_t launch_wy_kernel(Kern kern, const Problem &p, cudaStream_t stream) {
 }
 
 #define GDP_WY_KERNEL(name, f16, typed)                                                                          \
-  __global__ void __launch_bounds__(kWyThreads, 2)                                                              \
+  __global__ void __launch_bounds__(kWyThreads, kWyCtasPerSm)                                                   \
       name(Problem p, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,        \
            const __grid_constant__ CUtensorMap tm_v) {                                                            \
     wy_body<f16, typed>(p, tm_k, tm_q, tm_v);                                                                   \
