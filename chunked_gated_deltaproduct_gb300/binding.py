@@ -20,9 +20,13 @@ import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libgdp_gb300.so")
+DEBUG_LIB_PATH = os.path.join(_PKG, "libgdp_gb300_debug.so")  # the debug-bounds build
 
 GDP_OK, GDP_ERR_INVALID_ARG, GDP_ERR_UNSUPPORTED, GDP_ERR_ALIAS, GDP_ERR_WORKSPACE, GDP_ERR_CUDA = range(6)
 GDP_DEV_ERR_CU_SEQLENS, GDP_DEV_ERR_SLOT, GDP_DEV_ERR_DESC, GDP_DEV_ERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+GDP_DEV_ERR_BOUNDS = 0x10
+BOUNDS_SITES = {1: "desc", 2: "wy_tile", 3: "wy_scalars", 4: "scan_order", 5: "scan_tile", 6: "scan_state",
+                7: "scan_out", 8: "decode"}
 GDP_DTYPE_DEFAULT, GDP_DTYPE_F32, GDP_DTYPE_BF16, GDP_DTYPE_F16 = range(4)
 GDP_ABI_VERSION = 2
 _DTYPE_CODE = {torch.float32: GDP_DTYPE_F32, torch.bfloat16: GDP_DTYPE_BF16, torch.float16: GDP_DTYPE_F16}
@@ -93,6 +97,10 @@ def load_library(path: str | None = None):
     lib.gdp_static_scratch_bytes.restype = _sz
     lib.gdp_arm_wait_expiry_test.restype = _int
     lib.gdp_arm_wait_expiry_test.argtypes = [ctypes.c_uint64]
+    lib.gdp_debug_bounds_record.restype = _int
+    lib.gdp_debug_bounds_record.argtypes = [ctypes.POINTER(_i64)]
+    lib.gdp_arm_bounds_test.restype = _int
+    lib.gdp_arm_bounds_test.argtypes = []
     lib.gdp_static_scratch_bytes.argtypes = []
     lib.gdp_prefill_varlen_backward.restype = _int
     lib.gdp_prefill_varlen_backward.argtypes = [ctypes.POINTER(GdpBackwardArgs), _vp]
@@ -223,6 +231,27 @@ def gdp_arm_wait_expiry_test(limit_ns: int) -> None:
     (its scan waits give up after limit_ns; one of them runs out); see the header."""
     lib = load_library()
     st = lib.gdp_arm_wait_expiry_test(int(limit_ns))
+    if st != GDP_OK:
+        raise GdpError(st, lib.gdp_last_error().decode())
+
+
+def gdp_debug_bounds_record() -> dict:
+    """Debug-bounds builds: the range-check violations recorded since the last read (count, the
+    first one's site, index and bound), then cleared; GdpError (UNSUPPORTED) in other builds."""
+    lib = load_library()
+    out = (_i64 * 4)()
+    st = lib.gdp_debug_bounds_record(out)
+    if st != GDP_OK:
+        raise GdpError(st, lib.gdp_last_error().decode())
+    return {"count": int(out[0]), "site": BOUNDS_SITES.get(int(out[1]), int(out[1])), "index": int(out[2]),
+            "bound": int(out[3])}
+
+
+def gdp_arm_bounds_test() -> None:
+    """Debug-bounds builds: the calling thread's next prefill checks its output rows against T - 1
+    (the last token's output stores fail their check and are skipped); see the header."""
+    lib = load_library()
+    st = lib.gdp_arm_bounds_test()
     if st != GDP_OK:
         raise GdpError(st, lib.gdp_last_error().decode())
 

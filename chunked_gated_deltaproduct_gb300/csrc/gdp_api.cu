@@ -17,6 +17,8 @@ namespace {
 thread_local char g_last_error[512] = "";
 // gdp_arm_wait_expiry_test: the wait limit (ns) of the calling thread's next prefill, 0 = not armed
 thread_local uint64_t g_expiry_test_ns = 0;
+// gdp_arm_bounds_test: the calling thread's next prefill checks its output rows against T - 1
+thread_local bool g_bounds_test = false;
 
 gdp_status fail(gdp_status st, const char *fmt, ...) {
   va_list ap;
@@ -160,6 +162,21 @@ gdp_status record(cudaEvent_t ev, cudaStream_t stream) {
 }
 
 }  // namespace
+
+#if GDP_DEBUG_BOUNDS
+// The debug-bounds record of the kernels' range checks (count, first site, index, bound); the
+// runtime keeps one copy per CUDA context
+__device__ unsigned long long g_bounds_rec[4];
+#endif
+// The record's device address in the current context (NULL in other builds or on failure)
+unsigned long long *gdp::bounds_record() {
+#if GDP_DEBUG_BOUNDS
+  void *ptr = nullptr;
+  return cudaGetSymbolAddress(&ptr, g_bounds_rec) == cudaSuccess ? static_cast<unsigned long long *>(ptr) : nullptr;
+#else
+  return nullptr;
+#endif
+}
 
 // The input-variant tail of gdp_prefill_args (FlashInfer page, parameters q, k, v, g,
 // beta, initial_state): checks it and fills the matching Problem fields.
@@ -355,6 +372,9 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
     p.test_withhold_copy = 1;
     g_expiry_test_ns = 0;
   }
+  p.bounds = gdp::bounds_record();
+  p.bounds_shrink = g_bounds_test ? 1 : 0;  // armed by gdp_arm_bounds_test: this call only
+  g_bounds_test = false;
   if (xfer_out) {  // B (rows 0 .. N-1) and Phi (rows N .. 2N-1) of every sequence, no outputs
     p.xfer = 1;
     p.xfer_out = xfer_out;
@@ -379,10 +399,10 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
   cudaError_t e;
   if (nprebuilt == 3)  // only the internal expanded-stream offsets
     e = gdp::launch_descriptors(p.cu, p.cu64, T, N, M, nullptr, 0, nullptr, 0, nullptr, (int32_t *)p.cod, p.status,
-                                stream, ord);
+                                stream, ord, p.bounds);
   else
     e = gdp::launch_descriptors(p.cu, p.cu64, T, N, M, (int32_t *)p.ci, nt_pad, (int32_t *)p.cid, ntdp_pad,
-                                co_desc, (int32_t *)p.cod, p.status, stream, ord);
+                                co_desc, (int32_t *)p.cod, p.status, stream, ord, p.bounds);
   if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "descriptor kernel: %s", cudaGetErrorString(e));
   if (ev && (st = record(ev[1], stream)) != GDP_OK) return st;
   if (fused) {  // no WY stage of its own: events 1 and 2 mark the same point
@@ -502,6 +522,34 @@ GDP_EXPORT int gdp_prefill_fused(int64_t T, int64_t N, int H, int K, int V, int 
 }
 
 GDP_EXPORT const char *gdp_last_error(void) { return g_last_error; }
+
+GDP_EXPORT gdp_status gdp_debug_bounds_record(int64_t out[4]) {
+  g_last_error[0] = 0;
+#if GDP_DEBUG_BOUNDS
+  if (!out) return fail(GDP_ERR_INVALID_ARG, "out is NULL");
+  unsigned long long rec[4] = {0, 0, 0, 0};
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(rec, g_bounds_rec, sizeof rec);
+  const unsigned long long zero[4] = {0, 0, 0, 0};
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_bounds_rec, zero, sizeof zero);
+  if (e != cudaSuccess) return fail(GDP_ERR_CUDA, "debug-bounds record: %s", cudaGetErrorString(e));
+  for (int i = 0; i < 4; ++i) out[i] = (int64_t)rec[i];
+  return GDP_OK;
+#else
+  (void)out;
+  return fail(GDP_ERR_UNSUPPORTED, "not a debug-bounds build (GDP_DEBUG_BOUNDS)");
+#endif
+}
+
+GDP_EXPORT gdp_status gdp_arm_bounds_test(void) {
+  g_last_error[0] = 0;
+#if GDP_DEBUG_BOUNDS
+  g_bounds_test = true;
+  return GDP_OK;
+#else
+  return fail(GDP_ERR_UNSUPPORTED, "not a debug-bounds build (GDP_DEBUG_BOUNDS)");
+#endif
+}
 
 GDP_EXPORT gdp_status gdp_arm_wait_expiry_test(uint64_t limit_ns) {
   g_last_error[0] = 0;

@@ -44,6 +44,7 @@ struct DecodeProblem {
   void *out;              // the q / k / v type
   float *out_state;
   uint32_t *status;
+  unsigned long long *bounds;  // debug-bounds record (see in_range)
 };
 
 __device__ __forceinline__ float load16(const void *base, int64_t i, int f16) {
@@ -70,12 +71,14 @@ __global__ void __launch_bounds__(kDecThreads) gdp_decode_kernel(DecodeProblem p
   const float *src = nullptr;
   const __nv_bfloat16 *src16 = nullptr;  // a bf16 initial state
   float *dst = nullptr;
+  if (!in_range(p.bounds, p.status, GDP_BOUNDS_SITE_DECODE, i, p.N)) return;
   if (p.cache) {
     slot = p.slots[i];
     if (slot < -1 || slot >= p.num_slots) {
       if (tid == 0 && blockIdx.y == 0 && blockIdx.z == 0) set_status(p.status, GDP_DEV_ERR_SLOT);
       slot = -1;
     }
+    if (slot >= 0 && !in_range(p.bounds, p.status, GDP_BOUNDS_SITE_DECODE, slot, p.num_slots)) slot = -1;
     if (slot >= 0) src = dst = p.cache + ((int64_t)slot * p.H + h) * (int64_t)p.V * D;
   } else {
     if (p.init && p.init_bf16)
@@ -230,6 +233,7 @@ GDP_EXPORT gdp_status gdp_decode_step(const gdp_prefill_args *a, void *stream) {
   p.l2norm = a->use_qk_l2norm ? 1 : 0;
   p.init = a->initial_state; p.cache = a->state; p.slots = a->state_indices; p.num_slots = a->num_slots;
   p.out = a->output; p.out_state = a->output_state; p.status = a->device_status;
+  p.bounds = gdp::bounds_record();
   dim3 grid((unsigned)N, (unsigned)H, (unsigned)(V / gdp::kDecRows));
   cudaStream_t s = (cudaStream_t)stream;
   if (K == 128)

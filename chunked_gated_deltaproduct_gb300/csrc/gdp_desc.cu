@@ -73,7 +73,8 @@ constexpr int64_t kOrderMaxSeqs = kDescThreads;
 __global__ void __launch_bounds__(kDescThreads) gdp_desc_kernel(const void *cu, int cu64, int64_t T, int64_t N,
                                                                 int M, int32_t *ci, int64_t nt_pad, int32_t *cid,
                                                                 int64_t ntdp_pad, int32_t *co, int32_t *cod,
-                                                                int32_t *order, uint32_t *status) {
+                                                                int32_t *order, uint32_t *status,
+                                                                unsigned long long *bounds) {
   __shared__ int warp_sums[32];
   __shared__ int tot_a, tot_b;
   __shared__ int carry_a, carry_b;
@@ -136,7 +137,7 @@ __global__ void __launch_bounds__(kDescThreads) gdp_desc_kernel(const void *cu, 
           const int nj = s_cod[j + 1] - s_cod[j];
           rank += (nj > ni) || (nj == ni && j < i);
         }
-        order[rank] = (int32_t)i;
+        if (in_range(bounds, status, GDP_BOUNDS_SITE_DESC, rank, N)) order[rank] = (int32_t)i;
       }
     } else {
       for (int64_t i = threadIdx.x; i < N; i += blockDim.x) order[i] = (int32_t)i;
@@ -148,9 +149,9 @@ __global__ void __launch_bounds__(kDescThreads) gdp_desc_kernel(const void *cu, 
 
 cudaError_t launch_descriptors(const void *cu, int cu64, int64_t T, int64_t N, int M, int32_t *ci, int64_t nt_pad,
                                int32_t *cid, int64_t ntdp_pad, int32_t *co, int32_t *cod, uint32_t *status,
-                               cudaStream_t stream, int32_t *order) {
+                               cudaStream_t stream, int32_t *order, unsigned long long *bounds) {
   gdp_desc_kernel<<<1, kDescThreads, 0, stream>>>(cu, cu64, T, N, M, ci, nt_pad, cid, ntdp_pad, co, cod, order,
-                                                  status);
+                                                  status, bounds);
   return cudaGetLastError();
 }
 

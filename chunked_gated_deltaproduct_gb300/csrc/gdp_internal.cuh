@@ -160,6 +160,10 @@ struct Problem {
   // The fused kernel's CTA order (NULL: sequence by sequence): linear CTA index l runs sequence
   // order[l / H], head l % H, so the longest sequences start first (the descriptor kernel's order)
   const int32_t *order;
+  // Debug-bounds builds: the library's violation record (see in_range) and the output-row bound
+  // reduction of the bounds test (gdp_arm_bounds_test; 0 otherwise)
+  unsigned long long *bounds;
+  int64_t bounds_shrink;
 };
 
 // Everything the backward kernels need about one call (gdp_backward.cu).  Heads are
@@ -295,12 +299,36 @@ __device__ __forceinline__ void set_status(uint32_t *status, uint32_t bits) {
   if (status) atomicOr(status, bits);
 }
 
+// Range check of a global index before its access (debug-bounds builds, -DGDP_DEBUG_BOUNDS=1):
+// false when idx is outside [0, bound), after counting the violation in rec[0], recording the
+// first one's site, index and bound in rec[1..3] and setting GDP_DEV_ERR_BOUNDS; the caller then
+// skips the access.  Other builds: always true, no code.
+#ifndef GDP_DEBUG_BOUNDS
+#define GDP_DEBUG_BOUNDS 0
+#endif
+__device__ __forceinline__ bool in_range([[maybe_unused]] unsigned long long *rec, [[maybe_unused]] uint32_t *status,
+                                         [[maybe_unused]] int site, [[maybe_unused]] int64_t idx,
+                                         [[maybe_unused]] int64_t bound) {
+#if GDP_DEBUG_BOUNDS
+  if (idx >= 0 && idx < bound) return true;
+  if (rec && atomicAdd(&rec[0], 1ull) == 0ull) {
+    rec[1] = (unsigned long long)site;
+    rec[2] = (unsigned long long)idx;
+    rec[3] = (unsigned long long)bound;
+  }
+  set_status(status, GDP_DEV_ERR_BOUNDS);
+  return false;
+#else
+  return true;
+#endif
+}
+
 // Kernel launchers (defined in their .cu files).  Each returns a CUDA error.
 // order (optional, [N]): the sequences longest first (by expanded chunks; ties in their own
 // order) for batches of up to 1024 sequences, the identity beyond.
 cudaError_t launch_descriptors(const void *cu, int cu64, int64_t T, int64_t N, int M, int32_t *ci, int64_t nt_pad,
                                int32_t *cid, int64_t ntdp_pad, int32_t *co, int32_t *cod, uint32_t *status,
-                               cudaStream_t stream, int32_t *order = nullptr);
+                               cudaStream_t stream, int32_t *order = nullptr, unsigned long long *bounds = nullptr);
 cudaError_t launch_wy(const Problem &p, cudaStream_t stream);
 // The WY kernel for float16 inputs (f16) and / or 16-bit or linear-space gates (typed).
 cudaError_t launch_wy_variant(const Problem &p, cudaStream_t stream, bool f16, bool typed);
@@ -336,5 +364,7 @@ cudaError_t tmap_out_rows(void *map, void *base, int64_t T, int H, int V, int bo
 void set_last_error(const char *fmt, ...);
 // Checks the input-variant fields of the arguments and fills p's Hq/Hk/Hv and type fields.
 gdp_status resolve_variants(const gdp_prefill_args *a, Problem *p);
+// The debug-bounds record of the current CUDA context (gdp_api.cu; NULL outside debug-bounds builds).
+unsigned long long *bounds_record();
 
 }  // namespace gdp

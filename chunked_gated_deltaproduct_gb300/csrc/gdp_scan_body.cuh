@@ -147,8 +147,10 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
     // from the descriptor kernel
     pdl_wait();
     const int64_t l = (int64_t)blockIdx.x + (int64_t)blockIdx.y * gridDim.x;
+    if (!in_range(p.bounds, p.status, GDP_BOUNDS_SITE_SCAN_ORDER, l / p.H, p.N)) return;
     seq = p.order[l / p.H];
     h = (int)(l % p.H);
+    if (!in_range(p.bounds, p.status, GDP_BOUNDS_SITE_SCAN_ORDER, seq, p.N)) return;
   }
   if (pieces) {
     // the piece table comes from the descriptors; every CTA waits for its predecessor grid
@@ -198,6 +200,7 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
   int slot = -1;
   const float *src = nullptr;
   [[maybe_unused]] const __nv_bfloat16 *src16 = nullptr;  // a bf16 dense initial state (INIT16)
+  if (!in_range(p.bounds, p.status, GDP_BOUNDS_SITE_SCAN_STATE, seq, p.N)) return;
   if (p.cache) {
     slot = p.slots[seq];
     if (slot < -1 || slot >= p.num_slots) {
@@ -289,16 +292,25 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
   auto image = [&](int64_t e) { return p.img + (size_t)((cod_i + e0 + e) * H + h) * p.img_stride; };
   // producer thread: part 1 / part 2 of chunk e's image into stage e % nst (n1, n2: copies issued)
   int n1[2] = {0, 0}, n2[2] = {0, 0};
+  // (a workspace row that fails its debug range check is not copied: the stage completes empty)
   auto load_part1 = [&](int64_t e) {
     const int st = (int)(e % nst);
-    mbar_arrive_expect_tx(&full1[st], il.part1);
-    bulk_g2s(sm + st * sbytes, image(e), il.part1, &full1[st]);
+    if (in_range(p.bounds, p.status, GDP_BOUNDS_SITE_SCAN_TILE, cod_i + e0 + e, p.ws_rows)) {
+      mbar_arrive_expect_tx(&full1[st], il.part1);
+      bulk_g2s(sm + st * sbytes, image(e), il.part1, &full1[st]);
+    } else {
+      mbar_arrive(&full1[st]);
+    }
     ++n1[st];
   };
   auto load_part2 = [&](int64_t e) {
     const int st = (int)(e % nst);
-    mbar_arrive_expect_tx(&full2[st], il.part2);
-    bulk_g2s(sm + st * sbytes + il.b2, image(e) + il.b2, il.part2, &full2[st]);
+    if (in_range(p.bounds, p.status, GDP_BOUNDS_SITE_SCAN_TILE, cod_i + e0 + e, p.ws_rows)) {
+      mbar_arrive_expect_tx(&full2[st], il.part2);
+      bulk_g2s(sm + st * sbytes + il.b2, image(e) + il.b2, il.part2, &full2[st]);
+    } else {
+      mbar_arrive(&full2[st]);
+    }
     ++n2[st];
   };
 
@@ -354,9 +366,11 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
     auto load_u = [&](int64_t e) {  // row v of U^T: one 512-byte segment per load instruction of the warp
       const float4 *Ut = reinterpret_cast<const float4 *>(p.U + ((cod_i + e0 + e) * H + h) * (int64_t)V * kChunk) +
                          (v < V ? q4 * 512 + lane : 0);
+      const bool urow = v < V && !transfer &&
+                        in_range(p.bounds, p.status, GDP_BOUNDS_SITE_SCAN_TILE, cod_i + e0 + e, p.ws_rows);
 #pragma unroll
       for (int s4 = 0; s4 < 16; ++s4) {
-        const float4 x = (v < V && !transfer) ? Ut[s4 * 32] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 x = urow ? Ut[s4 * 32] : make_float4(0.f, 0.f, 0.f, 0.f);
         u[4 * s4] = x.x; u[4 * s4 + 1] = x.y; u[4 * s4 + 2] = x.z; u[4 * s4 + 3] = x.w;
       }
     };
@@ -488,7 +502,7 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
       const int64_t tq0 = (bos * M + (e0 + e) * kChunk + ci.p0) / M;  // readout rows are consecutive tokens
       if (p.out && p.out_tma && (ci.nq == kChunk / M || ci.nq == (kChunk + M - 1) / M)) {
         // one box of exactly nq token rows (x = 0, head h, token tq0)
-        if (tid == 128) {
+        if (tid == 128 && in_range(p.bounds, p.status, GDP_BOUNDS_SITE_SCAN_OUT, tq0 + ci.nq - 1, p.T - p.bounds_shrink)) {
           tma_store_3d(ci.nq == kChunk / M ? &tm_out_a : &tm_out_b, obuf, 0, h, (int)tq0);
           bulk_commit();
         }
@@ -496,8 +510,9 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
         const int cpr = V / 8;  // 16-byte chunks per output row
         for (int c = tid - 128; p.out && c < ci.nq * cpr; c += 128) {
           const int qi = c / cpr, ch = c % cpr;
-          *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + ((tq0 + qi) * H + h) * (int64_t)V + ch * 8) =
-              *reinterpret_cast<const uint4 *>(obuf + ((uint32_t)qi * V + ch * 8) * 2u);
+          if (in_range(p.bounds, p.status, GDP_BOUNDS_SITE_SCAN_OUT, tq0 + qi, p.T - p.bounds_shrink))
+            *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + ((tq0 + qi) * H + h) * (int64_t)V + ch * 8) =
+                *reinterpret_cast<const uint4 *>(obuf + ((uint32_t)qi * V + ch * 8) * 2u);
         }
       }
       if (emits(e)) {  // the prep warps copied S_e before batch 2 of this chunk was issued

@@ -240,6 +240,7 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
     row = p.cod[seq] + c;
   } else {
     row = blockIdx.x;
+    if (!in_range(p.bounds, p.status, GDP_BOUNDS_SITE_WY_TILE, 2 * (int64_t)row + 1, 2 * p.ntdp_pad)) return;
     seq = p.cid[2 * row];
     c = p.cid[2 * row + 1];
   }
@@ -298,7 +299,9 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
   // per-row beta and decay gate (the decay of token t sits on its first expanded row t*M),
   // fetched while the tiles land
   float b_r = 0.f, gate_r = 0.f;
-  if (tid < kChunk && tid < len) {
+  if (tid < kChunk && tid < len &&
+      in_range(p.bounds, p.status, GDP_BOUNDS_SITE_WY_SCALARS, (R0 + tid) * p.H + h, p.T * M * p.H) &&
+      in_range(p.bounds, p.status, GDP_BOUNDS_SITE_WY_SCALARS, (tok0 + (r0m + tid) / M) * p.H + h, p.T * p.H)) {
     const int pos = r0m + tid;
     if constexpr (TYPED) {
       b_r = p.beta ? load_typed(p.beta, (R0 + tid) * p.H + h, p.beta_type) : 1.f;

@@ -71,6 +71,8 @@ typedef enum gdp_dtype {
 #define GDP_DEV_ERR_DESC 0x4u       /* chunk counts exceed the padded descriptor lengths: tail skipped */
 #define GDP_DEV_ERR_TIMEOUT 0x8u    /* a kernel gave up a bounded wait on its own tensor-core or copy
                                        completion (about a second); its outputs are undefined */
+#define GDP_DEV_ERR_BOUNDS 0x10u    /* (GDP_DEBUG_BOUNDS builds only) a global index failed its range
+                                       check; the access was skipped: see gdp_debug_bounds_record */
 
 /*
  * Arguments of one prefill call.  Shapes use T real tokens, N sequences,
@@ -319,6 +321,38 @@ gdp_status gdp_chain_states(const float *s0, const float *phi, const float *b, i
  * outside the range.
  */
 gdp_status gdp_arm_wait_expiry_test(uint64_t limit_ns);
+
+/*
+ * Debug-bounds builds (libgdp_gb300_debug.so, compiled with -DGDP_DEBUG_BOUNDS=1;
+ * no counterpart on the pages).  Every global index that the kernels derive
+ * from the descriptors, the sequence table or the state-cache indices is
+ * range-checked before its access: a failing check skips the access, ORs
+ * GDP_DEV_ERR_BOUNDS into *device_status and records the first violation in a
+ * device record of the library (one per CUDA context).  Nothing traps.  The
+ * other builds carry no checks and return GDP_ERR_UNSUPPORTED from these calls.
+ *
+ * gdp_debug_bounds_record: after the calls of interest have completed, copies
+ * the record into out[4] = {violations since the last read, site of the first
+ * (a GDP_BOUNDS_SITE_* value), its index, its bound} and clears it.
+ * Synchronous (waits for the device).
+ */
+#define GDP_BOUNDS_SITE_DESC 1        /* descriptor kernel: descriptor rows, offsets, order */
+#define GDP_BOUNDS_SITE_WY_TILE 2     /* WY kernel: its tile's descriptor entry and workspace row */
+#define GDP_BOUNDS_SITE_WY_SCALARS 3  /* WY kernel: the beta / g entries of its rows */
+#define GDP_BOUNDS_SITE_SCAN_ORDER 4  /* scan kernel: the longest-first order entry */
+#define GDP_BOUNDS_SITE_SCAN_TILE 5   /* scan kernel: workspace row of an image / U^T copy */
+#define GDP_BOUNDS_SITE_SCAN_STATE 6  /* scan kernel: entering, chunk-state and final-state rows */
+#define GDP_BOUNDS_SITE_SCAN_OUT 7    /* scan kernel: output token rows */
+#define GDP_BOUNDS_SITE_DECODE 8      /* decode kernel: sequence row and cache slot */
+gdp_status gdp_debug_bounds_record(int64_t out[4]);
+/*
+ * gdp_arm_bounds_test: a test of the debug-bounds path.  Arms the calling host
+ * thread's NEXT gdp_prefill_varlen* call to check its output token rows against
+ * T - 1 instead of T, so that the (valid) stores of the last token's output fail
+ * their check: they are skipped and recorded (GDP_BOUNDS_SITE_SCAN_OUT), nothing
+ * outside the caller's buffers is touched.  Debug-bounds builds only.
+ */
+gdp_status gdp_arm_bounds_test(void);
 
 /*
  * gdp_prefill_varlen_static_scratch: the same prefill for callers that cannot

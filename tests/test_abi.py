@@ -41,6 +41,22 @@ def test_exports_every_declared_symbol(lib):
     assert lib.gdp_abi_version() == pkg.GDP_ABI_VERSION == 2
 
 
+def test_debug_bounds_build_exports_and_normal_build_declines(lib):
+    """The debug-bounds variant builds and exports the same symbols; in the normal build its two
+    entry points return GDP_ERR_UNSUPPORTED without touching the device."""
+    from chunked_gated_deltaproduct_gb300 import binding, build as libbuild
+
+    path = libbuild.build(debug_bounds=True)
+    dbg = ctypes.CDLL(path)
+    for name in _declared_functions():
+        assert hasattr(dbg, name), f"{name} missing from the debug-bounds build"
+    for fn in (pkg.gdp_debug_bounds_record, pkg.gdp_arm_bounds_test):
+        with pytest.raises(pkg.GdpError) as e:
+            fn()
+        assert e.value.status == pkg.GDP_ERR_UNSUPPORTED
+    assert binding.DEBUG_LIB_PATH == path
+
+
 def test_args_struct_layout(lib):
     assert lib.gdp_prefill_args_size() == ctypes.sizeof(pkg.GdpPrefillArgs)
 
