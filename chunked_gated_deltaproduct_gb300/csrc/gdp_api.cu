@@ -226,6 +226,8 @@ namespace {
 struct Recompute {
   float *states;
   float *final_state;
+  unsigned char *bimg;  // the WY tiles' operands in the reverse scan's layout (BwdImageLayout)
+  size_t bimg_stride;
 };
 
 // Checks + launches shared by gdp_prefill_varlen, its profiled form, the backward pass and the
@@ -344,6 +346,8 @@ gdp_status prefill(const gdp_prefill_args *a, cudaStream_t stream, cudaEvent_t c
     p.co = p.cod;
     p.nt_pad = ntdp_pad;
     p.cs_div = 1;
+    p.bimg = rc->bimg;
+    p.bimg_stride = rc->bimg_stride;
   }
   p.seg_lo = 0;
   p.seg_hi = INT64_MAX;
@@ -639,7 +643,7 @@ namespace {
 
 // Backward workspace: the forward's layout (recompute) followed by the backward's buffers.
 struct BwdLayout {
-  size_t Sx, Dx, fin, tot, sig, rho, total;
+  size_t Sx, Dx, fin, tot, sig, rho, bimg, bimg_stride, total;
 };
 
 BwdLayout bwd_layout_for(int64_t T, int64_t N, int H, int K, int V, int M) {
@@ -658,6 +662,8 @@ BwdLayout bwd_layout_for(int64_t T, int64_t N, int H, int K, int V, int M) {
   l.tot = take((size_t)N * H * sizeof(float));
   l.sig = take((size_t)T * M * H * sizeof(float));
   l.rho = take((size_t)T * H * sizeof(float));
+  l.bimg_stride = gdp::bwd_image_stride(K, gdp::qpad_for(M));
+  l.bimg = take((size_t)ntdp * H * l.bimg_stride);
   l.total = off;
   return l;
 }
@@ -709,7 +715,8 @@ gdp_status backward(const gdp_backward_args *b, cudaStream_t stream) {
   f.workspace = ws;
   f.workspace_bytes = layout_for(T, N, H, K, V, M).total;
   f.device_status = b->device_status;
-  Recompute rc{(float *)(ws + bl.Sx), b->d_final_state ? (float *)(ws + bl.fin) : nullptr};
+  Recompute rc{(float *)(ws + bl.Sx), b->d_final_state ? (float *)(ws + bl.fin) : nullptr,
+               (unsigned char *)(ws + bl.bimg), bl.bimg_stride};
   gdp_status st = prefill(&f, stream, nullptr, &rc);
   if (st != GDP_OK) return st;
   if (N == 0) return GDP_OK;
@@ -738,6 +745,8 @@ gdp_status backward(const gdp_backward_args *b, cudaStream_t stream) {
   p.ws_rows = ntdpb;
   p.img = (const unsigned char *)(ws + fl.img);
   p.img_stride = fl.img_stride;
+  p.bimg = (const unsigned char *)(ws + bl.bimg);
+  p.bimg_stride = bl.bimg_stride;
   p.Sx = (const float *)(ws + bl.Sx);
   p.Dx = (float *)(ws + bl.Dx);
   p.dout = (const __nv_bfloat16 *)b->d_output;

@@ -26,12 +26,10 @@
 // Everything above follows from the row recurrence by algebra alone; the float64 oracle
 // takes the derivative step by step instead and the parity tests compare the two.
 //
-// Kernels (warp-level tf32 MMAs, fp32 accumulation -- the triangular solves in the 3xTF32
-// split; the dense chunk products are small and varied, the serial part is the state scan):
-//   gdp_bwd_scan_kernel   one CTA per (sequence, head): D = dL/dS in registers (a warp per
-//                         16 state rows), chunks in reverse, operands from the forward's
-//                         per-chunk images (TMA bulk copies, double-buffered), writes D_C of
-//                         every chunk
+// Kernels: the reverse state scan (D_C of every chunk) runs on the tcgen05 tensor cores with D
+// resident in TMEM (gdp_bwd_scan_tc.cu); the kernels here use warp-level tf32 MMAs with fp32
+// accumulation (the triangular solves in the 3xTF32 split; the dense chunk products are small
+// and varied):
 //   gdp_bwd_chunk_kernel  one CTA per (expanded chunk, head), V in 16- (or 8-) column
 //                         slices: the per-row gradients above, the L2-norm chain rule
 //                         dx = dxhat / n - x (x . dxhat) / n^3, dq / dk / dv / dbeta stores
@@ -58,218 +56,6 @@ __device__ __forceinline__ void mma8(float *c, uint32_t a0, uint32_t a1, uint32_
       "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-// c += A B over ks k-steps of 8, with a(row, k) and b(k, col) relative to the tile origin.
-template <class FA, class FB>
-__device__ __forceinline__ void mma_tile(float *c, int ks, int g, int t, FA a, FB b) {
-#pragma unroll 2
-  for (int k = 0; k < ks; ++k) {
-    const int k0 = 8 * k;
-    mma8(c, tf32r(a(g, k0 + t)), tf32r(a(g + 8, k0 + t)), tf32r(a(g, k0 + t + 4)), tf32r(a(g + 8, k0 + t + 4)),
-         tf32r(b(k0 + t, g)), tf32r(b(k0 + t + 4, g)));
-  }
-}
-
-// ---------------------------------------------------------------------------------------
-// Reverse state scan.
-// ---------------------------------------------------------------------------------------
-constexpr uint32_t kBwdScanLimit = 227u * 1024u;
-
-__host__ __device__ inline uint32_t bwd_stage_bytes(int d, int qpad) {
-  return (ImageLayout(d, qpad).bytes + 1023u) & ~1023u;
-}
-// d_output rows of a chunk, bf16 [qpad][d + 8]
-__host__ __device__ inline uint32_t bwd_dos_bytes(int d, int qpad) { return (uint32_t)qpad * (d + 8) * 2u; }
-__host__ __device__ inline int bwd_scan_stages(int d, int qpad) {
-  return 2u * bwd_stage_bytes(d, qpad) + bwd_dos_bytes(d, qpad) + 1024u <= kBwdScanLimit ? 2 : 1;
-}
-__host__ inline size_t bwd_scan_smem(int d, int qpad) {
-  return (size_t)bwd_scan_stages(d, qpad) * bwd_stage_bytes(d, qpad) + bwd_dos_bytes(d, qpad) + 1024u;
-}
-
-// Warp w holds state rows 16 w .. 16 w + 15 of D (all columns) in the m16n8 accumulator layout.
-// Per chunk it forms its rows of Z = D Ktil^T + dO^T P, then D_in = gamma_C D - Z W + dO^T Qh.
-template <int D, int QP>
-__global__ void __launch_bounds__(2 * D, 1) gdp_bwd_scan_kernel(BwdProblem p) {
-  constexpr int NW = D / 16;     // warps
-  constexpr int LDO = D + 8;     // row stride (bf16 elements) of the staged d_output rows
-  const int seq = blockIdx.x, h = blockIdx.y;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
-  int64_t bos, L;
-  if (!seq_bounds(p.cu, p.cu64, p.T, seq, &bos, &L)) return;
-  const int M = p.M, H = p.H;
-  const ImageLayout il(D, QP);
-  const uint32_t sbytes = bwd_stage_bytes(D, QP);
-  const int nst = bwd_scan_stages(D, QP);
-  extern __shared__ __align__(1024) unsigned char bwd_scan_raw[];
-  unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)bwd_scan_raw + 1023) & ~(uintptr_t)1023);
-  __nv_bfloat16 *dos = reinterpret_cast<__nv_bfloat16 *>(sm + nst * sbytes);
-  __shared__ __align__(8) uint64_t full[2];
-  __shared__ float red[NW];
-  const int64_t KV = (int64_t)D * D, sh = (int64_t)seq * H + h;
-  const int64_t nchunks = (L * M + kChunk - 1) / kChunk;
-  const int64_t cod_i = p.cod[seq];
-  const int64_t nall = (cod_i < 0) ? 0 : max((int64_t)0, min(nchunks, p.ws_rows - cod_i));
-  const int r0 = 16 * warp + g;  // this thread's rows r0 and r0 + 8
-
-  // D = dL/dS_final; <dS_final, S_final> for the decay gradient
-  float dacc[D / 8][4];
-  {
-    const float *src = p.dfin ? p.dfin + sh * KV : nullptr;
-    const float *fin = (p.dfin && p.fin) ? p.fin + sh * KV : nullptr;
-    float part = 0.f;
-#pragma unroll
-    for (int j = 0; j < D / 8; ++j)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int64_t off = (int64_t)(r0 + 8 * hf) * D + 8 * j + 2 * t;
-        const float2 x = src ? *reinterpret_cast<const float2 *>(src + off) : make_float2(0.f, 0.f);
-        dacc[j][2 * hf] = x.x;
-        dacc[j][2 * hf + 1] = x.y;
-        if (fin) {
-          const float2 s2 = *reinterpret_cast<const float2 *>(fin + off);
-          part += x.x * s2.x + x.y * s2.y;
-        }
-      }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-    if (lane == 0) red[warp] = part;
-  }
-  if (tid == 0) {
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
-    mbar_init_fence();
-  }
-  __syncthreads();
-  if (tid == 0 && p.tot) {
-    float s2 = 0.f;
-    for (int w = 0; w < NW; ++w) s2 += red[w];
-    p.tot[sh] = s2;
-  }
-  auto image = [&](int64_t e) { return p.img + (size_t)((cod_i + e) * H + h) * p.img_stride; };
-  int issued[2] = {0, 0};
-  auto issue = [&](int64_t i) {  // chunk nall - 1 - i into stage i % nst (thread 0)
-    const int st = (int)(i % nst);
-    mbar_arrive_expect_tx(&full[st], il.bytes);
-    bulk_g2s(sm + st * sbytes, image(nall - 1 - i), il.bytes, &full[st]);
-    ++issued[st];
-  };
-  if (tid == 0)
-    for (int64_t i = 0; i < nst && i < nall; ++i) issue(i);
-  auto dO = [&](int qi, int v) { return __bfloat162float(dos[qi * LDO + v]); };
-  // per-thread parts of the operand addresses in the swizzled image (row r, column k: 1024-byte
-  // atoms of 8 rows; the 16-byte chunk (k % 32) / 4 of row r sits at chunk position
-  // ((k % 32) / 4) ^ (r % 8)), in floats; the rest are compile-time steps
-  const uint32_t gq = (uint32_t)(g & 3), gh = (uint32_t)(g >> 2);
-
-  bool aborted = false;
-  for (int64_t i = 0; i < nall; ++i) {
-    const int64_t e = nall - 1 - i;
-    const int st = (int)(i % nst);
-    const float *imf = reinterpret_cast<const float *>(sm + st * sbytes);
-    // the gradient at chunk e's exit
-    float *dst = p.Dx + ((cod_i + e) * H + h) * KV;
-#pragma unroll
-    for (int j = 0; j < D / 8; ++j)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf)
-        *reinterpret_cast<float2 *>(dst + (int64_t)(r0 + 8 * hf) * D + 8 * j + 2 * t) =
-            make_float2(dacc[j][2 * hf], dacc[j][2 * hf + 1]);
-    // d_output rows of the chunk's readouts (bf16, zero past the readout count)
-    const ImageMeta mt = *reinterpret_cast<const ImageMeta *>(image(e) + il.meta);
-    const int64_t tq0 = (bos * M + e * kChunk + mt.p0) / M;
-    for (int idx = tid; idx < QP * (D / 8); idx += 32 * NW) {
-      const int qi = idx / (D / 8), c8 = (idx % (D / 8)) * 8;
-      uint4 x = make_uint4(0u, 0u, 0u, 0u);
-      if (qi < mt.nq) x = *reinterpret_cast<const uint4 *>(p.dout + ((tq0 + qi) * H + h) * (int64_t)D + c8);
-      *reinterpret_cast<uint4 *>(dos + qi * LDO + c8) = x;
-    }
-    const bool ok = mbar_wait(&full[st], (uint32_t)((i / nst) & 1));
-    if (!__syncthreads_and(ok)) {
-      aborted = true;
-      break;
-    }
-    // Z = D Ktil^T + dO^T P (rows of this warp x 64 chunk rows s).  The D fragments serve as A
-    // with the k order permuted within each 8-column step (logical k = t <-> column 2t,
-    // k = t + 4 <-> 2t + 1); B is read in the same order.
-    float z[8][4];
-#pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      z[n][0] = z[n][1] = z[n][2] = z[n][3] = 0.f;
-      const uint32_t cq = 2u * (n & 3) + gh;  // chunk of column s = 8 n + g in its row
-      const uint32_t blk = (il.b2 + (uint32_t)(n >> 2) * il.b2_block) / 4u + gq;
-      // Ktil^T rows f = 8 j + 2 t (+1): atom j, row-in-atom 2t (+1)
-      const uint32_t ko0 = blk + 2u * t * 32u + (((cq ^ (2u * t)) & 7u) << 2);
-      const uint32_t ko1 = blk + (2u * t + 1u) * 32u + (((cq ^ (2u * t + 1u)) & 7u) << 2);
-#pragma unroll
-      for (int j = 0; j < D / 8; ++j)
-        mma8(z[n], tf32r(dacc[j][0]), tf32r(dacc[j][2]), tf32r(dacc[j][1]), tf32r(dacc[j][3]),
-             tf32r(imf[ko0 + 256u * j]), tf32r(imf[ko1 + 256u * j]));
-      // P rows d + k0 + t (+4): atom (d + k0) / 8, row-in-atom t (+4)
-      const uint32_t po0 = blk + (uint32_t)(D / 8) * 256u + t * 32u + (((cq ^ t) & 7u) << 2);
-      const uint32_t po1 = blk + (uint32_t)(D / 8) * 256u + (t + 4u) * 32u + (((cq ^ (t + 4u)) & 7u) << 2);
-#pragma unroll
-      for (int k = 0; k < QP / 8; ++k) {
-        const int k0 = 8 * k;
-        mma8(z[n], tf32r(dO(k0 + t, r0)), tf32r(dO(k0 + t, r0 + 8)), tf32r(dO(k0 + t + 4, r0)),
-             tf32r(dO(k0 + t + 4, r0 + 8)), tf32r(imf[po0 + 256u * k]), tf32r(imf[po1 + 256u * k]));
-      }
-    }
-    // D_in = gamma_C D + Z (-W) + dO^T Qh; a fast image holds -W and Qh divided by gamma_C
-    const float gam = mt.gamma_last;
-    if (!mt.fast)
-#pragma unroll
-      for (int j = 0; j < D / 8; ++j)
-#pragma unroll
-        for (int x = 0; x < 4; ++x) dacc[j][x] *= gam;
-#pragma unroll
-    for (int j = 0; j < D / 8; ++j) {
-      // column f = 8 j + g: K-block j / 4, chunk 2 (j % 4) + g / 4
-      const uint32_t cq = 2u * (j & 3) + gh;
-      const uint32_t blk = (il.b1 + (uint32_t)(j >> 2) * il.b1_block) / 4u + gq;
-      // -c W rows qp + 8 ks + 2 t (+1): atom qp / 8 + ks, row-in-atom 2t (+1)
-      const uint32_t wo0 = blk + (uint32_t)(QP / 8) * 256u + 2u * t * 32u + (((cq ^ (2u * t)) & 7u) << 2);
-      const uint32_t wo1 = blk + (uint32_t)(QP / 8) * 256u + (2u * t + 1u) * 32u + (((cq ^ (2u * t + 1u)) & 7u) << 2);
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
-        mma8(dacc[j], tf32r(z[ks][0]), tf32r(z[ks][2]), tf32r(z[ks][1]), tf32r(z[ks][3]), tf32r(imf[wo0 + 256u * ks]),
-             tf32r(imf[wo1 + 256u * ks]));
-      // c Qh rows k0 + t (+4): atom k0 / 8, row-in-atom t (+4)
-      const uint32_t qo0 = blk + t * 32u + (((cq ^ t) & 7u) << 2);
-      const uint32_t qo1 = blk + (t + 4u) * 32u + (((cq ^ (t + 4u)) & 7u) << 2);
-#pragma unroll
-      for (int k = 0; k < QP / 8; ++k) {
-        const int k0 = 8 * k;
-        mma8(dacc[j], tf32r(dO(k0 + t, r0)), tf32r(dO(k0 + t, r0 + 8)), tf32r(dO(k0 + t + 4, r0)),
-             tf32r(dO(k0 + t + 4, r0 + 8)), tf32r(imf[qo0 + 256u * k]), tf32r(imf[qo1 + 256u * k]));
-      }
-    }
-    if (mt.fast)
-#pragma unroll
-      for (int j = 0; j < D / 8; ++j)
-#pragma unroll
-        for (int x = 0; x < 4; ++x) dacc[j][x] *= gam;
-    __syncthreads();  // every warp is done with this stage and dos
-    if (tid == 0 && i + nst < nall) issue(i + nst);
-  }
-  if (aborted) {
-    if (tid == 0) {
-      set_status(p.status, GDP_DEV_ERR_TIMEOUT);
-      for (int st = 0; st < nst; ++st)  // bounded: the copies issued on each stage have landed
-        if (issued[st] > 0) mbar_wait(&full[st], (uint32_t)((issued[st] - 1) & 1));
-    }
-    __syncthreads();
-    return;
-  }
-  if (p.dinit) {
-    float *dst = p.dinit + sh * KV;
-#pragma unroll
-    for (int j = 0; j < D / 8; ++j)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf)
-        *reinterpret_cast<float2 *>(dst + (int64_t)(r0 + 8 * hf) * D + 8 * j + 2 * t) =
-            make_float2(dacc[j][2 * hf], dacc[j][2 * hf + 1]);
-  }
 }
 
 // ---------------------------------------------------------------------------------------
@@ -897,16 +683,6 @@ __global__ void __launch_bounds__(256) gdp_bwd_dg_kernel(BwdProblem p) {
 // Slice width of the per-chunk kernel: 16 V columns when the shared memory allows, else 8.
 int chunk_slice(int d, int qpad) { return ChunkSmem(d, qpad, 16).total <= 227u * 1024u ? 16 : 8; }
 
-template <int D, int QP>
-cudaError_t launch_bscan(const BwdProblem &p, cudaStream_t stream) {
-  const size_t smem = bwd_scan_smem(D, QP);
-  cudaError_t e = cudaFuncSetAttribute(gdp_bwd_scan_kernel<D, QP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e != cudaSuccess) return e;
-  gdp_bwd_scan_kernel<D, QP><<<dim3((unsigned)p.N, (unsigned)p.H), 2 * D, smem, stream>>>(p);
-  return cudaGetLastError();
-}
-
 template <int D, int VSL>
 cudaError_t launch_chunk(const BwdProblem &p, cudaStream_t stream) {
   const size_t smem = ChunkSmem(D, p.qpad, VSL).total;
@@ -922,15 +698,7 @@ cudaError_t launch_chunk(const BwdProblem &p, cudaStream_t stream) {
 cudaError_t launch_backward(const BwdProblem &p, cudaStream_t stream) {
   cudaError_t e;
   const int D = p.D, QP = p.qpad;
-  if (p.N > 0) {
-    if (D == 128)
-      e = QP == 16 ? launch_bscan<128, 16>(p, stream) : QP == 32 ? launch_bscan<128, 32>(p, stream)
-                                                    : launch_bscan<128, 64>(p, stream);
-    else
-      e = QP == 16 ? launch_bscan<64, 16>(p, stream) : QP == 32 ? launch_bscan<64, 32>(p, stream)
-                                                   : launch_bscan<64, 64>(p, stream);
-    if (e != cudaSuccess) return e;
-  }
+  if (p.N > 0 && (e = launch_bwd_tc_scan(p, stream)) != cudaSuccess) return e;
   if (p.ntdp_pad > 0) {
     const int vsl = chunk_slice(D, QP);
     if (D == 128)

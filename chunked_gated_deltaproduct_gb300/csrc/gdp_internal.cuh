@@ -66,6 +66,31 @@ struct ImageLayout {
     return ((uint32_t)r >> 3) * 1024u + ((uint32_t)r & 7u) * 128u + ((((b >> 4) ^ (uint32_t)r) & 7u) << 4) + (b & 15u);
   }
 };
+// The same operands laid out for the backward's reverse state scan, whose products read
+// every block transposed (so that each B operand is K-major again): batch 1 (N = 64 chunk rows
+// s) reads Ktil as [s][c] and P^T as [s][q]; batch 2 (N = d features c) reads (-W)^T as [c][s]
+// and Qh^T as [c][q], with -W and Qh divided by gamma_last in a fast image as above.  fp32,
+// 128-byte swizzle, 32-column K blocks; the chunk's ImageMeta follows batch 1's blocks.
+struct BwdImageLayout {
+  uint32_t kt, pt, meta, part1, b2, wt, wt_block, qt, part2, bytes;
+  __host__ __device__ BwdImageLayout(int d, int qpad) {
+    const uint32_t nqb = ((uint32_t)qpad + 31u) / 32u;  // K blocks of the readout dimension
+    kt = 0;                                             // [d/32][64 rows][128 B]
+    pt = kt + (uint32_t)(d / 32) * 8192u;               // [nqb][64 rows][128 B]
+    meta = pt + nqb * 8192u;
+    part1 = meta + 64u;
+    b2 = (part1 + 1023u) & ~1023u;
+    wt = b2;                                            // [2][d rows][128 B]
+    wt_block = (uint32_t)d * 128u;
+    qt = wt + 2u * wt_block;                            // [nqb][d rows][128 B]
+    part2 = qt + nqb * wt_block - b2;
+    bytes = b2 + part2;
+  }
+  __host__ __device__ uint32_t k_at(int s, int c) const { return kt + (c >> 5) * 8192u + ImageLayout::swz_off(s, c); }
+  __host__ __device__ uint32_t p_at(int s, int q) const { return pt + (q >> 5) * 8192u + ImageLayout::swz_off(s, q); }
+  __host__ __device__ uint32_t w_at(int c, int s) const { return wt + (s >> 5) * wt_block + ImageLayout::swz_off(c, s); }
+  __host__ __device__ uint32_t q_at(int c, int q) const { return qt + (q >> 5) * wt_block + ImageLayout::swz_off(c, q); }
+};
 struct ImageMeta {
   float gamma_last;  // 2^(G2_last): decay of the whole chunk
   int nq;            // readout rows in the chunk
@@ -164,6 +189,10 @@ struct Problem {
   // reduction of the bounds test (gdp_arm_bounds_test; 0 otherwise)
   unsigned long long *bounds;
   int64_t bounds_shrink;
+  // The backward's forward recompute: the WY kernel also writes each tile's BwdImageLayout image
+  // here, bimg_stride bytes apart (NULL otherwise)
+  unsigned char *bimg;
+  size_t bimg_stride;
 };
 
 // Everything the backward kernels need about one call (gdp_backward.cu).  Heads are
@@ -182,6 +211,8 @@ struct BwdProblem {
   int64_t ntdp_pad, ws_rows;
   const unsigned char *img;  // the forward's operand images (ImageLayout), img_stride apart
   size_t img_stride;
+  const unsigned char *bimg;  // the same operands for the reverse scan (BwdImageLayout), bimg_stride apart
+  size_t bimg_stride;
   const float *Sx;           // [ntdp][H][V][K] state entering each expanded chunk
   float *Dx;                 // [ntdp][H][V][K] dL/dS at each expanded chunk's exit
   const __nv_bfloat16 *dout; // [T][H][V] dL/do
@@ -194,6 +225,10 @@ struct BwdProblem {
   uint32_t *status;
 };
 cudaError_t launch_backward(const BwdProblem &p, cudaStream_t stream);
+// The reverse state scan on the tensor cores (gdp_bwd_scan_tc.cu) and the byte stride of its
+// per-tile operand images (BwdImageLayout rounded to 1 KB).
+cudaError_t launch_bwd_tc_scan(const BwdProblem &p, cudaStream_t stream);
+size_t bwd_image_stride(int d, int qpad);
 
 // Launch `kern` on `stream`, with programmatic stream serialization when `pdl`.
 template <typename... Params, typename... Args>

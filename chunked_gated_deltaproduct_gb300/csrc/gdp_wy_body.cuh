@@ -398,6 +398,9 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
   __syncthreads();
   const ImageLayout il(d, QP);
   unsigned char *img = p.img + (size_t)((int64_t)row * p.H + h) * p.img_stride;
+  // the backward's layout of the same operands (its forward recompute only)
+  const BwdImageLayout bl(d, QP);
+  unsigned char *bimg = p.bimg ? p.bimg + (size_t)((int64_t)row * p.H + h) * p.bimg_stride : nullptr;
   {
     // the TMEM row of this thread, this warp's half of the columns, in 16-column pieces
     const uint32_t taddr = tD1 + ((uint32_t)(quad * 32) << 16);
@@ -439,6 +442,9 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
               o[u] = (live && s_ <= pr) ? sc * exp2f(gp - G2[s_]) * rk[s_] * dv[u4 + u] : 0.f;
             }
             *reinterpret_cast<float4 *>(img + il.pm(d, qi, c0 + u4)) = o4;
+            if (bimg)  // P^T: row s, column qi (a row segment per warp instruction)
+#pragma unroll
+              for (int u = 0; u < 4; ++u) *reinterpret_cast<float *>(bimg + bl.p_at(c0 + u4 + u, qi)) = o[u];
           }
         }
       }
@@ -451,6 +457,9 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
               make_float4(qscale * x[0], qscale * x[1], qscale * x[2], qscale * x[3]);
           *reinterpret_cast<float4 *>(img + il.qh(qi, f0 + 4)) =
               make_float4(qscale * x[4], qscale * x[5], qscale * x[6], qscale * x[7]);
+          if (bimg)  // Qh^T: row f, column qi
+#pragma unroll
+            for (int j = 0; j < 8; ++j) *reinterpret_cast<float *>(bimg + bl.q_at(f0 + j, qi)) = qscale * x[j];
         }
       }
     }
@@ -602,6 +611,11 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
 #pragma unroll
         for (int u = 0; u < 16; ++u)
           *reinterpret_cast<float *>(w0 + (uint32_t)(u >> 3) * 1024u + xo[u & 7]) = -wv[u] * isw;
+        if (bimg)  // (-W)^T: row f, columns c0 .. c0 + 15, four 16-byte chunks
+#pragma unroll
+          for (int j = 0; j < 16; j += 4)
+            *reinterpret_cast<float4 *>(bimg + bl.w_at(f, c0 + j)) =
+                make_float4(-wv[j] * isw, -wv[j + 1] * isw, -wv[j + 2] * isw, -wv[j + 3] * isw);
       }
     }
     // Ktil^T image: row f = 2^(G2_last - G2_s) rk_s k[s][f], K-block s/32; lane = s, so each
@@ -621,6 +635,12 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
       unsigned char *r0 = kimg + (uint32_t)(f0 >> 3) * 1024u;
 #pragma unroll
       for (int j = 0; j < 8; ++j) *reinterpret_cast<float *>(r0 + yo[j]) = kss * x[j];
+      if (bimg) {  // Ktil: row s, features f0 .. f0 + 7, two 16-byte chunks
+        *reinterpret_cast<float4 *>(bimg + bl.k_at(s_, f0)) =
+            make_float4(kss * x[0], kss * x[1], kss * x[2], kss * x[3]);
+        *reinterpret_cast<float4 *>(bimg + bl.k_at(s_, f0 + 4)) =
+            make_float4(kss * x[4], kss * x[5], kss * x[6], kss * x[7]);
+      }
     }
   }
   if (tid == 0) {
@@ -630,6 +650,7 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
     mt->p0 = p0;
     mt->len = len;
     mt->fast = fast ? 1 : 0;
+    if (bimg) *reinterpret_cast<ImageMeta *>(bimg + bl.meta) = *mt;
     if (abort_flag) set_status(p.status, GDP_DEV_ERR_TIMEOUT);
   }
   tc_fence_before();
