@@ -308,6 +308,50 @@ __global__ void __launch_bounds__(kChunkThreads, 1) gdp_bwd_chunk_kernel(BwdProb
   }
   __syncthreads();
 
+  // ---- the V slices' rows: S and D_C rows v0 .. v0 + VSL - 1 (float4 items) and the v / d_output
+  // columns v0 .. (4 bf16 per item), at most one item of each per thread; each slice's items are
+  // loaded into registers one slice ahead (the first during the Gram and the inverse) and put
+  // into shared memory when the slice starts ----
+  const int64_t KV = (int64_t)D * D;
+  const float *Sg = p.Sx + (srow * H + h) * KV;
+  const float *Dg = p.Dx + (srow * H + h) * KV;
+  constexpr int NS = VSL * (D / 4), NV = (kChunk + 64) * (VSL / 4);
+  static_assert(NS <= kChunkThreads && NV <= kChunkThreads, "one slice item per thread");
+  float4 pre_s = make_float4(0.f, 0.f, 0.f, 0.f), pre_d = pre_s;
+  uint2 pre_v = make_uint2(0u, 0u);
+  auto fetch = [&](int v0) {
+    if (tid < NS) {
+      const int r = tid / (D / 4), c4 = (tid % (D / 4)) * 4;
+      pre_s = *reinterpret_cast<const float4 *>(Sg + (int64_t)(v0 + r) * D + c4);
+      pre_d = *reinterpret_cast<const float4 *>(Dg + (int64_t)(v0 + r) * D + c4);
+    }
+    if (tid < (kChunk + QP) * (VSL / 4)) {
+      const int r = tid / (VSL / 4), c4 = (tid % (VSL / 4)) * 4;
+      const bool isv = r < kChunk;
+      const int rr = isv ? r : r - kChunk;
+      pre_v = make_uint2(0u, 0u);
+      if (isv ? rr < len : rr < nq)
+        pre_v = *reinterpret_cast<const uint2 *>(isv ? p.v + (R0 + rr) * p.v_st + (int64_t)h * p.v_sh + v0 + c4
+                                                     : p.dout + ((tq0 + rr) * H + h) * (int64_t)D + v0 + c4);
+    }
+  };
+  auto put = [&](float *ss_, float *dcs_, float *vs_, float *dos_) {
+    if (tid < NS) {
+      const int r = tid / (D / 4), c4 = (tid % (D / 4)) * 4;
+      *reinterpret_cast<float4 *>(ss_ + r * lay.ldd + c4) = pre_s;
+      *reinterpret_cast<float4 *>(dcs_ + r * lay.ldd + c4) = pre_d;
+    }
+    if (tid < (kChunk + QP) * (VSL / 4)) {
+      const int r = tid / (VSL / 4), c4 = (tid % (VSL / 4)) * 4;
+      const bool isv = r < kChunk;
+      const int rr = isv ? r : r - kChunk;
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pre_v.x));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pre_v.y));
+      *reinterpret_cast<float4 *>((isv ? vs_ : dos_) + rr * lay.ldv + c4) = make_float4(a.x, a.y, b.x, b.y);
+    }
+  };
+  fetch(0);
+
   // ---- L [64 x 64] and P [qp x 64] ----
   for (int u = warp; u < 2 * (4 + QP / 16); u += kChunkThreads / 32) {  // (m-tile, 4 n-tiles) units
     float acc[4][4] = {};
@@ -333,24 +377,15 @@ __global__ void __launch_bounds__(kChunkThreads, 1) gdp_bwd_chunk_kernel(BwdProb
   for (int i = tid; i < kChunk * kLC; i += kChunkThreads) g23[i] = 0.f;
   for (int i = tid; i < QP * kLC; i += kChunkThreads) g4[i] = 0.f;
   __syncthreads();
-  // ---- T = (I + A)^-1, A = diag(beta) L: column c by forward substitution, 8 threads per column ----
+  // ---- T = (I + A)^-1, A = diag(beta) L: the forward recompute's WY kernel inverted it (its A is
+  // the same matrix: beta_r gamma_r / gamma_j (khat_r . khat_j), j < r) and left it beside the
+  // chunk's reverse-scan image ----
   {
-    const int col = tid >> 3, i = tid & 7;
-    float hist[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int r = 0; r < kChunk; ++r) {
-      float part = 0.f;
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj)
-        if (8 * jj < r) part += lm[r * kLC + 8 * jj + i] * hist[jj];  // L_rj = 0 for j >= r
-      part += __shfl_xor_sync(0xffffffffu, part, 1);
-      part += __shfl_xor_sync(0xffffffffu, part, 2);
-      part += __shfl_xor_sync(0xffffffffu, part, 4);
-      const float val = (r == col ? 1.f : 0.f) - bt[r] * part;
-      if ((r & 7) == i) {
-        hist[r >> 3] = val;
-        tm[r * kLC + col] = val;
-      }
+    const float *Tg = reinterpret_cast<const float *>(p.bimg + (size_t)(srow * H + h) * p.bimg_stride +
+                                                      BwdImageLayout(D, QP).tinv);
+    for (int idx = tid; idx < kChunk * kChunk / 4; idx += kChunkThreads) {
+      const int r = idx >> 4, c4 = (idx & 15) * 4;
+      *reinterpret_cast<float4 *>(tm + r * kLC + c4) = *reinterpret_cast<const float4 *>(Tg + r * kChunk + c4);
     }
   }
   __syncthreads();
@@ -373,35 +408,13 @@ __global__ void __launch_bounds__(kChunkThreads, 1) gdp_bwd_chunk_kernel(BwdProb
     return u < nqt;
   };
 
-  const int64_t KV = (int64_t)D * D;
-  const float *Sg = p.Sx + (srow * H + h) * KV;
-  const float *Dg = p.Dx + (srow * H + h) * KV;
   constexpr int NVS = VSL / 8;  // n-tiles per slice
 #pragma unroll 1
   for (int v0 = 0; v0 < D; v0 += VSL) {
-    // ---- slice loads: S and D_C rows v0 .., v and d_output columns v0 .. ----
-    for (int idx = tid; idx < VSL * (D / 4); idx += kChunkThreads) {
-      const int r = idx / (D / 4), c4 = (idx % (D / 4)) * 4;
-      *reinterpret_cast<float4 *>(ss + r * LDD + c4) =
-          *reinterpret_cast<const float4 *>(Sg + (int64_t)(v0 + r) * D + c4);
-      *reinterpret_cast<float4 *>(dcs + r * LDD + c4) =
-          *reinterpret_cast<const float4 *>(Dg + (int64_t)(v0 + r) * D + c4);
-    }
-    for (int idx = tid; idx < (kChunk + QP) * (VSL / 4); idx += kChunkThreads) {
-      const int r = idx / (VSL / 4), c4 = (idx % (VSL / 4)) * 4;
-      const bool isv = r < kChunk;
-      const int rr = isv ? r : r - kChunk;
-      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (isv ? rr < len : rr < nq) {
-        const __nv_bfloat16 *src = isv ? p.v + (R0 + rr) * p.v_st + (int64_t)h * p.v_sh + v0 + c4
-                                       : p.dout + ((tq0 + rr) * H + h) * (int64_t)D + v0 + c4;
-        const uint2 u = *reinterpret_cast<const uint2 *>(src);
-        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
-        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
-        x = make_float4(a.x, a.y, b.x, b.y);
-      }
-      *reinterpret_cast<float4 *>((isv ? vs : dos) + rr * LDV + c4) = x;
-    }
+    // ---- slice rows: S and D_C rows v0 .., v and d_output columns v0 .. (fetched a slice
+    // ahead); the next slice's go out now ----
+    put(ss, dcs, vs, dos);
+    if (v0 + VSL < D) fetch(v0 + VSL);
     __syncthreads();
     // ---- rhs = v - gamma (Khat S^T);  QS = qhat S^T;  Zt = Ktil D_C^T + P^T dO ----
     for (int u = warp; u < 8 + QP / 16; u += kChunkThreads / 32) {  // (m-tile, all NVS n-tiles) units

@@ -43,8 +43,9 @@ using namespace sm100;
 constexpr int kBtThreads = 320;
 constexpr uint32_t kBtStageBudget = 200u * 1024u;
 
+// a stage holds the image's two parts (the inverse after them stays in global memory)
 __host__ __device__ inline uint32_t bt_stage_bytes(int d, int qpad) {
-  return (BwdImageLayout(d, qpad).bytes + 1023u) & ~1023u;
+  return (BwdImageLayout(d, qpad).tinv + 1023u) & ~1023u;
 }
 __host__ __device__ inline int bt_stages(int d, int qpad) {
   return 2u * bt_stage_bytes(d, qpad) <= kBtStageBudget ? 2 : 1;
@@ -386,7 +387,7 @@ __global__ void __launch_bounds__(kBtThreads, 1)
 }  // namespace
 
 size_t bwd_tc_scan_smem(int d, int qpad) { return bt_smem_bytes(d, qpad); }
-size_t bwd_image_stride(int d, int qpad) { return bt_stage_bytes(d, qpad); }
+size_t bwd_image_stride(int d, int qpad) { return (BwdImageLayout(d, qpad).bytes + 1023u) & ~1023u; }
 
 cudaError_t launch_bwd_tc_scan(const BwdProblem &p, cudaStream_t stream) {
   const size_t smem = bt_smem_bytes(p.D, p.qpad);

@@ -72,7 +72,9 @@ struct ImageLayout {
 // and Qh^T as [c][q], with -W and Qh divided by gamma_last in a fast image as above.  fp32,
 // 128-byte swizzle, 32-column K blocks; the chunk's ImageMeta follows batch 1's blocks.
 struct BwdImageLayout {
-  uint32_t kt, pt, meta, part1, b2, wt, wt_block, qt, part2, bytes;
+  // tinv: T = (I + A)^-1 of the chunk, dense [64][64] fp32, after the two parts (read by the
+  // per-chunk gradient kernel; the scan's copies stop before it)
+  uint32_t kt, pt, meta, part1, b2, wt, wt_block, qt, part2, tinv, bytes;
   __host__ __device__ BwdImageLayout(int d, int qpad) {
     const uint32_t nqb = ((uint32_t)qpad + 31u) / 32u;  // K blocks of the readout dimension
     kt = 0;                                             // [d/32][64 rows][128 B]
@@ -84,7 +86,8 @@ struct BwdImageLayout {
     wt_block = (uint32_t)d * 128u;
     qt = wt + 2u * wt_block;                            // [nqb][d rows][128 B]
     part2 = qt + nqb * wt_block - b2;
-    bytes = b2 + part2;
+    tinv = b2 + part2;
+    bytes = tinv + 64u * 64u * 4u;
   }
   __host__ __device__ uint32_t k_at(int s, int c) const { return kt + (c >> 5) * 8192u + ImageLayout::swz_off(s, c); }
   __host__ __device__ uint32_t p_at(int s, int q) const { return pt + (q >> 5) * 8192u + ImageLayout::swz_off(s, q); }
@@ -225,8 +228,8 @@ struct BwdProblem {
   uint32_t *status;
 };
 cudaError_t launch_backward(const BwdProblem &p, cudaStream_t stream);
-// The reverse state scan on the tensor cores (gdp_bwd_scan_tc.cu) and the byte stride of its
-// per-tile operand images (BwdImageLayout rounded to 1 KB).
+// The reverse state scan on the tensor cores (gdp_bwd_scan_tc.cu) and the byte stride of the
+// per-tile backward images (BwdImageLayout, with the inverse, rounded to 1 KB).
 cudaError_t launch_bwd_tc_scan(const BwdProblem &p, cudaStream_t stream);
 size_t bwd_image_stride(int d, int qpad);
 

@@ -499,6 +499,12 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
   }
   __syncthreads();
   inverse_offdiag(A, Tm, Y, warp, lane);
+  if (bimg)  // T itself for the backward's per-chunk gradients, dense [64][64]
+    for (int idx = tid; idx < kChunk * kChunk / 4; idx += kWyThreads) {
+      const int r = idx >> 4, c4 = (idx & 15) * 4;
+      *reinterpret_cast<float4 *>(bimg + bl.tinv + (uint32_t)(r * kChunk + c4) * 4u) =
+          *reinterpret_cast<const float4 *>(Tm + r * kLdT + c4);
+    }
 
   // ---- T diag(beta gamma rk) and T diag(beta) as hi + lo of the input type, K-major swizzled
   // [64 s][64 j]; for float16 first scaled by sw, su (powers of two, see f16_split_scale) ----
