@@ -2,13 +2,14 @@
 summaries under profiles/ were captured on (the full-size workloads are too large for a
 multi-pass capture).
 
-    python -m chunked_gated_deltaproduct_gb300.profile_case {w3|w4|w2|decode|desc} [--calls N] [--fused]
+    python -m chunked_gated_deltaproduct_gb300.profile_case {w3|w4|w2|decode|desc|bwd} [--calls N] [--fused]
 
 w3: 8 sequences x 1024 tokens, H=16, d=128, M=3, unnormalised q/k with in-kernel L2 norm (the
     8 x 4096 batch cut to a quarter of its length); w4: one sequence of 12288 tokens, H=32, d=128,
     M=2, initial state and chunk states (the 65536-token sequence cut to its first six segments,
     the segmented plan); w2: the four-sequence varlen batch at full size; decode: the decode step
-    of the serving batch; desc: the descriptor kernel alone over 3000 sequences.
+    of the serving batch; desc: the descriptor kernel alone over 3000 sequences; bwd: the backward
+    pass of the 65536-token shape cut to 4096 tokens (H=32, d=128, M=2, initial state).
 """
 from __future__ import annotations
 
@@ -28,7 +29,7 @@ def main():
     from gdp_workloads import make_custom, make_workload
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["w2", "w3", "w4", "decode", "desc"])
+    ap.add_argument("case", choices=["w2", "w3", "w4", "decode", "desc", "bwd"])
     ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--fused", action="store_true")
     a = ap.parse_args()
@@ -50,6 +51,18 @@ def main():
         args = pkg.decode_args(q, k, v, g, b, w.M, w.scale, None, cache, sidx, out, None, False, None)
         for _ in range(a.calls):
             pkg.gdp_decode_step(args)
+        torch.cuda.synchronize()
+        return
+    if a.case == "bwd":
+        from gdp_workloads import make_cotangents
+
+        w = make_custom([4096], 32, 128, 2, seed=1004, decay=0.02, init_sigma=0.05)
+        d_out, d_fin = make_cotangents(w, seed=1, dfin_sigma=0.5)
+        dd = lambda x: None if x is None else x.to(dev)
+        for _ in range(a.calls):
+            pkg.chunk_gated_delta_product_backward(dd(w.q), dd(w.k), dd(w.v), dd(w.g), dd(w.beta), w.cu_seqlens.to(dev),
+                                                   w.M, dd(d_out), scale=w.scale, initial_state=dd(w.initial_state),
+                                                   d_final_state=dd(d_fin))
         torch.cuda.synchronize()
         return
     if a.case == "w2":
