@@ -45,6 +45,7 @@ struct DecodeProblem {
   float *out_state;
   uint32_t *status;
   unsigned long long *bounds;  // debug-bounds record (see in_range)
+  int vec_in;  // q, k, v rows start on 16-byte boundaries (bases and strides): 16-byte input loads
 };
 
 __device__ __forceinline__ float load16(const void *base, int64_t i, int f16) {
@@ -104,21 +105,59 @@ __global__ void __launch_bounds__(kDecThreads) gdp_decode_kernel(DecodeProblem p
     }
     s[4 * gi] = x.x; s[4 * gi + 1] = x.y; s[4 * gi + 2] = x.z; s[4 * gi + 3] = x.w;
   }
-  // inputs of the token: k rows i*M + j, q row i, this block's v entries, beta, gate
-  for (int idx = tid; idx < (M + 1) * D; idx += kDecThreads) {
-    const int j = idx / D, c = idx % D;
-    float x;
-    if (j < M)
-      x = load16(p.k, ((int64_t)i * M + j) * p.k_st + (int64_t)hk * p.k_sh + c, p.f16);
-    else
-      x = load16(p.q, (int64_t)i * p.q_st + (int64_t)hq * p.q_sh + c, p.f16);
-    if (j < M) kf[j][c] = x; else qf[c] = x;
+  // inputs of the token: k rows i*M + j, q row i, this block's v entries, beta, gate -- every load
+  // issued before any is used (16-byte groups of 8 elements when the layout allows)
+  const float graw = p.g ? load_typed(p.g, (int64_t)i * p.H + h, p.g_type) : 0.f;
+  const float braw = (tid < M && p.beta) ? load_typed(p.beta, ((int64_t)i * M + tid) * p.H + h, p.beta_type) : 1.f;
+  if (p.vec_in) {
+    constexpr int GPR = D / 8;  // 8-element groups per row
+    const int ng = (M + 1) * GPR;
+    auto kq_src = [&](int gi) {
+      const int j = gi / GPR, c8 = (gi % GPR) * 8;
+      return j < M ? static_cast<const uint16_t *>(p.k) + ((int64_t)i * M + j) * p.k_st + (int64_t)hk * p.k_sh + c8
+                   : static_cast<const uint16_t *>(p.q) + (int64_t)i * p.q_st + (int64_t)hq * p.q_sh + c8;
+    };
+    uint4 raw[3], rv = make_uint4(0u, 0u, 0u, 0u);  // (M + 1) * GPR <= 17 * 16 = 272 groups
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+      const int gi = tid + u * kDecThreads;
+      raw[u] = gi < ng ? *reinterpret_cast<const uint4 *>(kq_src(gi)) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (tid < M * (kDecRows / 8))
+      rv = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.v) +
+                                            ((int64_t)i * M + tid / (kDecRows / 8)) * p.v_st + (int64_t)hv * p.v_sh +
+                                            blockIdx.z * kDecRows + (tid % (kDecRows / 8)) * 8);
+    auto widen8 = [&](const uint4 &x, float *o) {
+      const uint16_t *e = reinterpret_cast<const uint16_t *>(&x);
+#pragma unroll
+      for (int w = 0; w < 8; ++w)
+        o[w] = p.f16 ? __half2float(__ushort_as_half(e[w])) : __uint_as_float((uint32_t)e[w] << 16);
+    };
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+      const int gi = tid + u * kDecThreads;
+      if (gi < ng) {
+        const int j = gi / GPR, c8 = (gi % GPR) * 8;
+        widen8(raw[u], j < M ? &kf[j][c8] : &qf[c8]);
+      }
+    }
+    if (tid < M * (kDecRows / 8)) widen8(rv, &vv[tid / (kDecRows / 8)][(tid % (kDecRows / 8)) * 8]);
+  } else {
+    for (int idx = tid; idx < (M + 1) * D; idx += kDecThreads) {
+      const int j = idx / D, c = idx % D;
+      float x;
+      if (j < M)
+        x = load16(p.k, ((int64_t)i * M + j) * p.k_st + (int64_t)hk * p.k_sh + c, p.f16);
+      else
+        x = load16(p.q, (int64_t)i * p.q_st + (int64_t)hq * p.q_sh + c, p.f16);
+      if (j < M) kf[j][c] = x; else qf[c] = x;
+    }
+    for (int idx = tid; idx < M * kDecRows; idx += kDecThreads) {
+      const int j = idx / kDecRows, rr = idx % kDecRows;
+      vv[j][rr] = load16(p.v, ((int64_t)i * M + j) * p.v_st + (int64_t)hv * p.v_sh + blockIdx.z * kDecRows + rr, p.f16);
+    }
   }
-  for (int idx = tid; idx < M * kDecRows; idx += kDecThreads) {
-    const int j = idx / kDecRows, rr = idx % kDecRows;
-    vv[j][rr] = load16(p.v, ((int64_t)i * M + j) * p.v_st + (int64_t)hv * p.v_sh + blockIdx.z * kDecRows + rr, p.f16);
-  }
-  if (tid < M) bt[tid] = p.beta ? load_typed(p.beta, ((int64_t)i * M + tid) * p.H + h, p.beta_type) : 1.f;
+  if (tid < M) bt[tid] = braw;
   __syncthreads();
   if (p.l2norm) {  // one warp per vector: 1 / sqrt(sum x^2 + eps)
     const int warp = tid >> 5, lane = tid & 31;
@@ -140,10 +179,7 @@ __global__ void __launch_bounds__(kDecThreads) gdp_decode_kernel(DecodeProblem p
 
   // alpha_t = exp(g_t), or g_t itself for a linear-space gate (floored like the prefill's)
   float decay = 1.f;
-  if (p.g) {
-    const float x = load_typed(p.g, (int64_t)i * p.H + h, p.g_type);
-    decay = p.g_alpha ? fmaxf(x, __expf(kMinLogAlpha)) : __expf(x);
-  }
+  if (p.g) decay = p.g_alpha ? fmaxf(graw, __expf(kMinLogAlpha)) : __expf(graw);
 #pragma unroll
   for (int c = 0; c < 4 * G; ++c) s[c] *= decay;
   for (int j = 0; j < M; ++j) {
@@ -234,6 +270,8 @@ GDP_EXPORT gdp_status gdp_decode_step(const gdp_prefill_args *a, void *stream) {
   p.init = a->initial_state; p.cache = a->state; p.slots = a->state_indices; p.num_slots = a->num_slots;
   p.out = a->output; p.out_state = a->output_state; p.status = a->device_status;
   p.bounds = gdp::bounds_record();
+  p.vec_in = (((uintptr_t)a->q | (uintptr_t)a->k | (uintptr_t)a->v) & 15u) == 0 && p.q_st % 8 == 0 &&
+             p.q_sh % 8 == 0 && p.k_st % 8 == 0 && p.k_sh % 8 == 0 && p.v_st % 8 == 0 && p.v_sh % 8 == 0;
   dim3 grid((unsigned)N, (unsigned)H, (unsigned)(V / gdp::kDecRows));
   cudaStream_t s = (cudaStream_t)stream;
   if (K == 128)
