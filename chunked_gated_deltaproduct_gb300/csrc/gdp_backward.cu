@@ -712,7 +712,11 @@ cudaError_t launch_backward(const BwdProblem &p, cudaStream_t stream) {
   cudaError_t e;
   const int D = p.D, QP = p.qpad;
   if (p.N > 0 && (e = launch_bwd_tc_scan(p, stream)) != cudaSuccess) return e;
-  if (p.ntdp_pad > 0) {
+  // the tensor-core kernel addresses the state rows through TMA with 32-bit coordinates
+  const bool tc = bwd_chunk_tc_serves(D, QP) && p.ntdp_pad * (int64_t)p.H * D < ((int64_t)1 << 31);
+  if (p.ntdp_pad > 0 && tc) {
+    if ((e = launch_bwd_chunk_tc(p, stream)) != cudaSuccess) return e;
+  } else if (p.ntdp_pad > 0) {
     const int vsl = chunk_slice(D, QP);
     if (D == 128)
       e = vsl == 16 ? launch_chunk<128, 16>(p, stream) : launch_chunk<128, 8>(p, stream);
