@@ -57,7 +57,7 @@ __device__ __forceinline__ uint32_t toff(uint32_t rows, int r, int c) {
 // rows read the rows past the valid ones from the region that follows (their accumulator lanes are
 // never read).
 struct CtLayout {
-  uint32_t rkq, kq, tt, lp, pt, b1, dot, b2, b3, dl, fb, fq, gb, dqb, stk, stq, total;
+  uint32_t rkq, kq, tt, lp, pt, b1, dot, b2, b3, dl, fb, fq, raw5, gb, dqb, stk, stq, total;
   static constexpr uint32_t kB1 = 4u * 64u * 128u;  // one slice buffer
   __host__ __device__ uint32_t b1s(int s) const { return b1 + (uint32_t)(s & 1) * kB1; }
   __host__ __device__ CtLayout(int qp) {
@@ -79,15 +79,26 @@ struct CtLayout {
     b2 = take(2u * 64u * 128u);  // [beta rhs^T; Zt^T] rows n, K = 64
     b3 = b2;                     //   then vt_s^T rows v, K = 64
     dl = b2 + 2u * 32u * 128u;   //   and Delta_s [64][32] (16-byte chunks swizzled by row)
-    fq = b2;                     //   at the end scale M4 rows p, K = 64
+    fq = b2 + 2u * 32u * 128u;   //   at the end scale M4 rows p, K = 64 (after the Gram staging)
     gb = take(rkq * 128u);       // [dv_s; dO_s], K = VS
     dqb = take((uint32_t)qp * 128u);  // scale gamma_p dO_s rows p, K = VS
+    raw5 = b1 + 3u * 64u * 128u; // the Gram sums as they leave TMEM, [128][kRawLd] (after fb)
     stk = b1;                    // the last staging: dkhat [64][132], dqhat [qpad][132]
     stq = b1 + 64u * 132u * 4u;
     total = o;
   }
 };
 constexpr int kStLd = 132;  // row stride of the staging rows (floats)
+constexpr int kRawLd = 100; // row stride of the raw Gram-sum staging (floats)
+constexpr int kRaw0Ld = 68; // row stride of the raw [L; P] staging (floats)
+
+// Round to the nearest tf32 value (the tensor cores would otherwise drop the low mantissa bits).
+__device__ __forceinline__ float tf32r(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+__device__ __forceinline__ float4 tf32r4(float4 x) { return make_float4(tf32r(x.x), tf32r(x.y), tf32r(x.z), tf32r(x.w)); }
 
 __device__ __forceinline__ void unpack8(const uint4 &u, float *x) {
   const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&u);
@@ -246,18 +257,19 @@ __global__ void __launch_bounds__(kCtThreads, 1)
 #pragma unroll
       for (int i = 0; i < 4; ++i)
         *reinterpret_cast<float4 *>(sm + lay.kq + toff(RKQ, r, part * 16 + 4 * i)) =
-            make_float4(x[4 * i] * inv, x[4 * i + 1] * inv, x[4 * i + 2] * inv, x[4 * i + 3] * inv);
+            tf32r4(make_float4(x[4 * i] * inv, x[4 * i + 1] * inv, x[4 * i + 2] * inv, x[4 * i + 3] * inv));
     }
   }
   // ---- [T; T^T] ----
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int idx = tid + kCtThreads * i, r = idx >> 4, c4 = (idx & 15) * 4;
-    *reinterpret_cast<float4 *>(sm + lay.tt + toff(128, r, c4)) = tr[i];
-    *at(lay.tt + toff(128, 64 + c4, r)) = tr[i].x;
-    *at(lay.tt + toff(128, 64 + c4 + 1, r)) = tr[i].y;
-    *at(lay.tt + toff(128, 64 + c4 + 2, r)) = tr[i].z;
-    *at(lay.tt + toff(128, 64 + c4 + 3, r)) = tr[i].w;
+    const float4 x = tf32r4(tr[i]);
+    *reinterpret_cast<float4 *>(sm + lay.tt + toff(128, r, c4)) = x;
+    *at(lay.tt + toff(128, 64 + c4, r)) = x.x;
+    *at(lay.tt + toff(128, 64 + c4 + 1, r)) = x.y;
+    *at(lay.tt + toff(128, 64 + c4 + 2, r)) = x.z;
+    *at(lay.tt + toff(128, 64 + c4 + 3, r)) = x.w;
   }
   // ---- slice 0's dO_s^T ----
   auto put_dot = [&](const uint2 &u) {
@@ -297,15 +309,18 @@ __global__ void __launch_bounds__(kCtThreads, 1)
   // brows rows), or A from TMEM columns
   auto mma_ss = [&](uint32_t tD, uint32_t a, uint32_t arows, uint32_t b, uint32_t brows, int ks, uint32_t id,
                     bool acc) {
+    // (the descriptors' start-address field is the byte address / 16: a K step adds its offset / 16)
+    const uint64_t da0 = desc_sw128(sb + a, 16, 1024), db0 = desc_sw128(sb + b, 16, 1024);
     for (int kk = 0; kk < ks; ++kk) {
-      const uint64_t da = desc_sw128(sb + a + (uint32_t)(kk >> 2) * arows * 128u + (uint32_t)(kk & 3) * 32u, 16, 1024);
-      const uint64_t db = desc_sw128(sb + b + (uint32_t)(kk >> 2) * brows * 128u + (uint32_t)(kk & 3) * 32u, 16, 1024);
+      const uint64_t da = da0 + (((uint32_t)(kk >> 2) * arows * 128u + (uint32_t)(kk & 3) * 32u) >> 4);
+      const uint64_t db = db0 + (((uint32_t)(kk >> 2) * brows * 128u + (uint32_t)(kk & 3) * 32u) >> 4);
       mma_tf32_ss(tb + tD, da, db, id, (acc || kk > 0) ? 1u : 0u);
     }
   };
   auto mma_ts = [&](uint32_t tD, uint32_t ta, uint32_t b, uint32_t brows, int ks, uint32_t id, bool acc) {
+    const uint64_t db0 = desc_sw128(sb + b, 16, 1024);
     for (int kk = 0; kk < ks; ++kk) {
-      const uint64_t db = desc_sw128(sb + b + (uint32_t)(kk >> 2) * brows * 128u + (uint32_t)(kk & 3) * 32u, 16, 1024);
+      const uint64_t db = db0 + (((uint32_t)(kk >> 2) * brows * 128u + (uint32_t)(kk & 3) * 32u) >> 4);
       mma_tf32_ts(tb + tD, tb + ta + (uint32_t)kk * 8u, db, id, (acc || kk > 0) ? 1u : 0u);
     }
   };
@@ -341,36 +356,39 @@ __global__ void __launch_bounds__(kCtThreads, 1)
     mma_commit(&bar);
   }
   wait_mma();
-  if (q4 < 3) {
-    float a[32];
-    tmem_ld32x(lanes + tA1 + 32 * hh, a);
-    if (m < 64) {
-      const int r = m;
+  // the raw products go through shared memory (b2 .. dqb, free until the first slice), so that the
+  // masks and decays run as short element loops: this code runs once per CTA and is kept small
+  {
+    float *raw = at(lay.b2);  // [64 + qpad][kRaw0Ld]
+    if (q4 < 3) {
+      float a[32];
+      tmem_ld32x(lanes + tA1 + 32 * hh, a);
+      if (m < 64 + QP) {
 #pragma unroll
-      for (int j4 = 0; j4 < 32; j4 += 4) {
-        float o4[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int j = 32 * hh + j4 + i;
-          o4[i] = (j < r) ? expf(sG[r] - sG[j]) * a[j4 + i] : 0.f;
-        }
-        *reinterpret_cast<float4 *>(sm + lay.lp + toff(RKQ, r, 32 * hh + j4)) = make_float4(o4[0], o4[1], o4[2], o4[3]);
+        for (int j4 = 0; j4 < 32; j4 += 4)
+          *reinterpret_cast<float4 *>(raw + m * kRaw0Ld + 32 * hh + j4) = make_float4(a[j4], a[j4 + 1], a[j4 + 2], a[j4 + 3]);
       }
-    } else if (m < 64 + QP) {
-      const int qi = m - 64;
-      const bool live = qi < nq;
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int idx = tid; idx < (64 + QP) * 16; idx += kCtThreads) {
+      const int mr = idx >> 4, j0 = (idx & 15) * 4;
+      const bool isl = mr < 64;
+      const int qi = mr - 64;
+      const bool live = !isl && qi < nq;
       const int pq = live ? pr(qi) : 0;
+      const float gref = isl ? sG[mr] : sG[pq], sc = isl ? 1.f : scale;
+      const float4 x = *reinterpret_cast<const float4 *>(raw + mr * kRaw0Ld + j0);
+      const float xv[4] = {x.x, x.y, x.z, x.w};
+      float o4[4];
 #pragma unroll
-      for (int j4 = 0; j4 < 32; j4 += 4) {
-        float o4[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int j = 32 * hh + j4 + i;
-          o4[i] = (live && j <= pq) ? scale * expf(sG[pq] - sG[j]) * a[j4 + i] : 0.f;
-          *at(lay.pt + toff(64, j, qi)) = o4[i];
-        }
-        *reinterpret_cast<float4 *>(sm + lay.lp + toff(RKQ, m, 32 * hh + j4)) = make_float4(o4[0], o4[1], o4[2], o4[3]);
+      for (int i = 0; i < 4; ++i) {
+        const int j = j0 + i;
+        const bool on = isl ? j < mr : (live && j <= pq);
+        o4[i] = on ? tf32r(sc * expf(gref - sG[j]) * xv[i]) : 0.f;
+        if (!isl) *at(lay.pt + toff(64, j, qi)) = o4[i];
       }
+      *reinterpret_cast<float4 *>(sm + lay.lp + toff(RKQ, mr, j0)) = make_float4(o4[0], o4[1], o4[2], o4[3]);
     }
   }
   to_mma();
@@ -398,14 +416,15 @@ __global__ void __launch_bounds__(kCtThreads, 1)
     {
       float x[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) x[i] = *at(b1 + toff(64, (hh ? 0 : 32) + i, m));
+      for (int i = 0; i < 32; ++i) x[i] = tf32r(*at(b1 + toff(64, (hh ? 0 : 32) + i, m)));
       tmem_st32x(lanes + tAT + 32 * hh, x);
     }
     if (dp < QP) {
       const float4 x = unpack4(do_cur);
       *reinterpret_cast<float4 *>(sm + lay.gb + toff(RKQ, 64 + dp, dv4)) = x;
       const float gq = sgq[dp];
-      *reinterpret_cast<float4 *>(sm + lay.dqb + toff(QP, dp, dv4)) = make_float4(gq * x.x, gq * x.y, gq * x.z, gq * x.w);
+      *reinterpret_cast<float4 *>(sm + lay.dqb + toff(QP, dp, dv4)) =
+          tf32r4(make_float4(gq * x.x, gq * x.y, gq * x.z, gq * x.w));
     }
     // ---- rhs = v - gamma Khat S^T, Zt = fc Khat D_C^T + P^T dO into [beta rhs^T; Zt^T] ----
     if (q4 < 2) {
@@ -422,8 +441,8 @@ __global__ void __launch_bounds__(kCtThreads, 1)
       for (int i = 0; i < 16; ++i) {
         rhs[i] = vin[i] - gm * __uint_as_float(sa[i]);
         const int n = 16 * hh + i;
-        *at(lay.b2 + toff(64, n, r)) = b * rhs[i];
-        *at(lay.b2 + toff(64, 32 + n, r)) = f * __uint_as_float(za[i]) + __uint_as_float(zp[i]);
+        *at(lay.b2 + toff(64, n, r)) = tf32r(b * rhs[i]);
+        *at(lay.b2 + toff(64, 32 + n, r)) = tf32r(f * __uint_as_float(za[i]) + __uint_as_float(zp[i]));
       }
     }
     // ---- batch 2: [vt | Delta] = [T; T^T] [beta rhs^T; Zt^T]^T ----
@@ -438,6 +457,8 @@ __global__ void __launch_bounds__(kCtThreads, 1)
       const int r = m;
       float vt[16];
       tmem_ld16(lanes + tA2 + 16 * hh, vt);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) vt[i] = tf32r(vt[i]);
 #pragma unroll
       for (int i = 0; i < 16; ++i) *at(lay.b3 + toff(32, 16 * hh + i, r)) = vt[i];
 #pragma unroll
@@ -455,9 +476,9 @@ __global__ void __launch_bounds__(kCtThreads, 1)
         const float4 x = make_float4(dl[i], dl[i + 1], dl[i + 2], dl[i + 3]);
         const float4 bx = make_float4(b * x.x, b * x.y, b * x.z, b * x.w);
         if (r < len) *reinterpret_cast<float4 *>(dvo + i) = bx;
-        *reinterpret_cast<float4 *>(sm + lay.gb + toff(RKQ, r, 16 * hh + i)) = bx;
+        *reinterpret_cast<float4 *>(sm + lay.gb + toff(RKQ, r, 16 * hh + i)) = tf32r4(bx);
         *reinterpret_cast<float4 *>(sm + dkb + toff(64, r, 32 + 16 * hh + i)) =
-            make_float4(mg * x.x, mg * x.y, mg * x.z, mg * x.w);
+            tf32r4(make_float4(mg * x.x, mg * x.y, mg * x.z, mg * x.w));
         const int ch = ((4 * hh + (i >> 2)) ^ (r & 7));
         *reinterpret_cast<float4 *>(sm + lay.dl + (uint32_t)r * 128u + (uint32_t)ch * 16u) = x;
       }
@@ -479,9 +500,9 @@ __global__ void __launch_bounds__(kCtThreads, 1)
       for (int i = 0; i < 16; i += 4) {
         const float4 e = make_float4(rhs[i] - lv[i], rhs[i + 1] - lv[i + 1], rhs[i + 2] - lv[i + 2],
                                      rhs[i + 3] - lv[i + 3]);
-        *reinterpret_cast<float4 *>(sm + ga + toff(128, r, 16 * hh + i)) = e;
+        *reinterpret_cast<float4 *>(sm + ga + toff(128, r, 16 * hh + i)) = tf32r4(e);
         *reinterpret_cast<float4 *>(sm + dkb + toff(64, r, 16 * hh + i)) =
-            make_float4(bf * e.x, bf * e.y, bf * e.z, bf * e.w);
+            tf32r4(make_float4(bf * e.x, bf * e.y, bf * e.z, bf * e.w));
         const int ch = ((4 * hh + (i >> 2)) ^ (r & 7));
         const float4 x = *reinterpret_cast<const float4 *>(sm + lay.dl + (uint32_t)r * 128u + (uint32_t)ch * 16u);
         sdb_acc += e.x * x.x + e.y * x.y + e.z * x.z + e.w * x.w;
@@ -525,57 +546,61 @@ __global__ void __launch_bounds__(kCtThreads, 1)
 
   // ---- masks and decays of the Gram sums into the last batch's B tiles; [Qhat^T | Khat^T] into
   // TMEM as its A operand ----
-  if (q4 < 2) {
-    const int r = m;
-    float g2[32];
-    tmem_ld32x(lanes + tGr + 32 * hh, g2);
-    const float b = sbt[r];
+  {
+    float *raw = at(lay.raw5);  // [128][kRawLd]: rows e (0-63) and vt (64-127) of the Gram sums
+    {
+      float a[32];
+      tmem_ld32x(lanes + tGr + 32 * hh, a);
 #pragma unroll
-    for (int jj = 0; jj < 32; ++jj) {
-      const int j = 32 * hh + jj;
-      if (j >= r) *at(lay.fb + toff(64, r, QP + j)) = (j > r) ? -(b * expf(sG[j] - sG[r]) * g2[jj]) : 0.f;
-    }
-    if (hh == 0) {
-      float g1[32];
-      tmem_ld32x(lanes + tGr + 64, g1);  // columns past 64 + qpad are not used
+      for (int j4 = 0; j4 < 32; j4 += 4)
+        *reinterpret_cast<float4 *>(raw + m * kRawLd + 32 * hh + j4) = make_float4(a[j4], a[j4 + 1], a[j4 + 2], a[j4 + 3]);
+      if (hh == 0) {
+        tmem_ld32x(lanes + tGr + 64, a);  // columns past 64 + qpad are not used
 #pragma unroll
-      for (int qi = 0; qi < 32; ++qi) {
-        if (qi >= QP) break;
-        const bool live = qi < nq && r <= pr(qi);
-        *at(lay.fb + toff(64, r, qi)) = live ? b * scale * expf(sG[pr(qi)] - sG[r]) * g1[qi] : 0.f;
+        for (int j4 = 0; j4 < 32; j4 += 4)
+          *reinterpret_cast<float4 *>(raw + m * kRawLd + 64 + j4) = make_float4(a[j4], a[j4 + 1], a[j4 + 2], a[j4 + 3]);
       }
     }
-  } else {
-    const int j = m - 64;
-    float g3[32];
-    tmem_ld32x(lanes + tGr + 32 * hh, g3);
-#pragma unroll
-    for (int rr = 0; rr < 32; ++rr) {
-      const int r = 32 * hh + rr;
-      if (r > j) *at(lay.fb + toff(64, r, QP + j)) = -(expf(sG[r] - sG[j]) * g3[rr]);
-    }
-    if (hh == 0) {
-      float g4[32];
-      tmem_ld32x(lanes + tGr + 64, g4);
-#pragma unroll
-      for (int qi = 0; qi < 32; ++qi) {
-        if (qi >= QP) break;
-        const bool live = qi < nq && j <= pr(qi);
-        *at(lay.fq + toff(QP, qi, j)) = live ? scale * expf(sG[pr(qi)] - sG[j]) * g4[qi] : 0.f;
+    __syncthreads();
+    // [beta M1 | -M23] rows r: beta_r M1 (readouts), -beta_r M2 (j > r, from e . dv), -M3 (j < r,
+    // from vt_j . dv_r)
+    const int W = QP + 64;
+#pragma unroll 1
+    for (int idx = tid; idx < 64 * W; idx += kCtThreads) {
+      const int r = idx / W, pos = idx - r * W;
+      float val;
+      if (pos < QP) {
+        const bool live = pos < nq && r <= pr(pos);
+        val = live ? sbt[r] * scale * expf(sG[pr(pos)] - sG[r]) * raw[r * kRawLd + 64 + pos] : 0.f;
+      } else {
+        const int j = pos - QP;
+        val = (j > r)   ? -(sbt[r] * expf(sG[j] - sG[r]) * raw[r * kRawLd + j])
+              : (j < r) ? -(expf(sG[r] - sG[j]) * raw[(64 + j) * kRawLd + r])
+                        : 0.f;
       }
+      *at(lay.fb + toff(64, r, pos)) = tf32r(val);
+    }
+    // scale M4 rows p (from vt_j . dO_p)
+#pragma unroll 1
+    for (int idx = tid; idx < QP * 64; idx += kCtThreads) {
+      const int qi = idx >> 6, j = idx & 63;
+      const bool live = qi < nq && j <= pr(qi);
+      *at(lay.fq + toff(QP, qi, j)) =
+          live ? tf32r(scale * expf(sG[pr(qi)] - sG[j]) * raw[(64 + j) * kRawLd + 64 + qi]) : 0.f;
     }
   }
+  // [Qhat^T | Khat^T]: 16 columns at a time (hh = 0: Qhat^T then Khat rows 0-31; hh = 1: rows 32-63)
   {
-    float x[32];
-    if (hh == 0) {  // Qhat^T at columns 0 .. qpad - 1
+    const int ng = (hh == 0 ? QP : 0) / 16 + 2;
+#pragma unroll 1
+    for (int gi = 0; gi < ng; ++gi) {
+      const int col = (hh == 0) ? 16 * gi : QP + 32 + 16 * gi;   // TMEM column
+      const int src = (hh == 0) ? (gi < QP / 16 ? 64 + 16 * gi : 16 * gi - QP) : 32 + 16 * gi;  // KQ row
+      float x[16];
 #pragma unroll
-      for (int qi = 0; qi < 32; ++qi) x[qi] = (qi < QP) ? *at(lay.kq + toff(RKQ, 64 + qi, m)) : 0.f;
-      tmem_st16(lanes + tAT, x);
-      if (QP > 16) tmem_st16(lanes + tAT + 16, x + 16);
+      for (int i = 0; i < 16; ++i) x[i] = *at(lay.kq + toff(RKQ, src + i, m));
+      tmem_st16(lanes + tAT + col, x);
     }
-#pragma unroll
-    for (int jj = 0; jj < 32; ++jj) x[jj] = *at(lay.kq + toff(RKQ, 32 * hh + jj, m));
-    tmem_st32x(lanes + tAT + QP + 32 * hh, x);  // Khat^T at columns qpad ..
   }
   // ---- last batch: dkhat^T += [Qhat^T | Khat^T] [beta M1 | -M23]^T, dqhat^T += Khat^T (M4)^T ----
   to_mma();
@@ -586,16 +611,20 @@ __global__ void __launch_bounds__(kCtThreads, 1)
     mma_commit(&bar);
   }
   wait_mma();
-  {
-    float a[32];
-    tmem_ld32x(lanes + tDK + 32 * hh, a);
+#pragma unroll 1
+  for (int r4 = 0; r4 < 32; r4 += 4) {
+    float a[4];
+    tmem_ld4(lanes + tDK + 32 * hh + r4, a);
 #pragma unroll
-    for (int rr = 0; rr < 32; ++rr) at(lay.stk)[(32 * hh + rr) * kStLd + m] = a[rr];
-    if (hh == 0) {
-      tmem_ld32x(lanes + tDQ, a);  // columns past qpad are not used
+    for (int i = 0; i < 4; ++i) at(lay.stk)[(32 * hh + r4 + i) * kStLd + m] = a[i];
+  }
+  if (hh == 0) {
+#pragma unroll 1
+    for (int q0 = 0; q0 < QP; q0 += 4) {
+      float a[4];
+      tmem_ld4(lanes + tDQ + q0, a);
 #pragma unroll
-      for (int qi = 0; qi < 32; ++qi)
-        if (qi < QP) at(lay.stq)[qi * kStLd + m] = a[qi];
+      for (int i = 0; i < 4; ++i) at(lay.stq)[(q0 + i) * kStLd + m] = a[i];
     }
   }
   if (q4 < 2) {
@@ -606,24 +635,28 @@ __global__ void __launch_bounds__(kCtThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  // ---- L2-norm chain rule (dx = rx (dxhat - (xhat . dxhat) xhat)), stores, row sums ----
+  // ---- L2-norm chain rule (dx = rx (dxhat - (xhat . dxhat) xhat), xhat from the input row in full
+  // precision), stores, row sums ----
   for (int r = warp; r < len + nq; r += kCtThreads / 32) {
     const bool isk = r < len;
     const int rr = isk ? r : r - len;
     const float *dh = at(isk ? lay.stk : lay.stq) + rr * kStLd;
-    const int xr = isk ? rr : 64 + rr;
-    float a[4], xv[4], dot = 0.f;
+    float a[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      a[i] = dh[lane + 32 * i];
-      xv[i] = *at(lay.kq + toff(RKQ, xr, lane + 32 * i));
-      dot += a[i] * xv[i];
-    }
+    for (int i = 0; i < 4; ++i) a[i] = dh[lane + 32 * i];
     float *out = isk ? p.dk + ((R0 + rr) * H + h) * (int64_t)kCtD : p.dq + ((tq0 + rr) * H + h) * (int64_t)kCtD;
     if (p.l2norm) {
+      const __nv_bfloat16 *src = isk ? p.k + (R0 + rr) * p.k_st + (int64_t)h * p.k_sh
+                                     : p.q + (tq0 + rr) * p.q_st + (int64_t)h * p.q_sh;
+      const float rx = (isk ? srk : srq)[rr];
+      float xv[4], dot = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        xv[i] = __bfloat162float(src[lane + 32 * i]) * rx;
+        dot += a[i] * xv[i];
+      }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-      const float rx = (isk ? srk : srq)[rr];
 #pragma unroll
       for (int i = 0; i < 4; ++i) out[lane + 32 * i] = rx * (a[i] - dot * xv[i]);
     } else {

@@ -115,6 +115,27 @@ def test_backward_parity(cuda_device, case):
     _compare(w, cuda_device, d_out, d_fin)
 
 
+# The per-chunk gradients run on the tensor cores for head size 128 with at most 32 readout rows per
+# expanded chunk (two or more updates per token) and on warp-level MMAs otherwise; both kernels
+# against the oracle at the shapes that pick them.
+PATH_CASES = {
+    "warp_mma_d128_m1": (dict(lengths=[130, 64, 7], H=2, d=128, M=1, init_sigma=0.1), 201),
+    "tensor_core_qpad16_m5_l2norm": (dict(lengths=[77, 30, 150], H=2, d=128, M=5, normalised=False,
+                                          use_qk_l2norm=True, init_sigma=0.1), 202),
+    "tensor_core_single_chunks": (dict(lengths=[1, 31, 32, 33], H=3, d=128, M=2, init_sigma=0.1), 203),
+}
+
+
+@pytest.mark.parametrize("case", sorted(PATH_CASES))
+def test_backward_kernel_paths(cuda_device, case):
+    kw, seed = PATH_CASES[case]
+    kw = dict(kw)
+    lengths = kw.pop("lengths")
+    w = make_custom(lengths, kw.pop("H"), kw.pop("d"), kw.pop("M"), seed=seed, **kw)
+    d_out, d_fin = make_cotangents(w, seed=seed + 1, dfin_sigma=0.5)
+    _compare(w, cuda_device, d_out, d_fin)
+
+
 def test_backward_without_final_state_gradient(cuda_device):
     w = make_custom([120, 33], 2, 128, 2, seed=5, init_sigma=0.1)
     d_out, _ = make_cotangents(w, seed=8, d_final_state=False)
