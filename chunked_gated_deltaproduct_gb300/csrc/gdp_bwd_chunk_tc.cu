@@ -140,7 +140,9 @@ __global__ void __launch_bounds__(kCtThreads, 1)
   const uint32_t RKQ = lay.rkq;
 
   extern __shared__ __align__(1024) unsigned char ct_raw[];
-  unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)ct_raw + 1023) & ~(uintptr_t)1023);
+  // the 1024-aligned base as an offset into the shared array (a pointer rebuilt from an integer
+  // would lose its address space and turn every access below into a generic one)
+  unsigned char *sm = ct_raw + ((1024u - (smem_u32(ct_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(sm);
   auto at = [&](uint32_t off) { return reinterpret_cast<float *>(sm + off); };
   __shared__ float sG[64], sbt[64], sgm[64], sfc[64], sbfc[64], smgb[64], srk[64], sgq[32], srq[32];
@@ -356,8 +358,8 @@ __global__ void __launch_bounds__(kCtThreads, 1)
     mma_commit(&bar);
   }
   wait_mma();
-  // the raw products go through shared memory (b2 .. dqb, free until the first slice), so that the
-  // masks and decays run as short element loops: this code runs once per CTA and is kept small
+  // the raw products go through shared memory (b2 .. dqb, free until the first slice); the masks and
+  // decays then run with each thread on a fixed row
   {
     float *raw = at(lay.b2);  // [64 + qpad][kRaw0Ld]
     if (q4 < 3) {
@@ -370,25 +372,38 @@ __global__ void __launch_bounds__(kCtThreads, 1)
       }
     }
     __syncthreads();
-#pragma unroll 1
-    for (int idx = tid; idx < (64 + QP) * 16; idx += kCtThreads) {
-      const int mr = idx >> 4, j0 = (idx & 15) * 4;
-      const bool isl = mr < 64;
-      const int qi = mr - 64;
-      const bool live = !isl && qi < nq;
-      const int pq = live ? pr(qi) : 0;
-      const float gref = isl ? sG[mr] : sG[pq], sc = isl ? 1.f : scale;
-      const float4 x = *reinterpret_cast<const float4 *>(raw + mr * kRaw0Ld + j0);
-      const float xv[4] = {x.x, x.y, x.z, x.w};
-      float o4[4];
+    {  // L: row tid / 4, columns 16 (tid % 4) .. + 15
+      const int r = tid >> 2, c0 = 16 * (tid & 3);
+      const float gr = sG[r];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int j = j0 + i;
-        const bool on = isl ? j < mr : (live && j <= pq);
-        o4[i] = on ? tf32r(sc * expf(gref - sG[j]) * xv[i]) : 0.f;
-        if (!isl) *at(lay.pt + toff(64, j, qi)) = o4[i];
+      for (int g = 0; g < 4; ++g) {
+        const int j0 = c0 + 4 * g;
+        const float4 x = *reinterpret_cast<const float4 *>(raw + r * kRaw0Ld + j0);
+        const float xv[4] = {x.x, x.y, x.z, x.w};
+        float o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = (j0 + i < r) ? tf32r(expf(gr - sG[j0 + i]) * xv[i]) : 0.f;
+        *reinterpret_cast<float4 *>(sm + lay.lp + toff(RKQ, r, j0)) = make_float4(o[0], o[1], o[2], o[3]);
       }
-      *reinterpret_cast<float4 *>(sm + lay.lp + toff(RKQ, mr, j0)) = make_float4(o4[0], o4[1], o4[2], o4[3]);
+    }
+    if ((tid >> 3) < QP) {  // P (and P^T): row tid / 8, columns 8 (tid % 8) .. + 7
+      const int qi = tid >> 3;
+      const bool live = qi < nq;
+      const int pq = live ? pr(qi) : 0;
+      const float gq = sG[pq];
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        const int j0 = 8 * (tid & 7) + 4 * g;
+        const float4 x = *reinterpret_cast<const float4 *>(raw + (64 + qi) * kRaw0Ld + j0);
+        const float xv[4] = {x.x, x.y, x.z, x.w};
+        float o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          o[i] = (live && j0 + i <= pq) ? tf32r(scale * expf(gq - sG[j0 + i]) * xv[i]) : 0.f;
+          *at(lay.pt + toff(64, j0 + i, qi)) = o[i];
+        }
+        *reinterpret_cast<float4 *>(sm + lay.lp + toff(RKQ, 64 + qi, j0)) = make_float4(o[0], o[1], o[2], o[3]);
+      }
     }
   }
   to_mma();
@@ -563,30 +578,51 @@ __global__ void __launch_bounds__(kCtThreads, 1)
     }
     __syncthreads();
     // [beta M1 | -M23] rows r: beta_r M1 (readouts), -beta_r M2 (j > r, from e . dv), -M3 (j < r,
-    // from vt_j . dv_r)
-    const int W = QP + 64;
-#pragma unroll 1
-    for (int idx = tid; idx < 64 * W; idx += kCtThreads) {
-      const int r = idx / W, pos = idx - r * W;
-      float val;
-      if (pos < QP) {
-        const bool live = pos < nq && r <= pr(pos);
-        val = live ? sbt[r] * scale * expf(sG[pr(pos)] - sG[r]) * raw[r * kRawLd + 64 + pos] : 0.f;
-      } else {
-        const int j = pos - QP;
-        val = (j > r)   ? -(sbt[r] * expf(sG[j] - sG[r]) * raw[r * kRawLd + j])
-              : (j < r) ? -(expf(sG[r] - sG[j]) * raw[(64 + j) * kRawLd + r])
-                        : 0.f;
+    // from vt_j . dv_r); groups of 4 columns (qpad is a multiple of 16: a group lies in one part)
+    {  // row tid / 4; 16-column blocks of [M1 | M23], 4 columns each (qpad is a multiple of 16)
+      const int r = tid >> 2, sub = tid & 3;
+      const float b = sbt[r], gr = sG[r];
+#pragma unroll
+      for (int k = 0; k < 6; ++k) {
+        if (16 * k >= QP + 64) break;
+        const int pos0 = 16 * k + 4 * sub;
+        float o[4];
+        if (16 * k < QP) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int qi = pos0 + i;
+            const bool live = qi < nq && r <= pr(qi);
+            o[i] = live ? tf32r(b * scale * expf(sG[live ? pr(qi) : 0] - gr) * raw[r * kRawLd + 64 + qi]) : 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int j = pos0 - QP + i;
+            const float gj = sG[j];
+            o[i] = (j > r)   ? tf32r(-(b * expf(gj - gr) * raw[r * kRawLd + j]))
+                   : (j < r) ? tf32r(-(expf(gr - gj) * raw[(64 + j) * kRawLd + r]))
+                             : 0.f;
+          }
+        }
+        *reinterpret_cast<float4 *>(sm + lay.fb + toff(64, r, pos0)) = make_float4(o[0], o[1], o[2], o[3]);
       }
-      *at(lay.fb + toff(64, r, pos)) = tf32r(val);
     }
-    // scale M4 rows p (from vt_j . dO_p)
-#pragma unroll 1
-    for (int idx = tid; idx < QP * 64; idx += kCtThreads) {
-      const int qi = idx >> 6, j = idx & 63;
-      const bool live = qi < nq && j <= pr(qi);
-      *at(lay.fq + toff(QP, qi, j)) =
-          live ? tf32r(scale * expf(sG[pr(qi)] - sG[j]) * raw[(64 + j) * kRawLd + 64 + qi]) : 0.f;
+    if ((tid >> 3) < QP) {  // scale M4 (from vt_j . dO_p): row tid / 8, columns 8 (tid % 8) .. + 7
+      const int qi = tid >> 3;
+      const bool qlive = qi < nq;
+      const int pq = qlive ? pr(qi) : 0;
+      const float gq = sG[pq];
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        const int j0 = 8 * (tid & 7) + 4 * g;
+        float o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int j = j0 + i;
+          o[i] = (qlive && j <= pq) ? tf32r(scale * expf(gq - sG[j]) * raw[(64 + j) * kRawLd + 64 + qi]) : 0.f;
+        }
+        *reinterpret_cast<float4 *>(sm + lay.fq + toff(QP, qi, j0)) = make_float4(o[0], o[1], o[2], o[3]);
+      }
     }
   }
   // [Qhat^T | Khat^T]: 16 columns at a time (hh = 0: Qhat^T then Khat rows 0-31; hh = 1: rows 32-63)
