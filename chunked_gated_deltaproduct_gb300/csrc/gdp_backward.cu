@@ -38,6 +38,11 @@
 #include "gdp_sm100.cuh"
 
 namespace gdp {
+
+// The per-chunk gradients on the tensor cores (gdp_bwd_chunk_tc.cu) for the shapes it serves.
+bool bwd_chunk_tc_serves(int d, int qpad);
+cudaError_t launch_bwd_chunk_tc(const BwdProblem &p, cudaStream_t stream);
+
 namespace {
 
 using namespace sm100;

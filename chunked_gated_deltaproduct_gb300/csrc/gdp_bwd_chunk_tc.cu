@@ -92,6 +92,17 @@ constexpr int kStLd = 132;  // row stride of the staging rows (floats)
 constexpr int kRawLd = 100; // row stride of the raw Gram-sum staging (floats)
 constexpr int kRaw0Ld = 68; // row stride of the raw [L; P] staging (floats)
 
+// 32 lanes x 32 bit, 4 consecutive columns per thread (thread i of the warp <-> lane 32*(warp%4)+i).
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float *v) {
+  uint32_t r[4];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // Round to the nearest tf32 value (the tensor cores would otherwise drop the low mantissa bits).
 __device__ __forceinline__ float tf32r(float x) {
   uint32_t r;

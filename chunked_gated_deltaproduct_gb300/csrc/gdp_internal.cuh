@@ -232,9 +232,6 @@ cudaError_t launch_backward(const BwdProblem &p, cudaStream_t stream);
 // per-tile backward images (BwdImageLayout, with the inverse, rounded to 1 KB).
 cudaError_t launch_bwd_tc_scan(const BwdProblem &p, cudaStream_t stream);
 size_t bwd_image_stride(int d, int qpad);
-// The per-chunk gradients on the tensor cores (gdp_bwd_chunk_tc.cu) for the shapes it serves.
-bool bwd_chunk_tc_serves(int d, int qpad);
-cudaError_t launch_bwd_chunk_tc(const BwdProblem &p, cudaStream_t stream);
 
 // Launch `kern` on `stream`, with programmatic stream serialization when `pdl`.
 template <typename... Params, typename... Args>

@@ -75,17 +75,7 @@ __device__ __forceinline__ void tmem_free(uint32_t base, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(ncols));
 }
 
-// 32 lanes x 32 bit, 4 consecutive columns per thread (thread i of the warp <-> lane 32*(warp%4)+i).
-__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float *v) {
-  uint32_t r[4];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
-}
-// As tmem_ld4 with 16 consecutive columns per thread.
+// 32 lanes x 32 bit, 16 consecutive columns per thread (thread i of the warp <-> lane 32*(warp%4)+i).
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
   uint32_t r[16];
   asm volatile(
