@@ -55,13 +55,13 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     # the 65536-token sequence: its segmented stage runs 16 scan launches of 128 expanded chunks x
     # 32 heads and 15 WY segments of 4096 tiles beside them.  Captured on the 12288-token cut of
-    # the same shape (profile_case w4): one middle-segment scan launch, 506176000 + 146059776 B,
-    # and one WY segment, 171744512 + 442974976 B (both launches cover exactly one full segment).
+    # the same shape (profile_case w4): one middle-segment scan launch, 506071808 + 145328896 B,
+    # and one WY segment, 171891200 + 443047168 B (both launches cover exactly one full segment).
     ("gdp_scan_kernel x16 (segmented, WY segments 2.. beside it)", 4): {
         "sources": ["gdp_scan_body.cuh", "gdp_scan.cu", "gdp_wy_body.cuh", "gdp_wy.cu", "gdp_sm100.cuh",
                     "gdp_internal.cuh"],
-        "sha": "0a4d231badd5ce58",
-        "bytes_per_call": 16 * (506176000 + 146059776) + 15 * (171744512 + 442974976),
+        "sha": "71d1476e59c6c77a",
+        "bytes_per_call": 16 * (506071808 + 145328896) + 15 * (171891200 + 443047168),
     },
 }
 

@@ -82,7 +82,9 @@ __global__ void __launch_bounds__(kBtThreads, 1)
   const int64_t nall = (cod_i < 0) ? 0 : max((int64_t)0, min(nchunks, p.ws_rows - cod_i));
 
   extern __shared__ __align__(1024) unsigned char bt_smem_raw[];
-  unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)bt_smem_raw + 1023) & ~(uintptr_t)1023);
+  // the 1024-aligned base as an offset into the shared array, so that accesses stay in the shared
+  // address space
+  unsigned char *sm = bt_smem_raw + ((1024u - (sm100::smem_u32(bt_smem_raw) & 1023u)) & 1023u);
   const uint16_t *dos = reinterpret_cast<const uint16_t *>(sm + nst * sbytes);  // [qpad][V] bf16
   unsigned char *sttiles = sm + nst * sbytes + bt_do_bytes(QP, V) + (uint32_t)q4 * 2u * kStTile;  // this store warp's
   __shared__ __align__(8) uint64_t full1[2], full2[2], o_ready[2], b1_done[2], b2_done[2], bk_free[2], mid_done,

@@ -184,7 +184,9 @@ __device__ __forceinline__ void scan_body(const Problem &p, const CUtensorMap &t
   const int nst = num_stages(d, QP);
 
   extern __shared__ __align__(1024) unsigned char scan_smem_raw[];
-  unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)scan_smem_raw + 1023) & ~(uintptr_t)1023);
+  // the 1024-aligned base as an offset into the shared array, so that accesses stay in the shared
+  // address space
+  unsigned char *sm = scan_smem_raw + ((1024u - (sm100::smem_u32(scan_smem_raw) & 1023u)) & 1023u);
   unsigned char *obuf = sm + nst * sbytes;  // [qpad][V] 16-bit output staging
   unsigned char *sttiles = obuf + obuf_bytes(QP, V) + (uint32_t)q4 * 2u * kStTile;  // this store warp's boxes
   __shared__ __align__(8) uint64_t full1[2], full2[2], yo_ready[2], yo_free[2], b1_done[2], b2_done[2], mid_done,

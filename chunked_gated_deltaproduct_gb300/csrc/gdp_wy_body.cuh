@@ -260,7 +260,9 @@ __device__ __forceinline__ void wy_body(const Problem &p, const CUtensorMap &tm_
   const int quad = warp & 3, chalf = warp >> 2;  // TMEM lane quadrant, column half of this warp
 
   extern __shared__ __align__(1024) unsigned char wy_smem_raw[];
-  unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)wy_smem_raw + 1023) & ~(uintptr_t)1023);
+  // the 1024-aligned base as an offset into the shared array, so that accesses stay in the shared
+  // address space
+  unsigned char *sm = wy_smem_raw + ((1024u - (sm100::smem_u32(wy_smem_raw) & 1023u)) & 1023u);
   const WyLayout lay(d);
   unsigned char *kq = sm + lay.kq, *vt = sm + lay.vt;
   float *A = reinterpret_cast<float *>(sm + lay.A);
