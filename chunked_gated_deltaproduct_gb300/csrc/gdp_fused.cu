@@ -255,7 +255,8 @@ __device__ __forceinline__ void fused_body(const Problem &p, const CUtensorMap &
   const uint64_t wl = p.wait_limit_ns;
 
   extern __shared__ __align__(1024) unsigned char fused_smem_raw[];
-  unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)fused_smem_raw + 1023) & ~(uintptr_t)1023);
+  // the 1024-aligned base as an offset into the shared array (accesses stay in the shared address space)
+  unsigned char *sm = fused_smem_raw + ((1024u - (sm100::smem_u32(fused_smem_raw) & 1023u)) & 1023u);
   const FusedLayout lay(QP);
   unsigned char *kq = sm + lay.kq, *vt = sm + lay.vt;
   float *A = reinterpret_cast<float *>(sm + lay.R);

@@ -173,7 +173,8 @@ __device__ __forceinline__ void run_chain(const ChainRows &c, const CUtensorMap 
 
 __device__ __forceinline__ unsigned char *cmb_smem_base() {
   extern __shared__ __align__(1024) unsigned char cmb_smem_raw[];
-  return reinterpret_cast<unsigned char *>(((uintptr_t)cmb_smem_raw + 1023) & ~(uintptr_t)1023);
+  // the 1024-aligned base as an offset into the shared array (accesses stay in the shared address space)
+  return cmb_smem_raw + ((1024u - (sm100::smem_u32(cmb_smem_raw) & 1023u)) & 1023u);
 }
 
 // Split chains: the pieces of sequence blockIdx.x, head blockIdx.y, state rows 16 blockIdx.z ..:
