@@ -25,9 +25,11 @@
 // three MMA batches alternate with the threads' epilogues (the accumulator rows on the TMEM lanes
 // are written back as the next batch's operand tiles), the slice's last products (Gram sums,
 // dkhat^T, dqhat^T, which stay in TMEM across the slices) going out with the next slice's first.
-// The masked, decayed Gram sums feed one last batch.  The products take the operands as tf32;
-// the triangular ones with T included (measured against the float64 oracle, the 3xTF32 split
-// changes the gradients' error by less than 1e-4 relative).
+// The masked, decayed Gram sums feed one last batch.  The threads round every operand they write
+// to the nearest tf32 value (the tensor cores would otherwise drop the low mantissa bits, which
+// doubled the gradients' error against the float64 oracle); the state slices that TMA brings are
+// taken as they are.  The triangular products with T run in plain tf32 as well: against the
+// oracle, the 3xTF32 split changed the gradients' relative error by less than 1e-4.
 //
 // One CTA of 256 threads per (expanded chunk, head): warp w reads TMEM lane quadrant w % 4 and the
 // half w / 4 of the columns; thread 0 issues the MMAs and the TMA loads.  Every wait is bounded
