@@ -20,9 +20,10 @@
 // Khat^T -- are written into TMEM (lanes = the K index), so that no state slice is transposed in
 // shared memory.  64-row operands are stacked in pairs to fill M = 128: [Khat; Qhat] against the
 // state slice gives rhs and QS in one accumulator, [T; T^T] against [beta rhs^T; Zt^T] gives vt and
-// Delta, [e; vt] against [dv; dO] gives the four Gram sums at once.  V runs in four slices of 32
+// Delta, [L T; P T] (formed once per chunk) against beta rhs^T gives L vt and P vt in the same
+// batch, [e; vt] against [dv; dO] gives the four Gram sums at once.  V runs in four slices of 32
 // columns, the slice's S and D_C rows brought by TMA (double-buffered, a slice ahead); per slice
-// three MMA batches alternate with the threads' epilogues (the accumulator rows on the TMEM lanes
+// two MMA round trips alternate with the threads' epilogues (the accumulator rows on the TMEM lanes
 // are written back as the next batch's operand tiles), the slice's last products (Gram sums,
 // dkhat^T, dqhat^T, which stay in TMEM across the slices) going out with the next slice's first.
 // The masked, decayed Gram sums feed one last batch.  The threads round every operand they write
@@ -59,7 +60,7 @@ __device__ __forceinline__ uint32_t toff(uint32_t rows, int r, int c) {
 // rows read the rows past the valid ones from the region that follows (their accumulator lanes are
 // never read).
 struct CtLayout {
-  uint32_t rkq, kq, tt, lp, pt, b1, dot, b2, b3, dl, fb, fq, raw5, gb, dqb, stk, stq, total;
+  uint32_t rkq, kq, tt, lp, pt, b1, dot, b2, dl, fb, fq, raw5, gb, dqb, stk, stq, total;
   static constexpr uint32_t kB1 = 4u * 64u * 128u;  // one slice buffer
   __host__ __device__ uint32_t b1s(int s) const { return b1 + (uint32_t)(s & 1) * kB1; }
   __host__ __device__ CtLayout(int qp) {
@@ -72,15 +73,14 @@ struct CtLayout {
     };
     kq = take(4u * rkq * 128u);  // [Khat; Qhat], K = d
     tt = take(2u * 128u * 128u); // [T; T^T], K = 64
-    lp = take(2u * rkq * 128u);  // [L; P], K = 64
+    lp = take(2u * rkq * 128u);  // [L; P], K = 64; then [L T; P T]
     pt = take(64u * 128u);       // P^T rows r, K = qpad
     b1 = take(2u * kB1);         // two slice buffers: [S_s; D_s] rows v, K = d (TMA), then [e_s; vt_s]
                                  // (K = VS, 128 rows) and [bfc e_s | -gamma beta Delta_s] (rows r, K = 2 VS)
     fb = b1;                  // at the end [beta M1 | -M23] rows r, K = qpad + 64
     dot = take(32u * 128u);      // dO_s^T rows v, K = qpad
     b2 = take(2u * 64u * 128u);  // [beta rhs^T; Zt^T] rows n, K = 64
-    b3 = b2;                     //   then vt_s^T rows v, K = 64
-    dl = b2 + 2u * 32u * 128u;   //   and Delta_s [64][32] (16-byte chunks swizzled by row)
+    dl = b2 + 2u * 32u * 128u;   //   then Delta_s [64][32] (16-byte chunks swizzled by row)
     fq = b2 + 2u * 32u * 128u;   //   at the end scale M4 rows p, K = 64 (after the Gram staging)
     gb = take(rkq * 128u);       // [dv_s; dO_s], K = VS
     dqb = take((uint32_t)qp * 128u);  // scale gamma_p dO_s rows p, K = VS
@@ -419,6 +419,25 @@ __global__ void __launch_bounds__(kCtThreads, 1)
       }
     }
   }
+  // ---- batch 0b: [L T; P T] = [L; P] T (T^T are rows 64-127 of [T; T^T]), written over [L; P]:
+  // the slices then take L vt and P vt from beta rhs with vt itself, one batch ----
+  to_mma();
+  if (tid == 0) {
+    tc_fence_after();
+    mma_ss(tA2, lay.lp, RKQ, lay.tt + 64u * 128u, 128, kChunk / 8, id64, false);
+    mma_commit(&bar);
+  }
+  wait_mma();
+  if (q4 < 3) {
+    float a[32];
+    tmem_ld32x(lanes + tA2 + 32 * hh, a);
+    if (m < 64 + QP) {
+#pragma unroll
+      for (int j4 = 0; j4 < 32; j4 += 4)
+        *reinterpret_cast<float4 *>(sm + lay.lp + toff(RKQ, m, 32 * hh + j4)) =
+            tf32r4(make_float4(a[j4], a[j4 + 1], a[j4 + 2], a[j4 + 3]));
+    }
+  }
   to_mma();
   if (tid == 0) {
     tc_fence_after();
@@ -473,27 +492,37 @@ __global__ void __launch_bounds__(kCtThreads, 1)
         *at(lay.b2 + toff(64, 32 + n, r)) = tf32r(f * __uint_as_float(za[i]) + __uint_as_float(zp[i]));
       }
     }
-    // ---- batch 2: [vt | Delta] = [T; T^T] [beta rhs^T; Zt^T]^T ----
+    // ---- batch 2: [vt | Delta] = [T; T^T] [beta rhs^T; Zt^T]^T and [L vt; P vt] = [L T; P T] beta rhs ----
     to_mma();
     if (tid == 0) {
       tc_fence_after();
       mma_ss(tA2, lay.tt, 128, lay.b2, 64, kChunk / 8, id64, false);
+      mma_ss(tA3, lay.lp, RKQ, lay.b2, 64, kChunk / 8, id32, false);
       mma_commit(&bar);
     }
     wait_mma();
-    if (q4 < 2) {
+    if (q4 < 2) {  // rows r: vt, e = rhs - L vt
       const int r = m;
-      float vt[16];
-      tmem_ld16(lanes + tA2 + 16 * hh, vt);
+      uint32_t vr[16], lr[16];
+      tmem_ld16_nw(lanes + tA2 + 16 * hh, vr);
+      tmem_ld16_nw(lanes + tA3 + 16 * hh, lr);
+      tmem_ld_wait();
+      const float bf = sbfc[r];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) vt[i] = tf32r(vt[i]);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) *at(lay.b3 + toff(32, 16 * hh + i, r)) = vt[i];
-#pragma unroll
-      for (int i = 0; i < 16; i += 4)
-        *reinterpret_cast<float4 *>(sm + ga + toff(128, 64 + r, 16 * hh + i)) =
-            make_float4(vt[i], vt[i + 1], vt[i + 2], vt[i + 3]);
-    } else {
+      for (int i = 0; i < 16; i += 4) {
+        const float4 vt = tf32r4(make_float4(__uint_as_float(vr[i]), __uint_as_float(vr[i + 1]),
+                                             __uint_as_float(vr[i + 2]), __uint_as_float(vr[i + 3])));
+        *reinterpret_cast<float4 *>(sm + ga + toff(128, 64 + r, 16 * hh + i)) = vt;
+        rhs[i] -= __uint_as_float(lr[i]);  // e
+        rhs[i + 1] -= __uint_as_float(lr[i + 1]);
+        rhs[i + 2] -= __uint_as_float(lr[i + 2]);
+        rhs[i + 3] -= __uint_as_float(lr[i + 3]);
+        const float4 e = make_float4(rhs[i], rhs[i + 1], rhs[i + 2], rhs[i + 3]);
+        *reinterpret_cast<float4 *>(sm + ga + toff(128, r, 16 * hh + i)) = tf32r4(e);
+        *reinterpret_cast<float4 *>(sm + dkb + toff(64, r, 16 * hh + i)) =
+            tf32r4(make_float4(bf * e.x, bf * e.y, bf * e.z, bf * e.w));
+      }
+    } else {  // rows r: Delta, dv; readout rows p (quadrant 2): rho_p += dO_p . o_p
       const int r = m - 64;
       float dl[16];
       tmem_ld16(lanes + tA2 + 32 + 16 * hh, dl);
@@ -510,48 +539,34 @@ __global__ void __launch_bounds__(kCtThreads, 1)
         const int ch = ((4 * hh + (i >> 2)) ^ (r & 7));
         *reinterpret_cast<float4 *>(sm + lay.dl + (uint32_t)r * 128u + (uint32_t)ch * 16u) = x;
       }
+      if (q4 == 2) {
+        const int qi = lane;
+        uint32_t qa[16], ea[16];
+        tmem_ld16_nw(lanes + tA1 + 16 * hh, qa);
+        tmem_ld16_nw(lanes + tA3 + 16 * hh, ea);
+        tmem_ld_wait();
+        if (qi < QP) {
+          const float gq = sgq[qi];
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) {
+            const float4 d = *reinterpret_cast<const float4 *>(sm + lay.gb + toff(RKQ, 64 + qi, 16 * hh + i));
+            rho_acc += d.x * (gq * __uint_as_float(qa[i]) + __uint_as_float(ea[i])) +
+                       d.y * (gq * __uint_as_float(qa[i + 1]) + __uint_as_float(ea[i + 1])) +
+                       d.z * (gq * __uint_as_float(qa[i + 2]) + __uint_as_float(ea[i + 2])) +
+                       d.w * (gq * __uint_as_float(qa[i + 3]) + __uint_as_float(ea[i + 3]));
+          }
+        }
+      }
     }
-    // ---- batch 3: [L vt | P vt] = [L; P] vt_s ----
-    to_mma();
-    if (tid == 0) {
-      tc_fence_after();
-      mma_ss(tA3, lay.lp, RKQ, lay.b3, 32, kChunk / 8, id32, false);
-      mma_commit(&bar);
-    }
-    wait_mma();
-    if (q4 < 2) {
+    __syncthreads();  // Delta rows -> the row sums
+    if (q4 < 2) {  // dbeta_r += e_r . Delta_r, sig_r += Delta_r . v_r
       const int r = m;
-      float lv[16];
-      tmem_ld16(lanes + tA3 + 16 * hh, lv);
-      const float bf = sbfc[r];
 #pragma unroll
       for (int i = 0; i < 16; i += 4) {
-        const float4 e = make_float4(rhs[i] - lv[i], rhs[i + 1] - lv[i + 1], rhs[i + 2] - lv[i + 2],
-                                     rhs[i + 3] - lv[i + 3]);
-        *reinterpret_cast<float4 *>(sm + ga + toff(128, r, 16 * hh + i)) = tf32r4(e);
-        *reinterpret_cast<float4 *>(sm + dkb + toff(64, r, 16 * hh + i)) =
-            tf32r4(make_float4(bf * e.x, bf * e.y, bf * e.z, bf * e.w));
         const int ch = ((4 * hh + (i >> 2)) ^ (r & 7));
         const float4 x = *reinterpret_cast<const float4 *>(sm + lay.dl + (uint32_t)r * 128u + (uint32_t)ch * 16u);
-        sdb_acc += e.x * x.x + e.y * x.y + e.z * x.z + e.w * x.w;
+        sdb_acc += rhs[i] * x.x + rhs[i + 1] * x.y + rhs[i + 2] * x.z + rhs[i + 3] * x.w;
         ssg_acc += x.x * vin[i] + x.y * vin[i + 1] + x.z * vin[i + 2] + x.w * vin[i + 3];
-      }
-    } else if (q4 == 2) {
-      const int qi = lane;
-      uint32_t qa[16], ea[16];
-      tmem_ld16_nw(lanes + tA1 + 16 * hh, qa);
-      tmem_ld16_nw(lanes + tA3 + 16 * hh, ea);
-      tmem_ld_wait();
-      if (qi < QP) {
-        const float gq = sgq[qi];
-#pragma unroll
-        for (int i = 0; i < 16; i += 4) {
-          const float4 d = *reinterpret_cast<const float4 *>(sm + lay.gb + toff(RKQ, 64 + qi, 16 * hh + i));
-          rho_acc += d.x * (gq * __uint_as_float(qa[i]) + __uint_as_float(ea[i])) +
-                     d.y * (gq * __uint_as_float(qa[i + 1]) + __uint_as_float(ea[i + 1])) +
-                     d.z * (gq * __uint_as_float(qa[i + 2]) + __uint_as_float(ea[i + 2])) +
-                     d.w * (gq * __uint_as_float(qa[i + 3]) + __uint_as_float(ea[i + 3]));
-        }
       }
     }
     if (s + 1 < kCtSlices) put_dot(do_nx);  // the next slice's batch 1 reads it
