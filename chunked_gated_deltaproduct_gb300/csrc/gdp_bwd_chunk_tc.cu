@@ -570,7 +570,7 @@ __global__ void __launch_bounds__(kCtThreads, 1)
       }
     }
     if (s + 1 < kCtSlices) put_dot(do_nx);  // the next slice's batch 1 reads it
-    // ---- batch 4: Gram sums [e; vt] [dv; dO]^T, dkhat^T += [D_s^T | S_s^T] [bfc e | -gb Delta]^T,
+    // ---- batch 3: Gram sums [e; vt] [dv; dO]^T, dkhat^T += [D_s^T | S_s^T] [bfc e | -gb Delta]^T,
     // dqhat^T += S_s^T (scale gamma_p dO_s)^T; with the next slice's batch 1 ----
     to_mma();
     if (tid == 0) {
