@@ -3,7 +3,7 @@
 The forward kernels (WY, scan) and the backward kernels (reverse scan, per-chunk gradients)
 evaluate the recurrence of the FlashInfer API page "flashinfer.gdp_prefill.chunk_gated_delta_product"
 (display equation) in 64-row chunks of the expanded stream, with formulas derived from the row
-recurrence by algebra (the headers of gdp_wy_body.cuh, gdp_scan_body.cuh, gdp_backward.cuh and
+recurrence by algebra (the headers of gdp_wy_body.cuh, gdp_scan_body.cuh, gdp_backward.cu and
 gdp_bwd_chunk_tc.cu state them).  Here the same formulas are written out in float64 numpy, one
 chunk at a time, and compared with the float64 oracle, which steps the recurrence row by row and
 takes the derivative step by step: a wrong sign, index or mask in a formula fails these tests at
