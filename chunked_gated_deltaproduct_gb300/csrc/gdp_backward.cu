@@ -27,9 +27,10 @@
 // takes the derivative step by step instead and the parity tests compare the two.
 //
 // Kernels: the reverse state scan (D_C of every chunk) runs on the tcgen05 tensor cores with D
-// resident in TMEM (gdp_bwd_scan_tc.cu); the kernels here use warp-level tf32 MMAs with fp32
-// accumulation (the triangular solves in the 3xTF32 split; the dense chunk products are small
-// and varied):
+// resident in TMEM (gdp_bwd_scan_tc.cu), and so do the per-chunk gradients for head size 128 with
+// two or more updates per token (gdp_bwd_chunk_tc.cu).  The per-chunk kernel here serves the other
+// shapes (head size 64, one update per token) with warp-level tf32 MMAs and fp32 accumulation (the
+// triangular solves in the 3xTF32 split):
 //   gdp_bwd_chunk_kernel  one CTA per (expanded chunk, head), V in 16- (or 8-) column
 //                         slices: the per-row gradients above, the L2-norm chain rule
 //                         dx = dxhat / n - x (x . dxhat) / n^3, dq / dk / dv / dbeta stores
